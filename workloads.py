@@ -1,0 +1,127 @@
+"""Seeded synthetic workloads for the softcap / sink attention path.
+
+This module holds shapes and random draws only -- none of the method's
+arithmetic.  Both the CUDA path (through ``bench.py`` and the GPU tests) and the
+fp64 oracle read their inputs from here, so the two always see the same numbers.
+
+Draw order (one ``torch.Generator`` on the CPU, seeded once per workload):
+q, k, v, dO, bias, sink, segment runs; each draw is fp32 N(0,1) scaled by the
+workload's standard deviation and then cast to the workload dtype.
+
+The workloads are the ones the softcap / sink pages motivate (a Gemma2-style local
+layer with a cap of 50, packed variable-length rows with a cap of 30, a learnable
+sink with offsets drawn as randn x 5, a long-context causal stress case) plus one
+tiny fp32 case with an additive bias that the oracle finishes in seconds.  No
+public dataset or benchmark suite is involved: the inputs are synthetic by design.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: str               # "f32" or "bf16"
+    B: int
+    Sq: int
+    Sk: int
+    Hq: int
+    Hkv: int
+    D: int
+    causal: bool
+    window: int = 0          # 0: no sliding window
+    softcap: float = 0.0     # 0: no cap
+    q_std: float = 1.0       # std of q and k
+    v_std: float = 1.0       # std of v and dO
+    bias: bool = False       # post-scale additive bias [1, Hq, Sq, Sk] ~ N(0,1), broadcast over b
+    sink: bool = False       # per-query-head sink offsets ~ randn * 5
+    segments: bool = False   # packed rows: run lengths ~ U[run_lo, run_hi], last truncated
+    run_lo: int = 64
+    run_hi: int = 4096
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def torch_dtype(self):
+        return {"f32": torch.float32, "bf16": torch.bfloat16}[self.dtype]
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+# The full-size workloads (the first is the tiny fp32 correctness case).
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("tiny_f32_softcap_bias", "f32", B=1, Sq=256, Sk=256, Hq=2, Hkv=2, D=64,
+                 causal=True, softcap=30.0, q_std=4.0, bias=True),
+        Workload("gemma2_local_w4096_cap50", "bf16", B=2, Sq=8192, Sk=8192, Hq=16, Hkv=8, D=256,
+                 causal=True, window=4096, softcap=50.0, q_std=3.0),
+        Workload("gemma2_local_w4096_cap0", "bf16", B=2, Sq=8192, Sk=8192, Hq=16, Hkv=8, D=256,
+                 causal=True, window=4096, softcap=0.0, q_std=3.0),
+        Workload("packed_varlen_cap30", "bf16", B=4, Sq=8192, Sk=8192, Hq=8, Hkv=8, D=128,
+                 causal=True, softcap=30.0, q_std=3.0, segments=True),
+        Workload("sink_gqa64_cap0", "bf16", B=2, Sq=4096, Sk=4096, Hq=64, Hkv=8, D=64,
+                 causal=True, softcap=0.0, sink=True),
+        Workload("sink_gqa64_cap30", "bf16", B=2, Sq=4096, Sk=4096, Hq=64, Hkv=8, D=64,
+                 causal=True, softcap=30.0, sink=True),
+        Workload("long_causal_32k_cap50", "bf16", B=1, Sq=32768, Sk=32768, Hq=32, Hkv=16, D=256,
+                 causal=True, softcap=50.0, q_std=3.0),
+        Workload("long_noncausal_16k_cap50", "bf16", B=1, Sq=16384, Sk=16384, Hq=32, Hkv=16, D=256,
+                 causal=False, softcap=50.0, q_std=3.0),
+    ]
+}
+
+
+def segment_runs(gen: torch.Generator, B: int, S: int, lo: int, hi: int, tile: int = 128):
+    """Segment ids [B,S] int32 from run lengths ~ U[lo,hi] per row, last run truncated.
+
+    Ids are increasing within a row (0, 1, 2, ...).  The whole draw is repeated until at
+    least one run boundary inside some row is not a multiple of ``tile``.
+    """
+    while True:
+        rows, unaligned = [], False
+        for _ in range(B):
+            lens, total = [], 0
+            while total < S:
+                L = int(torch.randint(lo, hi + 1, (1,), generator=gen).item())
+                L = min(L, S - total)
+                lens.append(L)
+                total += L
+                if total < S and total % tile != 0:
+                    unaligned = True
+            rows.append(torch.repeat_interleave(torch.arange(len(lens), dtype=torch.int32),
+                                                torch.tensor(lens)))
+        if unaligned:
+            return torch.stack(rows).to(torch.int32)
+
+
+def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
+    """CPU tensors for one workload: q, k, v, dO in the workload dtype; bias (workload dtype,
+    [1,Hq,Sq,Sk]) or None; sink fp32 [Hq] or None; seg int32 [B,S] or None."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    dt = w.torch_dtype
+
+    def draw(shape, std):
+        return (torch.randn(shape, generator=g, dtype=torch.float32) * std).to(dt)
+
+    q = draw((w.B, w.Sq, w.Hq, w.D), w.q_std)
+    k = draw((w.B, w.Sk, w.Hkv, w.D), w.q_std)
+    v = draw((w.B, w.Sk, w.Hkv, w.D), w.v_std)
+    dO = draw((w.B, w.Sq, w.Hq, w.D), w.v_std)
+    bias = draw((1, w.Hq, w.Sq, w.Sk), 1.0) if w.bias else None
+    sink = (torch.randn((w.Hq,), generator=g, dtype=torch.float32) * 5.0) if w.sink else None
+    seg = None
+    if w.segments:
+        assert w.Sq == w.Sk
+        seg = segment_runs(g, w.B, w.Sq, w.run_lo, w.run_hi)
+    return {"q": q, "k": k, "v": v, "dO": dO, "bias": bias, "sink": sink, "seg": seg}
