@@ -1,0 +1,165 @@
+"""GB300 (sm_103a) fused attention with tanh soft-capping, a learnable sink, GQA and
+causal / sliding-window / packed-segment masks.
+
+Thin Python binding over the C ABI of ``libattn_gb300.so`` (include/attn_gb300.h):
+PyTorch supplies device memory and the current stream; every step of the forward and
+backward runs in the library's CUDA kernels.  The names follow the C entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _capi
+from ._capi import AttnArgs, AttnError, lib  # noqa: F401
+
+__all__ = ["attn_fwd", "attn_bwd", "attn_check_device_status", "attn_path_name",
+           "attn_launch_counter", "attn_profile_next_main_kernel", "AttnError", "build_args"]
+
+_DTYPES = {torch.bfloat16: _capi.ATTN_DTYPE_BF16, torch.float32: _capi.ATTN_DTYPE_F32}
+_ws_cache: dict = {}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
+               bias=None, seg_q=None, seg_k=None, cu_seqlens=None):
+    """Fill an ``attn_args`` from tensors.  Returns (args, tensors kept alive)."""
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share dtype bfloat16 or float32")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, S, H, D]")
+    for t in (q, k, v):
+        if t.stride(-1) != 1:
+            raise ValueError("the head dimension must be contiguous")
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    a = AttnArgs()
+    a.dtype = _DTYPES[q.dtype]
+    a.B, a.Sq, a.Sk, a.Hq, a.Hkv, a.D = B, Sq, Sk, Hq, Hkv, D
+    a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    a.q_stride_b, a.q_stride_s, a.q_stride_h = q.stride(0), q.stride(1), q.stride(2)
+    a.k_stride_b, a.k_stride_s, a.k_stride_h = k.stride(0), k.stride(1), k.stride(2)
+    a.v_stride_b, a.v_stride_s, a.v_stride_h = v.stride(0), v.stride(1), v.stride(2)
+    keep = [q, k, v]
+    if bias is not None:
+        if bias.dtype != q.dtype or bias.dim() != 4 or tuple(bias.shape[2:]) != (Sq, Sk):
+            raise ValueError("bias must be [1|B, 1|Hq, Sq, Sk] in the dtype of q")
+        if bias.stride(-1) != 1 or bias.stride(-2) != Sk:
+            raise ValueError("bias rows must be dense [Sq, Sk]")
+        a.bias = bias.data_ptr()
+        a.bias_stride_b = 0 if bias.shape[0] == 1 else bias.stride(0)
+        a.bias_stride_h = 0 if bias.shape[1] == 1 else bias.stride(1)
+        keep.append(bias)
+    if seg_q is not None:
+        seg_k = seg_q if seg_k is None else seg_k
+        seg_q, seg_k = seg_q.to(torch.int32).contiguous(), seg_k.to(torch.int32).contiguous()
+        a.seg_q, a.seg_k = seg_q.data_ptr(), seg_k.data_ptr()
+        keep += [seg_q, seg_k]
+    if cu_seqlens is not None:
+        cu = cu_seqlens.to(torch.int32).contiguous()
+        a.cu_seqlens, a.nseq = cu.data_ptr(), cu.numel() - 1
+        keep.append(cu)
+    a.causal = int(bool(causal))
+    a.window = int(window)
+    a.softcap = float(softcap)
+    if sink is not None:
+        sink = sink.to(torch.float32).contiguous()
+        a.sink = sink.data_ptr()
+        keep.append(sink)
+    a.scale = float(D ** -0.5 if scale is None else scale)
+    return a, keep
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _workspace(device, nbytes: int) -> torch.Tensor:
+    """Per (device, stream) workspace, zero-filled when (re)allocated."""
+    key = (device.index, _stream(device))
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def _check(status: int, where: str):
+    if status != _capi.ATTN_OK:
+        raise AttnError(status, where)
+
+
+def attn_fwd(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
+             bias=None, seg_q=None, seg_k=None, cu_seqlens=None, out=None, lse=None):
+    """Forward: returns (O [B,Sq,Hq,D] in q's dtype, LSE [B,Hq,Sq] float32)."""
+    a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
+                         scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens)
+    L = lib()
+    need = L.attn_fwd_workspace_size(ctypes.byref(a))
+    if need == 0:
+        _check(_capi.ATTN_ERR_INVALID, "attn_fwd")
+    B, Sq, Hq, D = q.shape
+    O = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device) if out is None else out
+    LSE = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws = _workspace(q.device, need)
+    _check(L.attn_fwd(ctypes.byref(a), O.data_ptr(), LSE.data_ptr(), ws.data_ptr(), ws.numel(),
+                      _stream(q.device)), "attn_fwd")
+    del keep
+    return O, LSE
+
+
+def attn_bwd(q, k, v, O, LSE, dO, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
+             bias=None, seg_q=None, seg_k=None, cu_seqlens=None):
+    """Backward: returns (dQ, dK, dV, dbias or None, dsink or None)."""
+    a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
+                         scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens)
+    L = lib()
+    need = L.attn_bwd_workspace_size(ctypes.byref(a))
+    if need == 0:
+        _check(_capi.ATTN_ERR_INVALID, "attn_bwd")
+    if not O.is_contiguous() or not dO.is_contiguous() or not LSE.is_contiguous():
+        raise ValueError("O, dO and LSE must be contiguous")
+    dQ = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    dK = torch.empty(k.shape, dtype=q.dtype, device=q.device)
+    dV = torch.empty(v.shape, dtype=q.dtype, device=q.device)
+    dbias = None
+    if bias is not None:
+        dbias = torch.empty((bias.shape[0], bias.shape[1], q.shape[1], k.shape[1]),
+                            dtype=q.dtype, device=q.device)
+    dsink = torch.empty((q.shape[2],), dtype=torch.float32, device=q.device) if sink is not None else None
+    ws = _workspace(q.device, need)
+    _check(L.attn_bwd(ctypes.byref(a), O.data_ptr(), LSE.data_ptr(), dO.data_ptr(), dQ.data_ptr(),
+                      dK.data_ptr(), dV.data_ptr(), _ptr(dbias), _ptr(dsink), ws.data_ptr(),
+                      ws.numel(), _stream(q.device)), "attn_bwd")
+    del keep
+    return dQ, dK, dV, dbias, dsink
+
+
+def attn_check_device_status(device=None) -> int:
+    """Synchronise and read/clear the device status word of this stream's workspace."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    ws = _ws_cache.get((device.index, _stream(device)))
+    if ws is None:
+        return _capi.ATTN_OK
+    return lib().attn_check_device_status(ws.data_ptr(), _stream(device))
+
+
+def attn_path_name(q, k, v, **kw) -> str:
+    a, keep = build_args(q, k, v, **kw)
+    return lib().attn_path_name(ctypes.byref(a)).decode()
+
+
+def attn_launch_counter() -> int:
+    return int(lib().attn_launch_counter())
+
+
+def attn_profile_next_main_kernel(ev_start: "torch.cuda.Event", ev_end: "torch.cuda.Event"):
+    """Have the next attn_fwd / attn_bwd of this thread record the two events around its
+    main kernel, on the call's stream."""
+    lib().attn_profile_next_main_kernel(ctypes.c_void_p(ev_start.cuda_event),
+                                        ctypes.c_void_p(ev_end.cuda_event))

@@ -1,0 +1,270 @@
+// api.cu -- the C ABI declared in include/attn_gb300.h: argument validation (fail closed:
+// an invalid or unsupported request never launches anything), workspace layout, and the
+// launch sequence of the forward and backward passes on the caller's stream.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/attn_gb300.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+
+std::atomic<unsigned long long> g_launches{0};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Workspace carve-up.  Offsets are 0 when a region is absent.
+struct Layout {
+  size_t status = 0, mono = 0, qrange = 0, krange = 0, seg = 0;
+  size_t dvec = 0, dsink_part = 0, dqacc = 0, dbias_acc = 0;
+  size_t total = 0;
+};
+
+bool use_tc(const attn_args *a) {
+  return a->dtype == ATTN_DTYPE_BF16 && a->bias == nullptr && a->Sk > 0 && tc_supported(a->D);
+}
+
+size_t dbias_elems(const attn_args *a) {
+  if (!a->bias) return 0;
+  const size_t bb = a->bias_stride_b ? (size_t)a->B : 1, hb = a->bias_stride_h ? (size_t)a->Hq : 1;
+  return bb * hb * (size_t)a->Sq * (size_t)a->Sk;
+}
+
+Layout layout(const attn_args *a, bool bwd) {
+  Layout L;
+  size_t off = kAlign;  // [0, 256): status word
+  const bool seg = a->seg_q || a->cu_seqlens;
+  if (seg) {
+    const size_t nq = (a->Sq + 63) / 64, nk = (a->Sk + 63) / 64;
+    L.mono = off; off += align_up((size_t)a->B);
+    L.qrange = off; off += align_up((size_t)a->B * nq * sizeof(int2));
+    L.krange = off; off += align_up((size_t)a->B * nk * sizeof(int2));
+    if (a->cu_seqlens) { L.seg = off; off += align_up((size_t)a->Sq * sizeof(int)); }
+  }
+  if (bwd) {
+    L.dvec = off; off += align_up((size_t)a->B * a->Hq * a->Sq * sizeof(float));
+    if (a->sink) {
+      L.dsink_part = off;
+      off += align_up((size_t)a->Hq * bwd_pre_partials(a->B, a->Sq) * sizeof(float));
+    }
+    if (use_tc(a)) { L.dqacc = off; off += align_up((size_t)a->B * a->Sq * a->Hq * a->D * sizeof(float)); }
+    if (a->bias) { L.dbias_acc = off; off += align_up(dbias_elems(a) * sizeof(float)); }
+  }
+  L.total = off;
+  return L;
+}
+
+int validate(const attn_args *a) {
+  if (!a) return ATTN_ERR_INVALID;
+  if (a->dtype != ATTN_DTYPE_BF16 && a->dtype != ATTN_DTYPE_F32) return ATTN_ERR_INVALID;
+  if (a->B < 0 || a->Sq < 0 || a->Sk < 0 || a->Hq < 1 || a->Hkv < 1 || a->D < 1) return ATTN_ERR_INVALID;
+  if (a->Hq % a->Hkv != 0) return ATTN_ERR_INVALID;
+  if (a->D % 8 != 0) return ATTN_ERR_INVALID;
+  if (a->D > 256) return ATTN_ERR_UNSUPPORTED;
+  if (!isfinite(a->scale)) return ATTN_ERR_INVALID;
+  if (!isfinite(a->softcap) || a->softcap < 0.f) return ATTN_ERR_INVALID;
+  if (a->B > 0 && a->Sq > 0 && !a->q) return ATTN_ERR_INVALID;
+  if (a->B > 0 && a->Sk > 0 && (!a->k || !a->v)) return ATTN_ERR_INVALID;
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v)) return ATTN_ERR_INVALID;
+  const int64_t vec = a->dtype == ATTN_DTYPE_BF16 ? 8 : 4;  // elements per 16 bytes
+  const int64_t st[9] = {a->q_stride_b, a->q_stride_s, a->q_stride_h, a->k_stride_b, a->k_stride_s,
+                         a->k_stride_h, a->v_stride_b, a->v_stride_s, a->v_stride_h};
+  for (int64_t s : st)
+    if (s < 0 || s % vec != 0) return ATTN_ERR_INVALID;
+  if (a->Sq > 0 && a->q_stride_s < (int64_t)a->D) return ATTN_ERR_INVALID;
+  if (a->bias) {
+    if (a->bias_stride_b < 0 || a->bias_stride_h < 0 || !aligned16(a->bias)) return ATTN_ERR_INVALID;
+  }
+  if ((a->seg_q == nullptr) != (a->seg_k == nullptr)) return ATTN_ERR_INVALID;
+  if (a->cu_seqlens) {
+    if (a->seg_q) return ATTN_ERR_UNSUPPORTED;
+    if (a->B != 1 || a->Sq != a->Sk || a->nseq < 0) return ATTN_ERR_INVALID;
+  }
+  return ATTN_OK;
+}
+
+Params make_params(const attn_args *a, char *ws, const Layout &L) {
+  Params p;
+  memset(&p, 0, sizeof(p));
+  p.B = a->B; p.Sq = a->Sq; p.Sk = a->Sk; p.Hq = a->Hq; p.Hkv = a->Hkv; p.D = a->D;
+  p.G = a->Hq / a->Hkv;
+  p.causal = a->causal ? 1 : 0;
+  p.window = a->window > 0 ? a->window : 0;
+  p.cap = a->softcap;
+  p.inv_cap = a->softcap > 0.f ? 1.0f / a->softcap : 0.f;
+  p.scale = a->scale;
+  p.q = a->q; p.k = a->k; p.v = a->v;
+  p.q_sb = a->q_stride_b; p.q_ss = a->q_stride_s; p.q_sh = a->q_stride_h;
+  p.k_sb = a->k_stride_b; p.k_ss = a->k_stride_s; p.k_sh = a->k_stride_h;
+  p.v_sb = a->v_stride_b; p.v_ss = a->v_stride_s; p.v_sh = a->v_stride_h;
+  p.bias = a->bias;
+  p.bias_sb = a->bias_stride_b; p.bias_sh = a->bias_stride_h;
+  p.bias_B = a->bias_stride_b ? a->B : 1;
+  p.bias_H = a->bias_stride_h ? a->Hq : 1;
+  p.sink = a->sink;
+  p.status = reinterpret_cast<unsigned *>(ws);
+  if (a->seg_q || a->cu_seqlens) {
+    p.seg_mono = reinterpret_cast<unsigned char *>(ws + L.mono);
+    p.qrange = reinterpret_cast<int2 *>(ws + L.qrange);
+    p.krange = reinterpret_cast<int2 *>(ws + L.krange);
+    if (a->cu_seqlens) {
+      p.seg_q = p.seg_k = reinterpret_cast<int *>(ws + L.seg);
+    } else {
+      p.seg_q = a->seg_q;
+      p.seg_k = a->seg_k;
+    }
+  }
+  return p;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// Pending profiling events of this host thread (attn_profile_next_main_kernel).
+thread_local cudaEvent_t t_ev_start = nullptr, t_ev_end = nullptr;
+
+struct MainKernelEvents {
+  cudaEvent_t start, end;
+  cudaStream_t st;
+  MainKernelEvents(cudaStream_t s) : start(t_ev_start), end(t_ev_end), st(s) {
+    t_ev_start = t_ev_end = nullptr;
+    if (start) cudaEventRecord(start, st);
+  }
+  void done() {
+    if (end) cudaEventRecord(end, st);
+    end = nullptr;
+  }
+};
+
+int run_meta(const attn_args *a, Params &p, cudaStream_t st) {
+  if (!(a->seg_q || a->cu_seqlens) || a->B == 0) return ATTN_OK;
+  return cuda_status(launch_mask_meta(p, a->cu_seqlens, a->nseq, const_cast<int *>(p.seg_q),
+                                      const_cast<int *>(p.seg_k), const_cast<int2 *>(p.qrange),
+                                      const_cast<int2 *>(p.krange),
+                                      const_cast<unsigned char *>(p.seg_mono), st));
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+size_t attn_fwd_workspace_size(const attn_args *a) {
+  if (validate(a) != ATTN_OK) return 0;
+  return layout(a, false).total;
+}
+
+size_t attn_bwd_workspace_size(const attn_args *a) {
+  if (validate(a) != ATTN_OK) return 0;
+  return layout(a, true).total;
+}
+
+const char *attn_path_name(const attn_args *a) {
+  if (validate(a) != ATTN_OK) return "";
+  return use_tc(a) ? "tc" : "simt";
+}
+
+int attn_fwd(const attn_args *a, void *O, float *LSE, void *ws, size_t ws_bytes, attn_stream_t stream) {
+  int s = validate(a);
+  if (s != ATTN_OK) return s;
+  if (a->B == 0 || a->Sq == 0) return ATTN_OK;
+  if (!O || !LSE || !aligned16(O)) return ATTN_ERR_INVALID;
+  const Layout L = layout(a, false);
+  if (!ws || ws_bytes < L.total || ((uintptr_t)ws % kAlign) != 0) return ATTN_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Params p = make_params(a, static_cast<char *>(ws), L);
+  p.O = O;
+  p.LSE = LSE;
+  if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
+  MainKernelEvents ev(st);
+  cudaError_t e = use_tc(a) ? tc_forward(p, st) : simt_forward(p, a->dtype, st);
+  ev.done();
+  return cuda_status(e);
+}
+
+int attn_bwd(const attn_args *a, const void *O, const float *LSE, const void *dO, void *dQ, void *dK,
+             void *dV, void *dbias, float *dsink, void *ws, size_t ws_bytes, attn_stream_t stream) {
+  int s = validate(a);
+  if (s != ATTN_OK) return s;
+  if (a->B > 0 && a->Sq > 0 && (!O || !LSE || !dO || !dQ)) return ATTN_ERR_INVALID;
+  if (a->B > 0 && a->Sk > 0 && (!dK || !dV)) return ATTN_ERR_INVALID;
+  if (!aligned16(O) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
+    return ATTN_ERR_INVALID;
+  if ((a->bias != nullptr) != (dbias != nullptr)) return ATTN_ERR_INVALID;
+  if ((a->sink != nullptr) != (dsink != nullptr)) return ATTN_ERR_INVALID;
+  if (a->B == 0) return ATTN_OK;
+  const Layout L = layout(a, true);
+  if (!ws || ws_bytes < L.total || ((uintptr_t)ws % kAlign) != 0) return ATTN_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t esz = a->dtype == ATTN_DTYPE_BF16 ? 2 : 4;
+  if (a->Sq == 0) {  // no query rows: every gradient is zero
+    const size_t kv = (size_t)a->B * a->Sk * a->Hkv * a->D * esz;
+    if (cudaMemsetAsync(dK, 0, kv, st) != cudaSuccess || cudaMemsetAsync(dV, 0, kv, st) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (dsink && cudaMemsetAsync(dsink, 0, a->Hq * sizeof(float), st) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  char *w = static_cast<char *>(ws);
+  Params p = make_params(a, w, L);
+  p.O = const_cast<void *>(O);
+  p.LSE = const_cast<float *>(LSE);
+  p.dO = dO;
+  p.dQ = dQ; p.dK = dK; p.dV = dV; p.dbias = dbias; p.dsink = dsink;
+  p.Dvec = reinterpret_cast<float *>(w + L.dvec);
+  p.dsink_part = a->sink ? reinterpret_cast<float *>(w + L.dsink_part) : nullptr;
+  p.n_part = bwd_pre_partials(a->B, a->Sq);
+  const bool tc = use_tc(a);
+  p.dQacc = tc ? reinterpret_cast<float *>(w + L.dqacc) : nullptr;
+  p.dbias_acc = a->bias ? reinterpret_cast<float *>(w + L.dbias_acc) : nullptr;
+  if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
+  if (a->bias && cudaMemsetAsync(p.dbias_acc, 0, dbias_elems(a) * sizeof(float), st) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if ((s = cuda_status(launch_bwd_pre(p, a->dtype, tc, st))) != ATTN_OK) return s;
+  {
+    MainKernelEvents ev(st);
+    cudaError_t e = tc ? tc_backward(p, st) : simt_backward(p, a->dtype, st);
+    ev.done();
+    if ((s = cuda_status(e)) != ATTN_OK) return s;
+  }
+  return cuda_status(launch_bwd_post(p, a->dtype, tc, dbias_elems(a), st));
+}
+
+int attn_check_device_status(void *ws, attn_stream_t stream) {
+  if (!ws) return ATTN_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (word == 0) return ATTN_OK;
+  if (cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_ERR_DEVICE;
+}
+
+void attn_profile_next_main_kernel(void *ev_start, void *ev_end) {
+  t_ev_start = static_cast<cudaEvent_t>(ev_start);
+  t_ev_end = static_cast<cudaEvent_t>(ev_end);
+}
+
+uint64_t attn_launch_counter(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_DEVICE: return "device-side error recorded by a kernel";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+// bwd_aux.cu -- memory-bound pieces of the backward pass.
+//
+// bwd_pre:  D_i = sum_d dO_i[d] * O_i[d] (fp32) for every (b, h, i); the sink gradient's
+//           per-block partial sums -sum_i exp(sink_h - LSE_i) * D_i; and, when the
+//           tensor-core backward accumulates dQ in fp32, zeroing of that accumulator.
+//           The sink gradient follows TransformerEngine PR #3551 ("What changed"): the
+//           sink column's probability times (0 - D_i), summed over every row and batch.
+// bwd_post: the fp32 dQ accumulator converted to the output dtype, the deterministic
+//           final dsink reduction (fixed order), and the fp32 dbias accumulator written
+//           out in the bias dtype.
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kPreRows = 64;   // query positions per preprocess block
+constexpr int kPreWarps = 8;
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// 16-byte vector dot of dO and O rows.
+template <typename T>
+__device__ __forceinline__ float chunk_dot(const T *a, const T *b);
+template <>
+__device__ __forceinline__ float chunk_dot<__nv_bfloat16>(const __nv_bfloat16 *a, const __nv_bfloat16 *b) {
+  uint4 x = *reinterpret_cast<const uint4 *>(a), y = *reinterpret_cast<const uint4 *>(b);
+  const __nv_bfloat162 *xa = reinterpret_cast<const __nv_bfloat162 *>(&x);
+  const __nv_bfloat162 *ya = reinterpret_cast<const __nv_bfloat162 *>(&y);
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float2 fx = __bfloat1622float2(xa[k]), fy = __bfloat1622float2(ya[k]);
+    s = fmaf(fx.x, fy.x, s);
+    s = fmaf(fx.y, fy.y, s);
+  }
+  return s;
+}
+template <>
+__device__ __forceinline__ float chunk_dot<float>(const float *a, const float *b) {
+  float4 x = *reinterpret_cast<const float4 *>(a), y = *reinterpret_cast<const float4 *>(b);
+  return fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, x.w * y.w)));
+}
+
+// grid (ceil(Sq/64), B), block 256: warp w handles heads w, w+8, ...; rows in order, so the
+// per-(block, head) partial sums are deterministic.
+template <typename T>
+__global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int zero_dqacc) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int b = blockIdx.y;
+  const int i0 = blockIdx.x * kPreRows, i1 = min(i0 + kPreRows, p.Sq);
+  constexpr int per_chunk = 16 / sizeof(T);
+  const int nchunk = p.D / per_chunk;
+  const T *O = static_cast<const T *>(p.O);
+  const T *dO = static_cast<const T *>(p.dO);
+  for (int h = warp; h < p.Hq; h += kPreWarps) {
+    float part = 0.f;
+    const float sink = p.sink ? p.sink[h] : 0.f;
+    for (int i = i0; i < i1; ++i) {
+      const size_t row = (((size_t)b * p.Sq + i) * p.Hq + h) * p.D;
+      float s = 0.f;
+      for (int c = lane; c < nchunk; c += 32) s += chunk_dot<T>(dO + row + c * per_chunk, O + row + c * per_chunk);
+      s = warp_sum(s);
+      const size_t ri = ((size_t)b * p.Hq + h) * p.Sq + i;
+      if (lane == 0) p.Dvec[ri] = s;
+      if (p.sink) part = fmaf(expf(sink - p.LSE[ri]), s, part);
+      if (zero_dqacc) {
+        float4 *z = reinterpret_cast<float4 *>(p.dQacc + row);
+        for (int c = lane; c < p.D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    if (p.sink && lane == 0)
+      p.dsink_part[(size_t)h * p.n_part + (size_t)b * gridDim.x + blockIdx.x] = -part;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_post_kernel(Params p, int convert_dq, size_t dbias_elems) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const size_t gwarp = (size_t)blockIdx.x * 8 + warp;
+  if (p.dsink && gwarp < (size_t)p.Hq) {
+    const float *part = p.dsink_part + gwarp * p.n_part;
+    float s = 0.f;
+    for (int c = lane; c < p.n_part; c += 32) s += part[c];
+    s = warp_sum(s);
+    if (lane == 0) p.dsink[gwarp] = s;
+  }
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t nthr = (size_t)gridDim.x * blockDim.x;
+  if (convert_dq) {
+    const size_t n4 = (size_t)p.B * p.Sq * p.Hq * p.D / 4;
+    const float4 *src = reinterpret_cast<const float4 *>(p.dQacc);
+    T *dst = static_cast<T *>(p.dQ);
+    for (size_t e = tid; e < n4; e += nthr) {
+      float4 x = src[e];
+      dst[4 * e + 0] = from_f<T>(x.x);
+      dst[4 * e + 1] = from_f<T>(x.y);
+      dst[4 * e + 2] = from_f<T>(x.z);
+      dst[4 * e + 3] = from_f<T>(x.w);
+    }
+  }
+  if (dbias_elems) {
+    T *dst = static_cast<T *>(p.dbias);
+    for (size_t e = tid; e < dbias_elems; e += nthr) dst[e] = from_f<T>(p.dbias_acc[e]);
+  }
+}
+
+}  // namespace
+
+int bwd_pre_partials(int B, int Sq) { return B * ((Sq + kPreRows - 1) / kPreRows); }
+
+cudaError_t launch_bwd_pre(const Params &p, int dtype, bool zero_dqacc, cudaStream_t st) {
+  dim3 grid((p.Sq + kPreRows - 1) / kPreRows, p.B);
+  if (dtype == kF32)
+    bwd_pre_kernel<float><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc);
+  else
+    bwd_pre_kernel<__nv_bfloat16><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc);
+  return counted(cudaGetLastError());
+}
+
+cudaError_t launch_bwd_post(const Params &p, int dtype, bool convert_dq, size_t dbias_elems,
+                            cudaStream_t st) {
+  size_t work = 0;
+  if (convert_dq) work = (size_t)p.B * p.Sq * p.Hq * p.D / 4;
+  if (dbias_elems > work) work = dbias_elems;
+  size_t blocks = (work + 255) / 256;
+  const size_t sink_blocks = p.dsink ? (size_t)(p.Hq + 7) / 8 : 0;
+  if (blocks < sink_blocks) blocks = sink_blocks;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks == 0) return cudaSuccess;
+  if (dtype == kF32)
+    bwd_post_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(p, convert_dq, dbias_elems);
+  else
+    bwd_post_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(p, convert_dq, dbias_elems);
+  return counted(cudaGetLastError());
+}
+
+}  // namespace attn

@@ -1,0 +1,91 @@
+// common.cuh -- definitions shared by every kernel of the library: the kernel parameter
+// block, the score modification (scale, bias, tanh soft-cap, visibility) and the device
+// status word.  Forward and backward kernels call the same functions so that the
+// probabilities they form from a logit are computed identically.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace attn {
+
+// Device status bits (OR-ed into the first word of the workspace).
+enum : unsigned {
+  kStatusWaitTimeout = 1u,     // a bounded mbarrier / TMEM wait gave up
+  kStatusBadCuSeqlens = 2u,    // cu_seqlens not 0-based / non-decreasing / within Sq
+  kStatusBadTmemAlloc = 4u,    // tensor-memory allocation returned an unusable address
+};
+
+// Everything a kernel needs, passed by value.
+struct Params {
+  // problem
+  int B, Sq, Sk, Hq, Hkv, D, G;   // G = Hq / Hkv
+  int causal, window;             // window <= 0: off
+  float cap, inv_cap, scale;      // cap == 0: off
+  // inputs (element strides)
+  const void *q, *k, *v;
+  long long q_sb, q_ss, q_sh, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh;
+  const void *bias;
+  long long bias_sb, bias_sh;
+  int bias_B, bias_H;             // extents of the bias's own batch / head dims (1 = broadcast)
+  const int *seg_q, *seg_k;       // effective segment ids or null
+  const int2 *qrange;             // [B, ceil(Sq/64)]: key range [x, y) of each 64-row query tile
+  const int2 *krange;             // [B, ceil(Sk/64)]: query range [x, y) of each 64-key tile
+  const unsigned char *seg_mono;  // [B]: 1 if seg_q and seg_k rows are non-decreasing
+  const float *sink;              // [Hq] or null
+  // forward outputs / backward inputs
+  void *O;
+  float *LSE;
+  const void *dO;
+  // backward outputs and scratch
+  void *dQ, *dK, *dV, *dbias;
+  float *dsink;
+  float *Dvec;                    // [B, Hq, Sq]
+  float *dQacc;                   // [B, Sq, Hq, D] fp32 accumulator (tensor-core path)
+  float *dbias_acc;               // dense fp32 copy of dbias being accumulated
+  float *dsink_part;              // [Hq, n_part]
+  int n_part;                     // partial sums per head
+  unsigned *status;
+};
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Query position on the key axis (bottom-right alignment when Sq != Sk).
+__device__ __forceinline__ int qpos(const Params &p, int i) { return i + p.Sk - p.Sq; }
+
+// Visibility of key j to query i of batch b: causal, sliding window, segment equality.
+__device__ __forceinline__ bool visible(const Params &p, int b, int i, int j) {
+  const int ip = qpos(p, i);
+  if (p.causal && j > ip) return false;
+  if (p.window > 0 && ip - j >= p.window) return false;
+  if (p.seg_q && p.seg_q[(size_t)b * p.Sq + i] != p.seg_k[(size_t)b * p.Sk + j]) return false;
+  return true;
+}
+
+// Accurate soft-cap for the fp32 kernels: t = cap * tanh(u / cap) and the backward factor
+// 1 - tanh^2(u / cap).  With e = expm1(-2|y|) in (-1, 0]:
+//   tanh|y| = -e / (2 + e),   1 - tanh^2 y = 4 (1 + e) / (2 + e)^2,
+// which keeps full relative accuracy both near 0 and deep in saturation.
+__device__ __forceinline__ void softcap_accurate(float u, float cap, float inv_cap,
+                                                 float &t, float &factor) {
+  const float y = u * inv_cap;
+  const float e = expm1f(-2.0f * fabsf(y));
+  const float d = 2.0f + e;
+  const float th = -e / d;
+  t = copysignf(cap * th, y);
+  factor = 4.0f * (1.0f + e) / (d * d);
+}
+
+// Records a device-side error; never traps.
+__device__ __forceinline__ void set_status(unsigned *status, unsigned bits) {
+  if (status) atomicOr(status, bits);
+}
+
+}  // namespace attn

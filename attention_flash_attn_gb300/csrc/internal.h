@@ -1,0 +1,46 @@
+// internal.h -- host-side declarations shared by the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+namespace attn {
+
+struct Params;
+
+enum { kBF16 = 1, kF32 = 2 };
+
+// Kernels launched by this library in this process (see attn_launch_counter).
+extern std::atomic<unsigned long long> g_launches;
+inline cudaError_t counted(cudaError_t e, int n = 1) {
+  if (e == cudaSuccess) g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed);
+  return e;
+}
+
+// Mask metadata (segments / cu_seqlens): effective segment ids, per-batch monotonicity
+// and 64-granular tile ranges.  seg_q_out/seg_k_out are only written when cu_seqlens is
+// given (then B == 1).
+cudaError_t launch_mask_meta(const Params &p, const int *cu_seqlens, int nseq,
+                             int *seg_q_out, int *seg_k_out, int2 *qrange, int2 *krange,
+                             unsigned char *mono, cudaStream_t st);
+
+// fp32 FFMA kernels (any dtype; used for fp32 inputs and calls with a bias).
+cudaError_t simt_forward(const Params &p, int dtype, cudaStream_t st);
+cudaError_t simt_backward(const Params &p, int dtype, cudaStream_t st);
+
+// Backward preprocess: D = rowsum(dO * O), per-block dsink partials, zero the fp32 dQ
+// accumulator when one is used.
+cudaError_t launch_bwd_pre(const Params &p, int dtype, bool zero_dqacc, cudaStream_t st);
+int bwd_pre_partials(int B, int Sq);  // partial sums per head the preprocess writes
+
+// Backward epilogue: dQ accumulator -> dQ (when used), dsink reduction, dbias conversion.
+cudaError_t launch_bwd_post(const Params &p, int dtype, bool convert_dq, size_t dbias_elems,
+                            cudaStream_t st);
+
+// tcgen05 tensor-core kernels (bf16, D in {64, 128, 256}).
+bool tc_supported(int D);
+cudaError_t tc_forward(const Params &p, cudaStream_t st);
+cudaError_t tc_backward(const Params &p, cudaStream_t st);
+
+}  // namespace attn

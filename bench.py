@@ -1,0 +1,375 @@
+"""Benchmark: fused softcapped attention forward + backward on one GB300 (or N replicas).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = attn_fwd + attn_bwd (every kernel of the path) over one batch of the
+workload's synthetic inputs, already resident in HBM.  Prints one JSON line.
+
+Throughput counts algorithmic flops only: every visible (query, key) pair costs 4*D flops
+forward (QK^T and PV) and 10*D backward (QK^T recomputed, dP, dV, dK, dQ); masked pairs
+cost nothing.  ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, Workload, make_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "gemma2_local_w4096_cap50"
+METRIC = "fwd+bwd attention TFLOP/s (softcap, causal, bf16) and % of BF16 tensor peak"
+L2_BYTES = 129 * 2 ** 20
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def visible_pairs(w: Workload, seg) -> int:
+    """Visible (b, h, i, j) pairs under causal / window / contiguous-segment masking.
+
+    Per query row the visible keys form one interval [lo, hi); segments are runs of equal
+    ids (seg [B, S] with Sq == Sk)."""
+    off = w.Sk - w.Sq
+    ip = np.arange(w.Sq, dtype=np.int64) + off
+    hi = np.minimum(ip + 1, w.Sk) if w.causal else np.full(w.Sq, w.Sk, np.int64)
+    lo = np.maximum(ip - w.window + 1, 0) if w.window > 0 else np.zeros(w.Sq, np.int64)
+    total = 0
+    for b in range(w.B):
+        l, h = lo.copy(), hi.copy()
+        if seg is not None:
+            s = np.asarray(seg[b])
+            change = np.flatnonzero(np.diff(s)) + 1
+            starts = np.concatenate([[0], change])
+            ends = np.concatenate([change, [len(s)]])
+            run = np.repeat(np.arange(len(starts)), ends - starts)
+            l = np.maximum(l, starts[run])
+            h = np.minimum(h, ends[run])
+        total += int(np.maximum(h - l, 0).sum())
+    return total * w.Hq
+
+
+def flops(w: Workload, seg, which: str) -> float:
+    per_pair = {"fwd": 4, "bwd": 10, "fwdbwd": 14}[which] * w.D
+    return float(visible_pairs(w, seg)) * per_pair
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        rows = [r.split(",") for r in open(self.out.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 1900.0, 1700.0, "fallback"
+
+
+def run_ours(args, rank, world, local_rank):
+    import attention_flash_attn_gb300 as fa
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    seg = inp["seg"]
+    t = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    kw = dict(causal=w.causal, window=w.window, softcap=w.softcap, sink=t["sink"], scale=w.scale,
+              bias=t["bias"], seg_q=t["seg"], seg_k=t["seg"])
+    path = fa.attn_path_name(t["q"], t["k"], t["v"], **kw)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        O, LSE = fa.attn_fwd(t["q"], t["k"], t["v"], **kw)
+        dQ, dK, dV, db, ds = fa.attn_bwd(t["q"], t["k"], t["v"], O, LSE, t["dO"], **kw)
+        return O, dQ, dK, dV, ds
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+
+    # Timed region: K steps, L2 flushed (untimed) before each.
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    launches0 = fa.attn_launch_counter()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    for s in range(args.steps):
+        flush.zero_()
+        ev[s][0].record(stream)
+        fa.attn_profile_next_main_kernel(kev[s][0], kev[s][1])
+        O, LSE = fa.attn_fwd(t["q"], t["k"], t["v"], **kw)
+        fa.attn_profile_next_main_kernel(kev[s][2], kev[s][3])
+        fa.attn_bwd(t["q"], t["k"], t["v"], O, LSE, t["dO"], **kw)
+        ev[s][1].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    launches = fa.attn_launch_counter() - launches0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    fwd_ms = [a.elapsed_time(b) for a, b, _, _ in kev]
+    bwd_ms = [c.elapsed_time(d) for _, _, c, d in kev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    status = fa.attn_check_device_status(dev)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    # End to end through the public API with host buffers: pinned host inputs copied in and
+    # results (O, dQ, dK, dV, dsink) copied out inside the timed region of every step.
+    host = {k: (None if v is None else v.pin_memory()) for k, v in inp.items()}
+    h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v", "dO"))
+    outs = {"O": torch.empty(inp["q"].shape, dtype=inp["q"].dtype).pin_memory(),
+            "dQ": torch.empty(inp["q"].shape, dtype=inp["q"].dtype).pin_memory(),
+            "dK": torch.empty(inp["k"].shape, dtype=inp["k"].dtype).pin_memory(),
+            "dV": torch.empty(inp["v"].shape, dtype=inp["v"].dtype).pin_memory()}
+    d2h = sum(o.numel() * o.element_size() for o in outs.values())
+    if inp["sink"] is not None:
+        outs["dsink"] = torch.empty(inp["sink"].shape, dtype=torch.float32).pin_memory()
+        d2h += outs["dsink"].numel() * 4
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for s in range(args.steps + 1):
+        if s > 0:
+            flush.zero_()
+            e2e_ev[s - 1][0].record(stream)
+        q = host["q"].to(dev, non_blocking=True)
+        k = host["k"].to(dev, non_blocking=True)
+        v = host["v"].to(dev, non_blocking=True)
+        dO = host["dO"].to(dev, non_blocking=True)
+        O, LSE = fa.attn_fwd(q, k, v, **kw)
+        dQ, dK, dV, db, ds = fa.attn_bwd(q, k, v, O, LSE, dO, **kw)
+        outs["O"].copy_(O, non_blocking=True)
+        outs["dQ"].copy_(dQ, non_blocking=True)
+        outs["dK"].copy_(dK, non_blocking=True)
+        outs["dV"].copy_(dV, non_blocking=True)
+        if ds is not None:
+            outs["dsink"].copy_(ds, non_blocking=True)
+        if s > 0:
+            e2e_ev[s - 1][1].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    f_step = flops(w, seg, "fwdbwd")
+    value = f_step * args.steps * world / (total_ms * 1e-3) / 1e12
+    e2e_value = f_step * args.steps * world / (e2e_ms * 1e-3) / 1e12
+    burst, sustained, kind = peaks()
+    # Dominant kernel: the backward main kernel (10*D flops per visible pair).
+    bwd_kernel_ms = statistics.mean(bwd_ms)
+    fwd_kernel_ms = statistics.mean(fwd_ms)
+    bwd_tf = flops(w, seg, "bwd") / (bwd_kernel_ms * 1e-3) / 1e12
+    fwd_tf = flops(w, seg, "fwd") / (fwd_kernel_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,s^2) inputs of the workload's shape; no dataset)",
+        "config": {"workload": w.name, "B": w.B, "S": w.Sq, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "causal": w.causal, "window": w.window, "softcap": w.softcap, "sink": w.sink,
+                   "segments": w.segments, "visible_pairs": visible_pairs(w, seg),
+                   "kernel_path": path, "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
+        "pct_of_bf16_peak": round(100 * value / burst, 2),
+        "fwd_tflops": round(fwd_tf, 3),
+        "bwd_tflops": round(bwd_tf, 3),
+        "roofline": {"bound": "tensor", "kernel": "backward main kernel",
+                     "achieved": round(bwd_tf, 3), "peak": burst, "unit": "TFLOP/s",
+                     "frac": round(bwd_tf / burst, 4), "peak_kind": f"{kind} bf16 burst",
+                     "traffic": None},
+        "clocks": clk,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, seg)
+    return line
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+
+def oracle_sample(w: Workload, inp: dict, S: int):
+    """The workload cut to its first S tokens, batch 0 and kv group 0 (all rows and keys of
+    that cut): a bounded sample of the same shapes, masks and value distributions."""
+    G = w.Hq // w.Hkv
+    sw = w.replace(B=1, Sq=S, Sk=S, Hq=G, Hkv=1)
+    sub = {"q": inp["q"][:1, :S, :G], "k": inp["k"][:1, :S, :1], "v": inp["v"][:1, :S, :1],
+           "dO": inp["dO"][:1, :S, :G],
+           "bias": None if inp["bias"] is None else inp["bias"][:1, :G, :S, :S],
+           "sink": None if inp["sink"] is None else inp["sink"][:G],
+           "seg": None if inp["seg"] is None else inp["seg"][:1, :S]}
+    return sw, sub
+
+
+def time_oracle(w: Workload, inp: dict, S: int):
+    import oracle
+    sw, sub = oracle_sample(w, inp, S)
+    f64 = lambda x: None if x is None else x.to(torch.float32).double().numpy()  # noqa: E731
+    p = oracle.Problem(f64(sub["q"]), f64(sub["k"]), f64(sub["v"]), scale=w.scale, causal=w.causal,
+                       window=w.window, softcap=w.softcap, bias=f64(sub["bias"]),
+                       sink=None if sub["sink"] is None else sub["sink"].double().numpy(),
+                       seg_q=None if sub["seg"] is None else sub["seg"].numpy())
+    t0 = time.perf_counter()
+    O, LSE = oracle.forward(p)
+    oracle.backward(p, f64(sub["dO"]), O, LSE)
+    dt = time.perf_counter() - t0
+    return sw, sub, dt
+
+
+def cpu_baseline(w: Workload, inp: dict, seg):
+    import oracle
+    oracle.build()
+    S = min(w.Sq, 8192)
+    sw, sub, dt = time_oracle(w, inp, S)
+    f = flops(sw, sub["seg"], "fwdbwd")
+    return {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd on the first {S} tokens of batch 0, kv group 0 "
+                      f"({sw.Hq} query heads) of {w.name}; {dt:.1f} s"}
+
+
+def run_reference(args):
+    import oracle
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    S = min(w.Sq, 4096 if w.D >= 256 else 8192)
+    times = []
+    for _ in range(args.warmup):
+        time_oracle(w, inp, S)
+    for _ in range(args.steps):
+        sw, sub, dt = time_oracle(w, inp, S)
+        times.append(dt)
+    f = flops(sw, sub["seg"], "fwdbwd")
+    value = f * len(times) / sum(times) / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"fp64 oracle fwd+bwd on the first {S} tokens of batch 0, kv group 0 "
+              f"({sw.Hq} query heads) of {w.name}")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,s^2) inputs of the workload's shape; no dataset)",
+        "config": {"workload": w.name, "B": w.B, "S": w.Sq, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "causal": w.causal, "window": w.window, "softcap": w.softcap},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from attention_flash_attn_gb300 import build as b
+    if rank == 0 or world == 1:
+        b.build()
+    if world > 1:
+        torch.distributed.barrier()
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+/*
+ * attn_gb300.h -- C ABI of the GB300 (sm_103a) fused attention library.
+ *
+ * One fused attention forward and backward with these score modifications:
+ *   - tanh logit soft-capping t = cap * tanh(u / cap), applied after the scale and the
+ *     additive bias and before masking; its backward chains 1 - tanh^2(u / cap) into dS,
+ *     taken from the finite pre-mask logit
+ *       (TransformerEngine PR #3391 "Thread tanh logit softcapping through FlashAttention",
+ *        intro and "What changed"; openxla/tokamax PR #1121 "Support logits soft-capping in
+ *        the Pallas-Triton attention VJP", PR body);
+ *   - a learnable attention sink: one extra softmax column of logit sink[h] per query head,
+ *     entering each row exactly once and carrying no value; its gradient is
+ *     dsink[h] = -sum_{b,i} p_sink(b,h,i) * (dO_i . O_i)
+ *       (TransformerEngine PR #3551, "What was broken" / "What changed");
+ *   - GQA/MQA: query head h reads kv head h / (Hq / Hkv);
+ *   - causal, sliding-window and packed-segment masks (segment ids or cu_seqlens)
+ *       (MaxText commit message quoted on tokamax PR #1121: sliding window, packing with
+ *        segment ids lowered to cu_seqlens);
+ *   - an optional post-scale additive bias ("post_scale_bias", TransformerEngine PR #3551,
+ *     Greptile finding "Offset Corrupts Bias Gradient Shape": dbias takes the bias's shape).
+ *
+ * Definition (per batch b, query head h, kv head g = h / (Hq / Hkv), query i, key j):
+ *   u_ij   = scale * q_i . k_j + bias[b,h,i,j]
+ *   t_ij   = softcap > 0 ? softcap * tanh(u_ij / softcap) : u_ij
+ *   vis_ij = (!causal || j <= i + Sk - Sq) && (window <= 0 || (i + Sk - Sq) - j < window)
+ *            && (no segments || seg_q[b,i] == seg_k[b,j])
+ *   LSE_i  = ln( [sink ? exp(sink[h]) : 0] + sum_{vis} exp(t_ij) )       (natural log)
+ *   O_i    = sum_{vis} exp(t_ij - LSE_i) v_j
+ * A row with nothing visible and no sink gets O = 0, LSE = -inf and zero gradients.
+ *
+ * Layout: "bshd".  q, O, dO, dQ are [B, Sq, Hq, D]; k, v, dK, dV are [B, Sk, Hkv, D].
+ * q, k, v may be strided (element strides for b, s, h; d is contiguous); O, dO, dQ, dK, dV
+ * are dense.  LSE is float [B, Hq, Sq].  All device pointers.
+ *
+ * Ownership: the caller allocates every input, output and workspace; the library allocates
+ * no device memory and keeps no state besides one-time kernel attributes (set on first use
+ * per device; thread-safe).  Every call is asynchronous on `stream` and never synchronises,
+ * except attn_check_device_status.  Calls on distinct streams with distinct workspaces may
+ * run concurrently.
+ *
+ * Errors: every call validates its arguments first.  On any synchronous error no kernel is
+ * launched and no output is written.  Kernels that give up a bounded wait record it in the
+ * workspace's status word (read with attn_check_device_status) and exit cleanly; they never
+ * trap or spin forever.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *attn_stream_t;
+
+enum attn_dtype {
+    ATTN_DTYPE_BF16 = 1,  /* q, k, v, bias, O, dO, dQ, dK, dV, dbias in bfloat16       */
+    ATTN_DTYPE_F32 = 2    /* ... in float32 (fp32 FFMA kernels, for tight tolerances)   */
+};
+
+enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID = 1,      /* null required pointer, bad shape/stride/alignment,
+                                  negative or NaN softcap, non-finite scale, ...          */
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid but not built: D > 256; cu_seqlens together with
+                                  seg_q / seg_k                                          */
+    ATTN_ERR_WORKSPACE = 3,    /* ws NULL or smaller than the size query returned        */
+    ATTN_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed            */
+    ATTN_ERR_DEVICE = 5        /* a kernel recorded a device-side error (bounded wait
+                                  expired, malformed cu_seqlens) -- attn_check_device_status */
+};
+
+typedef struct {
+    int dtype;                 /* enum attn_dtype                                          */
+    int B, Sq, Sk, Hq, Hkv, D; /* B, Sq, Sk >= 0 (B == 0 or Sq == 0: nothing to compute);
+                                  Hq, Hkv >= 1 with Hq % Hkv == 0; D % 8 == 0, D <= 256   */
+    const void *q;             /* [B,Sq,Hq,D] with the strides below (elements)           */
+    int64_t q_stride_b, q_stride_s, q_stride_h;
+    const void *k;             /* [B,Sk,Hkv,D]                                             */
+    int64_t k_stride_b, k_stride_s, k_stride_h;
+    const void *v;             /* [B,Sk,Hkv,D]                                             */
+    int64_t v_stride_b, v_stride_s, v_stride_h;
+    /* Optional additive bias, logically [B,Hq,Sq,Sk]: element (b,h,i,j) lives at
+     * bias[b*bias_stride_b + h*bias_stride_h + i*Sk + j]; a stride of 0 broadcasts that
+     * dimension.  NULL: no bias.  Same dtype as q.                                        */
+    const void *bias;
+    int64_t bias_stride_b, bias_stride_h;
+    /* Optional packed segments: seg_q [B,Sq] and seg_k [B,Sk] int32 (both or neither).
+     * A pair is visible only if the ids are equal.  Any ids are accepted; runs of
+     * non-decreasing ids additionally let the kernels skip whole tiles.                   */
+    const int32_t *seg_q, *seg_k;
+    /* Alternative to seg_q/seg_k (not both): cu_seqlens [nseq+1] int32 with
+     * cu_seqlens[0] == 0, non-decreasing, cu_seqlens[nseq] <= Sq; requires B == 1 and
+     * Sq == Sk.  Token t belongs to sequence s with cu[s] <= t < cu[s+1]; tokens at or past
+     * cu[nseq] form one extra trailing sequence.  A malformed array is reported through the
+     * device status word.                                                                  */
+    const int32_t *cu_seqlens;
+    int nseq;
+    int causal;                /* nonzero: key j visible to query i only if j <= i + Sk - Sq */
+    int window;                /* > 0: key j visible only if (i + Sk - Sq) - j < window      */
+    float softcap;             /* 0: off; > 0: cap; negative, NaN or inf: ATTN_ERR_INVALID  */
+    const float *sink;         /* optional [Hq] float sink logits; NULL: no sink            */
+    float scale;               /* finite; usually 1/sqrt(D)                                 */
+} attn_args;
+
+/* Bytes of workspace attn_fwd needs for these arguments (256-byte multiple, >= 256). */
+size_t attn_fwd_workspace_size(const attn_args *a);
+
+/*
+ * Forward: O [B,Sq,Hq,D] (dtype of q) and LSE [B,Hq,Sq] float (natural log, sink included).
+ * ws: device workspace of at least attn_fwd_workspace_size(a) bytes, 256-byte aligned,
+ * zero-filled once before its first use (its first 256 bytes hold the sticky device status
+ * word).  Returns an attn_status.
+ */
+int attn_fwd(const attn_args *a, void *O, float *LSE, void *ws, size_t ws_bytes,
+             attn_stream_t stream);
+
+/* Bytes of workspace attn_bwd needs (same rules as attn_fwd_workspace_size). */
+size_t attn_bwd_workspace_size(const attn_args *a);
+
+/*
+ * Backward of O with respect to q, k, v, bias and sink, given dO.
+ *   O, LSE: the forward's outputs for the same arguments; dO [B,Sq,Hq,D] dense.
+ *   dQ [B,Sq,Hq,D], dK/dV [B,Sk,Hkv,D]: dense outputs, overwritten.
+ *   dbias: required iff a->bias != NULL; dense with the bias's own shape
+ *          [bias_stride_b ? B : 1, bias_stride_h ? Hq : 1, Sq, Sk]; broadcast dimensions are
+ *          summed over; overwritten.
+ *   dsink: required iff a->sink != NULL; float [Hq], summed over every batch and row;
+ *          overwritten (not accumulated).
+ * The 1 - tanh^2(u/cap) factor is applied before dK, dQ and dbias are formed, so those are
+ * gradients with respect to the pre-cap logits (tokamax PR #1121, PR body).
+ */
+int attn_bwd(const attn_args *a, const void *O, const float *LSE, const void *dO,
+             void *dQ, void *dK, void *dV, void *dbias, float *dsink,
+             void *ws, size_t ws_bytes, attn_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads and clears the workspace's device status word.
+ * Returns ATTN_OK, ATTN_ERR_DEVICE (a kernel recorded an error since the last check) or
+ * ATTN_ERR_CUDA (the stream itself reported an error).
+ */
+int attn_check_device_status(void *ws, attn_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char *attn_status_string(int status);
+
+/* Kernel path the forward / backward would take for these arguments, for tests and
+ * profiling: "tc" (tcgen05 tensor-core kernels), "simt" (FFMA kernels), or "" when the
+ * arguments are rejected.  Static string. */
+const char *attn_path_name(const attn_args *a);
+
+/*
+ * Profiling hook: the next attn_fwd or attn_bwd call made by this host thread records
+ * `ev_start` (a cudaEvent_t) on its stream immediately before launching its main kernel
+ * (the tensor-core or FFMA attention kernel; for the FFMA backward, the first of its two)
+ * and `ev_end` immediately after its last main kernel, then forgets both.  Passing NULLs
+ * cancels a pending request.  Adds no work to the call.
+ */
+void attn_profile_next_main_kernel(void *ev_start, void *ev_end);
+
+/* Number of kernels this library has launched in this process (all devices), for
+ * accounting in benchmarks; monotonic, thread-safe. */
+uint64_t attn_launch_counter(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,121 @@
+"""Host-side tests of the C ABI: the library builds and loads without a GPU, exports every
+function include/attn_gb300.h declares, and rejects invalid arguments before launching
+anything (no CUDA call is reached in these tests)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from attention_flash_attn_gb300 import build as b
+    b.build()
+    from attention_flash_attn_gb300 import _capi
+    return _capi
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[\w\s\*]+?\b(attn_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_function(capi):
+    names = declared_functions()
+    assert names, "no declarations found"
+    L = capi.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(capi.EXPORTS) == names
+
+
+def valid_args(capi, dtype=1, B=1, S=16, H=2, D=64, **kw):
+    a = capi.AttnArgs()
+    a.dtype, a.B, a.Sq, a.Sk, a.Hq, a.Hkv, a.D = dtype, B, S, S, H, H, D
+    fake = 0x10000  # never dereferenced: only validation runs in these tests
+    a.q = a.k = a.v = fake
+    a.q_stride_b = a.k_stride_b = a.v_stride_b = S * H * D
+    a.q_stride_s = a.k_stride_s = a.v_stride_s = H * D
+    a.q_stride_h = a.k_stride_h = a.v_stride_h = D
+    a.scale = D ** -0.5
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("dtype", 3, 1), ("Hq", 3, 1), ("Hkv", 0, 1), ("D", 60, 1), ("D", 264, 2),
+    ("softcap", -1.0, 1), ("softcap", float("nan"), 1), ("softcap", float("inf"), 1),
+    ("scale", float("inf"), 1), ("q", None, 1), ("q", 0x10008, 1), ("q_stride_s", 12, 1),
+    ("Sq", -1, 1), ("seg_q", 0x20000, 1),
+])
+def test_invalid_arguments_rejected_before_launch(capi, field, value, status):
+    L = capi.lib()
+    a = valid_args(capi, **{field: value})
+    assert L.attn_fwd_workspace_size(ctypes.byref(a)) == 0
+    assert L.attn_fwd(ctypes.byref(a), 0x30000, 0x40000, 0x50000, 1 << 20, None) == status
+    n = L.attn_launch_counter()
+    assert L.attn_bwd(ctypes.byref(a), 0x30000, 0x40000, 0x30000, 0x30000, 0x30000, 0x30000,
+                      None, None, 0x50000, 1 << 20, None) == status
+    assert L.attn_launch_counter() == n
+    assert L.attn_path_name(ctypes.byref(a)) == b""
+
+
+def test_cu_seqlens_with_segments_unsupported_and_shape_rules(capi):
+    L = capi.lib()
+    a = valid_args(capi, seg_q=0x20000, seg_k=0x20000, cu_seqlens=0x21000, nseq=2)
+    assert L.attn_fwd(ctypes.byref(a), 0x30000, 0x40000, 0x50000, 1 << 20, None) == 2
+    a = valid_args(capi, B=2, cu_seqlens=0x21000, nseq=2)
+    assert L.attn_fwd(ctypes.byref(a), 0x30000, 0x40000, 0x50000, 1 << 20, None) == 1
+
+
+def test_missing_outputs_and_workspace(capi):
+    L = capi.lib()
+    a = valid_args(capi)
+    need = L.attn_fwd_workspace_size(ctypes.byref(a))
+    assert need >= 256 and need % 256 == 0
+    assert L.attn_fwd(ctypes.byref(a), None, 0x40000, 0x50000, need, None) == 1
+    assert L.attn_fwd(ctypes.byref(a), 0x30000, 0x40000, None, need, None) == 3
+    assert L.attn_fwd(ctypes.byref(a), 0x30000, 0x40000, 0x50000, need - 1, None) == 3
+    assert L.attn_fwd(ctypes.byref(a), 0x30000, 0x40000, 0x50010, need, None) == 3
+    # dbias required iff bias; dsink iff sink
+    a = valid_args(capi, sink=0x60000)
+    nb = L.attn_bwd_workspace_size(ctypes.byref(a))
+    assert L.attn_bwd(ctypes.byref(a), 0x30000, 0x40000, 0x30000, 0x30000, 0x30000, 0x30000,
+                      None, None, 0x50000, nb, None) == 1
+    a = valid_args(capi, bias=0x70000)
+    assert L.attn_bwd(ctypes.byref(a), 0x30000, 0x40000, 0x30000, 0x30000, 0x30000, 0x30000,
+                      None, None, 0x50000, 1 << 30, None) == 1
+
+
+def test_empty_problem_is_a_no_op(capi):
+    L = capi.lib()
+    for kw in ({"B": 0}, {"Sq": 0}):
+        a = valid_args(capi, **kw)
+        n = L.attn_launch_counter()
+        assert L.attn_fwd(ctypes.byref(a), 0x30000, 0x40000, 0x50000, 1 << 20, None) == 0
+        assert L.attn_launch_counter() == n
+
+
+def test_workspace_grows_with_backward_needs(capi):
+    L = capi.lib()
+    a = valid_args(capi, S=4096, H=8, D=128)
+    f = L.attn_fwd_workspace_size(ctypes.byref(a))
+    b = L.attn_bwd_workspace_size(ctypes.byref(a))
+    assert b >= f + 4 * 8 * 4096  # at least D = rowsum(dO*O)
+    a2 = valid_args(capi, S=4096, H=8, D=128, seg_q=0x20000, seg_k=0x20000)
+    assert L.attn_fwd_workspace_size(ctypes.byref(a2)) > f
+
+
+def test_status_strings(capi):
+    L = capi.lib()
+    for s in range(7):
+        assert L.attn_status_string(s)

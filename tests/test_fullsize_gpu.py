@@ -1,0 +1,52 @@
+"""Full-size workloads, in the launch configuration bench.py times, checked against the fp64
+oracle on samples it can compute: every row of O / LSE and sampled rows of dQ and columns
+of dK / dV for one (batch, kv group), plus dsink over every batch for that group.
+Same tolerance as the small cases (Frobenius-relative 1e-2 for bf16)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import TOL, frob_rel, problem_from_inputs, run_gpu, to64
+from workloads import WORKLOADS, make_inputs
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def sample_positions(S, seg_row=None):
+    pos = {0, 1, 63, 64, 127, 128, 129, S // 2 - 1, S // 2, S - 129, S - 128, S - 2, S - 1}
+    if seg_row is not None:
+        b = np.flatnonzero(np.diff(seg_row)) + 1
+        for x in b[:6]:
+            pos |= {int(x) - 1, int(x)}
+    return sorted(p for p in pos if 0 <= p < S)
+
+
+@pytest.mark.parametrize("name", ["gemma2_local_w4096_cap50", "gemma2_local_w4096_cap0",
+                                  "packed_varlen_cap30", "sink_gqa64_cap0", "sink_gqa64_cap30",
+                                  "long_noncausal_16k_cap50", "long_causal_32k_cap50"])
+def test_fullsize_sampled(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    gpu = run_gpu(w, inp)
+    tol = TOL[w.dtype]
+    g = w.Hkv - 1
+    G = w.Hq // w.Hkv
+    heads = list(range(g * G, (g + 1) * G))
+    batches = list(range(w.B)) if w.sink else [w.B - 1]
+    p = problem_from_inputs(w, inp, heads=[g], batches=batches)
+    O, LSE = oracle.forward(p)
+    seg_row = None if inp["seg"] is None else inp["seg"][batches[-1]].numpy()
+    rows = sample_positions(w.Sq, seg_row)
+    ref = oracle.backward(p, to64(inp["dO"])[batches][:, :, heads], O, LSE, rows=rows, cols=rows)
+    Og = to64(gpu["O"])[batches][:, :, heads]
+    errs = {"O": frob_rel(Og, O)}
+    Lg = to64(gpu["LSE"])[batches][:, heads]
+    errs["LSE"] = frob_rel(Lg, LSE)
+    errs["dq"] = frob_rel(to64(gpu["dq"])[batches][:, rows][:, :, heads], ref["dq"][:, rows])
+    errs["dk"] = frob_rel(to64(gpu["dk"])[batches][:, rows][:, :, [g]], ref["dk"][:, rows])
+    errs["dv"] = frob_rel(to64(gpu["dv"])[batches][:, rows][:, :, [g]], ref["dv"][:, rows])
+    if w.sink:
+        errs["dsink"] = frob_rel(gpu["dsink"].double().cpu().numpy()[heads], ref["dsink"])
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, (name, errs)

@@ -1,0 +1,189 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element by element
+(Frobenius-relative error per output), on seeded inputs.
+
+Tolerances (max Frobenius-relative error of O, dQ, dK, dV, dbias, dsink): 1e-5 for fp32
+inputs, 1e-2 for bf16 inputs.  Sizes here span several 128-row tiles with a ragged tail;
+the full-size workloads are checked on sampled rows/columns in test_fullsize_gpu.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import TOL, compare_full, frob_rel, full_oracle, problem_from_inputs, run_gpu, to64
+from workloads import WORKLOADS, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+W = WORKLOADS
+# Scaled-down versions of each workload: same dtype, head dim, masks, cap, sink, GQA ratio
+# and value distributions, with ragged lengths that span several tiles.
+SMALL = [
+    W["tiny_f32_softcap_bias"],
+    W["gemma2_local_w4096_cap50"].replace(name="gemma2_small_cap50", B=1, Sq=700, Sk=700, Hq=4, Hkv=2, window=300),
+    W["gemma2_local_w4096_cap0"].replace(name="gemma2_small_cap0", B=1, Sq=700, Sk=700, Hq=4, Hkv=2, window=300),
+    W["packed_varlen_cap30"].replace(name="packed_small", B=2, Sq=1000, Sk=1000, Hq=2, Hkv=2, run_lo=40, run_hi=400),
+    W["sink_gqa64_cap0"].replace(name="sink_small_cap0", B=2, Sq=520, Sk=520, Hq=8, Hkv=2),
+    W["sink_gqa64_cap30"].replace(name="sink_small_cap30", B=2, Sq=520, Sk=520, Hq=8, Hkv=2),
+    W["long_causal_32k_cap50"].replace(name="long_small_causal", Sq=900, Sk=900, Hq=2, Hkv=1),
+    W["long_noncausal_16k_cap50"].replace(name="long_small_noncausal", Sq=650, Sk=650, Hq=2, Hkv=1),
+]
+
+
+def check(w, gpu, ref):
+    errs = compare_full(w, gpu, ref)
+    tol = TOL[w.dtype]
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, (w.name, errs)
+    return errs
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_parity_small(w):
+    inp = make_inputs(w)
+    gpu = run_gpu(w, inp)
+    ref = full_oracle(w, inp)
+    check(w, gpu, ref)
+
+
+def test_softcap_really_active_in_capped_workloads():
+    """The capped workloads drive pre-cap logits well past the cap (as the softcap pages'
+    own validation did with cap 30 and logits up to 168)."""
+    for w in (SMALL[0], SMALL[1], SMALL[6]):
+        inp = make_inputs(w)
+        q, k = to64(inp["q"])[0, :, 0], to64(inp["k"])[0, :, 0]
+        u = w.scale * q @ k.T
+        assert np.abs(u).max() > 1.5 * w.softcap, w.name
+
+
+EDGE = [
+    # Sq != Sk: bottom-right causal alignment, ragged tails on both axes
+    Workload("edge_sq_lt_sk", "bf16", B=1, Sq=200, Sk=333, Hq=2, Hkv=1, D=128, causal=True, softcap=30.0),
+    Workload("edge_sq_gt_sk", "bf16", B=1, Sq=300, Sk=130, Hq=2, Hkv=2, D=64, causal=True, sink=True),
+    # MQA, window without causal
+    Workload("edge_mqa_window_noncausal", "bf16", B=2, Sq=257, Sk=257, Hq=4, Hkv=1, D=64, causal=False,
+             window=100, softcap=20.0),
+    # single token
+    Workload("edge_single_token", "bf16", B=1, Sq=1, Sk=1, Hq=2, Hkv=1, D=64, causal=True, sink=True),
+    # bf16 with a bias (FFMA path), bias broadcast over batch
+    Workload("edge_bf16_bias", "bf16", B=2, Sq=130, Sk=130, Hq=2, Hkv=2, D=64, causal=True, softcap=10.0,
+             bias=True, q_std=2.0),
+    # fp32 with sink, GQA, window and segments all at once
+    Workload("edge_f32_everything", "f32", B=2, Sq=190, Sk=190, Hq=4, Hkv=2, D=32, causal=True, window=70,
+             softcap=5.0, sink=True, segments=True, run_lo=20, run_hi=90, q_std=2.0, bias=True),
+]
+
+
+@pytest.mark.parametrize("w", EDGE, ids=lambda w: w.name)
+def test_parity_edge(w):
+    inp = make_inputs(w)
+    check(w, run_gpu(w, inp), full_oracle(w, inp))
+
+
+def test_fully_masked_rows_with_and_without_sink():
+    """Queries whose segment id has no key: O = 0, LSE = -inf (no sink) or sink."""
+    w = Workload("masked_rows", "bf16", B=1, Sq=160, Sk=160, Hq=2, Hkv=1, D=64, causal=False)
+    inp = make_inputs(w)
+    seg_q = torch.zeros(1, 160, dtype=torch.int32)
+    seg_q[:, 100:] = 7
+    seg_k = torch.zeros(1, 160, dtype=torch.int32)
+    for sink in (None, torch.tensor([0.5, -1.0])):
+        inp["sink"] = sink
+        gpu = run_gpu(w, {**inp, "seg": None}, seg_q=seg_q.cuda(), seg_k=seg_k.cuda())
+        p = problem_from_inputs(w, {**inp, "seg": None})
+        p.seg_q, p.seg_k = seg_q.numpy(), seg_k.numpy()
+        O, LSE = oracle.forward(p)
+        g = oracle.backward(p, to64(inp["dO"]), O, LSE)
+        assert torch.all(gpu["O"][:, 100:] == 0)
+        assert frob_rel(to64(gpu["O"]), O) <= 1e-2
+        assert frob_rel(to64(gpu["dq"]), g["dq"]) <= 1e-2
+        assert frob_rel(to64(gpu["dk"]), g["dk"]) <= 1e-2
+        lse = to64(gpu["LSE"])
+        if sink is None:
+            assert np.all(np.isneginf(lse[..., 100:]))
+        else:
+            np.testing.assert_allclose(lse[0, :, 100:], sink.numpy()[:, None].repeat(60, 1), rtol=1e-6)
+
+
+def test_non_monotone_segment_ids():
+    """Arbitrary (interleaved) ids: visibility is id equality pair by pair."""
+    w = Workload("interleaved", "bf16", B=1, Sq=300, Sk=300, Hq=2, Hkv=2, D=64, causal=True, softcap=30.0)
+    inp = make_inputs(w)
+    inp["seg"] = (torch.arange(300, dtype=torch.int32) % 3).view(1, 300)
+    check(w, run_gpu(w, inp), full_oracle(w, inp))
+
+
+def test_cu_seqlens_equals_segment_ids():
+    w = Workload("cu", "bf16", B=1, Sq=700, Sk=700, Hq=2, Hkv=1, D=128, causal=True, softcap=30.0, sink=True)
+    inp = make_inputs(w)
+    lens = [130, 1, 250, 319]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    seg = torch.repeat_interleave(torch.arange(len(lens), dtype=torch.int32), torch.tensor(lens)).view(1, -1)
+    a = run_gpu(w, {**inp, "seg": None}, cu_seqlens=cu.cuda())
+    b = run_gpu(w, {**inp, "seg": seg})
+    for k in ("O", "LSE", "dq", "dk", "dv", "dsink"):
+        assert torch.equal(a[k], b[k]), k
+    check(w, b, full_oracle(w, {**inp, "seg": seg}))
+
+
+def test_cross_segment_perturbation_bit_identical():
+    """Changing every input of one packed segment leaves the other segments' outputs and
+    gradients bit-identical (no attention across boundaries, incl. a tile-unaligned one)."""
+    w = W["packed_varlen_cap30"].replace(name="leak", B=1, Sq=640, Sk=640, Hq=2, Hkv=2)
+    inp = make_inputs(w)
+    seg = torch.zeros(1, 640, dtype=torch.int32)
+    seg[:, 200:] = 1   # boundary at 200: not a multiple of 64 or 128
+    seg[:, 450:] = 2
+    inp["seg"] = seg
+    a = run_gpu(w, inp)
+    g = torch.Generator().manual_seed(1)
+    inp2 = dict(inp)
+    sel = (seg[0] == 1)
+    for key in ("q", "k", "v", "dO"):
+        t = inp[key].clone()
+        t[:, sel] = (torch.randn(t[:, sel].shape, generator=g) * 3).to(t.dtype)
+        inp2[key] = t
+    b = run_gpu(w, inp2)
+    keep = ~sel.cuda()
+    for key in ("O", "dq", "dk", "dv"):
+        assert torch.equal(a[key][:, keep], b[key][:, keep]), key
+    assert torch.equal(a["LSE"][..., keep], b["LSE"][..., keep])
+
+
+def test_strided_qkv_views():
+    """q, k, v as views into one packed [B, S, 3, H, D] tensor (non-dense strides)."""
+    w = Workload("strided", "bf16", B=2, Sq=200, Sk=200, Hq=2, Hkv=2, D=64, causal=True, softcap=30.0)
+    inp = make_inputs(w)
+    packed = torch.stack([inp["q"], inp["k"], inp["v"]], dim=2).cuda()  # [B,S,3,H,D]
+    q, k, v = packed[:, :, 0], packed[:, :, 1], packed[:, :, 2]
+    assert not q.is_contiguous()
+    import attention_flash_attn_gb300 as fa
+    O, LSE = fa.attn_fwd(q, k, v, causal=True, softcap=30.0)
+    O2, LSE2 = fa.attn_fwd(q.contiguous(), k.contiguous(), v.contiguous(), causal=True, softcap=30.0)
+    assert torch.equal(O, O2) and torch.equal(LSE, LSE2)
+
+
+def test_empty_key_axis_and_empty_queries():
+    import attention_flash_attn_gb300 as fa
+    q = torch.randn(1, 5, 2, 64, device="cuda").bfloat16()
+    k = torch.randn(1, 0, 1, 64, device="cuda").bfloat16()
+    sink = torch.tensor([0.25, 2.0], device="cuda")
+    O, LSE = fa.attn_fwd(q, k, k, sink=sink)
+    assert torch.all(O == 0) and torch.allclose(LSE, sink.view(1, 2, 1).expand(1, 2, 5))
+    O, LSE = fa.attn_fwd(q, k, k)
+    assert torch.all(O == 0) and torch.all(torch.isneginf(LSE))
+    q0 = torch.randn(1, 0, 2, 64, device="cuda").bfloat16()
+    k0 = torch.randn(1, 9, 1, 64, device="cuda").bfloat16()
+    O, LSE = fa.attn_fwd(q0, k0, k0)
+    dQ, dK, dV, _, ds = fa.attn_bwd(q0, k0, k0, O, LSE, O, sink=sink)
+    assert torch.all(dK == 0) and torch.all(dV == 0) and torch.all(ds == 0)
+
+
+def test_forward_deterministic():
+    w = SMALL[3]
+    inp = make_inputs(w)
+    a = run_gpu(w, inp)
+    b = run_gpu(w, inp)
+    for k in ("O", "LSE", "dk", "dv", "dsink"):
+        assert torch.equal(a[k], b[k]), k
+    assert frob_rel(to64(a["dq"]), to64(b["dq"])) <= 1e-6
