@@ -30,6 +30,7 @@ struct Layout {
 bool use_tc(const attn_args *a) {
   return a->dtype == ATTN_DTYPE_BF16 && a->bias == nullptr && a->Sk > 0 && tc_supported(a->D);
 }
+bool use_tc_bwd(const attn_args *a) { return use_tc(a) && tc_bwd_supported(a->D); }
 
 size_t dbias_elems(const attn_args *a) {
   if (!a->bias) return 0;
@@ -54,7 +55,7 @@ Layout layout(const attn_args *a, bool bwd) {
       L.dsink_part = off;
       off += align_up((size_t)a->Hq * bwd_pre_partials(a->B, a->Sq) * sizeof(float));
     }
-    if (use_tc(a)) { L.dqacc = off; off += align_up((size_t)a->B * a->Sq * a->Hq * a->D * sizeof(float)); }
+    if (use_tc_bwd(a)) { L.dqacc = off; off += align_up((size_t)a->B * a->Sq * a->Hq * a->D * sizeof(float)); }
     if (a->bias) { L.dbias_acc = off; off += align_up(dbias_elems(a) * sizeof(float)); }
   }
   L.total = off;
@@ -169,7 +170,7 @@ size_t attn_bwd_workspace_size(const attn_args *a) {
 
 const char *attn_path_name(const attn_args *a) {
   if (validate(a) != ATTN_OK) return "";
-  return use_tc(a) ? "tc" : "simt";
+  return use_tc(a) ? (use_tc_bwd(a) ? "tc" : "tc-fwd/simt-bwd") : "simt";
 }
 
 int attn_fwd(const attn_args *a, void *O, float *LSE, void *ws, size_t ws_bytes, attn_stream_t stream) {
@@ -221,7 +222,7 @@ int attn_bwd(const attn_args *a, const void *O, const float *LSE, const void *dO
   p.Dvec = reinterpret_cast<float *>(w + L.dvec);
   p.dsink_part = a->sink ? reinterpret_cast<float *>(w + L.dsink_part) : nullptr;
   p.n_part = bwd_pre_partials(a->B, a->Sq);
-  const bool tc = use_tc(a);
+  const bool tc = use_tc_bwd(a);
   p.dQacc = tc ? reinterpret_cast<float *>(w + L.dqacc) : nullptr;
   p.dbias_acc = a->bias ? reinterpret_cast<float *>(w + L.dbias_acc) : nullptr;
   if ((s = run_meta(a, p, st)) != ATTN_OK) return s;

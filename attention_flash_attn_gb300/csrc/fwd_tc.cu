@@ -1,0 +1,409 @@
+// fwd_tc.cu -- tcgen05 tensor-core forward for bf16, D in {64, 128, 256}.
+//
+// One CTA computes one 128-row query tile of one (batch, query head):
+//   warp 0      TMA producer: the Q tile once, then K/V tiles into an NS-deep ring;
+//   warp 1      MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one of two TMEM
+//               score buffers, then O += P_{j-1} V_{j-1} with P read from TMEM;
+//   warps 2..5  softmax: each thread owns one query row (= one TMEM lane).  Per KV tile it
+//               reads its row of S, applies scale, the tanh soft-cap and the mask, keeps a
+//               running max / sum (started from the sink column, so the sink enters the
+//               row exactly once), writes P as bf16 over the score buffer, and rescales the
+//               O accumulator in TMEM only when the running max grew by more than 2^8.
+//               At the end it normalises O, writes O (bf16) and LSE (natural log).
+// The score modification follows the soft-capping pages: cap * tanh(u / cap) applied
+// after the scale and before the mask (TransformerEngine PR #3391; tokamax PR #1121).
+// The sink column's role follows TransformerEngine PR #3551 ("What changed").
+//
+// Every wait is bounded: a wait that gives up records kStatusWaitTimeout in the status
+// word and the CTA winds down without trapping.
+#include "common.cuh"
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace attn {
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128;
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;  // tolerate P <= 2^8 before rescaling O
+
+template <int D, int BN, int NS>
+struct FwdCfg {
+  static constexpr int KCH = D / 64;
+  static constexpr int Q_BYTES = kBM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = Q_BYTES;
+  static constexpr int OFF_V = OFF_K + NS * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + NS * KV_BYTES;
+  static constexpr int NBAR = 1 + 2 * NS + 5;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;
+  static constexpr int TM_O = 2 * BN;
+  static constexpr int TM_COLS = 512;
+  static_assert(2 * BN + D <= TM_COLS, "TMEM budget");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(KV_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzle atoms must stay 1 KiB aligned");
+};
+
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int e = 0; e < N; ++e) asm volatile("" : "+r"(r[e]));
+}
+
+__device__ __forceinline__ int lower_bound_i(const int *a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(a + mid) < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+__device__ __forceinline__ int upper_bound_i(const int *a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(a + mid) <= x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int D, int BN, int NS>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using C = FwdCfg<D, BN, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // A wait elsewhere already gave up: do nothing (the caller learns it from the status word).
+  if (status_peek(p.status) & kStatusWaitTimeout) return;
+
+  const int nqt = (p.Sq + kBM - 1) / kBM;
+  const int qt = nqt - 1 - (int)blockIdx.x;  // latest (heaviest under causal) tiles first
+  const int h = blockIdx.y, b = blockIdx.z, g = h / p.G;
+  const int i0 = qt * kBM, i1 = min(i0 + kBM, p.Sq) - 1;
+  const int off = p.Sk - p.Sq;
+
+  // Keys this query tile can see (uniform across the CTA).
+  int klo = 0, khi = p.Sk;
+  if (p.window > 0) klo = max(klo, i0 + off - p.window + 1);
+  if (p.causal) khi = min(khi, i1 + off + 1);
+  if (p.qrange) {
+    const int nt = (p.Sq + 63) / 64;
+    const int2 a = p.qrange[(size_t)b * nt + i0 / 64], c = p.qrange[(size_t)b * nt + i1 / 64];
+    klo = max(klo, min(a.x, c.x));
+    khi = min(khi, max(a.y, c.y));
+  }
+  const int t0 = klo / BN;
+  const int n = (klo < khi) ? (khi + BN - 1) / BN - t0 : 0;
+
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t q_full = bar0;
+  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + NS + s); };
+  auto s_full = [&](int x) { return bar0 + 8u * (1 + 2 * NS + x); };
+  auto p_full = [&](int x) { return bar0 + 8u * (3 + 2 * NS + x); };
+  const uint32_t o_done = bar0 + 8u * (5 + 2 * NS);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  int *red = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(s_full(x), 1);
+      mbar_init(p_full(x), 128);
+    }
+    mbar_init(o_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0 && (tmem & 0xFFFFu) + C::TM_COLS > 512) set_status(p.status, kStatusBadTmemAlloc);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c)
+        tma_load_4d(sbase + C::OFF_Q + c * (kBM * 128), &tmQ, q_full, c * 64, i0, h, b);
+      for (int j = 0; j < n; ++j) {
+        const int s = j % NS;
+        if (j >= NS && !mbar_wait(kv_empty(s), ((j / NS) - 1) & 1, p.status)) break;
+        mbar_arrive_expect_tx(kv_full(s), 2 * C::KV_BYTES);
+        const int kt = (t0 + j) * BN;
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES + c * (BN * 128), &tmK, kv_full(s), c * 64, kt, g, b);
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(sbase + C::OFF_V + s * C::KV_BYTES + c * (BN * 128), &tmV, kv_full(s), c * 64, kt, g, b);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idS = idesc_bf16(kBM, BN, false, false);
+      constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
+      bool ok = mbar_wait(q_full, 0, p.status);
+      for (int j = 0; ok && j <= n; ++j) {
+        if (j < n) {
+          const int s = j % NS;
+          if (!mbar_wait(kv_full(s), (j / NS) & 1, p.status)) break;
+          tc_fence_after();
+          const uint32_t dS = tmem + (uint32_t)((j & 1) * BN);
+          const uint32_t qa = sbase + C::OFF_Q, ka = sbase + C::OFF_K + s * C::KV_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad = sw128_desc(qa + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = sw128_desc(ka + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
+            mma_ss(dS, ad, bd, idS, kk > 0);
+          }
+          mma_commit(s_full(j & 1));
+        }
+        if (j >= 1) {
+          const int jj = j - 1, s = jj % NS;
+          if (!mbar_wait(p_full(jj & 1), (jj >> 1) & 1, p.status)) break;
+          tc_fence_after();
+          const uint32_t va = sbase + C::OFF_V + s * C::KV_BYTES;
+          const uint32_t pa = tmem + (uint32_t)((jj & 1) * BN);
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t bd = sw128_desc(va + kk * (16 * 128), BN * 128, 1024);
+            mma_ts(tmem + C::TM_O, pa + kk * 8, bd, idO, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(kv_empty(s));
+          mma_commit(o_done);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int wq = warp & 3;  // TMEM sub-partition of this warp
+    const int r = wq * 32 + lane;
+    const int i = i0 + r;
+    const bool row_ok = i < p.Sq;
+    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+
+    const int ip = i + off;
+    int lo = 0, hi = p.Sk;
+    if (p.window > 0) lo = max(lo, ip - p.window + 1);
+    if (p.causal) hi = min(hi, ip + 1);
+    bool seg_pairwise = false;
+    int sid = 0;
+    const int *segk = nullptr;
+    if (p.seg_q && row_ok) {
+      sid = __ldg(p.seg_q + (size_t)b * p.Sq + i);
+      segk = p.seg_k + (size_t)b * p.Sk;
+      if (p.seg_mono[b]) {
+        lo = max(lo, lower_bound_i(segk, p.Sk, sid));
+        hi = min(hi, upper_bound_i(segk, p.Sk, sid));
+      } else {
+        seg_pairwise = true;
+      }
+    }
+    if (!row_ok) {  // never stored; neutral for the tile classification
+      lo = 0;
+      hi = p.Sk;
+    }
+    {
+      int mlo = __reduce_max_sync(0xffffffffu, lo);
+      int mhi = __reduce_min_sync(0xffffffffu, hi);
+      if (lane == 0) {
+        red[wq] = mlo;
+        red[4 + wq] = mhi;
+      }
+    }
+    softmax_bar();
+    const int cta_lo = max(max(red[0], red[1]), max(red[2], red[3]));
+    const int cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
+    const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
+
+    const bool has_cap = p.cap > 0.f;
+    const float sc2 = p.scale * kLog2e;                        // uncapped: t2 = s * sc2
+    const float capc = -2.f * kLog2e * p.scale * p.inv_cap;    // e = 2^(|s| * capc) = exp(-2|u|/cap)
+    const float cap2 = p.cap * kLog2e;                         // t2 = tanh * cap * log2(e)
+    float m_ref = p.sink ? p.sink[h] * kLog2e : -INFINITY;     // running max (log2 units)
+    float l = p.sink ? 1.f : 0.f;                              // running sum relative to m_ref
+    bool ok = true;
+
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait(s_full(j & 1), (j >> 1) & 1, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sa = lane_addr + (uint32_t)((j & 1) * BN);
+      uint32_t xr[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(sa + c * 32, *reinterpret_cast<uint32_t(*)[32]>(xr + c * 32));
+      tmem_wait_ld();
+      reg_fence(xr);
+
+      const int j0 = (t0 + j) * BN;
+      const bool full = !any_pairwise && j0 >= cta_lo && j0 + BN <= cta_hi;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < BN; ++e) {
+        const float s = __uint_as_float(xr[e]);
+        float t2;
+        if (has_cap) {
+          const float ee = ex2_approx(fabsf(s) * capc);
+          const float th = (1.f - ee) * rcp_approx(1.f + ee);
+          t2 = copysignf(th * cap2, s);
+        } else {
+          t2 = s * sc2;
+        }
+        if (!full) {
+          const int jj = j0 + e;
+          bool vis = jj >= lo && jj < hi;
+          if (seg_pairwise) vis = vis && __ldg(segk + jj) == sid;
+          t2 = vis ? t2 : -INFINITY;
+        }
+        xr[e] = __float_as_uint(t2);
+        mx = fmaxf(mx, t2);
+      }
+
+      const float m_new = fmaxf(m_ref, mx);
+      float alpha_o = 1.f;
+      bool resc = false;
+      if (m_new != -INFINITY) {
+        if (j == 0 || m_ref == -INFINITY) {
+          // first finite max: O is either about to be overwritten (j == 0) or all-zero
+          l = (m_ref == -INFINITY) ? 0.f : l * ex2_approx(m_ref - m_new);
+          m_ref = m_new;
+        } else if (m_new > m_ref + kRescaleLog2) {
+          alpha_o = ex2_approx(m_ref - m_new);
+          l *= alpha_o;
+          m_ref = m_new;
+          resc = true;
+        }
+      }
+      const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float rs = 0.f;
+      uint32_t pk[BN / 2];
+#pragma unroll
+      for (int e = 0; e < BN / 2; ++e) {
+        const float p0 = ex2_approx(__uint_as_float(xr[2 * e]) - mr);
+        const float p1 = ex2_approx(__uint_as_float(xr[2 * e + 1]) - mr);
+        rs += p0 + p1;
+        pk[e] = pack_bf16(p0, p1);
+      }
+      l += rs;
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) tmem_st32(sa + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + c * 32));
+      if constexpr (BN / 2 < 32) tmem_st16(sa, pk);
+
+      if (j >= 1 && !mbar_wait(o_done, (j - 1) & 1, p.status)) ok = false;
+      if (j >= 1 && __any_sync(0xffffffffu, resc)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(lane_addr + C::TM_O + c * 32, orr);
+          tmem_wait_ld();
+          reg_fence(orr);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha_o);
+          tmem_st32(lane_addr + C::TM_O + c * 32, orr);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full(j & 1));
+      if (!ok) break;
+    }
+
+    if (ok && n > 0) {
+      ok = mbar_wait(o_done, (n - 1) & 1, p.status);
+      tc_fence_after();
+    }
+    const bool has = l > 0.f;
+    const float inv = has ? 1.f / l : 0.f;
+    const float lse = has ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) + (((size_t)b * p.Sq + i) * p.Hq + h) * D;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t orr[32];
+      if (n > 0) {
+        tmem_ld32(lane_addr + C::TM_O + c * 32, orr);
+        tmem_wait_ld();
+        reg_fence(orr);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) orr[e] = 0u;
+      }
+      if (row_ok) {
+        uint32_t out[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          out[e] = pack_bf16(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
+      }
+    }
+    if (row_ok) p.LSE[((size_t)b * p.Hq + h) * p.Sq + i] = lse;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TM_COLS);
+  }
+}
+
+template <int D, int BN, int NS>
+cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
+  using C = FwdCfg<D, BN, NS>;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bshd(&tq, p.q, D, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, kBM) ||
+      !make_tmap_bshd(&tk, p.k, D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, BN) ||
+      !make_tmap_bshd(&tv, p.v, D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, BN))
+    return cudaErrorInvalidValue;
+  auto kern = fwd_tc_kernel<D, BN, NS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.Sq + kBM - 1) / kBM, p.Hq, p.B);
+  kern<<<grid, kThreads, C::SMEM, st>>>(tq, tk, tv, p);
+  return counted(cudaGetLastError());
+}
+
+}  // namespace
+
+bool tc_supported(int D) { return D == 64 || D == 128 || D == 256; }
+
+cudaError_t tc_forward(const Params &p, cudaStream_t st) {
+  switch (p.D) {
+    case 64: return launch_fwd<64, 128, 4>(p, st);
+    case 128: return launch_fwd<128, 128, 2>(p, st);
+    case 256: return launch_fwd<256, 64, 2>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace attn

@@ -39,7 +39,8 @@ cudaError_t launch_bwd_post(const Params &p, int dtype, bool convert_dq, size_t 
                             cudaStream_t st);
 
 // tcgen05 tensor-core kernels (bf16, D in {64, 128, 256}).
-bool tc_supported(int D);
+bool tc_supported(int D);      // forward
+bool tc_bwd_supported(int D);  // backward
 cudaError_t tc_forward(const Params &p, cudaStream_t st);
 cudaError_t tc_backward(const Params &p, cudaStream_t st);
 

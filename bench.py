@@ -153,6 +153,8 @@ def run_ours(args, rank, world, local_rank):
     # Timed region: K steps, L2 flushed (untimed) before each.
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for e in [x for pair in ev for x in pair] + [x for four in kev for x in four]:
+        e.record(stream)  # torch creates the CUDA event lazily, on first record
     clocks = ClockSampler(local_rank)
     clocks.start()
     launches0 = fa.attn_launch_counter()
