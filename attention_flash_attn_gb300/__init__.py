@@ -15,7 +15,7 @@ import torch
 from . import _capi
 from ._capi import AttnArgs, AttnError, lib  # noqa: F401
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_check_device_status", "attn_path_name",
+__all__ = ["attn_fwd", "attn_fwd_noalloc", "attn_bwd", "attn_check_device_status", "attn_path_name",
            "attn_launch_counter", "attn_profile_next_main_kernel", "AttnError", "build_args"]
 
 _DTYPES = {torch.bfloat16: _capi.ATTN_DTYPE_BF16, torch.float32: _capi.ATTN_DTYPE_F32}
@@ -109,6 +109,21 @@ def attn_fwd(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=N
     ws = _workspace(q.device, need)
     _check(L.attn_fwd(ctypes.byref(a), O.data_ptr(), LSE.data_ptr(), ws.data_ptr(), ws.numel(),
                       _stream(q.device)), "attn_fwd")
+    del keep
+    return O, LSE
+
+
+def attn_fwd_noalloc(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
+                     bias=None, seg_q=None, seg_k=None, cu_seqlens=None, out=None, lse=None):
+    """attn_fwd with the library's built-in scratch instead of a workspace (for callers that
+    cannot allocate device memory; see include/attn_gb300.h).  Returns (O, LSE)."""
+    a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
+                         scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens)
+    B, Sq, Hq, D = q.shape
+    O = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device) if out is None else out
+    LSE = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(lib().attn_fwd_noalloc(ctypes.byref(a), O.data_ptr(), LSE.data_ptr(), _stream(q.device)),
+           "attn_fwd_noalloc")
     del keep
     return O, LSE
 

@@ -26,7 +26,7 @@ ATTN_ERR_DEVICE = 5
 EXPORTS = (
     "attn_fwd_workspace_size", "attn_fwd", "attn_bwd_workspace_size", "attn_bwd",
     "attn_check_device_status", "attn_status_string", "attn_path_name", "attn_launch_counter",
-    "attn_profile_next_main_kernel",
+    "attn_profile_next_main_kernel", "attn_fwd_noalloc",
 )
 
 
@@ -71,6 +71,8 @@ def lib():
         L.attn_bwd_workspace_size.restype = sz
         L.attn_fwd.argtypes = [A, vp, vp, vp, sz, vp]
         L.attn_fwd.restype = ctypes.c_int
+        L.attn_fwd_noalloc.argtypes = [A, vp, vp, vp]
+        L.attn_fwd_noalloc.restype = ctypes.c_int
         L.attn_bwd.argtypes = [A, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.attn_bwd.restype = ctypes.c_int
         L.attn_check_device_status.argtypes = [vp, vp]

@@ -119,6 +119,26 @@ size_t attn_fwd_workspace_size(const attn_args *a);
 int attn_fwd(const attn_args *a, void *O, float *LSE, void *ws, size_t ws_bytes,
              attn_stream_t stream);
 
+/*
+ * attn_fwd without a caller-provided workspace, for callers that cannot allocate device
+ * memory: plugins hosted by a runtime that owns every device allocation and hands them no
+ * allocator, or deployments whose device-memory budget is fixed up front.  The pages this
+ * library follows have no counterpart to this entry point.
+ *
+ * Computes exactly what attn_fwd computes (same arguments, same outputs, same errors), with
+ * its scratch taken from a 4 MiB array compiled into the library (one per GPU that loads the
+ * library, resident until the process exits).  Calls whose attn_fwd_workspace_size exceeds
+ * 4 MiB are rejected with ATTN_ERR_WORKSPACE before anything is launched.  It allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * The first call on a device looks up the array's device address (with that device
+ * current); make that first call before any stream capture.  Every call shares the array:
+ * calls whose work overlaps on the GPU (other streams, other threads) race and must not be
+ * issued.  Each call clears the status word at its start, so device-side errors cannot be
+ * read back through attn_check_device_status for this entry point.
+ */
+int attn_fwd_noalloc(const attn_args *a, void *O, float *LSE, attn_stream_t stream);
+
 /* Bytes of workspace attn_bwd needs (same rules as attn_fwd_workspace_size). */
 size_t attn_bwd_workspace_size(const attn_args *a);
 
