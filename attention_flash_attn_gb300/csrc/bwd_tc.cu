@@ -1,8 +1,604 @@
-// bwd_tc.cu -- tcgen05 tensor-core backward (bf16).  Not yet built: the FFMA backward
-// serves every call until it lands.
+// bwd_tc.cu -- tcgen05 tensor-core backward for bf16, D in {64, 128, 256}.
+//
+// One CTA owns one 128-key tile of one (batch, kv head).  It keeps K and V in shared memory,
+// loops over the query heads of its GQA group and the query steps (BQ rows) that can see the
+// tile, and accumulates dV and dK for its keys in tensor memory:
+//
+//   S^T  = K Q^T          (M = 128 keys, N = BQ)       -> TMEM
+//   dP^T = V dO^T                                      -> TMEM
+//   softmax warpgroup (one key per thread = TMEM lane): t = cap*tanh(u/cap), mask,
+//       P = exp(t - LSE_q), dS = P (dP - D_q) (1 - tanh^2(u/cap)) * scale
+//       -> P^T (bf16) into TMEM, dS^T (bf16, 128-byte swizzled) into shared memory
+//   dV  += P^T dO         (A = P^T from TMEM)
+//   dK  += dS^T Q         (A = dS^T from shared memory)
+//   dQ  = dS K  (or dQ^T = K^T dS^T)   -> TMEM, drained by a fourth warpgroup into the fp32
+//       dQ accumulator with red.global.add
+//
+// The chain-rule factor is applied before dK, dQ (and so dbias would be) formed, as the
+// tokamax soft-capping VJP page prescribes; P is recomputed from the forward's LSE with the
+// same score function as the forward.  At head dim 256 dK and dV together fill all 512 TMEM
+// columns, so that size runs two passes over the query steps: the first accumulates dV, the
+// second dK and dQ (S^T is recomputed).
+//
+// Warps: 0 TMA, 1 MMA issuer + TMEM owner, 2..5 softmax / dS, 6..9 dQ drain.  Every wait is
+// bounded (see tc_common.cuh).
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
+
 namespace attn {
-bool tc_bwd_supported(int) { return false; }
-cudaError_t tc_backward(const Params &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+using namespace tc;
+
+constexpr int kBK = 128;  // keys per CTA
+constexpr int kThreads = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D_, int BQ_, bool DQT_, bool TWO_, int NS_>
+struct BwdCfg {
+  static constexpr int D = D_, BQ = BQ_, NS = NS_;
+  static constexpr bool DQT = DQT_, TWO = TWO_;
+  static constexpr int KCH = D / 64;
+  static constexpr int KV_BYTES = kBK * D * 2;
+  static constexpr int QT_BYTES = BQ * D * 2;
+  static constexpr int DS_BYTES = kBK * BQ * 2;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + KV_BYTES;
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;             // NS stages
+  static constexpr int OFF_DO = OFF_Q + NS * QT_BYTES;       // NS stages
+  static constexpr int OFF_DS = OFF_DO + NS * QT_BYTES;
+  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;           // 2 x BQ floats
+  static constexpr int OFF_DV = OFF_LSE + 2 * BQ * 4;         // 2 x BQ floats
+  static constexpr int OFF_BAR = OFF_DV + 2 * BQ * 4;
+  static constexpr int NBAR = 1 + 2 * NS + 9;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;
+  // TMEM columns
+  static constexpr int TM_DV = 0;
+  static constexpr int TM_DK = TWO ? 0 : D;
+  static constexpr int TM_S = TWO ? 256 : 2 * D;
+  static constexpr int TM_DP = TM_S + BQ;
+  // Two-pass form: P lives in the dQ columns, which are idle during the dV pass (it must not
+  // share the dP columns: the first dP of the second pass is issued before the last dV MMA
+  // of the first pass has read P).
+  static constexpr int TM_P = TWO ? 384 : TM_DP + BQ;
+  static constexpr int TM_DQ = TWO ? 384 : TM_P + BQ / 2;
+  static constexpr int DQ_COLS = DQT ? (D / 128) * BQ : D;
+  static_assert(TM_DQ + DQ_COLS <= 512, "TMEM budget");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(!DQT || D % 128 == 0, "transposed dQ needs whole 128-row halves of D");
+  static_assert(DQT || BQ == 128, "row-major dQ needs M = BQ = 128");
+};
+
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int e = 0; e < N; ++e) asm volatile("" : "+r"(r[e]));
+}
+
+__device__ __forceinline__ int lower_bound_i(const int *a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(a + mid) < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+__device__ __forceinline__ int upper_bound_i(const int *a, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(a + mid) <= x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void sm_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void red_add(float *p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ void red_add4(float *p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+template <class C>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const Params p) {
+  constexpr int D = C::D, BQ = C::BQ, NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {  // A wait elsewhere already gave up: do nothing (decided once for the whole CTA).
+    int *abort_flag = reinterpret_cast<int *>(smem + C::OFF_MISC + 48);
+    if (threadIdx.x == 0) *abort_flag = (status_peek(p.status) & kStatusWaitTimeout) ? 1 : 0;
+    __syncthreads();
+    if (*abort_flag) return;
+  }
+
+  const int kt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int k0 = kt * kBK, k1 = min(k0 + kBK, p.Sk) - 1;
+  const int off = p.Sk - p.Sq;
+
+  // Query rows that can see this key tile (uniform across the CTA).
+  int qlo = 0, qhi = p.Sq;
+  if (p.causal) qlo = max(qlo, k0 - off);
+  if (p.window > 0) qhi = min(qhi, k1 - off + p.window);
+  if (p.krange) {
+    const int nt = (p.Sk + 63) / 64;
+    const int2 a = p.krange[(size_t)b * nt + k0 / 64], c = p.krange[(size_t)b * nt + k1 / 64];
+    qlo = max(qlo, min(a.x, c.x));
+    qhi = min(qhi, max(a.y, c.y));
+  }
+  const int s0 = qlo / BQ;
+  const int nq = (qlo < qhi) ? (qhi + BQ - 1) / BQ - s0 : 0;  // query steps per head
+  const int nper = nq * p.G;                                   // steps per pass
+  const int nsteps = C::TWO ? 2 * nper : nper;
+
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t kv_full = bar0;
+  auto qdo_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto qdo_empty = [&](int s) { return bar0 + 8u * (1 + NS + s); };
+  const uint32_t s_full = bar0 + 8u * (1 + 2 * NS);
+  const uint32_t p_ready = bar0 + 8u * (2 + 2 * NS);
+  const uint32_t mma_done = bar0 + 8u * (3 + 2 * NS);
+  const uint32_t dq_full = bar0 + 8u * (4 + 2 * NS);
+  const uint32_t dq_empty = bar0 + 8u * (5 + 2 * NS);
+  const uint32_t acc_free = bar0 + 8u * (6 + 2 * NS);
+  const uint32_t fin_done = bar0 + 8u * (7 + 2 * NS);
+  auto lse_bar = [&](int x) { return bar0 + 8u * (8 + 2 * NS + x); };  // LSE / D staged (128 arrivals)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  int *red = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);
+  float *s_lse = reinterpret_cast<float *>(smem + C::OFF_LSE);
+  float *s_dv = reinterpret_cast<float *>(smem + C::OFF_DV);
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(qdo_full(s), 1);
+      mbar_init(qdo_empty(s), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, 128);
+    mbar_init(mma_done, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(acc_free, 128);
+    mbar_init(fin_done, 1);
+    mbar_init(lse_bar(0), 128);
+    mbar_init(lse_bar(1), 128);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // step -> (head, first query row) ; steps [0, nper) and, in the two-pass form, again
+  auto step_h = [&](int j) { return g * p.G + (j % nper) / nq; };
+  auto step_q0 = [&](int j) { return (s0 + (j % nper) % nq) * BQ; };
+  // passes: FUSED (0), dV only (1), dK + dQ (2)
+  auto step_kind = [&](int j) { return C::TWO ? (j < nper ? 1 : 2) : 0; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_load_4d(sbase + C::OFF_K + c * (kBK * 128), &tmK, kv_full, c * 64, k0, g, b);
+        tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, kv_full, c * 64, k0, g, b);
+      }
+      for (int j = 0; j < nsteps; ++j) {
+        const int s = j % NS;
+        if (j >= NS && !mbar_wait(qdo_empty(s), ((j / NS) - 1) & 1, p.status)) break;
+        mbar_arrive_expect_tx(qdo_full(s), 2 * C::QT_BYTES);
+        const int h = step_h(j), q0 = step_q0(j);
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_4d(sbase + C::OFF_Q + s * C::QT_BYTES + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, q0, h, b);
+          tma_load_4d(sbase + C::OFF_DO + s * C::QT_BYTES + c * (BQ * 128), &tmdO, qdo_full(s), c * 64, q0, h, b);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idST = idesc_bf16(kBK, BQ, false, false);  // S^T, dP^T
+      constexpr uint32_t idKV = idesc_bf16(kBK, D, false, true);    // dV, dK
+      constexpr uint32_t idDQ = C::DQT ? idesc_bf16(128, BQ, true, true) : idesc_bf16(BQ, D, true, true);
+      bool ok = mbar_wait(kv_full, 0, p.status);
+      int dq_steps = 0;
+      // dV / dK / dQ of step jj (P^T in TMEM and dS^T in shared memory are ready).
+      auto issue_back = [&](int jj) -> bool {
+        const int s = jj % NS, kind = step_kind(jj);
+        const uint32_t qa = sbase + C::OFF_Q + s * C::QT_BYTES;
+        const uint32_t oa = sbase + C::OFF_DO + s * C::QT_BYTES;
+        const uint32_t dsa = sbase + C::OFF_DS;
+        const bool first = C::TWO ? (jj == 0 || jj == nper) : (jj == 0);
+        if (C::TWO && jj == nper) {  // dV has been stored: the accumulator is free for dK
+          if (!mbar_wait(acc_free, 0, p.status)) return false;
+          tc_fence_after();
+        }
+        if (kind != 2) {  // dV += P^T dO
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk)
+            mma_ts(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, sw128_desc(oa + kk * 2048, BQ * 128, 1024), idKV,
+                   (!first || kk > 0) ? 1u : 0u);
+        }
+        if (kind != 1) {
+          // dK += dS^T Q   (A = dS^T, K-major in shared memory)
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            const uint32_t dso = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
+            mma_ss(tmem + C::TM_DK, sw128_desc(dsa + dso, 16, 1024), sw128_desc(qa + kk * 2048, BQ * 128, 1024),
+                   idKV, (!first || kk > 0) ? 1u : 0u);
+          }
+          // dQ for this step: the previous one must have been drained
+          if (dq_steps >= 1 && !mbar_wait(dq_empty, (dq_steps - 1) & 1, p.status)) return false;
+          tc_fence_after();
+          if constexpr (C::DQT) {
+            // dQ^T[d, q] = K^T dS^T : A = K (MN-major, d contiguous), B = dS^T (MN-major, q contiguous)
+#pragma unroll
+            for (int m = 0; m < D / 128; ++m)
+#pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk)
+                mma_ss(tmem + C::TM_DQ + m * BQ,
+                       sw128_desc(sbase + C::OFF_K + (2 * m) * (kBK * 128) + kk * 2048, kBK * 128, 1024),
+                       sw128_desc(dsa + kk * 2048, kBK * 128, 1024), idDQ, kk > 0);
+          } else {
+            // dQ[q, d] = dS K : A = dS (MN-major, q contiguous), B = K (MN-major, d contiguous)
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_ss(tmem + C::TM_DQ, sw128_desc(dsa + kk * 2048, kBK * 128, 1024),
+                     sw128_desc(sbase + C::OFF_K + kk * 2048, kBK * 128, 1024), idDQ, kk > 0);
+          }
+          mma_commit(dq_full);
+          ++dq_steps;
+        }
+        mma_commit(mma_done);
+        mma_commit(qdo_empty(s));
+        return true;
+      };
+      // S^T (and dP^T) of step j.
+      auto issue_front = [&](int j) {
+        const int s = j % NS, kind = step_kind(j);
+        const uint32_t qa = sbase + C::OFF_Q + s * C::QT_BYTES;
+        const uint32_t oa = sbase + C::OFF_DO + s * C::QT_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
+          const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+          mma_ss(tmem + C::TM_S, sw128_desc(sbase + C::OFF_K + ko, 16, 1024), sw128_desc(qa + qo, 16, 1024), idST,
+                 kk > 0);
+        }
+        if (kind != 1) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
+            const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+            mma_ss(tmem + C::TM_DP, sw128_desc(sbase + C::OFF_V + ko, 16, 1024), sw128_desc(oa + qo, 16, 1024),
+                   idST, kk > 0);
+          }
+        }
+        mma_commit(s_full);
+      };
+      // With two or more Q/dO stages, S^T / dP^T of step j go ahead of dV / dK / dQ of step
+      // j - 1 (the softmax of step j overlaps them).  With a single stage, step j's Q / dO
+      // can only arrive once step j - 1's MMAs have released the stage, so the order is
+      // back-to-front.
+      for (int j = 0; ok && j <= nsteps; ++j) {
+        if (j >= 1) {
+          if (!mbar_wait(p_ready, (j - 1) & 1, p.status)) break;
+          tc_fence_after();
+        }
+        if (NS == 1 && j >= 1 && !issue_back(j - 1)) break;
+        if (j < nsteps) {
+          if (!mbar_wait(qdo_full(j % NS), (j / NS) & 1, p.status)) break;
+          tc_fence_after();
+          issue_front(j);
+        }
+        if (NS > 1 && j >= 1 && !issue_back(j - 1)) break;
+      }
+      mma_commit(fin_done);  // every MMA issued by this CTA has completed
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ softmax / dS warpgroup
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // key row within the tile == TMEM lane
+    const int k = k0 + r;
+    const bool key_ok = k < p.Sk;
+    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    const int t = threadIdx.x - 64;  // 0..127 within the warpgroup
+
+    // Query interval [lo, hi) that sees this key; keys past Sk see nothing.
+    int lo = 0, hi = p.Sq;
+    if (p.causal) lo = max(lo, k - off);
+    if (p.window > 0) hi = min(hi, k - off + p.window);
+    bool seg_pairwise = false;
+    int sid = 0;
+    const int *segq = nullptr;
+    if (p.seg_q && key_ok) {
+      sid = __ldg(p.seg_k + (size_t)b * p.Sk + k);
+      segq = p.seg_q + (size_t)b * p.Sq;
+      if (p.seg_mono[b]) {
+        lo = max(lo, lower_bound_i(segq, p.Sq, sid));
+        hi = min(hi, upper_bound_i(segq, p.Sq, sid));
+      } else {
+        seg_pairwise = true;
+      }
+    }
+    if (!key_ok) {
+      lo = p.Sq;
+      hi = 0;
+    }
+    {
+      int mlo = __reduce_max_sync(0xffffffffu, lo);
+      int mhi = __reduce_min_sync(0xffffffffu, hi);
+      if (lane == 0) {
+        red[wq] = mlo;
+        red[4 + wq] = mhi;
+      }
+    }
+    sm_bar();
+    const int cta_lo = max(max(red[0], red[1]), max(red[2], red[3]));
+    const int cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
+    const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
+
+    const bool has_cap = p.cap > 0.f;
+    const float sc2 = p.scale * kLog2e;
+    const float capc = -2.f * kLog2e * p.scale * p.inv_cap;
+    const float cap2 = p.cap * kLog2e;
+    const float dscale = p.scale;
+    // dS^T row of this key in the 128-byte-swizzled tile: row r of each 64-query chunk
+    uint8_t *ds_row = smem + C::OFF_DS + r * 128;
+    bool ok = true;
+
+    for (int j = 0; j < nsteps && ok; ++j) {
+      const int kind = step_kind(j);
+      const int h = step_h(j), q0 = step_q0(j);
+      // LSE (log2 units) and D of this step's queries, staged by the warpgroup itself.
+      float *lse_s = s_lse + (j & 1) * BQ;
+      float *d_s = s_dv + (j & 1) * BQ;
+      for (int e = t; e < BQ; e += 128) {
+        const int q = q0 + e;
+        const size_t ri = ((size_t)b * p.Hq + h) * p.Sq + q;
+        lse_s[e] = q < p.Sq ? p.LSE[ri] * kLog2e : INFINITY;
+        d_s[e] = (q < p.Sq && kind != 1) ? p.Dvec[ri] : 0.f;
+      }
+      // Everyone's values for this step are in place (bounded wait; the buffer written at
+      // step j is rewritten at step j + 2, after every thread has arrived at step j + 1).
+      mbar_arrive(lse_bar(j & 1));
+      if (!mbar_wait(lse_bar(j & 1), (j >> 1) & 1, p.status)) { ok = false; break; }
+      const bool full = !any_pairwise && q0 >= cta_lo && q0 + BQ <= cta_hi;
+
+      if (!mbar_wait(s_full, j & 1, p.status)) { ok = false; break; }
+      // P^T and dS^T buffers are free once the previous step's MMAs are done.
+      if (j >= 1 && !mbar_wait(mma_done, (j - 1) & 1, p.status)) { ok = false; break; }
+      tc_fence_after();
+
+#pragma unroll 1
+      for (int c = 0; c < BQ / 32; ++c) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(lane_addr + C::TM_S + c * 32, sr);
+        if (kind != 1) tmem_ld32(lane_addr + C::TM_DP + c * 32, dr);
+        tmem_wait_ld();
+        reg_fence(sr);
+        if (kind != 1) reg_fence(dr);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e2 = 0; e2 < 16; ++e2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int e = 2 * e2 + u;
+            const int qq = c * 32 + e;
+            const float s = __uint_as_float(sr[e]);
+            float t2, f = 1.f;
+            if (has_cap) {
+              const float ee = ex2_approx(fabsf(s) * capc);
+              const float rr = rcp_approx(1.f + ee);
+              const float th = (1.f - ee) * rr;
+              t2 = copysignf(th * cap2, s);
+              f = 4.f * ee * rr * rr;  // 1 - tanh^2
+            } else {
+              t2 = s * sc2;
+            }
+            bool vis = true;
+            if (!full) {
+              const int q = q0 + qq;
+              vis = q >= lo && q < hi;
+              if (seg_pairwise) vis = vis && __ldg(segq + q) == sid;
+            }
+            const float pr = vis ? ex2_approx(t2 - lse_s[qq]) : 0.f;
+            pv[u] = pr;
+            dv[u] = (kind != 1) ? pr * (__uint_as_float(dr[e]) - d_s[qq]) * f * dscale : 0.f;
+          }
+          pk[e2] = pack_bf16(pv[0], pv[1]);
+          dk[e2] = pack_bf16(dv[0], dv[1]);
+        }
+        if (kind != 2) tmem_st16(lane_addr + C::TM_P + c * 16, pk);
+        if (kind != 1) {
+          // 32 queries = 64 bytes = four 16-byte units of this row, swizzled by (row & 7)
+          uint8_t *chunk = ds_row + (c >> 1) * (kBK * 128);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int unit = ((c & 1) * 4 + v) ^ (r & 7);
+            *reinterpret_cast<uint4 *>(chunk + unit * 16) =
+                make_uint4(dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
+          }
+        }
+      }
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+
+      if (C::TWO && j == nper - 1) {
+        // End of the dV pass: store dV, then hand the accumulator over to dK.
+        if (!mbar_wait(mma_done, j & 1, p.status)) { ok = false; break; }
+        tc_fence_after();
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.dV) + (((size_t)b * p.Sk + k) * p.Hkv + g) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + C::TM_DV + c * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          if (key_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              reinterpret_cast<uint4 *>(dst + c * 32)[v] =
+                  make_uint4(pack_bf16(__uint_as_float(o[8 * v]), __uint_as_float(o[8 * v + 1])),
+                             pack_bf16(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3])),
+                             pack_bf16(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5])),
+                             pack_bf16(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7])));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(acc_free);
+      }
+    }
+
+    // Epilogue: dK (and dV in the single-pass form) for this key.
+    if (ok && nsteps > 0) {
+      ok = mbar_wait(fin_done, 0, p.status);
+      tc_fence_after();
+    }
+    const bool have = nsteps > 0;
+    for (int which = C::TWO ? 1 : 0; which < 2; ++which) {
+      const uint32_t col = which == 0 ? C::TM_DV : C::TM_DK;
+      __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(which == 0 ? p.dV : p.dK) +
+                           (((size_t)b * p.Sk + k) * p.Hkv + g) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (have) {
+          tmem_ld32(lane_addr + col + c * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (key_ok) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            reinterpret_cast<uint4 *>(dst + c * 32)[v] =
+                make_uint4(pack_bf16(__uint_as_float(o[8 * v]), __uint_as_float(o[8 * v + 1])),
+                           pack_bf16(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3])),
+                           pack_bf16(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5])),
+                           pack_bf16(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7])));
+        }
+      }
+    }
+    if (C::TWO && nsteps == 0 && key_ok) {  // no query sees these keys: dV is zero too
+      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dV) +
+                                             (((size_t)b * p.Sk + k) * p.Hkv + g) * D);
+      for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain warpgroup
+    const int wq = warp & 3;
+    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    const int row = wq * 32 + lane;  // TMEM lane: a d index (dQ^T) or a query row (dQ)
+    int dq_steps = 0;
+    for (int j = 0; j < nsteps; ++j) {
+      if (step_kind(j) == 1) continue;
+      const int h = step_h(j), q0 = step_q0(j);
+      if (!mbar_wait(dq_full, dq_steps & 1, p.status)) break;
+      tc_fence_after();
+      if constexpr (C::DQT) {
+        uint32_t v[C::DQ_COLS];
+#pragma unroll
+        for (int c = 0; c < C::DQ_COLS / 32; ++c)
+          tmem_ld32(lane_addr + C::TM_DQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+        tmem_wait_ld();
+        reg_fence(v);
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+#pragma unroll
+        for (int m = 0; m < D / 128; ++m) {
+          const int d = m * 128 + row;
+#pragma unroll
+          for (int qq = 0; qq < BQ; ++qq) {
+            const int q = q0 + qq;
+            if (q < p.Sq) red_add(p.dQacc + (((size_t)b * p.Sq + q) * p.Hq + h) * D + d, __uint_as_float(v[m * BQ + qq]));
+          }
+        }
+      } else {
+        uint32_t v[D];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+          tmem_ld32(lane_addr + C::TM_DQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+        tmem_wait_ld();
+        reg_fence(v);
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        const int q = q0 + row;
+        if (q < p.Sq) {
+          float *dst = p.dQacc + (((size_t)b * p.Sq + q) * p.Hq + h) * D;
+#pragma unroll
+          for (int c = 0; c < D / 4; ++c)
+            red_add4(dst + 4 * c, __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                     __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+        }
+      }
+      ++dq_steps;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <class C>
+cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_bshd(&tq, p.q, C::D, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, C::BQ) ||
+      !make_tmap_bshd(&tk, p.k, C::D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, kBK) ||
+      !make_tmap_bshd(&tv, p.v, C::D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, kBK) ||
+      !make_tmap_bshd(&tdo, p.dO, C::D, p.Sq, p.Hq, p.B, (long long)p.Hq * C::D, C::D,
+                      (long long)p.Sq * p.Hq * C::D, C::BQ))
+    return cudaErrorInvalidValue;
+  auto kern = bwd_tc_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.Sk + kBK - 1) / kBK, p.Hkv, p.B);
+  kern<<<grid, kThreads, C::SMEM, st>>>(tq, tk, tv, tdo, p);
+  return counted(cudaGetLastError());
+}
+
+}  // namespace
+
+bool tc_bwd_supported(int D) { return D == 64 || D == 128 || D == 256; }
+
+cudaError_t tc_backward(const Params &p, cudaStream_t st) {
+  switch (p.D) {
+    case 64: return launch_bwd<BwdCfg<64, 128, false, false, 2>>(p, st);
+    case 128: return launch_bwd<BwdCfg<128, 64, true, false, 2>>(p, st);
+    case 256: return launch_bwd<BwdCfg<256, 64, true, true, 1>>(p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace attn

@@ -84,8 +84,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // A wait elsewhere already gave up: do nothing (the caller learns it from the status word).
-  if (status_peek(p.status) & kStatusWaitTimeout) return;
+  {  // A wait elsewhere already gave up: do nothing (decided once for the whole CTA; the
+     // caller learns it from the status word).
+    int *abort_flag = reinterpret_cast<int *>(smem + C::OFF_MISC + 48);
+    if (threadIdx.x == 0) *abort_flag = (status_peek(p.status) & kStatusWaitTimeout) ? 1 : 0;
+    __syncthreads();
+    if (*abort_flag) return;
+  }
 
   const int nqt = (p.Sq + kBM - 1) / kBM;
   const int qt = nqt - 1 - (int)blockIdx.x;  // latest (heaviest under causal) tiles first
