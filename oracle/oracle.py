@@ -163,16 +163,18 @@ def backward(p: Problem, dO, O, LSE, rows=None, cols=None, want=("dq", "dk", "dv
     c = p._c()
     Dv = np.nan_to_num(rowdot(p, dO, np.nan_to_num(O)), nan=0.0)
     out = {"D": Dv}
+    # masks are bound to names so they outlive the C calls that read them
+    row_mask, col_mask = _mask(rows, p.Sq), _mask(cols, p.Sk)
     if "dq" in want:
         dQ = np.full(p.q.shape, np.nan)
         lib.oracle_backward_dq(ctypes.byref(c), _ptr(dO), _ptr(LSE), _ptr(Dv),
-                               _ptr(_mask(rows, p.Sq)), _ptr(dQ))
+                               _ptr(row_mask), _ptr(dQ))
         out["dq"] = dQ
     if "dk" in want or "dv" in want:
         dK = np.full(p.k.shape, np.nan)
         dV = np.full(p.v.shape, np.nan)
         lib.oracle_backward_dkdv(ctypes.byref(c), _ptr(dO), _ptr(LSE), _ptr(Dv),
-                                 _ptr(_mask(cols, p.Sk)), _ptr(dK), _ptr(dV))
+                                 _ptr(col_mask), _ptr(dK), _ptr(dV))
         out["dk"], out["dv"] = dK, dV
     out["dbias"] = None
     if "dbias" in want and p.bias is not None:

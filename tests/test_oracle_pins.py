@@ -467,3 +467,17 @@ def test_tile_schedule_emulation_matches_oracle(BM, BN):
     O, LSE = oracle.forward(p)
     Oe, Le = _blockwise_forward(p, BM, BN)
     assert np.max(np.abs(Oe - O)) <= 1e-13 and np.max(np.abs(Le - LSE)) <= 1e-13
+
+
+def test_row_and_column_selection_equals_full_backward():
+    """Selecting rows / columns in the backward returns exactly the full backward's values on
+    them (and the selection masks stay alive while the C code reads them)."""
+    p, dO = full_problem(S=7, B=2)
+    O, LSE = oracle.forward(p)
+    full = oracle.backward(p, dO, O, LSE)
+    for _ in range(20):
+        part = oracle.backward(p, dO, O, LSE, rows=[1, 4, 6], cols=[0, 5])
+        assert np.array_equal(part["dq"][:, [1, 4, 6]], full["dq"][:, [1, 4, 6]])
+        assert np.array_equal(part["dk"][:, [0, 5]], full["dk"][:, [0, 5]])
+        assert np.array_equal(part["dv"][:, [0, 5]], full["dv"][:, [0, 5]])
+        assert np.all(np.isnan(part["dq"][:, [0, 2, 3, 5]]))
