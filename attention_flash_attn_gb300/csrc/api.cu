@@ -23,7 +23,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // Workspace carve-up.  Offsets are 0 when a region is absent.
 struct Layout {
   size_t status = 0, mono = 0, qrange = 0, krange = 0, seg = 0;
-  size_t dvec = 0, dsink_part = 0, dqacc = 0, dbias_acc = 0;
+  size_t dvec = 0, lse2 = 0, dsink_part = 0, dqacc = 0, dbias_acc = 0;
   size_t total = 0;
 };
 
@@ -50,7 +50,9 @@ Layout layout(const attn_args *a, bool bwd) {
     if (a->cu_seqlens) { L.seg = off; off += align_up((size_t)a->Sq * sizeof(int)); }
   }
   if (bwd) {
-    L.dvec = off; off += align_up((size_t)a->B * a->Hq * a->Sq * sizeof(float));
+    const size_t sq_pad = (size_t)(a->Sq + 127) / 128 * 128;
+    L.dvec = off; off += align_up((size_t)a->B * a->Hq * sq_pad * sizeof(float));
+    if (use_tc_bwd(a)) { L.lse2 = off; off += align_up((size_t)a->B * a->Hq * sq_pad * sizeof(float)); }
     if (a->sink) {
       L.dsink_part = off;
       off += align_up((size_t)a->Hq * bwd_pre_partials(a->B, a->Sq) * sizeof(float));
@@ -220,10 +222,12 @@ int attn_bwd(const attn_args *a, const void *O, const float *LSE, const void *dO
   p.dO = dO;
   p.dQ = dQ; p.dK = dK; p.dV = dV; p.dbias = dbias; p.dsink = dsink;
   p.Dvec = reinterpret_cast<float *>(w + L.dvec);
+  p.sq_pad = (a->Sq + 127) / 128 * 128;
   p.dsink_part = a->sink ? reinterpret_cast<float *>(w + L.dsink_part) : nullptr;
   p.n_part = bwd_pre_partials(a->B, a->Sq);
   const bool tc = use_tc_bwd(a);
   p.dQacc = tc ? reinterpret_cast<float *>(w + L.dqacc) : nullptr;
+  p.lse2p = tc ? reinterpret_cast<float *>(w + L.lse2) : nullptr;
   p.dbias_acc = a->bias ? reinterpret_cast<float *>(w + L.dbias_acc) : nullptr;
   if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
   if (a->bias && cudaMemsetAsync(p.dbias_acc, 0, dbias_elems(a) * sizeof(float), st) != cudaSuccess)

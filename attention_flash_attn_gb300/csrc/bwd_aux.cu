@@ -1,6 +1,8 @@
 // bwd_aux.cu -- memory-bound pieces of the backward pass.
 //
-// bwd_pre:  D_i = sum_d dO_i[d] * O_i[d] (fp32) for every (b, h, i); the sink gradient's
+// bwd_pre:  D_i = sum_d dO_i[d] * O_i[d] (fp32) for every (b, h, i), and, for the
+//           tensor-core backward, LSE_i * log2(e), both in rows padded to a multiple of 128
+//           so that the backward can fetch them with bulk copies; the sink gradient's
 //           per-block partial sums -sum_i exp(sink_h - LSE_i) * D_i; and, when the
 //           tensor-core backward accumulates dQ in fp32, zeroing of that accumulator.
 //           The sink gradient follows TransformerEngine PR #3551 ("What changed"): the
@@ -66,7 +68,11 @@ __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int z
       for (int c = lane; c < nchunk; c += 32) s += chunk_dot<T>(dO + row + c * per_chunk, O + row + c * per_chunk);
       s = warp_sum(s);
       const size_t ri = ((size_t)b * p.Hq + h) * p.Sq + i;
-      if (lane == 0) p.Dvec[ri] = s;
+      const size_t rp = ((size_t)b * p.Hq + h) * p.sq_pad + i;
+      if (lane == 0) {
+        p.Dvec[rp] = s;
+        if (p.lse2p) p.lse2p[rp] = p.LSE[ri] * 1.4426950408889634f;
+      }
       if (p.sink) part = fmaf(expf(sink - p.LSE[ri]), s, part);
       if (zero_dqacc) {
         float4 *z = reinterpret_cast<float4 *>(p.dQacc + row);
@@ -75,6 +81,13 @@ __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int z
     }
     if (p.sink && lane == 0)
       p.dsink_part[(size_t)h * p.n_part + (size_t)b * gridDim.x + blockIdx.x] = -part;
+    // The last block of the row also fills the padding: D = 0, LSE = +inf (P = 0 there).
+    if (i1 == p.Sq)
+      for (int i = p.Sq + lane; i < p.sq_pad; i += 32) {
+        const size_t rp = ((size_t)b * p.Hq + h) * p.sq_pad + i;
+        p.Dvec[rp] = 0.f;
+        if (p.lse2p) p.lse2p[rp] = INFINITY;
+      }
   }
 }
 

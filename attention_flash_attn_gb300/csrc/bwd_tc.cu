@@ -1,27 +1,29 @@
 // bwd_tc.cu -- tcgen05 tensor-core backward for bf16, D in {64, 128, 256}.
 //
-// One CTA owns one 128-key tile of one (batch, kv head).  It keeps K and V in shared memory,
-// loops over the query heads of its GQA group and the query steps (BQ rows) that can see the
+// One CTA owns one 128-key tile of one (batch, kv head).  K and V stay in shared memory; the
+// CTA walks the query heads of its GQA group and the query steps (BQ rows) that can see the
 // tile, and accumulates dV and dK for its keys in tensor memory:
 //
-//   S^T  = K Q^T          (M = 128 keys, N = BQ)       -> TMEM
-//   dP^T = V dO^T                                      -> TMEM
-//   softmax warpgroup (one key per thread = TMEM lane): t = cap*tanh(u/cap), mask,
-//       P = exp(t - LSE_q), dS = P (dP - D_q) (1 - tanh^2(u/cap)) * scale
+//   S^T  = K Q^T,  dP^T = V dO^T            (M = 128 keys, N = BQ; TMEM)
+//   softmax warps (key = TMEM lane; two warps per lane quarter split the BQ columns):
+//       t = cap*tanh(u/cap), mask, P = exp(t - LSE), dS = P (dP - D) (1 - tanh^2) * scale
 //       -> P^T (bf16) into TMEM, dS^T (bf16, 128-byte swizzled) into shared memory
-//   dV  += P^T dO         (A = P^T from TMEM)
-//   dK  += dS^T Q         (A = dS^T from shared memory)
-//   dQ  = dS K  (or dQ^T = K^T dS^T)   -> TMEM, drained by a fourth warpgroup into the fp32
-//       dQ accumulator with red.global.add
+//   dV += P^T dO  (A = P^T from TMEM),  dK += dS^T Q  (A = dS^T from shared memory)
+//   dQ  = dS K  (or dQ^T = K^T dS^T)  -> TMEM -> staged in shared memory -> TMA bulk
+//       reduce-add into the fp32 dQ accumulator.
 //
-// The chain-rule factor is applied before dK, dQ (and so dbias would be) formed, as the
-// tokamax soft-capping VJP page prescribes; P is recomputed from the forward's LSE with the
-// same score function as the forward.  At head dim 256 dK and dV together fill all 512 TMEM
-// columns, so that size runs two passes over the query steps: the first accumulates dV, the
-// second dK and dQ (S^T is recomputed).
+// The cap's chain-rule factor is applied before dK and dQ are formed (tokamax soft-capping
+// VJP page).  P is recomputed from the forward's LSE with the forward's score function.  Each
+// query step's Q, dO, LSE*log2(e) and D arrive together by TMA / bulk copy.
 //
-// Warps: 0 TMA, 1 MMA issuer + TMEM owner, 2..5 softmax / dS, 6..9 dQ drain.  Every wait is
-// bounded (see tc_common.cuh).
+// Head dim 256: dK and dV fill all 512 TMEM columns, so the CTA runs two passes over its
+// query steps -- dV first, then dK and dQ (S^T recomputed).  V is not needed in the dV pass,
+// so its shared-memory slot doubles as a second Q/dO stage there and V is loaded for the
+// second pass.
+//
+// Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 2..9 softmax / dS, 10..13 dQ drain.
+// Every wait is bounded (tc_common.cuh); named barriers are only used where every
+// participating thread is guaranteed to arrive.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -32,7 +34,8 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 128;  // keys per CTA
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
+constexpr int kSoftmaxThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D_, int BQ_, bool DQT_, bool TWO_, int NS_>
@@ -42,16 +45,18 @@ struct BwdCfg {
   static constexpr int KCH = D / 64;
   static constexpr int KV_BYTES = kBK * D * 2;
   static constexpr int QT_BYTES = BQ * D * 2;
+  static constexpr int SLOT_BYTES = 2 * QT_BYTES;  // Q, then dO
+  static constexpr int NSLOT = TWO ? 2 : NS;       // two-pass: slot 1 is V's space (dV pass only)
   static constexpr int DS_BYTES = kBK * BQ * 2;
+  static constexpr int DQS_BYTES = 16384;          // one bulk reduce box of fp32 dQ
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + KV_BYTES;             // NS stages
-  static constexpr int OFF_DO = OFF_Q + NS * QT_BYTES;       // NS stages
-  static constexpr int OFF_DS = OFF_DO + NS * QT_BYTES;
-  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;           // 2 x BQ floats
-  static constexpr int OFF_DV = OFF_LSE + 2 * BQ * 4;         // 2 x BQ floats
-  static constexpr int OFF_BAR = OFF_DV + 2 * BQ * 4;
-  static constexpr int NBAR = 1 + 2 * NS + 9;
+  static constexpr int OFF_V = KV_BYTES;
+  static constexpr int OFF_SLOT0 = 2 * KV_BYTES;
+  static constexpr int OFF_DS = OFF_SLOT0 + NS * SLOT_BYTES;
+  static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
+  static constexpr int OFF_LD = OFF_DQS + DQS_BYTES;  // per slot: LSE*log2e [BQ], D [BQ]
+  static constexpr int OFF_BAR = OFF_LD + NSLOT * 2 * BQ * 4;
+  static constexpr int NBAR = 9 + 2 * NSLOT;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   // TMEM columns
@@ -59,16 +64,16 @@ struct BwdCfg {
   static constexpr int TM_DK = TWO ? 0 : D;
   static constexpr int TM_S = TWO ? 256 : 2 * D;
   static constexpr int TM_DP = TM_S + BQ;
-  // Two-pass form: P lives in the dQ columns, which are idle during the dV pass (it must not
-  // share the dP columns: the first dP of the second pass is issued before the last dV MMA
-  // of the first pass has read P).
+  // Two-pass form: P lives in the dQ columns, idle during the dV pass.
   static constexpr int TM_P = TWO ? 384 : TM_DP + BQ;
   static constexpr int TM_DQ = TWO ? 384 : TM_P + BQ / 2;
   static constexpr int DQ_COLS = DQT ? (D / 128) * BQ : D;
   static_assert(TM_DQ + DQ_COLS <= 512, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(!TWO || SLOT_BYTES == KV_BYTES, "the V slot must hold one Q/dO stage");
   static_assert(!DQT || D % 128 == 0, "transposed dQ needs whole 128-row halves of D");
-  static_assert(DQT || BQ == 128, "row-major dQ needs M = BQ = 128");
+  static_assert(DQT || (BQ == 128 && D == 64), "row-major dQ is the D = 64, BQ = 128 form");
+  static_assert(BQ % 64 == 0, "dS^T rows are whole 128-byte swizzle rows");
 };
 
 template <int N>
@@ -94,32 +99,28 @@ __device__ __forceinline__ int upper_bound_i(const int *a, int n, int x) {
   return lo;
 }
 
-__device__ __forceinline__ void sm_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-__device__ __forceinline__ void red_add(float *p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
-}
-__device__ __forceinline__ void red_add4(float *p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
+__device__ __forceinline__ uint4 pack8(const uint32_t *o, int v) {
+  return make_uint4(pack_bf16(__uint_as_float(o[8 * v]), __uint_as_float(o[8 * v + 1])),
+                    pack_bf16(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3])),
+                    pack_bf16(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5])),
+                    pack_bf16(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7])));
 }
 
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                  const Params p) {
+                  const __grid_constant__ CUtensorMap tmDQ, const Params p) {
   constexpr int D = C::D, BQ = C::BQ, NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int *misc_i = reinterpret_cast<int *>(smem + C::OFF_MISC);
   {  // A wait elsewhere already gave up: do nothing (decided once for the whole CTA).
-    int *abort_flag = reinterpret_cast<int *>(smem + C::OFF_MISC + 48);
-    if (threadIdx.x == 0) *abort_flag = (status_peek(p.status) & kStatusWaitTimeout) ? 1 : 0;
+    if (threadIdx.x == 0) misc_i[12] = (status_peek(p.status) & kStatusWaitTimeout) ? 1 : 0;
     __syncthreads();
-    if (*abort_flag) return;
+    if (misc_i[12]) return;
   }
 
   const int kt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -142,37 +143,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nsteps = C::TWO ? 2 * nper : nper;
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t kv_full = bar0;
-  auto qdo_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto qdo_empty = [&](int s) { return bar0 + 8u * (1 + NS + s); };
-  const uint32_t s_full = bar0 + 8u * (1 + 2 * NS);
-  const uint32_t p_ready = bar0 + 8u * (2 + 2 * NS);
-  const uint32_t mma_done = bar0 + 8u * (3 + 2 * NS);
-  const uint32_t dq_full = bar0 + 8u * (4 + 2 * NS);
-  const uint32_t dq_empty = bar0 + 8u * (5 + 2 * NS);
-  const uint32_t acc_free = bar0 + 8u * (6 + 2 * NS);
-  const uint32_t fin_done = bar0 + 8u * (7 + 2 * NS);
-  auto lse_bar = [&](int x) { return bar0 + 8u * (8 + 2 * NS + x); };  // LSE / D staged (128 arrivals)
+  const uint32_t kv_full = bar0, v_full = bar0 + 8u;
+  const uint32_t s_full = bar0 + 16u, p_ready = bar0 + 24u, mma_done = bar0 + 32u;
+  const uint32_t dq_full = bar0 + 40u, dq_empty = bar0 + 48u, acc_free = bar0 + 56u, fin_done = bar0 + 64u;
+  auto qdo_full = [&](int s) { return bar0 + 8u * (9 + s); };
+  auto qdo_empty = [&](int s) { return bar0 + 8u * (9 + C::NSLOT + s); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
-  int *red = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);
-  float *s_lse = reinterpret_cast<float *>(smem + C::OFF_LSE);
-  float *s_dv = reinterpret_cast<float *>(smem + C::OFF_DV);
+  int *red = misc_i + 4;  // [8]
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    mbar_init(v_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, kSoftmaxThreads);
+    mbar_init(mma_done, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 1);
+    mbar_init(acc_free, kSoftmaxThreads);
+    mbar_init(fin_done, 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(qdo_full(s), 1);
       mbar_init(qdo_empty(s), 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_ready, 128);
-    mbar_init(mma_done, 1);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
-    mbar_init(acc_free, 128);
-    mbar_init(fin_done, 1);
-    mbar_init(lse_bar(0), 128);
-    mbar_init(lse_bar(1), 128);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -184,11 +176,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // step -> (head, first query row) ; steps [0, nper) and, in the two-pass form, again
+  // step j -> (head, first query row, pass kind: 0 fused, 1 dV pass, 2 dK+dQ pass),
+  // its Q/dO slot and that slot's use count (for mbarrier phases).
   auto step_h = [&](int j) { return g * p.G + (j % nper) / nq; };
   auto step_q0 = [&](int j) { return (s0 + (j % nper) % nq) * BQ; };
-  // passes: FUSED (0), dV only (1), dK + dQ (2)
   auto step_kind = [&](int j) { return C::TWO ? (j < nper ? 1 : 2) : 0; };
+  auto slot_of = [&](int j) { return C::TWO ? (j < nper ? (j & 1) : 0) : (j % NS); };
+  auto use_of = [&](int j) { return C::TWO ? (j < nper ? (j >> 1) : ((nper + 1) >> 1) + (j - nper)) : (j / NS); };
+  auto slot_addr = [&](int s) -> uint32_t {
+    return (C::TWO && s == 1) ? sbase + C::OFF_V : sbase + C::OFF_SLOT0 + s * C::SLOT_BYTES;
+  };
+  auto ld_addr = [&](int s) { return reinterpret_cast<const float *>(smem + C::OFF_LD + s * 2 * BQ * 4); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -197,22 +195,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+      mbar_arrive_expect_tx(kv_full, (C::TWO ? 1 : 2) * C::KV_BYTES);
 #pragma unroll
       for (int c = 0; c < C::KCH; ++c) {
         tma_load_4d(sbase + C::OFF_K + c * (kBK * 128), &tmK, kv_full, c * 64, k0, g, b);
-        tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, kv_full, c * 64, k0, g, b);
+        if (!C::TWO) tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, kv_full, c * 64, k0, g, b);
       }
       for (int j = 0; j < nsteps; ++j) {
-        const int s = j % NS;
-        if (j >= NS && !mbar_wait(qdo_empty(s), ((j / NS) - 1) & 1, p.status)) break;
-        mbar_arrive_expect_tx(qdo_full(s), 2 * C::QT_BYTES);
+        if (C::TWO && j == nper) {
+          // The dK pass needs V: wait until the dV pass has released V's slot, then load it.
+          if (nper >= 2 && !mbar_wait(qdo_empty(1), ((nper >> 1) - 1) & 1, p.status)) break;
+          mbar_arrive_expect_tx(v_full, C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
+        }
+        const int s = slot_of(j), u = use_of(j);
+        if (u >= 1 && !mbar_wait(qdo_empty(s), (u - 1) & 1, p.status)) break;
         const int h = step_h(j), q0 = step_q0(j);
+        const uint32_t sa = slot_addr(s);
+        mbar_arrive_expect_tx(qdo_full(s), 2 * C::QT_BYTES + 2 * BQ * 4);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c) {
-          tma_load_4d(sbase + C::OFF_Q + s * C::QT_BYTES + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, q0, h, b);
-          tma_load_4d(sbase + C::OFF_DO + s * C::QT_BYTES + c * (BQ * 128), &tmdO, qdo_full(s), c * 64, q0, h, b);
+          tma_load_4d(sa + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, q0, h, b);
+          tma_load_4d(sa + C::QT_BYTES + c * (BQ * 128), &tmdO, qdo_full(s), c * 64, q0, h, b);
         }
+        const size_t row = ((size_t)b * p.Hq + h) * p.sq_pad + q0;
+        const uint32_t lda = sbase + C::OFF_LD + s * 2 * BQ * 4;
+        bulk_g2s(lda, p.lse2p + row, BQ * 4, qdo_full(s));
+        bulk_g2s(lda + BQ * 4, p.Dvec + row, BQ * 4, qdo_full(s));
       }
     }
   } else if (warp == 1) {
@@ -225,9 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int dq_steps = 0;
       // dV / dK / dQ of step jj (P^T in TMEM and dS^T in shared memory are ready).
       auto issue_back = [&](int jj) -> bool {
-        const int s = jj % NS, kind = step_kind(jj);
-        const uint32_t qa = sbase + C::OFF_Q + s * C::QT_BYTES;
-        const uint32_t oa = sbase + C::OFF_DO + s * C::QT_BYTES;
+        const int s = slot_of(jj), kind = step_kind(jj);
+        const uint32_t qa = slot_addr(s), oa = qa + C::QT_BYTES;
         const uint32_t dsa = sbase + C::OFF_DS;
         const bool first = C::TWO ? (jj == 0 || jj == nper) : (jj == 0);
         if (C::TWO && jj == nper) {  // dV has been stored: the accumulator is free for dK
@@ -275,10 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       // S^T (and dP^T) of step j.
-      auto issue_front = [&](int j) {
-        const int s = j % NS, kind = step_kind(j);
-        const uint32_t qa = sbase + C::OFF_Q + s * C::QT_BYTES;
-        const uint32_t oa = sbase + C::OFF_DO + s * C::QT_BYTES;
+      auto issue_front = [&](int j) -> bool {
+        const int s = slot_of(j), kind = step_kind(j);
+        if (C::TWO && j == nper) {
+          if (!mbar_wait(v_full, 0, p.status)) return false;
+        }
+        if (!mbar_wait(qdo_full(s), use_of(j) & 1, p.status)) return false;
+        tc_fence_after();
+        const uint32_t qa = slot_addr(s), oa = qa + C::QT_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
@@ -296,34 +310,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mma_commit(s_full);
+        return true;
       };
-      // With two or more Q/dO stages, S^T / dP^T of step j go ahead of dV / dK / dQ of step
-      // j - 1 (the softmax of step j overlaps them).  With a single stage, step j's Q / dO
-      // can only arrive once step j - 1's MMAs have released the stage, so the order is
-      // back-to-front.
+      // With two or more stages, S^T / dP^T of step j go ahead of dV / dK / dQ of step j - 1,
+      // so the softmax of step j overlaps them.  Where a step's stage can only be refilled
+      // after the previous step's MMAs release it (single stage; the dK pass of the two-pass
+      // form), the order is back-to-front.
       for (int j = 0; ok && j <= nsteps; ++j) {
+        const bool back_first = C::TWO ? (j >= nper) : (NS == 1);
         if (j >= 1) {
           if (!mbar_wait(p_ready, (j - 1) & 1, p.status)) break;
           tc_fence_after();
         }
-        if (NS == 1 && j >= 1 && !issue_back(j - 1)) break;
-        if (j < nsteps) {
-          if (!mbar_wait(qdo_full(j % NS), (j / NS) & 1, p.status)) break;
-          tc_fence_after();
-          issue_front(j);
-        }
-        if (NS > 1 && j >= 1 && !issue_back(j - 1)) break;
+        if (back_first && j >= 1 && !issue_back(j - 1)) break;
+        if (j < nsteps && !issue_front(j)) break;
+        if (!back_first && j >= 1 && !issue_back(j - 1)) break;
       }
       mma_commit(fin_done);  // every MMA issued by this CTA has completed
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ softmax / dS warpgroup
+  } else if (warp < 10) {
+    // ------------------------------------------------------------ softmax / dS warps
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // key row within the tile == TMEM lane
+    const int half = (warp - 2) >> 2;  // which half of the BQ query columns
+    const int r = wq * 32 + lane;      // key row within the tile == TMEM lane
     const int k = k0 + r;
     const bool key_ok = k < p.Sk;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-    const int t = threadIdx.x - 64;  // 0..127 within the warpgroup
 
     // Query interval [lo, hi) that sees this key; keys past Sk see nothing.
     int lo = 0, hi = p.Sq;
@@ -346,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       lo = p.Sq;
       hi = 0;
     }
-    {
+    if (half == 0) {
       int mlo = __reduce_max_sync(0xffffffffu, lo);
       int mhi = __reduce_min_sync(0xffffffffu, hi);
       if (lane == 0) {
@@ -354,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         red[4 + wq] = mhi;
       }
     }
-    sm_bar();
+    named_bar<1, kSoftmaxThreads>();
     const int cta_lo = max(max(red[0], red[1]), max(red[2], red[3]));
     const int cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
@@ -363,36 +375,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sc2 = p.scale * kLog2e;
     const float capc = -2.f * kLog2e * p.scale * p.inv_cap;
     const float cap2 = p.cap * kLog2e;
-    const float dscale = p.scale;
-    // dS^T row of this key in the 128-byte-swizzled tile: row r of each 64-query chunk
+    const float fscale = 4.f * p.scale;  // 1 - tanh^2 = 4 e / (1 + e)^2, times the softmax scale
     uint8_t *ds_row = smem + C::OFF_DS + r * 128;
     bool ok = true;
 
     for (int j = 0; j < nsteps && ok; ++j) {
-      const int kind = step_kind(j);
-      const int h = step_h(j), q0 = step_q0(j);
-      // LSE (log2 units) and D of this step's queries, staged by the warpgroup itself.
-      float *lse_s = s_lse + (j & 1) * BQ;
-      float *d_s = s_dv + (j & 1) * BQ;
-      for (int e = t; e < BQ; e += 128) {
-        const int q = q0 + e;
-        const size_t ri = ((size_t)b * p.Hq + h) * p.Sq + q;
-        lse_s[e] = q < p.Sq ? p.LSE[ri] * kLog2e : INFINITY;
-        d_s[e] = (q < p.Sq && kind != 1) ? p.Dvec[ri] : 0.f;
-      }
-      // Everyone's values for this step are in place (bounded wait; the buffer written at
-      // step j is rewritten at step j + 2, after every thread has arrived at step j + 1).
-      mbar_arrive(lse_bar(j & 1));
-      if (!mbar_wait(lse_bar(j & 1), (j >> 1) & 1, p.status)) { ok = false; break; }
-      const bool full = !any_pairwise && q0 >= cta_lo && q0 + BQ <= cta_hi;
-
+      const int kind = step_kind(j), q0 = step_q0(j), s = slot_of(j);
+      if (!mbar_wait(qdo_full(s), use_of(j) & 1, p.status)) { ok = false; break; }
       if (!mbar_wait(s_full, j & 1, p.status)) { ok = false; break; }
       // P^T and dS^T buffers are free once the previous step's MMAs are done.
       if (j >= 1 && !mbar_wait(mma_done, (j - 1) & 1, p.status)) { ok = false; break; }
       tc_fence_after();
+      const float *lse2 = ld_addr(s);
+      const float *dvv = lse2 + BQ;
+      const bool full = !any_pairwise && q0 >= cta_lo && q0 + BQ <= cta_hi;
 
 #pragma unroll 1
-      for (int c = 0; c < BQ / 32; ++c) {
+      for (int cc = 0; cc < BQ / 64; ++cc) {
+        const int c = half * (BQ / 64) + cc;  // 32-column chunk of this step
         uint32_t sr[32], dr[32];
         tmem_ld32(lane_addr + C::TM_S + c * 32, sr);
         if (kind != 1) tmem_ld32(lane_addr + C::TM_DP + c * 32, dr);
@@ -407,16 +407,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < 2; ++u) {
             const int e = 2 * e2 + u;
             const int qq = c * 32 + e;
-            const float s = __uint_as_float(sr[e]);
-            float t2, f = 1.f;
+            const float sv = __uint_as_float(sr[e]);
+            float t2, f;
             if (has_cap) {
-              const float ee = ex2_approx(fabsf(s) * capc);
+              const float ee = ex2_approx(fabsf(sv) * capc);
               const float rr = rcp_approx(1.f + ee);
-              const float th = (1.f - ee) * rr;
-              t2 = copysignf(th * cap2, s);
-              f = 4.f * ee * rr * rr;  // 1 - tanh^2
+              const float th = fmaf(-ee, rr, rr);  // (1 - e) / (1 + e)
+              t2 = copysignf(th * cap2, sv);
+              f = fscale * ee * rr * rr;
             } else {
-              t2 = s * sc2;
+              t2 = sv * sc2;
+              f = p.scale;
             }
             bool vis = true;
             if (!full) {
@@ -424,9 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               vis = q >= lo && q < hi;
               if (seg_pairwise) vis = vis && __ldg(segq + q) == sid;
             }
-            const float pr = vis ? ex2_approx(t2 - lse_s[qq]) : 0.f;
+            const float pr = vis ? ex2_approx(t2 - lse2[qq]) : 0.f;
             pv[u] = pr;
-            dv[u] = (kind != 1) ? pr * (__uint_as_float(dr[e]) - d_s[qq]) * f * dscale : 0.f;
+            dv[u] = (kind != 1) ? pr * (__uint_as_float(dr[e]) - dvv[qq]) * f : 0.f;
           }
           pk[e2] = pack_bf16(pv[0], pv[1]);
           dk[e2] = pack_bf16(dv[0], dv[1]);
@@ -449,24 +450,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(p_ready);
 
       if (C::TWO && j == nper - 1) {
-        // End of the dV pass: store dV, then hand the accumulator over to dK.
+        // End of the dV pass: store dV (this warp's half of the columns), then hand the
+        // accumulator over to dK.
         if (!mbar_wait(mma_done, j & 1, p.status)) { ok = false; break; }
         tc_fence_after();
         __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.dV) + (((size_t)b * p.Sk + k) * p.Hkv + g) * D;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
           uint32_t o[32];
           tmem_ld32(lane_addr + C::TM_DV + c * 32, o);
           tmem_wait_ld();
           reg_fence(o);
           if (key_ok) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              reinterpret_cast<uint4 *>(dst + c * 32)[v] =
-                  make_uint4(pack_bf16(__uint_as_float(o[8 * v]), __uint_as_float(o[8 * v + 1])),
-                             pack_bf16(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3])),
-                             pack_bf16(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5])),
-                             pack_bf16(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7])));
+            for (int v = 0; v < 4; ++v) reinterpret_cast<uint4 *>(dst + c * 32)[v] = pack8(o, v);
           }
         }
         tc_fence_before();
@@ -474,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    // Epilogue: dK (and dV in the single-pass form) for this key.
+    // Epilogue: dK (and dV in the single-pass form), this warp's half of the columns.
     if (ok && nsteps > 0) {
       ok = mbar_wait(fin_done, 0, p.status);
       tc_fence_after();
@@ -485,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(which == 0 ? p.dV : p.dK) +
                            (((size_t)b * p.Sk + k) * p.Hkv + g) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         uint32_t o[32];
         if (have) {
           tmem_ld32(lane_addr + col + c * 32, o);
@@ -497,69 +494,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (key_ok) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            reinterpret_cast<uint4 *>(dst + c * 32)[v] =
-                make_uint4(pack_bf16(__uint_as_float(o[8 * v]), __uint_as_float(o[8 * v + 1])),
-                           pack_bf16(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3])),
-                           pack_bf16(__uint_as_float(o[8 * v + 4]), __uint_as_float(o[8 * v + 5])),
-                           pack_bf16(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7])));
+          for (int v = 0; v < 4; ++v) reinterpret_cast<uint4 *>(dst + c * 32)[v] = pack8(o, v);
         }
       }
     }
     if (C::TWO && nsteps == 0 && key_ok) {  // no query sees these keys: dV is zero too
       uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dV) +
                                              (((size_t)b * p.Sk + k) * p.Hkv + g) * D);
-      for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+      for (int v = half * (D / 16); v < (half + 1) * (D / 16); ++v) dst[v] = make_uint4(0, 0, 0, 0);
     }
   } else {
-    // ------------------------------------------------------------ dQ drain warpgroup
+    // ------------------------------------------------------------ dQ drain warps
+    // One thread waits on the mbarriers and the four warps follow it through a named
+    // barrier, so their exits stay uniform.
     const int wq = warp & 3;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const int row = wq * 32 + lane;  // TMEM lane: a d index (dQ^T) or a query row (dQ)
+    const int t = threadIdx.x - 320;
+    int *flag = misc_i + 13;
+    float *stage = reinterpret_cast<float *>(smem + C::OFF_DQS);
+    const uint32_t stage_a = sbase + C::OFF_DQS;
     int dq_steps = 0;
     for (int j = 0; j < nsteps; ++j) {
       if (step_kind(j) == 1) continue;
       const int h = step_h(j), q0 = step_q0(j);
-      if (!mbar_wait(dq_full, dq_steps & 1, p.status)) break;
+      if (t == 0) *flag = mbar_wait(dq_full, dq_steps & 1, p.status) ? 1 : 0;
+      named_bar<2, 128>();
+      if (!*flag) break;
       tc_fence_after();
       if constexpr (C::DQT) {
-        uint32_t v[C::DQ_COLS];
-#pragma unroll
-        for (int c = 0; c < C::DQ_COLS / 32; ++c)
-          tmem_ld32(lane_addr + C::TM_DQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
-        tmem_wait_ld();
-        reg_fence(v);
-        tc_fence_before();
-        mbar_arrive(dq_empty);
-#pragma unroll
+        // dQ^T: lane = d within a 128-wide half, column = query.  Box [128 d, 32 q].
+#pragma unroll 1
         for (int m = 0; m < D / 128; ++m) {
-          const int d = m * 128 + row;
+#pragma unroll 1
+          for (int c = 0; c < BQ / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(lane_addr + C::TM_DQ + m * BQ + c * 32, v);
+            tmem_wait_ld();
+            reg_fence(v);
+            if (t == 0) bulk_wait_read_all();  // the previous box has left shared memory
+            named_bar<2, 128>();
 #pragma unroll
-          for (int qq = 0; qq < BQ; ++qq) {
-            const int q = q0 + qq;
-            if (q < p.Sq) red_add(p.dQacc + (((size_t)b * p.Sq + q) * p.Hq + h) * D + d, __uint_as_float(v[m * BQ + qq]));
+            for (int e = 0; e < 32; ++e) stage[e * 128 + row] = __uint_as_float(v[e]);
+            fence_async_smem();
+            named_bar<2, 128>();
+            if (t == 0) {
+              tma_reduce_add_4d(&tmDQ, stage_a, m * 128, q0 + c * 32, h, b);
+              bulk_commit();
+            }
           }
         }
       } else {
-        uint32_t v[D];
+        // dQ: lane = query row, column = d.  Box [32 d, 128 q], 128-byte swizzled.
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_addr + C::TM_DQ + c * 32, v);
+          tmem_wait_ld();
+          reg_fence(v);
+          if (t == 0) bulk_wait_read_all();
+          named_bar<2, 128>();
+          uint8_t *rowp = reinterpret_cast<uint8_t *>(stage) + row * 128;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c)
-          tmem_ld32(lane_addr + C::TM_DQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
-        tmem_wait_ld();
-        reg_fence(v);
-        tc_fence_before();
-        mbar_arrive(dq_empty);
-        const int q = q0 + row;
-        if (q < p.Sq) {
-          float *dst = p.dQacc + (((size_t)b * p.Sq + q) * p.Hq + h) * D;
-#pragma unroll
-          for (int c = 0; c < D / 4; ++c)
-            red_add4(dst + 4 * c, __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                     __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4 *>(rowp + ((u ^ (row & 7)) << 4)) =
+                make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+          fence_async_smem();
+          named_bar<2, 128>();
+          if (t == 0) {
+            tma_reduce_add_4d(&tmDQ, stage_a, c * 32, q0, h, b);
+            bulk_commit();
+          }
         }
       }
+      tc_fence_before();
+      if (t == 0) mbar_arrive(dq_empty);
       ++dq_steps;
     }
+    if (t == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -573,18 +585,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <class C>
 cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tmap_bshd(&tq, p.q, C::D, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, C::BQ) ||
       !make_tmap_bshd(&tk, p.k, C::D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, kBK) ||
       !make_tmap_bshd(&tv, p.v, C::D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, kBK) ||
       !make_tmap_bshd(&tdo, p.dO, C::D, p.Sq, p.Hq, p.B, (long long)p.Hq * C::D, C::D,
-                      (long long)p.Sq * p.Hq * C::D, C::BQ))
+                      (long long)p.Sq * p.Hq * C::D, C::BQ) ||
+      !make_tmap_f32_bshd(&tdq, p.dQacc, C::D, p.Sq, p.Hq, p.B, C::DQT ? 128 : 32, C::DQT ? 32 : 128, !C::DQT))
     return cudaErrorInvalidValue;
   auto kern = bwd_tc_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((p.Sk + kBK - 1) / kBK, p.Hkv, p.B);
-  kern<<<grid, kThreads, C::SMEM, st>>>(tq, tk, tv, tdo, p);
+  kern<<<grid, kThreads, C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
   return counted(cudaGetLastError());
 }
 
@@ -594,8 +607,8 @@ bool tc_bwd_supported(int D) { return D == 64 || D == 128 || D == 256; }
 
 cudaError_t tc_backward(const Params &p, cudaStream_t st) {
   switch (p.D) {
-    case 64: return launch_bwd<BwdCfg<64, 128, false, false, 2>>(p, st);
-    case 128: return launch_bwd<BwdCfg<128, 64, true, false, 2>>(p, st);
+    case 64: return launch_bwd<BwdCfg<64, 128, false, false, 3>>(p, st);
+    case 128: return launch_bwd<BwdCfg<128, 64, true, false, 3>>(p, st);
     case 256: return launch_bwd<BwdCfg<256, 64, true, true, 1>>(p, st);
     default: return cudaErrorInvalidValue;
   }

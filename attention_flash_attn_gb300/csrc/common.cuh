@@ -41,7 +41,9 @@ struct Params {
   // backward outputs and scratch
   void *dQ, *dK, *dV, *dbias;
   float *dsink;
-  float *Dvec;                    // [B, Hq, Sq]
+  float *Dvec;                    // [B, Hq, sq_pad]: D = rowsum(dO * O), 0 past Sq
+  float *lse2p;                   // [B, Hq, sq_pad]: LSE * log2(e), +inf past Sq
+  int sq_pad;                     // Sq rounded up to a multiple of 128
   float *dQacc;                   // [B, Sq, Hq, D] fp32 accumulator (tensor-core path)
   float *dbias_acc;               // dense fp32 copy of dbias being accumulated
   float *dsink_part;              // [Hq, n_part]

@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_dq_kernel(Params p) {
   }
   const size_t ri = ((size_t)b * p.Hq + h) * p.Sq + (row_ok ? i : 0);
   const float lse = row_ok ? p.LSE[ri] : -INFINITY;
-  const float Di = row_ok ? p.Dvec[ri] : 0.f;
+  const float Di = row_ok ? p.Dvec[((size_t)b * p.Hq + h) * p.sq_pad + i] : 0.f;
   const bool live = row_ok && lse != -INFINITY;
 
   int lo, hi;
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_dkdv_kernel(Params p) {
         const int i = r0 + threadIdx.x;
         const bool ok = i < hi;
         Ls[threadIdx.x] = ok ? p.LSE[((size_t)b * p.Hq + h) * p.Sq + i] : -INFINITY;
-        Ds[threadIdx.x] = ok ? p.Dvec[((size_t)b * p.Hq + h) * p.Sq + i] : 0.f;
+        Ds[threadIdx.x] = ok ? p.Dvec[((size_t)b * p.Hq + h) * p.sq_pad + i] : 0.f;
       }
       __syncthreads();
       const int i = r0 + lane;

@@ -97,6 +97,35 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, 
       : "memory");
 }
 
+// 1-D bulk copy global -> shared completing on `bar` (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// 4-D tiled reduce-add of a shared-memory box into global memory (fp32 add in L2).
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap *m, uint32_t src, int c0, int c1, int c2,
+                                                  int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// This thread's committed bulk groups have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// This thread's committed bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy shared-memory writes become visible to the async proxy (TMA, tcgen05).
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+template <int ID, int N>
+__device__ __forceinline__ void named_bar() {
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -227,5 +256,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // 128-byte swizzle.  Returns false if the driver entry point is unavailable or rejects it.
 bool make_tmap_bshd(CUtensorMap *m, const void *base, int D, int S, int H, int B, long long stride_s,
                     long long stride_h, long long stride_b, int box_rows);
+
+// Host: 4-D fp32 tensor map over a dense [B, S, H, D] array with a [box_d, box_rows, 1, 1]
+// box, 128-byte swizzle or none (for bulk reduce-adds into the dQ accumulator).
+bool make_tmap_f32_bshd(CUtensorMap *m, const void *base, int D, int S, int H, int B, int box_d, int box_rows,
+                        bool swizzle128);
 
 }  // namespace attn
