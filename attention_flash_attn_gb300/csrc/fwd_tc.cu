@@ -4,18 +4,22 @@
 //   warp 0      TMA producer: the Q tile once, then K/V tiles into an NS-deep ring;
 //   warp 1      MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one of two TMEM
 //               score buffers, then O += P_{j-1} V_{j-1} with P read from TMEM;
-//   warps 2..5  softmax: each thread owns one query row (= one TMEM lane).  Per KV tile it
-//               reads its row of S, applies scale, the tanh soft-cap and the mask, keeps a
-//               running max / sum (started from the sink column, so the sink enters the
-//               row exactly once), writes P as bf16 over the score buffer, and rescales the
-//               O accumulator in TMEM only when the running max grew by more than 2^8.
-//               At the end it normalises O, writes O (bf16) and LSE (natural log).
-// The score modification follows the soft-capping pages: cap * tanh(u / cap) applied
-// after the scale and before the mask (TransformerEngine PR #3391; tokamax PR #1121).
-// The sink column's role follows TransformerEngine PR #3551 ("What changed").
+//   warps 2..9  softmax: a query row is a TMEM lane, and the two warps that share a lane
+//               quarter split its BN key columns.  Per KV tile each thread reads its half
+//               row of S, applies scale, the tanh soft-cap and the mask, exchanges its half
+//               row maximum with its partner through shared memory, keeps a running max /
+//               sum (started from the sink column, so the sink enters the row exactly once),
+//               writes P as bf16 over the score buffer, and rescales its half of the O
+//               accumulator in TMEM only when the running max grew by more than 2^8.  At the
+//               end the two halves' sums are combined, O is normalised and stored (bf16) with
+//               LSE (natural log).
+// The score modification follows the soft-capping pages: cap * tanh(u / cap) applied after
+// the scale and before the mask (TransformerEngine PR #3391; tokamax PR #1121).  The sink
+// column's role follows TransformerEngine PR #3551 ("What changed").
 //
-// Every wait is bounded: a wait that gives up records kStatusWaitTimeout in the status
-// word and the CTA winds down without trapping.
+// Every mbarrier wait is bounded: a wait that gives up records kStatusWaitTimeout in the
+// status word and the CTA winds down without trapping.  The partner exchange carries each
+// thread's failure flag, so both warps of a pair leave together.
 #include "common.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -26,7 +30,8 @@ namespace {
 using namespace tc;
 
 constexpr int kBM = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // tolerate P <= 2^8 before rescaling O
@@ -39,15 +44,18 @@ struct FwdCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = Q_BYTES;
   static constexpr int OFF_V = OFF_K + NS * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NS * KV_BYTES;
+  static constexpr int OFF_X = OFF_V + NS * KV_BYTES;  // partner exchange: [2 halves][3 slots][128] floats
+  static constexpr int OFF_BAR = OFF_X + 6 * kBM * 4;
   static constexpr int NBAR = 1 + 2 * NS + 5;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   static constexpr int TM_O = 2 * BN;
   static constexpr int TM_COLS = 512;
+  static constexpr int HC = BN / 2;  // columns per softmax thread and tile
   static_assert(2 * BN + D <= TM_COLS, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(KV_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzle atoms must stay 1 KiB aligned");
+  static_assert(HC % 32 == 0, "half rows are whole 32-column TMEM loads");
 };
 
 template <int N>
@@ -73,23 +81,54 @@ __device__ __forceinline__ int upper_bound_i(const int *a, int n, int x) {
   return lo;
 }
 
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Pair barrier of the two softmax warps that share TMEM lane quarter `wq` (ids 2..5).
+__device__ __forceinline__ void pair_bar(int wq) { asm volatile("bar.sync %0, 64;" ::"r"(2 + wq) : "memory"); }
 
-template <int D, int BN, int NS>
+// Raw scores -> capped, masked base-2 logits in place; returns their maximum.
+template <bool CAP, bool MASKED, int N>
+__device__ __forceinline__ float logits2(uint32_t (&x)[N], float sc2, float capc, float cap2, int jbase, int lo,
+                                         int hi, bool pairwise, const int *segk, int sid) {
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < N; ++e) {
+    const float s = __uint_as_float(x[e]);
+    float t2;
+    if constexpr (CAP) {
+      const float ee = ex2_approx(fabsf(s) * capc);  // exp(-2|u|/cap)
+      const float rr = rcp_approx(1.f + ee);
+      const float th = fmaf(-ee, rr, rr);            // tanh(|u|/cap)
+      t2 = copysignf(th * cap2, s);
+    } else {
+      t2 = s * sc2;
+    }
+    if constexpr (MASKED) {
+      const int jj = jbase + e;
+      bool vis = jj >= lo && jj < hi;
+      if (pairwise) vis = vis && __ldg(segk + jj) == sid;
+      t2 = vis ? t2 : -INFINITY;
+    }
+    x[e] = __float_as_uint(t2);
+    if (e & 1) m1 = fmaxf(m1, t2); else m0 = fmaxf(m0, t2);
+  }
+  return fmaxf(m0, m1);
+}
+
+template <int D, int BN, int NS, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
   using C = FwdCfg<D, BN, NS>;
+  constexpr int HC = C::HC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int *misc_i = reinterpret_cast<int *>(smem + C::OFF_MISC);
   {  // A wait elsewhere already gave up: do nothing (decided once for the whole CTA; the
      // caller learns it from the status word).
-    int *abort_flag = reinterpret_cast<int *>(smem + C::OFF_MISC + 48);
-    if (threadIdx.x == 0) *abort_flag = (status_peek(p.status) & kStatusWaitTimeout) ? 1 : 0;
+    if (threadIdx.x == 0) misc_i[12] = (status_peek(p.status) & kStatusWaitTimeout) ? 1 : 0;
     __syncthreads();
-    if (*abort_flag) return;
+    if (misc_i[12]) return;
   }
 
   const int nqt = (p.Sq + kBM - 1) / kBM;
@@ -119,7 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto p_full = [&](int x) { return bar0 + 8u * (3 + 2 * NS + x); };
   const uint32_t o_done = bar0 + 8u * (5 + 2 * NS);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
-  int *red = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);
+  int *red = misc_i + 4;  // [8]
+  float *xbuf = reinterpret_cast<float *>(smem + C::OFF_X);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -129,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(s_full(x), 1);
-      mbar_init(p_full(x), 128);
+      mbar_init(p_full(x), kSoftmaxThreads);
     }
     mbar_init(o_done, 1);
     fence_barrier_init();
@@ -206,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int wq = warp & 3;  // TMEM sub-partition of this warp
+    const int wq = warp & 3;            // TMEM lane quarter of this warp
+    const int half = (warp - 2) >> 2;   // which half of the key columns it owns
     const int r = wq * 32 + lane;
     const int i = i0 + r;
     const bool row_ok = i < p.Sq;
@@ -233,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       lo = 0;
       hi = p.Sk;
     }
-    {
+    if (half == 0) {
       int mlo = __reduce_max_sync(0xffffffffu, lo);
       int mhi = __reduce_min_sync(0xffffffffu, hi);
       if (lane == 0) {
@@ -241,57 +282,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         red[4 + wq] = mhi;
       }
     }
-    softmax_bar();
+    asm volatile("bar.sync 1, 256;" ::: "memory");
     const int cta_lo = max(max(red[0], red[1]), max(red[2], red[3]));
     const int cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
 
-    const bool has_cap = p.cap > 0.f;
     const float sc2 = p.scale * kLog2e;                        // uncapped: t2 = s * sc2
     const float capc = -2.f * kLog2e * p.scale * p.inv_cap;    // e = 2^(|s| * capc) = exp(-2|u|/cap)
     const float cap2 = p.cap * kLog2e;                         // t2 = tanh * cap * log2(e)
     float m_ref = p.sink ? p.sink[h] * kLog2e : -INFINITY;     // running max (log2 units)
-    float l = p.sink ? 1.f : 0.f;                              // running sum relative to m_ref
+    float l = (p.sink && half == 0) ? 1.f : 0.f;               // this half's sum relative to m_ref
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
-      if (!mbar_wait(s_full(j & 1), (j >> 1) & 1, p.status)) {
+      // Warp-uniform, so that a failed wait takes the whole warp (and, through the exchange
+      // below, its partner) out of the loop together.
+      const bool got = __all_sync(0xffffffffu, mbar_wait(s_full(j & 1), (j >> 1) & 1, p.status));
+      tc_fence_after();
+      const uint32_t sa = lane_addr + (uint32_t)((j & 1) * BN + half * HC);
+      uint32_t xr[HC];
+      if (got) {
+#pragma unroll
+        for (int c = 0; c < HC / 32; ++c) tmem_ld32(sa + c * 32, *reinterpret_cast<uint32_t(*)[32]>(xr + c * 32));
+        tmem_wait_ld();
+        reg_fence(xr);
+      }
+      const int j0 = (t0 + j) * BN + half * HC;
+      const bool full = !any_pairwise && (t0 + j) * BN >= cta_lo && (t0 + j + 1) * BN <= cta_hi;
+      float mx = -INFINITY;
+      if (got) {
+        mx = full ? logits2<CAP, false>(xr, sc2, capc, cap2, j0, lo, hi, seg_pairwise, segk, sid)
+                  : logits2<CAP, true>(xr, sc2, capc, cap2, j0, lo, hi, seg_pairwise, segk, sid);
+      }
+      // Exchange half-row maxima (and failure flags, as NaN) with the partner warp; slot
+      // j & 1 is rewritten two tiles later, after the partner has passed the next barrier.
+      xbuf[(half * 3 + (j & 1)) * kBM + r] = (got && ok) ? mx : __int_as_float(0x7fffffff);
+      pair_bar(wq);
+      const float other = xbuf[((1 - half) * 3 + (j & 1)) * kBM + r];
+      if (!(got && ok) || isnan(other)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const uint32_t sa = lane_addr + (uint32_t)((j & 1) * BN);
-      uint32_t xr[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(sa + c * 32, *reinterpret_cast<uint32_t(*)[32]>(xr + c * 32));
-      tmem_wait_ld();
-      reg_fence(xr);
-
-      const int j0 = (t0 + j) * BN;
-      const bool full = !any_pairwise && j0 >= cta_lo && j0 + BN <= cta_hi;
-      float mx = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < BN; ++e) {
-        const float s = __uint_as_float(xr[e]);
-        float t2;
-        if (has_cap) {
-          const float ee = ex2_approx(fabsf(s) * capc);
-          const float th = (1.f - ee) * rcp_approx(1.f + ee);
-          t2 = copysignf(th * cap2, s);
-        } else {
-          t2 = s * sc2;
-        }
-        if (!full) {
-          const int jj = j0 + e;
-          bool vis = jj >= lo && jj < hi;
-          if (seg_pairwise) vis = vis && __ldg(segk + jj) == sid;
-          t2 = vis ? t2 : -INFINITY;
-        }
-        xr[e] = __float_as_uint(t2);
-        mx = fmaxf(mx, t2);
-      }
-
-      const float m_new = fmaxf(m_ref, mx);
+      const float m_new = fmaxf(m_ref, fmaxf(mx, other));
       float alpha_o = 1.f;
       bool resc = false;
       if (m_new != -INFINITY) {
@@ -307,25 +339,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float rs = 0.f;
-      uint32_t pk[BN / 2];
+      float rs0 = 0.f, rs1 = 0.f;
+      uint32_t pk[HC / 2];
 #pragma unroll
-      for (int e = 0; e < BN / 2; ++e) {
+      for (int e = 0; e < HC / 2; ++e) {
         const float p0 = ex2_approx(__uint_as_float(xr[2 * e]) - mr);
         const float p1 = ex2_approx(__uint_as_float(xr[2 * e + 1]) - mr);
-        rs += p0 + p1;
+        rs0 += p0;
+        rs1 += p1;
         pk[e] = pack_bf16(p0, p1);
       }
-      l += rs;
+      l += rs0 + rs1;
+      // P (bf16 pairs) over the first half of this score buffer's columns.
+      const uint32_t pa = lane_addr + (uint32_t)((j & 1) * BN + half * (HC / 2));
 #pragma unroll
-      for (int c = 0; c < BN / 64; ++c) tmem_st32(sa + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + c * 32));
-      if constexpr (BN / 2 < 32) tmem_st16(sa, pk);
+      for (int c = 0; c < HC / 64; ++c) tmem_st32(pa + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + c * 32));
+      if constexpr (HC / 2 == 16) tmem_st16(pa, pk);
 
-      if (j >= 1 && !mbar_wait(o_done, (j - 1) & 1, p.status)) ok = false;
+      if (j >= 1) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, p.status));
       if (j >= 1 && __any_sync(0xffffffffu, resc)) {
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
           uint32_t orr[32];
           tmem_ld32(lane_addr + C::TM_O + c * 32, orr);
           tmem_wait_ld();
@@ -338,19 +373,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full(j & 1));
-      if (!ok) break;
+      // a failed o_done wait travels to the partner in the next exchange
     }
 
     if (ok && n > 0) {
       ok = mbar_wait(o_done, (n - 1) & 1, p.status);
       tc_fence_after();
     }
+    // Combine the two halves' sums (the running maxima already agree); slot 2 is used
+    // only here.
+    xbuf[(half * 3 + 2) * kBM + r] = l;
+    pair_bar(wq);
+    l += xbuf[((1 - half) * 3 + 2) * kBM + r];
     const bool has = l > 0.f;
     const float inv = has ? 1.f / l : 0.f;
     const float lse = has ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
     __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) + (((size_t)b * p.Sq + i) * p.Hq + h) * D;
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
       uint32_t orr[32];
       if (n > 0) {
         tmem_ld32(lane_addr + C::TM_O + c * 32, orr);
@@ -370,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int v = 0; v < 4; ++v) dst[v] = make_uint4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
       }
     }
-    if (row_ok) p.LSE[((size_t)b * p.Hq + h) * p.Sq + i] = lse;
+    if (row_ok && half == 0) p.LSE[((size_t)b * p.Hq + h) * p.Sq + i] = lse;
   }
 
   tc_fence_before();
@@ -390,7 +430,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
       !make_tmap_bshd(&tk, p.k, D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, BN) ||
       !make_tmap_bshd(&tv, p.v, D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, BN))
     return cudaErrorInvalidValue;
-  auto kern = fwd_tc_kernel<D, BN, NS>;
+  auto kern = p.cap > 0.f ? fwd_tc_kernel<D, BN, NS, true> : fwd_tc_kernel<D, BN, NS, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((p.Sq + kBM - 1) / kBM, p.Hq, p.B);
