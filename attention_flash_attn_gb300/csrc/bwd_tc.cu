@@ -56,7 +56,7 @@ struct BwdCfg {
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
   static constexpr int OFF_LD = OFF_DQS + DQS_BYTES;  // per slot: LSE*log2e [BQ], D [BQ]
   static constexpr int OFF_BAR = OFF_LD + NSLOT * 2 * BQ * 4;
-  static constexpr int NBAR = 9 + 2 * NSLOT;
+  static constexpr int NBAR = 10 + 2 * NSLOT;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   // TMEM columns
@@ -106,7 +106,64 @@ __device__ __forceinline__ uint4 pack8(const uint32_t *o, int v) {
                     pack_bf16(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7])));
 }
 
-template <class C>
+// One 32-query chunk of a key row: P = exp2(t2 - LSE2) and dS = P (dP - D) f scale, packed
+// to bf16 pairs.  Compile-time variants keep the loop free of branches: CAP (soft-cap on),
+// KIND (0 both, 1 P only, 2 dS only), MASK (0 none, 1 query interval, 2 interval and
+// pairwise segment ids).  Masked entries go through exp2(-inf) = 0.
+template <bool CAP, int KIND, int MASK>
+__device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float *lse2c,
+                                          const float *dvc, uint32_t (&pk)[16], uint32_t (&dk)[16], float sc2,
+                                          float capc, float cap2, float fscale, float scale, int qbase, int lo,
+                                          int hi, int sq, const int *segq, int sid) {
+#pragma unroll
+  for (int e2 = 0; e2 < 16; ++e2) {
+    float pv[2], dv[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = 2 * e2 + u;
+      const float sv = __uint_as_float(sr[e]);
+      float t2, f;
+      if constexpr (CAP) {
+        const float ee = ex2_approx(fabsf(sv) * capc);  // exp(-2|u|/cap)
+        const float rr = rcp_approx(1.f + ee);
+        const float th = fmaf(-ee, rr, rr);             // tanh(|u|/cap)
+        t2 = copysignf(th * cap2, sv);
+        f = fscale * ee * rr * rr;                      // 4 e / (1 + e)^2 = 1 - tanh^2, times scale
+      } else {
+        t2 = sv * sc2;
+        f = scale;
+      }
+      float x = t2 - lse2c[e];
+      if constexpr (MASK >= 1) {
+        const int q = qbase + e;
+        bool vis = (q >= lo) & (q < hi);
+        if constexpr (MASK == 2) vis = vis & (__ldg(segq + min(q, sq - 1)) == sid);
+        x = vis ? x : -INFINITY;
+      }
+      const float pr = ex2_approx(x);
+      pv[u] = pr;
+      if constexpr (KIND != 1) dv[u] = pr * (__uint_as_float(dr[e]) - dvc[e]) * f;
+    }
+    if constexpr (KIND != 2) pk[e2] = pack_bf16(pv[0], pv[1]);
+    if constexpr (KIND != 1) dk[e2] = pack_bf16(dv[0], dv[1]);
+  }
+}
+
+template <bool CAP, int KIND>
+__device__ __forceinline__ void bwd_chunk_masked(int mask, const uint32_t (&sr)[32], const uint32_t (&dr)[32],
+                                                 const float *lse2c, const float *dvc, uint32_t (&pk)[16],
+                                                 uint32_t (&dk)[16], float sc2, float capc, float cap2, float fscale,
+                                                 float scale, int qbase, int lo, int hi, int sq, const int *segq,
+                                                 int sid) {
+  if (mask == 0)
+    bwd_chunk<CAP, KIND, 0>(sr, dr, lse2c, dvc, pk, dk, sc2, capc, cap2, fscale, scale, qbase, lo, hi, sq, segq, sid);
+  else if (mask == 1)
+    bwd_chunk<CAP, KIND, 1>(sr, dr, lse2c, dvc, pk, dk, sc2, capc, cap2, fscale, scale, qbase, lo, hi, sq, segq, sid);
+  else
+    bwd_chunk<CAP, KIND, 2>(sr, dr, lse2c, dvc, pk, dk, sc2, capc, cap2, fscale, scale, qbase, lo, hi, sq, segq, sid);
+}
+
+template <class C, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -146,8 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t kv_full = bar0, v_full = bar0 + 8u;
   const uint32_t s_full = bar0 + 16u, p_ready = bar0 + 24u, mma_done = bar0 + 32u;
   const uint32_t dq_full = bar0 + 40u, dq_empty = bar0 + 48u, acc_free = bar0 + 56u, fin_done = bar0 + 64u;
-  auto qdo_full = [&](int s) { return bar0 + 8u * (9 + s); };
-  auto qdo_empty = [&](int s) { return bar0 + 8u * (9 + C::NSLOT + s); };
+  const uint32_t sdp_free = bar0 + 72u;  // S^T / dP^T copied out of TMEM (256 arrivals)
+  auto qdo_full = [&](int s) { return bar0 + 8u * (10 + s); };
+  auto qdo_empty = [&](int s) { return bar0 + 8u * (10 + C::NSLOT + s); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *red = misc_i + 4;  // [8]
 
@@ -161,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dq_empty, 1);
     mbar_init(acc_free, kSoftmaxThreads);
     mbar_init(fin_done, 1);
+    mbar_init(sdp_free, kSoftmaxThreads);
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(qdo_full(s), 1);
       mbar_init(qdo_empty(s), 1);
@@ -316,15 +375,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // so the softmax of step j overlaps them.  Where a step's stage can only be refilled
       // after the previous step's MMAs release it (single stage; the dK pass of the two-pass
       // form), the order is back-to-front.
+      // S^T / dP^T of step j may start as soon as the softmax has copied step j - 1's out
+      // of TMEM (sdp_free); dV / dK / dQ of step j - 1 need its P and dS (p_ready).
       for (int j = 0; ok && j <= nsteps; ++j) {
         const bool back_first = C::TWO ? (j >= nper) : (NS == 1);
-        if (j >= 1) {
-          if (!mbar_wait(p_ready, (j - 1) & 1, p.status)) break;
-          tc_fence_after();
+        if (back_first) {
+          if (j >= 1) {
+            if (!mbar_wait(p_ready, (j - 1) & 1, p.status)) break;
+            tc_fence_after();
+            if (!issue_back(j - 1)) break;
+          }
+          if (j < nsteps && !issue_front(j)) break;
+        } else {
+          if (j < nsteps) {
+            if (j >= 1) {
+              if (!mbar_wait(sdp_free, (j - 1) & 1, p.status)) break;
+              tc_fence_after();
+            }
+            if (!issue_front(j)) break;
+          }
+          if (j >= 1) {
+            if (!mbar_wait(p_ready, (j - 1) & 1, p.status)) break;
+            tc_fence_after();
+            if (!issue_back(j - 1)) break;
+          }
         }
-        if (back_first && j >= 1 && !issue_back(j - 1)) break;
-        if (j < nsteps && !issue_front(j)) break;
-        if (!back_first && j >= 1 && !issue_back(j - 1)) break;
       }
       mma_commit(fin_done);  // every MMA issued by this CTA has completed
     }
@@ -371,7 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
 
-    const bool has_cap = p.cap > 0.f;
     const float sc2 = p.scale * kLog2e;
     const float capc = -2.f * kLog2e * p.scale * p.inv_cap;
     const float cap2 = p.cap * kLog2e;
@@ -383,56 +457,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kind = step_kind(j), q0 = step_q0(j), s = slot_of(j);
       if (!mbar_wait(qdo_full(s), use_of(j) & 1, p.status)) { ok = false; break; }
       if (!mbar_wait(s_full, j & 1, p.status)) { ok = false; break; }
-      // P^T and dS^T buffers are free once the previous step's MMAs are done.
-      if (j >= 1 && !mbar_wait(mma_done, (j - 1) & 1, p.status)) { ok = false; break; }
       tc_fence_after();
       const float *lse2 = ld_addr(s);
       const float *dvv = lse2 + BQ;
       const bool full = !any_pairwise && q0 >= cta_lo && q0 + BQ <= cta_hi;
 
-#pragma unroll 1
-      for (int cc = 0; cc < BQ / 64; ++cc) {
-        const int c = half * (BQ / 64) + cc;  // 32-column chunk of this step
+      // P and dS of this thread's columns are formed in registers while the previous
+      // step's dV / dK / dQ MMAs still read the P^T and dS^T buffers (and, once S^T / dP^T
+      // are copied out, while the next step's S^T / dP^T are computed) ...
+      constexpr int NCH = BQ / 64;  // 32-column chunks per thread and step
+      const int mask = full ? 0 : (seg_pairwise ? 2 : 1);
+      uint32_t pk[NCH][16], dk[NCH][16];
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int c = half * NCH + cc;  // 32-column chunk of this step
         uint32_t sr[32], dr[32];
         tmem_ld32(lane_addr + C::TM_S + c * 32, sr);
         if (kind != 1) tmem_ld32(lane_addr + C::TM_DP + c * 32, dr);
         tmem_wait_ld();
         reg_fence(sr);
         if (kind != 1) reg_fence(dr);
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int e2 = 0; e2 < 16; ++e2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int e = 2 * e2 + u;
-            const int qq = c * 32 + e;
-            const float sv = __uint_as_float(sr[e]);
-            float t2, f;
-            if (has_cap) {
-              const float ee = ex2_approx(fabsf(sv) * capc);
-              const float rr = rcp_approx(1.f + ee);
-              const float th = fmaf(-ee, rr, rr);  // (1 - e) / (1 + e)
-              t2 = copysignf(th * cap2, sv);
-              f = fscale * ee * rr * rr;
-            } else {
-              t2 = sv * sc2;
-              f = p.scale;
-            }
-            bool vis = true;
-            if (!full) {
-              const int q = q0 + qq;
-              vis = q >= lo && q < hi;
-              if (seg_pairwise) vis = vis && __ldg(segq + q) == sid;
-            }
-            const float pr = vis ? ex2_approx(t2 - lse2[qq]) : 0.f;
-            pv[u] = pr;
-            dv[u] = (kind != 1) ? pr * (__uint_as_float(dr[e]) - dvv[qq]) * f : 0.f;
-          }
-          pk[e2] = pack_bf16(pv[0], pv[1]);
-          dk[e2] = pack_bf16(dv[0], dv[1]);
+        if (cc == NCH - 1) {
+          tc_fence_before();
+          mbar_arrive(sdp_free);
         }
-        if (kind != 2) tmem_st16(lane_addr + C::TM_P + c * 16, pk);
+        const float *lc = lse2 + c * 32, *dc = dvv + c * 32;
+        const int qb = q0 + c * 32;
+        if (kind == 0)
+          bwd_chunk_masked<CAP, 0>(mask, sr, dr, lc, dc, pk[cc], dk[cc], sc2, capc, cap2, fscale, p.scale, qb, lo,
+                                   hi, p.Sq, segq, sid);
+        else if (kind == 1)
+          bwd_chunk_masked<CAP, 1>(mask, sr, dr, lc, dc, pk[cc], dk[cc], sc2, capc, cap2, fscale, p.scale, qb, lo,
+                                   hi, p.Sq, segq, sid);
+        else
+          bwd_chunk_masked<CAP, 2>(mask, sr, dr, lc, dc, pk[cc], dk[cc], sc2, capc, cap2, fscale, p.scale, qb, lo,
+                                   hi, p.Sq, segq, sid);
+      }
+      // ... and stored once those MMAs are done with the buffers.
+      if (j >= 1 && !mbar_wait(mma_done, (j - 1) & 1, p.status)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int c = half * NCH + cc;
+        if (kind != 2) tmem_st16(lane_addr + C::TM_P + c * 16, pk[cc]);
         if (kind != 1) {
           // 32 queries = 64 bytes = four 16-byte units of this row, swizzled by (row & 7)
           uint8_t *chunk = ds_row + (c >> 1) * (kBK * 128);
@@ -440,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int v = 0; v < 4; ++v) {
             const int unit = ((c & 1) * 4 + v) ^ (r & 7);
             *reinterpret_cast<uint4 *>(chunk + unit * 16) =
-                make_uint4(dk[4 * v], dk[4 * v + 1], dk[4 * v + 2], dk[4 * v + 3]);
+                make_uint4(dk[cc][4 * v], dk[cc][4 * v + 1], dk[cc][4 * v + 2], dk[cc][4 * v + 3]);
           }
         }
       }
@@ -522,20 +589,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar<2, 128>();
       if (!*flag) break;
       tc_fence_after();
+      // Copy the whole dQ tile out of TMEM first and release it at once, so the next dQ
+      // MMA never waits for the staging below.
+      uint32_t v[C::DQ_COLS];
+#pragma unroll
+      for (int c = 0; c < C::DQ_COLS / 32; ++c)
+        tmem_ld32(lane_addr + C::TM_DQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+      tmem_wait_ld();
+      reg_fence(v);
+      tc_fence_before();
+      if (t == 0) mbar_arrive(dq_empty);
       if constexpr (C::DQT) {
         // dQ^T: lane = d within a 128-wide half, column = query.  Box [128 d, 32 q].
-#pragma unroll 1
+#pragma unroll
         for (int m = 0; m < D / 128; ++m) {
-#pragma unroll 1
+#pragma unroll
           for (int c = 0; c < BQ / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(lane_addr + C::TM_DQ + m * BQ + c * 32, v);
-            tmem_wait_ld();
-            reg_fence(v);
             if (t == 0) bulk_wait_read_all();  // the previous box has left shared memory
             named_bar<2, 128>();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) stage[e * 128 + row] = __uint_as_float(v[e]);
+            for (int e = 0; e < 32; ++e) stage[e * 128 + row] = __uint_as_float(v[m * BQ + c * 32 + e]);
             fence_async_smem();
             named_bar<2, 128>();
             if (t == 0) {
@@ -546,19 +619,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // dQ: lane = query row, column = d.  Box [32 d, 128 q], 128-byte swizzled.
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_addr + C::TM_DQ + c * 32, v);
-          tmem_wait_ld();
-          reg_fence(v);
           if (t == 0) bulk_wait_read_all();
           named_bar<2, 128>();
           uint8_t *rowp = reinterpret_cast<uint8_t *>(stage) + row * 128;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             *reinterpret_cast<uint4 *>(rowp + ((u ^ (row & 7)) << 4)) =
-                make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                make_uint4(v[c * 32 + 4 * u], v[c * 32 + 4 * u + 1], v[c * 32 + 4 * u + 2], v[c * 32 + 4 * u + 3]);
           fence_async_smem();
           named_bar<2, 128>();
           if (t == 0) {
@@ -567,8 +636,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      if (t == 0) mbar_arrive(dq_empty);
       ++dq_steps;
     }
     if (t == 0) bulk_wait_all();
@@ -593,7 +660,7 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
                       (long long)p.Sq * p.Hq * C::D, C::BQ) ||
       !make_tmap_f32_bshd(&tdq, p.dQacc, C::D, p.Sq, p.Hq, p.B, C::DQT ? 128 : 32, C::DQT ? 32 : 128, !C::DQT))
     return cudaErrorInvalidValue;
-  auto kern = bwd_tc_kernel<C>;
+  auto kern = p.cap > 0.f ? bwd_tc_kernel<C, true> : bwd_tc_kernel<C, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((p.Sk + kBK - 1) / kBK, p.Hkv, p.B);
