@@ -1,7 +1,8 @@
 // fwd_tc.cu -- tcgen05 tensor-core forward for bf16, D in {64, 128, 256}.
 //
 // One CTA computes one 128-row query tile of one (batch, query head):
-//   warp 0      TMA producer: the Q tile once, then K/V tiles into an NS-deep ring;
+//   warp 0      TMA producers: the Q tile once, then K tiles (lane 0) and V tiles (lane 1)
+//               into separate rings, each slot released as soon as its MMA has read it;
 //   warp 1      MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one of two TMEM
 //               score buffers, then O += P_{j-1} V_{j-1} with P read from TMEM;
 //   warps 2..9  softmax: a query row is a TMEM lane, and the two warps that share a lane
@@ -36,17 +37,17 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // tolerate P <= 2^8 before rescaling O
 
-template <int D, int BN, int NS>
+template <int D, int BN, int NK, int NV>
 struct FwdCfg {
   static constexpr int KCH = D / 64;
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = Q_BYTES;
-  static constexpr int OFF_V = OFF_K + NS * KV_BYTES;
-  static constexpr int OFF_X = OFF_V + NS * KV_BYTES;  // partner exchange: [2 halves][3 slots][128] floats
+  static constexpr int OFF_K = Q_BYTES;                 // NK-deep K ring (released after S)
+  static constexpr int OFF_V = OFF_K + NK * KV_BYTES;   // NV-deep V ring (released after PV)
+  static constexpr int OFF_X = OFF_V + NV * KV_BYTES;   // partner exchange: [2 halves][3 slots][128] floats
   static constexpr int OFF_BAR = OFF_X + 6 * kBM * 4;
-  static constexpr int NBAR = 1 + 2 * NS + 5;
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 5;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   static constexpr int TM_O = 2 * BN;
@@ -113,11 +114,11 @@ __device__ __forceinline__ float logits2(uint32_t (&x)[N], float sc2, float capc
   return fmaxf(m0, m1);
 }
 
-template <int D, int BN, int NS, bool CAP>
+template <int D, int BN, int NK, int NV, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using C = FwdCfg<D, BN, NS>;
+  using C = FwdCfg<D, BN, NK, NV>;
   constexpr int HC = C::HC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -152,20 +153,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t q_full = bar0;
-  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + NS + s); };
-  auto s_full = [&](int x) { return bar0 + 8u * (1 + 2 * NS + x); };
-  auto p_full = [&](int x) { return bar0 + 8u * (3 + 2 * NS + x); };
-  const uint32_t o_done = bar0 + 8u * (5 + 2 * NS);
+  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto k_empty = [&](int s) { return bar0 + 8u * (1 + NK + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * NK + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * NK + NV + s); };
+  auto s_full = [&](int x) { return bar0 + 8u * (1 + 2 * NK + 2 * NV + x); };
+  auto p_full = [&](int x) { return bar0 + 8u * (3 + 2 * NK + 2 * NV + x); };
+  const uint32_t o_done = bar0 + 8u * (5 + 2 * NK + 2 * NV);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *red = misc_i + 4;  // [8]
   float *xbuf = reinterpret_cast<float *>(smem + C::OFF_X);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(s_full(x), 1);
@@ -185,26 +192,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && (tmem & 0xFFFFu) + C::TM_COLS > 512) set_status(p.status, kStatusBadTmemAlloc);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producers
+    // Lane 0 loads Q and the K ring, lane 1 the V ring: K slots free up as soon as their S
+    // MMA is done, V slots only after PV, so the two rings advance independently.
     if (lane == 0 && n > 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
 #pragma unroll
       for (int c = 0; c < C::KCH; ++c)
         tma_load_4d(sbase + C::OFF_Q + c * (kBM * 128), &tmQ, q_full, c * 64, i0, h, b);
       for (int j = 0; j < n; ++j) {
-        const int s = j % NS;
-        if (j >= NS && !mbar_wait(kv_empty(s), ((j / NS) - 1) & 1, p.status)) break;
-        mbar_arrive_expect_tx(kv_full(s), 2 * C::KV_BYTES);
+        const int s = j % NK;
+        if (j >= NK && !mbar_wait(k_empty(s), ((j / NK) - 1) & 1, p.status)) break;
+        mbar_arrive_expect_tx(k_full(s), C::KV_BYTES);
         const int kt = (t0 + j) * BN;
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES + c * (BN * 128), &tmK, kv_full(s), c * 64, kt, g, b);
+          tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES + c * (BN * 128), &tmK, k_full(s), c * 64, kt, g, b);
+      }
+    } else if (lane == 1 && n > 0) {
+      tma_prefetch_desc(&tmV);
+      for (int j = 0; j < n; ++j) {
+        const int s = j % NV;
+        if (j >= NV && !mbar_wait(v_empty(s), ((j / NV) - 1) & 1, p.status)) break;
+        mbar_arrive_expect_tx(v_full(s), C::KV_BYTES);
+        const int kt = (t0 + j) * BN;
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(sbase + C::OFF_V + s * C::KV_BYTES + c * (BN * 128), &tmV, kv_full(s), c * 64, kt, g, b);
+          tma_load_4d(sbase + C::OFF_V + s * C::KV_BYTES + c * (BN * 128), &tmV, v_full(s), c * 64, kt, g, b);
       }
     }
   } else if (warp == 1) {
@@ -215,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(q_full, 0, p.status);
       for (int j = 0; ok && j <= n; ++j) {
         if (j < n) {
-          const int s = j % NS;
-          if (!mbar_wait(kv_full(s), (j / NS) & 1, p.status)) break;
+          const int s = j % NK;
+          if (!mbar_wait(k_full(s), (j / NK) & 1, p.status)) break;
           tc_fence_after();
           const uint32_t dS = tmem + (uint32_t)((j & 1) * BN);
           const uint32_t qa = sbase + C::OFF_Q, ka = sbase + C::OFF_K + s * C::KV_BYTES;
@@ -227,9 +243,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(dS, ad, bd, idS, kk > 0);
           }
           mma_commit(s_full(j & 1));
+          mma_commit(k_empty(s));
         }
         if (j >= 1) {
-          const int jj = j - 1, s = jj % NS;
+          const int jj = j - 1, s = jj % NV;
+          if (!mbar_wait(v_full(s), (jj / NV) & 1, p.status)) break;
           if (!mbar_wait(p_full(jj & 1), (jj >> 1) & 1, p.status)) break;
           tc_fence_after();
           const uint32_t va = sbase + C::OFF_V + s * C::KV_BYTES;
@@ -239,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = sw128_desc(va + kk * (16 * 128), BN * 128, 1024);
             mma_ts(tmem + C::TM_O, pa + kk * 8, bd, idO, (jj > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(kv_empty(s));
+          mma_commit(v_empty(s));
           mma_commit(o_done);
         }
       }
@@ -422,15 +440,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int BN, int NS>
+template <int D, int BN, int NK, int NV>
 cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
-  using C = FwdCfg<D, BN, NS>;
+  using C = FwdCfg<D, BN, NK, NV>;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bshd(&tq, p.q, D, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, kBM) ||
       !make_tmap_bshd(&tk, p.k, D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, BN) ||
       !make_tmap_bshd(&tv, p.v, D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, BN))
     return cudaErrorInvalidValue;
-  auto kern = p.cap > 0.f ? fwd_tc_kernel<D, BN, NS, true> : fwd_tc_kernel<D, BN, NS, false>;
+  auto kern = p.cap > 0.f ? fwd_tc_kernel<D, BN, NK, NV, true> : fwd_tc_kernel<D, BN, NK, NV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid((p.Sq + kBM - 1) / kBM, p.Hq, p.B);
@@ -444,9 +462,9 @@ bool tc_supported(int D) { return D == 64 || D == 128 || D == 256; }
 
 cudaError_t tc_forward(const Params &p, cudaStream_t st) {
   switch (p.D) {
-    case 64: return launch_fwd<64, 128, 4>(p, st);
-    case 128: return launch_fwd<128, 128, 2>(p, st);
-    case 256: return launch_fwd<256, 64, 2>(p, st);
+    case 64: return launch_fwd<64, 128, 4, 4>(p, st);
+    case 128: return launch_fwd<128, 128, 3, 2>(p, st);
+    case 256: return launch_fwd<256, 64, 2, 2>(p, st);
     default: return cudaErrorInvalidValue;
   }
 }
