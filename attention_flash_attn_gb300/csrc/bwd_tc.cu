@@ -56,7 +56,7 @@ struct BwdCfg {
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
   static constexpr int OFF_LD = OFF_DQS + DQS_BYTES;  // per slot: LSE*log2e [BQ], D [BQ]
   static constexpr int OFF_BAR = OFF_LD + NSLOT * 2 * BQ * 4;
-  static constexpr int NBAR = 10 + 2 * NSLOT;
+  static constexpr int NBAR = 10 + 2 * NSLOT + (TWO ? 8 : 0);
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   // TMEM columns
@@ -204,14 +204,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_full = bar0 + 16u, p_ready = bar0 + 24u, mma_done = bar0 + 32u;
   const uint32_t dq_full = bar0 + 40u, dq_empty = bar0 + 48u, acc_free = bar0 + 56u, fin_done = bar0 + 64u;
   const uint32_t sdp_free = bar0 + 72u;  // S^T / dP^T copied out of TMEM (256 arrivals)
+  // Q/dO stages; in the two-pass form these are the Q ring, and do_full / do_empty the dO ring.
   auto qdo_full = [&](int s) { return bar0 + 8u * (10 + s); };
   auto qdo_empty = [&](int s) { return bar0 + 8u * (10 + C::NSLOT + s); };
+  auto do_full = [&](int s) { return bar0 + 8u * (10 + 2 * C::NSLOT + s); };
+  auto do_empty = [&](int s) { return bar0 + 8u * (12 + 2 * C::NSLOT + s); };
+  // Two-pass form: LSE*log2e / D of step j in their own two-deep ring (index j & 1), filled by
+  // the Q lane and released by the softmax warps once they have read it.
+  auto ld_full = [&](int x) { return bar0 + 8u * (14 + 2 * C::NSLOT + x); };
+  auto ld_empty = [&](int x) { return bar0 + 8u * (16 + 2 * C::NSLOT + x); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *red = misc_i + 4;  // [8]
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(v_full, 1);
+    mbar_init(v_full, C::TWO ? 2 : 1);  // two-pass: V arrives in two halves from two lanes
     mbar_init(s_full, 1);
     mbar_init(p_ready, kSoftmaxThreads);
     mbar_init(mma_done, 1);
@@ -223,6 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(qdo_full(s), 1);
       mbar_init(qdo_empty(s), 1);
+      if (C::TWO) {
+        mbar_init(do_full(s), 1);
+        mbar_init(do_empty(s), 1);
+        mbar_init(ld_full(s), 1);
+        mbar_init(ld_empty(s), kSoftmaxThreads);
+      }
     }
     fence_barrier_init();
   }
@@ -242,12 +255,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto step_kind = [&](int j) { return C::TWO ? (j < nper ? 1 : 2) : 0; };
   auto slot_of = [&](int j) { return C::TWO ? (j < nper ? (j & 1) : 0) : (j % NS); };
   auto use_of = [&](int j) { return C::TWO ? (j < nper ? (j >> 1) : ((nper + 1) >> 1) + (j - nper)) : (j / NS); };
+  // Q tile of slot s; its dO tile is QT_BYTES further (fused) -- in the two-pass form the Q
+  // ring is {R0, R2} and the dO ring {R1, R3}, R2/R3 being V's space during the dV pass.
   auto slot_addr = [&](int s) -> uint32_t {
     return (C::TWO && s == 1) ? sbase + C::OFF_V : sbase + C::OFF_SLOT0 + s * C::SLOT_BYTES;
   };
+  auto do_addr = [&](int s) -> uint32_t { return slot_addr(s) + C::QT_BYTES; };
   auto ld_addr = [&](int s) { return reinterpret_cast<const float *>(smem + C::OFF_LD + s * 2 * BQ * 4); };
 
-  if (warp == 0) {
+  if (warp == 0 && C::TWO) {
+    // ------------------------------------------------------------ TMA producers (two-pass)
+    // Lane 0: K, the Q ring, the LSE / D ring and V's first half; lane 1: the dO ring and
+    // V's second half.  Every ring has this one loader and its waits run in phase order.
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(kv_full, C::KV_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c) tma_load_4d(sbase + C::OFF_K + c * (kBK * 128), &tmK, kv_full, c * 64, k0, g, b);
+      for (int j = 0; j < nsteps; ++j) {
+        if (j == nper) {  // V[:, :128] into the Q ring's second slot, free after the dV pass
+          if (nper >= 2 && !mbar_wait(qdo_empty(1), ((nper >> 1) - 1) & 1, p.status)) break;
+          mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
+#pragma unroll
+          for (int c = 0; c < C::KCH / 2; ++c)
+            tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
+        }
+        const int s = slot_of(j), u = use_of(j), h = step_h(j), q0 = step_q0(j);
+        if (u >= 1 && !mbar_wait(qdo_empty(s), (u - 1) & 1, p.status)) break;
+        mbar_arrive_expect_tx(qdo_full(s), C::QT_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(slot_addr(s) + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, q0, h, b);
+        const int x = j & 1;
+        if (j >= 2 && !mbar_wait(ld_empty(x), ((j >> 1) - 1) & 1, p.status)) break;
+        mbar_arrive_expect_tx(ld_full(x), 2 * BQ * 4);
+        const size_t row = ((size_t)b * p.Hq + h) * p.sq_pad + q0;
+        const uint32_t lda = sbase + C::OFF_LD + x * 2 * BQ * 4;
+        bulk_g2s(lda, p.lse2p + row, BQ * 4, ld_full(x));
+        bulk_g2s(lda + BQ * 4, p.Dvec + row, BQ * 4, ld_full(x));
+      }
+    } else if (lane == 1) {
+      tma_prefetch_desc(&tmdO);
+      for (int j = 0; j < nsteps; ++j) {
+        if (j == nper) {  // V[:, 128:] into the dO ring's second slot, free after the dV pass
+          if (nper >= 2 && !mbar_wait(do_empty(1), ((nper >> 1) - 1) & 1, p.status)) break;
+          mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
+#pragma unroll
+          for (int c = C::KCH / 2; c < C::KCH; ++c)
+            tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
+        }
+        const int s = slot_of(j), u = use_of(j);
+        if (u >= 1 && !mbar_wait(do_empty(s), (u - 1) & 1, p.status)) break;
+        mbar_arrive_expect_tx(do_full(s), C::QT_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(do_addr(s) + c * (BQ * 128), &tmdO, do_full(s), c * 64, step_q0(j), step_h(j), b);
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -377,6 +444,103 @@ __global__ void __launch_bounds__(kThreads, 1)
       // form), the order is back-to-front.
       // S^T / dP^T of step j may start as soon as the softmax has copied step j - 1's out
       // of TMEM (sdp_free); dV / dK / dQ of step j - 1 need its P and dS (p_ready).
+      if constexpr (C::TWO) {
+        constexpr uint32_t idKVt = idesc_bf16(kBK, D, false, true);
+        // dV of a dV-pass step: P^T from TMEM, dO of its slot; releases that dO slot.
+        auto back_dv = [&](int jj) -> bool {
+          const int s = slot_of(jj);
+          if (!mbar_wait(do_full(s), use_of(jj) & 1, p.status)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk)
+            mma_ts(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, sw128_desc(do_addr(s) + kk * 2048, BQ * 128, 1024),
+                   idKVt, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(do_empty(s));
+          mma_commit(mma_done);
+          return true;
+        };
+        // dK (releases the Q slot) and dQ of a dK-pass step.
+        auto back_dkdq = [&](int jj) -> bool {
+          const uint32_t dsa = sbase + C::OFF_DS;
+          if (jj == nper) {  // dV has been stored: the accumulator is free for dK
+            if (!mbar_wait(acc_free, 0, p.status)) return false;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            const uint32_t dso = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
+            mma_ss(tmem + C::TM_DK, sw128_desc(dsa + dso, 16, 1024),
+                   sw128_desc(slot_addr(0) + kk * 2048, BQ * 128, 1024), idKVt, (jj > nper || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(qdo_empty(0));
+          if (dq_steps >= 1 && !mbar_wait(dq_empty, (dq_steps - 1) & 1, p.status)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int m = 0; m < D / 128; ++m)
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_ss(tmem + C::TM_DQ + m * BQ,
+                     sw128_desc(sbase + C::OFF_K + (2 * m) * (kBK * 128) + kk * 2048, kBK * 128, 1024),
+                     sw128_desc(dsa + kk * 2048, kBK * 128, 1024), idDQ, kk > 0);
+          mma_commit(dq_full);
+          ++dq_steps;
+          mma_commit(mma_done);
+          return true;
+        };
+        auto mma_s = [&](int j) {
+          const uint32_t qa = slot_addr(slot_of(j));
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
+            const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+            mma_ss(tmem + C::TM_S, sw128_desc(sbase + C::OFF_K + ko, 16, 1024), sw128_desc(qa + qo, 16, 1024),
+                   idST, kk > 0);
+          }
+        };
+        for (int j = 0; ok && j <= nsteps; ++j) {
+          if (j < nper) {
+            // dV pass, front first: S^T of step j (its Q slot is free again right after),
+            // then dV of step j - 1.
+            if (j >= 1 && !mbar_wait(sdp_free, (j - 1) & 1, p.status)) break;
+            const int s = slot_of(j);
+            if (!mbar_wait(qdo_full(s), use_of(j) & 1, p.status)) break;
+            tc_fence_after();
+            mma_s(j);
+            mma_commit(s_full);
+            mma_commit(qdo_empty(s));
+            if (j >= 1) {
+              if (!mbar_wait(p_ready, (j - 1) & 1, p.status)) break;
+              tc_fence_after();
+              if (!back_dv(j - 1)) break;
+            }
+          } else {
+            // dK pass, back first: dK / dQ of step j - 1 (dV for the last dV-pass step), then
+            // dP^T of step j (its dO slot is free again right after) and S^T once its Q arrives.
+            if (j >= 1) {
+              if (!mbar_wait(p_ready, (j - 1) & 1, p.status)) break;
+              tc_fence_after();
+              if (!(j - 1 < nper ? back_dv(j - 1) : back_dkdq(j - 1))) break;
+            }
+            if (j < nsteps) {
+              if (j == nper && !mbar_wait(v_full, 0, p.status)) break;
+              if (!mbar_wait(do_full(0), use_of(j) & 1, p.status)) break;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t ko = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
+                const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+                mma_ss(tmem + C::TM_DP, sw128_desc(sbase + C::OFF_V + ko, 16, 1024),
+                       sw128_desc(do_addr(0) + qo, 16, 1024), idST, kk > 0);
+              }
+              mma_commit(do_empty(0));
+              if (!mbar_wait(qdo_full(0), use_of(j) & 1, p.status)) break;
+              tc_fence_after();
+              mma_s(j);
+              mma_commit(s_full);
+            }
+          }
+        }
+      } else
       for (int j = 0; ok && j <= nsteps; ++j) {
         const bool back_first = C::TWO ? (j >= nper) : (NS == 1);
         if (back_first) {
@@ -455,10 +619,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int j = 0; j < nsteps && ok; ++j) {
       const int kind = step_kind(j), q0 = step_q0(j), s = slot_of(j);
-      if (!mbar_wait(qdo_full(s), use_of(j) & 1, p.status)) { ok = false; break; }
       if (!mbar_wait(s_full, j & 1, p.status)) { ok = false; break; }
+      if (C::TWO) {
+        if (!mbar_wait(ld_full(j & 1), (j >> 1) & 1, p.status)) { ok = false; break; }
+      } else {
+        if (!mbar_wait(qdo_full(s), use_of(j) & 1, p.status)) { ok = false; break; }
+      }
       tc_fence_after();
-      const float *lse2 = ld_addr(s);
+      const float *lse2 = ld_addr(C::TWO ? (j & 1) : s);
       const float *dvv = lse2 + BQ;
       const bool full = !any_pairwise && q0 >= cta_lo && q0 + BQ <= cta_hi;
 
@@ -493,6 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bwd_chunk_masked<CAP, 2>(mask, sr, dr, lc, dc, pk[cc], dk[cc], sc2, capc, cap2, fscale, p.scale, qb, lo,
                                    hi, p.Sq, segq, sid);
       }
+      if (C::TWO) mbar_arrive(ld_empty(j & 1));  // LSE / D of this step have been read
       // ... and stored once those MMAs are done with the buffers.
       if (j >= 1 && !mbar_wait(mma_done, (j - 1) & 1, p.status)) { ok = false; break; }
       tc_fence_after();
