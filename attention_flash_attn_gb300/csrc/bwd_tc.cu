@@ -19,9 +19,12 @@
 // Head dim 256: dK and dV fill all 512 TMEM columns, so the CTA runs two passes over its
 // query steps -- dV first, then dK and dQ (S^T recomputed).  V is not needed in the dV pass,
 // so its shared-memory slot doubles as a second Q/dO stage there and V is loaded for the
-// second pass.
+// second pass.  In the dK pass the two halves of the remaining stage swap roles each step
+// (the next Q lands where this step's dO was), so S^T of the next step is computed while the
+// softmax warps still work on this one, and those warps form P from S^T before dP^T is in.
 //
-// Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 2..9 softmax / dS, 10..13 dQ drain.
+// Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 2..9 softmax / dS, 10..13 dQ drain,
+// 14 second MMA issuer (two-pass form: dV / dK / dQ while warp 1 issues S^T / dP^T).
 // Every wait is bounded (tc_common.cuh); named barriers are only used where every
 // participating thread is guaranteed to arrive.
 #include "common.cuh"
@@ -34,8 +37,9 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 128;  // keys per CTA
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr int kSoftmaxThreads = 256;
+constexpr int kDrainThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D_, int BQ_, bool DQT_, bool TWO_, int NS_>
@@ -56,7 +60,7 @@ struct BwdCfg {
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
   static constexpr int OFF_LD = OFF_DQS + DQS_BYTES;  // per slot: LSE*log2e [BQ], D [BQ]
   static constexpr int OFF_BAR = OFF_LD + NSLOT * 2 * BQ * 4;
-  static constexpr int NBAR = 10 + 2 * NSLOT + (TWO ? 8 : 0);
+  static constexpr int NBAR = 11 + 2 * NSLOT + (TWO ? 18 : 0);  // + dQ half-1 release
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   // TMEM columns
@@ -149,6 +153,45 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32
   }
 }
 
+// The dK pass's chunk in two steps, so that the first runs before dP^T has been computed:
+// (1) in place, the raw score -> P f = exp2(t2 - LSE2) (1 - tanh^2) scale, masked entries 0;
+template <bool CAP, int MASK>
+__device__ __forceinline__ void ds_first(uint32_t (&sr)[32], const float *lse2c, float sc2, float capc, float cap2,
+                                         float fscale, float scale, int qbase, int lo, int hi, int sq,
+                                         const int *segq, int sid) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float sv = __uint_as_float(sr[e]);
+    float t2, f;
+    if constexpr (CAP) {
+      const float ee = ex2_approx(fabsf(sv) * capc);
+      const float rr = rcp_approx(1.f + ee);
+      const float th = fmaf(-ee, rr, rr);
+      t2 = copysignf(th * cap2, sv);
+      f = fscale * ee * rr * rr;
+    } else {
+      t2 = sv * sc2;
+      f = scale;
+    }
+    float x = t2 - lse2c[e];
+    if constexpr (MASK >= 1) {
+      const int q = qbase + e;
+      bool vis = (q >= lo) & (q < hi);
+      if constexpr (MASK == 2) vis = vis & (__ldg(segq + min(q, sq - 1)) == sid);
+      x = vis ? x : -INFINITY;
+    }
+    sr[e] = __float_as_uint(ex2_approx(x) * f);
+  }
+}
+// (2) dS = P f (dP - D), packed to bf16 pairs.
+__device__ __forceinline__ void ds_second(const uint32_t (&pf)[32], const uint32_t (&dr)[32], const float *dvc,
+                                          uint32_t (&dk)[16]) {
+#pragma unroll
+  for (int e2 = 0; e2 < 16; ++e2)
+    dk[e2] = pack_bf16(__uint_as_float(pf[2 * e2]) * (__uint_as_float(dr[2 * e2]) - dvc[2 * e2]),
+                       __uint_as_float(pf[2 * e2 + 1]) * (__uint_as_float(dr[2 * e2 + 1]) - dvc[2 * e2 + 1]));
+}
+
 template <bool CAP, int KIND>
 __device__ __forceinline__ void bwd_chunk_masked(int mask, const uint32_t (&sr)[32], const uint32_t (&dr)[32],
                                                  const float *lse2c, const float *dvc, uint32_t (&pk)[16],
@@ -202,7 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t kv_full = bar0, v_full = bar0 + 8u;
   const uint32_t s_full = bar0 + 16u, p_ready = bar0 + 24u, mma_done = bar0 + 32u;
-  const uint32_t dq_full = bar0 + 40u, dq_empty = bar0 + 48u, acc_free = bar0 + 56u, fin_done = bar0 + 64u;
+  const uint32_t dq_full = bar0 + 40u, acc_free = bar0 + 56u, fin_done = bar0 + 64u;
+  // dq_empty(m): the drain has copied half m (d rows 128 m .. 128 m + 127 of dQ^T) out of TMEM.
+  auto dq_empty = [&](int m) { return m == 0 ? bar0 + 48u : bar0 + 8u * (C::NBAR - 1); };
   const uint32_t sdp_free = bar0 + 72u;  // S^T / dP^T copied out of TMEM (256 arrivals)
   // Q/dO stages; in the two-pass form these are the Q ring, and do_full / do_empty the dO ring.
   auto qdo_full = [&](int s) { return bar0 + 8u * (10 + s); };
@@ -213,6 +258,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the Q lane and released by the softmax warps once they have read it.
   auto ld_full = [&](int x) { return bar0 + 8u * (14 + 2 * C::NSLOT + x); };
   auto ld_empty = [&](int x) { return bar0 + 8u * (16 + 2 * C::NSLOT + x); };
+  // Two-pass form, dK pass: stage 0 (64 KiB) becomes a ring of four 16 KiB slots, each one
+  // half (128 of the 256 columns) of a Q or dO tile.  In ring order, step i brings Q_i (for
+  // S^T), Q_{i-1} again (for dK_{i-1}, which runs once the softmax of step i - 1 is done) and
+  // dO_i (for dP^T): no tile stays resident from its S^T to its dK, and every slot is refilled
+  // from one that an earlier MMA of the same order has already released.
+  auto ring_full = [&](int r) { return bar0 + 8u * (18 + 2 * C::NSLOT + r); };
+  auto ring_empty = [&](int r) { return bar0 + 8u * (22 + 2 * C::NSLOT + r); };
+  const uint32_t dp_full = bar0 + 8u * (26 + 2 * C::NSLOT);  // dP^T of a dK-pass step is in TMEM
+  const uint32_t dp_free = bar0 + 8u * (27 + 2 * C::NSLOT);  // ... and has been copied out (256)
+  constexpr int kRing = 4, kHalf = C::QT_BYTES / 2;
+  auto ring_addr = [&](int n) -> uint32_t { return sbase + C::OFF_SLOT0 + (n % kRing) * kHalf; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *red = misc_i + 4;  // [8]
 
@@ -223,9 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(p_ready, kSoftmaxThreads);
     mbar_init(mma_done, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 1);
+    mbar_init(dq_empty(0), kDrainThreads);  // every drain thread has read (its half of) the dQ tile
+    mbar_init(dq_empty(1), kDrainThreads);
     mbar_init(acc_free, kSoftmaxThreads);
-    mbar_init(fin_done, 1);
+    mbar_init(fin_done, C::TWO ? 2 : 1);  // two-pass: both MMA warps finish
     mbar_init(sdp_free, kSoftmaxThreads);
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(qdo_full(s), 1);
@@ -236,6 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(ld_full(s), 1);
         mbar_init(ld_empty(s), kSoftmaxThreads);
       }
+    }
+    if (C::TWO) {
+      for (int r = 0; r < kRing; ++r) {
+        mbar_init(ring_full(r), 1);
+        mbar_init(ring_empty(r), 1);
+      }
+      mbar_init(dp_full, 1);
+      mbar_init(dp_free, kSoftmaxThreads);
     }
     fence_barrier_init();
   }
@@ -265,53 +330,93 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && C::TWO) {
     // ------------------------------------------------------------ TMA producers (two-pass)
-    // Lane 0: K, the Q ring, the LSE / D ring and V's first half; lane 1: the dO ring and
-    // V's second half.  Every ring has this one loader and its waits run in phase order.
+    // dV pass: lane 0 loads K, the Q ring and the LSE / D ring, lane 1 the dO ring.  Between
+    // the passes each lane loads half of V into the dV pass's second stage.  dK pass: lane 0
+    // alone fills the half-tile ring (Q_i, then Q_{i-1} again, then dO_i) and the LSE / D
+    // ring, in the order the MMAs consume them.  Every ring has one loader at a time and its waits run
+    // in phase order.
+    const int u_last0 = ((nper + 1) >> 1) - 1;  // last dV-pass use of stage 0
+    const int u_last1 = (nper >> 1) - 1;        // ... and of stage 1
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
       mbar_arrive_expect_tx(kv_full, C::KV_BYTES);
 #pragma unroll
       for (int c = 0; c < C::KCH; ++c) tma_load_4d(sbase + C::OFF_K + c * (kBK * 128), &tmK, kv_full, c * 64, k0, g, b);
-      for (int j = 0; j < nsteps; ++j) {
-        if (j == nper) {  // V[:, :128] into the Q ring's second slot, free after the dV pass
-          if (nper >= 2 && !mbar_wait(qdo_empty(1), ((nper >> 1) - 1) & 1, p.status)) break;
-          mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
+      int n = 0;  // dK-pass ring position
+      // One half tile (columns 128*hf .. 128*hf + 127 of Q or dO rows q0 .. q0 + BQ - 1) into
+      // the next ring slot.  The first four slots are stage 0 of the dV pass: wait for its last
+      // Q (slots 0, 1) or dO (slots 2, 3) to be released.
+      auto ring_load = [&](const CUtensorMap *tm, int hf, int q0, int h) -> bool {
+        const int r = n % kRing, u = n / kRing;
+        const bool ok = u == 0 ? (r < 2 ? mbar_wait(qdo_empty(0), u_last0 & 1, p.status)
+                                        : mbar_wait(do_empty(0), u_last0 & 1, p.status))
+                               : mbar_wait(ring_empty(r), (u - 1) & 1, p.status);
+        if (!ok) return false;
+        mbar_arrive_expect_tx(ring_full(r), kHalf);
 #pragma unroll
-          for (int c = 0; c < C::KCH / 2; ++c)
-            tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(ring_addr(n) + c * (BQ * 128), tm, ring_full(r), (2 * hf + c) * 64, q0, h, b);
+        ++n;
+        return true;
+      };
+      for (int j = 0; j <= nsteps; ++j) {
+        if (j < nsteps) {  // LSE / D of step j first: the softmax needs them with S^T_j
+          const int x = j & 1, h = step_h(j), q0 = step_q0(j);
+          if (j >= 2 && !mbar_wait(ld_empty(x), ((j >> 1) - 1) & 1, p.status)) break;
+          mbar_arrive_expect_tx(ld_full(x), 2 * BQ * 4);
+          const size_t row = ((size_t)b * p.Hq + h) * p.sq_pad + q0;
+          const uint32_t lda = sbase + C::OFF_LD + x * 2 * BQ * 4;
+          bulk_g2s(lda, p.lse2p + row, BQ * 4, ld_full(x));
+          bulk_g2s(lda + BQ * 4, p.Dvec + row, BQ * 4, ld_full(x));
         }
-        const int s = slot_of(j), u = use_of(j), h = step_h(j), q0 = step_q0(j);
-        if (u >= 1 && !mbar_wait(qdo_empty(s), (u - 1) & 1, p.status)) break;
-        mbar_arrive_expect_tx(qdo_full(s), C::QT_BYTES);
+        if (j < nper) {
+          const int s = slot_of(j), u = use_of(j);
+          if (u >= 1 && !mbar_wait(qdo_empty(s), (u - 1) & 1, p.status)) break;
+          mbar_arrive_expect_tx(qdo_full(s), C::QT_BYTES);
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(slot_addr(s) + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, q0, h, b);
-        const int x = j & 1;
-        if (j >= 2 && !mbar_wait(ld_empty(x), ((j >> 1) - 1) & 1, p.status)) break;
-        mbar_arrive_expect_tx(ld_full(x), 2 * BQ * 4);
-        const size_t row = ((size_t)b * p.Hq + h) * p.sq_pad + q0;
-        const uint32_t lda = sbase + C::OFF_LD + x * 2 * BQ * 4;
-        bulk_g2s(lda, p.lse2p + row, BQ * 4, ld_full(x));
-        bulk_g2s(lda + BQ * 4, p.Dvec + row, BQ * 4, ld_full(x));
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(slot_addr(s) + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, step_q0(j), step_h(j), b);
+        } else if (j < nsteps) {
+          if (j == nper) {  // V[:, :128] into the dV pass's second Q stage
+            if (u_last1 >= 0 && !mbar_wait(qdo_empty(1), u_last1 & 1, p.status)) break;
+            mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
+#pragma unroll
+            for (int c = 0; c < C::KCH / 2; ++c)
+              tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
+          }
+          // Q_i for S^T, Q_{i-1} again for dK of the previous step, dO_i for dP^T
+          const int h = step_h(j), q0 = step_q0(j);
+          if (!ring_load(&tmQ, 0, q0, h) || !ring_load(&tmQ, 1, q0, h)) break;
+          if (j > nper && (!ring_load(&tmQ, 0, step_q0(j - 1), step_h(j - 1)) ||
+                           !ring_load(&tmQ, 1, step_q0(j - 1), step_h(j - 1))))
+            break;
+          if (!ring_load(&tmdO, 0, q0, h) || !ring_load(&tmdO, 1, q0, h)) break;
+        }
+        if (j == nsteps && j > nper) {  // Q of the last step again, for its dK
+          const int h = step_h(j - 1), q0 = step_q0(j - 1);
+          if (!ring_load(&tmQ, 0, q0, h) || !ring_load(&tmQ, 1, q0, h)) break;
+        }
       }
     } else if (lane == 1) {
       tma_prefetch_desc(&tmdO);
-      for (int j = 0; j < nsteps; ++j) {
-        if (j == nper) {  // V[:, 128:] into the dO ring's second slot, free after the dV pass
-          if (nper >= 2 && !mbar_wait(do_empty(1), ((nper >> 1) - 1) & 1, p.status)) break;
-          mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
-#pragma unroll
-          for (int c = C::KCH / 2; c < C::KCH; ++c)
-            tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
-        }
+      bool ok = true;
+      for (int j = 0; j < nper; ++j) {
         const int s = slot_of(j), u = use_of(j);
-        if (u >= 1 && !mbar_wait(do_empty(s), (u - 1) & 1, p.status)) break;
+        if (u >= 1 && !mbar_wait(do_empty(s), (u - 1) & 1, p.status)) { ok = false; break; }
         mbar_arrive_expect_tx(do_full(s), C::QT_BYTES);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
           tma_load_4d(do_addr(s) + c * (BQ * 128), &tmdO, do_full(s), c * 64, step_q0(j), step_h(j), b);
+      }
+      // V[:, 128:] into the dV pass's second dO stage
+      if (ok && nper > 0 && (u_last1 < 0 || mbar_wait(do_empty(1), u_last1 & 1, p.status))) {
+        mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
+#pragma unroll
+        for (int c = C::KCH / 2; c < C::KCH; ++c)
+          tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
       }
     }
   } else if (warp == 0) {
@@ -352,220 +457,226 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_g2s(lda + BQ * 4, p.Dvec + row, BQ * 4, qdo_full(s));
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp == 1 || warp == 14) {
+    // ------------------------------------------------------------ MMA issuers
+    // Each issuing warp runs its loop with warp-uniform values and one elected lane issues
+    // each MMA and commit; descriptors are built once per operand and advanced by constant
+    // offsets.  In the two-pass form warp 1 issues the front MMAs (S^T, dP^T) and warp 14 the
+    // back ones (dV, dK, dQ), so neither waits behind the other's queue; the fused form uses
+    // warp 1 alone.
+    const bool back_warp = warp == 14;
+    if (C::TWO || !back_warp) {
       constexpr uint32_t idST = idesc_bf16(kBK, BQ, false, false);  // S^T, dP^T
       constexpr uint32_t idKV = idesc_bf16(kBK, D, false, true);    // dV, dK
+      constexpr uint32_t idKh = idesc_bf16(kBK, D / 2, false, true);  // one half of dK (two-pass)
       constexpr uint32_t idDQ = C::DQT ? idesc_bf16(128, BQ, true, true) : idesc_bf16(BQ, D, true, true);
-      bool ok = mbar_wait(kv_full, 0, p.status);
-      int dq_steps = 0;
-      // dV / dK / dQ of step jj (P^T in TMEM and dS^T in shared memory are ready).
-      auto issue_back = [&](int jj) -> bool {
-        const int s = slot_of(jj), kind = step_kind(jj);
-        const uint32_t qa = slot_addr(s), oa = qa + C::QT_BYTES;
-        const uint32_t dsa = sbase + C::OFF_DS;
-        const bool first = C::TWO ? (jj == 0 || jj == nper) : (jj == 0);
-        if (C::TWO && jj == nper) {  // dV has been stored: the accumulator is free for dK
-          if (!mbar_wait(acc_free, 0, p.status)) return false;
-          tc_fence_after();
+      const uint64_t dK_k = sw128_desc(sbase + C::OFF_K, 16, 1024);          // K, K-major (A of S^T)
+      const uint64_t dV_k = sw128_desc(sbase + C::OFF_V, 16, 1024);          // V, K-major (A of dP^T)
+      const uint64_t dK_mn = sw128_desc(sbase + C::OFF_K, kBK * 128, 1024);  // K, d contiguous
+      const uint64_t dS_k = sw128_desc(sbase + C::OFF_DS, 16, 1024);         // dS^T, K-major (A of dK)
+      const uint64_t dS_mn = sw128_desc(sbase + C::OFF_DS, kBK * 128, 1024); // dS^T, q contiguous
+      // S^T (A = K) or dP^T (A = V) over D from a Q / dO tile whose 64-column chunks lie
+      // chunk_stride bytes apart.
+      // Loops over 64-column chunks stay rolled (the descriptors advance by one add per
+      // chunk) and the four 16-deep MMAs of a chunk are unrolled: compact code that still
+      // issues faster than the tensor pipe retires.
+      auto mma_front = [&](uint64_t a_k, uint32_t b_addr, uint32_t d_col) {
+        uint64_t b_k = sw128_desc(b_addr, 16, 1024);
+#pragma unroll 1
+        for (int c = 0; c < D / 64; ++c) {
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            mma_ss_w(tmem + d_col, desc_at(a_k, k4 * 32), desc_at(b_k, k4 * 32), idST, (c | k4) != 0);
+          a_k = desc_at(a_k, kBK * 128);
+          b_k = desc_at(b_k, BQ * 128);
         }
-        if (kind != 2) {  // dV += P^T dO
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, sw128_desc(oa + kk * 2048, BQ * 128, 1024), idKV,
-                   (!first || kk > 0) ? 1u : 0u);
-        }
-        if (kind != 1) {
-          // dK += dS^T Q   (A = dS^T, K-major in shared memory)
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk) {
-            const uint32_t dso = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
-            mma_ss(tmem + C::TM_DK, sw128_desc(dsa + dso, 16, 1024), sw128_desc(qa + kk * 2048, BQ * 128, 1024),
-                   idKV, (!first || kk > 0) ? 1u : 0u);
-          }
-          // dQ for this step: the previous one must have been drained
-          if (dq_steps >= 1 && !mbar_wait(dq_empty, (dq_steps - 1) & 1, p.status)) return false;
-          tc_fence_after();
-          if constexpr (C::DQT) {
-            // dQ^T[d, q] = K^T dS^T : A = K (MN-major, d contiguous), B = dS^T (MN-major, q contiguous)
-#pragma unroll
-            for (int m = 0; m < D / 128; ++m)
-#pragma unroll
-              for (int kk = 0; kk < kBK / 16; ++kk)
-                mma_ss(tmem + C::TM_DQ + m * BQ,
-                       sw128_desc(sbase + C::OFF_K + (2 * m) * (kBK * 128) + kk * 2048, kBK * 128, 1024),
-                       sw128_desc(dsa + kk * 2048, kBK * 128, 1024), idDQ, kk > 0);
-          } else {
-            // dQ[q, d] = dS K : A = dS (MN-major, q contiguous), B = K (MN-major, d contiguous)
+      };
+      // dQ of a step from dS^T in shared memory, each half of D once the drain has copied the
+      // previous step's out of TMEM.
+      auto mma_dq = [&](int dq_steps) -> bool {
+        if constexpr (C::DQT) {
+          // dQ^T[d, q] = K^T dS^T : A = K (d contiguous), B = dS^T (q contiguous)
+#pragma unroll 1
+          for (int m = 0; m < D / 128; ++m) {
+            if (dq_steps >= 1 && !mbar_wait_warp(dq_empty(m), (dq_steps - 1) & 1, p.status)) return false;
+            tc_fence_after();
+            const uint64_t a_m = desc_at(dK_mn, (2 * m) * (kBK * 128));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_ss(tmem + C::TM_DQ, sw128_desc(dsa + kk * 2048, kBK * 128, 1024),
-                     sw128_desc(sbase + C::OFF_K + kk * 2048, kBK * 128, 1024), idDQ, kk > 0);
+              mma_ss_w(tmem + C::TM_DQ + m * BQ, desc_at(a_m, kk * 2048), desc_at(dS_mn, kk * 2048), idDQ, kk > 0);
           }
-          mma_commit(dq_full);
-          ++dq_steps;
+        } else {
+          // dQ[q, d] = dS K : A = dS (q contiguous), B = K (d contiguous)
+          if (dq_steps >= 1 && !mbar_wait_warp(dq_empty(0), (dq_steps - 1) & 1, p.status)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_ss_w(tmem + C::TM_DQ, desc_at(dS_mn, kk * 2048), desc_at(dK_mn, kk * 2048), idDQ, kk > 0);
         }
-        mma_commit(mma_done);
-        mma_commit(qdo_empty(s));
         return true;
       };
-      // S^T (and dP^T) of step j.
-      auto issue_front = [&](int j) -> bool {
-        const int s = slot_of(j), kind = step_kind(j);
-        if (C::TWO && j == nper) {
-          if (!mbar_wait(v_full, 0, p.status)) return false;
-        }
-        if (!mbar_wait(qdo_full(s), use_of(j) & 1, p.status)) return false;
-        tc_fence_after();
-        const uint32_t qa = slot_addr(s), oa = qa + C::QT_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
-          const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-          mma_ss(tmem + C::TM_S, sw128_desc(sbase + C::OFF_K + ko, 16, 1024), sw128_desc(qa + qo, 16, 1024), idST,
-                 kk > 0);
-        }
-        if (kind != 1) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
-            const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-            mma_ss(tmem + C::TM_DP, sw128_desc(sbase + C::OFF_V + ko, 16, 1024), sw128_desc(oa + qo, 16, 1024),
-                   idST, kk > 0);
-          }
-        }
-        mma_commit(s_full);
-        return true;
-      };
-      // With two or more stages, S^T / dP^T of step j go ahead of dV / dK / dQ of step j - 1,
-      // so the softmax of step j overlaps them.  Where a step's stage can only be refilled
-      // after the previous step's MMAs release it (single stage; the dK pass of the two-pass
-      // form), the order is back-to-front.
-      // S^T / dP^T of step j may start as soon as the softmax has copied step j - 1's out
-      // of TMEM (sdp_free); dV / dK / dQ of step j - 1 need its P and dS (p_ready).
+      bool ok = mbar_wait_warp(kv_full, 0, p.status);
+      int dq_steps = 0;
       if constexpr (C::TWO) {
-        constexpr uint32_t idKVt = idesc_bf16(kBK, D, false, true);
+        const int nB = nsteps - nper;  // dK-pass steps
+        // Ring positions of dK-pass step i's tiles, in the order the loader fills the ring:
+        // Q_0 dO_0 | Q_1 Qb_0 dO_1 | Q_2 Qb_1 dO_2 | ... | Qb_{nB-1}  (Qb: Q again, for dK).
+        auto pos_q = [&](int i) { return i == 0 ? 0 : 6 * i - 2; };
+        auto pos_do = [&](int i) { return i == 0 ? 2 : 6 * i + 2; };
+        auto pos_qb = [&](int i) { return i + 1 < nB ? 6 * (i + 1) : 6 * nB - 2; };
         // dV of a dV-pass step: P^T from TMEM, dO of its slot; releases that dO slot.
         auto back_dv = [&](int jj) -> bool {
           const int s = slot_of(jj);
-          if (!mbar_wait(do_full(s), use_of(jj) & 1, p.status)) return false;
+          if (!mbar_wait_warp(do_full(s), use_of(jj) & 1, p.status)) return false;
           tc_fence_after();
+          const uint64_t o_mn = sw128_desc(do_addr(s), BQ * 128, 1024);
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, sw128_desc(do_addr(s) + kk * 2048, BQ * 128, 1024),
-                   idKVt, (jj > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(do_empty(s));
-          mma_commit(mma_done);
+            mma_ts_w(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, desc_at(o_mn, kk * 2048), idKV,
+                     (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_w(do_empty(s));
+          mma_commit_w(mma_done);
           return true;
         };
-        // dK (releases the Q slot) and dQ of a dK-pass step.
+        // dK (Q of the step again, from two ring slots, each released after its 128-column
+        // half of dK) and dQ of a dK-pass step.
         auto back_dkdq = [&](int jj) -> bool {
-          const uint32_t dsa = sbase + C::OFF_DS;
           if (jj == nper) {  // dV has been stored: the accumulator is free for dK
-            if (!mbar_wait(acc_free, 0, p.status)) return false;
+            if (!mbar_wait_warp(acc_free, 0, p.status)) return false;
             tc_fence_after();
           }
+          const int n0 = pos_qb(jj - nper);
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            const int n = n0 + hf, r = n % kRing;
+            if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
+            tc_fence_after();
+            const uint64_t q_mn = sw128_desc(ring_addr(n), BQ * 128, 1024);
 #pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk) {
-            const uint32_t dso = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
-            mma_ss(tmem + C::TM_DK, sw128_desc(dsa + dso, 16, 1024),
-                   sw128_desc(slot_addr(0) + kk * 2048, BQ * 128, 1024), idKVt, (jj > nper || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BQ / 16; ++kk)
+              mma_ss_w(tmem + C::TM_DK + hf * (D / 2), desc_at(dS_k, (kk >> 2) * (kBK * 128) + (kk & 3) * 32),
+                       desc_at(q_mn, kk * 2048), idKh, (jj > nper || kk > 0) ? 1u : 0u);
+            mma_commit_w(ring_empty(r));
           }
-          mma_commit(qdo_empty(0));
-          if (dq_steps >= 1 && !mbar_wait(dq_empty, (dq_steps - 1) & 1, p.status)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int m = 0; m < D / 128; ++m)
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_ss(tmem + C::TM_DQ + m * BQ,
-                     sw128_desc(sbase + C::OFF_K + (2 * m) * (kBK * 128) + kk * 2048, kBK * 128, 1024),
-                     sw128_desc(dsa + kk * 2048, kBK * 128, 1024), idDQ, kk > 0);
-          mma_commit(dq_full);
+          if (!mma_dq(dq_steps)) return false;
+          mma_commit_w(dq_full);
           ++dq_steps;
-          mma_commit(mma_done);
+          mma_commit_w(mma_done);
           return true;
         };
-        auto mma_s = [&](int j) {
-          const uint32_t qa = slot_addr(slot_of(j));
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
-            const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-            mma_ss(tmem + C::TM_S, sw128_desc(sbase + C::OFF_K + ko, 16, 1024), sw128_desc(qa + qo, 16, 1024),
-                   idST, kk > 0);
-          }
-        };
-        for (int j = 0; ok && j <= nsteps; ++j) {
-          if (j < nper) {
-            // dV pass, front first: S^T of step j (its Q slot is free again right after),
-            // then dV of step j - 1.
-            if (j >= 1 && !mbar_wait(sdp_free, (j - 1) & 1, p.status)) break;
-            const int s = slot_of(j);
-            if (!mbar_wait(qdo_full(s), use_of(j) & 1, p.status)) break;
+        // S^T (A = K) or dP^T (A = V) of a dK-pass step from the two ring slots at n0, n0 + 1
+        // (the two column halves of Q or dO), each slot released once read.
+        auto front_ring = [&](uint64_t a_k, uint32_t d_col, int n0) -> bool {
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            const int n = n0 + hf, r = n % kRing;
+            if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
             tc_fence_after();
-            mma_s(j);
-            mma_commit(s_full);
-            mma_commit(qdo_empty(s));
-            if (j >= 1) {
-              if (!mbar_wait(p_ready, (j - 1) & 1, p.status)) break;
-              tc_fence_after();
-              if (!back_dv(j - 1)) break;
-            }
-          } else {
-            // dK pass, back first: dK / dQ of step j - 1 (dV for the last dV-pass step), then
-            // dP^T of step j (its dO slot is free again right after) and S^T once its Q arrives.
-            if (j >= 1) {
-              if (!mbar_wait(p_ready, (j - 1) & 1, p.status)) break;
-              tc_fence_after();
-              if (!(j - 1 < nper ? back_dv(j - 1) : back_dkdq(j - 1))) break;
-            }
-            if (j < nsteps) {
-              if (j == nper && !mbar_wait(v_full, 0, p.status)) break;
-              if (!mbar_wait(do_full(0), use_of(j) & 1, p.status)) break;
-              tc_fence_after();
+            uint64_t b_k = sw128_desc(ring_addr(n), 16, 1024);
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {  // the two 64-column chunks of this half
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t ko = (kk >> 2) * (kBK * 128) + (kk & 3) * 32;
-                const uint32_t qo = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-                mma_ss(tmem + C::TM_DP, sw128_desc(sbase + C::OFF_V + ko, 16, 1024),
-                       sw128_desc(do_addr(0) + qo, 16, 1024), idST, kk > 0);
-              }
-              mma_commit(do_empty(0));
-              if (!mbar_wait(qdo_full(0), use_of(j) & 1, p.status)) break;
-              tc_fence_after();
-              mma_s(j);
-              mma_commit(s_full);
+              for (int k4 = 0; k4 < 4; ++k4)
+                mma_ss_w(tmem + d_col, desc_at(a_k, k4 * 32), desc_at(b_k, k4 * 32), idST, (hf | c | k4) != 0);
+              a_k = desc_at(a_k, kBK * 128);
+              b_k = desc_at(b_k, BQ * 128);
             }
+            mma_commit_w(ring_empty(r));
+          }
+          return true;
+        };
+        if (!back_warp) {
+          // Front: S^T of every step (dV pass: from its Q stage, which is free again right
+          // after), dP^T of every dK-pass step, each as soon as the softmax has copied out
+          // the previous one.
+          for (int j = 0; ok && j < nsteps; ++j) {
+            if (j >= 1 && !mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
+            if (j < nper) {
+              const int s = slot_of(j);
+              if (!mbar_wait_warp(qdo_full(s), use_of(j) & 1, p.status)) break;
+              tc_fence_after();
+              mma_front(dK_k, slot_addr(s), C::TM_S);
+              mma_commit_w(s_full);
+              mma_commit_w(qdo_empty(s));
+            } else {
+              const int i = j - nper;
+              if (!front_ring(dK_k, C::TM_S, pos_q(i))) break;
+              mma_commit_w(s_full);
+              if (i == 0 && !mbar_wait_warp(v_full, 0, p.status)) break;
+              if (i >= 1 && !mbar_wait_warp(dp_free, (i - 1) & 1, p.status)) break;
+              if (!front_ring(dV_k, C::TM_DP, pos_do(i))) break;
+              mma_commit_w(dp_full);
+            }
+          }
+        } else {
+          // Back: dV (dV pass) or dK and dQ (dK pass) of step j - 1 once its P or dS is in.
+          for (int j = 1; ok && j <= nsteps; ++j) {
+            if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+            tc_fence_after();
+            if (!(j - 1 < nper ? back_dv(j - 1) : back_dkdq(j - 1))) break;
           }
         }
-      } else
-      for (int j = 0; ok && j <= nsteps; ++j) {
-        const bool back_first = C::TWO ? (j >= nper) : (NS == 1);
-        if (back_first) {
-          if (j >= 1) {
-            if (!mbar_wait(p_ready, (j - 1) & 1, p.status)) break;
-            tc_fence_after();
-            if (!issue_back(j - 1)) break;
-          }
-          if (j < nsteps && !issue_front(j)) break;
-        } else {
-          if (j < nsteps) {
+      } else {
+        // dV / dK / dQ of step jj (P^T in TMEM and dS^T in shared memory are ready).
+        auto issue_back = [&](int jj) -> bool {
+          const int s = slot_of(jj);
+          const uint64_t q_mn = sw128_desc(slot_addr(s), BQ * 128, 1024);
+          const uint64_t o_mn = desc_at(q_mn, C::QT_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO
+            mma_ts_w(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, desc_at(o_mn, kk * 2048), idKV,
+                     (jj > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
+            mma_ss_w(tmem + C::TM_DK, desc_at(dS_k, (kk >> 2) * (kBK * 128) + (kk & 3) * 32),
+                     desc_at(q_mn, kk * 2048), idKV, (jj > 0 || kk > 0) ? 1u : 0u);
+          if (!mma_dq(dq_steps)) return false;
+          mma_commit_w(dq_full);
+          ++dq_steps;
+          mma_commit_w(mma_done);
+          mma_commit_w(qdo_empty(s));
+          return true;
+        };
+        // S^T and dP^T of step j.
+        auto issue_front = [&](int j) -> bool {
+          const int s = slot_of(j);
+          if (!mbar_wait_warp(qdo_full(s), use_of(j) & 1, p.status)) return false;
+          tc_fence_after();
+          mma_front(dK_k, slot_addr(s), C::TM_S);
+          mma_front(dV_k, slot_addr(s) + C::QT_BYTES, C::TM_DP);
+          mma_commit_w(s_full);
+          return true;
+        };
+        // With two or more stages, S^T / dP^T of step j go ahead of dV / dK / dQ of step
+        // j - 1, so the softmax of step j overlaps them: S^T / dP^T of step j may start as
+        // soon as the softmax has copied step j - 1's out of TMEM (sdp_free); dV / dK / dQ of
+        // step j - 1 need its P and dS (p_ready).  A single stage can only be refilled after
+        // the previous step's MMAs release it, so there the order is back-to-front.
+        for (int j = 0; ok && j <= nsteps; ++j) {
+          if (NS == 1) {
             if (j >= 1) {
-              if (!mbar_wait(sdp_free, (j - 1) & 1, p.status)) break;
+              if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
               tc_fence_after();
+              if (!issue_back(j - 1)) break;
             }
-            if (!issue_front(j)) break;
-          }
-          if (j >= 1) {
-            if (!mbar_wait(p_ready, (j - 1) & 1, p.status)) break;
-            tc_fence_after();
-            if (!issue_back(j - 1)) break;
+            if (j < nsteps && !issue_front(j)) break;
+          } else {
+            if (j < nsteps) {
+              if (j >= 1) {
+                if (!mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
+                tc_fence_after();
+              }
+              if (!issue_front(j)) break;
+            }
+            if (j >= 1) {
+              if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+              tc_fence_after();
+              if (!issue_back(j - 1)) break;
+            }
           }
         }
       }
-      mma_commit(fin_done);  // every MMA issued by this CTA has completed
+      mma_commit_w(fin_done);  // every MMA issued by this CTA has completed
     }
   } else if (warp < 10) {
     // ------------------------------------------------------------ softmax / dS warps
@@ -636,30 +747,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int NCH = BQ / 64;  // 32-column chunks per thread and step
       const int mask = full ? 0 : (seg_pairwise ? 2 : 1);
       uint32_t pk[NCH][16], dk[NCH][16];
+      if (C::TWO && kind == 2) {
+        // dK pass: P f from S^T first, then dP^T (computed meanwhile) for dS.
+        uint32_t pf[NCH][32];
 #pragma unroll
-      for (int cc = 0; cc < NCH; ++cc) {
-        const int c = half * NCH + cc;  // 32-column chunk of this step
-        uint32_t sr[32], dr[32];
-        tmem_ld32(lane_addr + C::TM_S + c * 32, sr);
-        if (kind != 1) tmem_ld32(lane_addr + C::TM_DP + c * 32, dr);
-        tmem_wait_ld();
-        reg_fence(sr);
-        if (kind != 1) reg_fence(dr);
-        if (cc == NCH - 1) {
-          tc_fence_before();
-          mbar_arrive(sdp_free);
+        for (int cc = 0; cc < NCH; ++cc) {
+          const int c = half * NCH + cc;
+          tmem_ld32(lane_addr + C::TM_S + c * 32, pf[cc]);
+          tmem_wait_ld();
+          reg_fence(pf[cc]);
+          if (cc == NCH - 1) {
+            tc_fence_before();
+            mbar_arrive(sdp_free);
+          }
+          const float *lc = lse2 + c * 32;
+          const int qb = q0 + c * 32;
+          if (mask == 0)
+            ds_first<CAP, 0>(pf[cc], lc, sc2, capc, cap2, fscale, p.scale, qb, lo, hi, p.Sq, segq, sid);
+          else if (mask == 1)
+            ds_first<CAP, 1>(pf[cc], lc, sc2, capc, cap2, fscale, p.scale, qb, lo, hi, p.Sq, segq, sid);
+          else
+            ds_first<CAP, 2>(pf[cc], lc, sc2, capc, cap2, fscale, p.scale, qb, lo, hi, p.Sq, segq, sid);
         }
-        const float *lc = lse2 + c * 32, *dc = dvv + c * 32;
-        const int qb = q0 + c * 32;
-        if (kind == 0)
-          bwd_chunk_masked<CAP, 0>(mask, sr, dr, lc, dc, pk[cc], dk[cc], sc2, capc, cap2, fscale, p.scale, qb, lo,
-                                   hi, p.Sq, segq, sid);
-        else if (kind == 1)
-          bwd_chunk_masked<CAP, 1>(mask, sr, dr, lc, dc, pk[cc], dk[cc], sc2, capc, cap2, fscale, p.scale, qb, lo,
-                                   hi, p.Sq, segq, sid);
-        else
-          bwd_chunk_masked<CAP, 2>(mask, sr, dr, lc, dc, pk[cc], dk[cc], sc2, capc, cap2, fscale, p.scale, qb, lo,
-                                   hi, p.Sq, segq, sid);
+        if (!mbar_wait(dp_full, (j - nper) & 1, p.status)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < NCH; ++cc) {
+          const int c = half * NCH + cc;
+          uint32_t dr[32];
+          tmem_ld32(lane_addr + C::TM_DP + c * 32, dr);
+          tmem_wait_ld();
+          reg_fence(dr);
+          if (cc == NCH - 1) {
+            tc_fence_before();
+            mbar_arrive(dp_free);
+          }
+          ds_second(pf[cc], dr, dvv + c * 32, dk[cc]);
+        }
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < NCH; ++cc) {
+          const int c = half * NCH + cc;  // 32-column chunk of this step
+          uint32_t sr[32], dr[32];
+          tmem_ld32(lane_addr + C::TM_S + c * 32, sr);
+          if (kind != 1) tmem_ld32(lane_addr + C::TM_DP + c * 32, dr);
+          tmem_wait_ld();
+          reg_fence(sr);
+          if (kind != 1) reg_fence(dr);
+          if (cc == NCH - 1) {
+            tc_fence_before();
+            mbar_arrive(sdp_free);
+          }
+          const float *lc = lse2 + c * 32, *dc = dvv + c * 32;
+          const int qb = q0 + c * 32;
+          if (kind == 0)
+            bwd_chunk_masked<CAP, 0>(mask, sr, dr, lc, dc, pk[cc], dk[cc], sc2, capc, cap2, fscale, p.scale, qb, lo,
+                                     hi, p.Sq, segq, sid);
+          else
+            bwd_chunk_masked<CAP, 1>(mask, sr, dr, lc, dc, pk[cc], dk[cc], sc2, capc, cap2, fscale, p.scale, qb, lo,
+                                     hi, p.Sq, segq, sid);
+        }
       }
       if (C::TWO) mbar_arrive(ld_empty(j & 1));  // LSE / D of this step have been read
       // ... and stored once those MMAs are done with the buffers.
@@ -758,26 +905,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar<2, 128>();
       if (!*flag) break;
       tc_fence_after();
-      // Copy the whole dQ tile out of TMEM first and release it at once, so the next dQ
-      // MMA never waits for the staging below.
-      uint32_t v[C::DQ_COLS];
-#pragma unroll
-      for (int c = 0; c < C::DQ_COLS / 32; ++c)
-        tmem_ld32(lane_addr + C::TM_DQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
-      tmem_wait_ld();
-      reg_fence(v);
-      tc_fence_before();
-      if (t == 0) mbar_arrive(dq_empty);
       if constexpr (C::DQT) {
-        // dQ^T: lane = d within a 128-wide half, column = query.  Box [128 d, 32 q].
-#pragma unroll
+        // dQ^T: lane = d within a 128-wide half of D, column = query.  One half at a time goes
+        // to registers and is released at once (the next step's dQ MMAs for that half may
+        // start), then leaves through [128 d, 32 q] boxes staged in shared memory for bulk
+        // reduce-adds into the fp32 accumulator.
+#pragma unroll 1
         for (int m = 0; m < D / 128; ++m) {
+          uint32_t v[BQ];
+#pragma unroll
+          for (int c = 0; c < BQ / 32; ++c)
+            tmem_ld32(lane_addr + C::TM_DQ + m * BQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+          tmem_wait_ld();
+          reg_fence(v);
+          tc_fence_before();
+          mbar_arrive(dq_empty(m));  // this thread is done with this half of the TMEM tile
 #pragma unroll
           for (int c = 0; c < BQ / 32; ++c) {
             if (t == 0) bulk_wait_read_all();  // the previous box has left shared memory
             named_bar<2, 128>();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) stage[e * 128 + row] = __uint_as_float(v[m * BQ + c * 32 + e]);
+            for (int e = 0; e < 32; ++e) stage[e * 128 + row] = __uint_as_float(v[c * 32 + e]);
             fence_async_smem();
             named_bar<2, 128>();
             if (t == 0) {
@@ -787,7 +935,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        // dQ: lane = query row, column = d.  Box [32 d, 128 q], 128-byte swizzled.
+        // dQ: lane = query row, column = d.  Copy the whole tile out of TMEM and release it
+        // at once, then stage [32 d, 128 q] boxes (128-byte swizzled) for bulk reduce-adds.
+        uint32_t v[C::DQ_COLS];
+#pragma unroll
+        for (int c = 0; c < C::DQ_COLS / 32; ++c)
+          tmem_ld32(lane_addr + C::TM_DQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+        tmem_wait_ld();
+        reg_fence(v);
+        tc_fence_before();
+        mbar_arrive(dq_empty(0));  // this thread is done with the TMEM tile
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           if (t == 0) bulk_wait_read_all();

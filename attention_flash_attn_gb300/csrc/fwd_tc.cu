@@ -3,7 +3,7 @@
 // One CTA computes one 128-row query tile of one (batch, query head):
 //   warp 0      TMA producers: the Q tile once, then K tiles (lane 0) and V tiles (lane 1)
 //               into separate rings, each slot released as soon as its MMA has read it;
-//   warp 1      MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one of two TMEM
+//   warp 1      MMA issuer (one elected lane of the converged warp) and TMEM owner: S_j = Q K_j^T into one of two TMEM
 //               score buffers, then O += P_{j-1} V_{j-1} with P read from TMEM;
 //   warps 2..9  softmax: a query row is a TMEM lane, and the two warps that share a lane
 //               quarter split its BN key columns.  Per KV tile each thread reads its half
@@ -225,40 +225,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
+    // The whole warp runs this loop with warp-uniform values; one elected lane issues each
+    // MMA and commit.  Descriptors are built once and advanced by constant offsets.
+    if (n > 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, BN, false, false);
       constexpr uint32_t idO = idesc_bf16(kBM, D, false, true);
-      bool ok = mbar_wait(q_full, 0, p.status);
+      const uint64_t dq0 = sw128_desc(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t dk0 = sw128_desc(sbase + C::OFF_K, 16, 1024);
+      const uint64_t dv0 = sw128_desc(sbase + C::OFF_V, BN * 128, 1024);
+      bool ok = mbar_wait_warp(q_full, 0, p.status);
       for (int j = 0; ok && j <= n; ++j) {
         if (j < n) {
           const int s = j % NK;
-          if (!mbar_wait(k_full(s), (j / NK) & 1, p.status)) break;
+          if (!mbar_wait_warp(k_full(s), (j / NK) & 1, p.status)) break;
           tc_fence_after();
           const uint32_t dS = tmem + (uint32_t)((j & 1) * BN);
-          const uint32_t qa = sbase + C::OFF_Q, ka = sbase + C::OFF_K + s * C::KV_BYTES;
+          // 64-column chunks rolled (one descriptor add each), their four MMAs unrolled.
+          uint64_t qd = dq0, kd = desc_at(dk0, s * C::KV_BYTES);
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad = sw128_desc(qa + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sw128_desc(ka + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-            mma_ss(dS, ad, bd, idS, kk > 0);
+            for (int k4 = 0; k4 < 4; ++k4) mma_ss_w(dS, desc_at(qd, k4 * 32), desc_at(kd, k4 * 32), idS, (c | k4) != 0);
+            qd = desc_at(qd, kBM * 128);
+            kd = desc_at(kd, BN * 128);
           }
-          mma_commit(s_full(j & 1));
-          mma_commit(k_empty(s));
+          mma_commit_w(s_full(j & 1));
+          mma_commit_w(k_empty(s));
         }
         if (j >= 1) {
           const int jj = j - 1, s = jj % NV;
-          if (!mbar_wait(v_full(s), (jj / NV) & 1, p.status)) break;
-          if (!mbar_wait(p_full(jj & 1), (jj >> 1) & 1, p.status)) break;
+          if (!mbar_wait_warp(v_full(s), (jj / NV) & 1, p.status)) break;
+          if (!mbar_wait_warp(p_full(jj & 1), (jj >> 1) & 1, p.status)) break;
           tc_fence_after();
-          const uint32_t va = sbase + C::OFF_V + s * C::KV_BYTES;
+          const uint64_t dvs = desc_at(dv0, s * C::KV_BYTES);
           const uint32_t pa = tmem + (uint32_t)((jj & 1) * BN);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t bd = sw128_desc(va + kk * (16 * 128), BN * 128, 1024);
-            mma_ts(tmem + C::TM_O, pa + kk * 8, bd, idO, (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(v_empty(s));
-          mma_commit(o_done);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts_w(tmem + C::TM_O, pa + kk * 8, desc_at(dvs, kk * (16 * 128)), idO, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_w(v_empty(s));
+          mma_commit_w(o_done);
         }
       }
     }
