@@ -249,7 +249,7 @@ int attn_check_device_status(void *ws, attn_stream_t stream) {
   unsigned word = 0;
   if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
   if (word == 0) return ATTN_OK;
-  if (cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return ATTN_ERR_CUDA;  // detail words stay
   return ATTN_ERR_DEVICE;
 }
 

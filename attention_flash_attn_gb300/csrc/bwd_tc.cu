@@ -24,7 +24,9 @@
 // softmax warps still work on this one, and those warps form P from S^T before dP^T is in.
 //
 // Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 2..9 softmax / dS, 10..13 dQ drain,
-// 14 second MMA issuer (two-pass form: dV / dK / dQ while warp 1 issues S^T / dP^T).
+// 14 second MMA issuer (the MMAs that consume P and dS while warp 1 issues S^T / dP^T).
+// Every mbarrier is waited on phase by phase by each of its waiters: a parity wait cannot
+// tell a phase from the one two later, so no waiter may skip one or fall two behind.
 // Every wait is bounded (tc_common.cuh); named barriers are only used where every
 // participating thread is guaranteed to arrive.
 #include "common.cuh"
@@ -60,7 +62,7 @@ struct BwdCfg {
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
   static constexpr int OFF_LD = OFF_DQS + DQS_BYTES;  // per slot: LSE*log2e [BQ], D [BQ]
   static constexpr int OFF_BAR = OFF_LD + NSLOT * 2 * BQ * 4;
-  static constexpr int NBAR = 11 + 2 * NSLOT + (TWO ? 18 : 0);  // + dQ half-1 release
+  static constexpr int NBAR = 12 + 2 * NSLOT + (TWO ? 18 : 0);  // + dQ half-1 release, dO stage hand-over
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   // TMEM columns
@@ -248,6 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t dq_full = bar0 + 40u, acc_free = bar0 + 56u, fin_done = bar0 + 64u;
   // dq_empty(m): the drain has copied half m (d rows 128 m .. 128 m + 127 of dQ^T) out of TMEM.
   auto dq_empty = [&](int m) { return m == 0 ? bar0 + 48u : bar0 + 8u * (C::NBAR - 1); };
+  // Two-pass form: the dV pass's first dO stage is free for the ring.  Lane 1, which waits on
+  // that stage's releases in order, hands it to lane 0 through this single-phase barrier (a
+  // waiter that has not seen a barrier's earlier phases could mistake one for the next).
+  const uint32_t do0_free = bar0 + 8u * (C::NBAR - 2);
   const uint32_t sdp_free = bar0 + 72u;  // S^T / dP^T copied out of TMEM (256 arrivals)
   // Q/dO stages; in the two-pass form these are the Q ring, and do_full / do_empty the dO ring.
   auto qdo_full = [&](int s) { return bar0 + 8u * (10 + s); };
@@ -261,8 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Two-pass form, dK pass: stage 0 (64 KiB) becomes a ring of four 16 KiB slots, each one
   // half (128 of the 256 columns) of a Q or dO tile.  In ring order, step i brings Q_i (for
   // S^T), Q_{i-1} again (for dK_{i-1}, which runs once the softmax of step i - 1 is done) and
-  // dO_i (for dP^T): no tile stays resident from its S^T to its dK, and every slot is refilled
-  // from one that an earlier MMA of the same order has already released.
+  // dO_i (for dP^T): no tile stays resident from its S^T to its dK.
   auto ring_full = [&](int r) { return bar0 + 8u * (18 + 2 * C::NSLOT + r); };
   auto ring_empty = [&](int r) { return bar0 + 8u * (22 + 2 * C::NSLOT + r); };
   const uint32_t dp_full = bar0 + 8u * (26 + 2 * C::NSLOT);  // dP^T of a dK-pass step is in TMEM
@@ -277,12 +282,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(v_full, C::TWO ? 2 : 1);  // two-pass: V arrives in two halves from two lanes
     mbar_init(s_full, 1);
     mbar_init(p_ready, kSoftmaxThreads);
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, C::TWO ? 2 : 1);  // two-pass: dV / dQ (back warp) and dK (front warp)
+    mbar_init(do0_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty(0), kDrainThreads);  // every drain thread has read (its half of) the dQ tile
     mbar_init(dq_empty(1), kDrainThreads);
     mbar_init(acc_free, kSoftmaxThreads);
-    mbar_init(fin_done, C::TWO ? 2 : 1);  // two-pass: both MMA warps finish
+    mbar_init(fin_done, 2);  // both MMA warps have finished
     mbar_init(sdp_free, kSoftmaxThreads);
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(qdo_full(s), 1);
@@ -332,8 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producers (two-pass)
     // dV pass: lane 0 loads K, the Q ring and the LSE / D ring, lane 1 the dO ring.  Between
     // the passes each lane loads half of V into the dV pass's second stage.  dK pass: lane 0
-    // alone fills the half-tile ring (Q_i, then Q_{i-1} again, then dO_i) and the LSE / D
-    // ring, in the order the MMAs consume them.  Every ring has one loader at a time and its waits run
+    // alone fills the half-tile ring (Q_i, Q_{i-1} again, dO_i) and the LSE / D ring.  Every ring has one loader at a time and its waits run
     // in phase order.
     const int u_last0 = ((nper + 1) >> 1) - 1;  // last dV-pass use of stage 0
     const int u_last1 = (nper >> 1) - 1;        // ... and of stage 1
@@ -352,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto ring_load = [&](const CUtensorMap *tm, int hf, int q0, int h) -> bool {
         const int r = n % kRing, u = n / kRing;
         const bool ok = u == 0 ? (r < 2 ? mbar_wait(qdo_empty(0), u_last0 & 1, p.status)
-                                        : mbar_wait(do_empty(0), u_last0 & 1, p.status))
+                                        : mbar_wait(do0_free, 0, p.status))
                                : mbar_wait(ring_empty(r), (u - 1) & 1, p.status);
         if (!ok) return false;
         mbar_arrive_expect_tx(ring_full(r), kHalf);
@@ -417,6 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = C::KCH / 2; c < C::KCH; ++c)
           tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
+        // the first dO stage, once its last dV-pass use is released, goes to the ring
+        if (mbar_wait(do_empty(0), u_last0 & 1, p.status)) mbar_arrive(do0_free);
       }
     }
   } else if (warp == 0) {
@@ -461,11 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuers
     // Each issuing warp runs its loop with warp-uniform values and one elected lane issues
     // each MMA and commit; descriptors are built once per operand and advanced by constant
-    // offsets.  In the two-pass form warp 1 issues the front MMAs (S^T, dP^T) and warp 14 the
-    // back ones (dV, dK, dQ), so neither waits behind the other's queue; the fused form uses
-    // warp 1 alone.
+    // offsets.  Warp 1 issues the front MMAs (S^T, dP^T; in the dK pass also dK, so that it is
+    // the only reader of the ring) and warp 14 the back ones (dV, dQ; in the fused form dV,
+    // dK, dQ), so neither waits behind the other's queue.
     const bool back_warp = warp == 14;
-    if (C::TWO || !back_warp) {
+    {
       constexpr uint32_t idST = idesc_bf16(kBK, BQ, false, false);  // S^T, dP^T
       constexpr uint32_t idKV = idesc_bf16(kBK, D, false, true);    // dV, dK
       constexpr uint32_t idKh = idesc_bf16(kBK, D / 2, false, true);  // one half of dK (two-pass)
@@ -519,8 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int dq_steps = 0;
       if constexpr (C::TWO) {
         const int nB = nsteps - nper;  // dK-pass steps
-        // Ring positions of dK-pass step i's tiles, in the order the loader fills the ring:
-        // Q_0 dO_0 | Q_1 Qb_0 dO_1 | Q_2 Qb_1 dO_2 | ... | Qb_{nB-1}  (Qb: Q again, for dK).
+        // Ring positions of dK-pass step i's tiles, in the order the loader fills the ring and
+        // the front warp reads it: Q_0 dO_0 | Q_1 Qb_0 dO_1 | Q_2 Qb_1 dO_2 | ... | Qb_{nB-1}
+        // (Qb: Q again, for dK).  A slot is refilled four positions later: Q_i where Qb_{i-2}
+        // was (free after dK_{i-2}), Qb_{i-1} where dO_{i-1} was (after dP^T_{i-1}), dO_i where
+        // Q_i was (after S^T_i).
         auto pos_q = [&](int i) { return i == 0 ? 0 : 6 * i - 2; };
         auto pos_do = [&](int i) { return i == 0 ? 2 : 6 * i + 2; };
         auto pos_qb = [&](int i) { return i + 1 < nB ? 6 * (i + 1) : 6 * nB - 2; };
@@ -536,11 +546,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                      (jj > 0 || kk > 0) ? 1u : 0u);
           mma_commit_w(do_empty(s));
           mma_commit_w(mma_done);
+          mma_commit_w(mma_done);  // both arrivals of the step: no dK in the dV pass
           return true;
         };
-        // dK (Q of the step again, from two ring slots, each released after its 128-column
-        // half of dK) and dQ of a dK-pass step.
-        auto back_dkdq = [&](int jj) -> bool {
+        // dK of a dK-pass step (front warp): Q of the step again, from two ring slots, each
+        // released after its 128-column half of dK.
+        auto mma_dk = [&](int jj) -> bool {
           if (jj == nper) {  // dV has been stored: the accumulator is free for dK
             if (!mbar_wait_warp(acc_free, 0, p.status)) return false;
             tc_fence_after();
@@ -558,6 +569,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                        desc_at(q_mn, kk * 2048), idKh, (jj > nper || kk > 0) ? 1u : 0u);
             mma_commit_w(ring_empty(r));
           }
+          mma_commit_w(mma_done);
+          return true;
+        };
+        // dQ of a dK-pass step (back warp).
+        auto back_dq = [&]() -> bool {
           if (!mma_dq(dq_steps)) return false;
           mma_commit_w(dq_full);
           ++dq_steps;
@@ -588,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!back_warp) {
           // Front: S^T of every step (dV pass: from its Q stage, which is free again right
           // after), dP^T of every dK-pass step, each as soon as the softmax has copied out
-          // the previous one.
+          // the previous one, and dK of the previous dK-pass step.  The front warp is the
+          // only reader of the ring, so every ring slot is waited on in fill order.
           for (int j = 0; ok && j < nsteps; ++j) {
             if (j >= 1 && !mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
             if (j < nper) {
@@ -602,18 +619,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int i = j - nper;
               if (!front_ring(dK_k, C::TM_S, pos_q(i))) break;
               mma_commit_w(s_full);
+              if (i >= 1) {  // dK of the previous step once its dS is in shared memory
+                if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+                tc_fence_after();
+                if (!mma_dk(j - 1)) break;
+              }
               if (i == 0 && !mbar_wait_warp(v_full, 0, p.status)) break;
               if (i >= 1 && !mbar_wait_warp(dp_free, (i - 1) & 1, p.status)) break;
               if (!front_ring(dV_k, C::TM_DP, pos_do(i))) break;
               mma_commit_w(dp_full);
             }
           }
+          if (ok && nsteps > 0 && mbar_wait_warp(p_ready, (nsteps - 1) & 1, p.status)) {
+            tc_fence_after();
+            mma_dk(nsteps - 1);
+          }
         } else {
-          // Back: dV (dV pass) or dK and dQ (dK pass) of step j - 1 once its P or dS is in.
+          // Back: dV (dV pass) or dQ (dK pass) of step j - 1 once its P or dS is in.
           for (int j = 1; ok && j <= nsteps; ++j) {
             if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
             tc_fence_after();
-            if (!(j - 1 < nper ? back_dv(j - 1) : back_dkdq(j - 1))) break;
+            if (!(j - 1 < nper ? back_dv(j - 1) : back_dq())) break;
           }
         }
       } else {
@@ -647,32 +673,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit_w(s_full);
           return true;
         };
-        // With two or more stages, S^T / dP^T of step j go ahead of dV / dK / dQ of step
-        // j - 1, so the softmax of step j overlaps them: S^T / dP^T of step j may start as
-        // soon as the softmax has copied step j - 1's out of TMEM (sdp_free); dV / dK / dQ of
-        // step j - 1 need its P and dS (p_ready).  A single stage can only be refilled after
-        // the previous step's MMAs release it, so there the order is back-to-front.
-        for (int j = 0; ok && j <= nsteps; ++j) {
-          if (NS == 1) {
+        // Front: S^T / dP^T of step j as soon as the softmax has copied step j - 1's out of
+        // TMEM (sdp_free) and its stage is loaded.  Back: dV / dK / dQ of step j - 1 once its
+        // P and dS are in place (p_ready); they release the stage.
+        if (!back_warp) {
+          for (int j = 0; ok && j < nsteps; ++j) {
             if (j >= 1) {
-              if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+              if (!mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
               tc_fence_after();
-              if (!issue_back(j - 1)) break;
             }
-            if (j < nsteps && !issue_front(j)) break;
-          } else {
-            if (j < nsteps) {
-              if (j >= 1) {
-                if (!mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
-                tc_fence_after();
-              }
-              if (!issue_front(j)) break;
-            }
-            if (j >= 1) {
-              if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
-              tc_fence_after();
-              if (!issue_back(j - 1)) break;
-            }
+            if (!issue_front(j)) break;
+          }
+        } else {
+          for (int j = 1; ok && j <= nsteps; ++j) {
+            if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+            tc_fence_after();
+            if (!issue_back(j - 1)) break;
           }
         }
       }
@@ -967,10 +983,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (t == 0) bulk_wait_all();
   }
 
+  __syncwarp();  // every warp reconverges (producer and drain lanes finish at different times)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

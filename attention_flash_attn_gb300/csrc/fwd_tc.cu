@@ -83,6 +83,7 @@ __device__ __forceinline__ int upper_bound_i(const int *a, int n, int x) {
 }
 
 // Pair barrier of the two softmax warps that share TMEM lane quarter `wq` (ids 2..5).
+// Both warps of the pair arrive converged, so the aligned form applies.
 __device__ __forceinline__ void pair_bar(int wq) { asm volatile("bar.sync %0, 64;" ::"r"(2 + wq) : "memory"); }
 
 // Raw scores -> capped, masked base-2 logits in place; returns their maximum.
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         red[4 + wq] = mhi;
       }
     }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
+    asm volatile("barrier.sync 1, 256;" ::: "memory");
     const int cta_lo = max(max(red[0], red[1]), max(red[2], red[3]));
     const int cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
@@ -436,10 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (row_ok && half == 0) p.LSE[((size_t)b * p.Hq + h) * p.Sq + i] = lse;
   }
 
+  __syncwarp();  // every warp reconverges (producer lanes leave their loops at different times)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::TM_COLS);
   }

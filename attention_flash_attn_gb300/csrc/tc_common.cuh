@@ -56,6 +56,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The first wait to give up also leaves where it was: words 1..6 of the status area hold a
+// marker, the barrier's shared-memory offset and parity, and the CTA and thread indices.
+__device__ __forceinline__ void record_timeout(unsigned *status, uint32_t bar, uint32_t parity) {
+  if (!status) return;
+  if (atomicCAS(status + 1, 0u, 1u) == 0u) {
+    status[2] = bar;
+    status[3] = parity;
+    status[4] = blockIdx.x | (blockIdx.y << 16);
+    status[5] = blockIdx.z;
+    status[6] = threadIdx.x;
+    __threadfence();
+  }
+  atomicOr(status, kStatusWaitTimeout);
+}
+
 __device__ __forceinline__ unsigned status_peek(const unsigned *status) {
   unsigned v = 0;
   if (status) asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(status));
@@ -66,15 +81,29 @@ __device__ __forceinline__ unsigned status_peek(const unsigned *status) {
 // early if another CTA has already recorded a timeout (so one fault cannot turn into every
 // CTA timing out in turn).  Returns false, with kStatusWaitTimeout recorded, if it gave up.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+// Waits that give up inside the CTA that recorded the first timeout also leave, per warp,
+// the barrier and parity they were waiting on (words 8 + 2 w, 9 + 2 w; w < 16).
+__device__ __forceinline__ void record_abort(unsigned *status, uint32_t bar, uint32_t parity) {
+  if (!status) return;
+  const unsigned w = threadIdx.x >> 5;
+  if (w < 16 && status[1] == 1u && status[4] == (blockIdx.x | (blockIdx.y << 16)) && status[5] == blockIdx.z) {
+    status[8 + 2 * w] = bar;
+    status[9 + 2 * w] = parity | 0x100u;
+  }
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u) {
-      if (status_peek(status) & kStatusWaitTimeout) return false;
+      if (status_peek(status) & kStatusWaitTimeout) {
+        record_abort(status, bar, parity);
+        return false;
+      }
       if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        set_status(status, kStatusWaitTimeout);
+        record_timeout(status, bar, parity);
         return false;
       }
     }
@@ -121,9 +150,12 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // Generic-proxy shared-memory writes become visible to the async proxy (TMA, tcgen05).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Named barrier over N threads.  The non-aligned form: threads of one warp may arrive at
+// different times (one lane finishing a wait the others do not take part in), which the
+// aligned bar.sync does not allow.
 template <int ID, int N>
 __device__ __forceinline__ void named_bar() {
-  asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
