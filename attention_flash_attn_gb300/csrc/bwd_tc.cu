@@ -23,8 +23,8 @@
 // (the next Q lands where this step's dO was), so S^T of the next step is computed while the
 // softmax warps still work on this one, and those warps form P from S^T before dP^T is in.
 //
-// Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 2..9 softmax / dS, 10..13 dQ drain,
-// 14 second MMA issuer (the MMAs that consume P and dS while warp 1 issues S^T / dP^T).
+// Warps: 0..7 softmax / dS, 8 TMA producer, 9 MMA issuer + TMEM owner, 10 second MMA issuer
+// (the MMAs that consume P and dS while warp 9 issues S^T / dP^T), 12..15 dQ drain.
 // Every mbarrier is waited on phase by phase by each of its waiters: a parity wait cannot
 // tell a phase from the one two later, so no waiter may skip one or fall two behind.
 // Every wait is bounded (tc_common.cuh); named barriers are only used where every
@@ -39,7 +39,13 @@ namespace {
 using namespace tc;
 
 constexpr int kBK = 128;  // keys per CTA
-constexpr int kThreads = 480;
+constexpr int kThreads = 512;
+// Warpgroups: 0-1 softmax / dS (warps 0..7), 2 producers and MMA issuers (8 TMA, 9 front MMA
+// and TMEM owner, 10 back MMA, 11 idle), 3 dQ drain (12..15).  Registers are moved from the
+// producers and the drain to the softmax warpgroups (setmaxnreg): the element-wise loops need
+// many values in flight to keep the MUFU busy.  128 threads x (184 + 184 + 64 + 72) stays
+// within the 512 x 128 registers the CTA is launched with.
+constexpr int kRegSoftmax = 184, kRegProducer = 64, kRegDrain = 72;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kDrainThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -334,370 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto do_addr = [&](int s) -> uint32_t { return slot_addr(s) + C::QT_BYTES; };
   auto ld_addr = [&](int s) { return reinterpret_cast<const float *>(smem + C::OFF_LD + s * 2 * BQ * 4); };
 
-  if (warp == 0 && C::TWO) {
-    // ------------------------------------------------------------ TMA producers (two-pass)
-    // dV pass: lane 0 loads K, the Q ring and the LSE / D ring, lane 1 the dO ring.  Between
-    // the passes each lane loads half of V into the dV pass's second stage.  dK pass: lane 0
-    // alone fills the half-tile ring (Q_i, Q_{i-1} again, dO_i) and the LSE / D ring.  Every ring has one loader at a time and its waits run
-    // in phase order.
-    const int u_last0 = ((nper + 1) >> 1) - 1;  // last dV-pass use of stage 0
-    const int u_last1 = (nper >> 1) - 1;        // ... and of stage 1
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(kv_full, C::KV_BYTES);
-#pragma unroll
-      for (int c = 0; c < C::KCH; ++c) tma_load_4d(sbase + C::OFF_K + c * (kBK * 128), &tmK, kv_full, c * 64, k0, g, b);
-      int n = 0;  // dK-pass ring position
-      // One half tile (columns 128*hf .. 128*hf + 127 of Q or dO rows q0 .. q0 + BQ - 1) into
-      // the next ring slot.  The first four slots are stage 0 of the dV pass: wait for its last
-      // Q (slots 0, 1) or dO (slots 2, 3) to be released.
-      auto ring_load = [&](const CUtensorMap *tm, int hf, int q0, int h) -> bool {
-        const int r = n % kRing, u = n / kRing;
-        const bool ok = u == 0 ? (r < 2 ? mbar_wait(qdo_empty(0), u_last0 & 1, p.status)
-                                        : mbar_wait(do0_free, 0, p.status))
-                               : mbar_wait(ring_empty(r), (u - 1) & 1, p.status);
-        if (!ok) return false;
-        mbar_arrive_expect_tx(ring_full(r), kHalf);
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          tma_load_4d(ring_addr(n) + c * (BQ * 128), tm, ring_full(r), (2 * hf + c) * 64, q0, h, b);
-        ++n;
-        return true;
-      };
-      for (int j = 0; j <= nsteps; ++j) {
-        if (j < nsteps) {  // LSE / D of step j first: the softmax needs them with S^T_j
-          const int x = j & 1, h = step_h(j), q0 = step_q0(j);
-          if (j >= 2 && !mbar_wait(ld_empty(x), ((j >> 1) - 1) & 1, p.status)) break;
-          mbar_arrive_expect_tx(ld_full(x), 2 * BQ * 4);
-          const size_t row = ((size_t)b * p.Hq + h) * p.sq_pad + q0;
-          const uint32_t lda = sbase + C::OFF_LD + x * 2 * BQ * 4;
-          bulk_g2s(lda, p.lse2p + row, BQ * 4, ld_full(x));
-          bulk_g2s(lda + BQ * 4, p.Dvec + row, BQ * 4, ld_full(x));
-        }
-        if (j < nper) {
-          const int s = slot_of(j), u = use_of(j);
-          if (u >= 1 && !mbar_wait(qdo_empty(s), (u - 1) & 1, p.status)) break;
-          mbar_arrive_expect_tx(qdo_full(s), C::QT_BYTES);
-#pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(slot_addr(s) + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, step_q0(j), step_h(j), b);
-        } else if (j < nsteps) {
-          if (j == nper) {  // V[:, :128] into the dV pass's second Q stage
-            if (u_last1 >= 0 && !mbar_wait(qdo_empty(1), u_last1 & 1, p.status)) break;
-            mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
-#pragma unroll
-            for (int c = 0; c < C::KCH / 2; ++c)
-              tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
-          }
-          // Q_i for S^T, Q_{i-1} again for dK of the previous step, dO_i for dP^T
-          const int h = step_h(j), q0 = step_q0(j);
-          if (!ring_load(&tmQ, 0, q0, h) || !ring_load(&tmQ, 1, q0, h)) break;
-          if (j > nper && (!ring_load(&tmQ, 0, step_q0(j - 1), step_h(j - 1)) ||
-                           !ring_load(&tmQ, 1, step_q0(j - 1), step_h(j - 1))))
-            break;
-          if (!ring_load(&tmdO, 0, q0, h) || !ring_load(&tmdO, 1, q0, h)) break;
-        }
-        if (j == nsteps && j > nper) {  // Q of the last step again, for its dK
-          const int h = step_h(j - 1), q0 = step_q0(j - 1);
-          if (!ring_load(&tmQ, 0, q0, h) || !ring_load(&tmQ, 1, q0, h)) break;
-        }
-      }
-    } else if (lane == 1) {
-      tma_prefetch_desc(&tmdO);
-      bool ok = true;
-      for (int j = 0; j < nper; ++j) {
-        const int s = slot_of(j), u = use_of(j);
-        if (u >= 1 && !mbar_wait(do_empty(s), (u - 1) & 1, p.status)) { ok = false; break; }
-        mbar_arrive_expect_tx(do_full(s), C::QT_BYTES);
-#pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(do_addr(s) + c * (BQ * 128), &tmdO, do_full(s), c * 64, step_q0(j), step_h(j), b);
-      }
-      // V[:, 128:] into the dV pass's second dO stage
-      if (ok && nper > 0 && (u_last1 < 0 || mbar_wait(do_empty(1), u_last1 & 1, p.status))) {
-        mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
-#pragma unroll
-        for (int c = C::KCH / 2; c < C::KCH; ++c)
-          tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
-        // the first dO stage, once its last dV-pass use is released, goes to the ring
-        if (mbar_wait(do_empty(0), u_last0 & 1, p.status)) mbar_arrive(do0_free);
-      }
-    }
-  } else if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(kv_full, (C::TWO ? 1 : 2) * C::KV_BYTES);
-#pragma unroll
-      for (int c = 0; c < C::KCH; ++c) {
-        tma_load_4d(sbase + C::OFF_K + c * (kBK * 128), &tmK, kv_full, c * 64, k0, g, b);
-        if (!C::TWO) tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, kv_full, c * 64, k0, g, b);
-      }
-      for (int j = 0; j < nsteps; ++j) {
-        if (C::TWO && j == nper) {
-          // The dK pass needs V: wait until the dV pass has released V's slot, then load it.
-          if (nper >= 2 && !mbar_wait(qdo_empty(1), ((nper >> 1) - 1) & 1, p.status)) break;
-          mbar_arrive_expect_tx(v_full, C::KV_BYTES);
-#pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
-        }
-        const int s = slot_of(j), u = use_of(j);
-        if (u >= 1 && !mbar_wait(qdo_empty(s), (u - 1) & 1, p.status)) break;
-        const int h = step_h(j), q0 = step_q0(j);
-        const uint32_t sa = slot_addr(s);
-        mbar_arrive_expect_tx(qdo_full(s), 2 * C::QT_BYTES + 2 * BQ * 4);
-#pragma unroll
-        for (int c = 0; c < C::KCH; ++c) {
-          tma_load_4d(sa + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, q0, h, b);
-          tma_load_4d(sa + C::QT_BYTES + c * (BQ * 128), &tmdO, qdo_full(s), c * 64, q0, h, b);
-        }
-        const size_t row = ((size_t)b * p.Hq + h) * p.sq_pad + q0;
-        const uint32_t lda = sbase + C::OFF_LD + s * 2 * BQ * 4;
-        bulk_g2s(lda, p.lse2p + row, BQ * 4, qdo_full(s));
-        bulk_g2s(lda + BQ * 4, p.Dvec + row, BQ * 4, qdo_full(s));
-      }
-    }
-  } else if (warp == 1 || warp == 14) {
-    // ------------------------------------------------------------ MMA issuers
-    // Each issuing warp runs its loop with warp-uniform values and one elected lane issues
-    // each MMA and commit; descriptors are built once per operand and advanced by constant
-    // offsets.  Warp 1 issues the front MMAs (S^T, dP^T; in the dK pass also dK, so that it is
-    // the only reader of the ring) and warp 14 the back ones (dV, dQ; in the fused form dV,
-    // dK, dQ), so neither waits behind the other's queue.
-    const bool back_warp = warp == 14;
-    {
-      constexpr uint32_t idST = idesc_bf16(kBK, BQ, false, false);  // S^T, dP^T
-      constexpr uint32_t idKV = idesc_bf16(kBK, D, false, true);    // dV, dK
-      constexpr uint32_t idKh = idesc_bf16(kBK, D / 2, false, true);  // one half of dK (two-pass)
-      constexpr uint32_t idDQ = C::DQT ? idesc_bf16(128, BQ, true, true) : idesc_bf16(BQ, D, true, true);
-      const uint64_t dK_k = sw128_desc(sbase + C::OFF_K, 16, 1024);          // K, K-major (A of S^T)
-      const uint64_t dV_k = sw128_desc(sbase + C::OFF_V, 16, 1024);          // V, K-major (A of dP^T)
-      const uint64_t dK_mn = sw128_desc(sbase + C::OFF_K, kBK * 128, 1024);  // K, d contiguous
-      const uint64_t dS_k = sw128_desc(sbase + C::OFF_DS, 16, 1024);         // dS^T, K-major (A of dK)
-      const uint64_t dS_mn = sw128_desc(sbase + C::OFF_DS, kBK * 128, 1024); // dS^T, q contiguous
-      // S^T (A = K) or dP^T (A = V) over D from a Q / dO tile whose 64-column chunks lie
-      // chunk_stride bytes apart.
-      // Loops over 64-column chunks stay rolled (the descriptors advance by one add per
-      // chunk) and the four 16-deep MMAs of a chunk are unrolled: compact code that still
-      // issues faster than the tensor pipe retires.
-      auto mma_front = [&](uint64_t a_k, uint32_t b_addr, uint32_t d_col) {
-        uint64_t b_k = sw128_desc(b_addr, 16, 1024);
-#pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4)
-            mma_ss_w(tmem + d_col, desc_at(a_k, k4 * 32), desc_at(b_k, k4 * 32), idST, (c | k4) != 0);
-          a_k = desc_at(a_k, kBK * 128);
-          b_k = desc_at(b_k, BQ * 128);
-        }
-      };
-      // dQ of a step from dS^T in shared memory, each half of D once the drain has copied the
-      // previous step's out of TMEM.
-      auto mma_dq = [&](int dq_steps) -> bool {
-        if constexpr (C::DQT) {
-          // dQ^T[d, q] = K^T dS^T : A = K (d contiguous), B = dS^T (q contiguous)
-#pragma unroll 1
-          for (int m = 0; m < D / 128; ++m) {
-            if (dq_steps >= 1 && !mbar_wait_warp(dq_empty(m), (dq_steps - 1) & 1, p.status)) return false;
-            tc_fence_after();
-            const uint64_t a_m = desc_at(dK_mn, (2 * m) * (kBK * 128));
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_ss_w(tmem + C::TM_DQ + m * BQ, desc_at(a_m, kk * 2048), desc_at(dS_mn, kk * 2048), idDQ, kk > 0);
-          }
-        } else {
-          // dQ[q, d] = dS K : A = dS (q contiguous), B = K (d contiguous)
-          if (dq_steps >= 1 && !mbar_wait_warp(dq_empty(0), (dq_steps - 1) & 1, p.status)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_ss_w(tmem + C::TM_DQ, desc_at(dS_mn, kk * 2048), desc_at(dK_mn, kk * 2048), idDQ, kk > 0);
-        }
-        return true;
-      };
-      bool ok = mbar_wait_warp(kv_full, 0, p.status);
-      int dq_steps = 0;
-      if constexpr (C::TWO) {
-        const int nB = nsteps - nper;  // dK-pass steps
-        // Ring positions of dK-pass step i's tiles, in the order the loader fills the ring and
-        // the front warp reads it: Q_0 dO_0 | Q_1 Qb_0 dO_1 | Q_2 Qb_1 dO_2 | ... | Qb_{nB-1}
-        // (Qb: Q again, for dK).  A slot is refilled four positions later: Q_i where Qb_{i-2}
-        // was (free after dK_{i-2}), Qb_{i-1} where dO_{i-1} was (after dP^T_{i-1}), dO_i where
-        // Q_i was (after S^T_i).
-        auto pos_q = [&](int i) { return i == 0 ? 0 : 6 * i - 2; };
-        auto pos_do = [&](int i) { return i == 0 ? 2 : 6 * i + 2; };
-        auto pos_qb = [&](int i) { return i + 1 < nB ? 6 * (i + 1) : 6 * nB - 2; };
-        // dV of a dV-pass step: P^T from TMEM, dO of its slot; releases that dO slot.
-        auto back_dv = [&](int jj) -> bool {
-          const int s = slot_of(jj);
-          if (!mbar_wait_warp(do_full(s), use_of(jj) & 1, p.status)) return false;
-          tc_fence_after();
-          const uint64_t o_mn = sw128_desc(do_addr(s), BQ * 128, 1024);
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts_w(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, desc_at(o_mn, kk * 2048), idKV,
-                     (jj > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_w(do_empty(s));
-          mma_commit_w(mma_done);
-          mma_commit_w(mma_done);  // both arrivals of the step: no dK in the dV pass
-          return true;
-        };
-        // dK of a dK-pass step (front warp): Q of the step again, from two ring slots, each
-        // released after its 128-column half of dK.
-        auto mma_dk = [&](int jj) -> bool {
-          if (jj == nper) {  // dV has been stored: the accumulator is free for dK
-            if (!mbar_wait_warp(acc_free, 0, p.status)) return false;
-            tc_fence_after();
-          }
-          const int n0 = pos_qb(jj - nper);
-#pragma unroll 1
-          for (int hf = 0; hf < 2; ++hf) {
-            const int n = n0 + hf, r = n % kRing;
-            if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
-            tc_fence_after();
-            const uint64_t q_mn = sw128_desc(ring_addr(n), BQ * 128, 1024);
-#pragma unroll
-            for (int kk = 0; kk < BQ / 16; ++kk)
-              mma_ss_w(tmem + C::TM_DK + hf * (D / 2), desc_at(dS_k, (kk >> 2) * (kBK * 128) + (kk & 3) * 32),
-                       desc_at(q_mn, kk * 2048), idKh, (jj > nper || kk > 0) ? 1u : 0u);
-            mma_commit_w(ring_empty(r));
-          }
-          mma_commit_w(mma_done);
-          return true;
-        };
-        // dQ of a dK-pass step (back warp).
-        auto back_dq = [&]() -> bool {
-          if (!mma_dq(dq_steps)) return false;
-          mma_commit_w(dq_full);
-          ++dq_steps;
-          mma_commit_w(mma_done);
-          return true;
-        };
-        // S^T (A = K) or dP^T (A = V) of a dK-pass step from the two ring slots at n0, n0 + 1
-        // (the two column halves of Q or dO), each slot released once read.
-        auto front_ring = [&](uint64_t a_k, uint32_t d_col, int n0) -> bool {
-#pragma unroll 1
-          for (int hf = 0; hf < 2; ++hf) {
-            const int n = n0 + hf, r = n % kRing;
-            if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
-            tc_fence_after();
-            uint64_t b_k = sw128_desc(ring_addr(n), 16, 1024);
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {  // the two 64-column chunks of this half
-#pragma unroll
-              for (int k4 = 0; k4 < 4; ++k4)
-                mma_ss_w(tmem + d_col, desc_at(a_k, k4 * 32), desc_at(b_k, k4 * 32), idST, (hf | c | k4) != 0);
-              a_k = desc_at(a_k, kBK * 128);
-              b_k = desc_at(b_k, BQ * 128);
-            }
-            mma_commit_w(ring_empty(r));
-          }
-          return true;
-        };
-        if (!back_warp) {
-          // Front: S^T of every step (dV pass: from its Q stage, which is free again right
-          // after), dP^T of every dK-pass step, each as soon as the softmax has copied out
-          // the previous one, and dK of the previous dK-pass step.  The front warp is the
-          // only reader of the ring, so every ring slot is waited on in fill order.
-          for (int j = 0; ok && j < nsteps; ++j) {
-            if (j >= 1 && !mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
-            if (j < nper) {
-              const int s = slot_of(j);
-              if (!mbar_wait_warp(qdo_full(s), use_of(j) & 1, p.status)) break;
-              tc_fence_after();
-              mma_front(dK_k, slot_addr(s), C::TM_S);
-              mma_commit_w(s_full);
-              mma_commit_w(qdo_empty(s));
-            } else {
-              const int i = j - nper;
-              if (!front_ring(dK_k, C::TM_S, pos_q(i))) break;
-              mma_commit_w(s_full);
-              if (i >= 1) {  // dK of the previous step once its dS is in shared memory
-                if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
-                tc_fence_after();
-                if (!mma_dk(j - 1)) break;
-              }
-              if (i == 0 && !mbar_wait_warp(v_full, 0, p.status)) break;
-              if (i >= 1 && !mbar_wait_warp(dp_free, (i - 1) & 1, p.status)) break;
-              if (!front_ring(dV_k, C::TM_DP, pos_do(i))) break;
-              mma_commit_w(dp_full);
-            }
-          }
-          if (ok && nsteps > 0 && mbar_wait_warp(p_ready, (nsteps - 1) & 1, p.status)) {
-            tc_fence_after();
-            mma_dk(nsteps - 1);
-          }
-        } else {
-          // Back: dV (dV pass) or dQ (dK pass) of step j - 1 once its P or dS is in.
-          for (int j = 1; ok && j <= nsteps; ++j) {
-            if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
-            tc_fence_after();
-            if (!(j - 1 < nper ? back_dv(j - 1) : back_dq())) break;
-          }
-        }
-      } else {
-        // dV / dK / dQ of step jj (P^T in TMEM and dS^T in shared memory are ready).
-        auto issue_back = [&](int jj) -> bool {
-          const int s = slot_of(jj);
-          const uint64_t q_mn = sw128_desc(slot_addr(s), BQ * 128, 1024);
-          const uint64_t o_mn = desc_at(q_mn, C::QT_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO
-            mma_ts_w(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, desc_at(o_mn, kk * 2048), idKV,
-                     (jj > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
-            mma_ss_w(tmem + C::TM_DK, desc_at(dS_k, (kk >> 2) * (kBK * 128) + (kk & 3) * 32),
-                     desc_at(q_mn, kk * 2048), idKV, (jj > 0 || kk > 0) ? 1u : 0u);
-          if (!mma_dq(dq_steps)) return false;
-          mma_commit_w(dq_full);
-          ++dq_steps;
-          mma_commit_w(mma_done);
-          mma_commit_w(qdo_empty(s));
-          return true;
-        };
-        // S^T and dP^T of step j.
-        auto issue_front = [&](int j) -> bool {
-          const int s = slot_of(j);
-          if (!mbar_wait_warp(qdo_full(s), use_of(j) & 1, p.status)) return false;
-          tc_fence_after();
-          mma_front(dK_k, slot_addr(s), C::TM_S);
-          mma_front(dV_k, slot_addr(s) + C::QT_BYTES, C::TM_DP);
-          mma_commit_w(s_full);
-          return true;
-        };
-        // Front: S^T / dP^T of step j as soon as the softmax has copied step j - 1's out of
-        // TMEM (sdp_free) and its stage is loaded.  Back: dV / dK / dQ of step j - 1 once its
-        // P and dS are in place (p_ready); they release the stage.
-        if (!back_warp) {
-          for (int j = 0; ok && j < nsteps; ++j) {
-            if (j >= 1) {
-              if (!mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
-              tc_fence_after();
-            }
-            if (!issue_front(j)) break;
-          }
-        } else {
-          for (int j = 1; ok && j <= nsteps; ++j) {
-            if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
-            tc_fence_after();
-            if (!issue_back(j - 1)) break;
-          }
-        }
-      }
-      mma_commit_w(fin_done);  // every MMA issued by this CTA has completed
-    }
-  } else if (warp < 10) {
+  // Each warpgroup sets its register budget as the first statement of its own branch, so
+  // the code of a role is only reachable under that role's budget.
+  if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
     // ------------------------------------------------------------ softmax / dS warps
     const int wq = warp & 3;
-    const int half = (warp - 2) >> 2;  // which half of the BQ query columns
+    const int half = warp >> 2;  // which half of the BQ query columns
     const int r = wq * 32 + lane;      // key row within the tile == TMEM lane
     const int k = k0 + r;
     const bool key_ok = k < p.Sk;
@@ -902,14 +551,378 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              (((size_t)b * p.Sk + k) * p.Hkv + g) * D);
       for (int v = half * (D / 16); v < (half + 1) * (D / 16); ++v) dst[v] = make_uint4(0, 0, 0, 0);
     }
+  } else if (warp < 12) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegProducer));
+    if (warp == 8 && C::TWO) {
+      // ------------------------------------------------------------ TMA producers (two-pass)
+      // dV pass: lane 0 loads K, the Q ring and the LSE / D ring, lane 1 the dO ring.  Between
+      // the passes each lane loads half of V into the dV pass's second stage.  dK pass: lane 0
+      // alone fills the half-tile ring (Q_i, Q_{i-1} again, dO_i) and the LSE / D ring.  Every ring has one loader at a time and its waits run
+      // in phase order.
+      const int u_last0 = ((nper + 1) >> 1) - 1;  // last dV-pass use of stage 0
+      const int u_last1 = (nper >> 1) - 1;        // ... and of stage 1
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdO);
+        mbar_arrive_expect_tx(kv_full, C::KV_BYTES);
+  #pragma unroll
+        for (int c = 0; c < C::KCH; ++c) tma_load_4d(sbase + C::OFF_K + c * (kBK * 128), &tmK, kv_full, c * 64, k0, g, b);
+        int n = 0;  // dK-pass ring position
+        // One half tile (columns 128*hf .. 128*hf + 127 of Q or dO rows q0 .. q0 + BQ - 1) into
+        // the next ring slot.  The first four slots are stage 0 of the dV pass: wait for its last
+        // Q (slots 0, 1) or dO (slots 2, 3) to be released.
+        auto ring_load = [&](const CUtensorMap *tm, int hf, int q0, int h) -> bool {
+          const int r = n % kRing, u = n / kRing;
+          const bool ok = u == 0 ? (r < 2 ? mbar_wait(qdo_empty(0), u_last0 & 1, p.status)
+                                          : mbar_wait(do0_free, 0, p.status))
+                                 : mbar_wait(ring_empty(r), (u - 1) & 1, p.status);
+          if (!ok) return false;
+          mbar_arrive_expect_tx(ring_full(r), kHalf);
+  #pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(ring_addr(n) + c * (BQ * 128), tm, ring_full(r), (2 * hf + c) * 64, q0, h, b);
+          ++n;
+          return true;
+        };
+        for (int j = 0; j <= nsteps; ++j) {
+          if (j < nsteps) {  // LSE / D of step j first: the softmax needs them with S^T_j
+            const int x = j & 1, h = step_h(j), q0 = step_q0(j);
+            if (j >= 2 && !mbar_wait(ld_empty(x), ((j >> 1) - 1) & 1, p.status)) break;
+            mbar_arrive_expect_tx(ld_full(x), 2 * BQ * 4);
+            const size_t row = ((size_t)b * p.Hq + h) * p.sq_pad + q0;
+            const uint32_t lda = sbase + C::OFF_LD + x * 2 * BQ * 4;
+            bulk_g2s(lda, p.lse2p + row, BQ * 4, ld_full(x));
+            bulk_g2s(lda + BQ * 4, p.Dvec + row, BQ * 4, ld_full(x));
+          }
+          if (j < nper) {
+            const int s = slot_of(j), u = use_of(j);
+            if (u >= 1 && !mbar_wait(qdo_empty(s), (u - 1) & 1, p.status)) break;
+            mbar_arrive_expect_tx(qdo_full(s), C::QT_BYTES);
+  #pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_4d(slot_addr(s) + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, step_q0(j), step_h(j), b);
+          } else if (j < nsteps) {
+            if (j == nper) {  // V[:, :128] into the dV pass's second Q stage
+              if (u_last1 >= 0 && !mbar_wait(qdo_empty(1), u_last1 & 1, p.status)) break;
+              mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
+  #pragma unroll
+              for (int c = 0; c < C::KCH / 2; ++c)
+                tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
+            }
+            // Q_i for S^T, Q_{i-1} again for dK of the previous step, dO_i for dP^T
+            const int h = step_h(j), q0 = step_q0(j);
+            if (!ring_load(&tmQ, 0, q0, h) || !ring_load(&tmQ, 1, q0, h)) break;
+            if (j > nper && (!ring_load(&tmQ, 0, step_q0(j - 1), step_h(j - 1)) ||
+                             !ring_load(&tmQ, 1, step_q0(j - 1), step_h(j - 1))))
+              break;
+            if (!ring_load(&tmdO, 0, q0, h) || !ring_load(&tmdO, 1, q0, h)) break;
+          }
+          if (j == nsteps && j > nper) {  // Q of the last step again, for its dK
+            const int h = step_h(j - 1), q0 = step_q0(j - 1);
+            if (!ring_load(&tmQ, 0, q0, h) || !ring_load(&tmQ, 1, q0, h)) break;
+          }
+        }
+      } else if (lane == 1) {
+        tma_prefetch_desc(&tmdO);
+        bool ok = true;
+        for (int j = 0; j < nper; ++j) {
+          const int s = slot_of(j), u = use_of(j);
+          if (u >= 1 && !mbar_wait(do_empty(s), (u - 1) & 1, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(do_full(s), C::QT_BYTES);
+  #pragma unroll
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(do_addr(s) + c * (BQ * 128), &tmdO, do_full(s), c * 64, step_q0(j), step_h(j), b);
+        }
+        // V[:, 128:] into the dV pass's second dO stage
+        if (ok && nper > 0 && (u_last1 < 0 || mbar_wait(do_empty(1), u_last1 & 1, p.status))) {
+          mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
+  #pragma unroll
+          for (int c = C::KCH / 2; c < C::KCH; ++c)
+            tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
+          // the first dO stage, once its last dV-pass use is released, goes to the ring
+          if (mbar_wait(do_empty(0), u_last0 & 1, p.status)) mbar_arrive(do0_free);
+        }
+      }
+    } else if (warp == 8) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmdO);
+        mbar_arrive_expect_tx(kv_full, (C::TWO ? 1 : 2) * C::KV_BYTES);
+  #pragma unroll
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_4d(sbase + C::OFF_K + c * (kBK * 128), &tmK, kv_full, c * 64, k0, g, b);
+          if (!C::TWO) tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, kv_full, c * 64, k0, g, b);
+        }
+        for (int j = 0; j < nsteps; ++j) {
+          if (C::TWO && j == nper) {
+            // The dK pass needs V: wait until the dV pass has released V's slot, then load it.
+            if (nper >= 2 && !mbar_wait(qdo_empty(1), ((nper >> 1) - 1) & 1, p.status)) break;
+            mbar_arrive_expect_tx(v_full, C::KV_BYTES);
+  #pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
+          }
+          const int s = slot_of(j), u = use_of(j);
+          if (u >= 1 && !mbar_wait(qdo_empty(s), (u - 1) & 1, p.status)) break;
+          const int h = step_h(j), q0 = step_q0(j);
+          const uint32_t sa = slot_addr(s);
+          mbar_arrive_expect_tx(qdo_full(s), 2 * C::QT_BYTES + 2 * BQ * 4);
+  #pragma unroll
+          for (int c = 0; c < C::KCH; ++c) {
+            tma_load_4d(sa + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, q0, h, b);
+            tma_load_4d(sa + C::QT_BYTES + c * (BQ * 128), &tmdO, qdo_full(s), c * 64, q0, h, b);
+          }
+          const size_t row = ((size_t)b * p.Hq + h) * p.sq_pad + q0;
+          const uint32_t lda = sbase + C::OFF_LD + s * 2 * BQ * 4;
+          bulk_g2s(lda, p.lse2p + row, BQ * 4, qdo_full(s));
+          bulk_g2s(lda + BQ * 4, p.Dvec + row, BQ * 4, qdo_full(s));
+        }
+      }
+    } else if (warp == 9 || warp == 10) {
+      // ------------------------------------------------------------ MMA issuers
+      // Each issuing warp runs its loop with warp-uniform values and one elected lane issues
+      // each MMA and commit; descriptors are built once per operand and advanced by constant
+      // offsets.  Warp 9 issues the front MMAs (S^T, dP^T; in the dK pass also dK, so that it is
+      // the only reader of the ring) and warp 10 the back ones (dV, dQ; in the fused form dV,
+      // dK, dQ), so neither waits behind the other's queue.
+      const bool back_warp = warp == 10;
+      {
+        constexpr uint32_t idST = idesc_bf16(kBK, BQ, false, false);  // S^T, dP^T
+        constexpr uint32_t idKV = idesc_bf16(kBK, D, false, true);    // dV, dK
+        constexpr uint32_t idKh = idesc_bf16(kBK, D / 2, false, true);  // one half of dK (two-pass)
+        constexpr uint32_t idDQ = C::DQT ? idesc_bf16(128, BQ, true, true) : idesc_bf16(BQ, D, true, true);
+        const uint64_t dK_k = sw128_desc(sbase + C::OFF_K, 16, 1024);          // K, K-major (A of S^T)
+        const uint64_t dV_k = sw128_desc(sbase + C::OFF_V, 16, 1024);          // V, K-major (A of dP^T)
+        const uint64_t dK_mn = sw128_desc(sbase + C::OFF_K, kBK * 128, 1024);  // K, d contiguous
+        const uint64_t dS_k = sw128_desc(sbase + C::OFF_DS, 16, 1024);         // dS^T, K-major (A of dK)
+        const uint64_t dS_mn = sw128_desc(sbase + C::OFF_DS, kBK * 128, 1024); // dS^T, q contiguous
+        // S^T (A = K) or dP^T (A = V) over D from a Q / dO tile whose 64-column chunks lie
+        // chunk_stride bytes apart.
+        // Loops over 64-column chunks stay rolled (the descriptors advance by one add per
+        // chunk) and the four 16-deep MMAs of a chunk are unrolled: compact code that still
+        // issues faster than the tensor pipe retires.
+        auto mma_front = [&](uint64_t a_k, uint32_t b_addr, uint32_t d_col) {
+          uint64_t b_k = sw128_desc(b_addr, 16, 1024);
+  #pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
+  #pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+              mma_ss_w(tmem + d_col, desc_at(a_k, k4 * 32), desc_at(b_k, k4 * 32), idST, (c | k4) != 0);
+            a_k = desc_at(a_k, kBK * 128);
+            b_k = desc_at(b_k, BQ * 128);
+          }
+        };
+        // dQ of a step from dS^T in shared memory, each half of D once the drain has copied the
+        // previous step's out of TMEM.
+        auto mma_dq = [&](int dq_steps) -> bool {
+          if constexpr (C::DQT) {
+            // dQ^T[d, q] = K^T dS^T : A = K (d contiguous), B = dS^T (q contiguous)
+  #pragma unroll 1
+            for (int m = 0; m < D / 128; ++m) {
+              if (dq_steps >= 1 && !mbar_wait_warp(dq_empty(m), (dq_steps - 1) & 1, p.status)) return false;
+              tc_fence_after();
+              const uint64_t a_m = desc_at(dK_mn, (2 * m) * (kBK * 128));
+  #pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk)
+                mma_ss_w(tmem + C::TM_DQ + m * BQ, desc_at(a_m, kk * 2048), desc_at(dS_mn, kk * 2048), idDQ, kk > 0);
+            }
+          } else {
+            // dQ[q, d] = dS K : A = dS (q contiguous), B = K (d contiguous)
+            if (dq_steps >= 1 && !mbar_wait_warp(dq_empty(0), (dq_steps - 1) & 1, p.status)) return false;
+            tc_fence_after();
+  #pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_ss_w(tmem + C::TM_DQ, desc_at(dS_mn, kk * 2048), desc_at(dK_mn, kk * 2048), idDQ, kk > 0);
+          }
+          return true;
+        };
+        bool ok = mbar_wait_warp(kv_full, 0, p.status);
+        int dq_steps = 0;
+        if constexpr (C::TWO) {
+          const int nB = nsteps - nper;  // dK-pass steps
+          // Ring positions of dK-pass step i's tiles, in the order the loader fills the ring and
+          // the front warp reads it: Q_0 dO_0 | Q_1 Qb_0 dO_1 | Q_2 Qb_1 dO_2 | ... | Qb_{nB-1}
+          // (Qb: Q again, for dK).  A slot is refilled four positions later: Q_i where Qb_{i-2}
+          // was (free after dK_{i-2}), Qb_{i-1} where dO_{i-1} was (after dP^T_{i-1}), dO_i where
+          // Q_i was (after S^T_i).
+          auto pos_q = [&](int i) { return i == 0 ? 0 : 6 * i - 2; };
+          auto pos_do = [&](int i) { return i == 0 ? 2 : 6 * i + 2; };
+          auto pos_qb = [&](int i) { return i + 1 < nB ? 6 * (i + 1) : 6 * nB - 2; };
+          // dV of a dV-pass step: P^T from TMEM, dO of its slot; releases that dO slot.
+          auto back_dv = [&](int jj) -> bool {
+            const int s = slot_of(jj);
+            if (!mbar_wait_warp(do_full(s), use_of(jj) & 1, p.status)) return false;
+            tc_fence_after();
+            const uint64_t o_mn = sw128_desc(do_addr(s), BQ * 128, 1024);
+  #pragma unroll
+            for (int kk = 0; kk < BQ / 16; ++kk)
+              mma_ts_w(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, desc_at(o_mn, kk * 2048), idKV,
+                       (jj > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_w(do_empty(s));
+            mma_commit_w(mma_done);
+            mma_commit_w(mma_done);  // both arrivals of the step: no dK in the dV pass
+            return true;
+          };
+          // dK of a dK-pass step (front warp): Q of the step again, from two ring slots, each
+          // released after its 128-column half of dK.
+          auto mma_dk = [&](int jj) -> bool {
+            if (jj == nper) {  // dV has been stored: the accumulator is free for dK
+              if (!mbar_wait_warp(acc_free, 0, p.status)) return false;
+              tc_fence_after();
+            }
+            const int n0 = pos_qb(jj - nper);
+  #pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+              const int n = n0 + hf, r = n % kRing;
+              if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
+              tc_fence_after();
+              const uint64_t q_mn = sw128_desc(ring_addr(n), BQ * 128, 1024);
+  #pragma unroll
+              for (int kk = 0; kk < BQ / 16; ++kk)
+                mma_ss_w(tmem + C::TM_DK + hf * (D / 2), desc_at(dS_k, (kk >> 2) * (kBK * 128) + (kk & 3) * 32),
+                         desc_at(q_mn, kk * 2048), idKh, (jj > nper || kk > 0) ? 1u : 0u);
+              mma_commit_w(ring_empty(r));
+            }
+            mma_commit_w(mma_done);
+            return true;
+          };
+          // dQ of a dK-pass step (back warp).
+          auto back_dq = [&]() -> bool {
+            if (!mma_dq(dq_steps)) return false;
+            mma_commit_w(dq_full);
+            ++dq_steps;
+            mma_commit_w(mma_done);
+            return true;
+          };
+          // S^T (A = K) or dP^T (A = V) of a dK-pass step from the two ring slots at n0, n0 + 1
+          // (the two column halves of Q or dO), each slot released once read.
+          auto front_ring = [&](uint64_t a_k, uint32_t d_col, int n0) -> bool {
+  #pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+              const int n = n0 + hf, r = n % kRing;
+              if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
+              tc_fence_after();
+              uint64_t b_k = sw128_desc(ring_addr(n), 16, 1024);
+  #pragma unroll 1
+              for (int c = 0; c < 2; ++c) {  // the two 64-column chunks of this half
+  #pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                  mma_ss_w(tmem + d_col, desc_at(a_k, k4 * 32), desc_at(b_k, k4 * 32), idST, (hf | c | k4) != 0);
+                a_k = desc_at(a_k, kBK * 128);
+                b_k = desc_at(b_k, BQ * 128);
+              }
+              mma_commit_w(ring_empty(r));
+            }
+            return true;
+          };
+          if (!back_warp) {
+            // Front: S^T of every step (dV pass: from its Q stage, which is free again right
+            // after), dP^T of every dK-pass step, each as soon as the softmax has copied out
+            // the previous one, and dK of the previous dK-pass step.  The front warp is the
+            // only reader of the ring, so every ring slot is waited on in fill order.
+            for (int j = 0; ok && j < nsteps; ++j) {
+              if (j >= 1 && !mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
+              if (j < nper) {
+                const int s = slot_of(j);
+                if (!mbar_wait_warp(qdo_full(s), use_of(j) & 1, p.status)) break;
+                tc_fence_after();
+                mma_front(dK_k, slot_addr(s), C::TM_S);
+                mma_commit_w(s_full);
+                mma_commit_w(qdo_empty(s));
+              } else {
+                const int i = j - nper;
+                if (!front_ring(dK_k, C::TM_S, pos_q(i))) break;
+                mma_commit_w(s_full);
+                if (i >= 1) {  // dK of the previous step once its dS is in shared memory
+                  if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+                  tc_fence_after();
+                  if (!mma_dk(j - 1)) break;
+                }
+                if (i == 0 && !mbar_wait_warp(v_full, 0, p.status)) break;
+                if (i >= 1 && !mbar_wait_warp(dp_free, (i - 1) & 1, p.status)) break;
+                if (!front_ring(dV_k, C::TM_DP, pos_do(i))) break;
+                mma_commit_w(dp_full);
+              }
+            }
+            if (ok && nsteps > 0 && mbar_wait_warp(p_ready, (nsteps - 1) & 1, p.status)) {
+              tc_fence_after();
+              mma_dk(nsteps - 1);
+            }
+          } else {
+            // Back: dV (dV pass) or dQ (dK pass) of step j - 1 once its P or dS is in.
+            for (int j = 1; ok && j <= nsteps; ++j) {
+              if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+              tc_fence_after();
+              if (!(j - 1 < nper ? back_dv(j - 1) : back_dq())) break;
+            }
+          }
+        } else {
+          // dV / dK / dQ of step jj (P^T in TMEM and dS^T in shared memory are ready).
+          auto issue_back = [&](int jj) -> bool {
+            const int s = slot_of(jj);
+            const uint64_t q_mn = sw128_desc(slot_addr(s), BQ * 128, 1024);
+            const uint64_t o_mn = desc_at(q_mn, C::QT_BYTES);
+  #pragma unroll
+            for (int kk = 0; kk < BQ / 16; ++kk)  // dV += P^T dO
+              mma_ts_w(tmem + C::TM_DV, tmem + C::TM_P + kk * 8, desc_at(o_mn, kk * 2048), idKV,
+                       (jj > 0 || kk > 0) ? 1u : 0u);
+  #pragma unroll
+            for (int kk = 0; kk < BQ / 16; ++kk)  // dK += dS^T Q
+              mma_ss_w(tmem + C::TM_DK, desc_at(dS_k, (kk >> 2) * (kBK * 128) + (kk & 3) * 32),
+                       desc_at(q_mn, kk * 2048), idKV, (jj > 0 || kk > 0) ? 1u : 0u);
+            if (!mma_dq(dq_steps)) return false;
+            mma_commit_w(dq_full);
+            ++dq_steps;
+            mma_commit_w(mma_done);
+            mma_commit_w(qdo_empty(s));
+            return true;
+          };
+          // S^T and dP^T of step j.
+          auto issue_front = [&](int j) -> bool {
+            const int s = slot_of(j);
+            if (!mbar_wait_warp(qdo_full(s), use_of(j) & 1, p.status)) return false;
+            tc_fence_after();
+            mma_front(dK_k, slot_addr(s), C::TM_S);
+            mma_front(dV_k, slot_addr(s) + C::QT_BYTES, C::TM_DP);
+            mma_commit_w(s_full);
+            return true;
+          };
+          // Front: S^T / dP^T of step j as soon as the softmax has copied step j - 1's out of
+          // TMEM (sdp_free) and its stage is loaded.  Back: dV / dK / dQ of step j - 1 once its
+          // P and dS are in place (p_ready); they release the stage.
+          if (!back_warp) {
+            for (int j = 0; ok && j < nsteps; ++j) {
+              if (j >= 1) {
+                if (!mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
+                tc_fence_after();
+              }
+              if (!issue_front(j)) break;
+            }
+          } else {
+            for (int j = 1; ok && j <= nsteps; ++j) {
+              if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+              tc_fence_after();
+              if (!issue_back(j - 1)) break;
+            }
+          }
+        }
+        mma_commit_w(fin_done);  // every MMA issued by this CTA has completed
+      }
+    }
   } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegDrain));
     // ------------------------------------------------------------ dQ drain warps
     // One thread waits on the mbarriers and the four warps follow it through a named
     // barrier, so their exits stay uniform.
     const int wq = warp & 3;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const int row = wq * 32 + lane;  // TMEM lane: a d index (dQ^T) or a query row (dQ)
-    const int t = threadIdx.x - 320;
+    const int t = threadIdx.x - 384;
     int *flag = misc_i + 13;
     float *stage = reinterpret_cast<float *>(smem + C::OFF_DQS);
     const uint32_t stage_a = sbase + C::OFF_DQS;
@@ -922,54 +935,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!*flag) break;
       tc_fence_after();
       if constexpr (C::DQT) {
-        // dQ^T: lane = d within a 128-wide half of D, column = query.  One half at a time goes
-        // to registers and is released at once (the next step's dQ MMAs for that half may
-        // start), then leaves through [128 d, 32 q] boxes staged in shared memory for bulk
-        // reduce-adds into the fp32 accumulator.
+        // dQ^T: lane = d within a 128-wide half of D, column = query.  32 queries at a time go
+        // to registers (a half of D is released once its last 32 are in: the next step's dQ
+        // MMAs for that half may start), then leave through a [128 d, 32 q] box staged in
+        // shared memory for a bulk reduce-add into the fp32 accumulator.
 #pragma unroll 1
-        for (int m = 0; m < D / 128; ++m) {
-          uint32_t v[BQ];
-#pragma unroll
-          for (int c = 0; c < BQ / 32; ++c)
-            tmem_ld32(lane_addr + C::TM_DQ + m * BQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
+        for (int c = 0; c < C::DQ_COLS / 32; ++c) {
+          const int m = c / (BQ / 32), cq = c % (BQ / 32);
+          uint32_t v[32];
+          tmem_ld32(lane_addr + C::TM_DQ + c * 32, v);
           tmem_wait_ld();
           reg_fence(v);
-          tc_fence_before();
-          mbar_arrive(dq_empty(m));  // this thread is done with this half of the TMEM tile
+          if (cq == BQ / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(dq_empty(m));  // this thread is done with this half of the TMEM tile
+          }
+          if (t == 0) bulk_wait_read_all();  // the previous box has left shared memory
+          named_bar<2, 128>();
 #pragma unroll
-          for (int c = 0; c < BQ / 32; ++c) {
-            if (t == 0) bulk_wait_read_all();  // the previous box has left shared memory
-            named_bar<2, 128>();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) stage[e * 128 + row] = __uint_as_float(v[c * 32 + e]);
-            fence_async_smem();
-            named_bar<2, 128>();
-            if (t == 0) {
-              tma_reduce_add_4d(&tmDQ, stage_a, m * 128, q0 + c * 32, h, b);
-              bulk_commit();
-            }
+          for (int e = 0; e < 32; ++e) stage[e * 128 + row] = __uint_as_float(v[e]);
+          fence_async_smem();
+          named_bar<2, 128>();
+          if (t == 0) {
+            tma_reduce_add_4d(&tmDQ, stage_a, m * 128, q0 + cq * 32, h, b);
+            bulk_commit();
           }
         }
       } else {
-        // dQ: lane = query row, column = d.  Copy the whole tile out of TMEM and release it
-        // at once, then stage [32 d, 128 q] boxes (128-byte swizzled) for bulk reduce-adds.
-        uint32_t v[C::DQ_COLS];
-#pragma unroll
-        for (int c = 0; c < C::DQ_COLS / 32; ++c)
-          tmem_ld32(lane_addr + C::TM_DQ + c * 32, *reinterpret_cast<uint32_t(*)[32]>(v + c * 32));
-        tmem_wait_ld();
-        reg_fence(v);
-        tc_fence_before();
-        mbar_arrive(dq_empty(0));  // this thread is done with the TMEM tile
-#pragma unroll
+        // dQ: lane = query row, column = d.  32 columns of d at a time (the tile is released
+        // once the last of them is in), staged as [32 d, 128 q] boxes (128-byte swizzled) for
+        // bulk reduce-adds.
+#pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_addr + C::TM_DQ + c * 32, v);
+          tmem_wait_ld();
+          reg_fence(v);
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(dq_empty(0));  // this thread is done with the TMEM tile
+          }
           if (t == 0) bulk_wait_read_all();
           named_bar<2, 128>();
           uint8_t *rowp = reinterpret_cast<uint8_t *>(stage) + row * 128;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             *reinterpret_cast<uint4 *>(rowp + ((u ^ (row & 7)) << 4)) =
-                make_uint4(v[c * 32 + 4 * u], v[c * 32 + 4 * u + 1], v[c * 32 + 4 * u + 2], v[c * 32 + 4 * u + 3]);
+                make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
           fence_async_smem();
           named_bar<2, 128>();
           if (t == 0) {
@@ -986,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();  // every warp reconverges (producer and drain lanes finish at different times)
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
