@@ -40,7 +40,7 @@ def _stamp() -> str:
     files = _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")))
     files.append(os.path.join(ROOT, "include", "attn_gb300.h"))
     for f in files:
-        h.update(f.encode())
+        h.update(os.path.relpath(f, ROOT).encode())  # relative: the same sources hash alike anywhere
         with open(f, "rb") as fh:
             h.update(fh.read())
     h.update(" ".join(ARCH + FLAGS).encode())

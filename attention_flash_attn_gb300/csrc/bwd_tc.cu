@@ -19,9 +19,10 @@
 // Head dim 256: dK and dV fill all 512 TMEM columns, so the CTA runs two passes over its
 // query steps -- dV first, then dK and dQ (S^T recomputed).  V is not needed in the dV pass,
 // so its shared-memory slot doubles as a second Q/dO stage there and V is loaded for the
-// second pass.  In the dK pass the two halves of the remaining stage swap roles each step
-// (the next Q lands where this step's dO was), so S^T of the next step is computed while the
-// softmax warps still work on this one, and those warps form P from S^T before dP^T is in.
+// second pass.  In the dK pass the remaining stage is a ring of four half tiles (128 of the
+// 256 columns each), filled in the order Q_i, Q_{i-1} (again, for dK of the previous step),
+// dO_i and read by one MMA warp alone, so S^T of the next step is computed while the softmax
+// warps still work on this one, and those warps form P from S^T before dP^T is in.
 //
 // Warps: 0..7 softmax / dS, 8 TMA producer, 9 MMA issuer + TMEM owner, 10 second MMA issuer
 // (the MMAs that consume P and dS while warp 9 issues S^T / dP^T), 12..15 dQ drain.

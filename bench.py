@@ -117,6 +117,20 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm
 
+def captured_traffic(workload):
+    """DRAM bytes per launch of the backward main kernel from a committed ncu capture, only
+    while the library's sources are the ones that capture was taken of."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        from attention_flash_attn_gb300 import build as _b
+        entry = json.load(open(p)).get(workload)
+        if entry and entry.get("source_stamp") == _b._stamp():
+            return entry["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -257,7 +271,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "tensor", "kernel": "backward main kernel",
                      "achieved": round(bwd_tf, 3), "peak": burst, "unit": "TFLOP/s",
                      "frac": round(bwd_tf / burst, 4), "peak_kind": f"{kind} bf16 burst",
-                     "traffic": None},
+                     "frac_of_sustained": round(bwd_tf / sustained, 4),
+                     "traffic": captured_traffic(w.name)},
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

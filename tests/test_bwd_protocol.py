@@ -1,0 +1,263 @@
+"""Model check of the head-dim-256 backward's mbarrier protocol (two-pass form of
+attention_flash_attn_gb300/csrc/bwd_tc.cu), run on the CPU.
+
+Each agent of the kernel -- TMA lanes 0 and 1, the front MMA warp (S^T, dK, dP^T), the
+back MMA warp (dV, dQ), the softmax warps, the dQ drain -- is a generator that yields the
+waits and arrivals it performs, in program order.  MMAs complete at once (a commit is an
+arrival).  Waits use the hardware's parity rule: a wait for phase k of a barrier returns
+when the barrier's completed-phase count has the other parity, so it is only sound if the
+count is k or k + 1 when the waiter looks.  Random schedules must always finish, and no
+waiter may ever see a count outside {k, k + 1}.
+
+The negative control replays the earlier layout, in which the half-tile ring was read by
+two warps; the model must flag it (that layout timed out intermittently on the GPU).
+"""
+import random
+from collections import defaultdict
+
+import pytest
+
+
+def simulate(nper, design="single_reader", rng=None, order="q_qb_do"):
+    """Returns (finished, hazards).  nper: query steps per pass (dV pass = dK pass).
+    order: the ring's fill order within a dK-pass step (the kernel uses Q_i, Q_{i-1}, dO_i)."""
+    rng = rng or random.Random(0)
+    nsteps, nB = 2 * nper, nper
+    need = defaultdict(lambda: 1)
+    need.update({"v_full": 2, "fin_done": 2})
+    if design == "single_reader":
+        need["mma_done"] = 2
+    count, done, hazards = defaultdict(int), defaultdict(int), []
+
+    def arrive(b):
+        count[b] += 1
+        if count[b] == need[b]:
+            count[b] = 0
+            done[b] += 1
+
+    slot_of = lambda j: j & 1
+    use_of = lambda j: j >> 1
+    u_last0, u_last1 = ((nper + 1) >> 1) - 1, (nper >> 1) - 1
+    pos_q = lambda i: 0 if i == 0 else 6 * i - 2
+    if order == "q_qb_do":  # as in bwd_tc.cu
+        pos_do = lambda i: 2 if i == 0 else 6 * i + 2
+        pos_qb = lambda i: 6 * (i + 1) if i + 1 < nB else 6 * nB - 2
+    else:  # "q_do_qb"
+        pos_do = lambda i: 2 if i == 0 else 6 * i
+        pos_qb = lambda i: 6 * i + 8 if i + 1 < nB else 6 * nB - 2
+
+    def loader0():
+        yield ("arrive", "kv_full")
+        n = 0
+
+        def ring_load():
+            nonlocal n
+            r, u = n % 4, n // 4
+            if u == 0:
+                if r < 2:
+                    yield ("wait", "qdo_empty0", u_last0)
+                elif design == "single_reader":
+                    yield ("wait", "do0_free", 0)
+                else:
+                    yield ("wait", "do_empty0", u_last0)
+            else:
+                yield ("wait", f"ring_empty{r}", u - 1)
+            yield ("arrive", f"ring_full{r}")
+            n += 1
+
+        for j in range(nsteps + 1):
+            if j < nsteps:
+                if j >= 2:
+                    yield ("wait", f"ld_empty{j & 1}", (j >> 1) - 1)
+                yield ("arrive", f"ld_full{j & 1}")
+            if j < nper:
+                s, u = slot_of(j), use_of(j)
+                if u >= 1:
+                    yield ("wait", f"qdo_empty{s}", u - 1)
+                yield ("arrive", f"qdo_full{s}")
+            elif j < nsteps:
+                if j == nper:
+                    if u_last1 >= 0:
+                        yield ("wait", "qdo_empty1", u_last1)
+                    yield ("arrive", "v_full")
+                for _ in range(2):  # Q_i
+                    yield from ring_load()
+                if order == "q_qb_do" and j > nper:  # Q_{i-1} again
+                    for _ in range(2):
+                        yield from ring_load()
+                for _ in range(2):  # dO_i
+                    yield from ring_load()
+                if order == "q_do_qb" and j > nper:
+                    for _ in range(2):
+                        yield from ring_load()
+            if j == nsteps and j > nper:
+                for _ in range(2):
+                    yield from ring_load()
+
+    def loader1():
+        for j in range(nper):
+            s, u = slot_of(j), use_of(j)
+            if u >= 1:
+                yield ("wait", f"do_empty{s}", u - 1)
+            yield ("arrive", f"do_full{s}")
+        if nper > 0:
+            if u_last1 >= 0:
+                yield ("wait", "do_empty1", u_last1)
+            yield ("arrive", "v_full")
+            if design == "single_reader":
+                yield ("wait", "do_empty0", u_last0)
+                yield ("arrive", "do0_free")
+
+    def ring(n0):
+        for hf in range(2):
+            n = n0 + hf
+            yield ("wait", f"ring_full{n % 4}", n // 4)
+            yield ("arrive", f"ring_empty{n % 4}")
+
+    def dk(i):  # dK of dK-pass step i (the front warp in the single-reader design)
+        yield ("wait", "p_ready", nper + i)
+        if i == 0:
+            yield ("wait", "acc_free", 0)
+        yield from ring(pos_qb(i))
+        yield ("arrive", "mma_done")
+
+    def front():
+        yield ("wait", "kv_full", 0)
+        for j in range(nsteps):
+            if j >= 1:
+                yield ("wait", "sdp_free", j - 1)
+            if j < nper:
+                s = slot_of(j)
+                yield ("wait", f"qdo_full{s}", use_of(j))
+                yield ("arrive", "s_full")
+                yield ("arrive", f"qdo_empty{s}")
+                continue
+            i = j - nper
+            yield from ring(pos_q(i))
+            yield ("arrive", "s_full")
+            if design == "single_reader" and i >= 1:
+                yield from dk(i - 1)
+            if i == 0:
+                yield ("wait", "v_full", 0)
+            else:
+                yield ("wait", "dp_free", i - 1)
+            yield from ring(pos_do(i))
+            yield ("arrive", "dp_full")
+        if design == "single_reader" and nsteps > 0:
+            yield from dk(nB - 1)
+        yield ("arrive", "fin_done")
+
+    def back():
+        yield ("wait", "kv_full", 0)
+        dq = 0
+        for j in range(1, nsteps + 1):
+            yield ("wait", "p_ready", j - 1)
+            jj = j - 1
+            if jj < nper:
+                s = slot_of(jj)
+                yield ("wait", f"do_full{s}", use_of(jj))
+                yield ("arrive", f"do_empty{s}")
+                yield ("arrive", "mma_done")
+                if design == "single_reader":
+                    yield ("arrive", "mma_done")
+                continue
+            if design == "shared_ring":  # the earlier layout: dK read the ring from this warp
+                if jj == nper:
+                    yield ("wait", "acc_free", 0)
+                yield from ring(pos_qb(jj - nper))
+            for m in range(2):
+                if dq >= 1:
+                    yield ("wait", f"dq_empty{m}", dq - 1)
+            yield ("arrive", "dq_full")
+            dq += 1
+            yield ("arrive", "mma_done")
+        yield ("arrive", "fin_done")
+
+    def softmax():
+        for j in range(nsteps):
+            yield ("wait", "s_full", j)
+            yield ("wait", f"ld_full{j & 1}", j >> 1)
+            yield ("arrive", "sdp_free")
+            if j >= nper:
+                yield ("wait", "dp_full", j - nper)
+                yield ("arrive", "dp_free")
+            yield ("arrive", f"ld_empty{j & 1}")
+            if j >= 1:
+                yield ("wait", "mma_done", j - 1)
+            yield ("arrive", "p_ready")
+            if j == nper - 1:
+                yield ("wait", "mma_done", j)
+                yield ("arrive", "acc_free")
+        if nsteps > 0:
+            yield ("wait", "fin_done", 0)
+
+    def drain():
+        for d in range(nB):
+            yield ("wait", "dq_full", d)
+            yield ("arrive", "dq_empty0")
+            yield ("arrive", "dq_empty1")
+
+    agents = {"loader0": loader0(), "loader1": loader1(), "front": front(), "back": back(),
+              "softmax": softmax(), "drain": drain()}
+    pending = dict.fromkeys(agents)
+    finished = set()
+    while len(finished) < len(agents):
+        progress = False
+        turn = list(agents)
+        rng.shuffle(turn)
+        for name in turn:
+            if name in finished:
+                continue
+            for _ in range(rng.randint(1, 8)):
+                op = pending[name]
+                if op is None:
+                    try:
+                        op = pending[name] = next(agents[name])
+                    except StopIteration:
+                        finished.add(name)
+                        progress = True
+                        break
+                if op[0] == "arrive":
+                    arrive(op[1])
+                    pending[name] = None
+                    progress = True
+                    continue
+                _, bar, phase = op
+                if done[bar] not in (phase, phase + 1):
+                    hazards.append((name, bar, phase, done[bar]))
+                if (done[bar] & 1) != (phase & 1):  # the hardware's parity test
+                    pending[name] = None
+                    progress = True
+                else:
+                    break
+        if not progress:
+            return False, hazards
+    return True, hazards
+
+
+STEP_COUNTS = [1, 2, 3, 4, 5, 6, 8, 13, 33, 66, 80]
+
+
+def test_single_reader_protocol_never_deadlocks_or_aliases():
+    rng = random.Random(1234)
+    for trial in range(1500):
+        nper = STEP_COUNTS[trial % len(STEP_COUNTS)]
+        finished, hazards = simulate(nper, "single_reader", rng)
+        assert finished and not hazards, (nper, hazards[:3])
+
+
+def test_model_flags_the_shared_ring_layout():
+    """Negative control: with the ring (filled Q_i, dO_i, Q_{i-1}) read by two warps, the
+    dK warp can wait for a slot's next fill while the previous one is still in flight."""
+    rng = random.Random(99)
+    flagged = 0
+    for trial in range(400):
+        finished, hazards = simulate(66, "shared_ring", rng, order="q_do_qb")
+        flagged += (not finished) or bool(hazards)
+    assert flagged > 0
+
+
+@pytest.mark.parametrize("nper", [1, 2, 7, 66])
+def test_greedy_schedule_finishes(nper):
+    finished, hazards = simulate(nper, "single_reader", random.Random(nper))
+    assert finished and not hazards
