@@ -273,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto ld_empty = [&](int x) { return bar0 + 8u * (16 + 2 * C::NSLOT + x); };
   // Two-pass form, dK pass: stage 0 (64 KiB) becomes a ring of four 16 KiB slots, each one
   // half (128 of the 256 columns) of a Q or dO tile.  In ring order, step i brings Q_i (for
-  // S^T), Q_{i-1} again (for dK_{i-1}, which runs once the softmax of step i - 1 is done) and
-  // dO_i (for dP^T): no tile stays resident from its S^T to its dK.
+  // S^T), dO_i (for dP^T) and Q_{i-1} again (for dK_{i-1}, which runs once the softmax of step
+  // i - 1 is done): no tile stays resident from its S^T to its dK.
   auto ring_full = [&](int r) { return bar0 + 8u * (18 + 2 * C::NSLOT + r); };
   auto ring_empty = [&](int r) { return bar0 + 8u * (22 + 2 * C::NSLOT + r); };
   const uint32_t dp_full = bar0 + 8u * (26 + 2 * C::NSLOT);  // dP^T of a dK-pass step is in TMEM
@@ -558,8 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ TMA producers (two-pass)
       // dV pass: lane 0 loads K, the Q ring and the LSE / D ring, lane 1 the dO ring.  Between
       // the passes each lane loads half of V into the dV pass's second stage.  dK pass: lane 0
-      // alone fills the half-tile ring (Q_i, Q_{i-1} again, dO_i) and the LSE / D ring.  Every ring has one loader at a time and its waits run
-      // in phase order.
+      // alone fills the half-tile ring (Q_i, dO_i, Q_{i-1} again) and the LSE / D ring.  Every
+      // ring has one loader at a time and its waits run in phase order.
       const int u_last0 = ((nper + 1) >> 1) - 1;  // last dV-pass use of stage 0
       const int u_last1 = (nper >> 1) - 1;        // ... and of stage 1
       if (lane == 0) {
@@ -612,13 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int c = 0; c < C::KCH / 2; ++c)
                 tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
             }
-            // Q_i for S^T, Q_{i-1} again for dK of the previous step, dO_i for dP^T
+            // Q_i for S^T, dO_i for dP^T, Q_{i-1} again for dK of the previous step
             const int h = step_h(j), q0 = step_q0(j);
             if (!ring_load(&tmQ, 0, q0, h) || !ring_load(&tmQ, 1, q0, h)) break;
+            if (!ring_load(&tmdO, 0, q0, h) || !ring_load(&tmdO, 1, q0, h)) break;
             if (j > nper && (!ring_load(&tmQ, 0, step_q0(j - 1), step_h(j - 1)) ||
                              !ring_load(&tmQ, 1, step_q0(j - 1), step_h(j - 1))))
               break;
-            if (!ring_load(&tmdO, 0, q0, h) || !ring_load(&tmdO, 1, q0, h)) break;
           }
           if (j == nsteps && j > nper) {  // Q of the last step again, for its dK
             const int h = step_h(j - 1), q0 = step_q0(j - 1);
@@ -747,13 +747,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (C::TWO) {
           const int nB = nsteps - nper;  // dK-pass steps
           // Ring positions of dK-pass step i's tiles, in the order the loader fills the ring and
-          // the front warp reads it: Q_0 dO_0 | Q_1 Qb_0 dO_1 | Q_2 Qb_1 dO_2 | ... | Qb_{nB-1}
-          // (Qb: Q again, for dK).  A slot is refilled four positions later: Q_i where Qb_{i-2}
-          // was (free after dK_{i-2}), Qb_{i-1} where dO_{i-1} was (after dP^T_{i-1}), dO_i where
+          // the front warp reads it: Q_0 dO_0 | Q_1 dO_1 Qb_0 | Q_2 dO_2 Qb_1 | ... | Qb_{nB-1}
+          // (Qb: Q again, for dK).  A slot is refilled four positions later: Q_i where dO_{i-1}
+          // was (free after dP^T_{i-1}), dO_i where Qb_{i-2} was (after dK_{i-2}), Qb_{i-1} where
           // Q_i was (after S^T_i).
           auto pos_q = [&](int i) { return i == 0 ? 0 : 6 * i - 2; };
-          auto pos_do = [&](int i) { return i == 0 ? 2 : 6 * i + 2; };
-          auto pos_qb = [&](int i) { return i + 1 < nB ? 6 * (i + 1) : 6 * nB - 2; };
+          auto pos_do = [&](int i) { return i == 0 ? 2 : 6 * i; };
+          auto pos_qb = [&](int i) { return i + 1 < nB ? 6 * i + 8 : 6 * nB - 2; };
           // dV of a dV-pass step: P^T from TMEM, dO of its slot; releases that dO slot.
           auto back_dv = [&](int jj) -> bool {
             const int s = slot_of(jj);
@@ -823,9 +823,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           };
           if (!back_warp) {
             // Front: S^T of every step (dV pass: from its Q stage, which is free again right
-            // after), dP^T of every dK-pass step, each as soon as the softmax has copied out
-            // the previous one, and dK of the previous dK-pass step.  The front warp is the
-            // only reader of the ring, so every ring slot is waited on in fill order.
+            // after) and dP^T of every dK-pass step, each as soon as the softmax has copied out
+            // the previous one, then dK of the previous dK-pass step: the softmax finds S^T and
+            // dP^T of a step in TMEM while dK / dQ of the step before run.  The front warp is
+            // the only reader of the ring, so every ring slot is waited on in fill order.
             for (int j = 0; ok && j < nsteps; ++j) {
               if (j >= 1 && !mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
               if (j < nper) {
@@ -839,15 +840,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int i = j - nper;
                 if (!front_ring(dK_k, C::TM_S, pos_q(i))) break;
                 mma_commit_w(s_full);
+                if (i == 0 && !mbar_wait_warp(v_full, 0, p.status)) break;
+                if (i >= 1 && !mbar_wait_warp(dp_free, (i - 1) & 1, p.status)) break;
+                tc_fence_after();
+                if (!front_ring(dV_k, C::TM_DP, pos_do(i))) break;
+                mma_commit_w(dp_full);
                 if (i >= 1) {  // dK of the previous step once its dS is in shared memory
                   if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
                   tc_fence_after();
                   if (!mma_dk(j - 1)) break;
                 }
-                if (i == 0 && !mbar_wait_warp(v_full, 0, p.status)) break;
-                if (i >= 1 && !mbar_wait_warp(dp_free, (i - 1) & 1, p.status)) break;
-                if (!front_ring(dV_k, C::TM_DP, pos_do(i))) break;
-                mma_commit_w(dp_full);
               }
             }
             if (ok && nsteps > 0 && mbar_wait_warp(p_ready, (nsteps - 1) & 1, p.status)) {

@@ -18,9 +18,11 @@ from collections import defaultdict
 import pytest
 
 
-def simulate(nper, design="single_reader", rng=None, order="q_qb_do"):
+def simulate(nper, design="single_reader", rng=None, order="q_do_qb"):
     """Returns (finished, hazards).  nper: query steps per pass (dV pass = dK pass).
-    order: the ring's fill order within a dK-pass step (the kernel uses Q_i, Q_{i-1}, dO_i)."""
+    order: the ring's fill order within a dK-pass step.  The kernel fills Q_i, dO_i, Q_{i-1}
+    and its front warp issues S^T_i, dP^T_i, dK_{i-1} ("q_do_qb"); "q_qb_do" is the earlier
+    single-reader layout (S^T_i, dK_{i-1}, dP^T_i)."""
     rng = rng or random.Random(0)
     nsteps, nB = 2 * nper, nper
     need = defaultdict(lambda: 1)
@@ -39,10 +41,10 @@ def simulate(nper, design="single_reader", rng=None, order="q_qb_do"):
     use_of = lambda j: j >> 1
     u_last0, u_last1 = ((nper + 1) >> 1) - 1, (nper >> 1) - 1
     pos_q = lambda i: 0 if i == 0 else 6 * i - 2
-    if order == "q_qb_do":  # as in bwd_tc.cu
+    if order == "q_qb_do":
         pos_do = lambda i: 2 if i == 0 else 6 * i + 2
         pos_qb = lambda i: 6 * (i + 1) if i + 1 < nB else 6 * nB - 2
-    else:  # "q_do_qb"
+    else:  # "q_do_qb", as in bwd_tc.cu
         pos_do = lambda i: 2 if i == 0 else 6 * i
         pos_qb = lambda i: 6 * i + 8 if i + 1 < nB else 6 * nB - 2
 
@@ -135,7 +137,7 @@ def simulate(nper, design="single_reader", rng=None, order="q_qb_do"):
             i = j - nper
             yield from ring(pos_q(i))
             yield ("arrive", "s_full")
-            if design == "single_reader" and i >= 1:
+            if design == "single_reader" and order == "q_qb_do" and i >= 1:
                 yield from dk(i - 1)
             if i == 0:
                 yield ("wait", "v_full", 0)
@@ -143,6 +145,8 @@ def simulate(nper, design="single_reader", rng=None, order="q_qb_do"):
                 yield ("wait", "dp_free", i - 1)
             yield from ring(pos_do(i))
             yield ("arrive", "dp_full")
+            if design == "single_reader" and order == "q_do_qb" and i >= 1:
+                yield from dk(i - 1)
         if design == "single_reader" and nsteps > 0:
             yield from dk(nB - 1)
         yield ("arrive", "fin_done")
@@ -238,11 +242,12 @@ def simulate(nper, design="single_reader", rng=None, order="q_qb_do"):
 STEP_COUNTS = [1, 2, 3, 4, 5, 6, 8, 13, 33, 66, 80]
 
 
-def test_single_reader_protocol_never_deadlocks_or_aliases():
+@pytest.mark.parametrize("order", ["q_do_qb", "q_qb_do"])
+def test_single_reader_protocol_never_deadlocks_or_aliases(order):
     rng = random.Random(1234)
-    for trial in range(1500):
+    for trial in range(1000):
         nper = STEP_COUNTS[trial % len(STEP_COUNTS)]
-        finished, hazards = simulate(nper, "single_reader", rng)
+        finished, hazards = simulate(nper, "single_reader", rng, order=order)
         assert finished and not hazards, (nper, hazards[:3])
 
 
