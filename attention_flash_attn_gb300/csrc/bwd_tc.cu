@@ -232,7 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (misc_i[12]) return;
   }
 
-  const int kt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // One-dimensional grid, key tile slowest: the early key tiles, which see the most queries
+  // under causal masks, start before any later tile, so the last wave holds the light ones.
+  const int gb = (int)(blockIdx.x % (unsigned)(p.Hkv * p.B));
+  const int kt = (int)(blockIdx.x / (unsigned)(p.Hkv * p.B)), g = gb % p.Hkv, b = gb / p.Hkv;
   const int k0 = kt * kBK, k1 = min(k0 + kBK, p.Sk) - 1;
   const int off = p.Sk - p.Sq;
 
@@ -1020,8 +1023,9 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   auto kern = p.cap > 0.f ? bwd_tc_kernel<C, true> : bwd_tc_kernel<C, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((p.Sk + kBK - 1) / kBK, p.Hkv, p.B);
-  kern<<<grid, kThreads, C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
+  const long long nblk = (long long)((p.Sk + kBK - 1) / kBK) * p.Hkv * p.B;
+  if (nblk > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<(unsigned)nblk, kThreads, C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
   return counted(cudaGetLastError());
 }
 

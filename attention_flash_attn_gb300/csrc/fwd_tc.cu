@@ -133,9 +133,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (misc_i[12]) return;
   }
 
+  // One-dimensional grid, query tile slowest: every (batch, head) takes its latest (heaviest
+  // under causal) tile before any takes an earlier one, so the last wave holds the light tiles.
   const int nqt = (p.Sq + kBM - 1) / kBM;
-  const int qt = nqt - 1 - (int)blockIdx.x;  // latest (heaviest under causal) tiles first
-  const int h = blockIdx.y, b = blockIdx.z, g = h / p.G;
+  const int bh = (int)(blockIdx.x % (unsigned)(p.Hq * p.B));
+  const int qt = nqt - 1 - (int)(blockIdx.x / (unsigned)(p.Hq * p.B));
+  const int h = bh % p.Hq, b = bh / p.Hq, g = h / p.G;
   const int i0 = qt * kBM, i1 = min(i0 + kBM, p.Sq) - 1;
   const int off = p.Sk - p.Sq;
 
@@ -457,8 +460,9 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   auto kern = p.cap > 0.f ? fwd_tc_kernel<D, BN, NK, NV, true> : fwd_tc_kernel<D, BN, NK, NV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((p.Sq + kBM - 1) / kBM, p.Hq, p.B);
-  kern<<<grid, kThreads, C::SMEM, st>>>(tq, tk, tv, p);
+  const long long nblk = (long long)((p.Sq + kBM - 1) / kBM) * p.Hq * p.B;
+  if (nblk > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<(unsigned)nblk, kThreads, C::SMEM, st>>>(tq, tk, tv, p);
   return counted(cudaGetLastError());
 }
 
