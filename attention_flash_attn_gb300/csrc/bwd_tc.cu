@@ -119,100 +119,126 @@ __device__ __forceinline__ uint4 pack8(const uint32_t *o, int v) {
                     pack_bf16(__uint_as_float(o[8 * v + 6]), __uint_as_float(o[8 * v + 7])));
 }
 
-// One 32-query chunk of a key row: P = exp2(t2 - LSE2) and dS = P (dP - D) f scale, packed
-// to bf16 pairs.  Compile-time variants keep the loop free of branches: CAP (soft-cap on),
-// KIND (0 both, 1 P only, 2 dS only), MASK (0 none, 1 query interval, 2 interval and
-// pairwise segment ids).  Masked entries go through exp2(-inf) = 0.
-template <bool CAP, int KIND, int MASK>
+// Score constants of the element-wise backward, as packed pairs.  With the soft-cap,
+// e = exp(2 u / cap) for u = scale s, r = 1 / (1 + e), so tanh(u / cap) = 1 - 2 r and
+// 1 - tanh^2 = 4 r (1 - r); the capped logit in log2 units is cap log2(e) (1 - 2 r).  An
+// overflowing e gives r = 0 (tanh = 1) and an underflowing one r = 1 (tanh = -1).
+struct BwdScore {
+  uint64_t cin, one, mcap2, cap2, mfs, fs, sc2, scale;
+  __device__ BwdScore(float scale_, float inv_cap, float cap) {
+    cin = f2_splat(2.f * kLog2e * scale_ * inv_cap);
+    one = f2_splat(1.f);
+    mcap2 = f2_splat(-2.f * cap * kLog2e);
+    cap2 = f2_splat(cap * kLog2e);
+    mfs = f2_splat(-4.f * scale_);
+    fs = f2_splat(4.f * scale_);
+    sc2 = f2_splat(scale_ * kLog2e);
+    scale = f2_splat(scale_);
+  }
+};
+
+// One pair of raw scores -> (t2 - LSE2, f): t2 the (capped) logit in log2 units, f the
+// cap's chain-rule factor times the softmax scale.
+template <bool CAP>
+__device__ __forceinline__ void score_pair(uint32_t s0, uint32_t s1, uint64_t lse2, const BwdScore &k, uint64_t &y,
+                                           uint64_t &f) {
+  const uint64_t s2 = f2_pack(__uint_as_float(s0), __uint_as_float(s1));
+  if constexpr (CAP) {
+    float xa, xb, da, db;
+    f2_unpack(f2_mul(s2, k.cin), xa, xb);
+    f2_unpack(f2_add(f2_pack(ex2_approx(xa), ex2_approx(xb)), k.one), da, db);
+    const uint64_t r2 = f2_pack(rcp_approx(da), rcp_approx(db));
+    y = f2_sub(f2_fma(r2, k.mcap2, k.cap2), lse2);
+    f = f2_mul(r2, f2_fma(r2, k.mfs, k.fs));  // 4 scale r (1 - r)
+  } else {
+    y = f2_sub(f2_mul(s2, k.sc2), lse2);
+    f = k.scale;
+  }
+}
+__device__ __forceinline__ uint64_t ex2_pair(uint64_t y) {
+  float a, b;
+  f2_unpack(y, a, b);
+  return f2_pack(ex2_approx(a), ex2_approx(b));
+}
+__device__ __forceinline__ uint32_t bf16_pair(uint64_t v) {
+  float a, b;
+  f2_unpack(v, a, b);
+  return pack_bf16(a, b);
+}
+
+// One 32-query chunk of a key row, every column treated as visible (masked columns are
+// cleared afterwards by the fix-ups below, only on chunks that need it):
+//   KIND 1: P, packed to bf16 pairs;  KIND 0: P and dS = P f (dP - D), both packed.
+template <bool CAP, int KIND>
 __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float *lse2c,
-                                          const float *dvc, uint32_t (&pk)[16], uint32_t (&dk)[16], float sc2,
-                                          float capc, float cap2, float fscale, float scale, int qbase, int lo,
-                                          int hi, int sq, const int *segq, int sid) {
+                                          const float *dvc, uint32_t (&pk)[16], uint32_t (&dk)[16],
+                                          const BwdScore &k) {
+  const uint64_t *l2 = reinterpret_cast<const uint64_t *>(lse2c);
+  const uint64_t *d2 = reinterpret_cast<const uint64_t *>(dvc);
 #pragma unroll
   for (int e2 = 0; e2 < 16; ++e2) {
-    float pv[2], dv[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int e = 2 * e2 + u;
-      const float sv = __uint_as_float(sr[e]);
-      float t2, f;
-      if constexpr (CAP) {
-        const float ee = ex2_approx(fabsf(sv) * capc);  // exp(-2|u|/cap)
-        const float rr = rcp_approx(1.f + ee);
-        const float th = fmaf(-ee, rr, rr);             // tanh(|u|/cap)
-        t2 = copysignf(th * cap2, sv);
-        f = fscale * ee * rr * rr;                      // 4 e / (1 + e)^2 = 1 - tanh^2, times scale
-      } else {
-        t2 = sv * sc2;
-        f = scale;
-      }
-      float x = t2 - lse2c[e];
-      if constexpr (MASK >= 1) {
-        const int q = qbase + e;
-        bool vis = (q >= lo) & (q < hi);
-        if constexpr (MASK == 2) vis = vis & (__ldg(segq + min(q, sq - 1)) == sid);
-        x = vis ? x : -INFINITY;
-      }
-      const float pr = ex2_approx(x);
-      pv[u] = pr;
-      if constexpr (KIND != 1) dv[u] = pr * (__uint_as_float(dr[e]) - dvc[e]) * f;
+    uint64_t y, f;
+    score_pair<CAP>(sr[2 * e2], sr[2 * e2 + 1], l2[e2], k, y, f);
+    const uint64_t p2 = ex2_pair(y);
+    pk[e2] = bf16_pair(p2);
+    if constexpr (KIND == 0) {
+      const uint64_t dp = f2_pack(__uint_as_float(dr[2 * e2]), __uint_as_float(dr[2 * e2 + 1]));
+      dk[e2] = bf16_pair(f2_mul(f2_mul(p2, f), f2_sub(dp, d2[e2])));
     }
-    if constexpr (KIND != 2) pk[e2] = pack_bf16(pv[0], pv[1]);
-    if constexpr (KIND != 1) dk[e2] = pack_bf16(dv[0], dv[1]);
   }
 }
 
 // The dK pass's chunk in two steps, so that the first runs before dP^T has been computed:
-// (1) in place, the raw score -> P f = exp2(t2 - LSE2) (1 - tanh^2) scale, masked entries 0;
-template <bool CAP, int MASK>
-__device__ __forceinline__ void ds_first(uint32_t (&sr)[32], const float *lse2c, float sc2, float capc, float cap2,
-                                         float fscale, float scale, int qbase, int lo, int hi, int sq,
-                                         const int *segq, int sid) {
+// (1) in place, the raw score -> P f;
+template <bool CAP>
+__device__ __forceinline__ void ds_first(uint32_t (&sr)[32], const float *lse2c, const BwdScore &k) {
+  const uint64_t *l2 = reinterpret_cast<const uint64_t *>(lse2c);
 #pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const float sv = __uint_as_float(sr[e]);
-    float t2, f;
-    if constexpr (CAP) {
-      const float ee = ex2_approx(fabsf(sv) * capc);
-      const float rr = rcp_approx(1.f + ee);
-      const float th = fmaf(-ee, rr, rr);
-      t2 = copysignf(th * cap2, sv);
-      f = fscale * ee * rr * rr;
-    } else {
-      t2 = sv * sc2;
-      f = scale;
-    }
-    float x = t2 - lse2c[e];
-    if constexpr (MASK >= 1) {
-      const int q = qbase + e;
-      bool vis = (q >= lo) & (q < hi);
-      if constexpr (MASK == 2) vis = vis & (__ldg(segq + min(q, sq - 1)) == sid);
-      x = vis ? x : -INFINITY;
-    }
-    sr[e] = __float_as_uint(ex2_approx(x) * f);
+  for (int e2 = 0; e2 < 16; ++e2) {
+    uint64_t y, f;
+    score_pair<CAP>(sr[2 * e2], sr[2 * e2 + 1], l2[e2], k, y, f);
+    float a, b;
+    f2_unpack(f2_mul(ex2_pair(y), f), a, b);
+    sr[2 * e2] = __float_as_uint(a);
+    sr[2 * e2 + 1] = __float_as_uint(b);
   }
 }
 // (2) dS = P f (dP - D), packed to bf16 pairs.
 __device__ __forceinline__ void ds_second(const uint32_t (&pf)[32], const uint32_t (&dr)[32], const float *dvc,
                                           uint32_t (&dk)[16]) {
+  const uint64_t *d2 = reinterpret_cast<const uint64_t *>(dvc);
 #pragma unroll
-  for (int e2 = 0; e2 < 16; ++e2)
-    dk[e2] = pack_bf16(__uint_as_float(pf[2 * e2]) * (__uint_as_float(dr[2 * e2]) - dvc[2 * e2]),
-                       __uint_as_float(pf[2 * e2 + 1]) * (__uint_as_float(dr[2 * e2 + 1]) - dvc[2 * e2 + 1]));
+  for (int e2 = 0; e2 < 16; ++e2) {
+    const uint64_t pf2 = f2_pack(__uint_as_float(pf[2 * e2]), __uint_as_float(pf[2 * e2 + 1]));
+    const uint64_t dp = f2_pack(__uint_as_float(dr[2 * e2]), __uint_as_float(dr[2 * e2 + 1]));
+    dk[e2] = bf16_pair(f2_mul(pf2, f2_sub(dp, d2[e2])));
+  }
 }
 
-template <bool CAP, int KIND>
-__device__ __forceinline__ void bwd_chunk_masked(int mask, const uint32_t (&sr)[32], const uint32_t (&dr)[32],
-                                                 const float *lse2c, const float *dvc, uint32_t (&pk)[16],
-                                                 uint32_t (&dk)[16], float sc2, float capc, float cap2, float fscale,
-                                                 float scale, int qbase, int lo, int hi, int sq, const int *segq,
-                                                 int sid) {
-  if (mask == 0)
-    bwd_chunk<CAP, KIND, 0>(sr, dr, lse2c, dvc, pk, dk, sc2, capc, cap2, fscale, scale, qbase, lo, hi, sq, segq, sid);
-  else if (mask == 1)
-    bwd_chunk<CAP, KIND, 1>(sr, dr, lse2c, dvc, pk, dk, sc2, capc, cap2, fscale, scale, qbase, lo, hi, sq, segq, sid);
-  else
-    bwd_chunk<CAP, KIND, 2>(sr, dr, lse2c, dvc, pk, dk, sc2, capc, cap2, fscale, scale, qbase, lo, hi, sq, segq, sid);
+// Visibility of the 32 query columns qb .. qb + 31 for this thread's key: bit e is set when
+// query qb + e lies in [lo, hi) and, with unsorted segment ids, shares the key's segment.
+__device__ __forceinline__ uint32_t chunk_vis(int qb, int lo, int hi, bool pairwise, const int *segq, int sq,
+                                              int sid) {
+  const int a = max(lo - qb, 0), b = min(hi - qb, 32);
+  if (a >= b) return 0u;
+  uint32_t v = (b == 32 ? 0xffffffffu : ((1u << b) - 1u)) & ~((1u << a) - 1u);
+  if (pairwise) {
+    uint32_t same = 0u;
+#pragma unroll 1
+    for (int e = 0; e < 32; ++e) same |= (uint32_t)(__ldg(segq + min(qb + e, sq - 1)) == sid) << e;
+    v &= same;
+  }
+  return v;
+}
+// Clear the hidden columns of a chunk: 32 fp32 values, or 16 bf16 pairs.
+__device__ __forceinline__ void clear_hidden(uint32_t (&x)[32], uint32_t vis) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e) x[e] = ((vis >> e) & 1u) ? x[e] : 0u;
+}
+__device__ __forceinline__ void clear_hidden(uint32_t (&x)[16], uint32_t vis) {
+#pragma unroll
+  for (int e2 = 0; e2 < 16; ++e2)
+    x[e2] &= (((vis >> (2 * e2)) & 1u) ? 0x0000ffffu : 0u) | (((vis >> (2 * e2 + 1)) & 1u) ? 0xffff0000u : 0u);
 }
 
 template <class C, bool CAP>
@@ -390,10 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
 
-    const float sc2 = p.scale * kLog2e;
-    const float capc = -2.f * kLog2e * p.scale * p.inv_cap;
-    const float cap2 = p.cap * kLog2e;
-    const float fscale = 4.f * p.scale;  // 1 - tanh^2 = 4 e / (1 + e)^2, times the softmax scale
+    const BwdScore ks(p.scale, p.inv_cap, p.cap);
     uint8_t *ds_row = smem + C::OFF_DS + r * 128;
     bool ok = true;
 
@@ -414,7 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // step's dV / dK / dQ MMAs still read the P^T and dS^T buffers (and, once S^T / dP^T
       // are copied out, while the next step's S^T / dP^T are computed) ...
       constexpr int NCH = BQ / 64;  // 32-column chunks per thread and step
-      const int mask = full ? 0 : (seg_pairwise ? 2 : 1);
       uint32_t pk[NCH][16], dk[NCH][16];
       if (C::TWO && kind == 2) {
         // dK pass: P f from S^T first, then dP^T (computed meanwhile) for dS.
@@ -429,14 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(sdp_free);
           }
-          const float *lc = lse2 + c * 32;
-          const int qb = q0 + c * 32;
-          if (mask == 0)
-            ds_first<CAP, 0>(pf[cc], lc, sc2, capc, cap2, fscale, p.scale, qb, lo, hi, p.Sq, segq, sid);
-          else if (mask == 1)
-            ds_first<CAP, 1>(pf[cc], lc, sc2, capc, cap2, fscale, p.scale, qb, lo, hi, p.Sq, segq, sid);
-          else
-            ds_first<CAP, 2>(pf[cc], lc, sc2, capc, cap2, fscale, p.scale, qb, lo, hi, p.Sq, segq, sid);
+          ds_first<CAP>(pf[cc], lse2 + c * 32, ks);
+          if (!full) clear_hidden(pf[cc], chunk_vis(q0 + c * 32, lo, hi, seg_pairwise, segq, p.Sq, sid));
         }
         if (!mbar_wait(dp_full, (j - nper) & 1, p.status)) { ok = false; break; }
         tc_fence_after();
@@ -459,22 +475,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = half * NCH + cc;  // 32-column chunk of this step
           uint32_t sr[32], dr[32];
           tmem_ld32(lane_addr + C::TM_S + c * 32, sr);
-          if (kind != 1) tmem_ld32(lane_addr + C::TM_DP + c * 32, dr);
+          if constexpr (!C::TWO) tmem_ld32(lane_addr + C::TM_DP + c * 32, dr);
           tmem_wait_ld();
           reg_fence(sr);
-          if (kind != 1) reg_fence(dr);
+          if constexpr (!C::TWO) reg_fence(dr);
           if (cc == NCH - 1) {
             tc_fence_before();
             mbar_arrive(sdp_free);
           }
-          const float *lc = lse2 + c * 32, *dc = dvv + c * 32;
-          const int qb = q0 + c * 32;
-          if (kind == 0)
-            bwd_chunk_masked<CAP, 0>(mask, sr, dr, lc, dc, pk[cc], dk[cc], sc2, capc, cap2, fscale, p.scale, qb, lo,
-                                     hi, p.Sq, segq, sid);
-          else
-            bwd_chunk_masked<CAP, 1>(mask, sr, dr, lc, dc, pk[cc], dk[cc], sc2, capc, cap2, fscale, p.scale, qb, lo,
-                                     hi, p.Sq, segq, sid);
+          bwd_chunk<CAP, C::TWO ? 1 : 0>(sr, dr, lse2 + c * 32, dvv + c * 32, pk[cc], dk[cc], ks);
+          if (!full) {
+            const uint32_t vis = chunk_vis(q0 + c * 32, lo, hi, seg_pairwise, segq, p.Sq, sid);
+            clear_hidden(pk[cc], vis);
+            if (!C::TWO) clear_hidden(dk[cc], vis);
+          }
         }
       }
       if (C::TWO) mbar_arrive(ld_empty(j & 1));  // LSE / D of this step have been read

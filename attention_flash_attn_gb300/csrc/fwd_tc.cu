@@ -86,31 +86,53 @@ __device__ __forceinline__ int upper_bound_i(const int *a, int n, int x) {
 // Both warps of the pair arrive converged, so the aligned form applies.
 __device__ __forceinline__ void pair_bar(int wq) { asm volatile("bar.sync %0, 64;" ::"r"(2 + wq) : "memory"); }
 
+// Score constants as packed pairs.  With the soft-cap, e = exp(2 u / cap) for u = scale s and
+// r = 1 / (1 + e): tanh(u / cap) = 1 - 2 r, so the capped logit in log2 units is
+// cap log2(e) (1 - 2 r).  An overflowing e gives r = 0 (tanh = 1), an underflowing one r = 1.
+struct FwdScore {
+  uint64_t cin, one, mcap2, cap2, sc2;
+  __device__ FwdScore(float scale, float inv_cap, float cap) {
+    cin = f2_splat(2.f * kLog2e * scale * inv_cap);
+    one = f2_splat(1.f);
+    mcap2 = f2_splat(-2.f * cap * kLog2e);
+    cap2 = f2_splat(cap * kLog2e);
+    sc2 = f2_splat(scale * kLog2e);
+  }
+};
+
 // Raw scores -> capped, masked base-2 logits in place; returns their maximum.
 template <bool CAP, bool MASKED, int N>
-__device__ __forceinline__ float logits2(uint32_t (&x)[N], float sc2, float capc, float cap2, int jbase, int lo,
-                                         int hi, bool pairwise, const int *segk, int sid) {
+__device__ __forceinline__ float logits2(uint32_t (&x)[N], const FwdScore &k, int jbase, int lo, int hi,
+                                         bool pairwise, const int *segk, int sid) {
   float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < N; ++e) {
-    const float s = __uint_as_float(x[e]);
-    float t2;
+  for (int e = 0; e < N; e += 2) {
+    const uint64_t s2 = f2_pack(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+    uint64_t t2;
     if constexpr (CAP) {
-      const float ee = ex2_approx(fabsf(s) * capc);  // exp(-2|u|/cap)
-      const float rr = rcp_approx(1.f + ee);
-      const float th = fmaf(-ee, rr, rr);            // tanh(|u|/cap)
-      t2 = copysignf(th * cap2, s);
+      float xa, xb, da, db;
+      f2_unpack(f2_mul(s2, k.cin), xa, xb);
+      f2_unpack(f2_add(f2_pack(ex2_approx(xa), ex2_approx(xb)), k.one), da, db);
+      t2 = f2_fma(f2_pack(rcp_approx(da), rcp_approx(db)), k.mcap2, k.cap2);
     } else {
-      t2 = s * sc2;
+      t2 = f2_mul(s2, k.sc2);
     }
+    float ta, tb;
+    f2_unpack(t2, ta, tb);
     if constexpr (MASKED) {
-      const int jj = jbase + e;
-      bool vis = jj >= lo && jj < hi;
-      if (pairwise) vis = vis && __ldg(segk + jj) == sid;
-      t2 = vis ? t2 : -INFINITY;
+      const int ja = jbase + e, jb = ja + 1;
+      bool va = ja >= lo && ja < hi, vb = jb >= lo && jb < hi;
+      if (pairwise) {
+        va = va && __ldg(segk + ja) == sid;
+        vb = vb && __ldg(segk + jb) == sid;
+      }
+      ta = va ? ta : -INFINITY;
+      tb = vb ? tb : -INFINITY;
     }
-    x[e] = __float_as_uint(t2);
-    if (e & 1) m1 = fmaxf(m1, t2); else m0 = fmaxf(m0, t2);
+    x[e] = __float_as_uint(ta);
+    x[e + 1] = __float_as_uint(tb);
+    m0 = fmaxf(m0, ta);
+    m1 = fmaxf(m1, tb);
   }
   return fmaxf(m0, m1);
 }
@@ -314,9 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
 
-    const float sc2 = p.scale * kLog2e;                        // uncapped: t2 = s * sc2
-    const float capc = -2.f * kLog2e * p.scale * p.inv_cap;    // e = 2^(|s| * capc) = exp(-2|u|/cap)
-    const float cap2 = p.cap * kLog2e;                         // t2 = tanh * cap * log2(e)
+    const FwdScore ks(p.scale, p.inv_cap, p.cap);
     float m_ref = p.sink ? p.sink[h] * kLog2e : -INFINITY;     // running max (log2 units)
     float l = (p.sink && half == 0) ? 1.f : 0.f;               // this half's sum relative to m_ref
     bool ok = true;
@@ -338,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool full = !any_pairwise && (t0 + j) * BN >= cta_lo && (t0 + j + 1) * BN <= cta_hi;
       float mx = -INFINITY;
       if (got) {
-        mx = full ? logits2<CAP, false>(xr, sc2, capc, cap2, j0, lo, hi, seg_pairwise, segk, sid)
-                  : logits2<CAP, true>(xr, sc2, capc, cap2, j0, lo, hi, seg_pairwise, segk, sid);
+        mx = full ? logits2<CAP, false>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid)
+                  : logits2<CAP, true>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid);
       }
       // Exchange half-row maxima (and failure flags, as NaN) with the partner warp; slot
       // j & 1 is rewritten two tiles later, after the partner has passed the next barrier.
@@ -366,17 +386,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float rs0 = 0.f, rs1 = 0.f;
+      const uint64_t mr2 = f2_splat(mr);
+      uint64_t rs2 = f2_splat(0.f);
       uint32_t pk[HC / 2];
 #pragma unroll
       for (int e = 0; e < HC / 2; ++e) {
-        const float p0 = ex2_approx(__uint_as_float(xr[2 * e]) - mr);
-        const float p1 = ex2_approx(__uint_as_float(xr[2 * e + 1]) - mr);
-        rs0 += p0;
-        rs1 += p1;
+        float ya, yb;
+        f2_unpack(f2_sub(f2_pack(__uint_as_float(xr[2 * e]), __uint_as_float(xr[2 * e + 1])), mr2), ya, yb);
+        const float p0 = ex2_approx(ya), p1 = ex2_approx(yb);
+        const uint64_t p2 = f2_pack(p0, p1);
+        rs2 = f2_add(rs2, p2);
         pk[e] = pack_bf16(p0, p1);
       }
-      l += rs0 + rs1;
+      {
+        float ra, rb;
+        f2_unpack(rs2, ra, rb);
+        l += ra + rb;
+      }
       // P (bf16 pairs) over the first half of this score buffer's columns.
       const uint32_t pa = lane_addr + (uint32_t)((j & 1) * BN + half * (HC / 2));
 #pragma unroll
