@@ -19,10 +19,10 @@
 // Head dim 256: dK and dV fill all 512 TMEM columns, so the CTA runs two passes over its
 // query steps -- dV first, then dK and dQ (S^T recomputed).  V is not needed in the dV pass,
 // so its shared-memory slot doubles as a second Q/dO stage there and V is loaded for the
-// second pass.  In the dK pass the remaining stage is a ring of four half tiles (128 of the
-// 256 columns each), filled in the order Q_i, Q_{i-1} (again, for dK of the previous step),
-// dO_i and read by one MMA warp alone, so S^T of the next step is computed while the softmax
-// warps still work on this one, and those warps form P from S^T before dP^T is in.
+// second pass.  In the dK pass the remaining stage is a ring of two tile slots, filled in the
+// order Q_i, dO_i, Q_{i-1} (again, for dK of the previous step) and read by one MMA warp
+// alone, so S^T of the next step is computed while the softmax warps still work on this one,
+// and those warps form P from S^T before dP^T is in.
 //
 // Warps: 0..7 softmax / dS, 8 TMA producer, 9 MMA issuer + TMEM owner, 10 second MMA issuer
 // (the MMAs that consume P and dS while warp 9 issues S^T / dP^T), 12..15 dQ drain.
@@ -300,16 +300,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the Q lane and released by the softmax warps once they have read it.
   auto ld_full = [&](int x) { return bar0 + 8u * (14 + 2 * C::NSLOT + x); };
   auto ld_empty = [&](int x) { return bar0 + 8u * (16 + 2 * C::NSLOT + x); };
-  // Two-pass form, dK pass: stage 0 (64 KiB) becomes a ring of four 16 KiB slots, each one
-  // half (128 of the 256 columns) of a Q or dO tile.  In ring order, step i brings Q_i (for
-  // S^T), dO_i (for dP^T) and Q_{i-1} again (for dK_{i-1}, which runs once the softmax of step
-  // i - 1 is done): no tile stays resident from its S^T to its dK.
+  // Two-pass form, dK pass: stage 0 (64 KiB) becomes a ring of two 32 KiB tile slots.  In ring
+  // order, step i brings Q_i (for S^T), dO_i (for dP^T) and Q_{i-1} again (for dK_{i-1}, which
+  // runs once the softmax of step i - 1 is done): no tile stays resident from its S^T to its
+  // dK.  Each slot has one full and one empty barrier, so the MMA warp waits and commits once
+  // per tile (a commit between MMA groups costs the tensor pipe a drain).
   auto ring_full = [&](int r) { return bar0 + 8u * (18 + 2 * C::NSLOT + r); };
   auto ring_empty = [&](int r) { return bar0 + 8u * (22 + 2 * C::NSLOT + r); };
   const uint32_t dp_full = bar0 + 8u * (26 + 2 * C::NSLOT);  // dP^T of a dK-pass step is in TMEM
   const uint32_t dp_free = bar0 + 8u * (27 + 2 * C::NSLOT);  // ... and has been copied out (256)
-  constexpr int kRing = 4, kHalf = C::QT_BYTES / 2;
-  auto ring_addr = [&](int n) -> uint32_t { return sbase + C::OFF_SLOT0 + (n % kRing) * kHalf; };
+  constexpr int kRing = 2;
+  auto ring_addr = [&](int n) -> uint32_t { return sbase + C::OFF_SLOT0 + (n % kRing) * C::QT_BYTES; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *red = misc_i + 4;  // [8]
 
@@ -588,19 +589,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
         for (int c = 0; c < C::KCH; ++c) tma_load_4d(sbase + C::OFF_K + c * (kBK * 128), &tmK, kv_full, c * 64, k0, g, b);
         int n = 0;  // dK-pass ring position
-        // One half tile (columns 128*hf .. 128*hf + 127 of Q or dO rows q0 .. q0 + BQ - 1) into
-        // the next ring slot.  The first four slots are stage 0 of the dV pass: wait for its last
-        // Q (slots 0, 1) or dO (slots 2, 3) to be released.
-        auto ring_load = [&](const CUtensorMap *tm, int hf, int q0, int h) -> bool {
+        // One Q or dO tile (rows q0 .. q0 + BQ - 1) into the next ring slot.  The two slots are
+        // stage 0 of the dV pass: the first use of slot 0 waits for its last Q to be released,
+        // that of slot 1 for its last dO.
+        auto ring_load = [&](const CUtensorMap *tm, int q0, int h) -> bool {
           const int r = n % kRing, u = n / kRing;
-          const bool ok = u == 0 ? (r < 2 ? mbar_wait(qdo_empty(0), u_last0 & 1, p.status)
-                                          : mbar_wait(do0_free, 0, p.status))
+          const bool ok = u == 0 ? (r == 0 ? mbar_wait(qdo_empty(0), u_last0 & 1, p.status)
+                                           : mbar_wait(do0_free, 0, p.status))
                                  : mbar_wait(ring_empty(r), (u - 1) & 1, p.status);
           if (!ok) return false;
-          mbar_arrive_expect_tx(ring_full(r), kHalf);
+          mbar_arrive_expect_tx(ring_full(r), C::QT_BYTES);
   #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            tma_load_4d(ring_addr(n) + c * (BQ * 128), tm, ring_full(r), (2 * hf + c) * 64, q0, h, b);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(ring_addr(n) + c * (BQ * 128), tm, ring_full(r), c * 64, q0, h, b);
           ++n;
           return true;
         };
@@ -631,15 +632,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // Q_i for S^T, dO_i for dP^T, Q_{i-1} again for dK of the previous step
             const int h = step_h(j), q0 = step_q0(j);
-            if (!ring_load(&tmQ, 0, q0, h) || !ring_load(&tmQ, 1, q0, h)) break;
-            if (!ring_load(&tmdO, 0, q0, h) || !ring_load(&tmdO, 1, q0, h)) break;
-            if (j > nper && (!ring_load(&tmQ, 0, step_q0(j - 1), step_h(j - 1)) ||
-                             !ring_load(&tmQ, 1, step_q0(j - 1), step_h(j - 1))))
-              break;
+            if (!ring_load(&tmQ, q0, h) || !ring_load(&tmdO, q0, h)) break;
+            if (j > nper && !ring_load(&tmQ, step_q0(j - 1), step_h(j - 1))) break;
           }
           if (j == nsteps && j > nper) {  // Q of the last step again, for its dK
-            const int h = step_h(j - 1), q0 = step_q0(j - 1);
-            if (!ring_load(&tmQ, 0, q0, h) || !ring_load(&tmQ, 1, q0, h)) break;
+            if (!ring_load(&tmQ, step_q0(j - 1), step_h(j - 1))) break;
           }
         }
       } else if (lane == 1) {
@@ -765,12 +762,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nB = nsteps - nper;  // dK-pass steps
           // Ring positions of dK-pass step i's tiles, in the order the loader fills the ring and
           // the front warp reads it: Q_0 dO_0 | Q_1 dO_1 Qb_0 | Q_2 dO_2 Qb_1 | ... | Qb_{nB-1}
-          // (Qb: Q again, for dK).  A slot is refilled four positions later: Q_i where dO_{i-1}
+          // (Qb: Q again, for dK).  A slot is refilled two positions later: Q_i where dO_{i-1}
           // was (free after dP^T_{i-1}), dO_i where Qb_{i-2} was (after dK_{i-2}), Qb_{i-1} where
           // Q_i was (after S^T_i).
-          auto pos_q = [&](int i) { return i == 0 ? 0 : 6 * i - 2; };
-          auto pos_do = [&](int i) { return i == 0 ? 2 : 6 * i; };
-          auto pos_qb = [&](int i) { return i + 1 < nB ? 6 * i + 8 : 6 * nB - 2; };
+          auto pos_q = [&](int i) { return i == 0 ? 0 : 3 * i - 1; };
+          auto pos_do = [&](int i) { return i == 0 ? 1 : 3 * i; };
+          auto pos_qb = [&](int i) { return i + 1 < nB ? 3 * i + 4 : 3 * nB - 1; };
           // dV of a dV-pass step: P^T from TMEM, dO of its slot; releases that dO slot.
           auto back_dv = [&](int jj) -> bool {
             const int s = slot_of(jj);
@@ -786,26 +783,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_w(mma_done);  // both arrivals of the step: no dK in the dV pass
             return true;
           };
-          // dK of a dK-pass step (front warp): Q of the step again, from two ring slots, each
-          // released after its 128-column half of dK.
+          // dK of a dK-pass step (front warp): Q of the step again, from its ring slot, in two
+          // N = 128 halves of D (each half's columns are a 16 KiB run of the tile).
           auto mma_dk = [&](int jj) -> bool {
             if (jj == nper) {  // dV has been stored: the accumulator is free for dK
               if (!mbar_wait_warp(acc_free, 0, p.status)) return false;
               tc_fence_after();
             }
-            const int n0 = pos_qb(jj - nper);
+            const int n = pos_qb(jj - nper), r = n % kRing;
+            if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
+            tc_fence_after();
   #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
-              const int n = n0 + hf, r = n % kRing;
-              if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
-              tc_fence_after();
-              const uint64_t q_mn = sw128_desc(ring_addr(n), BQ * 128, 1024);
+              const uint64_t q_mn = sw128_desc(ring_addr(n) + hf * (C::QT_BYTES / 2), BQ * 128, 1024);
   #pragma unroll
               for (int kk = 0; kk < BQ / 16; ++kk)
                 mma_ss_w(tmem + C::TM_DK + hf * (D / 2), desc_at(dS_k, (kk >> 2) * (kBK * 128) + (kk & 3) * 32),
                          desc_at(q_mn, kk * 2048), idKh, (jj > nper || kk > 0) ? 1u : 0u);
-              mma_commit_w(ring_empty(r));
             }
+            mma_commit_w(ring_empty(r));
             mma_commit_w(mma_done);
             return true;
           };
@@ -817,25 +813,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_w(mma_done);
             return true;
           };
-          // S^T (A = K) or dP^T (A = V) of a dK-pass step from the two ring slots at n0, n0 + 1
-          // (the two column halves of Q or dO), each slot released once read.
-          auto front_ring = [&](uint64_t a_k, uint32_t d_col, int n0) -> bool {
-  #pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {
-              const int n = n0 + hf, r = n % kRing;
-              if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
-              tc_fence_after();
-              uint64_t b_k = sw128_desc(ring_addr(n), 16, 1024);
-  #pragma unroll 1
-              for (int c = 0; c < 2; ++c) {  // the two 64-column chunks of this half
-  #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4)
-                  mma_ss_w(tmem + d_col, desc_at(a_k, k4 * 32), desc_at(b_k, k4 * 32), idST, (hf | c | k4) != 0);
-                a_k = desc_at(a_k, kBK * 128);
-                b_k = desc_at(b_k, BQ * 128);
-              }
-              mma_commit_w(ring_empty(r));
-            }
+          // S^T (A = K) or dP^T (A = V) of a dK-pass step from the Q or dO tile at ring position
+          // n, whose slot is released once read.
+          auto front_ring = [&](uint64_t a_k, uint32_t d_col, int n) -> bool {
+            const int r = n % kRing;
+            if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
+            tc_fence_after();
+            mma_front(a_k, ring_addr(n), d_col);
+            mma_commit_w(ring_empty(r));
             return true;
           };
           if (!back_warp) {

@@ -18,11 +18,12 @@ from collections import defaultdict
 import pytest
 
 
-def simulate(nper, design="single_reader", rng=None, order="q_do_qb"):
+def simulate(nper, design="single_reader", rng=None, order="q_do_qb", tiles=True):
     """Returns (finished, hazards).  nper: query steps per pass (dV pass = dK pass).
     order: the ring's fill order within a dK-pass step.  The kernel fills Q_i, dO_i, Q_{i-1}
     and its front warp issues S^T_i, dP^T_i, dK_{i-1} ("q_do_qb"); "q_qb_do" is the earlier
-    single-reader layout (S^T_i, dK_{i-1}, dP^T_i)."""
+    single-reader layout (S^T_i, dK_{i-1}, dP^T_i).  tiles: the ring holds two whole tiles
+    (as in the kernel) rather than four half tiles."""
     rng = rng or random.Random(0)
     nsteps, nB = 2 * nper, nper
     need = defaultdict(lambda: 1)
@@ -40,13 +41,15 @@ def simulate(nper, design="single_reader", rng=None, order="q_do_qb"):
     slot_of = lambda j: j & 1
     use_of = lambda j: j >> 1
     u_last0, u_last1 = ((nper + 1) >> 1) - 1, (nper >> 1) - 1
-    pos_q = lambda i: 0 if i == 0 else 6 * i - 2
+    H = 1 if tiles else 2  # ring slots per tile
+    R = 2 * H               # ring depth in slots
+    pos_q = lambda i: H * (0 if i == 0 else 3 * i - 1)
     if order == "q_qb_do":
-        pos_do = lambda i: 2 if i == 0 else 6 * i + 2
-        pos_qb = lambda i: 6 * (i + 1) if i + 1 < nB else 6 * nB - 2
+        pos_do = lambda i: H * (1 if i == 0 else 3 * i + 1)
+        pos_qb = lambda i: H * (3 * (i + 1) if i + 1 < nB else 3 * nB - 1)
     else:  # "q_do_qb", as in bwd_tc.cu
-        pos_do = lambda i: 2 if i == 0 else 6 * i
-        pos_qb = lambda i: 6 * i + 8 if i + 1 < nB else 6 * nB - 2
+        pos_do = lambda i: H * (1 if i == 0 else 3 * i)
+        pos_qb = lambda i: H * (3 * i + 4 if i + 1 < nB else 3 * nB - 1)
 
     def loader0():
         yield ("arrive", "kv_full")
@@ -54,9 +57,9 @@ def simulate(nper, design="single_reader", rng=None, order="q_do_qb"):
 
         def ring_load():
             nonlocal n
-            r, u = n % 4, n // 4
+            r, u = n % R, n // R
             if u == 0:
-                if r < 2:
+                if r < H:
                     yield ("wait", "qdo_empty0", u_last0)
                 elif design == "single_reader":
                     yield ("wait", "do0_free", 0)
@@ -82,18 +85,18 @@ def simulate(nper, design="single_reader", rng=None, order="q_do_qb"):
                     if u_last1 >= 0:
                         yield ("wait", "qdo_empty1", u_last1)
                     yield ("arrive", "v_full")
-                for _ in range(2):  # Q_i
+                for _ in range(H):  # Q_i
                     yield from ring_load()
                 if order == "q_qb_do" and j > nper:  # Q_{i-1} again
-                    for _ in range(2):
+                    for _ in range(H):
                         yield from ring_load()
-                for _ in range(2):  # dO_i
+                for _ in range(H):  # dO_i
                     yield from ring_load()
                 if order == "q_do_qb" and j > nper:
-                    for _ in range(2):
+                    for _ in range(H):
                         yield from ring_load()
             if j == nsteps and j > nper:
-                for _ in range(2):
+                for _ in range(H):
                     yield from ring_load()
 
     def loader1():
@@ -111,10 +114,10 @@ def simulate(nper, design="single_reader", rng=None, order="q_do_qb"):
                 yield ("arrive", "do0_free")
 
     def ring(n0):
-        for hf in range(2):
+        for hf in range(H):
             n = n0 + hf
-            yield ("wait", f"ring_full{n % 4}", n // 4)
-            yield ("arrive", f"ring_empty{n % 4}")
+            yield ("wait", f"ring_full{n % R}", n // R)
+            yield ("arrive", f"ring_empty{n % R}")
 
     def dk(i):  # dK of dK-pass step i (the front warp in the single-reader design)
         yield ("wait", "p_ready", nper + i)
@@ -242,12 +245,12 @@ def simulate(nper, design="single_reader", rng=None, order="q_do_qb"):
 STEP_COUNTS = [1, 2, 3, 4, 5, 6, 8, 13, 33, 66, 80]
 
 
-@pytest.mark.parametrize("order", ["q_do_qb", "q_qb_do"])
-def test_single_reader_protocol_never_deadlocks_or_aliases(order):
+@pytest.mark.parametrize("order,tiles", [("q_do_qb", True), ("q_do_qb", False), ("q_qb_do", False)])
+def test_single_reader_protocol_never_deadlocks_or_aliases(order, tiles):
     rng = random.Random(1234)
     for trial in range(1000):
         nper = STEP_COUNTS[trial % len(STEP_COUNTS)]
-        finished, hazards = simulate(nper, "single_reader", rng, order=order)
+        finished, hazards = simulate(nper, "single_reader", rng, order=order, tiles=tiles)
         assert finished and not hazards, (nper, hazards[:3])
 
 
@@ -257,7 +260,7 @@ def test_model_flags_the_shared_ring_layout():
     rng = random.Random(99)
     flagged = 0
     for trial in range(400):
-        finished, hazards = simulate(66, "shared_ring", rng, order="q_do_qb")
+        finished, hazards = simulate(66, "shared_ring", rng, order="q_do_qb", tiles=False)
         flagged += (not finished) or bool(hazards)
     assert flagged > 0
 
