@@ -17,12 +17,13 @@
 // query step's Q, dO, LSE*log2(e) and D arrive together by TMA / bulk copy.
 //
 // Head dim 256: dK and dV fill all 512 TMEM columns, so the CTA runs two passes over its
-// query steps -- dV first, then dK and dQ (S^T recomputed).  V is not needed in the dV pass,
-// so its shared-memory slot doubles as a second Q/dO stage there and V is loaded for the
-// second pass.  In the dK pass the remaining stage is a ring of two tile slots, filled in the
-// order Q_i, dO_i, Q_{i-1} (again, for dK of the previous step) and read by one MMA warp
-// alone, so S^T of the next step is computed while the softmax warps still work on this one,
-// and those warps form P from S^T before dP^T is in.
+// query steps -- dV first, then dK and dQ (S^T recomputed).  V is not needed in the dV pass, so
+// its shared-memory slot doubles as a second Q/dO stage there.  For the dK pass V moves into
+// tensor memory (the A operand of dP^T = V dO^T), S^T and dP^T share one score buffer and dQ^T
+// is produced one 128-row half at a time; both dV-pass stages then form a ring of four
+// whole-tile slots (Q_i, dO_i, ...) read by one MMA warp alone, in which Q_i stays from its
+// S^T to its dK.  S^T of the next step is computed while the softmax warps still work on this
+// one, and those warps form P from S^T before dP^T is in.
 //
 // Warps: 0..7 softmax / dS, 8 TMA producer, 9 MMA issuer + TMEM owner, 10 second MMA issuer
 // (the MMAs that consume P and dS while warp 9 issues S^T / dP^T), 12..15 dQ drain.
@@ -44,9 +45,9 @@ constexpr int kThreads = 512;
 // Warpgroups: 0-1 softmax / dS (warps 0..7), 2 producers and MMA issuers (8 TMA, 9 front MMA
 // and TMEM owner, 10 back MMA, 11 idle), 3 dQ drain (12..15).  Registers are moved from the
 // producers and the drain to the softmax warpgroups (setmaxnreg): the element-wise loops need
-// many values in flight to keep the MUFU busy.  128 threads x (184 + 184 + 64 + 72) stays
+// many values in flight to keep the MUFU busy.  128 threads x (176 + 176 + 72 + 80) stays
 // within the 512 x 128 registers the CTA is launched with.
-constexpr int kRegSoftmax = 184, kRegProducer = 64, kRegDrain = 72;
+constexpr int kRegSoftmax = 176, kRegProducer = 72, kRegDrain = 80;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kDrainThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -69,7 +70,7 @@ struct BwdCfg {
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
   static constexpr int OFF_LD = OFF_DQS + DQS_BYTES;  // per slot: LSE*log2e [BQ], D [BQ]
   static constexpr int OFF_BAR = OFF_LD + NSLOT * 2 * BQ * 4;
-  static constexpr int NBAR = 12 + 2 * NSLOT + (TWO ? 18 : 0);  // + dQ half-1 release, dO stage hand-over
+  static constexpr int NBAR = 12 + 2 * NSLOT + (TWO ? 19 : 0);  // + dQ half-1 release, dO stage hand-overs
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   // TMEM columns
@@ -80,6 +81,9 @@ struct BwdCfg {
   // Two-pass form: P lives in the dQ columns, idle during the dV pass.
   static constexpr int TM_P = TWO ? 384 : TM_DP + BQ;
   static constexpr int TM_DQ = TWO ? 384 : TM_P + BQ / 2;
+  // Two-pass form, dK pass: V (bf16 pairs, the A operand of dP^T), one score buffer shared by
+  // S^T and then dP^T, and one 128-row half of dQ^T at a time.
+  static constexpr int TM_V = 256, TM_SDP = 384, TM_DQH = 448;
   static constexpr int DQ_COLS = DQT ? (D / 128) * BQ : D;
   static_assert(TM_DQ + DQ_COLS <= 512, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -290,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // that stage's releases in order, hands it to lane 0 through this single-phase barrier (a
   // waiter that has not seen a barrier's earlier phases could mistake one for the next).
   const uint32_t do0_free = bar0 + 8u * (C::NBAR - 2);
+  const uint32_t do1_free = bar0 + 8u * (C::NBAR - 3);  // the same for the second dO stage
   const uint32_t sdp_free = bar0 + 72u;  // S^T / dP^T copied out of TMEM (256 arrivals)
   // Q/dO stages; in the two-pass form these are the Q ring, and do_full / do_empty the dO ring.
   auto qdo_full = [&](int s) { return bar0 + 8u * (10 + s); };
@@ -300,27 +305,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the Q lane and released by the softmax warps once they have read it.
   auto ld_full = [&](int x) { return bar0 + 8u * (14 + 2 * C::NSLOT + x); };
   auto ld_empty = [&](int x) { return bar0 + 8u * (16 + 2 * C::NSLOT + x); };
-  // Two-pass form, dK pass: stage 0 (64 KiB) becomes a ring of two 32 KiB tile slots.  In ring
-  // order, step i brings Q_i (for S^T), dO_i (for dP^T) and Q_{i-1} again (for dK_{i-1}, which
-  // runs once the softmax of step i - 1 is done): no tile stays resident from its S^T to its
-  // dK.  Each slot has one full and one empty barrier, so the MMA warp waits and commits once
-  // per tile (a commit between MMA groups costs the tensor pipe a drain).
+  // Two-pass form, dK pass: V moves to tensor memory, so both dV-pass stages (128 KiB) become a
+  // ring of four 32 KiB tile slots, filled Q_0 dO_0 Q_1 dO_1 ...  Q_i stays resident from its
+  // S^T to its dK (after the softmax of step i); dO_i is released by dP^T_i.  Each slot has one
+  // full and one empty barrier, so the MMA warp waits and commits once per tile (a commit
+  // between MMA groups costs the tensor pipe a drain).
   auto ring_full = [&](int r) { return bar0 + 8u * (18 + 2 * C::NSLOT + r); };
   auto ring_empty = [&](int r) { return bar0 + 8u * (22 + 2 * C::NSLOT + r); };
   const uint32_t dp_full = bar0 + 8u * (26 + 2 * C::NSLOT);  // dP^T of a dK-pass step is in TMEM
   const uint32_t dp_free = bar0 + 8u * (27 + 2 * C::NSLOT);  // ... and has been copied out (256)
-  constexpr int kRing = 2;
-  auto ring_addr = [&](int n) -> uint32_t { return sbase + C::OFF_SLOT0 + (n % kRing) * C::QT_BYTES; };
+  constexpr int kRing = 4;
+  // slots 0, 1: the first stage (Q, dO), slots 2, 3: the second stage, V's space in the fused form
+  auto ring_addr = [&](int n) -> uint32_t {
+    const int r = n % kRing;
+    return sbase + (r < 2 ? C::OFF_SLOT0 : C::OFF_V) + (r & 1) * C::QT_BYTES;
+  };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *red = misc_i + 4;  // [8]
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(v_full, C::TWO ? 2 : 1);  // two-pass: V arrives in two halves from two lanes
+    mbar_init(v_full, C::TWO ? kSoftmaxThreads : 1);  // two-pass: every softmax thread stores its part of V
     mbar_init(s_full, 1);
     mbar_init(p_ready, kSoftmaxThreads);
     mbar_init(mma_done, C::TWO ? 2 : 1);  // two-pass: dV / dQ (back warp) and dK (front warp)
     mbar_init(do0_free, 1);
+    if (C::TWO) mbar_init(do1_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty(0), kDrainThreads);  // every drain thread has read (its half of) the dQ tile
     mbar_init(dq_empty(1), kDrainThreads);
@@ -445,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < NCH; ++cc) {
           const int c = half * NCH + cc;
-          tmem_ld32(lane_addr + C::TM_S + c * 32, pf[cc]);
+          tmem_ld32(lane_addr + C::TM_SDP + c * 32, pf[cc]);
           tmem_wait_ld();
           reg_fence(pf[cc]);
           if (cc == NCH - 1) {
@@ -461,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < NCH; ++cc) {
           const int c = half * NCH + cc;
           uint32_t dr[32];
-          tmem_ld32(lane_addr + C::TM_DP + c * 32, dr);
+          tmem_ld32(lane_addr + C::TM_SDP + c * 32, dr);
           tmem_wait_ld();
           reg_fence(dr);
           if (cc == NCH - 1) {
@@ -535,6 +545,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(acc_free);
+        // V into tensor memory for the dK pass (A operand of dP^T): this thread's key row,
+        // its half of D as bf16 pairs (the last dV-pass S^T, which lived there, is read).
+        const uint4 *vsrc = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.v) + (size_t)b * p.v_sb +
+                                                            (size_t)(key_ok ? k : 0) * p.v_ss + (size_t)g * p.v_sh +
+                                                            half * (D / 2));
+#pragma unroll 1
+        for (int c = 0; c < D / 128; ++c) {
+          uint32_t vv[32];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint4 x = key_ok ? __ldg(vsrc + c * 8 + v) : make_uint4(0, 0, 0, 0);
+            vv[4 * v] = x.x;
+            vv[4 * v + 1] = x.y;
+            vv[4 * v + 2] = x.z;
+            vv[4 * v + 3] = x.w;
+          }
+          tmem_st32(lane_addr + C::TM_V + half * (D / 4) + c * 32, vv);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(v_full);
       }
     }
 
@@ -574,10 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegProducer));
     if (warp == 8 && C::TWO) {
       // ------------------------------------------------------------ TMA producers (two-pass)
-      // dV pass: lane 0 loads K, the Q ring and the LSE / D ring, lane 1 the dO ring.  Between
-      // the passes each lane loads half of V into the dV pass's second stage.  dK pass: lane 0
-      // alone fills the half-tile ring (Q_i, dO_i, Q_{i-1} again) and the LSE / D ring.  Every
-      // ring has one loader at a time and its waits run in phase order.
+      // dV pass: lane 0 loads K, the Q ring and the LSE / D ring, lane 1 the dO ring.  dK pass:
+      // lane 0 alone fills the tile ring (Q_i, dO_i) and the LSE / D ring; lane 1 hands the dV
+      // pass's dO stages over.  Every ring has one loader at a time and its waits run in phase
+      // order.
       const int u_last0 = ((nper + 1) >> 1) - 1;  // last dV-pass use of stage 0
       const int u_last1 = (nper >> 1) - 1;        // ... and of stage 1
       if (lane == 0) {
@@ -589,14 +620,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
         for (int c = 0; c < C::KCH; ++c) tma_load_4d(sbase + C::OFF_K + c * (kBK * 128), &tmK, kv_full, c * 64, k0, g, b);
         int n = 0;  // dK-pass ring position
-        // One Q or dO tile (rows q0 .. q0 + BQ - 1) into the next ring slot.  The two slots are
-        // stage 0 of the dV pass: the first use of slot 0 waits for its last Q to be released,
-        // that of slot 1 for its last dO.
+        // One Q or dO tile (rows q0 .. q0 + BQ - 1) into the next ring slot.  The first use of
+        // a slot waits for the dV pass's last use of that stage's Q (slots 0, 2) or dO (slots
+        // 1, 3; handed over by lane 1).
         auto ring_load = [&](const CUtensorMap *tm, int q0, int h) -> bool {
           const int r = n % kRing, u = n / kRing;
-          const bool ok = u == 0 ? (r == 0 ? mbar_wait(qdo_empty(0), u_last0 & 1, p.status)
-                                           : mbar_wait(do0_free, 0, p.status))
-                                 : mbar_wait(ring_empty(r), (u - 1) & 1, p.status);
+          bool ok = true;
+          if (u >= 1)
+            ok = mbar_wait(ring_empty(r), (u - 1) & 1, p.status);
+          else if (r == 0)
+            ok = mbar_wait(qdo_empty(0), u_last0 & 1, p.status);
+          else if (r == 1)
+            ok = mbar_wait(do0_free, 0, p.status);
+          else if (r == 2)
+            ok = u_last1 < 0 || mbar_wait(qdo_empty(1), u_last1 & 1, p.status);
+          else
+            ok = mbar_wait(do1_free, 0, p.status);
           if (!ok) return false;
           mbar_arrive_expect_tx(ring_full(r), C::QT_BYTES);
   #pragma unroll
@@ -605,8 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n;
           return true;
         };
-        for (int j = 0; j <= nsteps; ++j) {
-          if (j < nsteps) {  // LSE / D of step j first: the softmax needs them with S^T_j
+        for (int j = 0; j < nsteps; ++j) {
+          {  // LSE / D of step j first: the softmax needs them with S^T_j
             const int x = j & 1, h = step_h(j), q0 = step_q0(j);
             if (j >= 2 && !mbar_wait(ld_empty(x), ((j >> 1) - 1) & 1, p.status)) break;
             mbar_arrive_expect_tx(ld_full(x), 2 * BQ * 4);
@@ -622,21 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
               tma_load_4d(slot_addr(s) + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, step_q0(j), step_h(j), b);
-          } else if (j < nsteps) {
-            if (j == nper) {  // V[:, :128] into the dV pass's second Q stage
-              if (u_last1 >= 0 && !mbar_wait(qdo_empty(1), u_last1 & 1, p.status)) break;
-              mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
-  #pragma unroll
-              for (int c = 0; c < C::KCH / 2; ++c)
-                tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
-            }
-            // Q_i for S^T, dO_i for dP^T, Q_{i-1} again for dK of the previous step
+          } else {
+            // Q_i for S^T and dK, dO_i for dP^T
             const int h = step_h(j), q0 = step_q0(j);
             if (!ring_load(&tmQ, q0, h) || !ring_load(&tmdO, q0, h)) break;
-            if (j > nper && !ring_load(&tmQ, step_q0(j - 1), step_h(j - 1))) break;
-          }
-          if (j == nsteps && j > nper) {  // Q of the last step again, for its dK
-            if (!ring_load(&tmQ, step_q0(j - 1), step_h(j - 1))) break;
           }
         }
       } else if (lane == 1) {
@@ -650,14 +678,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < C::KCH; ++c)
             tma_load_4d(do_addr(s) + c * (BQ * 128), &tmdO, do_full(s), c * 64, step_q0(j), step_h(j), b);
         }
-        // V[:, 128:] into the dV pass's second dO stage
-        if (ok && nper > 0 && (u_last1 < 0 || mbar_wait(do_empty(1), u_last1 & 1, p.status))) {
-          mbar_arrive_expect_tx(v_full, C::KV_BYTES / 2);
-  #pragma unroll
-          for (int c = C::KCH / 2; c < C::KCH; ++c)
-            tma_load_4d(sbase + C::OFF_V + c * (kBK * 128), &tmV, v_full, c * 64, k0, g, b);
-          // the first dO stage, once its last dV-pass use is released, goes to the ring
-          if (mbar_wait(do_empty(0), u_last0 & 1, p.status)) mbar_arrive(do0_free);
+        // The dV pass's dO stages, once their last uses are released, go to the ring.
+        if (ok && nper > 0 && mbar_wait(do_empty(0), u_last0 & 1, p.status)) {
+          mbar_arrive(do0_free);
+          if (u_last1 < 0 || mbar_wait(do_empty(1), u_last1 & 1, p.status)) mbar_arrive(do1_free);
         }
       }
     } else if (warp == 8) {
@@ -759,15 +783,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = mbar_wait_warp(kv_full, 0, p.status);
         int dq_steps = 0;
         if constexpr (C::TWO) {
-          const int nB = nsteps - nper;  // dK-pass steps
           // Ring positions of dK-pass step i's tiles, in the order the loader fills the ring and
-          // the front warp reads it: Q_0 dO_0 | Q_1 dO_1 Qb_0 | Q_2 dO_2 Qb_1 | ... | Qb_{nB-1}
-          // (Qb: Q again, for dK).  A slot is refilled two positions later: Q_i where dO_{i-1}
-          // was (free after dP^T_{i-1}), dO_i where Qb_{i-2} was (after dK_{i-2}), Qb_{i-1} where
-          // Q_i was (after S^T_i).
-          auto pos_q = [&](int i) { return i == 0 ? 0 : 3 * i - 1; };
-          auto pos_do = [&](int i) { return i == 0 ? 1 : 3 * i; };
-          auto pos_qb = [&](int i) { return i + 1 < nB ? 3 * i + 4 : 3 * nB - 1; };
+          // the front warp reads it: Q_0 dO_0 Q_1 dO_1 ...; a slot is refilled four positions
+          // later (Q_{i+2} where Q_i was, free after dK_i; dO_{i+2} where dO_i was, after dP^T_i).
+          auto pos_q = [&](int i) { return 2 * i; };
+          auto pos_do = [&](int i) { return 2 * i + 1; };
           // dV of a dV-pass step: P^T from TMEM, dO of its slot; releases that dO slot.
           auto back_dv = [&](int jj) -> bool {
             const int s = slot_of(jj);
@@ -783,16 +803,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_w(mma_done);  // both arrivals of the step: no dK in the dV pass
             return true;
           };
-          // dK of a dK-pass step (front warp): Q of the step again, from its ring slot, in two
-          // N = 128 halves of D (each half's columns are a 16 KiB run of the tile).
+          // dK of a dK-pass step (front warp): from Q of the step, still in its ring slot (waited
+          // on by the step's S^T), in two N = 128 halves of D (each a 16 KiB run of the tile);
+          // releases the slot.
           auto mma_dk = [&](int jj) -> bool {
-            if (jj == nper) {  // dV has been stored: the accumulator is free for dK
-              if (!mbar_wait_warp(acc_free, 0, p.status)) return false;
-              tc_fence_after();
-            }
-            const int n = pos_qb(jj - nper), r = n % kRing;
-            if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
-            tc_fence_after();
+            const int n = pos_q(jj - nper), r = n % kRing;
   #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
               const uint64_t q_mn = sw128_desc(ring_addr(n) + hf * (C::QT_BYTES / 2), BQ * 128, 1024);
@@ -805,56 +820,81 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit_w(mma_done);
             return true;
           };
-          // dQ of a dK-pass step (back warp).
+          // dQ^T of a dK-pass step (back warp), one 128-row half of D at a time in the same 64
+          // columns, each once the drain has copied the previous half out.
           auto back_dq = [&]() -> bool {
-            if (!mma_dq(dq_steps)) return false;
-            mma_commit_w(dq_full);
+  #pragma unroll 1
+            for (int m = 0; m < 2; ++m) {
+              const int hh = 2 * dq_steps + m;
+              if (hh >= 1 && !mbar_wait_warp(dq_empty(0), (hh - 1) & 1, p.status)) return false;
+              tc_fence_after();
+              const uint64_t a_m = desc_at(dK_mn, (2 * m) * (kBK * 128));
+  #pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk)
+                mma_ss_w(tmem + C::TM_DQH, desc_at(a_m, kk * 2048), desc_at(dS_mn, kk * 2048), idDQ, kk > 0);
+              mma_commit_w(dq_full);
+            }
             ++dq_steps;
             mma_commit_w(mma_done);
             return true;
           };
-          // S^T (A = K) or dP^T (A = V) of a dK-pass step from the Q or dO tile at ring position
-          // n, whose slot is released once read.
-          auto front_ring = [&](uint64_t a_k, uint32_t d_col, int n) -> bool {
-            const int r = n % kRing;
-            if (!mbar_wait_warp(ring_full(r), (n / kRing) & 1, p.status)) return false;
+          // Waits for ring position n (the front warp is its only reader, in fill order).
+          auto ring_wait = [&](int n) -> bool {
+            if (!mbar_wait_warp(ring_full(n % kRing), (n / kRing) & 1, p.status)) return false;
             tc_fence_after();
-            mma_front(a_k, ring_addr(n), d_col);
-            mma_commit_w(ring_empty(r));
             return true;
           };
           if (!back_warp) {
             // Front: S^T of every step (dV pass: from its Q stage, which is free again right
-            // after) and dP^T of every dK-pass step, each as soon as the softmax has copied out
-            // the previous one, then dK of the previous dK-pass step: the softmax finds S^T and
-            // dP^T of a step in TMEM while dK / dQ of the step before run.  The front warp is
-            // the only reader of the ring, so every ring slot is waited on in fill order.
-            for (int j = 0; ok && j < nsteps; ++j) {
+            // after); in the dK pass S^T_i (once the softmax has copied dP^T_{i-1} out of the
+            // shared score buffer), dP^T_i = V dO_i^T with V in TMEM (once S^T_i is copied out),
+            // then dK of the previous step: the softmax works on a step while dK / dQ of the one
+            // before run.
+            for (int j = 0; ok && j < nper; ++j) {
               if (j >= 1 && !mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
-              if (j < nper) {
-                const int s = slot_of(j);
-                if (!mbar_wait_warp(qdo_full(s), use_of(j) & 1, p.status)) break;
-                tc_fence_after();
-                mma_front(dK_k, slot_addr(s), C::TM_S);
-                mma_commit_w(s_full);
-                mma_commit_w(qdo_empty(s));
-              } else {
-                const int i = j - nper;
-                if (!front_ring(dK_k, C::TM_S, pos_q(i))) break;
-                mma_commit_w(s_full);
-                if (i == 0 && !mbar_wait_warp(v_full, 0, p.status)) break;
-                if (i >= 1 && !mbar_wait_warp(dp_free, (i - 1) & 1, p.status)) break;
-                tc_fence_after();
-                if (!front_ring(dV_k, C::TM_DP, pos_do(i))) break;
-                mma_commit_w(dp_full);
-                if (i >= 1) {  // dK of the previous step once its dS is in shared memory
-                  if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
-                  tc_fence_after();
-                  if (!mma_dk(j - 1)) break;
+              const int s = slot_of(j);
+              if (!mbar_wait_warp(qdo_full(s), use_of(j) & 1, p.status)) break;
+              tc_fence_after();
+              mma_front(dK_k, slot_addr(s), C::TM_S);
+              mma_commit_w(s_full);
+              mma_commit_w(qdo_empty(s));
+            }
+            for (int j = nper; ok && j < nsteps; ++j) {
+              const int i = j - nper;
+              if (i == 0) {
+                // the last dV-pass scores are read, and dV is stored (its accumulator becomes
+                // dK's, P's columns become the score buffer)
+                if (nper >= 1 && !mbar_wait_warp(sdp_free, (nper - 1) & 1, p.status)) break;
+                if (!mbar_wait_warp(acc_free, 0, p.status)) break;
+              } else if (!mbar_wait_warp(dp_free, (i - 1) & 1, p.status)) {
+                break;
+              }
+              if (!ring_wait(pos_q(i))) break;
+              mma_front(dK_k, ring_addr(pos_q(i)), C::TM_SDP);
+              mma_commit_w(s_full);
+              if (!mbar_wait_warp(sdp_free, j & 1, p.status)) break;
+              if (i == 0 && !mbar_wait_warp(v_full, 0, p.status)) break;
+              if (!ring_wait(pos_do(i))) break;
+              {  // dP^T = V dO^T: A = V from TMEM (bf16 pairs along D), B = dO (K-major chunks)
+                uint64_t b_k = sw128_desc(ring_addr(pos_do(i)), 16, 1024);
+  #pragma unroll 1
+                for (int c = 0; c < D / 64; ++c) {
+  #pragma unroll
+                  for (int k4 = 0; k4 < 4; ++k4)
+                    mma_ts_w(tmem + C::TM_SDP, tmem + C::TM_V + c * 32 + k4 * 8, desc_at(b_k, k4 * 32), idST,
+                             (c | k4) != 0 ? 1u : 0u);
+                  b_k = desc_at(b_k, BQ * 128);
                 }
               }
+              mma_commit_w(ring_empty(pos_do(i) % kRing));
+              mma_commit_w(dp_full);
+              if (i >= 1) {  // dK of the previous step once its dS is in shared memory
+                if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+                tc_fence_after();
+                if (!mma_dk(j - 1)) break;
+              }
             }
-            if (ok && nsteps > 0 && mbar_wait_warp(p_ready, (nsteps - 1) & 1, p.status)) {
+            if (ok && nsteps > nper && mbar_wait_warp(p_ready, (nsteps - 1) & 1, p.status)) {
               tc_fence_after();
               mma_dk(nsteps - 1);
             }
@@ -935,6 +975,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nsteps; ++j) {
       if (step_kind(j) == 1) continue;
       const int h = step_h(j), q0 = step_q0(j);
+      if constexpr (C::TWO) {
+        // dK pass: one 128-row half of dQ^T at a time in 64 columns; each half is released
+        // once its two 32-query chunks are in registers, then leaves through [128 d, 32 q]
+        // boxes staged in shared memory for bulk reduce-adds into the fp32 accumulator.
+        bool okh = true;
+#pragma unroll 1
+        for (int m = 0; m < 2 && okh; ++m) {
+          const int hh = 2 * dq_steps + m;
+          if (t == 0) *flag = mbar_wait(dq_full, hh & 1, p.status) ? 1 : 0;
+          named_bar<2, 128>();
+          okh = *flag != 0;
+          if (!okh) break;
+          tc_fence_after();
+          uint32_t v0[32], v1[32];
+          tmem_ld32(lane_addr + C::TM_DQH, v0);
+          tmem_ld32(lane_addr + C::TM_DQH + 32, v1);
+          tmem_wait_ld();
+          reg_fence(v0);
+          reg_fence(v1);
+          tc_fence_before();
+          mbar_arrive(dq_empty(0));  // this thread is done with the half
+#pragma unroll
+          for (int cq = 0; cq < 2; ++cq) {
+            if (t == 0) bulk_wait_read_all();  // the previous box has left shared memory
+            named_bar<2, 128>();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) stage[e * 128 + row] = __uint_as_float(cq == 0 ? v0[e] : v1[e]);
+            fence_async_smem();
+            named_bar<2, 128>();
+            if (t == 0) {
+              tma_reduce_add_4d(&tmDQ, stage_a, m * 128, q0 + cq * 32, h, b);
+              bulk_commit();
+            }
+          }
+        }
+        if (!okh) break;
+        ++dq_steps;
+        continue;
+      }
       if (t == 0) *flag = mbar_wait(dq_full, dq_steps & 1, p.status) ? 1 : 0;
       named_bar<2, 128>();
       if (!*flag) break;

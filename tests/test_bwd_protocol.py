@@ -269,3 +269,191 @@ def test_model_flags_the_shared_ring_layout():
 def test_greedy_schedule_finishes(nper):
     finished, hazards = simulate(nper, "single_reader", random.Random(nper))
     assert finished and not hazards
+
+
+def simulate_vtmem(nper, rng):
+    """The head-dim-256 protocol with V in tensor memory during the dK pass: a four-slot ring
+    of whole Q / dO tiles (Q_i stays resident from S^T_i to dK_i), S^T and dP^T sharing one
+    score buffer, dQ^T drained one 128-row half at a time.  Returns (finished, hazards)."""
+    nsteps, nB = 2 * nper, nper
+    need = defaultdict(lambda: 1)
+    need.update({"mma_done": 2, "fin_done": 2, "sdp_free": 1, "p_ready": 1, "acc_free": 1, "v_full": 1})
+    count, done, hazards = defaultdict(int), defaultdict(int), []
+
+    def arrive(b):
+        count[b] += 1
+        if count[b] == need[b]:
+            count[b] = 0
+            done[b] += 1
+
+    u_last0, u_last1 = ((nper + 1) >> 1) - 1, (nper >> 1) - 1
+
+    def loader0():
+        yield ("arrive", "kv_full")
+        n = 0
+        for j in range(nsteps):
+            if j >= 2:
+                yield ("wait", f"ld_empty{j & 1}", (j >> 1) - 1)
+            yield ("arrive", f"ld_full{j & 1}")
+            if j < nper:
+                s, u = j & 1, j >> 1
+                if u >= 1:
+                    yield ("wait", f"qdo_empty{s}", u - 1)
+                yield ("arrive", f"qdo_full{s}")
+                continue
+            for _ in range(2):  # Q_i, dO_i
+                r, u = n % 4, n // 4
+                if u == 0:
+                    if r == 0:
+                        yield ("wait", "qdo_empty0", u_last0)
+                    elif r == 1:
+                        yield ("wait", "do0_free", 0)
+                    elif r == 2:
+                        if u_last1 >= 0:
+                            yield ("wait", "qdo_empty1", u_last1)
+                    else:
+                        yield ("wait", "do1_free", 0)
+                else:
+                    yield ("wait", f"ring_empty{r}", u - 1)
+                yield ("arrive", f"ring_full{r}")
+                n += 1
+
+    def loader1():
+        for j in range(nper):
+            s, u = j & 1, j >> 1
+            if u >= 1:
+                yield ("wait", f"do_empty{s}", u - 1)
+            yield ("arrive", f"do_full{s}")
+        if nper > 0:
+            yield ("wait", "do_empty0", u_last0)
+            yield ("arrive", "do0_free")
+            if u_last1 >= 0:
+                yield ("wait", "do_empty1", u_last1)
+            yield ("arrive", "do1_free")
+
+    def front():
+        yield ("wait", "kv_full", 0)
+        for j in range(nper):
+            if j >= 1:
+                yield ("wait", "sdp_free", j - 1)
+            yield ("wait", f"qdo_full{j & 1}", j >> 1)
+            yield ("arrive", "s_full")
+            yield ("arrive", f"qdo_empty{j & 1}")
+
+        def dk(i):
+            yield ("wait", "p_ready", nper + i)
+            yield ("arrive", f"ring_empty{(2 * i) % 4}")
+            yield ("arrive", "mma_done")
+
+        for i in range(nB):
+            j = nper + i
+            if i == 0:
+                yield ("wait", "sdp_free", nper - 1)
+                yield ("wait", "acc_free", 0)
+            else:
+                yield ("wait", "dp_free", i - 1)
+            yield ("wait", f"ring_full{(2 * i) % 4}", (2 * i) // 4)
+            yield ("arrive", "s_full")
+            yield ("wait", "sdp_free", j)
+            if i == 0:
+                yield ("wait", "v_full", 0)
+            yield ("wait", f"ring_full{(2 * i + 1) % 4}", (2 * i + 1) // 4)
+            yield ("arrive", f"ring_empty{(2 * i + 1) % 4}")
+            yield ("arrive", "dp_full")
+            if i >= 1:
+                yield from dk(i - 1)
+        if nB > 0:
+            yield from dk(nB - 1)
+        yield ("arrive", "fin_done")
+
+    def back():
+        yield ("wait", "kv_full", 0)
+        h = 0
+        for j in range(1, nsteps + 1):
+            yield ("wait", "p_ready", j - 1)
+            jj = j - 1
+            if jj < nper:
+                yield ("wait", f"do_full{jj & 1}", jj >> 1)
+                yield ("arrive", f"do_empty{jj & 1}")
+                yield ("arrive", "mma_done")
+                yield ("arrive", "mma_done")
+                continue
+            for _ in range(2):
+                if h >= 1:
+                    yield ("wait", "dq_empty", h - 1)
+                yield ("arrive", "dq_full")
+                h += 1
+            yield ("arrive", "mma_done")
+        yield ("arrive", "fin_done")
+
+    def softmax():
+        for j in range(nsteps):
+            yield ("wait", "s_full", j)
+            yield ("wait", f"ld_full{j & 1}", j >> 1)
+            yield ("arrive", "sdp_free")
+            if j >= nper:
+                yield ("wait", "dp_full", j - nper)
+                yield ("arrive", "dp_free")
+            yield ("arrive", f"ld_empty{j & 1}")
+            if j >= 1:
+                yield ("wait", "mma_done", j - 1)
+            yield ("arrive", "p_ready")
+            if j == nper - 1:
+                yield ("wait", "mma_done", j)
+                yield ("arrive", "acc_free")
+                yield ("arrive", "v_full")
+        if nsteps > 0:
+            yield ("wait", "fin_done", 0)
+
+    def drain():
+        for h in range(2 * nB):
+            yield ("wait", "dq_full", h)
+            yield ("arrive", "dq_empty")
+
+    return run_agents({"loader0": loader0(), "loader1": loader1(), "front": front(), "back": back(),
+                       "softmax": softmax(), "drain": drain()}, arrive, done, hazards, rng)
+
+
+def run_agents(agents, arrive, done, hazards, rng):
+    pending = dict.fromkeys(agents)
+    finished = set()
+    while len(finished) < len(agents):
+        progress = False
+        turn = list(agents)
+        rng.shuffle(turn)
+        for name in turn:
+            if name in finished:
+                continue
+            for _ in range(rng.randint(1, 8)):
+                op = pending[name]
+                if op is None:
+                    try:
+                        op = pending[name] = next(agents[name])
+                    except StopIteration:
+                        finished.add(name)
+                        progress = True
+                        break
+                if op[0] == "arrive":
+                    arrive(op[1])
+                    pending[name] = None
+                    progress = True
+                    continue
+                _, bar, phase = op
+                if done[bar] not in (phase, phase + 1):
+                    hazards.append((name, bar, phase, done[bar]))
+                if (done[bar] & 1) != (phase & 1):
+                    pending[name] = None
+                    progress = True
+                else:
+                    break
+        if not progress:
+            return False, hazards
+    return True, hazards
+
+
+def test_vtmem_protocol_never_deadlocks_or_aliases():
+    rng = random.Random(4321)
+    for trial in range(1500):
+        nper = STEP_COUNTS[trial % len(STEP_COUNTS)]
+        finished, hazards = simulate_vtmem(nper, rng)
+        assert finished and not hazards, (nper, hazards[:3])
