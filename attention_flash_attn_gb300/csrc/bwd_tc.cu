@@ -996,16 +996,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           reg_fence(v1);
           tc_fence_before();
           mbar_arrive(dq_empty(0));  // this thread is done with the half
+          // four [128 d, 16 q] boxes through two alternating 8 KiB buffers, so that staging
+          // one box overlaps the reduce-add of the one before
 #pragma unroll
-          for (int cq = 0; cq < 2; ++cq) {
-            if (t == 0) bulk_wait_read_all();  // the previous box has left shared memory
+          for (int bx = 0; bx < 4; ++bx) {
+            const int bf = bx & 1;
+            if (t == 0) bulk_wait_read_but_one();  // the box two back has left this buffer
             named_bar<2, 128>();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) stage[e * 128 + row] = __uint_as_float(cq == 0 ? v0[e] : v1[e]);
+            for (int e = 0; e < 16; ++e)
+              stage[bf * 2048 + e * 128 + row] = __uint_as_float(bx < 2 ? v0[(bx & 1) * 16 + e] : v1[(bx & 1) * 16 + e]);
             fence_async_smem();
             named_bar<2, 128>();
             if (t == 0) {
-              tma_reduce_add_4d(&tmDQ, stage_a, m * 128, q0 + cq * 32, h, b);
+              tma_reduce_add_4d(&tmDQ, stage_a + bf * 8192, m * 128, q0 + bx * 16, h, b);
               bulk_commit();
             }
           }
@@ -1096,7 +1100,8 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
       !make_tmap_bshd(&tv, p.v, C::D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, kBK) ||
       !make_tmap_bshd(&tdo, p.dO, C::D, p.Sq, p.Hq, p.B, (long long)p.Hq * C::D, C::D,
                       (long long)p.Sq * p.Hq * C::D, C::BQ) ||
-      !make_tmap_f32_bshd(&tdq, p.dQacc, C::D, p.Sq, p.Hq, p.B, C::DQT ? 128 : 32, C::DQT ? 32 : 128, !C::DQT))
+      !make_tmap_f32_bshd(&tdq, p.dQacc, C::D, p.Sq, p.Hq, p.B, C::DQT ? 128 : 32, C::DQT ? (C::TWO ? 16 : 32) : 128,
+                          !C::DQT))
     return cudaErrorInvalidValue;
   auto kern = p.cap > 0.f ? bwd_tc_kernel<C, true> : bwd_tc_kernel<C, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
