@@ -847,9 +847,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!back_warp) {
             // Front: S^T of every step (dV pass: from its Q stage, which is free again right
             // after); in the dK pass S^T_i (once the softmax has copied dP^T_{i-1} out of the
-            // shared score buffer), dP^T_i = V dO_i^T with V in TMEM (once S^T_i is copied out),
-            // then dK of the previous step: the softmax works on a step while dK / dQ of the one
-            // before run.
+            // shared score buffer), dK of the previous step (once its dS is in), then
+            // dP^T_i = V dO_i^T with V in TMEM (once S^T_i is copied out): the softmax works on a
+            // step while dK / dQ of the one before run.
             for (int j = 0; ok && j < nper; ++j) {
               if (j >= 1 && !mbar_wait_warp(sdp_free, (j - 1) & 1, p.status)) break;
               const int s = slot_of(j);
@@ -872,6 +872,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ring_wait(pos_q(i))) break;
               mma_front(dK_k, ring_addr(pos_q(i)), C::TM_SDP);
               mma_commit_w(s_full);
+              if (i >= 1) {  // dK of the previous step as soon as its dS is in: frees its Q slot
+                if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+                tc_fence_after();
+                if (!mma_dk(j - 1)) break;
+              }
               if (!mbar_wait_warp(sdp_free, j & 1, p.status)) break;
               if (i == 0 && !mbar_wait_warp(v_full, 0, p.status)) break;
               if (!ring_wait(pos_do(i))) break;
@@ -888,11 +893,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               mma_commit_w(ring_empty(pos_do(i) % kRing));
               mma_commit_w(dp_full);
-              if (i >= 1) {  // dK of the previous step once its dS is in shared memory
-                if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
-                tc_fence_after();
-                if (!mma_dk(j - 1)) break;
-              }
             }
             if (ok && nsteps > nper && mbar_wait_warp(p_ready, (nsteps - 1) & 1, p.status)) {
               tc_fence_after();

@@ -354,14 +354,14 @@ def simulate_vtmem(nper, rng):
                 yield ("wait", "dp_free", i - 1)
             yield ("wait", f"ring_full{(2 * i) % 4}", (2 * i) // 4)
             yield ("arrive", "s_full")
+            if i >= 1:  # dK of the previous step as soon as its dS is in: frees its Q slot
+                yield from dk(i - 1)
             yield ("wait", "sdp_free", j)
             if i == 0:
                 yield ("wait", "v_full", 0)
             yield ("wait", f"ring_full{(2 * i + 1) % 4}", (2 * i + 1) // 4)
             yield ("arrive", f"ring_empty{(2 * i + 1) % 4}")
             yield ("arrive", "dp_full")
-            if i >= 1:
-                yield from dk(i - 1)
         if nB > 0:
             yield from dk(nB - 1)
         yield ("arrive", "fin_done")
