@@ -70,7 +70,11 @@ struct BwdCfg {
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
   static constexpr int OFF_LD = OFF_DQS + DQS_BYTES;  // per slot: LSE*log2e [BQ], D [BQ]
   static constexpr int OFF_BAR = OFF_LD + NSLOT * 2 * BQ * 4;
-  static constexpr int NBAR = 12 + 2 * NSLOT + (TWO ? 19 : 0);  // + dQ half-1 release, dO stage hand-overs
+  static constexpr int NBAR = 12 + 2 * NSLOT + (TWO ? 23 : 0);  // + dQ half-1 release, dO hand-over, dS buffers
+  // Two-pass form, dK pass: the dV pass's second dO stage holds the second dS^T buffer and two
+  // more dQ staging boxes.
+  static constexpr int OFF_DS1 = OFF_V + QT_BYTES;
+  static constexpr int OFF_DQS2 = OFF_DS1 + DS_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   // TMEM columns
@@ -88,6 +92,7 @@ struct BwdCfg {
   static_assert(TM_DQ + DQ_COLS <= 512, "TMEM budget");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(!TWO || SLOT_BYTES == KV_BYTES, "the V slot must hold one Q/dO stage");
+  static_assert(!TWO || DS_BYTES + DQS_BYTES <= QT_BYTES, "second dS^T buffer and staging fit a dO stage");
   static_assert(!DQT || D % 128 == 0, "transposed dQ needs whole 128-row halves of D");
   static_assert(DQT || (BQ == 128 && D == 64), "row-major dQ is the D = 64, BQ = 128 form");
   static_assert(BQ % 64 == 0, "dS^T rows are whole 128-byte swizzle rows");
@@ -294,7 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // that stage's releases in order, hands it to lane 0 through this single-phase barrier (a
   // waiter that has not seen a barrier's earlier phases could mistake one for the next).
   const uint32_t do0_free = bar0 + 8u * (C::NBAR - 2);
-  const uint32_t do1_free = bar0 + 8u * (C::NBAR - 3);  // the same for the second dO stage
+  // Two-pass form, dK pass: dS^T is double-buffered (buffer i & 1 for step i).  p_ready_b(x):
+  // the softmax has stored buffer x; dsb_done(x): dK and dQ of the step that read buffer x have
+  // completed.  Per-buffer barriers keep a barrier's phases two steps apart.
+  auto p_ready_b = [&](int x) { return bar0 + 8u * (C::NBAR - 7 + x); };
+  auto dsb_done = [&](int x) { return bar0 + 8u * (C::NBAR - 5 + x); };
   const uint32_t sdp_free = bar0 + 72u;  // S^T / dP^T copied out of TMEM (256 arrivals)
   // Q/dO stages; in the two-pass form these are the Q ring, and do_full / do_empty the dO ring.
   auto qdo_full = [&](int s) { return bar0 + 8u * (10 + s); };
@@ -305,20 +314,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the Q lane and released by the softmax warps once they have read it.
   auto ld_full = [&](int x) { return bar0 + 8u * (14 + 2 * C::NSLOT + x); };
   auto ld_empty = [&](int x) { return bar0 + 8u * (16 + 2 * C::NSLOT + x); };
-  // Two-pass form, dK pass: V moves to tensor memory, so both dV-pass stages (128 KiB) become a
-  // ring of four 32 KiB tile slots, filled Q_0 dO_0 Q_1 dO_1 ...  Q_i stays resident from its
-  // S^T to its dK (after the softmax of step i); dO_i is released by dP^T_i.  Each slot has one
-  // full and one empty barrier, so the MMA warp waits and commits once per tile (a commit
-  // between MMA groups costs the tensor pipe a drain).
+  // Two-pass form, dK pass: V moves to tensor memory, and the dV pass's stages become two Q tile
+  // slots (Q_i in slot i & 1, resident from its S^T to its dK after the softmax of step i) and
+  // one dO slot (released by dP^T_i); the second dO stage holds the second dS^T buffer and more
+  // dQ staging.  Each slot has one full and one empty barrier, so the MMA warp waits and
+  // commits once per tile (a commit between MMA groups costs the tensor pipe a drain).
   auto ring_full = [&](int r) { return bar0 + 8u * (18 + 2 * C::NSLOT + r); };
   auto ring_empty = [&](int r) { return bar0 + 8u * (22 + 2 * C::NSLOT + r); };
   const uint32_t dp_full = bar0 + 8u * (26 + 2 * C::NSLOT);  // dP^T of a dK-pass step is in TMEM
   const uint32_t dp_free = bar0 + 8u * (27 + 2 * C::NSLOT);  // ... and has been copied out (256)
-  constexpr int kRing = 4;
-  // slots 0, 1: the first stage (Q, dO), slots 2, 3: the second stage, V's space in the fused form
-  auto ring_addr = [&](int n) -> uint32_t {
-    const int r = n % kRing;
-    return sbase + (r < 2 ? C::OFF_SLOT0 : C::OFF_V) + (r & 1) * C::QT_BYTES;
+  // slots 0, 1 (Q): the first stage's Q and dO; slot 2 (dO): the second stage's Q
+  auto ring_addr = [&](int r) -> uint32_t {
+    return sbase + (r < 2 ? C::OFF_SLOT0 + r * C::QT_BYTES : C::OFF_V);
   };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *red = misc_i + 4;  // [8]
@@ -330,7 +337,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(p_ready, kSoftmaxThreads);
     mbar_init(mma_done, C::TWO ? 2 : 1);  // two-pass: dV / dQ (back warp) and dK (front warp)
     mbar_init(do0_free, 1);
-    if (C::TWO) mbar_init(do1_free, 1);
+    if (C::TWO) {
+      for (int x = 0; x < 2; ++x) {
+        mbar_init(p_ready_b(x), kSoftmaxThreads);
+        mbar_init(dsb_done(x), 2);  // dK (front warp) and dQ (back warp)
+      }
+    }
     mbar_init(dq_full, 1);
     mbar_init(dq_empty(0), kDrainThreads);  // every drain thread has read (its half of) the dQ tile
     mbar_init(dq_empty(1), kDrainThreads);
@@ -348,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (C::TWO) {
-      for (int r = 0; r < kRing; ++r) {
+      for (int r = 0; r < 3; ++r) {
         mbar_init(ring_full(r), 1);
         mbar_init(ring_empty(r), 1);
       }
@@ -503,16 +515,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (C::TWO) mbar_arrive(ld_empty(j & 1));  // LSE / D of this step have been read
-      // ... and stored once those MMAs are done with the buffers.
-      if (j >= 1 && !mbar_wait(mma_done, (j - 1) & 1, p.status)) { ok = false; break; }
+      // ... and stored once those MMAs are done with the buffers (the dK pass double-buffers
+      // dS^T: buffer i & 1 was last read by dK / dQ of step i - 2).
+      const int ib = j - nper;
+      if (C::TWO && kind == 2) {
+        if (ib >= 2 && !mbar_wait(dsb_done(ib & 1), ((ib >> 1) - 1) & 1, p.status)) { ok = false; break; }
+      } else if (j >= 1 && !mbar_wait(mma_done, (j - 1) & 1, p.status)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
+      uint8_t *ds_buf = (C::TWO && kind == 2 && (ib & 1)) ? smem + C::OFF_DS1 + r * 128 : ds_row;
 #pragma unroll
       for (int cc = 0; cc < NCH; ++cc) {
         const int c = half * NCH + cc;
         if (kind != 2) tmem_st16(lane_addr + C::TM_P + c * 16, pk[cc]);
         if (kind != 1) {
           // 32 queries = 64 bytes = four 16-byte units of this row, swizzled by (row & 7)
-          uint8_t *chunk = ds_row + (c >> 1) * (kBK * 128);
+          uint8_t *chunk = ds_buf + (c >> 1) * (kBK * 128);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int unit = ((c & 1) * 4 + v) ^ (r & 7);
@@ -524,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(p_ready);
+      mbar_arrive((C::TWO && kind == 2) ? p_ready_b(ib & 1) : p_ready);
 
       if (C::TWO && j == nper - 1) {
         // End of the dV pass: store dV (this warp's half of the columns), then hand the
@@ -619,12 +639,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(kv_full, C::KV_BYTES);
   #pragma unroll
         for (int c = 0; c < C::KCH; ++c) tma_load_4d(sbase + C::OFF_K + c * (kBK * 128), &tmK, kv_full, c * 64, k0, g, b);
-        int n = 0;  // dK-pass ring position
-        // One Q or dO tile (rows q0 .. q0 + BQ - 1) into the next ring slot.  The first use of
-        // a slot waits for the dV pass's last use of that stage's Q (slots 0, 2) or dO (slots
-        // 1, 3; handed over by lane 1).
-        auto ring_load = [&](const CUtensorMap *tm, int q0, int h) -> bool {
-          const int r = n % kRing, u = n / kRing;
+        // One Q or dO tile (rows q0 .. q0 + BQ - 1) into ring slot r for its use u.  The first
+        // use of a slot waits for the dV pass's last use of that region: the first stage's Q
+        // (slot 0) and dO (slot 1, handed over by lane 1), the second stage's Q (slot 2).
+        auto ring_load = [&](const CUtensorMap *tm, int r, int u, int q0, int h) -> bool {
           bool ok = true;
           if (u >= 1)
             ok = mbar_wait(ring_empty(r), (u - 1) & 1, p.status);
@@ -632,16 +650,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(qdo_empty(0), u_last0 & 1, p.status);
           else if (r == 1)
             ok = mbar_wait(do0_free, 0, p.status);
-          else if (r == 2)
-            ok = u_last1 < 0 || mbar_wait(qdo_empty(1), u_last1 & 1, p.status);
           else
-            ok = mbar_wait(do1_free, 0, p.status);
+            ok = u_last1 < 0 || mbar_wait(qdo_empty(1), u_last1 & 1, p.status);
           if (!ok) return false;
           mbar_arrive_expect_tx(ring_full(r), C::QT_BYTES);
   #pragma unroll
           for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(ring_addr(n) + c * (BQ * 128), tm, ring_full(r), c * 64, q0, h, b);
-          ++n;
+            tma_load_4d(ring_addr(r) + c * (BQ * 128), tm, ring_full(r), c * 64, q0, h, b);
           return true;
         };
         for (int j = 0; j < nsteps; ++j) {
@@ -662,9 +677,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < C::KCH; ++c)
               tma_load_4d(slot_addr(s) + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, step_q0(j), step_h(j), b);
           } else {
-            // Q_i for S^T and dK, dO_i for dP^T
-            const int h = step_h(j), q0 = step_q0(j);
-            if (!ring_load(&tmQ, q0, h) || !ring_load(&tmdO, q0, h)) break;
+            // Q_i (slot i & 1) for S^T and dK, dO_i (slot 2) for dP^T
+            const int i = j - nper, h = step_h(j), q0 = step_q0(j);
+            if (!ring_load(&tmQ, i & 1, i >> 1, q0, h) || !ring_load(&tmdO, 2, i, q0, h)) break;
           }
         }
       } else if (lane == 1) {
@@ -678,11 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < C::KCH; ++c)
             tma_load_4d(do_addr(s) + c * (BQ * 128), &tmdO, do_full(s), c * 64, step_q0(j), step_h(j), b);
         }
-        // The dV pass's dO stages, once their last uses are released, go to the ring.
-        if (ok && nper > 0 && mbar_wait(do_empty(0), u_last0 & 1, p.status)) {
-          mbar_arrive(do0_free);
-          if (u_last1 < 0 || mbar_wait(do_empty(1), u_last1 & 1, p.status)) mbar_arrive(do1_free);
-        }
+        // The first dO stage, once its last dV-pass use is released, becomes Q slot 1.  (The
+        // second dO stage's new uses start after the dV pass's last MMAs have completed.)
+        if (ok && nper > 0 && mbar_wait(do_empty(0), u_last0 & 1, p.status)) mbar_arrive(do0_free);
       }
     } else if (warp == 8) {
       // ------------------------------------------------------------ TMA producer
@@ -783,11 +796,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = mbar_wait_warp(kv_full, 0, p.status);
         int dq_steps = 0;
         if constexpr (C::TWO) {
-          // Ring positions of dK-pass step i's tiles, in the order the loader fills the ring and
-          // the front warp reads it: Q_0 dO_0 Q_1 dO_1 ...; a slot is refilled four positions
-          // later (Q_{i+2} where Q_i was, free after dK_i; dO_{i+2} where dO_i was, after dP^T_i).
-          auto pos_q = [&](int i) { return 2 * i; };
-          auto pos_do = [&](int i) { return 2 * i + 1; };
+          // dK-pass step i: Q_i in ring slot i & 1 (its use i >> 1), dO_i in slot 2 (use i), dS^T
+          // in buffer i & 1.
+          const uint64_t dS_k1 = sw128_desc(sbase + C::OFF_DS1, 16, 1024);
+          const uint64_t dS_mn1 = sw128_desc(sbase + C::OFF_DS1, kBK * 128, 1024);
           // dV of a dV-pass step: P^T from TMEM, dO of its slot; releases that dO slot.
           auto back_dv = [&](int jj) -> bool {
             const int s = slot_of(jj);
@@ -807,22 +819,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           // on by the step's S^T), in two N = 128 halves of D (each a 16 KiB run of the tile);
           // releases the slot.
           auto mma_dk = [&](int jj) -> bool {
-            const int n = pos_q(jj - nper), r = n % kRing;
+            const int i = jj - nper, r = i & 1;
+            const uint64_t dsk = r ? dS_k1 : dS_k;
   #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
-              const uint64_t q_mn = sw128_desc(ring_addr(n) + hf * (C::QT_BYTES / 2), BQ * 128, 1024);
+              const uint64_t q_mn = sw128_desc(ring_addr(r) + hf * (C::QT_BYTES / 2), BQ * 128, 1024);
   #pragma unroll
               for (int kk = 0; kk < BQ / 16; ++kk)
-                mma_ss_w(tmem + C::TM_DK + hf * (D / 2), desc_at(dS_k, (kk >> 2) * (kBK * 128) + (kk & 3) * 32),
+                mma_ss_w(tmem + C::TM_DK + hf * (D / 2), desc_at(dsk, (kk >> 2) * (kBK * 128) + (kk & 3) * 32),
                          desc_at(q_mn, kk * 2048), idKh, (jj > nper || kk > 0) ? 1u : 0u);
             }
             mma_commit_w(ring_empty(r));
-            mma_commit_w(mma_done);
+            mma_commit_w(dsb_done(r));
             return true;
           };
           // dQ^T of a dK-pass step (back warp), one 128-row half of D at a time in the same 64
           // columns, each once the drain has copied the previous half out.
           auto back_dq = [&]() -> bool {
+            const int x = dq_steps & 1;  // dK-pass step dq_steps reads dS^T buffer x
+            const uint64_t dsmn = x ? dS_mn1 : dS_mn;
   #pragma unroll 1
             for (int m = 0; m < 2; ++m) {
               const int hh = 2 * dq_steps + m;
@@ -831,16 +846,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t a_m = desc_at(dK_mn, (2 * m) * (kBK * 128));
   #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
-                mma_ss_w(tmem + C::TM_DQH, desc_at(a_m, kk * 2048), desc_at(dS_mn, kk * 2048), idDQ, kk > 0);
+                mma_ss_w(tmem + C::TM_DQH, desc_at(a_m, kk * 2048), desc_at(dsmn, kk * 2048), idDQ, kk > 0);
               mma_commit_w(dq_full);
             }
             ++dq_steps;
-            mma_commit_w(mma_done);
+            mma_commit_w(dsb_done(x));
             return true;
           };
-          // Waits for ring position n (the front warp is its only reader, in fill order).
-          auto ring_wait = [&](int n) -> bool {
-            if (!mbar_wait_warp(ring_full(n % kRing), (n / kRing) & 1, p.status)) return false;
+          // Waits for use u of ring slot r (the front warp is its only reader, in fill order).
+          auto ring_wait = [&](int r, int u) -> bool {
+            if (!mbar_wait_warp(ring_full(r), u & 1, p.status)) return false;
             tc_fence_after();
             return true;
           };
@@ -869,19 +884,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else if (!mbar_wait_warp(dp_free, (i - 1) & 1, p.status)) {
                 break;
               }
-              if (!ring_wait(pos_q(i))) break;
-              mma_front(dK_k, ring_addr(pos_q(i)), C::TM_SDP);
+              if (!ring_wait(i & 1, i >> 1)) break;
+              mma_front(dK_k, ring_addr(i & 1), C::TM_SDP);
               mma_commit_w(s_full);
               if (i >= 1) {  // dK of the previous step as soon as its dS is in: frees its Q slot
-                if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+                if (!mbar_wait_warp(p_ready_b((i - 1) & 1), ((i - 1) >> 1) & 1, p.status)) break;
                 tc_fence_after();
                 if (!mma_dk(j - 1)) break;
               }
               if (!mbar_wait_warp(sdp_free, j & 1, p.status)) break;
               if (i == 0 && !mbar_wait_warp(v_full, 0, p.status)) break;
-              if (!ring_wait(pos_do(i))) break;
+              if (!ring_wait(2, i)) break;
               {  // dP^T = V dO^T: A = V from TMEM (bf16 pairs along D), B = dO (K-major chunks)
-                uint64_t b_k = sw128_desc(ring_addr(pos_do(i)), 16, 1024);
+                uint64_t b_k = sw128_desc(ring_addr(2), 16, 1024);
   #pragma unroll 1
                 for (int c = 0; c < D / 64; ++c) {
   #pragma unroll
@@ -891,19 +906,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                   b_k = desc_at(b_k, BQ * 128);
                 }
               }
-              mma_commit_w(ring_empty(pos_do(i) % kRing));
+              mma_commit_w(ring_empty(2));
               mma_commit_w(dp_full);
             }
-            if (ok && nsteps > nper && mbar_wait_warp(p_ready, (nsteps - 1) & 1, p.status)) {
+            const int nB = nsteps - nper;
+            if (ok && nB > 0 && mbar_wait_warp(p_ready_b((nB - 1) & 1), ((nB - 1) >> 1) & 1, p.status)) {
               tc_fence_after();
               mma_dk(nsteps - 1);
             }
           } else {
             // Back: dV (dV pass) or dQ (dK pass) of step j - 1 once its P or dS is in.
             for (int j = 1; ok && j <= nsteps; ++j) {
-              if (!mbar_wait_warp(p_ready, (j - 1) & 1, p.status)) break;
+              const int jj = j - 1, i = jj - nper;
+              if (!(jj < nper ? mbar_wait_warp(p_ready, jj & 1, p.status)
+                              : mbar_wait_warp(p_ready_b(i & 1), (i >> 1) & 1, p.status)))
+                break;
               tc_fence_after();
-              if (!(j - 1 < nper ? back_dv(j - 1) : back_dq())) break;
+              if (!(jj < nper ? back_dv(jj) : back_dq())) break;
             }
           }
         } else {
@@ -996,20 +1015,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           reg_fence(v1);
           tc_fence_before();
           mbar_arrive(dq_empty(0));  // this thread is done with the half
-          // four [128 d, 16 q] boxes through two alternating 8 KiB buffers, so that staging
-          // one box overlaps the reduce-add of the one before
+          // four [128 d, 16 q] boxes through four 8 KiB buffers, so that staging a box
+          // overlaps the reduce-adds of the ones before
 #pragma unroll
           for (int bx = 0; bx < 4; ++bx) {
-            const int bf = bx & 1;
-            if (t == 0) bulk_wait_read_but_one();  // the box two back has left this buffer
+            const int boff = bx < 2 ? C::OFF_DQS + bx * 8192 : C::OFF_DQS2 + (bx - 2) * 8192;
+            float *sb = reinterpret_cast<float *>(smem + boff);
+            if (t == 0) bulk_wait_read_but<3>();  // the box four back has left this buffer
             named_bar<2, 128>();
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              stage[bf * 2048 + e * 128 + row] = __uint_as_float(bx < 2 ? v0[(bx & 1) * 16 + e] : v1[(bx & 1) * 16 + e]);
+              sb[e * 128 + row] = __uint_as_float(bx < 2 ? v0[(bx & 1) * 16 + e] : v1[(bx & 1) * 16 + e]);
             fence_async_smem();
             named_bar<2, 128>();
             if (t == 0) {
-              tma_reduce_add_4d(&tmDQ, stage_a + bf * 8192, m * 128, q0 + bx * 16, h, b);
+              tma_reduce_add_4d(&tmDQ, sbase + boff, m * 128, q0 + bx * 16, h, b);
               bulk_commit();
             }
           }

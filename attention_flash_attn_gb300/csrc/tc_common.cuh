@@ -145,8 +145,9 @@ __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap *m, uint32_t
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // This thread's committed bulk groups have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// All but this thread's most recently committed bulk group have finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_but_one() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// All but this thread's N most recently committed bulk groups have finished reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_but() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 // This thread's committed bulk groups have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Generic-proxy shared-memory writes become visible to the async proxy (TMA, tcgen05).

@@ -457,3 +457,156 @@ def test_vtmem_protocol_never_deadlocks_or_aliases():
         nper = STEP_COUNTS[trial % len(STEP_COUNTS)]
         finished, hazards = simulate_vtmem(nper, rng)
         assert finished and not hazards, (nper, hazards[:3])
+
+
+def simulate_split_rings(nper, rng):
+    """As simulate_vtmem, with the dK pass's tiles in two rings (two Q slots, one dO slot) and
+    dS double-buffered: each dS buffer has its own MMA-completion barrier (dK + dQ of the step
+    that read it), so the softmax never waits on the step it has just handed over."""
+    nsteps, nB = 2 * nper, nper
+    need = defaultdict(lambda: 1)
+    need.update({"mma_done": 2, "mdb0": 2, "mdb1": 2, "fin_done": 2})  # p_ready etc.: one arrival (the model's softmax is one agent)
+    count, done, hazards = defaultdict(int), defaultdict(int), []
+
+    def arrive(b):
+        count[b] += 1
+        if count[b] == need[b]:
+            count[b] = 0
+            done[b] += 1
+
+    u_last0, u_last1 = ((nper + 1) >> 1) - 1, (nper >> 1) - 1
+
+    def loader0():
+        yield ("arrive", "kv_full")
+        for j in range(nsteps):
+            if j >= 2:
+                yield ("wait", f"ld_empty{j & 1}", (j >> 1) - 1)
+            yield ("arrive", f"ld_full{j & 1}")
+            if j < nper:
+                s, u = j & 1, j >> 1
+                if u >= 1:
+                    yield ("wait", f"qdo_empty{s}", u - 1)
+                yield ("arrive", f"qdo_full{s}")
+                continue
+            i = j - nper
+            r = i & 1  # Q_i
+            if i >= 2:
+                yield ("wait", f"ring_empty{r}", (i >> 1) - 1)
+            elif r == 0:
+                yield ("wait", "qdo_empty0", u_last0)
+            else:
+                yield ("wait", "do0_free", 0)
+            yield ("arrive", f"ring_full{r}")
+            if i >= 1:  # dO_i
+                yield ("wait", "ring_empty2", i - 1)
+            elif u_last1 >= 0:
+                yield ("wait", "qdo_empty1", u_last1)
+            yield ("arrive", "ring_full2")
+
+    def loader1():
+        for j in range(nper):
+            s, u = j & 1, j >> 1
+            if u >= 1:
+                yield ("wait", f"do_empty{s}", u - 1)
+            yield ("arrive", f"do_full{s}")
+        if nper > 0:
+            yield ("wait", "do_empty0", u_last0)
+            yield ("arrive", "do0_free")
+
+    def front():
+        yield ("wait", "kv_full", 0)
+        for j in range(nper):
+            if j >= 1:
+                yield ("wait", "sdp_free", j - 1)
+            yield ("wait", f"qdo_full{j & 1}", j >> 1)
+            yield ("arrive", "s_full")
+            yield ("arrive", f"qdo_empty{j & 1}")
+
+        def dk(i):
+            yield ("wait", f"prb{i & 1}", i >> 1)
+            yield ("arrive", f"ring_empty{i & 1}")
+            yield ("arrive", f"mdb{i & 1}")
+
+        for i in range(nB):
+            j = nper + i
+            if i == 0:
+                yield ("wait", "sdp_free", nper - 1)
+                yield ("wait", "acc_free", 0)
+            else:
+                yield ("wait", "dp_free", i - 1)
+            yield ("wait", f"ring_full{i & 1}", i >> 1)
+            yield ("arrive", "s_full")
+            if i >= 1:
+                yield from dk(i - 1)
+            yield ("wait", "sdp_free", j)
+            if i == 0:
+                yield ("wait", "v_full", 0)
+            yield ("wait", "ring_full2", i)
+            yield ("arrive", "ring_empty2")
+            yield ("arrive", "dp_full")
+        if nB > 0:
+            yield from dk(nB - 1)
+        yield ("arrive", "fin_done")
+
+    def back():
+        yield ("wait", "kv_full", 0)
+        h = 0
+        for j in range(1, nsteps + 1):
+            jj = j - 1
+            if jj < nper:
+                yield ("wait", "p_ready", jj)
+                yield ("wait", f"do_full{jj & 1}", jj >> 1)
+                yield ("arrive", f"do_empty{jj & 1}")
+                yield ("arrive", "mma_done")
+                yield ("arrive", "mma_done")
+                continue
+            yield ("wait", f"prb{(jj - nper) & 1}", (jj - nper) >> 1)
+            for _ in range(2):
+                if h >= 1:
+                    yield ("wait", "dq_empty", h - 1)
+                yield ("arrive", "dq_full")
+                h += 1
+            yield ("arrive", f"mdb{(jj - nper) & 1}")
+        yield ("arrive", "fin_done")
+
+    def softmax():
+        for j in range(nsteps):
+            yield ("wait", "s_full", j)
+            yield ("wait", f"ld_full{j & 1}", j >> 1)
+            yield ("arrive", "sdp_free")
+            if j >= nper:
+                yield ("wait", "dp_full", j - nper)
+                yield ("arrive", "dp_free")
+            yield ("arrive", f"ld_empty{j & 1}")
+            if j < nper:
+                if j >= 1:
+                    yield ("wait", "mma_done", j - 1)
+            else:
+                i = j - nper
+                if i >= 2:  # dS buffer i & 1 was last read by dK / dQ of step i - 2
+                    yield ("wait", f"mdb{i & 1}", (i >> 1) - 1)
+            # dV pass: one p_ready; dK pass: one per dS buffer, so that its phases are two
+            # steps apart and the MMA warps cannot be overtaken twice
+            yield ("arrive", "p_ready" if j < nper else f"prb{(j - nper) & 1}")
+            if j == nper - 1:
+                yield ("wait", "mma_done", j)
+                yield ("arrive", "acc_free")
+                yield ("arrive", "v_full")
+        if nsteps > 0:
+            yield ("wait", "fin_done", 0)
+
+    def drain():
+        for h in range(2 * nB):
+            yield ("wait", "dq_full", h)
+            yield ("arrive", "dq_empty")
+
+    return run_agents({"loader0": loader0(), "loader1": loader1(), "front": front(), "back": back(),
+                       "softmax": softmax(), "drain": drain()}, arrive, done, hazards, rng)
+
+
+def test_split_rings_protocol_never_deadlocks_or_aliases():
+    rng = random.Random(777)
+    for trial in range(1500):
+        nper = STEP_COUNTS[trial % len(STEP_COUNTS)]
+        finished, hazards = simulate_split_rings(nper, rng)
+        assert finished and not hazards, (nper, hazards[:3])
