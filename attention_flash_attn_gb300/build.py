@@ -47,6 +47,23 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
+# Sources that the backward main kernel's code depends on: a DRAM-traffic figure recorded by
+# ncu for that kernel stays valid while these files (and the flags) are unchanged.
+BWD_MAIN_SOURCES = ("bwd_tc.cu", "tc_common.cuh", "tc_host.cu", "common.cuh", "internal.h")
+
+
+def kernel_stamp(names=BWD_MAIN_SOURCES) -> str:
+    """Hash of the named csrc files, the public header and the compile flags."""
+    h = hashlib.sha256()
+    files = [os.path.join(CSRC, n) for n in names] + [os.path.join(ROOT, "include", "attn_gb300.h")]
+    for f in files:
+        h.update(os.path.relpath(f, ROOT).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(ARCH + FLAGS).encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile (if sources changed) and return the path of the shared library."""
     os.makedirs(BUILD, exist_ok=True)

@@ -119,12 +119,12 @@ class ClockSampler:
 
 def captured_traffic(workload):
     """DRAM bytes per launch of the backward main kernel from a committed ncu capture, only
-    while the library's sources are the ones that capture was taken of."""
+    while that kernel's sources are the ones the capture was taken of."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         from attention_flash_attn_gb300 import build as _b
         entry = json.load(open(p)).get(workload)
-        if entry and entry.get("source_stamp") == _b._stamp():
+        if entry and entry.get("source_stamp") == _b.kernel_stamp():
             return entry["dram_bytes_per_launch"]
     except Exception:
         pass
