@@ -48,35 +48,111 @@ __device__ __forceinline__ float chunk_dot<float>(const float *a, const float *b
   return fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, x.w * y.w)));
 }
 
+// One query row's (dO, O) chunk pair: 16 bytes of each.
+template <typename T>
+__device__ __forceinline__ float chunk_dot_raw(const uint4 &x, const uint4 &y);
+template <>
+__device__ __forceinline__ float chunk_dot_raw<__nv_bfloat16>(const uint4 &x, const uint4 &y) {
+  const __nv_bfloat162 *xa = reinterpret_cast<const __nv_bfloat162 *>(&x);
+  const __nv_bfloat162 *ya = reinterpret_cast<const __nv_bfloat162 *>(&y);
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 fx = __bfloat1622float2(xa[k]), fy = __bfloat1622float2(ya[k]);
+    s = fmaf(fx.x, fy.x, s);
+    s = fmaf(fx.y, fy.y, s);
+  }
+  return s;
+}
+template <>
+__device__ __forceinline__ float chunk_dot_raw<float>(const uint4 &x, const uint4 &y) {
+  return fmaf(__uint_as_float(x.x), __uint_as_float(y.x),
+              fmaf(__uint_as_float(x.y), __uint_as_float(y.y),
+                   fmaf(__uint_as_float(x.z), __uint_as_float(y.z), __uint_as_float(x.w) * __uint_as_float(y.w))));
+}
+
 // grid (ceil(Sq/64), B), block 256: warp w handles heads w, w+8, ...; rows in order, so the
 // per-(block, head) partial sums are deterministic.
-template <typename T>
+//
+// NC > 0 (a row is NC 16-byte chunks and NC divides 32): a warp covers 32 / NC rows per load,
+// one lane per chunk, and keeps kPreUnroll such loads in flight per lane before reducing each
+// row over its NC lanes.  NC == 0: any other row length, one row per warp at a time.
+constexpr int kPreUnroll = 4;
+template <typename T, int NC>
 __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int zero_dqacc) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int b = blockIdx.y;
   const int i0 = blockIdx.x * kPreRows, i1 = min(i0 + kPreRows, p.Sq);
   constexpr int per_chunk = 16 / sizeof(T);
-  const int nchunk = p.D / per_chunk;
   const T *O = static_cast<const T *>(p.O);
   const T *dO = static_cast<const T *>(p.dO);
   for (int h = warp; h < p.Hq; h += kPreWarps) {
     float part = 0.f;
     const float sink = p.sink ? p.sink[h] : 0.f;
-    for (int i = i0; i < i1; ++i) {
-      const size_t row = (((size_t)b * p.Sq + i) * p.Hq + h) * p.D;
-      float s = 0.f;
-      for (int c = lane; c < nchunk; c += 32) s += chunk_dot<T>(dO + row + c * per_chunk, O + row + c * per_chunk);
-      s = warp_sum(s);
-      const size_t ri = ((size_t)b * p.Hq + h) * p.Sq + i;
-      const size_t rp = ((size_t)b * p.Hq + h) * p.sq_pad + i;
-      if (lane == 0) {
-        p.Dvec[rp] = s;
-        if (p.lse2p) p.lse2p[rp] = p.LSE[ri] * 1.4426950408889634f;
+    if constexpr (NC > 0) {
+      constexpr int RPL = 32 / NC;  // rows per warp-wide load
+      const int sub = lane / NC, c = lane % NC;
+      for (int ib = i0; ib < i1; ib += RPL * kPreUnroll) {
+        uint4 xa[kPreUnroll], xb[kPreUnroll];
+#pragma unroll
+        for (int u = 0; u < kPreUnroll; ++u) {
+          const int i = ib + u * RPL + sub;
+          if (i < i1) {
+            const size_t row = (((size_t)b * p.Sq + i) * p.Hq + h) * p.D + (size_t)c * per_chunk;
+            xa[u] = __ldg(reinterpret_cast<const uint4 *>(dO + row));
+            xb[u] = __ldg(reinterpret_cast<const uint4 *>(O + row));
+          } else {
+            xa[u] = xb[u] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        float s[kPreUnroll];
+#pragma unroll
+        for (int u = 0; u < kPreUnroll; ++u) s[u] = chunk_dot_raw<T>(xa[u], xb[u]);
+#pragma unroll
+        for (int o = NC / 2; o > 0; o >>= 1) {
+#pragma unroll
+          for (int u = 0; u < kPreUnroll; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], o);
+        }
+#pragma unroll
+        for (int u = 0; u < kPreUnroll; ++u) {
+          const int i = ib + u * RPL + sub;
+          if (i >= i1) continue;
+          if (c == 0) {
+            const size_t ri = ((size_t)b * p.Hq + h) * p.Sq + i;
+            const size_t rp = ((size_t)b * p.Hq + h) * p.sq_pad + i;
+            const float lse = p.LSE[ri];
+            p.Dvec[rp] = s[u];
+            if (p.lse2p) p.lse2p[rp] = lse * 1.4426950408889634f;
+            if (p.sink) part = fmaf(expf(sink - lse), s[u], part);
+          }
+          if (zero_dqacc) {
+            float4 *z = reinterpret_cast<float4 *>(p.dQacc + (((size_t)b * p.Sq + i) * p.Hq + h) * p.D +
+                                                   (size_t)c * per_chunk);
+#pragma unroll
+            for (int v = 0; v < per_chunk / 4; ++v) z[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
       }
-      if (p.sink) part = fmaf(expf(sink - p.LSE[ri]), s, part);
-      if (zero_dqacc) {
-        float4 *z = reinterpret_cast<float4 *>(p.dQacc + row);
-        for (int c = lane; c < p.D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      // Only the first lane of each row segment holds a partial sum: add them in a fixed order.
+      part = warp_sum(part);
+    } else {
+      const int nchunk = p.D / per_chunk;
+      for (int i = i0; i < i1; ++i) {
+        const size_t row = (((size_t)b * p.Sq + i) * p.Hq + h) * p.D;
+        float s = 0.f;
+        for (int c = lane; c < nchunk; c += 32) s += chunk_dot<T>(dO + row + c * per_chunk, O + row + c * per_chunk);
+        s = warp_sum(s);
+        const size_t ri = ((size_t)b * p.Hq + h) * p.Sq + i;
+        const size_t rp = ((size_t)b * p.Hq + h) * p.sq_pad + i;
+        if (lane == 0) {
+          p.Dvec[rp] = s;
+          if (p.lse2p) p.lse2p[rp] = p.LSE[ri] * 1.4426950408889634f;
+        }
+        if (p.sink) part = fmaf(expf(sink - p.LSE[ri]), s, part);
+        if (zero_dqacc) {
+          float4 *z = reinterpret_cast<float4 *>(p.dQacc + row);
+          for (int c = lane; c < p.D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
     }
     if (p.sink && lane == 0)
@@ -89,6 +165,25 @@ __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int z
         if (p.lse2p) p.lse2p[rp] = INFINITY;
       }
   }
+}
+
+// Eight fp32 values -> eight output values in one 16-byte store (bf16) or two (fp32).
+template <typename T>
+__device__ __forceinline__ void store8(T *dst, const float4 &x, const float4 &y);
+template <>
+__device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16 *dst, const float4 &x, const float4 &y) {
+  uint4 o;
+  __nv_bfloat162 t;
+  t = __floats2bfloat162_rn(x.x, x.y); o.x = *reinterpret_cast<uint32_t *>(&t);
+  t = __floats2bfloat162_rn(x.z, x.w); o.y = *reinterpret_cast<uint32_t *>(&t);
+  t = __floats2bfloat162_rn(y.x, y.y); o.z = *reinterpret_cast<uint32_t *>(&t);
+  t = __floats2bfloat162_rn(y.z, y.w); o.w = *reinterpret_cast<uint32_t *>(&t);
+  *reinterpret_cast<uint4 *>(dst) = o;
+}
+template <>
+__device__ __forceinline__ void store8<float>(float *dst, const float4 &x, const float4 &y) {
+  reinterpret_cast<float4 *>(dst)[0] = x;
+  reinterpret_cast<float4 *>(dst)[1] = y;
 }
 
 template <typename T>
@@ -105,16 +200,11 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(Params p, int convert_dq,
   const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t nthr = (size_t)gridDim.x * blockDim.x;
   if (convert_dq) {
-    const size_t n4 = (size_t)p.B * p.Sq * p.Hq * p.D / 4;
+    // D is a multiple of 8 and dQ 16-byte aligned: whole groups of eight.
+    const size_t n8 = (size_t)p.B * p.Sq * p.Hq * p.D / 8;
     const float4 *src = reinterpret_cast<const float4 *>(p.dQacc);
     T *dst = static_cast<T *>(p.dQ);
-    for (size_t e = tid; e < n4; e += nthr) {
-      float4 x = src[e];
-      dst[4 * e + 0] = from_f<T>(x.x);
-      dst[4 * e + 1] = from_f<T>(x.y);
-      dst[4 * e + 2] = from_f<T>(x.z);
-      dst[4 * e + 3] = from_f<T>(x.w);
-    }
+    for (size_t e = tid; e < n8; e += nthr) store8<T>(dst + 8 * e, __ldg(src + 2 * e), __ldg(src + 2 * e + 1));
   }
   if (dbias_elems) {
     T *dst = static_cast<T *>(p.dbias);
@@ -122,23 +212,32 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(Params p, int convert_dq,
   }
 }
 
+template <typename T>
+cudaError_t launch_pre_t(const Params &p, bool zero_dqacc, cudaStream_t st) {
+  dim3 grid((p.Sq + kPreRows - 1) / kPreRows, p.B);
+  const int nc = p.D * (int)sizeof(T) / 16;
+  switch (nc) {
+    case 4: bwd_pre_kernel<T, 4><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+    case 8: bwd_pre_kernel<T, 8><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+    case 16: bwd_pre_kernel<T, 16><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+    case 32: bwd_pre_kernel<T, 32><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+    default: bwd_pre_kernel<T, 0><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+  }
+  return counted(cudaGetLastError());
+}
+
 }  // namespace
 
 int bwd_pre_partials(int B, int Sq) { return B * ((Sq + kPreRows - 1) / kPreRows); }
 
 cudaError_t launch_bwd_pre(const Params &p, int dtype, bool zero_dqacc, cudaStream_t st) {
-  dim3 grid((p.Sq + kPreRows - 1) / kPreRows, p.B);
-  if (dtype == kF32)
-    bwd_pre_kernel<float><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc);
-  else
-    bwd_pre_kernel<__nv_bfloat16><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc);
-  return counted(cudaGetLastError());
+  return dtype == kF32 ? launch_pre_t<float>(p, zero_dqacc, st) : launch_pre_t<__nv_bfloat16>(p, zero_dqacc, st);
 }
 
 cudaError_t launch_bwd_post(const Params &p, int dtype, bool convert_dq, size_t dbias_elems,
                             cudaStream_t st) {
   size_t work = 0;
-  if (convert_dq) work = (size_t)p.B * p.Sq * p.Hq * p.D / 4;
+  if (convert_dq) work = (size_t)p.B * p.Sq * p.Hq * p.D / 8;
   if (dbias_elems > work) work = dbias_elems;
   size_t blocks = (work + 255) / 256;
   const size_t sink_blocks = p.dsink ? (size_t)(p.Hq + 7) / 8 : 0;

@@ -74,13 +74,17 @@ EDGE = [
     # bf16 with a bias (FFMA path), bias broadcast over batch
     Workload("edge_bf16_bias", "bf16", B=2, Sq=130, Sk=130, Hq=2, Hkv=2, D=64, causal=True, softcap=10.0,
              bias=True, q_std=2.0),
-    # head dim 256 (the cluster-pair backward): key tiles that no query sees (their dK / dV
+    # head dim 256 (the two-pass backward): key tiles that no query sees (their dK / dV
     # are zero), Sq != Sk, a window without causal
     Workload("edge_d256_unseen_key_tiles", "bf16", B=1, Sq=64, Sk=400, Hq=2, Hkv=1, D=256, causal=False,
              window=30, softcap=30.0, q_std=2.0),
     # head dim 256 with MQA (G = 4), a sink, packed segments and the cap
     Workload("edge_d256_mqa_sink_segments", "bf16", B=2, Sq=300, Sk=300, Hq=4, Hkv=1, D=256, causal=True,
              softcap=30.0, sink=True, segments=True, run_lo=40, run_hi=150, q_std=2.0),
+    # head dim 40 (FFMA path): a row of 5 chunks does not divide a warp, so the backward
+    # preprocess takes its one-row-per-warp form; a sink and a ragged tail past 128 rows
+    Workload("edge_bf16_d40_sink", "bf16", B=1, Sq=150, Sk=150, Hq=3, Hkv=1, D=40, causal=True,
+             softcap=20.0, sink=True, q_std=2.0),
     # fp32 with sink, GQA, window and segments all at once
     Workload("edge_f32_everything", "f32", B=2, Sq=190, Sk=190, Hq=4, Hkv=2, D=32, causal=True, window=70,
              softcap=5.0, sink=True, segments=True, run_lo=20, run_hi=90, q_std=2.0, bias=True),
