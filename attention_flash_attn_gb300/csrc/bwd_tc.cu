@@ -131,7 +131,8 @@ __device__ __forceinline__ uint4 pack8(const uint32_t *o, int v) {
 // Score constants of the element-wise backward, as packed pairs.  With the soft-cap,
 // e = exp(2 u / cap) for u = scale s, r = 1 / (1 + e), so tanh(u / cap) = 1 - 2 r and
 // 1 - tanh^2 = 4 r (1 - r); the capped logit in log2 units is cap log2(e) (1 - 2 r).  An
-// overflowing e gives r = 0 (tanh = 1) and an underflowing one r = 1 (tanh = -1).
+// overflowing e gives r = 0 (tanh = 1) and an underflowing one r = 1 (tanh = -1); the FMA-pipe
+// form (f2_sigmoid2_neg) clamps the exponent at 126 instead, which gives r ~ 0 as well.
 struct BwdScore {
   uint64_t cin, one, mcap2, cap2, mfs, fs, sc2, scale;
   __device__ BwdScore(float scale_, float inv_cap, float cap) {
@@ -147,16 +148,24 @@ struct BwdScore {
 };
 
 // One pair of raw scores -> (t2 - LSE2, f): t2 the (capped) logit in log2 units, f the
-// cap's chain-rule factor times the softmax scale.
-template <bool CAP>
+// cap's chain-rule factor times the softmax scale.  FRCP: the cap's reciprocal on the FMA pipe
+// (f2_sigmoid2_neg); otherwise ex2 + rcp on the special-function unit.  The head-dim-256 dK pass
+// keeps the latter: its element-wise work sits on the S^T -> dP^T dependency chain and is not
+// bound by the special-function unit, and the longer FMA sequence measured 5 % slower there.
+template <bool CAP, bool FRCP>
 __device__ __forceinline__ void score_pair(uint32_t s0, uint32_t s1, uint64_t lse2, const BwdScore &k, uint64_t &y,
                                            uint64_t &f) {
   const uint64_t s2 = f2_pack(__uint_as_float(s0), __uint_as_float(s1));
   if constexpr (CAP) {
-    float xa, xb, da, db;
-    f2_unpack(f2_mul(s2, k.cin), xa, xb);
-    f2_unpack(f2_add(f2_pack(ex2_approx(xa), ex2_approx(xb)), k.one), da, db);
-    const uint64_t r2 = f2_pack(rcp_approx(da), rcp_approx(db));
+    uint64_t r2;
+    if constexpr (FRCP) {
+      r2 = f2_sigmoid2_neg(f2_mul(s2, k.cin));
+    } else {
+      float xa, xb, da, db;
+      f2_unpack(f2_mul(s2, k.cin), xa, xb);
+      f2_unpack(f2_add(f2_pack(ex2_approx(xa), ex2_approx(xb)), k.one), da, db);
+      r2 = f2_pack(rcp_approx(da), rcp_approx(db));
+    }
     y = f2_sub(f2_fma(r2, k.mcap2, k.cap2), lse2);
     f = f2_mul(r2, f2_fma(r2, k.mfs, k.fs));  // 4 scale r (1 - r)
   } else {
@@ -178,7 +187,7 @@ __device__ __forceinline__ uint32_t bf16_pair(uint64_t v) {
 // One 32-query chunk of a key row, every column treated as visible (masked columns are
 // cleared afterwards by the fix-ups below, only on chunks that need it):
 //   KIND 1: P, packed to bf16 pairs;  KIND 0: P and dS = P f (dP - D), both packed.
-template <bool CAP, int KIND>
+template <bool CAP, bool FRCP, int KIND>
 __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float *lse2c,
                                           const float *dvc, uint32_t (&pk)[16], uint32_t (&dk)[16],
                                           const BwdScore &k) {
@@ -187,7 +196,7 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32
 #pragma unroll
   for (int e2 = 0; e2 < 16; ++e2) {
     uint64_t y, f;
-    score_pair<CAP>(sr[2 * e2], sr[2 * e2 + 1], l2[e2], k, y, f);
+    score_pair<CAP, FRCP>(sr[2 * e2], sr[2 * e2 + 1], l2[e2], k, y, f);
     const uint64_t p2 = ex2_pair(y);
     pk[e2] = bf16_pair(p2);
     if constexpr (KIND == 0) {
@@ -199,13 +208,13 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32
 
 // The dK pass's chunk in two steps, so that the first runs before dP^T has been computed:
 // (1) in place, the raw score -> P f;
-template <bool CAP>
+template <bool CAP, bool FRCP>
 __device__ __forceinline__ void ds_first(uint32_t (&sr)[32], const float *lse2c, const BwdScore &k) {
   const uint64_t *l2 = reinterpret_cast<const uint64_t *>(lse2c);
 #pragma unroll
   for (int e2 = 0; e2 < 16; ++e2) {
     uint64_t y, f;
-    score_pair<CAP>(sr[2 * e2], sr[2 * e2 + 1], l2[e2], k, y, f);
+    score_pair<CAP, FRCP>(sr[2 * e2], sr[2 * e2 + 1], l2[e2], k, y, f);
     float a, b;
     f2_unpack(f2_mul(ex2_pair(y), f), a, b);
     sr[2 * e2] = __float_as_uint(a);
@@ -474,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(sdp_free);
           }
-          ds_first<CAP>(pf[cc], lse2 + c * 32, ks);
+          ds_first<CAP, false>(pf[cc], lse2 + c * 32, ks);
           if (!full) clear_hidden(pf[cc], chunk_vis(q0 + c * 32, lo, hi, seg_pairwise, segq, p.Sq, sid));
         }
         if (!mbar_wait(dp_full, (j - nper) & 1, p.status)) { ok = false; break; }
@@ -506,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(sdp_free);
           }
-          bwd_chunk<CAP, C::TWO ? 1 : 0>(sr, dr, lse2 + c * 32, dvv + c * 32, pk[cc], dk[cc], ks);
+          bwd_chunk<CAP, true, C::TWO ? 1 : 0>(sr, dr, lse2 + c * 32, dvv + c * 32, pk[cc], dk[cc], ks);
           if (!full) {
             const uint32_t vis = chunk_vis(q0 + c * 32, lo, hi, seg_pairwise, segq, p.Sq, sid);
             clear_hidden(pk[cc], vis);
