@@ -27,8 +27,9 @@ def _ptr(t: Optional[torch.Tensor]):
 
 
 def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
-               bias=None, seg_q=None, seg_k=None, cu_seqlens=None):
-    """Fill an ``attn_args`` from tensors.  Returns (args, tensors kept alive)."""
+               bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False):
+    """Fill an ``attn_args`` from tensors.  Returns (args, tensors kept alive).
+    off_by_one: the off-by-one softmax (an extra column of logit 0 per row, no gradient)."""
     if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share dtype bfloat16 or float32")
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -72,6 +73,7 @@ def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale
         a.sink = sink.data_ptr()
         keep.append(sink)
     a.scale = float(D ** -0.5 if scale is None else scale)
+    a.softmax_type = _capi.ATTN_SOFTMAX_OFF_BY_ONE if off_by_one else _capi.ATTN_SOFTMAX_DEFAULT
     return a, keep
 
 
@@ -95,10 +97,11 @@ def _check(status: int, where: str):
 
 
 def attn_fwd(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
-             bias=None, seg_q=None, seg_k=None, cu_seqlens=None, out=None, lse=None):
+             bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, out=None, lse=None):
     """Forward: returns (O [B,Sq,Hq,D] in q's dtype, LSE [B,Hq,Sq] float32)."""
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
-                         scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens)
+                         scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
+                         off_by_one=off_by_one)
     L = lib()
     need = L.attn_fwd_workspace_size(ctypes.byref(a))
     if need == 0:
@@ -114,11 +117,13 @@ def attn_fwd(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=N
 
 
 def attn_fwd_noalloc(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
-                     bias=None, seg_q=None, seg_k=None, cu_seqlens=None, out=None, lse=None):
+                     bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, out=None,
+                     lse=None):
     """attn_fwd with the library's built-in scratch instead of a workspace (for callers that
     cannot allocate device memory; see include/attn_gb300.h).  Returns (O, LSE)."""
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
-                         scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens)
+                         scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
+                         off_by_one=off_by_one)
     B, Sq, Hq, D = q.shape
     O = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device) if out is None else out
     LSE = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
@@ -129,10 +134,11 @@ def attn_fwd_noalloc(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None,
 
 
 def attn_bwd(q, k, v, O, LSE, dO, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
-             bias=None, seg_q=None, seg_k=None, cu_seqlens=None):
+             bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False):
     """Backward: returns (dQ, dK, dV, dbias or None, dsink or None)."""
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
-                         scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens)
+                         scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
+                         off_by_one=off_by_one)
     L = lib()
     need = L.attn_bwd_workspace_size(ctypes.byref(a))
     if need == 0:

@@ -15,6 +15,9 @@ LIB_PATH = os.path.join(PKG, "libattn_gb300.so")
 ATTN_DTYPE_BF16 = 1
 ATTN_DTYPE_F32 = 2
 
+ATTN_SOFTMAX_DEFAULT = 0
+ATTN_SOFTMAX_OFF_BY_ONE = 1
+
 ATTN_OK = 0
 ATTN_ERR_INVALID = 1
 ATTN_ERR_UNSUPPORTED = 2
@@ -48,6 +51,7 @@ class AttnArgs(ctypes.Structure):
         ("cu_seqlens", ctypes.c_void_p), ("nseq", ctypes.c_int),
         ("causal", ctypes.c_int), ("window", ctypes.c_int),
         ("softcap", ctypes.c_float), ("sink", ctypes.c_void_p), ("scale", ctypes.c_float),
+        ("softmax_type", ctypes.c_int),
     ]
 
 

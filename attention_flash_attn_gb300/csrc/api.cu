@@ -86,6 +86,8 @@ int validate(const attn_args *a) {
     if (a->bias_stride_b < 0 || a->bias_stride_h < 0 || !aligned16(a->bias)) return ATTN_ERR_INVALID;
   }
   if ((a->seg_q == nullptr) != (a->seg_k == nullptr)) return ATTN_ERR_INVALID;
+  if (a->softmax_type != ATTN_SOFTMAX_DEFAULT && a->softmax_type != ATTN_SOFTMAX_OFF_BY_ONE) return ATTN_ERR_INVALID;
+  if (a->softmax_type == ATTN_SOFTMAX_OFF_BY_ONE && a->sink) return ATTN_ERR_INVALID;
   if (a->cu_seqlens) {
     if (a->seg_q) return ATTN_ERR_UNSUPPORTED;
     if (a->B != 1 || a->Sq != a->Sk || a->nseq < 0) return ATTN_ERR_INVALID;
@@ -112,6 +114,7 @@ Params make_params(const attn_args *a, char *ws, const Layout &L) {
   p.bias_B = a->bias_stride_b ? a->B : 1;
   p.bias_H = a->bias_stride_h ? a->Hq : 1;
   p.sink = a->sink;
+  p.off_by_one = a->softmax_type == ATTN_SOFTMAX_OFF_BY_ONE ? 1 : 0;
   p.status = reinterpret_cast<unsigned *>(ws);
   if (a->seg_q || a->cu_seqlens) {
     p.seg_mono = reinterpret_cast<unsigned char *>(ws + L.mono);

@@ -34,6 +34,7 @@ struct Params {
   const int2 *krange;             // [B, ceil(Sk/64)]: query range [x, y) of each 64-key tile
   const unsigned char *seg_mono;  // [B]: 1 if seg_q and seg_k rows are non-decreasing
   const float *sink;              // [Hq] or null
+  int off_by_one;                 // one extra column of logit 0 per row (no sink array)
   // forward outputs / backward inputs
   void *O;
   float *LSE;
@@ -50,6 +51,11 @@ struct Params {
   int n_part;                     // partial sums per head
   unsigned *status;
 };
+
+// The extra softmax column of a row, if any: the learnable sink (logit sink[h]) or the
+// off-by-one column (logit 0).  It enters the row's normaliser once and carries no value.
+__device__ __forceinline__ bool has_sink_col(const Params &p) { return p.sink != nullptr || p.off_by_one != 0; }
+__device__ __forceinline__ float sink_logit(const Params &p, int h) { return p.sink ? p.sink[h] : 0.f; }
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }

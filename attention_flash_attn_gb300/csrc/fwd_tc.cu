@@ -334,8 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
 
     const FwdScore ks(p.scale, p.inv_cap, p.cap);
-    float m_ref = p.sink ? p.sink[h] * kLog2e : -INFINITY;     // running max (log2 units)
-    float l = (p.sink && half == 0) ? 1.f : 0.f;               // this half's sum relative to m_ref
+    const bool sink_col = has_sink_col(p);
+    float m_ref = sink_col ? sink_logit(p, h) * kLog2e : -INFINITY;  // running max (log2 units)
+    float l = (sink_col && half == 0) ? 1.f : 0.f;                   // this half's sum relative to m_ref
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {

@@ -4,8 +4,8 @@
 // segments) with accurate expf / expm1f / logf, for fp32 inputs (where a tensor-core
 // tf32 product could not meet a 1e-5 relative error) and for calls with an additive bias.
 // One warp owns one query row (forward, dQ) or one key row (dK/dV); K/V (or Q/dO) tiles
-// are staged through shared memory as fp32.  The online softmax starts from the sink
-// (m = sink, l = 1) so the sink enters each row exactly once.
+// are staged through shared memory as fp32.  The online softmax starts from the sink or the
+// off-by-one column (m = its logit, l = 1) so that column enters each row exactly once.
 #include "common.cuh"
 #include "internal.h"
 
@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(Params p) {
 
   int lo, hi;
   key_range(p, b, i0, i1, lo, hi);
-  float m = p.sink ? p.sink[h] : -INFINITY;
-  float l = p.sink ? 1.f : 0.f;
+  float m = has_sink_col(p) ? sink_logit(p, h) : -INFINITY;
+  float l = has_sink_col(p) ? 1.f : 0.f;
   float acc[kMaxPerLane];
 #pragma unroll
   for (int t = 0; t < kMaxPerLane; ++t) acc[t] = 0.f;

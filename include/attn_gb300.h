@@ -12,6 +12,10 @@
  *     entering each row exactly once and carrying no value; its gradient is
  *     dsink[h] = -sum_{b,i} p_sink(b,h,i) * (dO_i . O_i)
  *       (TransformerEngine PR #3551, "What was broken" / "What changed");
+ *   - the off-by-one softmax: the same extra column with its logit fixed at 0 for every
+ *     head and no gradient (the "off-by-one" softmax type that TransformerEngine PR #3551
+ *     tests beside "learnable", "Verification" table; the page gives no formula -- this is
+ *     the learnable sink at its default zero offset, held fixed);
  *   - GQA/MQA: query head h reads kv head h / (Hq / Hkv);
  *   - causal, sliding-window and packed-segment masks (segment ids or cu_seqlens)
  *       (MaxText commit message quoted on tokamax PR #1121: sliding window, packing with
@@ -24,9 +28,11 @@
  *   t_ij   = softcap > 0 ? softcap * tanh(u_ij / softcap) : u_ij
  *   vis_ij = (!causal || j <= i + Sk - Sq) && (window <= 0 || (i + Sk - Sq) - j < window)
  *            && (no segments || seg_q[b,i] == seg_k[b,j])
- *   LSE_i  = ln( [sink ? exp(sink[h]) : 0] + sum_{vis} exp(t_ij) )       (natural log)
+ *   LSE_i  = ln( [sink ? exp(sink[h]) : off-by-one ? 1 : 0] + sum_{vis} exp(t_ij) )
+ *                                                                         (natural log)
  *   O_i    = sum_{vis} exp(t_ij - LSE_i) v_j
- * A row with nothing visible and no sink gets O = 0, LSE = -inf and zero gradients.
+ * A row with nothing visible gets O = 0 and zero gradients, with LSE = -inf -- or, with a
+ * sink or the off-by-one column, LSE = that column's logit.
  *
  * Layout: "bshd".  q, O, dO, dQ are [B, Sq, Hq, D]; k, v, dK, dV are [B, Sk, Hkv, D].
  * q, k, v may be strided (element strides for b, s, h; d is contiguous); O, dO, dQ, dK, dV
@@ -60,6 +66,12 @@ typedef struct CUstream_st *attn_stream_t;
 enum attn_dtype {
     ATTN_DTYPE_BF16 = 1,  /* q, k, v, bias, O, dO, dQ, dK, dV, dbias in bfloat16       */
     ATTN_DTYPE_F32 = 2    /* ... in float32 (fp32 FFMA kernels, for tight tolerances)   */
+};
+
+enum attn_softmax_type {
+    ATTN_SOFTMAX_DEFAULT = 0,     /* plain softmax, or the learnable sink when sink != NULL */
+    ATTN_SOFTMAX_OFF_BY_ONE = 1   /* one extra column of logit 0 per row; sink must be NULL,
+                                     and there is no dsink                                   */
 };
 
 enum attn_status {
@@ -105,6 +117,8 @@ typedef struct {
     float softcap;             /* 0: off; > 0: cap; negative, NaN or inf: ATTN_ERR_INVALID  */
     const float *sink;         /* optional [Hq] float sink logits; NULL: no sink            */
     float scale;               /* finite; usually 1/sqrt(D)                                 */
+    int softmax_type;          /* enum attn_softmax_type; zero-initialised = DEFAULT.  Any
+                                  other value, or OFF_BY_ONE with a sink: ATTN_ERR_INVALID  */
 } attn_args;
 
 /* Bytes of workspace attn_fwd needs for these arguments (256-byte multiple, >= 256). */

@@ -55,7 +55,7 @@ def valid_args(capi, dtype=1, B=1, S=16, H=2, D=64, **kw):
     ("dtype", 3, 1), ("Hq", 3, 1), ("Hkv", 0, 1), ("D", 60, 1), ("D", 264, 2),
     ("softcap", -1.0, 1), ("softcap", float("nan"), 1), ("softcap", float("inf"), 1),
     ("scale", float("inf"), 1), ("q", None, 1), ("q", 0x10008, 1), ("q_stride_s", 12, 1),
-    ("Sq", -1, 1), ("seg_q", 0x20000, 1),
+    ("Sq", -1, 1), ("seg_q", 0x20000, 1), ("softmax_type", 2, 1), ("softmax_type", -1, 1),
 ])
 def test_invalid_arguments_rejected_before_launch(capi, field, value, status):
     L = capi.lib()
@@ -67,6 +67,23 @@ def test_invalid_arguments_rejected_before_launch(capi, field, value, status):
                       None, None, 0x50000, 1 << 20, None) == status
     assert L.attn_launch_counter() == n
     assert L.attn_path_name(ctypes.byref(a)) == b""
+
+
+def test_off_by_one_softmax_arguments(capi):
+    """The off-by-one column replaces the sink array: valid alone, invalid with a sink; its
+    backward takes no dsink (there is no sink array to differentiate)."""
+    L = capi.lib()
+    a = valid_args(capi, softmax_type=capi.ATTN_SOFTMAX_OFF_BY_ONE)
+    assert L.attn_fwd_workspace_size(ctypes.byref(a)) >= 256
+    assert L.attn_bwd_workspace_size(ctypes.byref(a)) >= 256
+    need = L.attn_bwd_workspace_size(ctypes.byref(a))
+    n = L.attn_launch_counter()
+    assert L.attn_bwd(ctypes.byref(a), 0x30000, 0x40000, 0x30000, 0x30000, 0x30000, 0x30000,
+                      None, 0x60000, 0x50000, need, None) == 1
+    assert L.attn_launch_counter() == n
+    a = valid_args(capi, softmax_type=capi.ATTN_SOFTMAX_OFF_BY_ONE, sink=0x60000)
+    assert L.attn_fwd_workspace_size(ctypes.byref(a)) == 0
+    assert L.attn_fwd(ctypes.byref(a), 0x30000, 0x40000, 0x50000, 1 << 20, None) == 1
 
 
 def test_cu_seqlens_with_segments_unsupported_and_shape_rules(capi):

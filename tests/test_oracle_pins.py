@@ -251,6 +251,36 @@ def test_sink_limits():
     assert np.max(np.abs(O2)) < 1e-300 and np.allclose(L2, 1e3)
 
 
+def test_off_by_one_equals_sdpa_with_a_zero_key():
+    """The off-by-one softmax -- one extra column of logit 0 in every row, the "off-by-one"
+    softmax type TransformerEngine PR #3551 tests beside "learnable" -- is the oracle's sink
+    held at 0.  It equals plain attention over the keys plus one all-zero key (logit 0 under
+    any scale) with an all-zero value that every query sees: torch SDPA in fp64, with
+    autograd for dq, dk, dv."""
+    F = torch.nn.functional
+    r = rng(11)
+    B, S, H, D, scale = 2, 9, 2, 4, 0.5
+    q, k, v = r.normal(0, 1.5, (B, S, H, D)), r.normal(0, 1.5, (B, S, H, D)), r.normal(0, 1, (B, S, H, D))
+    dO = r.normal(0, 1, (B, S, H, D))
+    for causal in (False, True):
+        p = Problem(q, k, v, scale=scale, causal=causal, sink=np.zeros(H))
+        O, LSE = oracle.forward(p)
+        g = oracle.backward(p, dO, O, LSE)
+        qt, kt, vt = (torch.tensor(x).permute(0, 2, 1, 3).requires_grad_() for x in (q, k, v))
+        zero = torch.zeros(B, H, 1, D, dtype=torch.float64)
+        mask = torch.ones(S, S + 1, dtype=torch.bool)
+        if causal:
+            mask[:, :S] = torch.tril(torch.ones(S, S, dtype=torch.bool))
+        out = F.scaled_dot_product_attention(qt, torch.cat([kt, zero], 2), torch.cat([vt, zero], 2),
+                                             attn_mask=mask, scale=scale)
+        (out * torch.tensor(dO).permute(0, 2, 1, 3)).sum().backward()
+        t = lambda x: x.detach().permute(0, 2, 1, 3).numpy()
+        assert rel(O, t(out)) < 1e-13
+        assert rel(g["dq"], t(qt.grad)) < 1e-12
+        assert rel(g["dk"], t(kt.grad)) < 1e-12
+        assert rel(g["dv"], t(vt.grad)) < 1e-12
+
+
 def test_dsink_two_ways():
     """dsink equals -sum p0 D with p0 = exp(sink - LSE) and D = dO.O computed here, and
     the sum runs over every batch and row."""

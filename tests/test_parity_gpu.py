@@ -97,6 +97,40 @@ def test_parity_edge(w):
     check(w, run_gpu(w, inp), full_oracle(w, inp))
 
 
+# The off-by-one softmax on each kernel family: D = 64 / 128 (fused backward), 256 (two-pass)
+# and the fp32 FFMA path.
+OFF_BY_ONE = [
+    W["sink_gqa64_cap30"].replace(name="obo_d64_cap30", B=1, Sq=520, Sk=520, Hq=8, Hkv=2, sink=False),
+    W["packed_varlen_cap30"].replace(name="obo_d128_packed", B=1, Sq=600, Sk=600, Hq=2, Hkv=2, run_lo=40,
+                                     run_hi=300),
+    W["gemma2_local_w4096_cap50"].replace(name="obo_d256_window", B=1, Sq=700, Sk=700, Hq=4, Hkv=2,
+                                          window=300),
+    Workload("obo_f32", "f32", B=1, Sq=130, Sk=130, Hq=2, Hkv=1, D=32, causal=True, softcap=5.0, q_std=2.0),
+]
+
+
+@pytest.mark.parametrize("w", OFF_BY_ONE, ids=lambda w: w.name)
+def test_off_by_one_softmax(w):
+    """Against the oracle with its sink held at 0 (no dsink), and equal to the learnable-sink
+    path at a zero sink: the same kernels do the same arithmetic, so O, LSE, dK and dV match
+    bit for bit (dQ's reduce-adds land in a run-dependent order)."""
+    inp = make_inputs(w)
+    assert inp["sink"] is None
+    gpu = run_gpu(w, inp, off_by_one=True)
+    assert gpu["dsink"] is None
+    inp0 = dict(inp, sink=torch.zeros(w.Hq, dtype=torch.float32))
+    ref = full_oracle(w, inp0)
+    ref["dsink"] = None
+    check(w, gpu, ref)
+    gz = run_gpu(w, inp0)
+    for key in ("O", "LSE", "dk", "dv"):
+        assert torch.equal(gpu[key], gz[key]), key
+    assert frob_rel(to64(gpu["dq"]), to64(gz["dq"])) < 1e-6
+    # and it is not plain attention: the extra column takes probability mass
+    van = run_gpu(w, inp)
+    assert not torch.equal(gpu["LSE"], van["LSE"])
+
+
 def test_fully_masked_rows_with_and_without_sink():
     """Queries whose segment id has no key: O = 0, LSE = -inf (no sink) or sink."""
     w = Workload("masked_rows", "bf16", B=1, Sq=160, Sk=160, Hq=2, Hkv=1, D=64, causal=False)
