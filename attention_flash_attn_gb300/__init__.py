@@ -27,9 +27,10 @@ def _ptr(t: Optional[torch.Tensor]):
 
 
 def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
-               bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False):
+               bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0):
     """Fill an ``attn_args`` from tensors.  Returns (args, tensors kept alive).
-    off_by_one: the off-by-one softmax (an extra column of logit 0 per row, no gradient)."""
+    off_by_one: the off-by-one softmax (an extra column of logit 0 per row, no gradient).
+    kv_splits: split-KV forward into that many key shares per query tile (0 / 1: off)."""
     if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share dtype bfloat16 or float32")
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -74,6 +75,7 @@ def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale
         keep.append(sink)
     a.scale = float(D ** -0.5 if scale is None else scale)
     a.softmax_type = _capi.ATTN_SOFTMAX_OFF_BY_ONE if off_by_one else _capi.ATTN_SOFTMAX_DEFAULT
+    a.kv_splits = int(kv_splits)
     return a, keep
 
 
@@ -97,11 +99,12 @@ def _check(status: int, where: str):
 
 
 def attn_fwd(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
-             bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, out=None, lse=None):
+             bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0,
+             out=None, lse=None):
     """Forward: returns (O [B,Sq,Hq,D] in q's dtype, LSE [B,Hq,Sq] float32)."""
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
                          scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
-                         off_by_one=off_by_one)
+                         off_by_one=off_by_one, kv_splits=kv_splits)
     L = lib()
     need = L.attn_fwd_workspace_size(ctypes.byref(a))
     if need == 0:
@@ -117,13 +120,13 @@ def attn_fwd(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=N
 
 
 def attn_fwd_noalloc(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
-                     bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, out=None,
-                     lse=None):
+                     bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0,
+                     out=None, lse=None):
     """attn_fwd with the library's built-in scratch instead of a workspace (for callers that
     cannot allocate device memory; see include/attn_gb300.h).  Returns (O, LSE)."""
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
                          scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
-                         off_by_one=off_by_one)
+                         off_by_one=off_by_one, kv_splits=kv_splits)
     B, Sq, Hq, D = q.shape
     O = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device) if out is None else out
     LSE = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
@@ -134,8 +137,9 @@ def attn_fwd_noalloc(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None,
 
 
 def attn_bwd(q, k, v, O, LSE, dO, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
-             bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False):
-    """Backward: returns (dQ, dK, dV, dbias or None, dsink or None)."""
+             bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0):
+    """Backward: returns (dQ, dK, dV, dbias or None, dsink or None).  (kv_splits, a forward
+    setting, is accepted and ignored so that one set of keyword arguments serves both.)"""
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
                          scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
                          off_by_one=off_by_one)

@@ -51,7 +51,7 @@ class AttnArgs(ctypes.Structure):
         ("cu_seqlens", ctypes.c_void_p), ("nseq", ctypes.c_int),
         ("causal", ctypes.c_int), ("window", ctypes.c_int),
         ("softcap", ctypes.c_float), ("sink", ctypes.c_void_p), ("scale", ctypes.c_float),
-        ("softmax_type", ctypes.c_int),
+        ("softmax_type", ctypes.c_int), ("kv_splits", ctypes.c_int),
     ]
 
 

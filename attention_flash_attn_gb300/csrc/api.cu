@@ -24,6 +24,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 struct Layout {
   size_t status = 0, mono = 0, qrange = 0, krange = 0, seg = 0;
   size_t dvec = 0, lse2 = 0, dsink_part = 0, dqacc = 0, dbias_acc = 0;
+  size_t o_part = 0, lse_part = 0;
   size_t total = 0;
 };
 
@@ -31,6 +32,10 @@ bool use_tc(const attn_args *a) {
   return a->dtype == ATTN_DTYPE_BF16 && a->bias == nullptr && a->Sk > 0 && tc_supported(a->D);
 }
 bool use_tc_bwd(const attn_args *a) { return use_tc(a) && tc_bwd_supported(a->D); }
+
+constexpr int kMaxKvSplits = 64;
+// The split-KV forward applies to the tensor-core path only.
+bool split_kv(const attn_args *a) { return a->kv_splits > 1 && use_tc(a); }
 
 size_t dbias_elems(const attn_args *a) {
   if (!a->bias) return 0;
@@ -48,6 +53,11 @@ Layout layout(const attn_args *a, bool bwd) {
     L.qrange = off; off += align_up((size_t)a->B * nq * sizeof(int2));
     L.krange = off; off += align_up((size_t)a->B * nk * sizeof(int2));
     if (a->cu_seqlens) { L.seg = off; off += align_up((size_t)a->Sq * sizeof(int)); }
+  }
+  if (!bwd && split_kv(a)) {
+    const size_t rows = (size_t)a->kv_splits * a->B * a->Hq * a->Sq;
+    L.o_part = off; off += align_up(rows * a->D * sizeof(float));
+    L.lse_part = off; off += align_up(rows * sizeof(float));
   }
   if (bwd) {
     const size_t sq_pad = (size_t)(a->Sq + 127) / 128 * 128;
@@ -88,6 +98,7 @@ int validate(const attn_args *a) {
   if ((a->seg_q == nullptr) != (a->seg_k == nullptr)) return ATTN_ERR_INVALID;
   if (a->softmax_type != ATTN_SOFTMAX_DEFAULT && a->softmax_type != ATTN_SOFTMAX_OFF_BY_ONE) return ATTN_ERR_INVALID;
   if (a->softmax_type == ATTN_SOFTMAX_OFF_BY_ONE && a->sink) return ATTN_ERR_INVALID;
+  if (a->kv_splits < 0 || a->kv_splits > kMaxKvSplits) return ATTN_ERR_INVALID;
   if (a->cu_seqlens) {
     if (a->seg_q) return ATTN_ERR_UNSUPPORTED;
     if (a->B != 1 || a->Sq != a->Sk || a->nseq < 0) return ATTN_ERR_INVALID;
@@ -189,9 +200,15 @@ int attn_fwd(const attn_args *a, void *O, float *LSE, void *ws, size_t ws_bytes,
   Params p = make_params(a, static_cast<char *>(ws), L);
   p.O = O;
   p.LSE = LSE;
+  if (split_kv(a)) {
+    p.kv_splits = a->kv_splits;
+    p.o_part = reinterpret_cast<float *>(static_cast<char *>(ws) + L.o_part);
+    p.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + L.lse_part);
+  }
   if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
   MainKernelEvents ev(st);
   cudaError_t e = use_tc(a) ? tc_forward(p, st) : simt_forward(p, a->dtype, st);
+  if (e == cudaSuccess && p.kv_splits > 1) e = launch_splitkv_merge(p, st);
   ev.done();
   return cuda_status(e);
 }

@@ -35,6 +35,11 @@ struct Params {
   const unsigned char *seg_mono;  // [B]: 1 if seg_q and seg_k rows are non-decreasing
   const float *sink;              // [Hq] or null
   int off_by_one;                 // one extra column of logit 0 per row (no sink array)
+  // Split-KV forward (kv_splits > 1): each split writes its normalised partial output and LSE
+  // (without the sink column) here; a merge kernel combines them.
+  int kv_splits;
+  float *o_part;                  // [kv_splits, B, Hq, Sq, D]
+  float *lse_part;                // [kv_splits, B, Hq, Sq]
   // forward outputs / backward inputs
   void *O;
   float *LSE;

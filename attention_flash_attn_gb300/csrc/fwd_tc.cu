@@ -154,9 +154,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // One-dimensional grid, query tile slowest: every (batch, head) takes its latest (heaviest
   // under causal) tile before any takes an earlier one, so the last wave holds the light tiles.
+  // With a split-KV forward the split index varies fastest.
   const int nqt = (p.Sq + kBM - 1) / kBM;
-  const int bh = (int)(blockIdx.x % (unsigned)(p.Hq * p.B));
-  const int qt = nqt - 1 - (int)(blockIdx.x / (unsigned)(p.Hq * p.B));
+  const int ns = p.kv_splits > 1 ? p.kv_splits : 1;
+  const int bhs = (int)(blockIdx.x % (unsigned)(p.Hq * p.B * ns));
+  const int qt = nqt - 1 - (int)(blockIdx.x / (unsigned)(p.Hq * p.B * ns));
+  const int split = bhs % ns, bh = bhs / ns;
   const int h = bh % p.Hq, b = bh / p.Hq, g = h / p.G;
   const int i0 = qt * kBM, i1 = min(i0 + kBM, p.Sq) - 1;
   const int off = p.Sk - p.Sq;
@@ -171,8 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     klo = max(klo, min(a.x, c.x));
     khi = min(khi, max(a.y, c.y));
   }
-  const int t0 = klo / BN;
-  const int n = (klo < khi) ? (khi + BN - 1) / BN - t0 : 0;
+  const int tv0 = klo / BN;
+  const int nv = (klo < khi) ? (khi + BN - 1) / BN - tv0 : 0;
+  // Split s of ns takes key tiles [tv0 + s nv / ns, tv0 + (s + 1) nv / ns) of the visible ones.
+  const int t0 = tv0 + (int)((long long)split * nv / ns);
+  const int n = tv0 + (int)((long long)(split + 1) * nv / ns) - t0;
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t q_full = bar0;
@@ -334,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
 
     const FwdScore ks(p.scale, p.inv_cap, p.cap);
-    const bool sink_col = has_sink_col(p);
+    const bool sink_col = has_sink_col(p) && ns == 1;  // split partials leave it to the merge
     float m_ref = sink_col ? sink_logit(p, h) * kLog2e : -INFINITY;  // running max (log2 units)
     float l = (sink_col && half == 0) ? 1.f : 0.f;                   // this half's sum relative to m_ref
     bool ok = true;
@@ -439,29 +445,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool has = l > 0.f;
     const float inv = has ? 1.f / l : 0.f;
     const float lse = has ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
-    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) + (((size_t)b * p.Sq + i) * p.Hq + h) * D;
+    if (ns > 1) {
+      // Split partial: this split's normalised output (fp32) and its LSE, for the merge.
+      const size_t prow = (((size_t)split * p.B + b) * p.Hq + h) * p.Sq + i;
+      float *op = p.o_part + prow * D;
 #pragma unroll 1
-    for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
-      uint32_t orr[32];
-      if (n > 0) {
-        tmem_ld32(lane_addr + C::TM_O + c * 32, orr);
-        tmem_wait_ld();
-        reg_fence(orr);
-      } else {
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
+        uint32_t orr[32];
+        if (n > 0) {
+          tmem_ld32(lane_addr + C::TM_O + c * 32, orr);
+          tmem_wait_ld();
+          reg_fence(orr);
+        } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) orr[e] = 0u;
+          for (int e = 0; e < 32; ++e) orr[e] = 0u;
+        }
+        if (row_ok) {
+          float4 *dst = reinterpret_cast<float4 *>(op + c * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(orr[4 * v]) * inv, __uint_as_float(orr[4 * v + 1]) * inv,
+                                 __uint_as_float(orr[4 * v + 2]) * inv, __uint_as_float(orr[4 * v + 3]) * inv);
+        }
       }
-      if (row_ok) {
-        uint32_t out[16];
+      if (row_ok && half == 0) p.lse_part[prow] = lse;
+    } else {
+      __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) + (((size_t)b * p.Sq + i) * p.Hq + h) * D;
+#pragma unroll 1
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
+        uint32_t orr[32];
+        if (n > 0) {
+          tmem_ld32(lane_addr + C::TM_O + c * 32, orr);
+          tmem_wait_ld();
+          reg_fence(orr);
+        } else {
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          out[e] = pack_bf16(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+          for (int e = 0; e < 32; ++e) orr[e] = 0u;
+        }
+        if (row_ok) {
+          uint32_t out[16];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
+          for (int e = 0; e < 16; ++e)
+            out[e] = pack_bf16(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
+        }
       }
+      if (row_ok && half == 0) p.LSE[((size_t)b * p.Hq + h) * p.Sq + i] = lse;
     }
-    if (row_ok && half == 0) p.LSE[((size_t)b * p.Hq + h) * p.Sq + i] = lse;
   }
 
   __syncwarp();  // every warp reconverges (producer lanes leave their loops at different times)
@@ -484,7 +516,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   auto kern = p.cap > 0.f ? fwd_tc_kernel<D, BN, NK, NV, true> : fwd_tc_kernel<D, BN, NK, NV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const long long nblk = (long long)((p.Sq + kBM - 1) / kBM) * p.Hq * p.B;
+  const long long nblk = (long long)((p.Sq + kBM - 1) / kBM) * p.Hq * p.B * (p.kv_splits > 1 ? p.kv_splits : 1);
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<(unsigned)nblk, kThreads, C::SMEM, st>>>(tq, tk, tv, p);
   return counted(cudaGetLastError());

@@ -38,6 +38,10 @@ int bwd_pre_partials(int B, int Sq);  // partial sums per head the preprocess wr
 cudaError_t launch_bwd_post(const Params &p, int dtype, bool convert_dq, size_t dbias_elems,
                             cudaStream_t st);
 
+// Split-KV forward: merges the kv_splits partial outputs / LSEs into O and LSE, adding the
+// sink (or off-by-one) column once.
+cudaError_t launch_splitkv_merge(const Params &p, cudaStream_t st);
+
 // tcgen05 tensor-core kernels (bf16, D in {64, 128, 256}).
 bool tc_supported(int D);      // forward
 bool tc_bwd_supported(int D);  // backward

@@ -147,8 +147,10 @@ def run_ours(args, rank, world, local_rank):
     inp = make_inputs(w)
     seg = inp["seg"]
     t = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    if args.kv_splits is not None:
+        w = w.replace(kv_splits=args.kv_splits)
     kw = dict(causal=w.causal, window=w.window, softcap=w.softcap, sink=t["sink"], scale=w.scale,
-              bias=t["bias"], seg_q=t["seg"], seg_k=t["seg"])
+              bias=t["bias"], seg_q=t["seg"], seg_k=t["seg"], kv_splits=w.kv_splits)
     path = fa.attn_path_name(t["q"], t["k"], t["v"], **kw)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -262,7 +264,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,s^2) inputs of the workload's shape; no dataset)",
         "config": {"workload": w.name, "B": w.B, "S": w.Sq, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                    "causal": w.causal, "window": w.window, "softcap": w.softcap, "sink": w.sink,
-                   "segments": w.segments, "visible_pairs": visible_pairs(w, seg),
+                   "segments": w.segments, "kv_splits": w.kv_splits, "visible_pairs": visible_pairs(w, seg),
                    "kernel_path": path, "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
         "pct_of_bf16_peak": round(100 * value / burst, 2),
@@ -286,15 +288,16 @@ def run_ours(args, rank, world, local_rank):
 # ------------------------------------------------------------------ oracle (CPU) arm
 
 def oracle_sample(w: Workload, inp: dict, S: int):
-    """The workload cut to its first S tokens, batch 0 and kv group 0 (all rows and keys of
-    that cut): a bounded sample of the same shapes, masks and value distributions."""
+    """The workload cut to its first S query rows and keys, batch 0 and kv group 0 (all rows and
+    keys of that cut): a bounded sample of the same shapes, masks and value distributions."""
     G = w.Hq // w.Hkv
-    sw = w.replace(B=1, Sq=S, Sk=S, Hq=G, Hkv=1)
-    sub = {"q": inp["q"][:1, :S, :G], "k": inp["k"][:1, :S, :1], "v": inp["v"][:1, :S, :1],
-           "dO": inp["dO"][:1, :S, :G],
-           "bias": None if inp["bias"] is None else inp["bias"][:1, :G, :S, :S],
+    sq, sk = min(S, w.Sq), min(S, w.Sk)
+    sw = w.replace(B=1, Sq=sq, Sk=sk, Hq=G, Hkv=1)
+    sub = {"q": inp["q"][:1, :sq, :G], "k": inp["k"][:1, :sk, :1], "v": inp["v"][:1, :sk, :1],
+           "dO": inp["dO"][:1, :sq, :G],
+           "bias": None if inp["bias"] is None else inp["bias"][:1, :G, :sq, :sk],
            "sink": None if inp["sink"] is None else inp["sink"][:G],
-           "seg": None if inp["seg"] is None else inp["seg"][:1, :S]}
+           "seg": None if inp["seg"] is None else inp["seg"][:1, :sq]}
     return sw, sub
 
 
@@ -364,6 +367,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-splits", type=int, default=None,
+                    help="split-KV forward shares per query tile (default: the workload's)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -119,6 +119,16 @@ typedef struct {
     float scale;               /* finite; usually 1/sqrt(D)                                 */
     int softmax_type;          /* enum attn_softmax_type; zero-initialised = DEFAULT.  Any
                                   other value, or OFF_BY_ONE with a sink: ATTN_ERR_INVALID  */
+    /* Split-KV forward, for rows too few to fill the GPU (decode-like shapes, long keys):
+     * 0 or 1: off.  n in 2..64: the tensor-core forward splits every query tile's visible key
+     * tiles into n contiguous shares, one CTA each, and a merge kernel combines their
+     * normalised partial outputs and log-normalisers, adding the sink or off-by-one column
+     * exactly once per row (TransformerEngine PR #3551, "What changed": the sink enters each
+     * row once when tiles' statistics are merged).  The workspace grows by
+     * n * B * Hq * Sq * (D + 1) * 4 bytes.  Results equal the unsplit forward up to rounding.
+     * The FFMA path (fp32 inputs, or a bias) computes unsplit.  Other values:
+     * ATTN_ERR_INVALID.  The backward ignores this field.                                   */
+    int kv_splits;
 } attn_args;
 
 /* Bytes of workspace attn_fwd needs for these arguments (256-byte multiple, >= 256). */
@@ -191,7 +201,8 @@ const char *attn_path_name(const attn_args *a);
  * Profiling hook: the next attn_fwd or attn_bwd call made by this host thread records
  * `ev_start` (a cudaEvent_t) on its stream immediately before launching its main kernel
  * (the tensor-core or FFMA attention kernel; for the FFMA backward, the first of its two)
- * and `ev_end` immediately after its last main kernel, then forgets both.  Passing NULLs
+ * and `ev_end` immediately after its last main kernel (with kv_splits, the merge), then
+ * forgets both.  Passing NULLs
  * cancels a pending request.  Adds no work to the call.
  */
 void attn_profile_next_main_kernel(void *ev_start, void *ev_end);

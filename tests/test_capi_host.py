@@ -56,6 +56,7 @@ def valid_args(capi, dtype=1, B=1, S=16, H=2, D=64, **kw):
     ("softcap", -1.0, 1), ("softcap", float("nan"), 1), ("softcap", float("inf"), 1),
     ("scale", float("inf"), 1), ("q", None, 1), ("q", 0x10008, 1), ("q_stride_s", 12, 1),
     ("Sq", -1, 1), ("seg_q", 0x20000, 1), ("softmax_type", 2, 1), ("softmax_type", -1, 1),
+    ("kv_splits", -1, 1), ("kv_splits", 65, 1),
 ])
 def test_invalid_arguments_rejected_before_launch(capi, field, value, status):
     L = capi.lib()
@@ -84,6 +85,22 @@ def test_off_by_one_softmax_arguments(capi):
     a = valid_args(capi, softmax_type=capi.ATTN_SOFTMAX_OFF_BY_ONE, sink=0x60000)
     assert L.attn_fwd_workspace_size(ctypes.byref(a)) == 0
     assert L.attn_fwd(ctypes.byref(a), 0x30000, 0x40000, 0x50000, 1 << 20, None) == 1
+
+
+def test_kv_splits_workspace(capi):
+    """A split-KV forward adds n * B * Hq * Sq * (D + 1) floats of partials to the forward's
+    workspace (tensor-core path: bf16 without a bias); the backward's is unchanged, and the
+    FFMA path (fp32) computes unsplit."""
+    L = capi.lib()
+    ws = lambda **kw: L.attn_fwd_workspace_size(ctypes.byref(valid_args(capi, S=100, **kw)))
+    base = ws()
+    for n in (2, 7, 64):
+        assert ws(kv_splits=n) >= base + n * 1 * 2 * 100 * (64 + 1) * 4
+    assert ws(kv_splits=1) == base
+    bw = lambda **kw: L.attn_bwd_workspace_size(ctypes.byref(valid_args(capi, S=100, **kw)))
+    assert bw(kv_splits=7) == bw()
+    f32 = lambda **kw: L.attn_fwd_workspace_size(ctypes.byref(valid_args(capi, dtype=2, S=100, **kw)))
+    assert f32(kv_splits=7) == f32()
 
 
 def test_cu_seqlens_with_segments_unsupported_and_shape_rules(capi):

@@ -131,6 +131,54 @@ def test_off_by_one_softmax(w):
     assert not torch.equal(gpu["LSE"], van["LSE"])
 
 
+# Split-KV forward (forced split counts), on decode-like rows (one query tile, many keys,
+# bottom-right causal with Sq < Sk) and on the edge cases of the key split: more splits than
+# key tiles (empty shares), windows and segments that leave shares empty, off-by-one.
+SPLITS = [
+    (Workload("split_decode_d128_sink", "bf16", B=2, Sq=64, Sk=3000, Hq=8, Hkv=2, D=128, causal=True,
+              softcap=30.0, sink=True, q_std=3.0), (2, 5, 16)),
+    (Workload("split_d64_more_splits_than_tiles", "bf16", B=1, Sq=150, Sk=200, Hq=4, Hkv=1, D=64,
+              causal=True, softcap=20.0, sink=True, q_std=2.0), (3, 8)),
+    (Workload("split_d256_window_segments", "bf16", B=2, Sq=300, Sk=300, Hq=4, Hkv=2, D=256, causal=True,
+              window=120, softcap=50.0, segments=True, run_lo=40, run_hi=150, q_std=3.0), (3,)),
+    (Workload("split_d64_noncausal_long_keys", "bf16", B=1, Sq=20, Sk=5000, Hq=4, Hkv=4, D=64,
+              causal=False, softcap=0.0), (7,)),
+]
+
+
+@pytest.mark.parametrize("w,splits", SPLITS, ids=lambda x: x.name if hasattr(x, "name") else str(x))
+def test_split_kv_forward(w, splits):
+    """Each forced split count against the oracle (the backward runs from the merged LSE), and
+    against the unsplit forward: same O up to bf16 rounding, LSE to fp32 rounding."""
+    inp = make_inputs(w)
+    ref = full_oracle(w, inp)
+    base = run_gpu(w, inp)
+    for n in splits:
+        gpu = run_gpu(w, inp, kv_splits=n)
+        check(w, gpu, ref)
+        fin = torch.isfinite(base["LSE"])
+        assert torch.equal(fin, torch.isfinite(gpu["LSE"]))
+        assert float((gpu["LSE"][fin] - base["LSE"][fin]).abs().max()) < 1e-4, n
+        assert frob_rel(to64(gpu["O"]), to64(base["O"])) < 4e-3, n
+
+
+def test_split_kv_off_by_one_and_noalloc():
+    """The merge adds the off-by-one column once; the no-allocation entry point takes the
+    partials from its built-in scratch when they fit."""
+    import attention_flash_attn_gb300 as fa
+    w = Workload("split_obo", "bf16", B=1, Sq=100, Sk=1500, Hq=4, Hkv=2, D=64, causal=True, softcap=10.0)
+    inp = make_inputs(w)
+    gpu = run_gpu(w, inp, off_by_one=True, kv_splits=4)
+    ref = full_oracle(w, dict(inp, sink=torch.zeros(w.Hq, dtype=torch.float32)))
+    ref["dsink"] = None
+    check(w, gpu, ref)
+    t = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    O1, L1 = fa.attn_fwd_noalloc(t["q"], t["k"], t["v"], causal=True, softcap=10.0, scale=w.scale,
+                                 off_by_one=True, kv_splits=4)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, gpu["O"]) and torch.equal(L1, gpu["LSE"])
+
+
 def test_fully_masked_rows_with_and_without_sink():
     """Queries whose segment id has no key: O = 0, LSE = -inf (no sink) or sink."""
     w = Workload("masked_rows", "bf16", B=1, Sq=160, Sk=160, Hq=2, Hkv=1, D=64, causal=False)

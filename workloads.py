@@ -45,6 +45,7 @@ class Workload:
     run_lo: int = 64
     run_hi: int = 4096
     seed: int = 0
+    kv_splits: int = 0       # split-KV forward: key shares per query tile (0: off)
 
     @property
     def scale(self) -> float:
@@ -77,6 +78,10 @@ WORKLOADS = {
                  causal=True, softcap=50.0, q_std=3.0),
         Workload("long_noncausal_16k_cap50", "bf16", B=1, Sq=16384, Sk=16384, Hq=32, Hkv=16, D=256,
                  causal=False, softcap=50.0, q_std=3.0),
+        # Decode-like rows for the split-KV forward: one 128-row query tile per head against
+        # 32k keys (bottom-right causal), too few query tiles to fill the GPU unsplit.
+        Workload("decode_sq128_sk32k_cap30_sink", "bf16", B=1, Sq=128, Sk=32768, Hq=32, Hkv=8, D=128,
+                 causal=True, softcap=30.0, q_std=3.0, sink=True, kv_splits=4),
     ]
 }
 
