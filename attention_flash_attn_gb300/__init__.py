@@ -27,8 +27,10 @@ def _ptr(t: Optional[torch.Tensor]):
 
 
 def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
-               bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0):
+               bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0,
+               cu_seqlens_k=None):
     """Fill an ``attn_args`` from tensors.  Returns (args, tensors kept alive).
+    cu_seqlens_k: key boundaries of the cu_seqlens sequences (varlen with Sq != Sk per sequence).
     off_by_one: the off-by-one softmax (an extra column of logit 0 per row, no gradient).
     kv_splits: split-KV forward into that many key shares per query tile (0 / 1: off)."""
     if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
@@ -66,6 +68,12 @@ def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale
         cu = cu_seqlens.to(torch.int32).contiguous()
         a.cu_seqlens, a.nseq = cu.data_ptr(), cu.numel() - 1
         keep.append(cu)
+    if cu_seqlens_k is not None:
+        cuk = cu_seqlens_k.to(torch.int32).contiguous()
+        if cu_seqlens is None or cuk.numel() != a.nseq + 1:
+            raise ValueError("cu_seqlens_k needs cu_seqlens with the same number of sequences")
+        a.cu_seqlens_k = cuk.data_ptr()
+        keep.append(cuk)
     a.causal = int(bool(causal))
     a.window = int(window)
     a.softcap = float(softcap)
@@ -100,11 +108,11 @@ def _check(status: int, where: str):
 
 def attn_fwd(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
              bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0,
-             out=None, lse=None):
+             cu_seqlens_k=None, out=None, lse=None):
     """Forward: returns (O [B,Sq,Hq,D] in q's dtype, LSE [B,Hq,Sq] float32)."""
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
                          scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
-                         off_by_one=off_by_one, kv_splits=kv_splits)
+                         off_by_one=off_by_one, kv_splits=kv_splits, cu_seqlens_k=cu_seqlens_k)
     L = lib()
     need = L.attn_fwd_workspace_size(ctypes.byref(a))
     if need == 0:
@@ -121,12 +129,12 @@ def attn_fwd(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=N
 
 def attn_fwd_noalloc(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
                      bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0,
-                     out=None, lse=None):
+                     cu_seqlens_k=None, out=None, lse=None):
     """attn_fwd with the library's built-in scratch instead of a workspace (for callers that
     cannot allocate device memory; see include/attn_gb300.h).  Returns (O, LSE)."""
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
                          scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
-                         off_by_one=off_by_one, kv_splits=kv_splits)
+                         off_by_one=off_by_one, kv_splits=kv_splits, cu_seqlens_k=cu_seqlens_k)
     B, Sq, Hq, D = q.shape
     O = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device) if out is None else out
     LSE = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
@@ -137,12 +145,13 @@ def attn_fwd_noalloc(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None,
 
 
 def attn_bwd(q, k, v, O, LSE, dO, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
-             bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0):
+             bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0,
+             cu_seqlens_k=None):
     """Backward: returns (dQ, dK, dV, dbias or None, dsink or None).  (kv_splits, a forward
     setting, is accepted and ignored so that one set of keyword arguments serves both.)"""
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
                          scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
-                         off_by_one=off_by_one)
+                         off_by_one=off_by_one, kv_splits=kv_splits, cu_seqlens_k=cu_seqlens_k)
     L = lib()
     need = L.attn_bwd_workspace_size(ctypes.byref(a))
     if need == 0:

@@ -52,6 +52,7 @@ class AttnArgs(ctypes.Structure):
         ("causal", ctypes.c_int), ("window", ctypes.c_int),
         ("softcap", ctypes.c_float), ("sink", ctypes.c_void_p), ("scale", ctypes.c_float),
         ("softmax_type", ctypes.c_int), ("kv_splits", ctypes.c_int),
+        ("cu_seqlens_k", ctypes.c_void_p),
     ]
 
 

@@ -22,7 +22,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Workspace carve-up.  Offsets are 0 when a region is absent.
 struct Layout {
-  size_t status = 0, mono = 0, qrange = 0, krange = 0, seg = 0;
+  size_t status = 0, mono = 0, qrange = 0, krange = 0, seg = 0, segk = 0, qoff = 0, koff = 0;
   size_t dvec = 0, lse2 = 0, dsink_part = 0, dqacc = 0, dbias_acc = 0;
   size_t o_part = 0, lse_part = 0;
   size_t total = 0;
@@ -53,6 +53,11 @@ Layout layout(const attn_args *a, bool bwd) {
     L.qrange = off; off += align_up((size_t)a->B * nq * sizeof(int2));
     L.krange = off; off += align_up((size_t)a->B * nk * sizeof(int2));
     if (a->cu_seqlens) { L.seg = off; off += align_up((size_t)a->Sq * sizeof(int)); }
+    if (a->cu_seqlens_k) {
+      L.segk = off; off += align_up((size_t)a->Sk * sizeof(int));
+      L.qoff = off; off += align_up((size_t)a->Sq * sizeof(int));
+      L.koff = off; off += align_up((size_t)a->Sk * sizeof(int));
+    }
   }
   if (!bwd && split_kv(a)) {
     const size_t rows = (size_t)a->kv_splits * a->B * a->Hq * a->Sq;
@@ -101,7 +106,10 @@ int validate(const attn_args *a) {
   if (a->kv_splits < 0 || a->kv_splits > kMaxKvSplits) return ATTN_ERR_INVALID;
   if (a->cu_seqlens) {
     if (a->seg_q) return ATTN_ERR_UNSUPPORTED;
-    if (a->B != 1 || a->Sq != a->Sk || a->nseq < 0) return ATTN_ERR_INVALID;
+    if (a->B != 1 || a->nseq < 0) return ATTN_ERR_INVALID;
+    if (!a->cu_seqlens_k && a->Sq != a->Sk) return ATTN_ERR_INVALID;
+  } else if (a->cu_seqlens_k) {
+    return ATTN_ERR_INVALID;
   }
   return ATTN_OK;
 }
@@ -133,6 +141,11 @@ Params make_params(const attn_args *a, char *ws, const Layout &L) {
     p.krange = reinterpret_cast<int2 *>(ws + L.krange);
     if (a->cu_seqlens) {
       p.seg_q = p.seg_k = reinterpret_cast<int *>(ws + L.seg);
+      if (a->cu_seqlens_k) {
+        p.seg_k = reinterpret_cast<int *>(ws + L.segk);
+        p.qoff = reinterpret_cast<int *>(ws + L.qoff);
+        p.koff = reinterpret_cast<int *>(ws + L.koff);
+      }
     } else {
       p.seg_q = a->seg_q;
       p.seg_k = a->seg_k;
@@ -161,10 +174,10 @@ struct MainKernelEvents {
 
 int run_meta(const attn_args *a, Params &p, cudaStream_t st) {
   if (!(a->seg_q || a->cu_seqlens) || a->B == 0) return ATTN_OK;
-  return cuda_status(launch_mask_meta(p, a->cu_seqlens, a->nseq, const_cast<int *>(p.seg_q),
-                                      const_cast<int *>(p.seg_k), const_cast<int2 *>(p.qrange),
-                                      const_cast<int2 *>(p.krange),
-                                      const_cast<unsigned char *>(p.seg_mono), st));
+  return cuda_status(launch_mask_meta(p, a->cu_seqlens, a->cu_seqlens_k, a->nseq, const_cast<int *>(p.seg_q),
+                                      const_cast<int *>(p.seg_k), const_cast<int *>(p.qoff),
+                                      const_cast<int *>(p.koff), const_cast<int2 *>(p.qrange),
+                                      const_cast<int2 *>(p.krange), const_cast<unsigned char *>(p.seg_mono), st));
 }
 
 }  // namespace

@@ -285,8 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Query rows that can see this key tile (uniform across the CTA).
   int qlo = 0, qhi = p.Sq;
-  if (p.causal) qlo = max(qlo, k0 - off);
-  if (p.window > 0) qhi = min(qhi, k1 - off + p.window);
+  if (!p.koff) {  // per-sequence offsets: the tile ranges below carry the causal / window bounds
+    if (p.causal) qlo = max(qlo, k0 - off);
+    if (p.window > 0) qhi = min(qhi, k1 - off + p.window);
+  }
   if (p.krange) {
     const int nt = (p.Sk + 63) / 64;
     const int2 a = p.krange[(size_t)b * nt + k0 / 64], c = p.krange[(size_t)b * nt + k1 / 64];
@@ -416,8 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Query interval [lo, hi) that sees this key; keys past Sk see nothing.
     int lo = 0, hi = p.Sq;
-    if (p.causal) lo = max(lo, k - off);
-    if (p.window > 0) hi = min(hi, k - off + p.window);
+    const int koff = key_ok ? key_off(p, k) : off;
+    if (p.causal) lo = max(lo, k - koff);
+    if (p.window > 0) hi = min(hi, k - koff + p.window);
     bool seg_pairwise = false;
     int sid = 0;
     const int *segq = nullptr;

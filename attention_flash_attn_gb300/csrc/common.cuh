@@ -33,6 +33,11 @@ struct Params {
   const int2 *qrange;             // [B, ceil(Sq/64)]: key range [x, y) of each 64-row query tile
   const int2 *krange;             // [B, ceil(Sk/64)]: query range [x, y) of each 64-key tile
   const unsigned char *seg_mono;  // [B]: 1 if seg_q and seg_k rows are non-decreasing
+  // Varlen with separate key boundaries (B == 1): per token, the causal / window offset of its
+  // sequence, end_k(s) - end_q(s) (bottom-right alignment within every sequence); null: the
+  // whole matrix's Sk - Sq.
+  const int *qoff;                // [Sq]
+  const int *koff;                // [Sk]
   const float *sink;              // [Hq] or null
   int off_by_one;                 // one extra column of logit 0 per row (no sink array)
   // Split-KV forward (kv_splits > 1): each split writes its normalised partial output and LSE
@@ -70,8 +75,12 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
   return __float2bfloat16_rn(x);
 }
 
-// Query position on the key axis (bottom-right alignment when Sq != Sk).
-__device__ __forceinline__ int qpos(const Params &p, int i) { return i + p.Sk - p.Sq; }
+// Query position on the key axis (bottom-right alignment when Sq != Sk, per sequence when
+// the sequences have their own key boundaries).
+__device__ __forceinline__ int qpos(const Params &p, int i) { return i + (p.qoff ? p.qoff[i] : p.Sk - p.Sq); }
+// The offset that places key j's sequence on the query axis (query i sees key j causally iff
+// j <= i + key_off(j) within one sequence).
+__device__ __forceinline__ int key_off(const Params &p, int j) { return p.koff ? p.koff[j] : p.Sk - p.Sq; }
 
 // Visibility of key j to query i of batch b: causal, sliding window, segment equality.
 __device__ __forceinline__ bool visible(const Params &p, int b, int i, int j) {

@@ -166,8 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Keys this query tile can see (uniform across the CTA).
   int klo = 0, khi = p.Sk;
-  if (p.window > 0) klo = max(klo, i0 + off - p.window + 1);
-  if (p.causal) khi = min(khi, i1 + off + 1);
+  if (!p.qoff) {  // per-sequence offsets: the tile ranges below carry the causal / window bounds
+    if (p.window > 0) klo = max(klo, i0 + off - p.window + 1);
+    if (p.causal) khi = min(khi, i1 + off + 1);
+  }
   if (p.qrange) {
     const int nt = (p.Sq + 63) / 64;
     const int2 a = p.qrange[(size_t)b * nt + i0 / 64], c = p.qrange[(size_t)b * nt + i1 / 64];
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = i < p.Sq;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
 
-    const int ip = i + off;
+    const int ip = row_ok ? qpos(p, i) : i + off;
     int lo = 0, hi = p.Sk;
     if (p.window > 0) lo = max(lo, ip - p.window + 1);
     if (p.causal) hi = min(hi, ip + 1);

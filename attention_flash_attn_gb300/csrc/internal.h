@@ -19,11 +19,11 @@ inline cudaError_t counted(cudaError_t e, int n = 1) {
 }
 
 // Mask metadata (segments / cu_seqlens): effective segment ids, per-batch monotonicity
-// and 64-granular tile ranges.  seg_q_out/seg_k_out are only written when cu_seqlens is
-// given (then B == 1).
-cudaError_t launch_mask_meta(const Params &p, const int *cu_seqlens, int nseq,
-                             int *seg_q_out, int *seg_k_out, int2 *qrange, int2 *krange,
-                             unsigned char *mono, cudaStream_t st);
+// and 64-granular tile ranges.  seg_q_out is only written when cu_seqlens is given (then
+// B == 1); seg_k_out, qoff_out and koff_out only when cu_seqlens_k is given as well.
+cudaError_t launch_mask_meta(const Params &p, const int *cu_seqlens, const int *cu_seqlens_k, int nseq,
+                             int *seg_q_out, int *seg_k_out, int *qoff_out, int *koff_out, int2 *qrange,
+                             int2 *krange, unsigned char *mono, cudaStream_t st);
 
 // fp32 FFMA kernels (any dtype; used for fp32 inputs and calls with a bias).
 cudaError_t simt_forward(const Params &p, int dtype, cudaStream_t st);

@@ -70,8 +70,10 @@ __device__ __forceinline__ void score(const Params &p, float s, int b, int h, in
 __device__ __forceinline__ void key_range(const Params &p, int b, int i0, int i1, int &lo, int &hi) {
   lo = 0;
   hi = p.Sk;
-  if (p.causal) hi = min(hi, qpos(p, i1) + 1);
-  if (p.window > 0) lo = max(lo, qpos(p, i0) - p.window + 1);
+  if (!p.qoff) {  // per-sequence offsets: the tile ranges below carry the causal / window bounds
+    if (p.causal) hi = min(hi, qpos(p, i1) + 1);
+    if (p.window > 0) lo = max(lo, qpos(p, i0) - p.window + 1);
+  }
   if (p.qrange) {
     const int nt = (p.Sq + 63) / 64;
     int2 a = p.qrange[(size_t)b * nt + i0 / 64], c = p.qrange[(size_t)b * nt + i1 / 64];
@@ -84,9 +86,11 @@ __device__ __forceinline__ void key_range(const Params &p, int b, int i0, int i1
 __device__ __forceinline__ void query_range(const Params &p, int b, int j0, int j1, int &lo, int &hi) {
   lo = 0;
   hi = p.Sq;
-  const int off = p.Sk - p.Sq;
-  if (p.causal) lo = max(lo, j0 - off);
-  if (p.window > 0) hi = min(hi, j1 - off + p.window);
+  if (!p.koff) {
+    const int off = p.Sk - p.Sq;
+    if (p.causal) lo = max(lo, j0 - off);
+    if (p.window > 0) hi = min(hi, j1 - off + p.window);
+  }
   if (p.krange) {
     const int nt = (p.Sk + 63) / 64;
     int2 a = p.krange[(size_t)b * nt + j0 / 64], c = p.krange[(size_t)b * nt + j1 / 64];

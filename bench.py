@@ -36,11 +36,21 @@ L2_BYTES = 129 * 2 ** 20
 
 # ------------------------------------------------------------------ algorithmic work
 
-def visible_pairs(w: Workload, seg) -> int:
+def visible_pairs(w: Workload, seg, bounds=None) -> int:
     """Visible (b, h, i, j) pairs under causal / window / contiguous-segment masking.
 
     Per query row the visible keys form one interval [lo, hi); segments are runs of equal
-    ids (seg [B, S] with Sq == Sk)."""
+    ids (seg [B, S] with Sq == Sk).  bounds: (cu_q, cu_k) of a thd varlen batch (B = 1),
+    bottom-right aligned within every sequence (tokens past the last bounds form one more)."""
+    if bounds is not None:
+        cq = [int(x) for x in bounds[0]] + [w.Sq]
+        ck = [int(x) for x in bounds[1]] + [w.Sk]
+        total = 0
+        for s in range(len(cq) - 1):
+            part = w.replace(B=1, Sq=cq[s + 1] - cq[s], Sk=ck[s + 1] - ck[s], thd_prefix=False)
+            if part.Sq > 0 and part.Sk > 0:
+                total += visible_pairs(part, None)
+        return total
     off = w.Sk - w.Sq
     ip = np.arange(w.Sq, dtype=np.int64) + off
     hi = np.minimum(ip + 1, w.Sk) if w.causal else np.full(w.Sq, w.Sk, np.int64)
@@ -60,9 +70,9 @@ def visible_pairs(w: Workload, seg) -> int:
     return total * w.Hq
 
 
-def flops(w: Workload, seg, which: str) -> float:
+def flops(w: Workload, seg, which: str, bounds=None) -> float:
     per_pair = {"fwd": 4, "bwd": 10, "fwdbwd": 14}[which] * w.D
-    return float(visible_pairs(w, seg)) * per_pair
+    return float(visible_pairs(w, seg, bounds)) * per_pair
 
 
 # ------------------------------------------------------------------ clocks
@@ -150,7 +160,9 @@ def run_ours(args, rank, world, local_rank):
     if args.kv_splits is not None:
         w = w.replace(kv_splits=args.kv_splits)
     kw = dict(causal=w.causal, window=w.window, softcap=w.softcap, sink=t["sink"], scale=w.scale,
-              bias=t["bias"], seg_q=t["seg"], seg_k=t["seg"], kv_splits=w.kv_splits)
+              bias=t["bias"], seg_q=t["seg"], seg_k=t["seg"], kv_splits=w.kv_splits,
+              cu_seqlens=t["cu_q"], cu_seqlens_k=t["cu_k"])
+    bounds = None if inp["cu_q"] is None else (inp["cu_q"], inp["cu_k"])
     path = fa.attn_path_name(t["q"], t["k"], t["v"], **kw)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -240,15 +252,15 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(tt.item())
 
-    f_step = flops(w, seg, "fwdbwd")
+    f_step = flops(w, seg, "fwdbwd", bounds)
     value = f_step * args.steps * world / (total_ms * 1e-3) / 1e12
     e2e_value = f_step * args.steps * world / (e2e_ms * 1e-3) / 1e12
     burst, sustained, kind = peaks()
     # Dominant kernel: the backward main kernel (10*D flops per visible pair).
     bwd_kernel_ms = statistics.mean(bwd_ms)
     fwd_kernel_ms = statistics.mean(fwd_ms)
-    bwd_tf = flops(w, seg, "bwd") / (bwd_kernel_ms * 1e-3) / 1e12
-    fwd_tf = flops(w, seg, "fwd") / (fwd_kernel_ms * 1e-3) / 1e12
+    bwd_tf = flops(w, seg, "bwd", bounds) / (bwd_kernel_ms * 1e-3) / 1e12
+    fwd_tf = flops(w, seg, "fwd", bounds) / (fwd_kernel_ms * 1e-3) / 1e12
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -264,7 +276,8 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,s^2) inputs of the workload's shape; no dataset)",
         "config": {"workload": w.name, "B": w.B, "S": w.Sq, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                    "causal": w.causal, "window": w.window, "softcap": w.softcap, "sink": w.sink,
-                   "segments": w.segments, "kv_splits": w.kv_splits, "visible_pairs": visible_pairs(w, seg),
+                   "segments": w.segments, "kv_splits": w.kv_splits, "thd_prefix": w.thd_prefix,
+                   "visible_pairs": visible_pairs(w, seg, bounds),
                    "kernel_path": path, "l2": "flushed before every timed step (256 MiB write)",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
         "pct_of_bf16_peak": round(100 * value / burst, 2),
@@ -292,7 +305,9 @@ def oracle_sample(w: Workload, inp: dict, S: int):
     keys of that cut): a bounded sample of the same shapes, masks and value distributions."""
     G = w.Hq // w.Hkv
     sq, sk = min(S, w.Sq), min(S, w.Sk)
-    sw = w.replace(B=1, Sq=sq, Sk=sk, Hq=G, Hkv=1)
+    if inp.get("cu_q") is not None:  # thd varlen: the first sequence, whole
+        sq, sk = int(inp["cu_q"][1]), int(inp["cu_k"][1])
+    sw = w.replace(B=1, Sq=sq, Sk=sk, Hq=G, Hkv=1, thd_prefix=False)
     sub = {"q": inp["q"][:1, :sq, :G], "k": inp["k"][:1, :sk, :1], "v": inp["v"][:1, :sk, :1],
            "dO": inp["dO"][:1, :sq, :G],
            "bias": None if inp["bias"] is None else inp["bias"][:1, :G, :sq, :sk],
@@ -324,8 +339,8 @@ def cpu_baseline(w: Workload, inp: dict, seg):
     f = flops(sw, sub["seg"], "fwdbwd")
     return {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd on the first {S} tokens of batch 0, kv group 0 "
-                      f"({sw.Hq} query heads) of {w.name}; {dt:.1f} s"}
+            "sample": f"fp64 oracle fwd+bwd on the first {sw.Sq} query rows and {sw.Sk} keys of batch 0, "
+                      f"kv group 0 ({sw.Hq} query heads) of {w.name}; {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -343,8 +358,8 @@ def run_reference(args):
     f = flops(sw, sub["seg"], "fwdbwd")
     value = f * len(times) / sum(times) / 1e12
     cores = len(os.sched_getaffinity(0))
-    sample = (f"fp64 oracle fwd+bwd on the first {S} tokens of batch 0, kv group 0 "
-              f"({sw.Hq} query heads) of {w.name}")
+    sample = (f"fp64 oracle fwd+bwd on the first {sw.Sq} query rows and {sw.Sk} keys of batch 0, "
+              f"kv group 0 ({sw.Hq} query heads) of {w.name}")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,

@@ -106,8 +106,8 @@ typedef struct {
      * non-decreasing ids additionally let the kernels skip whole tiles.                   */
     const int32_t *seg_q, *seg_k;
     /* Alternative to seg_q/seg_k (not both): cu_seqlens [nseq+1] int32 with
-     * cu_seqlens[0] == 0, non-decreasing, cu_seqlens[nseq] <= Sq; requires B == 1 and
-     * Sq == Sk.  Token t belongs to sequence s with cu[s] <= t < cu[s+1]; tokens at or past
+     * cu_seqlens[0] == 0, non-decreasing, cu_seqlens[nseq] <= Sq; requires B == 1 and, unless
+     * cu_seqlens_k gives the keys their own boundaries, Sq == Sk.  Token t belongs to sequence s with cu[s] <= t < cu[s+1]; tokens at or past
      * cu[nseq] form one extra trailing sequence.  A malformed array is reported through the
      * device status word.                                                                  */
     const int32_t *cu_seqlens;
@@ -129,6 +129,17 @@ typedef struct {
      * The FFMA path (fp32 inputs, or a bias) computes unsplit.  Other values:
      * ATTN_ERR_INVALID.  The backward ignores this field.                                   */
     int kv_splits;
+    /* Optional key boundaries for cu_seqlens ("thd" varlen with Sq != Sk per sequence):
+     * cu_seqlens_k [nseq+1] int32 with the same rules on the key axis (cu_seqlens_k[nseq] <=
+     * Sk).  Sequence s then holds queries [cu_seqlens[s], cu_seqlens[s+1]) and keys
+     * [cu_seqlens_k[s], cu_seqlens_k[s+1]); tokens past either end form the trailing sequence
+     * nseq.  Causal and window masks align bottom-right within every sequence: with
+     * off_s = end_k(s) - end_q(s), key j is visible to query i of the same sequence iff
+     * (!causal || j <= i + off_s) && (window <= 0 || i + off_s - j < window), so a sequence
+     * with more queries than keys has leading queries that see nothing (MaxText commit message
+     * quoted on tokamax PR #1121: packing lowered to per-segment q / kv seqlens and offsets).
+     * Requires cu_seqlens; Sq == Sk is then not required.  NULL: the keys share cu_seqlens.  */
+    const int32_t *cu_seqlens_k;
 } attn_args;
 
 /* Bytes of workspace attn_fwd needs for these arguments (256-byte multiple, >= 256). */

@@ -59,6 +59,37 @@ def run_gpu(w: Workload, inp: dict, dev="cuda", **extra):
     return {"O": O, "LSE": LSE, "dq": dQ, "dk": dK, "dv": dV, "dbias": dbias, "dsink": dsink}
 
 
+def varlen_oracle(w: Workload, inp: dict, cu_q, cu_k):
+    """thd varlen: every sequence is an attention problem of its own (B = 1, its own query and
+    key lengths, bottom-right causal / window alignment) -- the oracle run per sequence, its
+    outputs placed back at the sequence's tokens.  Tokens past the last boundary form one more
+    sequence; a sequence without keys keeps O = 0 and LSE = its sink (or -inf)."""
+    q, k, v, dO = to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), to64(inp["dO"])
+    sink = None if inp["sink"] is None else inp["sink"].double().numpy()
+    bq, bk = list(cu_q) + [w.Sq], list(cu_k) + [w.Sk]
+    O, dq = np.zeros_like(q), np.zeros_like(q)
+    dk, dv = np.zeros_like(k), np.zeros_like(v)
+    LSE = np.full((1, w.Hq, w.Sq), -np.inf)
+    dsink = None if sink is None else np.zeros(w.Hq)
+    for s in range(len(bq) - 1):
+        q0, q1, k0, k1 = bq[s], bq[s + 1], bk[s], bk[s + 1]
+        if q1 == q0:
+            continue
+        if k1 == k0:
+            if sink is not None:
+                LSE[0, :, q0:q1] = sink[:, None]
+            continue
+        p = oracle.Problem(q[:, q0:q1], k[:, k0:k1], v[:, k0:k1], scale=w.scale, causal=w.causal,
+                           window=w.window, softcap=w.softcap, sink=sink)
+        Os, Ls = oracle.forward(p)
+        g = oracle.backward(p, dO[:, q0:q1], Os, Ls)
+        O[:, q0:q1], LSE[:, :, q0:q1] = Os, Ls
+        dq[:, q0:q1], dk[:, k0:k1], dv[:, k0:k1] = g["dq"], g["dk"], g["dv"]
+        if sink is not None:
+            dsink += g["dsink"]
+    return {"O": O, "LSE": LSE, "dq": dq, "dk": dk, "dv": dv, "dbias": None, "dsink": dsink}
+
+
 def full_oracle(w: Workload, inp: dict):
     p = problem_from_inputs(w, inp)
     O, LSE = oracle.forward(p)

@@ -105,6 +105,20 @@ def test_kv_splits_workspace(capi):
 
 def test_cu_seqlens_with_segments_unsupported_and_shape_rules(capi):
     L = capi.lib()
+    # separate key boundaries: need cu_seqlens; lift the Sq == Sk rule; B stays 1
+    a = valid_args(capi, cu_seqlens_k=0x22000, nseq=2)
+    assert L.attn_fwd(ctypes.byref(a), 0x30000, 0x40000, 0x50000, 1 << 20, None) == 1
+    a = valid_args(capi, cu_seqlens=0x21000, cu_seqlens_k=0x22000, nseq=2)
+    a.Sk = 40
+    assert L.attn_fwd_workspace_size(ctypes.byref(a)) >= 256
+    a.Sk = 16
+    a.Sq = 40
+    assert L.attn_fwd_workspace_size(ctypes.byref(a)) >= 256
+    a = valid_args(capi, B=2, cu_seqlens=0x21000, cu_seqlens_k=0x22000, nseq=2)
+    assert L.attn_fwd_workspace_size(ctypes.byref(a)) == 0
+    a = valid_args(capi, cu_seqlens=0x21000, nseq=2)
+    a.Sk = 40
+    assert L.attn_fwd_workspace_size(ctypes.byref(a)) == 0
     a = valid_args(capi, seg_q=0x20000, seg_k=0x20000, cu_seqlens=0x21000, nseq=2)
     assert L.attn_fwd(ctypes.byref(a), 0x30000, 0x40000, 0x50000, 1 << 20, None) == 2
     a = valid_args(capi, B=2, cu_seqlens=0x21000, nseq=2)

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from parity import TOL, compare_full, frob_rel, full_oracle, problem_from_inputs, run_gpu, to64
+from parity import TOL, compare_full, frob_rel, full_oracle, problem_from_inputs, run_gpu, to64, varlen_oracle
 from workloads import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -177,6 +177,60 @@ def test_split_kv_off_by_one_and_noalloc():
                                  off_by_one=True, kv_splits=4)
     torch.cuda.synchronize()
     assert torch.equal(O1, gpu["O"]) and torch.equal(L1, gpu["LSE"])
+
+
+# thd varlen with separate query and key boundaries (Sq != Sk per sequence, bottom-right
+# causal / window within each): sequences with more keys than queries, more queries than keys
+# (leading queries see nothing), one query, no query, no key, and a trailing sequence past the
+# last boundary; GQA (query heads index kv heads within each sequence's tokens).
+VARLEN = [
+    (Workload("varlen_d128_gqa_sink", "bf16", B=1, Sq=578, Sk=1424, Hq=4, Hkv=2, D=128, causal=True,
+              softcap=30.0, sink=True, q_std=3.0), [0, 50, 180, 181, 481], [0, 200, 330, 394, 684], 0),
+    (Workload("varlen_d256_window", "bf16", B=1, Sq=700, Sk=610, Hq=4, Hkv=1, D=256, causal=True,
+              window=100, softcap=50.0, q_std=3.0), [0, 300, 420, 640], [0, 250, 380, 600], 0),
+    (Workload("varlen_d64_noncausal_empty_seqs", "bf16", B=1, Sq=97, Sk=179, Hq=2, Hkv=1, D=64, causal=False,
+              softcap=20.0, sink=True, q_std=2.0), [0, 0, 64], [0, 50, 50], 0),
+    (Workload("varlen_f32_window", "f32", B=1, Sq=150, Sk=230, Hq=2, Hkv=1, D=32, causal=True, window=40,
+              softcap=5.0, sink=True, q_std=2.0), [0, 70, 120], [0, 60, 200], 0),
+    (Workload("varlen_d128_split", "bf16", B=1, Sq=578, Sk=1424, Hq=4, Hkv=2, D=128, causal=True,
+              softcap=30.0, sink=True, q_std=3.0), [0, 50, 180, 181, 481], [0, 200, 330, 394, 684], 3),
+]
+
+
+@pytest.mark.parametrize("w,cu_q,cu_k,splits", VARLEN, ids=lambda x: x.name if hasattr(x, "name") else None)
+def test_varlen_separate_key_boundaries(w, cu_q, cu_k, splits):
+    inp = make_inputs(w)
+    ref = varlen_oracle(w, inp, cu_q, cu_k)
+    cq = torch.tensor(cu_q, dtype=torch.int32, device="cuda")
+    ck = torch.tensor(cu_k, dtype=torch.int32, device="cuda")
+    gpu = run_gpu(w, inp, cu_seqlens=cq, cu_seqlens_k=ck, kv_splits=splits)
+    check(w, gpu, ref)
+
+
+def test_varlen_sequences_are_isolated_under_gqa():
+    """Perturbing the keys and values of one sequence leaves every other sequence's O, LSE,
+    dK and dV bit-identical (with four query heads per kv head: kv rows are addressed by
+    token, never scaled by the query head count)."""
+    w, cu_q, cu_k, _ = VARLEN[0]
+    w = w.replace(Hq=8, Hkv=2)
+    inp = make_inputs(w)
+    cq = torch.tensor(cu_q, dtype=torch.int32, device="cuda")
+    ck = torch.tensor(cu_k, dtype=torch.int32, device="cuda")
+    a = run_gpu(w, inp, cu_seqlens=cq, cu_seqlens_k=ck)
+    k0, k1 = cu_k[3], cu_k[4]
+    pert = dict(inp)
+    pert["k"], pert["v"] = inp["k"].clone(), inp["v"].clone()
+    pert["k"][:, k0:k1] += 1.0
+    pert["v"][:, k0:k1] -= 1.0
+    b = run_gpu(w, pert, cu_seqlens=cq, cu_seqlens_k=ck)
+    q0, q1 = cu_q[3], cu_q[4]
+    others_q = torch.cat([torch.arange(0, q0), torch.arange(q1, w.Sq)])
+    others_k = torch.cat([torch.arange(0, k0), torch.arange(k1, w.Sk)])
+    assert torch.equal(a["O"][:, others_q], b["O"][:, others_q])
+    assert torch.equal(a["LSE"][:, :, others_q], b["LSE"][:, :, others_q])
+    assert torch.equal(a["dk"][:, others_k], b["dk"][:, others_k])
+    assert torch.equal(a["dv"][:, others_k], b["dv"][:, others_k])
+    assert not torch.equal(a["O"][:, q0:q1], b["O"][:, q0:q1])
 
 
 def test_fully_masked_rows_with_and_without_sink():

@@ -46,6 +46,12 @@ class Workload:
     run_hi: int = 4096
     seed: int = 0
     kv_splits: int = 0       # split-KV forward: key shares per query tile (0: off)
+    # thd varlen with cached prefixes (B = 1): query runs ~ U[run_lo, run_hi] over Sq (last
+    # truncated); sequence s holds a cached prefix ~ U[0, prefix_hi] of keys before its own
+    # query tokens' keys (keys = prefix + queries, bottom-right causal), until Sk is used up;
+    # left-over keys form a trailing sequence without queries.
+    thd_prefix: bool = False
+    prefix_hi: int = 2048
 
     @property
     def scale(self) -> float:
@@ -82,6 +88,10 @@ WORKLOADS = {
         # 32k keys (bottom-right causal), too few query tiles to fill the GPU unsplit.
         Workload("decode_sq128_sk32k_cap30_sink", "bf16", B=1, Sq=128, Sk=32768, Hq=32, Hkv=8, D=128,
                  causal=True, softcap=30.0, q_std=3.0, sink=True, kv_splits=4),
+        # Chunked prefill against a KV cache, packed thd: per sequence a query chunk and its
+        # keys (cached prefix + the chunk), Sq != Sk per sequence, bottom-right causal.
+        Workload("thd_prefix_cap30", "bf16", B=1, Sq=8192, Sk=20480, Hq=8, Hkv=8, D=128,
+                 causal=True, softcap=30.0, q_std=3.0, thd_prefix=True, run_lo=64, run_hi=2048),
     ]
 }
 
@@ -109,9 +119,25 @@ def segment_runs(gen: torch.Generator, B: int, S: int, lo: int, hi: int, tile: i
             return torch.stack(rows).to(torch.int32)
 
 
+def thd_prefix_bounds(gen: torch.Generator, Sq: int, Sk: int, lo: int, hi: int, prefix_hi: int):
+    """Query and key boundaries (cu_q, cu_k, int32 [nseq + 1]) of a packed chunked-prefill
+    batch: query runs ~ U[lo, hi] (last truncated to Sq), each sequence's keys a prefix
+    ~ U[0, prefix_hi] plus its queries; sequences stop where the keys would pass Sk."""
+    cu_q, cu_k = [0], [0]
+    while cu_q[-1] < Sq:
+        L = min(int(torch.randint(lo, hi + 1, (1,), generator=gen).item()), Sq - cu_q[-1])
+        P = int(torch.randint(0, prefix_hi + 1, (1,), generator=gen).item())
+        if cu_k[-1] + P + L > Sk:
+            break
+        cu_q.append(cu_q[-1] + L)
+        cu_k.append(cu_k[-1] + P + L)
+    return torch.tensor(cu_q, dtype=torch.int32), torch.tensor(cu_k, dtype=torch.int32)
+
+
 def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
     """CPU tensors for one workload: q, k, v, dO in the workload dtype; bias (workload dtype,
-    [1,Hq,Sq,Sk]) or None; sink fp32 [Hq] or None; seg int32 [B,S] or None."""
+    [1,Hq,Sq,Sk]) or None; sink fp32 [Hq] or None; seg int32 [B,S] or None; cu_q / cu_k
+    int32 boundaries or None (thd_prefix workloads)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed if seed is None else seed)
     dt = w.torch_dtype
@@ -129,4 +155,8 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
     if w.segments:
         assert w.Sq == w.Sk
         seg = segment_runs(g, w.B, w.Sq, w.run_lo, w.run_hi)
-    return {"q": q, "k": k, "v": v, "dO": dO, "bias": bias, "sink": sink, "seg": seg}
+    cu_q = cu_k = None
+    if w.thd_prefix:
+        assert w.B == 1
+        cu_q, cu_k = thd_prefix_bounds(g, w.Sq, w.Sk, w.run_lo, w.run_hi, w.prefix_hi)
+    return {"q": q, "k": k, "v": v, "dO": dO, "bias": bias, "sink": sink, "seg": seg, "cu_q": cu_q, "cu_k": cu_k}
