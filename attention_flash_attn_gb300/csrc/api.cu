@@ -85,7 +85,7 @@ int validate(const attn_args *a) {
   if (a->B < 0 || a->Sq < 0 || a->Sk < 0 || a->Hq < 1 || a->Hkv < 1 || a->D < 1) return ATTN_ERR_INVALID;
   if (a->Hq % a->Hkv != 0) return ATTN_ERR_INVALID;
   if (a->D % 8 != 0) return ATTN_ERR_INVALID;
-  if (a->D > 256) return ATTN_ERR_UNSUPPORTED;
+  if (a->D > 512) return ATTN_ERR_UNSUPPORTED;
   if (!isfinite(a->scale)) return ATTN_ERR_INVALID;
   if (!isfinite(a->softcap) || a->softcap < 0.f) return ATTN_ERR_INVALID;
   if (a->B > 0 && a->Sq > 0 && !a->q) return ATTN_ERR_INVALID;

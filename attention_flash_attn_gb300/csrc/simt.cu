@@ -14,7 +14,9 @@ namespace {
 
 constexpr int kWarps = 8;     // rows per block
 constexpr int kTile = 32;     // keys (or queries) per shared-memory tile
-constexpr int kMaxPerLane = 8;  // D <= 256 -> at most 8 dims per lane
+constexpr int kMaxPerLane = 16;  // D <= 512 -> at most 16 dims per lane (head dims above 256
+                                 // exist only here: the dot products loop over D in shared
+                                 // memory, the lane-owned accumulators cover D in 32-wide slices)
 
 // Dims owned by this lane: lane, lane + 32, ... below D (unrolled so the arrays stay in
 // registers).
@@ -316,9 +318,9 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_dkdv_kernel(Params p) {
 template <typename T>
 cudaError_t launch_all_fwd(const Params &p, cudaStream_t st) {
   const int D = p.D;
-  size_t sm = sizeof(float) * (kTile * (D + 1) + kTile * D + kWarps * D);
+  size_t sm = sizeof(float) * (kTile * (D + 1) + kTile * D + kWarps * D);  // 148 KiB at D = 512
   // Set on every call: cheap, idempotent, and per device.
-  cudaError_t e = cudaFuncSetAttribute(simt_fwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+  cudaError_t e = cudaFuncSetAttribute(simt_fwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   dim3 grid((p.Sq + kWarps - 1) / kWarps, p.Hq, p.B);
   simt_fwd_kernel<T><<<grid, kWarps * 32, sm, st>>>(p);
@@ -328,17 +330,17 @@ cudaError_t launch_all_fwd(const Params &p, cudaStream_t st) {
 template <typename T>
 cudaError_t launch_all_bwd(const Params &p, cudaStream_t st) {
   const int D = p.D;
-  cudaError_t e = cudaFuncSetAttribute(simt_bwd_dq_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+  const size_t sm_dq = sizeof(float) * (2 * kTile * (D + 1) + 2 * kWarps * D);              // 160 KiB at D = 512
+  const size_t sm_kv = sizeof(float) * (2 * kTile * (D + 1) + 2 * kWarps * D + 2 * kTile);  // 161 KiB
+  cudaError_t e = cudaFuncSetAttribute(simt_bwd_dq_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_dq);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(simt_bwd_dkdv_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+  e = cudaFuncSetAttribute(simt_bwd_dkdv_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_kv);
   if (e != cudaSuccess) return e;
-  size_t sm_dq = sizeof(float) * (2 * kTile * (D + 1) + 2 * kWarps * D);
   dim3 g1((p.Sq + kWarps - 1) / kWarps, p.Hq, p.B);
   simt_bwd_dq_kernel<T><<<g1, kWarps * 32, sm_dq, st>>>(p);
   e = counted(cudaGetLastError());
   if (e != cudaSuccess) return e;
   if (p.Sk == 0) return cudaSuccess;  // no keys: no dK / dV
-  size_t sm_kv = sizeof(float) * (2 * kTile * (D + 1) + 2 * kWarps * D + 2 * kTile);
   dim3 g2((p.Sk + kWarps - 1) / kWarps, p.Hkv, p.B);
   simt_bwd_dkdv_kernel<T><<<g2, kWarps * 32, sm_kv, st>>>(p);
   return counted(cudaGetLastError());

@@ -78,7 +78,7 @@ enum attn_status {
     ATTN_OK = 0,
     ATTN_ERR_INVALID = 1,      /* null required pointer, bad shape/stride/alignment,
                                   negative or NaN softcap, non-finite scale, ...          */
-    ATTN_ERR_UNSUPPORTED = 2,  /* valid but not built: D > 256; cu_seqlens together with
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid but not built: D > 512; cu_seqlens together with
                                   seg_q / seg_k                                          */
     ATTN_ERR_WORKSPACE = 3,    /* ws NULL or smaller than the size query returned        */
     ATTN_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed            */
@@ -89,7 +89,11 @@ enum attn_status {
 typedef struct {
     int dtype;                 /* enum attn_dtype                                          */
     int B, Sq, Sk, Hq, Hkv, D; /* B, Sq, Sk >= 0 (B == 0 or Sq == 0: nothing to compute);
-                                  Hq, Hkv >= 1 with Hq % Hkv == 0; D % 8 == 0, D <= 256   */
+                                  Hq, Hkv >= 1 with Hq % Hkv == 0; D % 8 == 0, D <= 512.
+                                  Tensor-core kernels: bf16 with D in {64, 128, 256}; other
+                                  head dims (up to 512: MaxText's chunked head-dim
+                                  accumulation above 256, tokamax PR #1121) run on the fp32
+                                  FFMA kernels                                             */
     const void *q;             /* [B,Sq,Hq,D] with the strides below (elements)           */
     int64_t q_stride_b, q_stride_s, q_stride_h;
     const void *k;             /* [B,Sk,Hkv,D]                                             */

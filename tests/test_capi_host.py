@@ -52,7 +52,7 @@ def valid_args(capi, dtype=1, B=1, S=16, H=2, D=64, **kw):
 
 
 @pytest.mark.parametrize("field,value,status", [
-    ("dtype", 3, 1), ("Hq", 3, 1), ("Hkv", 0, 1), ("D", 60, 1), ("D", 264, 2),
+    ("dtype", 3, 1), ("Hq", 3, 1), ("Hkv", 0, 1), ("D", 60, 1), ("D", 520, 2),
     ("softcap", -1.0, 1), ("softcap", float("nan"), 1), ("softcap", float("inf"), 1),
     ("scale", float("inf"), 1), ("q", None, 1), ("q", 0x10008, 1), ("q_stride_s", 12, 1),
     ("Sq", -1, 1), ("seg_q", 0x20000, 1), ("softmax_type", 2, 1), ("softmax_type", -1, 1),

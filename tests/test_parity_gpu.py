@@ -85,6 +85,11 @@ EDGE = [
     # preprocess takes its one-row-per-warp form; a sink and a ragged tail past 128 rows
     Workload("edge_bf16_d40_sink", "bf16", B=1, Sq=150, Sk=150, Hq=3, Hkv=1, D=40, causal=True,
              softcap=20.0, sink=True, q_std=2.0),
+    # head dims above 256 (FFMA kernels, D accumulated in 32-wide lane slices): bf16 and fp32
+    Workload("edge_d320_bf16_gqa_sink_window", "bf16", B=1, Sq=200, Sk=200, Hq=4, Hkv=2, D=320, causal=True,
+             window=90, softcap=30.0, sink=True, q_std=2.0),
+    Workload("edge_d512_f32_cap", "f32", B=1, Sq=130, Sk=170, Hq=2, Hkv=1, D=512, causal=True,
+             softcap=20.0, sink=True, q_std=2.0),
     # fp32 with sink, GQA, window and segments all at once
     Workload("edge_f32_everything", "f32", B=2, Sq=190, Sk=190, Hq=4, Hkv=2, D=32, causal=True, window=70,
              softcap=5.0, sink=True, segments=True, run_lo=20, run_hi=90, q_std=2.0, bias=True),

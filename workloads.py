@@ -88,6 +88,9 @@ WORKLOADS = {
         # 32k keys (bottom-right causal), too few query tiles to fill the GPU unsplit.
         Workload("decode_sq128_sk32k_cap30_sink", "bf16", B=1, Sq=128, Sk=32768, Hq=32, Hkv=8, D=128,
                  causal=True, softcap=30.0, q_std=3.0, sink=True, kv_splits=4),
+        # Head dim above 256 (the FFMA kernels; the pages' chunked head-dim accumulation).
+        Workload("hd512_cap30", "bf16", B=1, Sq=2048, Sk=2048, Hq=8, Hkv=4, D=512, causal=True,
+                 softcap=30.0, q_std=2.0),
         # Chunked prefill against a KV cache, packed thd: per sequence a query chunk and its
         # keys (cached prefix + the chunk), Sq != Sk per sequence, bottom-right causal.
         Workload("thd_prefix_cap30", "bf16", B=1, Sq=8192, Sk=20480, Hq=8, Hkv=8, D=128,
