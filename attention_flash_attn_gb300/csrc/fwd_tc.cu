@@ -47,7 +47,14 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + NK * KV_BYTES;   // NV-deep V ring (released after PV)
   static constexpr int OFF_X = OFF_V + NV * KV_BYTES;   // partner exchange: [2 halves][3 slots][128] floats
   static constexpr int OFF_BAR = OFF_X + 6 * kBM * 4;
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 5;
+  // One K and one V tile (head dim 256): each is moved and released in two halves with
+  // barriers of their own -- K by head-dim halves (chunks 0-1, 2-3), V by key halves (rows
+  // 0-63, 64-127, the halves the PV MMAs read in turn) -- so that a step's MMAs start on the
+  // first half while the second lands, and the next tile's first half loads while the second
+  // is still read.
+  static constexpr bool HALF = NK == 1 && NV == 1;
+  static constexpr int RK = HALF ? 2 : NK, RV = HALF ? 2 : NV;  // barrier pairs per ring
+  static constexpr int NBAR = 1 + 2 * RK + 2 * RV + 5;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   static constexpr int TM_O = 2 * BN;
@@ -184,24 +191,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t q_full = bar0;
+  constexpr int RK = C::RK, RV = C::RV;
   auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto k_empty = [&](int s) { return bar0 + 8u * (1 + NK + s); };
-  auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * NK + s); };
-  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * NK + NV + s); };
-  auto s_full = [&](int x) { return bar0 + 8u * (1 + 2 * NK + 2 * NV + x); };
-  auto p_full = [&](int x) { return bar0 + 8u * (3 + 2 * NK + 2 * NV + x); };
-  const uint32_t o_done = bar0 + 8u * (5 + 2 * NK + 2 * NV);
+  auto k_empty = [&](int s) { return bar0 + 8u * (1 + RK + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * RK + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * RK + RV + s); };
+  auto s_full = [&](int x) { return bar0 + 8u * (1 + 2 * RK + 2 * RV + x); };
+  auto p_full = [&](int x) { return bar0 + 8u * (3 + 2 * RK + 2 * RV + x); };
+  const uint32_t o_done = bar0 + 8u * (5 + 2 * RK + 2 * RV);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *red = misc_i + 4;  // [8]
   float *xbuf = reinterpret_cast<float *>(smem + C::OFF_X);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < NK; ++s) {
+    for (int s = 0; s < RK; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
     }
-    for (int s = 0; s < NV; ++s) {
+    for (int s = 0; s < RV; ++s) {
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
     }
@@ -234,24 +242,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < C::KCH; ++c)
         tma_load_4d(sbase + C::OFF_Q + c * (kBM * 128), &tmQ, q_full, c * 64, i0, h, b);
       for (int j = 0; j < n; ++j) {
-        const int s = j % NK;
-        if (j >= NK && !mbar_wait(k_empty(s), ((j / NK) - 1) & 1, p.status)) break;
-        mbar_arrive_expect_tx(k_full(s), C::KV_BYTES);
         const int kt = (t0 + j) * BN;
+        if constexpr (C::HALF) {
+          bool okh = true;
+          for (int hf = 0; hf < 2 && okh; ++hf) {  // head-dim chunks 2 hf, 2 hf + 1
+            if (j >= 1 && !mbar_wait(k_empty(hf), (j - 1) & 1, p.status)) { okh = false; break; }
+            mbar_arrive_expect_tx(k_full(hf), C::KV_BYTES / 2);
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES + c * (BN * 128), &tmK, k_full(s), c * 64, kt, g, b);
+            for (int c = 2 * hf; c < 2 * hf + 2; ++c)
+              tma_load_4d(sbase + C::OFF_K + c * (BN * 128), &tmK, k_full(hf), c * 64, kt, g, b);
+          }
+          if (!okh) break;
+        } else {
+          const int s = j % NK;
+          if (j >= NK && !mbar_wait(k_empty(s), ((j / NK) - 1) & 1, p.status)) break;
+          mbar_arrive_expect_tx(k_full(s), C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES + c * (BN * 128), &tmK, k_full(s), c * 64, kt, g, b);
+        }
       }
     } else if (lane == 1 && n > 0) {
       tma_prefetch_desc(&tmV);
       for (int j = 0; j < n; ++j) {
-        const int s = j % NV;
-        if (j >= NV && !mbar_wait(v_empty(s), ((j / NV) - 1) & 1, p.status)) break;
-        mbar_arrive_expect_tx(v_full(s), C::KV_BYTES);
         const int kt = (t0 + j) * BN;
+        if constexpr (C::HALF) {
+          bool okh = true;
+          for (int hf = 0; hf < 2 && okh; ++hf) {  // key rows 64 hf .. 64 hf + 63 (64-row boxes)
+            if (j >= 1 && !mbar_wait(v_empty(hf), (j - 1) & 1, p.status)) { okh = false; break; }
+            mbar_arrive_expect_tx(v_full(hf), C::KV_BYTES / 2);
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_4d(sbase + C::OFF_V + s * C::KV_BYTES + c * (BN * 128), &tmV, v_full(s), c * 64, kt, g, b);
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_4d(sbase + C::OFF_V + c * (BN * 128) + hf * (64 * 128), &tmV, v_full(hf), c * 64, kt + 64 * hf,
+                          g, b);
+          }
+          if (!okh) break;
+        } else {
+          const int s = j % NV;
+          if (j >= NV && !mbar_wait(v_empty(s), ((j / NV) - 1) & 1, p.status)) break;
+          mbar_arrive_expect_tx(v_full(s), C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(sbase + C::OFF_V + s * C::KV_BYTES + c * (BN * 128), &tmV, v_full(s), c * 64, kt, g, b);
+        }
       }
     }
   } else if (warp == 1) {
@@ -266,7 +299,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv0 = sw128_desc(sbase + C::OFF_V, BN * 128, 1024);
       bool ok = mbar_wait_warp(q_full, 0, p.status);
       for (int j = 0; ok && j <= n; ++j) {
-        if (j < n) {
+        if (j < n && C::HALF) {
+          const uint32_t dS = tmem + (uint32_t)((j & 1) * BN);
+          uint64_t qd = dq0, kd = dk0;
+          bool okh = true;
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!mbar_wait_warp(k_full(hf), j & 1, p.status)) { okh = false; break; }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4) mma_ss_w(dS, desc_at(qd, k4 * 32), desc_at(kd, k4 * 32), idS, (c | k4) != 0);
+              qd = desc_at(qd, kBM * 128);
+              kd = desc_at(kd, BN * 128);
+            }
+            mma_commit_w(k_empty(hf));
+          }
+          if (!okh) break;
+          mma_commit_w(s_full(j & 1));
+        } else if (j < n) {
           const int s = j % NK;
           if (!mbar_wait_warp(k_full(s), (j / NK) & 1, p.status)) break;
           tc_fence_after();
@@ -283,7 +334,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit_w(s_full(j & 1));
           mma_commit_w(k_empty(s));
         }
-        if (j >= 1) {
+        if (j >= 1 && C::HALF) {
+          const int jj = j - 1;
+          if (!mbar_wait_warp(p_full(jj & 1), (jj >> 1) & 1, p.status)) break;
+          const uint32_t pa = tmem + (uint32_t)((jj & 1) * BN);
+          bool okh = true;
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!mbar_wait_warp(v_full(hf), jj & 1, p.status)) { okh = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 4 * hf; kk < 4 * hf + 4; ++kk)
+              mma_ts_w(tmem + C::TM_O, pa + kk * 8, desc_at(dv0, kk * (16 * 128)), idO, (jj > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_w(v_empty(hf));
+          }
+          if (!okh) break;
+          mma_commit_w(o_done);
+        } else if (j >= 1) {
           const int jj = j - 1, s = jj % NV;
           if (!mbar_wait_warp(v_full(s), (jj / NV) & 1, p.status)) break;
           if (!mbar_wait_warp(p_full(jj & 1), (jj >> 1) & 1, p.status)) break;
@@ -513,7 +579,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bshd(&tq, p.q, D, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, kBM) ||
       !make_tmap_bshd(&tk, p.k, D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, BN) ||
-      !make_tmap_bshd(&tv, p.v, D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, BN))
+      !make_tmap_bshd(&tv, p.v, D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, C::HALF ? 64 : BN))
     return cudaErrorInvalidValue;
   auto kern = p.cap > 0.f ? fwd_tc_kernel<D, BN, NK, NV, true> : fwd_tc_kernel<D, BN, NK, NV, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
