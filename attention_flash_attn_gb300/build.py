@@ -52,14 +52,40 @@ def _stamp() -> str:
 BWD_MAIN_SOURCES = ("bwd_tc.cu", "tc_common.cuh", "tc_host.cu", "common.cuh", "internal.h")
 
 
+def _code_only(text: str) -> str:
+    """C / C++ source with comments and whitespace removed (string literals kept), so that an
+    edit to comments alone leaves a kernel's stamp unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"' or c == "'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            if not c.isspace():
+                out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_stamp(names=BWD_MAIN_SOURCES) -> str:
-    """Hash of the named csrc files, the public header and the compile flags."""
+    """Hash of the code (comments and whitespace removed) of the named csrc files and the
+    public header, and of the compile flags."""
     h = hashlib.sha256()
     files = [os.path.join(CSRC, n) for n in names] + [os.path.join(ROOT, "include", "attn_gb300.h")]
     for f in files:
         h.update(os.path.relpath(f, ROOT).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     h.update(" ".join(ARCH + FLAGS).encode())
     return h.hexdigest()
 

@@ -20,10 +20,10 @@
 // query steps -- dV first, then dK and dQ (S^T recomputed).  V is not needed in the dV pass, so
 // its shared-memory slot doubles as a second Q/dO stage there.  For the dK pass V moves into
 // tensor memory (the A operand of dP^T = V dO^T), S^T and dP^T share one score buffer and dQ^T
-// is produced one 128-row half at a time; both dV-pass stages then form a ring of four
-// whole-tile slots (Q_i, dO_i, ...) read by one MMA warp alone, in which Q_i stays from its
-// S^T to its dK.  S^T of the next step is computed while the softmax warps still work on this
-// one, and those warps form P from S^T before dP^T is in.
+// is produced one 128-row half at a time.  The dV-pass stages become two Q tile slots (Q_i
+// resident from its S^T to its dK) and one dO slot, read by one MMA warp alone, and the rest
+// of the second stage holds a second dS^T buffer and more dQ staging.  dK of a step is issued
+// right after S^T of the next, and the softmax warps form P f from S^T before dP^T is in.
 //
 // Warps: 0..7 softmax / dS, 8 TMA producer, 9 MMA issuer + TMEM owner, 10 second MMA issuer
 // (the MMAs that consume P and dS while warp 9 issues S^T / dP^T), 12..15 dQ drain.
