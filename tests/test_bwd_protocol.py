@@ -11,6 +11,10 @@ waiter may ever see a count outside {k, k + 1}.
 
 The negative control replays the earlier layout, in which the half-tile ring was read by
 two warps; the model must flag it (that layout timed out intermittently on the GPU).
+
+simulate_split_rings is the kernel's current protocol (two Q slots and one dO slot in the dK
+pass, double-buffered dS^T).  simulate and simulate_vtmem are the two layouts before it, kept
+as models of the same rules on different ring shapes.
 """
 import random
 from collections import defaultdict
