@@ -13,6 +13,7 @@ same workload instead (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -78,8 +79,10 @@ def flops(w: Workload, seg, which: str, bounds=None) -> float:
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region: one
+    timestamped sample every 20 ms; only samples inside the region's wall-clock window count
+    (the nearest ones if the region is shorter than the interval)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -87,14 +90,23 @@ class ClockSampler:
         self.idx = gpu_index
         self.proc = None
         self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.window = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=self.out, stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
+            return
+        t_end = time.time() + 5.0  # the first sample marks a running sampler
+        while time.time() < t_end and os.path.getsize(self.out.name) == 0 and self.proc.poll() is None:
+            time.sleep(0.01)
+
+    def mark(self, t0: float, t1: float):
+        """Wall-clock bounds of the timed region."""
+        self.window = (t0, t1)
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -105,23 +117,26 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.flush()
-        rows = [r.split(",") for r in open(self.out.name).read().strip().splitlines() if r.strip()]
+        lines = [r.split(",") for r in open(self.out.name).read().strip().splitlines() if r.strip()]
         os.unlink(self.out.name)
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        rows = []
+        for r in lines:
             r = [x.strip() for x in r]
-            if len(r) < 9:
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                smax = float(r[2])
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(r[2]), float(r[3]), r[6:10]))
             except ValueError:
                 continue
-            for n, val in zip(names, r[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+        if self.window and rows:
+            t0, t1 = self.window
+            inside = [x for x in rows if t0 - 0.01 <= x[0] <= t1 + 0.01]
+            rows = inside or sorted(rows, key=lambda x: min(abs(x[0] - t0), abs(x[0] - t1)))[:2]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {n for _, _, _, v in rows for n, val in zip(names, v) if val.lower().startswith("active")}
+        sm = [x[1] for x in rows]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": rows[-1][2] if rows else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -189,6 +204,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
+    t_wall0 = time.time()
     for s in range(args.steps):
         flush.zero_()
         ev[s][0].record(stream)
@@ -201,6 +217,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     launches = fa.attn_launch_counter() - launches0
+    clocks.mark(t_wall0, time.time())
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     fwd_ms = [a.elapsed_time(b) for a, b, _, _ in kev]

@@ -25,6 +25,26 @@ def test_visible_pairs_matches_oracle_brute_force(w):
     assert visible_pairs(w, None if seg is None else seg.numpy()) == oracle.count_visible(p)
 
 
+def test_thd_visible_pairs_match_per_sequence_oracle_counts():
+    """thd varlen: the count over (cu_q, cu_k) bounds equals the oracle's brute-force count run
+    on each sequence as its own problem (bottom-right causal / window inside it), including the
+    trailing sequence past the last bounds."""
+    w = WORKLOADS["thd_prefix_cap30"].replace(Sq=300, Sk=700, Hq=2, Hkv=1, run_lo=20, run_hi=90,
+                                              prefix_hi=200, window=37)
+    inp = make_inputs(w)
+    cq = [int(x) for x in inp["cu_q"]] + [w.Sq]
+    ck = [int(x) for x in inp["cu_k"]] + [w.Sk]
+    z = np.zeros
+    ref = 0
+    for s in range(len(cq) - 1):
+        lq, lk = cq[s + 1] - cq[s], ck[s + 1] - ck[s]
+        if lq and lk:
+            p = oracle.Problem(z((1, lq, w.Hq, 1)), z((1, lk, w.Hkv, 1)), z((1, lk, w.Hkv, 1)), scale=1.0,
+                               causal=w.causal, window=w.window)
+            ref += oracle.count_visible(p)
+    assert visible_pairs(w, None, (inp["cu_q"], inp["cu_k"])) == ref > 0
+
+
 def test_headline_flop_counts():
     w = WORKLOADS["gemma2_local_w4096_cap50"]
     # causal with a 4096 window over 8192 tokens: 4096*4097/2 + 4096*4096 pairs per (b, h)
@@ -33,3 +53,35 @@ def test_headline_flop_counts():
     assert flops(w, None, "fwdbwd") == per * w.B * w.Hq * 14 * 256
     w5 = WORKLOADS["long_causal_32k_cap50"]
     assert visible_pairs(w5, None) == 32768 * 32769 // 2 * 32
+
+
+def test_clock_samples_are_taken_inside_the_timed_region(tmp_path):
+    """Only nvidia-smi samples whose timestamps fall in the timed region's wall-clock window
+    count (the idle ones before and after are dropped); throttle reasons come from those."""
+    import datetime
+    import time
+
+    import bench
+
+    c = bench.ClockSampler(0)
+    now = time.time()
+    ts = lambda t: datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]  # noqa: E731
+    idle = "0x0, Not Active, Not Active, Not Active, Not Active"
+    rows = [f"{ts(now - 1.0)}, 0, 1200, 2070, 300.0, {idle}",
+            f"{ts(now + 0.01)}, 0, 2070, 2070, 1300.0, 0x0, Not Active, Not Active, Not Active, Active",
+            f"{ts(now + 0.03)}, 0, 2040, 2070, 1350.0, 0x0, Not Active, Not Active, Not Active, Active",
+            f"{ts(now + 2.0)}, 0, 1000, 2070, 200.0, {idle}"]
+    c.out.write("\n".join(rows) + "\n")
+    c.out.flush()
+
+    class Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            pass
+
+    c.proc = Done()
+    c.mark(now, now + 0.05)
+    clk = c.stop()
+    assert clk == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 2}
