@@ -156,6 +156,22 @@ def captured_traffic(workload):
     return None
 
 
+def max_over_ranks(ms: float, world: int, dev) -> float:
+    """The slowest rank's time: every rank's number is the maximum over the job (NCCL with a
+    CUDA device, gloo with the CPU)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, ms: float) -> float:
+    """Units all ranks processed (each rank runs the whole workload: replicas, weak scaling)
+    over the slowest rank's time."""
+    return flops_per_step * steps * world / (ms * 1e-3) / 1e12
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -222,11 +238,7 @@ def run_ours(args, rank, world, local_rank):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     fwd_ms = [a.elapsed_time(b) for a, b, _, _ in kev]
     bwd_ms = [c.elapsed_time(d) for _, _, c, d in kev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     status = fa.attn_check_device_status(dev)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
@@ -294,15 +306,11 @@ def run_ours(args, rank, world, local_rank):
         return t_start.elapsed_time(t_end)
 
     e2e_run(2)  # warm-up: streams, input sets, allocator
-    e2e_ms = e2e_run(args.steps)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_run(args.steps), world, dev)
 
     f_step = flops(w, seg, "fwdbwd", bounds)
-    value = f_step * args.steps * world / (total_ms * 1e-3) / 1e12
-    e2e_value = f_step * args.steps * world / (e2e_ms * 1e-3) / 1e12
+    value = whole_job_tflops(f_step, args.steps, world, total_ms)
+    e2e_value = whole_job_tflops(f_step, args.steps, world, e2e_ms)
     burst, sustained, kind = peaks()
     # Dominant kernel: the backward main kernel (10*D flops per visible pair).
     bwd_kernel_ms = statistics.mean(bwd_ms)

@@ -1,0 +1,53 @@
+"""The replica path of bench.py (N > 1, one process per GPU under torchrun), on the CPU with
+the gloo backend: every rank ends with the slowest rank's time, the whole-job throughput counts
+the units of all ranks, and the reference arm runs on rank 0 only."""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import bench
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = bench.max_over_ranks(10.0 + 5.0 * rank, world, torch.device("cpu"))
+        torch.distributed.barrier()
+        out[rank] = (ms, bench.whole_job_tflops(1e12, 4, world, ms))
+    finally:
+        torch.distributed.destroy_process_group()
+
+
+def test_max_over_ranks_and_whole_job_throughput_gloo():
+    world = 2
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank, args=(world, _free_port(), out), nprocs=world, join=True)
+        res = dict(out)
+    assert res[0] == res[1]
+    ms, tf = res[0]
+    assert ms == 15.0
+    assert tf == pytest.approx(1e12 * 4 * world / 15e-3 / 1e12)
+
+
+def test_reference_arm_prints_only_on_rank_zero():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], capture_output=True, text=True, env=env,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
