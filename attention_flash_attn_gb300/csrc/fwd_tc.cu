@@ -54,7 +54,7 @@ struct FwdCfg {
   // is still read.
   static constexpr bool HALF = NK == 1 && NV == 1;
   static constexpr int RK = HALF ? 2 : NK, RV = HALF ? 2 : NV;  // barrier pairs per ring
-  static constexpr int NBAR = 1 + 2 * RK + 2 * RV + 5;
+  static constexpr int NBAR = 1 + 2 * RK + 2 * RV + 6;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;
   static constexpr int TM_O = 2 * BN;
@@ -141,7 +141,13 @@ __device__ __forceinline__ float logits2(uint32_t (&x)[N], const FwdScore &k, in
   return fmaxf(m0, m1);
 }
 
-template <int D, int BN, int NK, int NV, bool CAP>
+// FIXM (soft-cap on, cap <= kFixedMaxCap): every logit is at most cap, so the row's exponent
+// offset is fixed up front at max(cap, sink) instead of tracked -- no running maximum, no
+// partner exchange of maxima, no rescaling of O.  Softmax is invariant to the offset, and the
+// smallest visible probability, 2^(-2 cap log2(e)), stays a normal float for cap < 43.6.
+constexpr float kFixedMaxCap = 41.5f;
+
+template <int D, int BN, int NK, int NV, bool CAP, bool FIXM>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -199,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto s_full = [&](int x) { return bar0 + 8u * (1 + 2 * RK + 2 * RV + x); };
   auto p_full = [&](int x) { return bar0 + 8u * (3 + 2 * RK + 2 * RV + x); };
   const uint32_t o_done = bar0 + 8u * (5 + 2 * RK + 2 * RV);
+  const uint32_t o_fin = bar0 + 8u * (6 + 2 * RK + 2 * RV);  // FIXM: every PV MMA has completed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *red = misc_i + 4;  // [8]
   float *xbuf = reinterpret_cast<float *>(smem + C::OFF_X);
@@ -218,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(p_full(x), kSoftmaxThreads);
     }
     mbar_init(o_done, 1);
+    mbar_init(o_fin, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -363,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit_w(o_done);
         }
       }
+      if (FIXM) mma_commit_w(o_fin);  // the softmax warps skip the per-step o_done phases
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
@@ -411,6 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool sink_col = has_sink_col(p) && ns == 1;  // split partials leave it to the merge
     float m_ref = sink_col ? sink_logit(p, h) * kLog2e : -INFINITY;  // running max (log2 units)
     float l = (sink_col && half == 0) ? 1.f : 0.f;                   // this half's sum relative to m_ref
+    if (FIXM) {  // fixed offset: the cap bounds every logit
+      const float m_fix = fmaxf(p.cap * kLog2e, m_ref);
+      l = (sink_col && half == 0) ? ex2_approx(m_ref - m_fix) : 0.f;
+      m_ref = m_fix;
+    }
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
@@ -433,6 +447,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx = full ? logits2<CAP, false>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid)
                   : logits2<CAP, true>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid);
       }
+      float alpha_o = 1.f;
+      bool resc = false;
+      if (FIXM) {
+        (void)mx;
+        if (!(got && ok)) {  // the MMA warp then times out too; the CTA winds down
+          ok = false;
+          break;
+        }
+      } else {
       // Exchange half-row maxima (and failure flags, as NaN) with the partner warp; slot
       // j & 1 is rewritten two tiles later, after the partner has passed the next barrier.
       xbuf[(half * 3 + (j & 1)) * kBM + r] = (got && ok) ? mx : __int_as_float(0x7fffffff);
@@ -443,8 +466,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const float m_new = fmaxf(m_ref, fmaxf(mx, other));
-      float alpha_o = 1.f;
-      bool resc = false;
       if (m_new != -INFINITY) {
         if (j == 0 || m_ref == -INFINITY) {
           // first finite max: O is either about to be overwritten (j == 0) or all-zero
@@ -456,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = m_new;
           resc = true;
         }
+      }
       }
       const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
       const uint64_t mr2 = f2_splat(mr);
@@ -481,8 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < HC / 64; ++c) tmem_st32(pa + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + c * 32));
       if constexpr (HC / 2 == 16) tmem_st16(pa, pk);
 
-      if (j >= 1) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, p.status));
-      if (j >= 1 && __any_sync(0xffffffffu, resc)) {
+      if (!FIXM && j >= 1) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, p.status));
+      if (!FIXM && j >= 1 && __any_sync(0xffffffffu, resc)) {
         tc_fence_after();
 #pragma unroll 1
         for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
@@ -502,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (ok && n > 0) {
-      ok = mbar_wait(o_done, (n - 1) & 1, p.status);
+      ok = FIXM ? mbar_wait(o_fin, 0, p.status) : mbar_wait(o_done, (n - 1) & 1, p.status);
       tc_fence_after();
     }
     // Combine the two halves' sums (the running maxima already agree); slot 2 is used
@@ -581,7 +603,9 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
       !make_tmap_bshd(&tk, p.k, D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, BN) ||
       !make_tmap_bshd(&tv, p.v, D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, C::HALF ? 64 : BN))
     return cudaErrorInvalidValue;
-  auto kern = p.cap > 0.f ? fwd_tc_kernel<D, BN, NK, NV, true> : fwd_tc_kernel<D, BN, NK, NV, false>;
+  auto kern = p.cap <= 0.f                 ? fwd_tc_kernel<D, BN, NK, NV, false, false>
+              : p.cap <= kFixedMaxCap ? fwd_tc_kernel<D, BN, NK, NV, true, true>
+                                      : fwd_tc_kernel<D, BN, NK, NV, true, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const long long nblk = (long long)((p.Sq + kBM - 1) / kBM) * p.Hq * p.B * (p.kv_splits > 1 ? p.kv_splits : 1);
