@@ -130,17 +130,16 @@ __device__ __forceinline__ uint4 pack8(const uint32_t *o, int v) {
 
 // Score constants of the element-wise backward, as packed pairs.  With the soft-cap,
 // e = exp(2 u / cap) for u = scale s, r = 1 / (1 + e), so tanh(u / cap) = 1 - 2 r and
-// 1 - tanh^2 = 4 r (1 - r); the capped logit in log2 units is cap log2(e) (1 - 2 r).  An
-// overflowing e gives r = 0 (tanh = 1) and an underflowing one r = 1 (tanh = -1); the FMA-pipe
-// form (f2_sigmoid2_neg) clamps the exponent at 126 instead, which gives r ~ 0 as well.
+// 1 - tanh^2 = 4 r (1 - r) = 4 e r^2; the capped logit in log2 units is cap log2(e) (1 - 2 r).
+// The exponent is clamped at 126 (a huge e gives r ~ 0, tanh = 1, and e r^2 = 0 rather than
+// inf * 0); an underflowing e gives r = 1 (tanh = -1).
 struct BwdScore {
-  uint64_t cin, one, mcap2, cap2, mfs, fs, sc2, scale;
+  uint64_t cin, one, mcap2, cap2, fs, sc2, scale;
   __device__ BwdScore(float scale_, float inv_cap, float cap) {
     cin = f2_splat(2.f * kLog2e * scale_ * inv_cap);
     one = f2_splat(1.f);
     mcap2 = f2_splat(-2.f * cap * kLog2e);
     cap2 = f2_splat(cap * kLog2e);
-    mfs = f2_splat(-4.f * scale_);
     fs = f2_splat(4.f * scale_);
     sc2 = f2_splat(scale_ * kLog2e);
     scale = f2_splat(scale_);
@@ -157,17 +156,20 @@ __device__ __forceinline__ void score_pair(uint32_t s0, uint32_t s1, uint64_t ls
                                            uint64_t &f) {
   const uint64_t s2 = f2_pack(__uint_as_float(s0), __uint_as_float(s1));
   if constexpr (CAP) {
-    uint64_t r2;
+    uint64_t r2, e2;
     if constexpr (FRCP) {
-      r2 = f2_sigmoid2_neg(f2_mul(s2, k.cin));
+      r2 = f2_sigmoid2_neg(f2_mul(s2, k.cin), e2);
     } else {
       float xa, xb, da, db;
       f2_unpack(f2_mul(s2, k.cin), xa, xb);
-      f2_unpack(f2_add(f2_pack(ex2_approx(xa), ex2_approx(xb)), k.one), da, db);
+      e2 = f2_pack(ex2_approx(fminf(xa, 126.f)), ex2_approx(fminf(xb, 126.f)));
+      f2_unpack(f2_add(e2, k.one), da, db);
       r2 = f2_pack(rcp_approx(da), rcp_approx(db));
     }
     y = f2_sub(f2_fma(r2, k.mcap2, k.cap2), lse2);
-    f = f2_mul(r2, f2_fma(r2, k.mfs, k.fs));  // 4 scale r (1 - r)
+    // 1 - tanh^2 = 4 r (1 - r) = 4 e r^2: the second form keeps full relative accuracy where the
+    // cap saturates (r -> 1, where 1 - r would cancel), so the tiny gradients there stay right.
+    f = f2_mul(f2_mul(e2, k.fs), f2_mul(r2, r2));
   } else {
     y = f2_sub(f2_mul(s2, k.sc2), lse2);
     f = k.scale;

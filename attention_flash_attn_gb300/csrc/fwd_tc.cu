@@ -141,11 +141,16 @@ __device__ __forceinline__ float logits2(uint32_t (&x)[N], const FwdScore &k, in
   return fmaxf(m0, m1);
 }
 
-// FIXM (soft-cap on, cap <= kFixedMaxCap): every logit is at most cap, so the row's exponent
-// offset is fixed up front at max(cap, sink) instead of tracked -- no running maximum, no
-// partner exchange of maxima, no rescaling of O.  Softmax is invariant to the offset, and the
-// smallest visible probability, 2^(-2 cap log2(e)), stays a normal float for cap < 43.6.
-constexpr float kFixedMaxCap = 41.5f;
+// FIXM (soft-cap on, cap <= kFixedMaxCap): every capped logit lies in [-cap, cap], so the row's
+// exponent offset is fixed up front instead of tracked -- no running maximum, no partner
+// exchange of maxima, no rescaling of O.  Softmax is invariant to the offset.  In log2 units the
+// offset is max(cap - delta, sink) with delta = max(0, 2 cap - 124): the smallest visible
+// probability (2^(delta - 2 cap) without a sink) stays a normal float, and the largest is at
+// most 2^delta <= 2^32 (the tracked form lets P reach 2^8 before it rescales).  With a larger
+// sink the sink's own term (1) dominates the row sum, so probabilities that underflow there are
+// negligible.
+constexpr float kFixedMaxCap = 54.0f;  // 2 cap log2(e) - 124 <= 32
+__device__ __forceinline__ float fixed_delta(float cap) { return fmaxf(0.f, 2.f * cap * kLog2e - 124.f); }
 
 template <int D, int BN, int NK, int NV, bool CAP, bool FIXM>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_ref = sink_col ? sink_logit(p, h) * kLog2e : -INFINITY;  // running max (log2 units)
     float l = (sink_col && half == 0) ? 1.f : 0.f;                   // this half's sum relative to m_ref
     if (FIXM) {  // fixed offset: the cap bounds every logit
-      const float m_fix = fmaxf(p.cap * kLog2e, m_ref);
+      const float m_fix = fmaxf(p.cap * kLog2e - fixed_delta(p.cap), m_ref);
       l = (sink_col && half == 0) ? ex2_approx(m_ref - m_fix) : 0.f;
       m_ref = m_fix;
     }

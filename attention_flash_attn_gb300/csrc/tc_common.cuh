@@ -366,17 +366,23 @@ __device__ __forceinline__ uint64_t f2_splat(float a) { return f2_pack(a, a); }
 // r <- r + r (1 - d r) square that error twice, to 6.5e-6 (always from below).  With
 // t = cap (1 - 2 r) the logit error is at most 2 cap r 6.5e-6: vanishing for the largest
 // logits (r -> 0), largest for the smallest (r -> 1, where P is negligible).
-__device__ __forceinline__ uint64_t f2_sigmoid2_neg(uint64_t x2) {
+// Also returns e = 2^x (clamped like x), with which 1 - r = e r holds without cancellation.
+__device__ __forceinline__ uint64_t f2_sigmoid2_neg(uint64_t x2, uint64_t &e2) {
   float xa, xb;
   f2_unpack(x2, xa, xb);
   const uint64_t m1 = f2_splat(-1.f), one = f2_splat(1.f);
-  const uint64_t nd = f2_fma(f2_pack(ex2_approx(fminf(xa, 126.f)), ex2_approx(fminf(xb, 126.f))), m1, m1);
+  e2 = f2_pack(ex2_approx(fminf(xa, 126.f)), ex2_approx(fminf(xb, 126.f)));
+  const uint64_t nd = f2_fma(e2, m1, m1);
   float na, nb;
   f2_unpack(nd, na, nb);  // -d: its bits are those of d plus the sign bit, folded into the constant
   uint64_t r = f2_pack(__uint_as_float(0xFEF311C0u - __float_as_uint(na)), __uint_as_float(0xFEF311C0u - __float_as_uint(nb)));
   r = f2_fma(r, f2_fma(nd, r, one), r);
   r = f2_fma(r, f2_fma(nd, r, one), r);
   return r;
+}
+__device__ __forceinline__ uint64_t f2_sigmoid2_neg(uint64_t x2) {
+  uint64_t e2;
+  return f2_sigmoid2_neg(x2, e2);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {

@@ -238,6 +238,29 @@ def test_varlen_sequences_are_isolated_under_gqa():
     assert not torch.equal(a["O"][:, q0:q1], b["O"][:, q0:q1])
 
 
+@pytest.mark.parametrize("cap", [30.0, 50.0, 54.0, 60.0])
+def test_rows_saturated_at_minus_cap(cap):
+    """Every logit of every row near -cap (u / cap about -8, keys 10 % apart in length, queries
+    anti-aligned with them): the smallest probabilities the forward can produce, for caps on
+    both sides of the bound below which its exponent offset is fixed rather than tracked, and
+    gradients through a cap factor 1 - tanh^2 of about 1e-6 (deep enough to test the factor's
+    accuracy, shallow enough for the fp64 definition to resolve it).  Checked against the oracle,
+    forward and backward."""
+    w = Workload(f"saturated_cap{cap:g}", "bf16", B=1, Sq=300, Sk=300, Hq=2, Hkv=1, D=64, causal=True,
+                 softcap=cap)
+    inp = make_inputs(w)
+    g = torch.Generator().manual_seed(3)
+    direction = torch.randn(w.D, generator=g)
+    direction = direction / direction.norm()
+    a = (8.0 * cap * w.D ** 0.5) ** 0.5  # |q| |k| scale = 8 cap
+    lengths = 1.0 + 0.1 * (2 * torch.rand(w.Sk, generator=g) - 1)
+    inp["k"] = (a * lengths[None, :, None, None] * direction).expand(w.B, w.Sk, w.Hkv, w.D).to(torch.bfloat16).contiguous()
+    inp["q"] = (-a * direction).expand(w.B, w.Sq, w.Hq, w.D).to(torch.bfloat16).contiguous()
+    ref = full_oracle(w, inp)
+    assert np.all(ref["LSE"] < -0.9 * cap + np.log(w.Sk) + 1)  # the logits really sit near -cap
+    check(w, run_gpu(w, inp), ref)
+
+
 def test_fully_masked_rows_with_and_without_sink():
     """Queries whose segment id has no key: O = 0, LSE = -inf (no sink) or sink."""
     w = Workload("masked_rows", "bf16", B=1, Sq=160, Sk=160, Hq=2, Hkv=1, D=64, causal=False)
