@@ -12,7 +12,7 @@ SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
 
 
 def _source_constant():
-    body = open(SRC).read().split("f2_sigmoid2_neg(uint64_t x2)", 1)[1].split("\n}\n", 1)[0]
+    body = open(SRC).read().split("f2_sigmoid2_neg(uint64_t x2, uint64_t &e2)", 1)[1].split("\n}\n", 1)[0]
     (k,) = re.findall(r"0x([0-9A-Fa-f]{8})u - __float_as_uint\(na\)", body)
     steps = body.count("r = f2_fma(r, f2_fma(nd, r, one), r);")
     (clamp,) = re.findall(r"fminf\(xa, ([0-9.]+)f\)", body)
