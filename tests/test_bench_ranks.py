@@ -34,7 +34,7 @@ def _rank(rank, world, port, out):
 
 def test_max_over_ranks_and_whole_job_throughput_gloo():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank, args=(world, _free_port(), out), nprocs=world, join=True)
         res = dict(out)
