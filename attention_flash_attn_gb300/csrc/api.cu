@@ -23,7 +23,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // Workspace carve-up.  Offsets are 0 when a region is absent.
 struct Layout {
   size_t status = 0, mono = 0, qrange = 0, krange = 0, seg = 0, segk = 0, qoff = 0, koff = 0;
-  size_t dvec = 0, lse2 = 0, dsink_part = 0, dqacc = 0, dbias_acc = 0;
+  size_t dvec = 0, lse2 = 0, dsplit = 0, dsink_part = 0, dqacc = 0, dbias_acc = 0;
   size_t o_part = 0, lse_part = 0;
   size_t total = 0;
 };
@@ -68,6 +68,7 @@ Layout layout(const attn_args *a, bool bwd) {
     const size_t sq_pad = (size_t)(a->Sq + 127) / 128 * 128;
     L.dvec = off; off += align_up((size_t)a->B * a->Hq * sq_pad * sizeof(float));
     if (use_tc_bwd(a)) { L.lse2 = off; off += align_up((size_t)a->B * a->Hq * sq_pad * sizeof(float)); }
+    if (use_tc_bwd(a) && tc_bwd_fused(a->D)) { L.dsplit = off; off += align_up((size_t)a->B * a->Hq * sq_pad * 16); }
     if (a->sink) {
       L.dsink_part = off;
       off += align_up((size_t)a->Hq * bwd_pre_partials(a->B, a->Sq) * sizeof(float));
@@ -261,6 +262,7 @@ int attn_bwd(const attn_args *a, const void *O, const float *LSE, const void *dO
   const bool tc = use_tc_bwd(a);
   p.dQacc = tc ? reinterpret_cast<float *>(w + L.dqacc) : nullptr;
   p.lse2p = tc ? reinterpret_cast<float *>(w + L.lse2) : nullptr;
+  p.dsplit = tc && tc_bwd_fused(a->D) ? reinterpret_cast<uint4 *>(w + L.dsplit) : nullptr;
   p.dbias_acc = a->bias ? reinterpret_cast<float *>(w + L.dbias_acc) : nullptr;
   if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
   if (a->bias && cudaMemsetAsync(p.dbias_acc, 0, dbias_elems(a) * sizeof(float), st) != cudaSuccess)

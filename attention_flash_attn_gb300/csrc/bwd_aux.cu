@@ -71,6 +71,21 @@ __device__ __forceinline__ float chunk_dot_raw<float>(const uint4 &x, const uint
                    fmaf(__uint_as_float(x.z), __uint_as_float(y.z), __uint_as_float(x.w) * __uint_as_float(y.w))));
 }
 
+// -D as three bf16 parts, in the first three of a row's eight bf16 slots (the other five
+// zero): the row of the fused tensor-core backward's K = 16 operand that starts dP^T at -D.
+// Each part is the bf16 rounding of what the ones before it left; every subtraction is exact
+// in fp32 and the last remainder fits 8 bits, so the parts sum to -D exactly (barring
+// underflow).
+__device__ __forceinline__ uint4 neg_d_parts(float d) {
+  const float x = -d;
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+  return make_uint4((uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(mid) << 16),
+                    (uint32_t)__bfloat16_as_ushort(lo), 0u, 0u);
+}
+
 // grid (ceil(Sq/64), B), block 256: warp w handles heads w, w+8, ...; rows in order, so the
 // per-(block, head) partial sums are deterministic.
 //
@@ -123,6 +138,7 @@ __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int z
             const float lse = p.LSE[ri];
             p.Dvec[rp] = s[u];
             if (p.lse2p) p.lse2p[rp] = lse * 1.4426950408889634f;
+            if (p.dsplit) p.dsplit[rp] = neg_d_parts(s[u]);
             if (p.sink) part = fmaf(expf(sink - lse), s[u], part);
           }
           if (zero_dqacc) {
@@ -147,6 +163,7 @@ __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int z
         if (lane == 0) {
           p.Dvec[rp] = s;
           if (p.lse2p) p.lse2p[rp] = p.LSE[ri] * 1.4426950408889634f;
+          if (p.dsplit) p.dsplit[rp] = neg_d_parts(s);
         }
         if (p.sink) part = fmaf(expf(sink - p.LSE[ri]), s, part);
         if (zero_dqacc) {
@@ -163,6 +180,7 @@ __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int z
         const size_t rp = ((size_t)b * p.Hq + h) * p.sq_pad + i;
         p.Dvec[rp] = 0.f;
         if (p.lse2p) p.lse2p[rp] = INFINITY;
+        if (p.dsplit) p.dsplit[rp] = make_uint4(0u, 0u, 0u, 0u);
       }
   }
 }

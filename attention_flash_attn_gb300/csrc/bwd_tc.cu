@@ -14,7 +14,11 @@
 //
 // The cap's chain-rule factor is applied before dK and dQ are formed (tokamax soft-capping
 // VJP page).  P is recomputed from the forward's LSE with the forward's score function.  Each
-// query step's Q, dO, LSE*log2(e) and D arrive together by TMA / bulk copy.
+// query step's Q, dO, LSE*log2(e) and D arrive together by TMA / bulk copy.  In the one-pass
+// form (head dim 64 / 128) D arrives as -D split into bf16 parts and a K = 16 MMA against a
+// tile of ones starts the dP^T accumulator at -D: every softmax thread would otherwise read
+// each query's D from shared memory (a broadcast load that still costs the LSU several
+// wavefronts), and subtract it.
 //
 // Head dim 256: dK and dV fill all 512 TMEM columns, so the CTA runs two passes over its
 // query steps -- dV first, then dK and dQ (S^T recomputed).  V is not needed in the dV pass, so
@@ -63,9 +67,20 @@ struct BwdCfg {
   static constexpr int NSLOT = TWO ? 2 : NS;       // two-pass: slot 1 is V's space (dV pass only)
   static constexpr int DS_BYTES = kBK * BQ * 2;
   static constexpr int DQS_BYTES = 16384;          // one bulk reduce box of fp32 dQ
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = KV_BYTES;
-  static constexpr int OFF_SLOT0 = 2 * KV_BYTES;
+  // Fused form: dP^T starts at -D.  One K = 16 MMA of a tile of ones against the step's -D,
+  // split into three bf16 parts per query, fills the dP^T columns before the dP^T MMAs
+  // accumulate onto them, so the softmax warps form dS = P f (dP - D) without reading D.
+  // Both tiles use the no-swizzle K-major layout (8-row x 16-byte core matrices); per slot the
+  // -D parts are [BQ rows x 8] bf16 (k = 0..7), followed by the zeros of k = 8..15.  They sit
+  // below the K / V tiles.
+  static constexpr bool FOLD = !TWO;
+  static constexpr int ONES_BYTES = FOLD ? 4096 : 0;
+  static constexpr int DSP_BYTES = FOLD ? BQ * 32 : 0;
+  static constexpr int OFF_ONES = 0;
+  static constexpr int OFF_DSP = OFF_ONES + ONES_BYTES;
+  static constexpr int OFF_K = (ONES_BYTES + NSLOT * DSP_BYTES + 1023) / 1024 * 1024;
+  static constexpr int OFF_V = OFF_K + KV_BYTES;
+  static constexpr int OFF_SLOT0 = OFF_K + 2 * KV_BYTES;
   static constexpr int OFF_DS = OFF_SLOT0 + NS * SLOT_BYTES;
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
   static constexpr int OFF_LD = OFF_DQS + DQS_BYTES;  // per slot: LSE*log2e [BQ], D [BQ]
@@ -188,13 +203,12 @@ __device__ __forceinline__ uint32_t bf16_pair(uint64_t v) {
 
 // One 32-query chunk of a key row, every column treated as visible (masked columns are
 // cleared afterwards by the fix-ups below, only on chunks that need it):
-//   KIND 1: P, packed to bf16 pairs;  KIND 0: P and dS = P f (dP - D), both packed.
+//   KIND 1: P, packed to bf16 pairs;  KIND 0: P and dS = P f (dP - D), both packed, from the
+//   dP^T accumulator that started at -D.
 template <bool CAP, bool FRCP, int KIND>
 __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float *lse2c,
-                                          const float *dvc, uint32_t (&pk)[16], uint32_t (&dk)[16],
-                                          const BwdScore &k) {
+                                          uint32_t (&pk)[16], uint32_t (&dk)[16], const BwdScore &k) {
   const uint64_t *l2 = reinterpret_cast<const uint64_t *>(lse2c);
-  const uint64_t *d2 = reinterpret_cast<const uint64_t *>(dvc);
 #pragma unroll
   for (int e2 = 0; e2 < 16; ++e2) {
     uint64_t y, f;
@@ -202,8 +216,8 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32
     const uint64_t p2 = ex2_pair(y);
     pk[e2] = bf16_pair(p2);
     if constexpr (KIND == 0) {
-      const uint64_t dp = f2_pack(__uint_as_float(dr[2 * e2]), __uint_as_float(dr[2 * e2 + 1]));
-      dk[e2] = bf16_pair(f2_mul(f2_mul(p2, f), f2_sub(dp, d2[e2])));
+      const uint64_t dpd = f2_pack(__uint_as_float(dr[2 * e2]), __uint_as_float(dr[2 * e2 + 1]));
+      dk[e2] = bf16_pair(f2_mul(f2_mul(p2, f), dpd));
     }
   }
 }
@@ -382,6 +396,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_barrier_init();
   }
+  if constexpr (C::FOLD) {
+    // The tile of ones (bf16 1.0) and the zero half of each -D tile, written once: the TMA
+    // only ever writes the -D half.
+    for (int i = threadIdx.x; i < C::ONES_BYTES / 16; i += kThreads)
+      reinterpret_cast<uint4 *>(smem + C::OFF_ONES)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    for (int i = threadIdx.x; i < C::NSLOT * BQ; i += kThreads)
+      reinterpret_cast<uint4 *>(smem + C::OFF_DSP + (i / BQ) * C::DSP_BYTES + BQ * 16)[i % BQ] = make_uint4(0u, 0u, 0u, 0u);
+    fence_async_smem();  // visible to the tensor cores after the barrier below
+  }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -520,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(sdp_free);
           }
-          bwd_chunk<CAP, true, C::TWO ? 1 : 0>(sr, dr, lse2 + c * 32, dvv + c * 32, pk[cc], dk[cc], ks);
+          bwd_chunk<CAP, true, C::TWO ? 1 : 0>(sr, dr, lse2 + c * 32, pk[cc], dk[cc], ks);
           if (!full) {
             const uint32_t vis = chunk_vis(q0 + c * 32, lo, hi, seg_pairwise, segq, p.Sq, sid);
             clear_hidden(pk[cc], vis);
@@ -737,16 +760,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (u >= 1 && !mbar_wait(qdo_empty(s), (u - 1) & 1, p.status)) break;
           const int h = step_h(j), q0 = step_q0(j);
           const uint32_t sa = slot_addr(s);
-          mbar_arrive_expect_tx(qdo_full(s), 2 * C::QT_BYTES + 2 * BQ * 4);
+          mbar_arrive_expect_tx(qdo_full(s), 2 * C::QT_BYTES + BQ * 4 + BQ * 16);
   #pragma unroll
           for (int c = 0; c < C::KCH; ++c) {
             tma_load_4d(sa + c * (BQ * 128), &tmQ, qdo_full(s), c * 64, q0, h, b);
             tma_load_4d(sa + C::QT_BYTES + c * (BQ * 128), &tmdO, qdo_full(s), c * 64, q0, h, b);
           }
           const size_t row = ((size_t)b * p.Hq + h) * p.sq_pad + q0;
-          const uint32_t lda = sbase + C::OFF_LD + s * 2 * BQ * 4;
-          bulk_g2s(lda, p.lse2p + row, BQ * 4, qdo_full(s));
-          bulk_g2s(lda + BQ * 4, p.Dvec + row, BQ * 4, qdo_full(s));
+          bulk_g2s(sbase + C::OFF_LD + s * 2 * BQ * 4, p.lse2p + row, BQ * 4, qdo_full(s));
+          bulk_g2s(sbase + C::OFF_DSP + s * C::DSP_BYTES, p.dsplit + row, BQ * 16, qdo_full(s));
         }
       }
     } else if (warp == 9 || warp == 10) {
@@ -772,13 +794,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Loops over 64-column chunks stay rolled (the descriptors advance by one add per
         // chunk) and the four 16-deep MMAs of a chunk are unrolled: compact code that still
         // issues faster than the tensor pipe retires.
-        auto mma_front = [&](uint64_t a_k, uint32_t b_addr, uint32_t d_col) {
+        auto mma_front = [&](uint64_t a_k, uint32_t b_addr, uint32_t d_col, bool onto = false) {
           uint64_t b_k = sw128_desc(b_addr, 16, 1024);
   #pragma unroll 1
           for (int c = 0; c < D / 64; ++c) {
   #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4)
-              mma_ss_w(tmem + d_col, desc_at(a_k, k4 * 32), desc_at(b_k, k4 * 32), idST, (c | k4) != 0);
+              mma_ss_w(tmem + d_col, desc_at(a_k, k4 * 32), desc_at(b_k, k4 * 32), idST, onto || (c | k4) != 0);
             a_k = desc_at(a_k, kBK * 128);
             b_k = desc_at(b_k, BQ * 128);
           }
@@ -966,7 +988,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait_warp(qdo_full(s), use_of(j) & 1, p.status)) return false;
             tc_fence_after();
             mma_front(dK_k, slot_addr(s), C::TM_S);
-            mma_front(dV_k, slot_addr(s) + C::QT_BYTES, C::TM_DP);
+            // dP^T := -D (the ones tile: both offsets 128 bytes, every row reads ones), then
+            // += V dO^T.
+            mma_ss_w(tmem + C::TM_DP, plain_desc(sbase + C::OFF_ONES, 128, 128),
+                     plain_desc(sbase + C::OFF_DSP + s * C::DSP_BYTES, BQ * 16, 128), idST, 0u);
+            mma_front(dV_k, slot_addr(s) + C::QT_BYTES, C::TM_DP, true);
             mma_commit_w(s_full);
             return true;
           };
@@ -1149,6 +1175,7 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
 }  // namespace
 
 bool tc_bwd_supported(int D) { return D == 64 || D == 128 || D == 256; }
+bool tc_bwd_fused(int D) { return D == 64 || D == 128; }
 
 cudaError_t tc_backward(const Params &p, cudaStream_t st) {
   switch (p.D) {

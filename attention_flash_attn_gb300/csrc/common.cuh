@@ -54,6 +54,7 @@ struct Params {
   float *dsink;
   float *Dvec;                    // [B, Hq, sq_pad]: D = rowsum(dO * O), 0 past Sq
   float *lse2p;                   // [B, Hq, sq_pad]: LSE * log2(e), +inf past Sq
+  uint4 *dsplit;                  // [B, Hq, sq_pad]: -D as bf16 parts (hi, mid, lo, 5 zeros), 0 past Sq; fused tc backward only
   int sq_pad;                     // Sq rounded up to a multiple of 128
   float *dQacc;                   // [B, Sq, Hq, D] fp32 accumulator (tensor-core path)
   float *dbias_acc;               // dense fp32 copy of dbias being accumulated

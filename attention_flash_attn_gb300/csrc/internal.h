@@ -45,6 +45,7 @@ cudaError_t launch_splitkv_merge(const Params &p, cudaStream_t st);
 // tcgen05 tensor-core kernels (bf16, D in {64, 128, 256}).
 bool tc_supported(int D);      // forward
 bool tc_bwd_supported(int D);  // backward
+bool tc_bwd_fused(int D);      // the backward's one-pass form (it reads -D split into bf16 parts)
 cudaError_t tc_forward(const Params &p, cudaStream_t st);
 cudaError_t tc_backward(const Params &p, cudaStream_t st);
 

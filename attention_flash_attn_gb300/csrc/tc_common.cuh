@@ -290,6 +290,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr, uint32_t lbo_
   return d;
 }
 
+// The same for an operand without swizzling (swizzle mode 0), K-major: core matrices of
+// 8 rows x 16 bytes, lbo_bytes apart along K and sbo_bytes apart along M / N.
+__device__ __forceinline__ uint64_t plain_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and f32 accumulation.
 // b_mn_major: B operand stored with its N dimension contiguous (else K-major).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
