@@ -107,8 +107,11 @@ struct FwdScore {
   }
 };
 
-// Raw scores -> capped, masked base-2 logits in place; returns their maximum.
-template <bool CAP, bool MASKED, int N>
+// Raw scores -> capped, masked base-2 logits in place; returns their maximum.  MIX: every
+// other pair takes the cap's reciprocal from the special-function unit (rcp.approx) instead of
+// the FMA pipe -- 7 issue slots per pair instead of 11, for two more special-function ops --
+// for kernels whose softmax warps are issue-bound with that unit part idle.
+template <bool CAP, bool MASKED, bool MIX, int N>
 __device__ __forceinline__ float logits2(uint32_t (&x)[N], const FwdScore &k, int jbase, int lo, int hi,
                                          bool pairwise, const int *segk, int sid) {
   float m0 = -INFINITY, m1 = -INFINITY;
@@ -117,7 +120,17 @@ __device__ __forceinline__ float logits2(uint32_t (&x)[N], const FwdScore &k, in
     const uint64_t s2 = f2_pack(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
     uint64_t t2;
     if constexpr (CAP) {
-      t2 = f2_fma(f2_sigmoid2_neg(f2_mul(s2, k.cin)), k.mcap2, k.cap2);
+      const uint64_t x2 = f2_mul(s2, k.cin);
+      uint64_t r2;
+      if (MIX && (e & 2)) {
+        float xa, xb, da, db;
+        f2_unpack(x2, xa, xb);
+        f2_unpack(f2_add(f2_pack(ex2_approx(fminf(xa, 126.f)), ex2_approx(fminf(xb, 126.f))), f2_splat(1.f)), da, db);
+        r2 = f2_pack(rcp_approx(da), rcp_approx(db));
+      } else {
+        r2 = f2_sigmoid2_neg(x2);
+      }
+      t2 = f2_fma(r2, k.mcap2, k.cap2);
     } else {
       t2 = f2_mul(s2, k.sc2);
     }
@@ -449,8 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool full = !any_pairwise && (t0 + j) * BN >= cta_lo && (t0 + j + 1) * BN <= cta_hi;
       float mx = -INFINITY;
       if (got) {
-        mx = full ? logits2<CAP, false>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid)
-                  : logits2<CAP, true>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid);
+        mx = full ? logits2<CAP, false, (D <= 128)>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid)
+                  : logits2<CAP, true, (D <= 128)>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid);
       }
       float alpha_o = 1.f;
       bool resc = false;
