@@ -103,6 +103,22 @@ def test_kv_splits_workspace(capi):
     assert f32(kv_splits=7) == f32()
 
 
+def test_backward_workspace_regions(capi):
+    """The backward's workspace: a 256-byte status word, then 256-byte-aligned regions for D
+    (fp32 per padded query row, rows padded to 128), LSE*log2(e) and the fp32 dQ accumulator
+    on the tensor-core path, and -- for its one-pass form (head dim 64 or 128), which starts
+    dP^T at -D -- one 16-byte row of -D's bf16 parts per padded query row."""
+    L = capi.lib()
+    up = lambda x: (x + 255) // 256 * 256
+    B, S, H = 1, 100, 2
+    rows = B * H * 128  # Sq = 100 padded to 128
+    bw = lambda **kw: L.attn_bwd_workspace_size(ctypes.byref(valid_args(capi, B=B, S=S, H=H, **kw)))
+    for D in (64, 128):  # one-pass form
+        assert bw(D=D) == 256 + up(rows * 4) * 2 + up(rows * 16) + up(B * S * H * D * 4)
+    assert bw(D=256) == 256 + up(rows * 4) * 2 + up(B * S * H * 256 * 4)  # two-pass form
+    assert bw(D=64, dtype=2) == 256 + up(rows * 4)  # fp32: FFMA kernels, D only
+
+
 def test_cu_seqlens_with_segments_unsupported_and_shape_rules(capi):
     L = capi.lib()
     # separate key boundaries: need cu_seqlens; lift the Sq == Sk rule; B stays 1
