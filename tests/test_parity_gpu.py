@@ -261,6 +261,30 @@ def test_rows_saturated_at_minus_cap(cap):
     check(w, run_gpu(w, inp), ref)
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_large_d_against_small_dp_minus_d(D):
+    """V and dO with a common mean of 3 in every component: D = dO . O is large (up to 9 D)
+    while dP - D, all that dS keeps of it, stays at the noise level.  The head-dim 64 / 128
+    kernels subtract D inside the dP^T accumulator (a K = 16 MMA against -D split into three
+    bf16 parts); keeping -D only to bf16 precision there would put dQ about 7 % off at
+    D = 64.  The reference takes D from the kernel's own stored O, as the method defines it,
+    so that only the subtraction is under test."""
+    w = Workload(f"large_d_{D}", "bf16", B=1, Sq=300, Sk=300, Hq=2, Hkv=1, D=D, causal=True,
+                 softcap=30.0, sink=True)
+    inp = make_inputs(w)
+    g = torch.Generator().manual_seed(5)
+    inp["v"] = (3.0 + torch.randn(inp["v"].shape, generator=g)).to(torch.bfloat16)
+    inp["dO"] = (3.0 + torch.randn(inp["dO"].shape, generator=g)).to(torch.bfloat16)
+    gpu = run_gpu(w, inp)
+    p = problem_from_inputs(w, inp)
+    O, LSE = oracle.forward(p)
+    assert frob_rel(to64(gpu["O"]), O) <= TOL["bf16"]
+    ref = oracle.backward(p, to64(inp["dO"]), to64(gpu["O"]), LSE)
+    assert np.abs(ref["D"]).mean() > 3 * D  # the sink takes part of each row's mass
+    for key in ("dq", "dk", "dv", "dsink"):
+        assert frob_rel(to64(gpu[key]), ref[key]) <= TOL["bf16"], (key, frob_rel(to64(gpu[key]), ref[key]))
+
+
 def test_fully_masked_rows_with_and_without_sink():
     """Queries whose segment id has no key: O = 0, LSE = -inf (no sink) or sink."""
     w = Workload("masked_rows", "bf16", B=1, Sq=160, Sk=160, Hq=2, Hkv=1, D=64, causal=False)
