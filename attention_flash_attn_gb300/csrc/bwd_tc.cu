@@ -83,7 +83,7 @@ struct BwdCfg {
   static constexpr int OFF_SLOT0 = OFF_K + 2 * KV_BYTES;
   static constexpr int OFF_DS = OFF_SLOT0 + NS * SLOT_BYTES;
   static constexpr int OFF_DQS = OFF_DS + DS_BYTES;
-  static constexpr int OFF_LD = OFF_DQS + DQS_BYTES;  // per slot: LSE*log2e [BQ], D [BQ]
+  static constexpr int OFF_LD = OFF_DQS + DQS_BYTES;  // per slot: LSE*log2e [BQ], D [BQ] (D unused in the fused form)
   static constexpr int OFF_BAR = OFF_LD + NSLOT * 2 * BQ * 4;
   static constexpr int NBAR = 12 + 2 * NSLOT + (TWO ? 23 : 0);  // + dQ half-1 release, dO hand-over, dS buffers
   // Two-pass form, dK pass: the dV pass's second dO stage holds the second dS^T buffer and two
