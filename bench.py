@@ -389,6 +389,27 @@ def time_oracle(w: Workload, inp: dict, S: int):
     return sw, sub, dt
 
 
+def host_cpu() -> str:
+    """The host's processor, named beside the oracle's timings: the model name where the OS
+    reports one (x86), else the ARM implementer and part codes."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k = k.strip()
+                if k in ("model name", "CPU implementer", "CPU part") and k not in fields:
+                    fields[k] = v.strip()
+    except OSError:
+        pass
+    if "model name" in fields:
+        return f"{platform.machine()} {fields['model name']}"
+    if "CPU part" in fields:
+        return f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return platform.machine()
+
+
 def cpu_baseline(w: Workload, inp: dict, seg):
     import oracle
     oracle.build()
@@ -396,7 +417,7 @@ def cpu_baseline(w: Workload, inp: dict, seg):
     sw, sub, dt = time_oracle(w, inp, S)
     f = flops(sw, sub["seg"], "fwdbwd")
     return {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle",
+            "cpu": host_cpu(), "kind": "oracle",
             "sample": f"fp64 oracle fwd+bwd on the first {sw.Sq} query rows and {sw.Sk} keys of batch 0, "
                       f"kv group 0 ({sw.Hq} query heads) of {w.name}; {dt:.1f} s"}
 
@@ -426,8 +447,8 @@ def run_reference(args):
         "data": "synthetic (seeded N(0,s^2) inputs of the workload's shape; no dataset)",
         "config": {"workload": w.name, "B": w.B, "S": w.Sq, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                    "causal": w.causal, "window": w.window, "softcap": w.softcap},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "cpu": host_cpu(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

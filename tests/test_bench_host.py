@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import oracle
-from bench import flops, visible_pairs
+from bench import flops, host_cpu, visible_pairs
 from workloads import WORKLOADS, Workload, make_inputs
 
 
@@ -85,3 +85,13 @@ def test_clock_samples_are_taken_inside_the_timed_region(tmp_path):
     c.mark(now, now + 0.05)
     clk = c.stop()
     assert clk == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 2}
+
+
+def test_host_cpu_names_the_processor():
+    """The oracle's timings name the host processor: the machine type, then a model name or
+    the ARM implementer / part codes."""
+    import platform
+    name = host_cpu()
+    assert name.startswith(platform.machine())
+    assert len(name) > len(platform.machine())
+
