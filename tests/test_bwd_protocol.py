@@ -1,5 +1,5 @@
-"""Model check of the head-dim-256 backward's mbarrier protocol (two-pass form of
-attention_flash_attn_gb300/csrc/bwd_tc.cu), run on the CPU.
+"""Model check of the tensor-core backward's mbarrier protocols (attention_flash_attn_gb300/
+csrc/bwd_tc.cu), run on the CPU: the head-dim-256 two-pass form and the one-pass form.
 
 Each agent of the kernel -- TMA lanes 0 and 1, the front MMA warp (S^T, dK, dP^T), the
 back MMA warp (dV, dQ), the softmax warps, the dQ drain -- is a generator that yields the
@@ -12,9 +12,11 @@ waiter may ever see a count outside {k, k + 1}.
 The negative control replays the earlier layout, in which the half-tile ring was read by
 two warps; the model must flag it (that layout timed out intermittently on the GPU).
 
-simulate_split_rings is the kernel's current protocol (two Q slots and one dO slot in the dK
-pass, double-buffered dS^T).  simulate and simulate_vtmem are the two layouts before it, kept
-as models of the same rules on different ring shapes.
+simulate_split_rings is the two-pass form's current protocol (two Q slots and one dO slot in
+the dK pass, double-buffered dS^T).  simulate and simulate_vtmem are the two layouts before it,
+kept as models of the same rules on different ring shapes.  simulate_fused is the one-pass
+form (head dims 64 and 128), with the front warp's MMAs completing asynchronously, so that it
+can also check that no stage is refilled while they still read it.
 """
 import random
 from collections import defaultdict
@@ -614,3 +616,102 @@ def test_split_rings_protocol_never_deadlocks_or_aliases():
         nper = STEP_COUNTS[trial % len(STEP_COUNTS)]
         finished, hazards = simulate_split_rings(nper, rng)
         assert finished and not hazards, (nper, hazards[:3])
+
+
+def simulate_fused(nsteps, rng, ns=3, skip_chain=False):
+    """The one-pass form (head dims 64 and 128): a ring of ns Q / dO stages (each also holding
+    the step's LSE and -D tile), filled by the TMA lane and released by the back MMA warp's
+    commit; the front warp issues S^T, the K = 16 MMA that starts dP^T at -D, and dP^T; the
+    back warp dV, dK, dQ.  The front warp's commit does not cover the stage's release, so the
+    -D tile (read by the front warp's init MMA) may only be refilled once s_full of its step
+    has completed: the model's loader refills a stage on qdo_empty, which the back warp commits
+    only after p_ready, which the softmax arrives on only after s_full.  skip_chain drops the
+    softmax's wait on s_full (so nothing orders the refill after the front warp's MMAs) and the
+    model must then report the refill racing the init MMA."""
+    need = defaultdict(lambda: 1)
+    need.update({"fin_done": 2})  # front and back MMA warps
+    count, done, hazards = defaultdict(int), defaultdict(int), []
+    reads = defaultdict(int)  # stage -> front-warp MMAs issued on it and not yet complete
+
+    def arrive(b):
+        count[b] += 1
+        if count[b] == need[b]:
+            count[b] = 0
+            done[b] += 1
+
+    slot, use = (lambda j: j % ns), (lambda j: j // ns)
+
+    def loader():
+        yield ("arrive", "kv_full")
+        for j in range(nsteps):
+            s, u = slot(j), use(j)
+            if u >= 1:
+                yield ("wait", f"qdo_empty{s}", u - 1)
+                if reads[s]:
+                    hazards.append(("loader", f"stage{s}", u, "refilled under the init MMA"))
+            yield ("arrive", f"qdo_full{s}")
+
+    def front():
+        yield ("wait", "kv_full", 0)
+        for j in range(nsteps):
+            if j >= 1:
+                yield ("wait", "sdp_free", j - 1)
+            yield ("wait", f"qdo_full{slot(j)}", use(j))
+            reads[slot(j)] += 1  # S^T, the -D init and dP^T read the stage
+            yield ("arrive", f"issued{j}")  # handed to the tensor pipe; completes later
+        yield ("arrive", "fin_done")
+
+    def tensor_pipe():  # completes the front warp's MMAs in issue order, then its commit arrives
+        for j in range(nsteps):
+            yield ("wait", f"issued{j}", 0)
+            reads[slot(j)] -= 1
+            yield ("arrive", "s_full")
+
+    def back():
+        yield ("wait", "kv_full", 0)
+        for j in range(1, nsteps + 1):
+            jj = j - 1
+            yield ("wait", "p_ready", jj)
+            if jj >= 1:
+                yield ("wait", "dq_empty", jj - 1)
+            yield ("arrive", "dq_full")
+            yield ("arrive", "mma_done")
+            yield ("arrive", f"qdo_empty{slot(jj)}")
+        yield ("arrive", "fin_done")
+
+    def softmax():
+        for j in range(nsteps):
+            if not skip_chain:
+                yield ("wait", "s_full", j)
+            yield ("wait", f"qdo_full{slot(j)}", use(j))
+            yield ("arrive", "sdp_free")
+            if j >= 1:
+                yield ("wait", "mma_done", j - 1)
+            yield ("arrive", "p_ready")
+        if nsteps > 0:
+            yield ("wait", "fin_done", 0)
+
+    def drain():
+        for h in range(nsteps):
+            yield ("wait", "dq_full", h)
+            yield ("arrive", "dq_empty")
+
+    return run_agents({"loader": loader(), "front": front(), "tensor": tensor_pipe(), "back": back(),
+                       "softmax": softmax(), "drain": drain()}, arrive, done, hazards, rng)
+
+
+def test_fused_protocol_never_deadlocks_aliases_or_refills_under_the_init_mma():
+    rng = random.Random(4242)
+    for trial in range(1500):
+        nsteps = STEP_COUNTS[trial % len(STEP_COUNTS)]
+        finished, hazards = simulate_fused(nsteps, rng)
+        assert finished and not hazards, (nsteps, hazards[:3])
+
+
+def test_fused_model_flags_a_refill_without_the_s_full_chain():
+    rng = random.Random(5)
+    flagged = False
+    for trial in range(300):
+        finished, hazards = simulate_fused(12, rng, skip_chain=True)
+        flagged |= any(h[3] == "refilled under the init MMA" for h in hazards if len(h) == 4)
+    assert flagged
