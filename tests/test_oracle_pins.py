@@ -25,21 +25,24 @@ def rng(seed=0):
 
 
 def full_problem(S=7, D=4, Hq=2, Hkv=1, B=1, seed=0, cap=2.0, causal=True, window=4,
-                 bias=True, sink=True, segs=True, q_std=1.5):
+                 bias=True, sink=True, segs=True, q_std=1.5, Sk=None):
+    Sk = S if Sk is None else Sk
     r = rng(seed)
     q = r.normal(0, q_std, (B, S, Hq, D))
-    k = r.normal(0, q_std, (B, S, Hkv, D))
-    v = r.normal(0, 1, (B, S, Hkv, D))
+    k = r.normal(0, q_std, (B, Sk, Hkv, D))
+    v = r.normal(0, 1, (B, Sk, Hkv, D))
     kw = dict(scale=1 / math.sqrt(D), causal=causal, window=window, softcap=cap)
     if bias:
-        kw["bias"] = r.normal(0, 1, (1, Hq, S, S))
+        kw["bias"] = r.normal(0, 1, (1, Hq, S, Sk))
     if sink:
         kw["sink"] = r.normal(0, 1, (Hq,))
     if segs:
-        cut = S // 2 + 1
-        seg = np.zeros((B, S), np.int32)
-        seg[:, cut:] = 1
-        kw["seg_q"] = seg
+        # the last query and the last key share the second segment (bottom-right alignment)
+        seg_q = np.zeros((B, S), np.int32)
+        seg_q[:, S // 2 + 1:] = 1
+        seg_k = np.zeros((B, Sk), np.int32)
+        seg_k[:, Sk - (S - S // 2 - 1):] = 1
+        kw["seg_q"], kw["seg_k"] = seg_q, seg_k
     return Problem(q, k, v, **kw), r.normal(0, 1, (B, S, Hq, D))
 
 
@@ -55,11 +58,14 @@ def rel(a, b):
 
 # ----------------------------------------------------------------- whole fwd / bwd
 
-@pytest.mark.parametrize("S", [5, 7])
-def test_backward_matches_central_finite_differences(S):
+@pytest.mark.parametrize("S,Sk,causal", [(5, 5, True), (7, 7, True), (5, 8, True), (5, 8, False),
+                                         (8, 5, True)])
+def test_backward_matches_central_finite_differences(S, Sk, causal):
     """Analytic dQ, dK, dV, dbias, dsink equal central differences of sum(O*dO) in fp64
-    (bias + sink + cap + causal + window + segments all on)."""
-    p, dO = full_problem(S=S)
+    (bias + sink + cap + window + segments all on, causal or not), also with fewer queries
+    than keys and more queries than keys, where the window is measured from each query's
+    bottom-right aligned position."""
+    p, dO = full_problem(S=S, Sk=Sk, causal=causal, window=3 if Sk != S else 4)
     O, LSE = oracle.forward(p)
     g = oracle.backward(p, dO, O, LSE)
     h = 1e-5
@@ -401,7 +407,64 @@ def test_visible_pair_counts_closed_forms():
     assert _count(S, seg=seg) == sum(L * L for L in lens)
     # bottom-right causal with Sq < Sk: query i sees keys 0 .. i + Sk - Sq
     assert _count(5, Sk=9, causal=True) == sum(i + 4 + 1 for i in range(5))
+    # Windows with Sq != Sk, counted by hand from the bottom-right reading (query i stands at
+    # key position i + Sk - Sq and sees the W keys ending there; without causal, every key
+    # from that window's start to the end).  Sq = 5, Sk = 9, W = 3: every row sees 3 keys
+    # causally; without causal row i sees keys i + 2 .. 8, i.e. 7, 6, 5, 4, 3.
+    assert _count(5, Sk=9, causal=True, window=3) == 15
+    assert _count(5, Sk=9, window=3) == 25
+    # Sq = 9, Sk = 5, W = 2: query i stands at i - 4.  Causal: rows 0-3 see nothing, row 4
+    # sees key 0, rows 5-8 see two keys each.  Without causal: row i sees keys i - 5 .. 4,
+    # i.e. 5 for rows 0-5 and then 4, 3, 2.
+    assert _count(9, Sk=5, causal=True, window=2) == 9
+    assert _count(9, Sk=5, window=2) == 5 * 6 + 4 + 3 + 2
     assert _count(S, causal=True, B=2, Hq=3) == 6 * S * (S + 1) // 2
+
+
+@pytest.mark.parametrize("causal,window", [(True, 0), (True, 3), (False, 3)])
+def test_bottom_right_alignment_equals_square_problem(causal, window):
+    """With Sq < Sk, query i of the short problem is query i + Sk - Sq of the square problem on
+    the same keys (extra queries in front); with Sq > Sk under causal masking, queries past
+    Sq - Sk are the square problem's on their own keys and the leading ones see nothing.  The
+    square case is pinned above (closed-form counts, finite differences), so these fix the
+    alignment of the causal and window terms when the lengths differ: O, LSE and every
+    gradient."""
+    r = rng(21)
+    D, Hq, Hkv, Sq, Sk = 4, 2, 1, 5, 9
+    off = Sk - Sq
+    k = r.normal(0, 1.5, (1, Sk, Hkv, D))
+    v = r.normal(0, 1, (1, Sk, Hkv, D))
+    q_sq = r.normal(0, 1.5, (1, Sk, Hq, D))
+    dO_sq = r.normal(0, 1, (1, Sk, Hq, D))
+    kw = dict(scale=0.5, causal=causal, window=window, softcap=3.0, sink=r.normal(0, 1, (Hq,)))
+    square = Problem(q_sq, k, v, **kw)
+    short = Problem(q_sq[:, off:].copy(), k, v, **kw)
+    Os, Ls = oracle.forward(square)
+    O, L = oracle.forward(short)
+    np.testing.assert_allclose(O, Os[:, off:], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(L, Ls[:, :, off:], rtol=0, atol=1e-13)
+    # gradients: dO zero on the square problem's extra queries, so only the shared ones count
+    dO_sq[:, :off] = 0.0
+    gs = oracle.backward(square, dO_sq, Os, Ls)
+    g = oracle.backward(short, dO_sq[:, off:].copy(), O, L)
+    np.testing.assert_allclose(g["dq"], gs["dq"][:, off:], rtol=0, atol=1e-13)
+    for key in ("dk", "dv", "dsink"):
+        np.testing.assert_allclose(g[key], gs[key], rtol=0, atol=1e-13)
+    if not causal:
+        return
+    # Sq > Sk: the keys are the square problem's first Sq - off ... swap the roles: 9 queries
+    # against 5 keys; rows 4.. equal the 5 x 5 problem on those rows, rows 0..3 see nothing.
+    k5, v5 = k[:, :Sq], v[:, :Sq]
+    q9 = r.normal(0, 1.5, (1, Sk, Hq, D))
+    tall = Problem(q9, k5, v5, **kw)
+    sq5 = Problem(q9[:, off:].copy(), k5, v5, **kw)
+    Ot, Lt = oracle.forward(tall)
+    O5, L5 = oracle.forward(sq5)
+    np.testing.assert_allclose(Ot[:, off:], O5, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(Lt[:, :, off:], L5, rtol=0, atol=1e-13)
+    assert np.all(Ot[:, :off] == 0)
+    np.testing.assert_allclose(Lt[:, :, :off], np.broadcast_to(kw["sink"][:, None], (Hq, off))[None],
+                               rtol=0, atol=1e-15)
 
 
 def test_bias_gradient_follows_bias_broadcast_shape():
