@@ -9,14 +9,13 @@ when the barrier's completed-phase count has the other parity, so it is only sou
 count is k or k + 1 when the waiter looks.  Random schedules must always finish, and no
 waiter may ever see a count outside {k, k + 1}.
 
-The negative control replays the earlier layout, in which the half-tile ring was read by
-two warps; the model must flag it (that layout timed out intermittently on the GPU).
-
-simulate_split_rings is the two-pass form's current protocol (two Q slots and one dO slot in
-the dK pass, double-buffered dS^T).  simulate and simulate_vtmem are the two layouts before it,
-kept as models of the same rules on different ring shapes.  simulate_fused is the one-pass
+simulate_split_rings is the two-pass form's protocol (two Q slots and one dO slot in the dK
+pass, double-buffered dS^T with one ready barrier per buffer).  Its negative control hands
+both dS^T buffers over through a single ready barrier: the softmax can then complete two
+phases ahead of the back MMA warp, which the model must flag.  simulate_fused is the one-pass
 form (head dims 64 and 128), with the front warp's MMAs completing asynchronously, so that it
-can also check that no stage is refilled while they still read it.
+can also check that no stage is refilled while they still read it; its negative control drops
+the s_full chain.
 """
 import random
 from collections import defaultdict
@@ -24,400 +23,7 @@ from collections import defaultdict
 import pytest
 
 
-def simulate(nper, design="single_reader", rng=None, order="q_do_qb", tiles=True):
-    """Returns (finished, hazards).  nper: query steps per pass (dV pass = dK pass).
-    order: the ring's fill order within a dK-pass step.  The kernel fills Q_i, dO_i, Q_{i-1}
-    and its front warp issues S^T_i, dP^T_i, dK_{i-1} ("q_do_qb"); "q_qb_do" is the earlier
-    single-reader layout (S^T_i, dK_{i-1}, dP^T_i).  tiles: the ring holds two whole tiles
-    (as in the kernel) rather than four half tiles."""
-    rng = rng or random.Random(0)
-    nsteps, nB = 2 * nper, nper
-    need = defaultdict(lambda: 1)
-    need.update({"v_full": 2, "fin_done": 2})
-    if design == "single_reader":
-        need["mma_done"] = 2
-    count, done, hazards = defaultdict(int), defaultdict(int), []
-
-    def arrive(b):
-        count[b] += 1
-        if count[b] == need[b]:
-            count[b] = 0
-            done[b] += 1
-
-    slot_of = lambda j: j & 1
-    use_of = lambda j: j >> 1
-    u_last0, u_last1 = ((nper + 1) >> 1) - 1, (nper >> 1) - 1
-    H = 1 if tiles else 2  # ring slots per tile
-    R = 2 * H               # ring depth in slots
-    pos_q = lambda i: H * (0 if i == 0 else 3 * i - 1)
-    if order == "q_qb_do":
-        pos_do = lambda i: H * (1 if i == 0 else 3 * i + 1)
-        pos_qb = lambda i: H * (3 * (i + 1) if i + 1 < nB else 3 * nB - 1)
-    else:  # "q_do_qb", as in bwd_tc.cu
-        pos_do = lambda i: H * (1 if i == 0 else 3 * i)
-        pos_qb = lambda i: H * (3 * i + 4 if i + 1 < nB else 3 * nB - 1)
-
-    def loader0():
-        yield ("arrive", "kv_full")
-        n = 0
-
-        def ring_load():
-            nonlocal n
-            r, u = n % R, n // R
-            if u == 0:
-                if r < H:
-                    yield ("wait", "qdo_empty0", u_last0)
-                elif design == "single_reader":
-                    yield ("wait", "do0_free", 0)
-                else:
-                    yield ("wait", "do_empty0", u_last0)
-            else:
-                yield ("wait", f"ring_empty{r}", u - 1)
-            yield ("arrive", f"ring_full{r}")
-            n += 1
-
-        for j in range(nsteps + 1):
-            if j < nsteps:
-                if j >= 2:
-                    yield ("wait", f"ld_empty{j & 1}", (j >> 1) - 1)
-                yield ("arrive", f"ld_full{j & 1}")
-            if j < nper:
-                s, u = slot_of(j), use_of(j)
-                if u >= 1:
-                    yield ("wait", f"qdo_empty{s}", u - 1)
-                yield ("arrive", f"qdo_full{s}")
-            elif j < nsteps:
-                if j == nper:
-                    if u_last1 >= 0:
-                        yield ("wait", "qdo_empty1", u_last1)
-                    yield ("arrive", "v_full")
-                for _ in range(H):  # Q_i
-                    yield from ring_load()
-                if order == "q_qb_do" and j > nper:  # Q_{i-1} again
-                    for _ in range(H):
-                        yield from ring_load()
-                for _ in range(H):  # dO_i
-                    yield from ring_load()
-                if order == "q_do_qb" and j > nper:
-                    for _ in range(H):
-                        yield from ring_load()
-            if j == nsteps and j > nper:
-                for _ in range(H):
-                    yield from ring_load()
-
-    def loader1():
-        for j in range(nper):
-            s, u = slot_of(j), use_of(j)
-            if u >= 1:
-                yield ("wait", f"do_empty{s}", u - 1)
-            yield ("arrive", f"do_full{s}")
-        if nper > 0:
-            if u_last1 >= 0:
-                yield ("wait", "do_empty1", u_last1)
-            yield ("arrive", "v_full")
-            if design == "single_reader":
-                yield ("wait", "do_empty0", u_last0)
-                yield ("arrive", "do0_free")
-
-    def ring(n0):
-        for hf in range(H):
-            n = n0 + hf
-            yield ("wait", f"ring_full{n % R}", n // R)
-            yield ("arrive", f"ring_empty{n % R}")
-
-    def dk(i):  # dK of dK-pass step i (the front warp in the single-reader design)
-        yield ("wait", "p_ready", nper + i)
-        if i == 0:
-            yield ("wait", "acc_free", 0)
-        yield from ring(pos_qb(i))
-        yield ("arrive", "mma_done")
-
-    def front():
-        yield ("wait", "kv_full", 0)
-        for j in range(nsteps):
-            if j >= 1:
-                yield ("wait", "sdp_free", j - 1)
-            if j < nper:
-                s = slot_of(j)
-                yield ("wait", f"qdo_full{s}", use_of(j))
-                yield ("arrive", "s_full")
-                yield ("arrive", f"qdo_empty{s}")
-                continue
-            i = j - nper
-            yield from ring(pos_q(i))
-            yield ("arrive", "s_full")
-            if design == "single_reader" and order == "q_qb_do" and i >= 1:
-                yield from dk(i - 1)
-            if i == 0:
-                yield ("wait", "v_full", 0)
-            else:
-                yield ("wait", "dp_free", i - 1)
-            yield from ring(pos_do(i))
-            yield ("arrive", "dp_full")
-            if design == "single_reader" and order == "q_do_qb" and i >= 1:
-                yield from dk(i - 1)
-        if design == "single_reader" and nsteps > 0:
-            yield from dk(nB - 1)
-        yield ("arrive", "fin_done")
-
-    def back():
-        yield ("wait", "kv_full", 0)
-        dq = 0
-        for j in range(1, nsteps + 1):
-            yield ("wait", "p_ready", j - 1)
-            jj = j - 1
-            if jj < nper:
-                s = slot_of(jj)
-                yield ("wait", f"do_full{s}", use_of(jj))
-                yield ("arrive", f"do_empty{s}")
-                yield ("arrive", "mma_done")
-                if design == "single_reader":
-                    yield ("arrive", "mma_done")
-                continue
-            if design == "shared_ring":  # the earlier layout: dK read the ring from this warp
-                if jj == nper:
-                    yield ("wait", "acc_free", 0)
-                yield from ring(pos_qb(jj - nper))
-            for m in range(2):
-                if dq >= 1:
-                    yield ("wait", f"dq_empty{m}", dq - 1)
-            yield ("arrive", "dq_full")
-            dq += 1
-            yield ("arrive", "mma_done")
-        yield ("arrive", "fin_done")
-
-    def softmax():
-        for j in range(nsteps):
-            yield ("wait", "s_full", j)
-            yield ("wait", f"ld_full{j & 1}", j >> 1)
-            yield ("arrive", "sdp_free")
-            if j >= nper:
-                yield ("wait", "dp_full", j - nper)
-                yield ("arrive", "dp_free")
-            yield ("arrive", f"ld_empty{j & 1}")
-            if j >= 1:
-                yield ("wait", "mma_done", j - 1)
-            yield ("arrive", "p_ready")
-            if j == nper - 1:
-                yield ("wait", "mma_done", j)
-                yield ("arrive", "acc_free")
-        if nsteps > 0:
-            yield ("wait", "fin_done", 0)
-
-    def drain():
-        for d in range(nB):
-            yield ("wait", "dq_full", d)
-            yield ("arrive", "dq_empty0")
-            yield ("arrive", "dq_empty1")
-
-    agents = {"loader0": loader0(), "loader1": loader1(), "front": front(), "back": back(),
-              "softmax": softmax(), "drain": drain()}
-    pending = dict.fromkeys(agents)
-    finished = set()
-    while len(finished) < len(agents):
-        progress = False
-        turn = list(agents)
-        rng.shuffle(turn)
-        for name in turn:
-            if name in finished:
-                continue
-            for _ in range(rng.randint(1, 8)):
-                op = pending[name]
-                if op is None:
-                    try:
-                        op = pending[name] = next(agents[name])
-                    except StopIteration:
-                        finished.add(name)
-                        progress = True
-                        break
-                if op[0] == "arrive":
-                    arrive(op[1])
-                    pending[name] = None
-                    progress = True
-                    continue
-                _, bar, phase = op
-                if done[bar] not in (phase, phase + 1):
-                    hazards.append((name, bar, phase, done[bar]))
-                if (done[bar] & 1) != (phase & 1):  # the hardware's parity test
-                    pending[name] = None
-                    progress = True
-                else:
-                    break
-        if not progress:
-            return False, hazards
-    return True, hazards
-
-
 STEP_COUNTS = [1, 2, 3, 4, 5, 6, 8, 13, 33, 66, 80]
-
-
-@pytest.mark.parametrize("order,tiles", [("q_do_qb", True), ("q_do_qb", False), ("q_qb_do", False)])
-def test_single_reader_protocol_never_deadlocks_or_aliases(order, tiles):
-    rng = random.Random(1234)
-    for trial in range(1000):
-        nper = STEP_COUNTS[trial % len(STEP_COUNTS)]
-        finished, hazards = simulate(nper, "single_reader", rng, order=order, tiles=tiles)
-        assert finished and not hazards, (nper, hazards[:3])
-
-
-def test_model_flags_the_shared_ring_layout():
-    """Negative control: with the ring (filled Q_i, dO_i, Q_{i-1}) read by two warps, the
-    dK warp can wait for a slot's next fill while the previous one is still in flight."""
-    rng = random.Random(99)
-    flagged = 0
-    for trial in range(400):
-        finished, hazards = simulate(66, "shared_ring", rng, order="q_do_qb", tiles=False)
-        flagged += (not finished) or bool(hazards)
-    assert flagged > 0
-
-
-@pytest.mark.parametrize("nper", [1, 2, 7, 66])
-def test_greedy_schedule_finishes(nper):
-    finished, hazards = simulate(nper, "single_reader", random.Random(nper))
-    assert finished and not hazards
-
-
-def simulate_vtmem(nper, rng):
-    """The head-dim-256 protocol with V in tensor memory during the dK pass: a four-slot ring
-    of whole Q / dO tiles (Q_i stays resident from S^T_i to dK_i), S^T and dP^T sharing one
-    score buffer, dQ^T drained one 128-row half at a time.  Returns (finished, hazards)."""
-    nsteps, nB = 2 * nper, nper
-    need = defaultdict(lambda: 1)
-    need.update({"mma_done": 2, "fin_done": 2, "sdp_free": 1, "p_ready": 1, "acc_free": 1, "v_full": 1})
-    count, done, hazards = defaultdict(int), defaultdict(int), []
-
-    def arrive(b):
-        count[b] += 1
-        if count[b] == need[b]:
-            count[b] = 0
-            done[b] += 1
-
-    u_last0, u_last1 = ((nper + 1) >> 1) - 1, (nper >> 1) - 1
-
-    def loader0():
-        yield ("arrive", "kv_full")
-        n = 0
-        for j in range(nsteps):
-            if j >= 2:
-                yield ("wait", f"ld_empty{j & 1}", (j >> 1) - 1)
-            yield ("arrive", f"ld_full{j & 1}")
-            if j < nper:
-                s, u = j & 1, j >> 1
-                if u >= 1:
-                    yield ("wait", f"qdo_empty{s}", u - 1)
-                yield ("arrive", f"qdo_full{s}")
-                continue
-            for _ in range(2):  # Q_i, dO_i
-                r, u = n % 4, n // 4
-                if u == 0:
-                    if r == 0:
-                        yield ("wait", "qdo_empty0", u_last0)
-                    elif r == 1:
-                        yield ("wait", "do0_free", 0)
-                    elif r == 2:
-                        if u_last1 >= 0:
-                            yield ("wait", "qdo_empty1", u_last1)
-                    else:
-                        yield ("wait", "do1_free", 0)
-                else:
-                    yield ("wait", f"ring_empty{r}", u - 1)
-                yield ("arrive", f"ring_full{r}")
-                n += 1
-
-    def loader1():
-        for j in range(nper):
-            s, u = j & 1, j >> 1
-            if u >= 1:
-                yield ("wait", f"do_empty{s}", u - 1)
-            yield ("arrive", f"do_full{s}")
-        if nper > 0:
-            yield ("wait", "do_empty0", u_last0)
-            yield ("arrive", "do0_free")
-            if u_last1 >= 0:
-                yield ("wait", "do_empty1", u_last1)
-            yield ("arrive", "do1_free")
-
-    def front():
-        yield ("wait", "kv_full", 0)
-        for j in range(nper):
-            if j >= 1:
-                yield ("wait", "sdp_free", j - 1)
-            yield ("wait", f"qdo_full{j & 1}", j >> 1)
-            yield ("arrive", "s_full")
-            yield ("arrive", f"qdo_empty{j & 1}")
-
-        def dk(i):
-            yield ("wait", "p_ready", nper + i)
-            yield ("arrive", f"ring_empty{(2 * i) % 4}")
-            yield ("arrive", "mma_done")
-
-        for i in range(nB):
-            j = nper + i
-            if i == 0:
-                yield ("wait", "sdp_free", nper - 1)
-                yield ("wait", "acc_free", 0)
-            else:
-                yield ("wait", "dp_free", i - 1)
-            yield ("wait", f"ring_full{(2 * i) % 4}", (2 * i) // 4)
-            yield ("arrive", "s_full")
-            if i >= 1:  # dK of the previous step as soon as its dS is in: frees its Q slot
-                yield from dk(i - 1)
-            yield ("wait", "sdp_free", j)
-            if i == 0:
-                yield ("wait", "v_full", 0)
-            yield ("wait", f"ring_full{(2 * i + 1) % 4}", (2 * i + 1) // 4)
-            yield ("arrive", f"ring_empty{(2 * i + 1) % 4}")
-            yield ("arrive", "dp_full")
-        if nB > 0:
-            yield from dk(nB - 1)
-        yield ("arrive", "fin_done")
-
-    def back():
-        yield ("wait", "kv_full", 0)
-        h = 0
-        for j in range(1, nsteps + 1):
-            yield ("wait", "p_ready", j - 1)
-            jj = j - 1
-            if jj < nper:
-                yield ("wait", f"do_full{jj & 1}", jj >> 1)
-                yield ("arrive", f"do_empty{jj & 1}")
-                yield ("arrive", "mma_done")
-                yield ("arrive", "mma_done")
-                continue
-            for _ in range(2):
-                if h >= 1:
-                    yield ("wait", "dq_empty", h - 1)
-                yield ("arrive", "dq_full")
-                h += 1
-            yield ("arrive", "mma_done")
-        yield ("arrive", "fin_done")
-
-    def softmax():
-        for j in range(nsteps):
-            yield ("wait", "s_full", j)
-            yield ("wait", f"ld_full{j & 1}", j >> 1)
-            yield ("arrive", "sdp_free")
-            if j >= nper:
-                yield ("wait", "dp_full", j - nper)
-                yield ("arrive", "dp_free")
-            yield ("arrive", f"ld_empty{j & 1}")
-            if j >= 1:
-                yield ("wait", "mma_done", j - 1)
-            yield ("arrive", "p_ready")
-            if j == nper - 1:
-                yield ("wait", "mma_done", j)
-                yield ("arrive", "acc_free")
-                yield ("arrive", "v_full")
-        if nsteps > 0:
-            yield ("wait", "fin_done", 0)
-
-    def drain():
-        for h in range(2 * nB):
-            yield ("wait", "dq_full", h)
-            yield ("arrive", "dq_empty")
-
-    return run_agents({"loader0": loader0(), "loader1": loader1(), "front": front(), "back": back(),
-                       "softmax": softmax(), "drain": drain()}, arrive, done, hazards, rng)
 
 
 def run_agents(agents, arrive, done, hazards, rng):
@@ -457,18 +63,16 @@ def run_agents(agents, arrive, done, hazards, rng):
     return True, hazards
 
 
-def test_vtmem_protocol_never_deadlocks_or_aliases():
-    rng = random.Random(4321)
-    for trial in range(1500):
-        nper = STEP_COUNTS[trial % len(STEP_COUNTS)]
-        finished, hazards = simulate_vtmem(nper, rng)
-        assert finished and not hazards, (nper, hazards[:3])
-
-
-def simulate_split_rings(nper, rng):
-    """As simulate_vtmem, with the dK pass's tiles in two rings (two Q slots, one dO slot) and
-    dS double-buffered: each dS buffer has its own MMA-completion barrier (dK + dQ of the step
-    that read it), so the softmax never waits on the step it has just handed over."""
+def simulate_split_rings(nper, rng, single_ready=False):
+    """The head-dim-256 protocol: K resident; dV pass over two Q / dO stages; then V in tensor
+    memory, the dK pass's tiles in two rings (two Q slots, one dO slot), S^T and dP^T sharing
+    one score buffer, dQ^T drained one 128-row half at a time, and dS double-buffered: each dS
+    buffer has its own ready barrier and its own MMA-completion barrier (dK + dQ of the step
+    that read it), so the softmax never waits on the step it has just handed over.
+    single_ready: the dK pass's dS buffers share one ready barrier (negative control).
+    Returns (finished, hazards)."""
+    prb = (lambda i: "p_ready") if single_ready else (lambda i: f"prb{i & 1}")
+    prb_phase = (lambda i: nper + i) if single_ready else (lambda i: i >> 1)
     nsteps, nB = 2 * nper, nper
     need = defaultdict(lambda: 1)
     need.update({"mma_done": 2, "mdb0": 2, "mdb1": 2, "fin_done": 2})  # p_ready etc.: one arrival (the model's softmax is one agent)
@@ -529,7 +133,7 @@ def simulate_split_rings(nper, rng):
             yield ("arrive", f"qdo_empty{j & 1}")
 
         def dk(i):
-            yield ("wait", f"prb{i & 1}", i >> 1)
+            yield ("wait", prb(i), prb_phase(i))
             yield ("arrive", f"ring_empty{i & 1}")
             yield ("arrive", f"mdb{i & 1}")
 
@@ -566,7 +170,7 @@ def simulate_split_rings(nper, rng):
                 yield ("arrive", "mma_done")
                 yield ("arrive", "mma_done")
                 continue
-            yield ("wait", f"prb{(jj - nper) & 1}", (jj - nper) >> 1)
+            yield ("wait", prb(jj - nper), prb_phase(jj - nper))
             for _ in range(2):
                 if h >= 1:
                     yield ("wait", "dq_empty", h - 1)
@@ -593,7 +197,7 @@ def simulate_split_rings(nper, rng):
                     yield ("wait", f"mdb{i & 1}", (i >> 1) - 1)
             # dV pass: one p_ready; dK pass: one per dS buffer, so that its phases are two
             # steps apart and the MMA warps cannot be overtaken twice
-            yield ("arrive", "p_ready" if j < nper else f"prb{(j - nper) & 1}")
+            yield ("arrive", "p_ready" if j < nper else prb(j - nper))
             if j == nper - 1:
                 yield ("wait", "mma_done", j)
                 yield ("arrive", "acc_free")
@@ -616,6 +220,18 @@ def test_split_rings_protocol_never_deadlocks_or_aliases():
         nper = STEP_COUNTS[trial % len(STEP_COUNTS)]
         finished, hazards = simulate_split_rings(nper, rng)
         assert finished and not hazards, (nper, hazards[:3])
+
+
+def test_split_rings_model_flags_a_single_ready_barrier():
+    """Negative control: with one ready barrier for both dS^T buffers, the softmax can arrive
+    for two dK-pass steps before the back warp looks for the first, a phase the parity wait
+    cannot tell from the one two later."""
+    rng = random.Random(99)
+    flagged = 0
+    for trial in range(400):
+        finished, hazards = simulate_split_rings(13, rng, single_ready=True)
+        flagged += (not finished) or bool(hazards)
+    assert flagged > 0
 
 
 def simulate_fused(nsteps, rng, ns=3, skip_chain=False):
