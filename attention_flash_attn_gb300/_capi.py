@@ -29,7 +29,8 @@ ATTN_ERR_DEVICE = 5
 EXPORTS = (
     "attn_fwd_workspace_size", "attn_fwd", "attn_bwd_workspace_size", "attn_bwd",
     "attn_check_device_status", "attn_status_string", "attn_path_name", "attn_launch_counter",
-    "attn_profile_next_main_kernel", "attn_fwd_noalloc",
+    "attn_profile_next_main_kernel", "attn_fwd_noalloc", "attn_noalloc_check_device_status",
+    "attn_selftest_wait_expiry",
 )
 
 
@@ -78,6 +79,10 @@ def lib():
         L.attn_fwd.restype = ctypes.c_int
         L.attn_fwd_noalloc.argtypes = [A, vp, vp, vp]
         L.attn_fwd_noalloc.restype = ctypes.c_int
+        L.attn_noalloc_check_device_status.argtypes = [vp]
+        L.attn_noalloc_check_device_status.restype = ctypes.c_int
+        L.attn_selftest_wait_expiry.argtypes = [vp, sz, ctypes.c_uint64, vp]
+        L.attn_selftest_wait_expiry.restype = ctypes.c_int
         L.attn_bwd.argtypes = [A, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.attn_bwd.restype = ctypes.c_int
         L.attn_check_device_status.argtypes = [vp, vp]

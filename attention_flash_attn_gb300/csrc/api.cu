@@ -182,6 +182,19 @@ int run_meta(const attn_args *a, Params &p, cudaStream_t st) {
 }
 
 }  // namespace
+
+int fwd_precheck(const attn_args *a, const void *O, const float *LSE, bool *empty) {
+  *empty = false;
+  const int s = validate(a);
+  if (s != ATTN_OK) return s;
+  if (a->B == 0 || a->Sq == 0) {
+    *empty = true;
+    return ATTN_OK;
+  }
+  if (!O || !LSE || !aligned16(O)) return ATTN_ERR_INVALID;
+  return ATTN_OK;
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -204,10 +217,9 @@ const char *attn_path_name(const attn_args *a) {
 }
 
 int attn_fwd(const attn_args *a, void *O, float *LSE, void *ws, size_t ws_bytes, attn_stream_t stream) {
-  int s = validate(a);
-  if (s != ATTN_OK) return s;
-  if (a->B == 0 || a->Sq == 0) return ATTN_OK;
-  if (!O || !LSE || !aligned16(O)) return ATTN_ERR_INVALID;
+  bool empty = false;
+  int s = fwd_precheck(a, O, LSE, &empty);
+  if (s != ATTN_OK || empty) return s;
   const Layout L = layout(a, false);
   if (!ws || ws_bytes < L.total || ((uintptr_t)ws % kAlign) != 0) return ATTN_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -5,7 +5,14 @@
 
 #include <atomic>
 
+#include "../../include/attn_gb300.h"
+
 namespace attn {
+
+// attn_fwd's checks that come before any workspace is looked at: argument validation, then
+// (when there is something to compute) the outputs.  Returns an attn_status; *empty is set
+// when B == 0 or Sq == 0 (nothing to compute, ATTN_OK).
+int fwd_precheck(const attn_args *a, const void *O, const float *LSE, bool *empty);
 
 struct Params;
 

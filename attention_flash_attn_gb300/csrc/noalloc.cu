@@ -7,49 +7,49 @@
 // inputs and outputs as usual; the scratch the forward needs (the device status word and,
 // for packed segments, the segment metadata) comes from g_fwd_scratch below.
 //
-// The array exists once per GPU that loads the library and stays resident until the process
-// exits.  In host code its name is only a host-side stand-in: the device address is looked
-// up with cudaGetSymbolAddress, once per device, with that device current.
+// The array exists once per GPU context that loads the library and stays resident until the
+// process exits.  In host code its name is only a host-side stand-in: the device address is
+// looked up with cudaGetSymbolAddress on every call, in the context that is current then --
+// a plugin may run in a context of its own, and a context that was destroyed and created
+// again holds the array at a new address -- so no address is ever reused across contexts.
+// After the first call in a context the lookup is a table read.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
-#include "../../include/attn_gb300.h"
+#include "internal.h"
 
 namespace {
 
 constexpr size_t kScratchBytes = size_t(4) << 20;  // 4 MiB
 __device__ __align__(256) unsigned char g_fwd_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 128;
-std::mutex g_mu;
-void *g_dev_ptr[kMaxDevices];
-
-// Device address of g_fwd_scratch on the current device (looked up once per device).
-int scratch_for_current_device(void **out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_dev_ptr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_fwd_scratch) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
-    g_dev_ptr[dev] = p;
-  }
-  *out = g_dev_ptr[dev];
+// Device address of g_fwd_scratch in the current context.
+int scratch_in_current_context(void **out) {
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fwd_scratch) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
+  *out = p;
   return ATTN_OK;
 }
 
 }  // namespace
 
 extern "C" int attn_fwd_noalloc(const attn_args *a, void *O, float *LSE, attn_stream_t stream) {
-  const size_t need = attn_fwd_workspace_size(a);
-  if (need == 0) return attn_fwd(a, O, LSE, nullptr, 0, stream);  // reports the validation error
-  if (need > kScratchBytes) return ATTN_ERR_WORKSPACE;
+  // attn_fwd's own checks first, in its order, so that both entry points answer a request
+  // alike; only then the array's size limit.
+  bool empty = false;
+  int s = attn::fwd_precheck(a, O, LSE, &empty);
+  if (s != ATTN_OK || empty) return s;
+  if (attn_fwd_workspace_size(a) > kScratchBytes) return ATTN_ERR_WORKSPACE;
   void *ws = nullptr;
-  int s = scratch_for_current_device(&ws);
-  if (s != ATTN_OK) return s;
-  // The array keeps the previous call's contents; the status word must start at zero.
+  if ((s = scratch_in_current_context(&ws)) != ATTN_OK) return s;
+  // The array keeps the previous call's contents; the status area must start at zero.
   // The segment metadata is rewritten in full by every call that uses it.
   if (cudaMemsetAsync(ws, 0, 256, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
   return attn_fwd(a, O, LSE, ws, kScratchBytes, stream);
+}
+
+extern "C" int attn_noalloc_check_device_status(attn_stream_t stream) {
+  void *ws = nullptr;
+  const int s = scratch_in_current_context(&ws);
+  if (s != ATTN_OK) return s;
+  return attn_check_device_status(ws, stream);
 }

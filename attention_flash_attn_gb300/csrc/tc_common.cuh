@@ -92,7 +92,9 @@ __device__ __forceinline__ void record_abort(unsigned *status, uint32_t bar, uin
   }
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *status) {
+// limit_ns: the kernels pass kWaitLimitNs; the self-test of this path passes a short limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -102,7 +104,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
         record_abort(status, bar, parity);
         return false;
       }
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         record_timeout(status, bar, parity);
         return false;
       }

@@ -164,19 +164,31 @@ int attn_fwd(const attn_args *a, void *O, float *LSE, void *ws, size_t ws_bytes,
  * allocator, or deployments whose device-memory budget is fixed up front.  The pages this
  * library follows have no counterpart to this entry point.
  *
- * Computes exactly what attn_fwd computes (same arguments, same outputs, same errors), with
- * its scratch taken from a 4 MiB array compiled into the library (one per GPU that loads the
- * library, resident until the process exits).  Calls whose attn_fwd_workspace_size exceeds
- * 4 MiB are rejected with ATTN_ERR_WORKSPACE before anything is launched.  It allocates
- * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * Computes exactly what attn_fwd computes (same arguments, same outputs), with its scratch
+ * taken from a 4 MiB array compiled into the library (one per GPU context that loads the
+ * library, resident until the process exits).  It makes attn_fwd's checks in attn_fwd's
+ * order and answers them alike (B == 0 or Sq == 0: ATTN_OK, nothing launched); a request that
+ * passes them but whose attn_fwd_workspace_size exceeds 4 MiB is then rejected with
+ * ATTN_ERR_WORKSPACE before anything is launched.  It allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
  *
- * The first call on a device looks up the array's device address (with that device
- * current); make that first call before any stream capture.  Every call shares the array:
- * calls whose work overlaps on the GPU (other streams, other threads) race and must not be
- * issued.  Each call clears the status word at its start, so device-side errors cannot be
- * read back through attn_check_device_status for this entry point.
+ * Every call looks up the array's device address in the context that is current (the first
+ * call in a context loads the library's device code there); make the first call on a device
+ * before any stream capture.  Every call shares the array: calls whose work overlaps on the
+ * GPU (other streams, other threads) race and must not be issued.  Each call clears the
+ * array's status word at its start; attn_noalloc_check_device_status reads what the most
+ * recent call recorded there.
  */
 int attn_fwd_noalloc(const attn_args *a, void *O, float *LSE, attn_stream_t stream);
+
+/*
+ * attn_check_device_status for attn_fwd_noalloc: synchronises `stream`, reads and clears the
+ * status word of the built-in array in the current context.  Returns ATTN_OK, ATTN_ERR_DEVICE
+ * (the most recent attn_fwd_noalloc call on this device recorded a device-side error: an
+ * expired bounded wait, or a malformed cu_seqlens / cu_seqlens_k) or ATTN_ERR_CUDA.  Like the
+ * entry point itself, it allocates nothing and has no counterpart on the pages.
+ */
+int attn_noalloc_check_device_status(attn_stream_t stream);
 
 /* Bytes of workspace attn_bwd needs (same rules as attn_fwd_workspace_size). */
 size_t attn_bwd_workspace_size(const attn_args *a);
@@ -203,6 +215,21 @@ int attn_bwd(const attn_args *a, const void *O, const float *LSE, const void *dO
  * ATTN_ERR_CUDA (the stream itself reported an error).
  */
 int attn_check_device_status(void *ws, attn_stream_t stream);
+
+/*
+ * Self-test of the bounded-wait failure path (TransformerEngine PR #3391, "What changed":
+ * fail closed, never return a silently wrong result).  Launches one small kernel on `stream`
+ * whose first wait is on an mbarrier that nothing completes, with limit_ns as its time limit
+ * (1 us .. 2 s); the kernels' own waits behind it give up on the status bit.  Afterwards the
+ * workspace holds exactly what a real expired wait leaves: attn_check_device_status(ws)
+ * returns ATTN_ERR_DEVICE; status words 1..6 hold 1, the barrier's shared-memory address and
+ * parity (0), the CTA (0) and the thread (0) of the first wait to give up; words 10 and 11 the
+ * barrier and parity | 0x100 of warp 1 of that CTA; words 48 and 49 the addresses of the two
+ * barriers, for comparison.  Until that status is read and cleared, attn_fwd / attn_bwd with
+ * this workspace return from their kernels at once.  ws: at least 256 bytes, 256-byte
+ * aligned, zero-filled.  Nothing faults or traps; the context stays usable.
+ */
+int attn_selftest_wait_expiry(void *ws, size_t ws_bytes, uint64_t limit_ns, attn_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char *attn_status_string(int status);

@@ -111,3 +111,13 @@ def compare_full(w: Workload, gpu: dict, ref: dict) -> dict:
     assert np.array_equal(np.isfinite(lse_g), fin), "LSE -inf pattern differs"
     errs["LSE"] = frob_rel(lse_g[fin], ref["LSE"][fin]) if fin.any() else 0.0
     return errs
+
+
+def check_against_oracle_small(w: Workload, **extra):
+    """Run a small workload through the binding and assert every output is within the
+    dtype's tolerance of the fp64 oracle; returns the errors."""
+    inp = make_inputs(w)
+    errs = compare_full(w, run_gpu(w, inp, **extra), full_oracle(w, inp))
+    bad = {k: v for k, v in errs.items() if not v <= TOL[w.dtype]}
+    assert not bad, (w.name, errs)
+    return errs

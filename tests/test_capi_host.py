@@ -183,3 +183,38 @@ def test_status_strings(capi):
     L = capi.lib()
     for s in range(7):
         assert L.attn_status_string(s)
+
+
+def test_noalloc_answers_like_attn_fwd_before_its_size_limit(capi):
+    """attn_fwd_noalloc makes attn_fwd's checks first, in attn_fwd's order: invalid arguments
+    and missing or misaligned outputs are ATTN_ERR_INVALID even when the request would also
+    exceed its 4 MiB array, and a problem without query rows is ATTN_OK whatever its key axis
+    would need.  None of these reaches a CUDA call."""
+    L = capi.lib()
+    S = 1 << 20  # per-token key metadata alone needs more than 4 MiB
+    a = valid_args(capi, S=S, H=1, cu_seqlens=0x21000, cu_seqlens_k=0x22000, nseq=1)
+    assert L.attn_fwd_workspace_size(ctypes.byref(a)) > (4 << 20)
+    n = L.attn_launch_counter()
+    assert L.attn_fwd_noalloc(ctypes.byref(a), None, 0x40000, None) == 1
+    assert L.attn_fwd_noalloc(ctypes.byref(a), 0x30000, None, None) == 1
+    assert L.attn_fwd_noalloc(ctypes.byref(a), 0x30008, 0x40000, None) == 1
+    bad = valid_args(capi, S=S, H=1, cu_seqlens=0x21000, cu_seqlens_k=0x22000, nseq=1, softcap=-1.0)
+    assert L.attn_fwd_noalloc(ctypes.byref(bad), 0x30000, 0x40000, None) == 1
+    a.Sq = 0
+    assert L.attn_fwd(ctypes.byref(a), None, None, None, 0, None) == 0
+    assert L.attn_fwd_noalloc(ctypes.byref(a), None, None, None) == 0
+    b0 = valid_args(capi, B=0)
+    assert L.attn_fwd_noalloc(ctypes.byref(b0), None, None, None) == 0
+    assert L.attn_launch_counter() == n
+
+
+def test_selftest_wait_expiry_rejects_bad_arguments(capi):
+    """The failure-path self-test checks its workspace and its limit before launching."""
+    L = capi.lib()
+    n = L.attn_launch_counter()
+    assert L.attn_selftest_wait_expiry(None, 256, 10 ** 6, None) == 3
+    assert L.attn_selftest_wait_expiry(0x50000, 255, 10 ** 6, None) == 3
+    assert L.attn_selftest_wait_expiry(0x50010, 256, 10 ** 6, None) == 3
+    assert L.attn_selftest_wait_expiry(0x50000, 256, 999, None) == 1
+    assert L.attn_selftest_wait_expiry(0x50000, 256, 2 * 10 ** 9 + 1, None) == 1
+    assert L.attn_launch_counter() == n

@@ -76,3 +76,29 @@ def test_noalloc_rejects_requests_beyond_its_array():
     n = L.attn_launch_counter()
     assert L.attn_fwd_noalloc(ctypes.byref(a), 0x30000, 0x40000, None) == _capi.ATTN_ERR_WORKSPACE
     assert L.attn_launch_counter() == n
+
+
+def test_noalloc_device_errors_can_be_read_back():
+    """attn_noalloc_check_device_status reads the status word of the built-in array: a
+    cu_seqlens whose values all lie in [0, Sq] but out of order (every access stays inside
+    its array) is reported as a device-side error of that call; the next well-formed call
+    reports nothing and matches attn_fwd."""
+    import attention_flash_attn_gb300 as fa
+    from attention_flash_attn_gb300 import _capi
+    L = fa.lib()
+    w = Workload("noalloc_bad_cu", "bf16", B=1, Sq=515, Sk=515, Hq=2, Hkv=1, D=64, causal=True, softcap=20.0)
+    inp = make_inputs(w)
+    t = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    st = torch.cuda.current_stream().cuda_stream
+    bad = torch.tensor([0, 300, 100, 515], dtype=torch.int32, device="cuda")
+    good = torch.tensor([0, 100, 300, 515], dtype=torch.int32, device="cuda")
+    status, _, _ = _noalloc_fwd(fa, t, w, cu_seqlens=bad)
+    assert status == 0
+    assert L.attn_noalloc_check_device_status(st) == _capi.ATTN_ERR_DEVICE
+    assert L.attn_noalloc_check_device_status(st) == 0
+    status, O, LSE = _noalloc_fwd(fa, t, w, cu_seqlens=good)
+    assert status == 0
+    assert L.attn_noalloc_check_device_status(st) == 0
+    ref_O, ref_LSE = fa.attn_fwd(t["q"], t["k"], t["v"], causal=True, softcap=20.0, scale=w.scale,
+                                 cu_seqlens=good)
+    assert frob_rel(to64(O), to64(ref_O)) <= TOL[w.dtype]
