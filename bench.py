@@ -209,39 +209,59 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
 
-    # Timed region: K steps, L2 flushed (untimed) before each.
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    for e in [x for pair in ev for x in pair] + [x for four in kev for x in four]:
-        e.record(stream)  # torch creates the CUDA event lazily, on first record
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    launches0 = fa.attn_launch_counter()
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
-    t_wall0 = time.time()
-    for s in range(args.steps):
-        flush.zero_()
-        ev[s][0].record(stream)
-        fa.attn_profile_next_main_kernel(kev[s][0], kev[s][1])
-        O, LSE = fa.attn_fwd(t["q"], t["k"], t["v"], **kw)
-        fa.attn_profile_next_main_kernel(kev[s][2], kev[s][3])
-        fa.attn_bwd(t["q"], t["k"], t["v"], O, LSE, t["dO"], **kw)
-        ev[s][1].record(stream)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
-    launches = fa.attn_launch_counter() - launches0
-    clocks.mark(t_wall0, time.time())
-    clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    fwd_ms = [a.elapsed_time(b) for a, b, _, _ in kev]
-    bwd_ms = [c.elapsed_time(d) for _, _, c, d in kev]
-    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    def timed(kw_run, nsteps, clocks=None):
+        """nsteps timed steps (L2 flushed, untimed, before each).  Per step: the whole step, the
+        forward and backward phases (every kernel of attn_fwd, of attn_bwd), and the two main
+        kernels alone (events recorded by the library around them, on the same stream)."""
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(nsteps)]
+        for e in [x for seven in ev for x in seven]:
+            e.record(stream)  # torch creates the CUDA event lazily, on first record
+        if clocks is not None:
+            clocks.start()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        n0 = fa.attn_launch_counter()
+        t_wall0 = time.time()
+        for s in range(nsteps):
+            e = ev[s]
+            flush.zero_()
+            e[0].record(stream)
+            fa.attn_profile_next_main_kernel(e[3], e[4])
+            O, LSE = fa.attn_fwd(t["q"], t["k"], t["v"], **kw_run)
+            e[1].record(stream)
+            fa.attn_profile_next_main_kernel(e[5], e[6])
+            fa.attn_bwd(t["q"], t["k"], t["v"], O, LSE, t["dO"], **kw_run)
+            e[2].record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        n = fa.attn_launch_counter() - n0
+        clk = None
+        if clocks is not None:
+            clocks.mark(t_wall0, time.time())
+            clk = clocks.stop()
+        el = lambda i, j: [x[i].elapsed_time(x[j]) for x in ev]  # noqa: E731
+        return {"step": el(0, 2), "fwd": el(0, 1), "bwd": el(1, 2), "fwd_main": el(3, 4), "bwd_main": el(5, 6),
+                "launches": n, "clocks": clk}
+
+    # Timed region: K steps of the workload.
+    run = timed(kw, args.steps, ClockSampler(local_rank))
+    launches, clk = run["launches"], run["clocks"]
+    total_ms = max_over_ranks(sum(run["step"]), world, dev)
     status = fa.attn_check_device_status(dev)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
+    # The cap's cost: the same workload with softcap = 0, timed the same way right after.
+    twin = None
+    if w.softcap > 0 and not args.no_twin:
+        kw0 = dict(kw, softcap=0.0)
+        for _ in range(args.warmup):
+            O0, L0 = fa.attn_fwd(t["q"], t["k"], t["v"], **kw0)
+            fa.attn_bwd(t["q"], t["k"], t["v"], O0, L0, t["dO"], **kw0)
+        twin = timed(kw0, args.steps)
+        if fa.attn_check_device_status(dev) != 0:
+            raise RuntimeError("device status after the uncapped run")
 
     # End to end through the public API with host buffers: every step copies its inputs (q, k,
     # v, dO) in from pinned host memory and its results (O, dQ, dK, dV, dsink) out to pinned
@@ -309,14 +329,27 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(e2e_run(args.steps), world, dev)
 
     f_step = flops(w, seg, "fwdbwd", bounds)
+    f_fwd, f_bwd = flops(w, seg, "fwd", bounds), flops(w, seg, "bwd", bounds)
     value = whole_job_tflops(f_step, args.steps, world, total_ms)
     e2e_value = whole_job_tflops(f_step, args.steps, world, e2e_ms)
     burst, sustained, kind = peaks()
+    tf = lambda f, ms_list: f / (statistics.mean(ms_list) * 1e-3) / 1e12  # noqa: E731
     # Dominant kernel: the backward main kernel (10*D flops per visible pair).
-    bwd_kernel_ms = statistics.mean(bwd_ms)
-    fwd_kernel_ms = statistics.mean(fwd_ms)
-    bwd_tf = flops(w, seg, "bwd", bounds) / (bwd_kernel_ms * 1e-3) / 1e12
-    fwd_tf = flops(w, seg, "fwd", bounds) / (fwd_kernel_ms * 1e-3) / 1e12
+    bwd_tf = tf(f_bwd, run["bwd_main"])
+    fwd_tf = tf(f_fwd, run["fwd_main"])
+    phases = {}
+    for name, f, key in (("fwd", f_fwd, "fwd"), ("bwd", f_bwd, "bwd"), ("fwdbwd", f_step, "step")):
+        x = tf(f, run[key])
+        phases[name] = {"tflops": round(x, 3), "frac": round(x / burst, 4), "ms": round(statistics.mean(run[key]), 4)}
+    softcap_cost = None
+    if twin is not None:
+        cap_ms, unc_ms = statistics.mean(run["step"]), statistics.mean(twin["step"])
+        softcap_cost = {
+            "capped_ms": round(cap_ms, 4), "uncapped_ms": round(unc_ms, 4), "ratio": round(cap_ms / unc_ms, 4),
+            "fwd_ratio": round(statistics.mean(run["fwd"]) / statistics.mean(twin["fwd"]), 4),
+            "bwd_ratio": round(statistics.mean(run["bwd"]) / statistics.mean(twin["bwd"]), 4),
+            "uncapped_tflops": round(tf(f_step, twin["step"]), 3), "target": 1.1,
+            "note": "same workload and inputs with softcap = 0, timed right after, same steps"}
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -339,6 +372,10 @@ def run_ours(args, rank, world, local_rank):
         "pct_of_bf16_peak": round(100 * value / burst, 2),
         "fwd_tflops": round(fwd_tf, 3),
         "bwd_tflops": round(bwd_tf, 3),
+        "phases": dict(phases, note="fwd = every kernel of attn_fwd, bwd = every kernel of attn_bwd, "
+                                    "fwdbwd = the step; frac of the measured bf16 burst peak; "
+                                    "fwd_tflops / bwd_tflops above: the main kernels alone"),
+        "softcap_cost": softcap_cost,
         "roofline": {"bound": "tensor", "kernel": "backward main kernel",
                      "achieved": round(bwd_tf, 3), "peak": burst, "unit": "TFLOP/s",
                      "frac": round(bwd_tf / burst, 4), "peak_kind": f"{kind} bf16 burst",
@@ -456,11 +493,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-twin", action="store_true", help="skip the softcap = 0 timing of the same workload")
     ap.add_argument("--kv-splits", type=int, default=None,
                     help="split-KV forward shares per query tile (default: the workload's)")
     args = ap.parse_args()
