@@ -28,9 +28,7 @@ struct Layout {
   size_t total = 0;
 };
 
-bool use_tc(const attn_args *a) {
-  return a->dtype == ATTN_DTYPE_BF16 && a->bias == nullptr && a->Sk > 0 && tc_supported(a->D);
-}
+bool use_tc(const attn_args *a) { return a->dtype == ATTN_DTYPE_BF16 && a->Sk > 0 && tc_supported(a->D); }
 bool use_tc_bwd(const attn_args *a) { return use_tc(a) && tc_bwd_supported(a->D); }
 
 constexpr int kMaxKvSplits = 64;
@@ -133,6 +131,10 @@ Params make_params(const attn_args *a, char *ws, const Layout &L) {
   p.bias_sb = a->bias_stride_b; p.bias_sh = a->bias_stride_h;
   p.bias_B = a->bias_stride_b ? a->B : 1;
   p.bias_H = a->bias_stride_h ? a->Hq : 1;
+  {
+    const int64_t vec = a->dtype == ATTN_DTYPE_BF16 ? 8 : 4;  // elements per 16 bytes
+    p.bias_vec = a->bias && a->Sk % vec == 0 && a->bias_stride_b % vec == 0 && a->bias_stride_h % vec == 0;
+  }
   p.sink = a->sink;
   p.off_by_one = a->softmax_type == ATTN_SOFTMAX_OFF_BY_ONE ? 1 : 0;
   p.status = reinterpret_cast<unsigned *>(ws);

@@ -148,8 +148,12 @@ __device__ __forceinline__ uint4 pack8(const uint32_t *o, int v) {
 // 1 - tanh^2 = 4 r (1 - r) = 4 e r^2; the capped logit in log2 units is cap log2(e) (1 - 2 r).
 // The exponent is clamped at 126 (a huge e gives r ~ 0, tanh = 1, and e r^2 = 0 rather than
 // inf * 0); an underflowing e gives r = 1 (tanh = -1).
+// With a bias the logit is u = scale s + bias: the bias enters as its own term (bin: its
+// factor, 2 log2(e) / cap with the cap, log2(e) without), and the chain-rule factor is formed
+// without the softmax scale (f4 = 4, fone = 1), so that dU = P (dP - D) f -- the bias's own
+// gradient -- is at hand before the scale is applied for dS.
 struct BwdScore {
-  uint64_t cin, one, mcap2, cap2, fs, sc2, scale;
+  uint64_t cin, one, mcap2, cap2, fs, sc2, scale, bin, f4;
   __device__ BwdScore(float scale_, float inv_cap, float cap) {
     cin = f2_splat(2.f * kLog2e * scale_ * inv_cap);
     one = f2_splat(1.f);
@@ -158,25 +162,57 @@ struct BwdScore {
     fs = f2_splat(4.f * scale_);
     sc2 = f2_splat(scale_ * kLog2e);
     scale = f2_splat(scale_);
+    bin = f2_splat(cap > 0.f ? 2.f * kLog2e * inv_cap : kLog2e);
+    f4 = f2_splat(4.f);
   }
 };
+
+// The bias of one bf16 pair (low half first) as a pair of floats.
+__device__ __forceinline__ uint64_t bias_pair(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Bias of this thread's key for the 32 queries q0 .. q0 + 31 of a chunk, as 16 bf16 pairs
+// (query q0 + 2 e in the low half of pair e).  `col` points at the key's column of the head's
+// [Sq, Sk] bias rows; rows past Sq read row Sq - 1 (their probabilities are zero).  A warp's
+// 32 keys are consecutive, so each load instruction reads 64 contiguous bytes.
+__device__ __forceinline__ void load_bias_col(uint32_t (&bq)[16], const unsigned short *col, int q0, int Sq,
+                                              long long Sk) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const int qa = min(q0 + 2 * e, Sq - 1), qb = min(q0 + 2 * e + 1, Sq - 1);
+    bq[e] = (uint32_t)__ldg(col + qa * Sk) | ((uint32_t)__ldg(col + qb * Sk) << 16);
+  }
+}
+
+// dbias accumulation: dU of this thread's key for the visible queries of a chunk, added into
+// the fp32 accumulator (reduce-adds: broadcast dimensions and GQA heads may share elements).
+// Predicated in the instruction itself, so that per-lane visibility never splits the warp
+// ahead of the tensor-memory instructions, which need it converged.
+__device__ __forceinline__ void red_add_f32_if(float *addr, float v, uint32_t pred) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t@p red.global.add.f32 [%0], %1;\n\t}" ::"l"(addr),
+               "f"(v), "r"(pred)
+               : "memory");
+}
 
 // One pair of raw scores -> (t2 - LSE2, f): t2 the (capped) logit in log2 units, f the
 // cap's chain-rule factor times the softmax scale.  FRCP: the cap's reciprocal on the FMA pipe
 // (f2_sigmoid2_neg); otherwise ex2 + rcp on the special-function unit.  The head-dim-256 dK pass
 // keeps the latter: its element-wise work sits on the S^T -> dP^T dependency chain and is not
 // bound by the special-function unit, and the longer FMA sequence measured 5 % slower there.
-template <bool CAP, bool FRCP>
+// BIAS: b2 is the pair's bias, and f comes without the softmax scale.
+template <bool CAP, bool FRCP, bool BIAS = false>
 __device__ __forceinline__ void score_pair(uint32_t s0, uint32_t s1, uint64_t lse2, const BwdScore &k, uint64_t &y,
-                                           uint64_t &f) {
+                                           uint64_t &f, uint64_t b2 = 0) {
   const uint64_t s2 = f2_pack(__uint_as_float(s0), __uint_as_float(s1));
   if constexpr (CAP) {
     uint64_t r2, e2;
+    const uint64_t x2 = BIAS ? f2_fma(s2, k.cin, f2_mul(b2, k.bin)) : f2_mul(s2, k.cin);
     if constexpr (FRCP) {
-      r2 = f2_sigmoid2_neg(f2_mul(s2, k.cin), e2);
+      r2 = f2_sigmoid2_neg(x2, e2);
     } else {
       float xa, xb, da, db;
-      f2_unpack(f2_mul(s2, k.cin), xa, xb);
+      f2_unpack(x2, xa, xb);
       e2 = f2_pack(ex2_approx(fminf(xa, 126.f)), ex2_approx(fminf(xb, 126.f)));
       f2_unpack(f2_add(e2, k.one), da, db);
       r2 = f2_pack(rcp_approx(da), rcp_approx(db));
@@ -184,10 +220,10 @@ __device__ __forceinline__ void score_pair(uint32_t s0, uint32_t s1, uint64_t ls
     y = f2_sub(f2_fma(r2, k.mcap2, k.cap2), lse2);
     // 1 - tanh^2 = 4 r (1 - r) = 4 e r^2: the second form keeps full relative accuracy where the
     // cap saturates (r -> 1, where 1 - r would cancel), so the tiny gradients there stay right.
-    f = f2_mul(f2_mul(e2, k.fs), f2_mul(r2, r2));
+    f = f2_mul(f2_mul(e2, BIAS ? k.f4 : k.fs), f2_mul(r2, r2));
   } else {
-    y = f2_sub(f2_mul(s2, k.sc2), lse2);
-    f = k.scale;
+    y = f2_sub(BIAS ? f2_fma(s2, k.sc2, f2_mul(b2, k.bin)) : f2_mul(s2, k.sc2), lse2);
+    f = BIAS ? k.one : k.scale;
   }
 }
 __device__ __forceinline__ uint64_t ex2_pair(uint64_t y) {
@@ -205,47 +241,73 @@ __device__ __forceinline__ uint32_t bf16_pair(uint64_t v) {
 // cleared afterwards by the fix-ups below, only on chunks that need it):
 //   KIND 1: P, packed to bf16 pairs;  KIND 0: P and dS = P f (dP - D), both packed, from the
 //   dP^T accumulator that started at -D.
-template <bool CAP, bool FRCP, int KIND>
+//   BIAS: bq holds the chunk's bias pairs; with KIND 0, dU = P f (dP - D) of each visible
+//   query (vis bit e) is also added into the dbias accumulator at dbc + e Sk.
+template <bool CAP, bool FRCP, int KIND, bool BIAS = false>
 __device__ __forceinline__ void bwd_chunk(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float *lse2c,
-                                          uint32_t (&pk)[16], uint32_t (&dk)[16], const BwdScore &k) {
+                                          uint32_t (&pk)[16], uint32_t (&dk)[16], const BwdScore &k,
+                                          const uint32_t *bq = nullptr, float *dbc = nullptr, long long Sk = 0,
+                                          uint32_t vis = 0) {
   const uint64_t *l2 = reinterpret_cast<const uint64_t *>(lse2c);
 #pragma unroll
   for (int e2 = 0; e2 < 16; ++e2) {
     uint64_t y, f;
-    score_pair<CAP, FRCP>(sr[2 * e2], sr[2 * e2 + 1], l2[e2], k, y, f);
+    score_pair<CAP, FRCP, BIAS>(sr[2 * e2], sr[2 * e2 + 1], l2[e2], k, y, f, BIAS ? bias_pair(bq[e2]) : 0);
     const uint64_t p2 = ex2_pair(y);
     pk[e2] = bf16_pair(p2);
     if constexpr (KIND == 0) {
       const uint64_t dpd = f2_pack(__uint_as_float(dr[2 * e2]), __uint_as_float(dr[2 * e2 + 1]));
-      dk[e2] = bf16_pair(f2_mul(f2_mul(p2, f), dpd));
+      const uint64_t du = f2_mul(f2_mul(p2, f), dpd);
+      if constexpr (BIAS) {
+        float a, b;
+        f2_unpack(du, a, b);
+        red_add_f32_if(dbc + (2 * e2) * Sk, a, (vis >> (2 * e2)) & 1u);
+        red_add_f32_if(dbc + (2 * e2 + 1) * Sk, b, (vis >> (2 * e2 + 1)) & 1u);
+        dk[e2] = bf16_pair(f2_mul(du, k.scale));
+      } else {
+        dk[e2] = bf16_pair(du);
+      }
     }
   }
 }
 
 // The dK pass's chunk in two steps, so that the first runs before dP^T has been computed:
 // (1) in place, the raw score -> P f;
-template <bool CAP, bool FRCP>
-__device__ __forceinline__ void ds_first(uint32_t (&sr)[32], const float *lse2c, const BwdScore &k) {
+template <bool CAP, bool FRCP, bool BIAS = false>
+__device__ __forceinline__ void ds_first(uint32_t (&sr)[32], const float *lse2c, const BwdScore &k,
+                                         const uint32_t *bq = nullptr) {
   const uint64_t *l2 = reinterpret_cast<const uint64_t *>(lse2c);
 #pragma unroll
   for (int e2 = 0; e2 < 16; ++e2) {
     uint64_t y, f;
-    score_pair<CAP, FRCP>(sr[2 * e2], sr[2 * e2 + 1], l2[e2], k, y, f);
+    score_pair<CAP, FRCP, BIAS>(sr[2 * e2], sr[2 * e2 + 1], l2[e2], k, y, f, BIAS ? bias_pair(bq[e2]) : 0);
     float a, b;
     f2_unpack(f2_mul(ex2_pair(y), f), a, b);
     sr[2 * e2] = __float_as_uint(a);
     sr[2 * e2 + 1] = __float_as_uint(b);
   }
 }
-// (2) dS = P f (dP - D), packed to bf16 pairs.
+// (2) dS = P f (dP - D), packed to bf16 pairs.  BIAS: P f came without the softmax scale;
+// dU = P f (dP - D) of each visible query goes into the dbias accumulator first.
+template <bool BIAS = false>
 __device__ __forceinline__ void ds_second(const uint32_t (&pf)[32], const uint32_t (&dr)[32], const float *dvc,
-                                          uint32_t (&dk)[16]) {
+                                          uint32_t (&dk)[16], uint64_t scale2 = 0, float *dbc = nullptr,
+                                          long long Sk = 0, uint32_t vis = 0) {
   const uint64_t *d2 = reinterpret_cast<const uint64_t *>(dvc);
 #pragma unroll
   for (int e2 = 0; e2 < 16; ++e2) {
     const uint64_t pf2 = f2_pack(__uint_as_float(pf[2 * e2]), __uint_as_float(pf[2 * e2 + 1]));
     const uint64_t dp = f2_pack(__uint_as_float(dr[2 * e2]), __uint_as_float(dr[2 * e2 + 1]));
-    dk[e2] = bf16_pair(f2_mul(pf2, f2_sub(dp, d2[e2])));
+    const uint64_t du = f2_mul(pf2, f2_sub(dp, d2[e2]));
+    if constexpr (BIAS) {
+      float a, b;
+      f2_unpack(du, a, b);
+      red_add_f32_if(dbc + (2 * e2) * Sk, a, (vis >> (2 * e2)) & 1u);
+      red_add_f32_if(dbc + (2 * e2 + 1) * Sk, b, (vis >> (2 * e2 + 1)) & 1u);
+      dk[e2] = bf16_pair(f2_mul(du, scale2));
+    } else {
+      dk[e2] = bf16_pair(du);
+    }
   }
 }
 
@@ -275,7 +337,7 @@ __device__ __forceinline__ void clear_hidden(uint32_t (&x)[16], uint32_t vis) {
     x[e2] &= (((vis >> (2 * e2)) & 1u) ? 0x0000ffffu : 0u) | (((vis >> (2 * e2 + 1)) & 1u) ? 0xffff0000u : 0u);
 }
 
-template <class C, bool CAP>
+template <class C, bool CAP, bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -479,9 +541,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const BwdScore ks(p.scale, p.inv_cap, p.cap);
     uint8_t *ds_row = smem + C::OFF_DS + r * 128;
     bool ok = true;
+    // Bias: this key's column of the [Sq, Sk] rows of each query head (a key past Sk reads
+    // the last column; its queries are never visible), and the same column of the fp32 dbias
+    // accumulator, whose broadcast dimensions have extent 1.
+    const int kc = key_ok ? k : p.Sk - 1;
+    const unsigned short *bias_b =
+        BIAS ? static_cast<const unsigned short *>(p.bias) + (size_t)b * p.bias_sb + kc : nullptr;
+    float *dbias_b = BIAS ? p.dbias_acc + (size_t)(p.bias_B == 1 ? 0 : b) * p.bias_H * p.Sq * p.Sk + kc : nullptr;
 
     for (int j = 0; j < nsteps && ok; ++j) {
       const int kind = step_kind(j), q0 = step_q0(j), s = slot_of(j);
+      constexpr int NCH = BQ / 64;  // 32-column chunks per thread and step
+      uint32_t bq[NCH][BIAS ? 16 : 1];
+      const unsigned short *bcol = nullptr;
+      float *dbcol = nullptr;
+      if constexpr (BIAS) {  // the step's bias, in flight while S^T is computed
+        const int h = step_h(j);
+        bcol = bias_b + (size_t)h * p.bias_sh;
+        dbcol = dbias_b + (size_t)(p.bias_H == 1 ? 0 : h) * p.Sq * p.Sk;
+#pragma unroll
+        for (int cc = 0; cc < NCH; ++cc) load_bias_col(bq[cc], bcol, q0 + (half * NCH + cc) * 32, p.Sq, p.Sk);
+      }
       if (!mbar_wait(s_full, j & 1, p.status)) { ok = false; break; }
       if (C::TWO) {
         if (!mbar_wait(ld_full(j & 1), (j >> 1) & 1, p.status)) { ok = false; break; }
@@ -496,11 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P and dS of this thread's columns are formed in registers while the previous
       // step's dV / dK / dQ MMAs still read the P^T and dS^T buffers (and, once S^T / dP^T
       // are copied out, while the next step's S^T / dP^T are computed) ...
-      constexpr int NCH = BQ / 64;  // 32-column chunks per thread and step
       uint32_t pk[NCH][16], dk[NCH][16];
       if (C::TWO && kind == 2) {
         // dK pass: P f from S^T first, then dP^T (computed meanwhile) for dS.
         uint32_t pf[NCH][32];
+        uint32_t visc[NCH];
 #pragma unroll
         for (int cc = 0; cc < NCH; ++cc) {
           const int c = half * NCH + cc;
@@ -511,8 +591,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(sdp_free);
           }
-          ds_first<CAP, false>(pf[cc], lse2 + c * 32, ks);
-          if (!full) clear_hidden(pf[cc], chunk_vis(q0 + c * 32, lo, hi, seg_pairwise, segq, p.Sq, sid));
+          ds_first<CAP, false, BIAS>(pf[cc], lse2 + c * 32, ks, bq[cc]);
+          visc[cc] = full ? 0xffffffffu : chunk_vis(q0 + c * 32, lo, hi, seg_pairwise, segq, p.Sq, sid);
+          if (!full) clear_hidden(pf[cc], visc[cc]);
         }
         if (!mbar_wait(dp_full, (j - nper) & 1, p.status)) { ok = false; break; }
         tc_fence_after();
@@ -527,7 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(dp_free);
           }
-          ds_second(pf[cc], dr, dvv + c * 32, dk[cc]);
+          ds_second<BIAS>(pf[cc], dr, dvv + c * 32, dk[cc], ks.scale, BIAS ? dbcol + (size_t)(q0 + c * 32) * p.Sk : nullptr,
+                          p.Sk, visc[cc]);
         }
       } else {
 #pragma unroll
@@ -543,11 +625,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(sdp_free);
           }
-          bwd_chunk<CAP, true, C::TWO ? 1 : 0>(sr, dr, lse2 + c * 32, pk[cc], dk[cc], ks);
-          if (!full) {
-            const uint32_t vis = chunk_vis(q0 + c * 32, lo, hi, seg_pairwise, segq, p.Sq, sid);
-            clear_hidden(pk[cc], vis);
-            if (!C::TWO) clear_hidden(dk[cc], vis);
+          if constexpr (BIAS) {
+            const uint32_t vis = full ? 0xffffffffu : chunk_vis(q0 + c * 32, lo, hi, seg_pairwise, segq, p.Sq, sid);
+            bwd_chunk<CAP, true, C::TWO ? 1 : 0, true>(sr, dr, lse2 + c * 32, pk[cc], dk[cc], ks, bq[cc],
+                                                       dbcol + (size_t)(q0 + c * 32) * p.Sk, p.Sk, vis);
+            if (!full) {
+              clear_hidden(pk[cc], vis);
+              if (!C::TWO) clear_hidden(dk[cc], vis);
+            }
+          } else {
+            bwd_chunk<CAP, true, C::TWO ? 1 : 0>(sr, dr, lse2 + c * 32, pk[cc], dk[cc], ks);
+            if (!full) {
+              const uint32_t vis = chunk_vis(q0 + c * 32, lo, hi, seg_pairwise, segq, p.Sq, sid);
+              clear_hidden(pk[cc], vis);
+              if (!C::TWO) clear_hidden(dk[cc], vis);
+            }
           }
         }
       }
@@ -1163,7 +1255,8 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
       !make_tmap_f32_bshd(&tdq, p.dQacc, C::D, p.Sq, p.Hq, p.B, C::DQT ? 128 : 32, C::DQT ? (C::TWO ? 16 : 32) : 128,
                           !C::DQT))
     return cudaErrorInvalidValue;
-  auto kern = p.cap > 0.f ? bwd_tc_kernel<C, true> : bwd_tc_kernel<C, false>;
+  auto kern = p.bias ? (p.cap > 0.f ? bwd_tc_kernel<C, true, true> : bwd_tc_kernel<C, false, true>)
+                     : (p.cap > 0.f ? bwd_tc_kernel<C, true, false> : bwd_tc_kernel<C, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const long long nblk = (long long)((p.Sk + kBK - 1) / kBK) * p.Hkv * p.B;

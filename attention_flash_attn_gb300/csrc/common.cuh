@@ -29,6 +29,7 @@ struct Params {
   const void *bias;
   long long bias_sb, bias_sh;
   int bias_B, bias_H;             // extents of the bias's own batch / head dims (1 = broadcast)
+  int bias_vec;                   // every bias row starts on a 16-byte boundary (16-byte loads)
   const int *seg_q, *seg_k;       // effective segment ids or null
   const int2 *qrange;             // [B, ceil(Sq/64)]: key range [x, y) of each 64-row query tile
   const int2 *krange;             // [B, ceil(Sk/64)]: query range [x, y) of each 64-key tile

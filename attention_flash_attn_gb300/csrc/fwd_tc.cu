@@ -89,38 +89,86 @@ __device__ __forceinline__ int upper_bound_i(const int *a, int n, int x) {
   return lo;
 }
 
-// Pair barrier of the two softmax warps that share TMEM lane quarter `wq` (ids 2..5).
-// Both warps of the pair arrive converged, so the aligned form applies.
-__device__ __forceinline__ void pair_bar(int wq) { asm volatile("bar.sync %0, 64;" ::"r"(2 + wq) : "memory"); }
+// TMEM column (relative to its score buffer) of the bf16 P pairs that the PV MMA's 16-key
+// slice kk reads: the softmax half owning keys 16 kk .. 16 kk + 15 (HC keys per half) wrote
+// its P over the first HC / 2 columns of its own HC score columns.
+template <int HC>
+__device__ __forceinline__ constexpr uint32_t p_col(int kk) {
+  return (uint32_t)(kk * 8 + (kk * 16 / HC) * (HC / 2));
+}
+
+// Pair barrier of the two softmax warps that share TMEM lane quarter `wq` (ids 2..5).  The
+// aligned form needs each warp converged when it arrives: the __syncwarp makes it so, whatever
+// per-lane waits or branches came before.
+__device__ __forceinline__ void pair_bar(int wq) {
+  __syncwarp();
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + wq) : "memory");
+}
 
 // Score constants as packed pairs.  With the soft-cap, e = exp(2 u / cap) for u = scale s and
 // r = 1 / (1 + e): tanh(u / cap) = 1 - 2 r, so the capped logit in log2 units is
 // cap log2(e) (1 - 2 r), with r from f2_sigmoid2_neg (FMA-pipe reciprocal).  A huge e (its
 // exponent is clamped at 126) gives r ~ 0 (tanh = 1), an underflowing one r = 1.
+// With a bias the logit is u = scale s + bias; the bias enters as its own term (bin: its
+// factor, 2 log2(e) / cap with the cap, log2(e) without).
 struct FwdScore {
-  uint64_t cin, mcap2, cap2, sc2;
+  uint64_t cin, mcap2, cap2, sc2, bin;
   __device__ FwdScore(float scale, float inv_cap, float cap) {
     cin = f2_splat(2.f * kLog2e * scale * inv_cap);
     mcap2 = f2_splat(-2.f * cap * kLog2e);
     cap2 = f2_splat(cap * kLog2e);
     sc2 = f2_splat(scale * kLog2e);
+    bin = f2_splat(cap > 0.f ? 2.f * kLog2e * inv_cap : kLog2e);
   }
 };
+
+// The bias of one bf16 pair (low half first) as a pair of floats.
+__device__ __forceinline__ uint64_t bias_pair(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// This thread's N2 bias pairs of a tile: row `row`, columns j0 .. j0 + 2 N2 - 1; columns at
+// or past Sk read as 0 (they are masked).  16-byte loads when every row starts on a 16-byte
+// boundary and the columns lie inside the row.  The branch depends on warp-uniform values only,
+// so the warp stays converged for the tensor-memory instructions that follow.
+template <int N2>
+__device__ __forceinline__ void load_bias_row(uint32_t (&bq)[N2], const __nv_bfloat16 *row, int j0, int Sk,
+                                              bool vec) {
+  if (vec && j0 + 2 * N2 <= Sk) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(row + j0);
+#pragma unroll
+    for (int v = 0; v < N2 / 4; ++v) {
+      const uint4 x = __ldg(src + v);
+      bq[4 * v] = x.x;
+      bq[4 * v + 1] = x.y;
+      bq[4 * v + 2] = x.z;
+      bq[4 * v + 3] = x.w;
+    }
+  } else {
+    const unsigned short *r16 = reinterpret_cast<const unsigned short *>(row);
+#pragma unroll
+    for (int e = 0; e < N2; ++e) {
+      const int ja = j0 + 2 * e;  // clamped indices: every load stays inside the row
+      const uint32_t lo = __ldg(r16 + min(ja, Sk - 1)), hi = __ldg(r16 + min(ja + 1, Sk - 1));
+      bq[e] = (ja < Sk ? lo : 0u) | (ja + 1 < Sk ? hi << 16 : 0u);
+    }
+  }
+}
 
 // Raw scores -> capped, masked base-2 logits in place; returns their maximum.  MIX: every
 // other pair takes the cap's reciprocal from the special-function unit (rcp.approx) instead of
 // the FMA pipe -- 7 issue slots per pair instead of 11, for two more special-function ops --
 // for kernels whose softmax warps are issue-bound with that unit part idle.
-template <bool CAP, bool MASKED, bool MIX, int N>
+template <bool CAP, bool MASKED, bool MIX, bool BIAS, int N>
 __device__ __forceinline__ float logits2(uint32_t (&x)[N], const FwdScore &k, int jbase, int lo, int hi,
-                                         bool pairwise, const int *segk, int sid) {
+                                         bool pairwise, const int *segk, int sid, const uint32_t *bq) {
   float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
   for (int e = 0; e < N; e += 2) {
     const uint64_t s2 = f2_pack(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
     uint64_t t2;
     if constexpr (CAP) {
-      const uint64_t x2 = f2_mul(s2, k.cin);
+      const uint64_t x2 = BIAS ? f2_fma(s2, k.cin, f2_mul(bias_pair(bq[e / 2]), k.bin)) : f2_mul(s2, k.cin);
       uint64_t r2;
       if (MIX && (e & 2)) {
         float xa, xb, da, db;
@@ -132,7 +180,7 @@ __device__ __forceinline__ float logits2(uint32_t (&x)[N], const FwdScore &k, in
       }
       t2 = f2_fma(r2, k.mcap2, k.cap2);
     } else {
-      t2 = f2_mul(s2, k.sc2);
+      t2 = BIAS ? f2_fma(s2, k.sc2, f2_mul(bias_pair(bq[e / 2]), k.bin)) : f2_mul(s2, k.sc2);
     }
     float ta, tb;
     f2_unpack(t2, ta, tb);
@@ -165,7 +213,7 @@ __device__ __forceinline__ float logits2(uint32_t (&x)[N], const FwdScore &k, in
 constexpr float kFixedMaxCap = 54.0f;  // 2 cap log2(e) - 124 <= 32
 __device__ __forceinline__ float fixed_delta(float cap) { return fmaxf(0.f, 2.f * cap * kLog2e - 124.f); }
 
-template <int D, int BN, int NK, int NV, bool CAP, bool FIXM>
+template <int D, int BN, int NK, int NV, bool CAP, bool FIXM, bool BIAS>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -370,7 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int kk = 4 * hf; kk < 4 * hf + 4; ++kk)
-              mma_ts_w(tmem + C::TM_O, pa + kk * 8, desc_at(dv0, kk * (16 * 128)), idO, (jj > 0 || kk > 0) ? 1u : 0u);
+              mma_ts_w(tmem + C::TM_O, pa + p_col<HC>(kk), desc_at(dv0, kk * (16 * 128)), idO,
+                       (jj > 0 || kk > 0) ? 1u : 0u);
             mma_commit_w(v_empty(hf));
           }
           if (!okh) break;
@@ -384,7 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t pa = tmem + (uint32_t)((jj & 1) * BN);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts_w(tmem + C::TM_O, pa + kk * 8, desc_at(dvs, kk * (16 * 128)), idO, (jj > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_w(tmem + C::TM_O, pa + p_col<HC>(kk), desc_at(dvs, kk * (16 * 128)), idO,
+                     (jj > 0 || kk > 0) ? 1u : 0u);
           mma_commit_w(v_empty(s));
           mma_commit_w(o_done);
         }
@@ -435,6 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
 
     const FwdScore ks(p.scale, p.inv_cap, p.cap);
+    // This row's bias (logically [B, Hq, Sq, Sk]; broadcast dimensions have stride 0).  A row
+    // past Sq reads row Sq - 1 (never stored), so that every lane takes the same path.
+    const __nv_bfloat16 *brow =
+        BIAS ? static_cast<const __nv_bfloat16 *>(p.bias) + (size_t)b * p.bias_sb + (size_t)h * p.bias_sh +
+                   (size_t)min(i, p.Sq - 1) * p.Sk
+             : nullptr;
     const bool sink_col = has_sink_col(p) && ns == 1;  // split partials leave it to the merge
     float m_ref = sink_col ? sink_logit(p, h) * kLog2e : -INFINITY;  // running max (log2 units)
     float l = (sink_col && half == 0) ? 1.f : 0.f;                   // this half's sum relative to m_ref
@@ -446,6 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
+      const int j0 = (t0 + j) * BN + half * HC;
+      uint32_t bq[BIAS ? HC / 2 : 1];
+      if constexpr (BIAS) load_bias_row(bq, brow, j0, p.Sk, p.bias_vec != 0);  // in flight during the wait
       // Warp-uniform, so that a failed wait takes the whole warp (and, through the exchange
       // below, its partner) out of the loop together.
       const bool got = __all_sync(0xffffffffu, mbar_wait(s_full(j & 1), (j >> 1) & 1, p.status));
@@ -458,12 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence(xr);
       }
-      const int j0 = (t0 + j) * BN + half * HC;
       const bool full = !any_pairwise && (t0 + j) * BN >= cta_lo && (t0 + j + 1) * BN <= cta_hi;
       float mx = -INFINITY;
       if (got) {
-        mx = full ? logits2<CAP, false, (D <= 128)>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid)
-                  : logits2<CAP, true, (D <= 128)>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid);
+        mx = full ? logits2<CAP, false, (D <= 128), BIAS>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid, bq)
+                  : logits2<CAP, true, (D <= 128), BIAS>(xr, ks, j0, lo, hi, seg_pairwise, segk, sid, bq);
       }
       float alpha_o = 1.f;
       bool resc = false;
@@ -515,8 +573,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         f2_unpack(rs2, ra, rb);
         l += ra + rb;
       }
-      // P (bf16 pairs) over the first half of this score buffer's columns.
-      const uint32_t pa = lane_addr + (uint32_t)((j & 1) * BN + half * (HC / 2));
+      // P (bf16 pairs) over the first half of this thread's own score columns: the partner
+      // warp may still be reading its half of S, so neither writes into the other's columns.
+      const uint32_t pa = lane_addr + (uint32_t)((j & 1) * BN + half * HC);
 #pragma unroll
       for (int c = 0; c < HC / 64; ++c) tmem_st32(pa + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + c * 32));
       if constexpr (HC / 2 == 16) tmem_st16(pa, pk);
@@ -542,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (ok && n > 0) {
-      ok = FIXM ? mbar_wait(o_fin, 0, p.status) : mbar_wait(o_done, (n - 1) & 1, p.status);
+      ok = __all_sync(0xffffffffu, FIXM ? mbar_wait(o_fin, 0, p.status) : mbar_wait(o_done, (n - 1) & 1, p.status));
       tc_fence_after();
     }
     // Combine the two halves' sums (the running maxima already agree); slot 2 is used
@@ -621,9 +680,12 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
       !make_tmap_bshd(&tk, p.k, D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, BN) ||
       !make_tmap_bshd(&tv, p.v, D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, C::HALF ? 64 : BN))
     return cudaErrorInvalidValue;
-  auto kern = p.cap <= 0.f                 ? fwd_tc_kernel<D, BN, NK, NV, false, false>
-              : p.cap <= kFixedMaxCap ? fwd_tc_kernel<D, BN, NK, NV, true, true>
-                                      : fwd_tc_kernel<D, BN, NK, NV, true, false>;
+  auto kern = p.bias ? (p.cap <= 0.f                 ? fwd_tc_kernel<D, BN, NK, NV, false, false, true>
+                        : p.cap <= kFixedMaxCap ? fwd_tc_kernel<D, BN, NK, NV, true, true, true>
+                                                : fwd_tc_kernel<D, BN, NK, NV, true, false, true>)
+                     : (p.cap <= 0.f                 ? fwd_tc_kernel<D, BN, NK, NV, false, false, false>
+                        : p.cap <= kFixedMaxCap ? fwd_tc_kernel<D, BN, NK, NV, true, true, false>
+                                                : fwd_tc_kernel<D, BN, NK, NV, true, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const long long nblk = (long long)((p.Sq + kBM - 1) / kBM) * p.Hq * p.B * (p.kv_splits > 1 ? p.kv_splits : 1);

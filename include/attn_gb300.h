@@ -90,10 +90,11 @@ typedef struct {
     int dtype;                 /* enum attn_dtype                                          */
     int B, Sq, Sk, Hq, Hkv, D; /* B, Sq, Sk >= 0 (B == 0 or Sq == 0: nothing to compute);
                                   Hq, Hkv >= 1 with Hq % Hkv == 0; D % 8 == 0, D <= 512.
-                                  Tensor-core kernels: bf16 with D in {64, 128, 256}; other
-                                  head dims (up to 512: MaxText's chunked head-dim
-                                  accumulation above 256, tokamax PR #1121) run on the fp32
-                                  FFMA kernels                                             */
+                                  Tensor-core kernels: bf16 with D in {64, 128, 256} and
+                                  Sk > 0, with or without a bias, sink, segments or splits.
+                                  The fp32 FFMA kernels take every other call: fp32 inputs,
+                                  and other head dims (up to 512: MaxText's chunked head-dim
+                                  accumulation above 256, tokamax PR #1121)                */
     const void *q;             /* [B,Sq,Hq,D] with the strides below (elements)           */
     int64_t q_stride_b, q_stride_s, q_stride_h;
     const void *k;             /* [B,Sk,Hkv,D]                                             */
@@ -102,7 +103,9 @@ typedef struct {
     int64_t v_stride_b, v_stride_s, v_stride_h;
     /* Optional additive bias, logically [B,Hq,Sq,Sk]: element (b,h,i,j) lives at
      * bias[b*bias_stride_b + h*bias_stride_h + i*Sk + j]; a stride of 0 broadcasts that
-     * dimension.  NULL: no bias.  Same dtype as q.                                        */
+     * dimension.  NULL: no bias.  Same dtype as q; 16-byte aligned base.  Added after the
+     * scale and before the cap.  Rows that start on 16-byte boundaries (Sk and both strides
+     * multiples of 8 bf16 elements) are read with 16-byte loads, others element by element. */
     const void *bias;
     int64_t bias_stride_b, bias_stride_h;
     /* Optional packed segments: seg_q [B,Sq] and seg_k [B,Sk] int32 (both or neither).

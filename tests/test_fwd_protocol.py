@@ -10,7 +10,11 @@ phase k must see k or k + 1 completed phases), two data hazards are checked:
 * S_{j+2} reuses the score buffer of S_j and P_j: the MMA warp may issue it only after both
   softmax warps have finished step j (arrived on p_full for it);
 * the tracked-maximum form rescales O in TMEM at step j: no PV may be in flight then, so
-  exactly j PVs have completed.
+  exactly j PVs have completed;
+* each softmax warp writes P_j over score columns: in the kernel's layout a warp writes only
+  into its own half of S_j; in the earlier layout the second half's P went over columns of
+  the first half's S, which the fixed-offset form (no pair barrier per step) does not order
+  after the first half's reads -- the negative control.
 
 Ring shapes: head dim 64 (4 K / 4 V stages), 128 (3 / 2), 256 (one K and one V tile, each
 filled and released in two halves with barriers of their own).
@@ -25,7 +29,7 @@ from test_bwd_protocol import run_agents
 TILE_COUNTS = [1, 2, 3, 4, 5, 7, 9, 16, 33]
 
 
-def simulate_forward(n, nk, nv, halves, fixm, rng, skip_pv_wait=False):
+def simulate_forward(n, nk, nv, halves, fixm, rng, skip_pv_wait=False, p_layout="own"):
     """Returns (finished, hazards).  halves: the head-dim-256 form (K by head-dim halves, V by
     key halves, each half its own full / empty barrier pair).  skip_pv_wait drops the MMA
     warp's wait on p_full before PV (a negative control: P would be read before it is
@@ -92,9 +96,10 @@ def simulate_forward(n, nk, nv, halves, fixm, rng, skip_pv_wait=False):
         if fixm:
             yield ("arrive", "o_fin")
 
-    def softmax():
+    def softmax(half):
         for j in range(n):
             yield ("wait", f"s_full{j & 1}", j >> 1)
+            yield ("arrive", f"sread{half}")  # this half's S_j is in registers
             if not fixm:
                 yield ("arrive", f"pair{j}")  # exchange of half-row maxima
                 yield ("wait", f"pair{j}", 0)
@@ -102,6 +107,8 @@ def simulate_forward(n, nk, nv, halves, fixm, rng, skip_pv_wait=False):
                     yield ("wait", "o_done", j - 1)
                     if done["o_done"] != j:
                         hazards.append(("softmax", "O rescaled under a PV", j, done["o_done"]))
+            if p_layout == "shared" and half == 1 and done["sread0"] <= j:
+                hazards.append(("softmax1", "P over the partner's S", j, done["sread0"]))
             yield ("arrive", f"p_full{j & 1}")
         if n > 0:
             if fixm:
@@ -112,7 +119,7 @@ def simulate_forward(n, nk, nv, halves, fixm, rng, skip_pv_wait=False):
         yield ("wait", f"pair{n}", 0)
 
     agents = {"kload": kload(), "vload": ring_loader("v", nv), "mma": mma(),
-              "softmax0": softmax(), "softmax1": softmax()}
+              "softmax0": softmax(0), "softmax1": softmax(1)}
     return run_agents(agents, arrive, done, hazards, rng)
 
 
@@ -139,3 +146,16 @@ def test_forward_model_flags_pv_without_the_p_full_wait(fixm):
         _, hazards = simulate_forward(8, 4, 4, False, fixm, rng, skip_pv_wait=True)
         over_p += sum(1 for h in hazards if " over P" in h[1])
     assert over_p > 0
+
+
+def test_forward_model_flags_p_over_the_partner_s_without_a_pair_barrier():
+    """Negative control: with the second half's P written over the first half's score columns,
+    the fixed-offset form (no per-step pair barrier) lets the write overtake the partner's
+    read; the tracked form's pair barrier orders them."""
+    rng = random.Random(17)
+    flagged = {True: 0, False: 0}
+    for fixm in (True, False):
+        for trial in range(200):
+            _, hazards = simulate_forward(8, 1, 1, True, fixm, rng, p_layout="shared")
+            flagged[fixm] += sum(1 for h in hazards if "partner" in h[1])
+    assert flagged[True] > 0 and flagged[False] == 0

@@ -39,7 +39,8 @@ class Workload:
     softcap: float = 0.0     # 0: no cap
     q_std: float = 1.0       # std of q and k
     v_std: float = 1.0       # std of v and dO
-    bias: bool = False       # post-scale additive bias [1, Hq, Sq, Sk] ~ N(0,1), broadcast over b
+    bias: bool = False       # post-scale additive bias ~ N(0,1) [1|B, 1|Hq, Sq, Sk] (bias_dims)
+    bias_dims: str = "h"     # dimensions the bias has of its own: "h" [1,Hq], "b" [B,1], "bh", ""
     sink: bool = False       # per-query-head sink offsets ~ randn * 5
     segments: bool = False   # packed rows: run lengths ~ U[run_lo, run_hi], last truncated
     run_lo: int = 64
@@ -74,6 +75,10 @@ WORKLOADS = {
                  causal=True, window=4096, softcap=50.0, q_std=3.0),
         Workload("gemma2_local_w4096_cap0", "bf16", B=2, Sq=8192, Sk=8192, Hq=16, Hkv=8, D=256,
                  causal=True, window=4096, softcap=0.0, q_std=3.0),
+        # The same layer with a post-scale additive bias per query head ([1, Hq, S, S] bf16):
+        # the bias path of the tensor-core kernels (this build's own workload).
+        Workload("gemma2_local_w4096_cap50_bias", "bf16", B=2, Sq=8192, Sk=8192, Hq=16, Hkv=8, D=256,
+                 causal=True, window=4096, softcap=50.0, q_std=3.0, bias=True),
         Workload("packed_varlen_cap30", "bf16", B=4, Sq=8192, Sk=8192, Hq=8, Hkv=8, D=128,
                  causal=True, softcap=30.0, q_std=3.0, segments=True),
         Workload("sink_gqa64_cap0", "bf16", B=2, Sq=4096, Sk=4096, Hq=64, Hkv=8, D=64,
@@ -139,7 +144,7 @@ def thd_prefix_bounds(gen: torch.Generator, Sq: int, Sk: int, lo: int, hi: int, 
 
 def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
     """CPU tensors for one workload: q, k, v, dO in the workload dtype; bias (workload dtype,
-    [1,Hq,Sq,Sk]) or None; sink fp32 [Hq] or None; seg int32 [B,S] or None; cu_q / cu_k
+    [1|B, 1|Hq, Sq, Sk] per bias_dims) or None; sink fp32 [Hq] or None; seg int32 [B,S] or None; cu_q / cu_k
     int32 boundaries or None (thd_prefix workloads)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed if seed is None else seed)
@@ -152,7 +157,9 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
     k = draw((w.B, w.Sk, w.Hkv, w.D), w.q_std)
     v = draw((w.B, w.Sk, w.Hkv, w.D), w.v_std)
     dO = draw((w.B, w.Sq, w.Hq, w.D), w.v_std)
-    bias = draw((1, w.Hq, w.Sq, w.Sk), 1.0) if w.bias else None
+    bias = None
+    if w.bias:
+        bias = draw(("b" in w.bias_dims and w.B or 1, "h" in w.bias_dims and w.Hq or 1, w.Sq, w.Sk), 1.0)
     sink = (torch.randn((w.Hq,), generator=g, dtype=torch.float32) * 5.0) if w.sink else None
     seg = None
     if w.segments:
