@@ -15,7 +15,7 @@ import torch
 from . import _capi
 from ._capi import AttnArgs, AttnError, lib  # noqa: F401
 
-__all__ = ["attn_fwd", "attn_fwd_noalloc", "attn_bwd", "attn_check_device_status", "attn_path_name",
+__all__ = ["attn_fwd", "attn_fwd_noalloc", "attn_bwd", "attn_meta", "attn_check_device_status", "attn_path_name",
            "attn_launch_counter", "attn_profile_next_main_kernel", "AttnError", "build_args"]
 
 _DTYPES = {torch.bfloat16: _capi.ATTN_DTYPE_BF16, torch.float32: _capi.ATTN_DTYPE_F32}
@@ -28,11 +28,12 @@ def _ptr(t: Optional[torch.Tensor]):
 
 def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
                bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0,
-               cu_seqlens_k=None):
+               cu_seqlens_k=None, meta=None):
     """Fill an ``attn_args`` from tensors.  Returns (args, tensors kept alive).
     cu_seqlens_k: key boundaries of the cu_seqlens sequences (varlen with Sq != Sk per sequence).
     off_by_one: the off-by-one softmax (an extra column of logit 0 per row, no gradient).
-    kv_splits: split-KV forward into that many key shares per query tile (0 / 1: off)."""
+    kv_splits: split-KV forward into that many key shares per query tile (0 / 1: off).
+    meta: mask metadata from attn_meta for these same arguments (or None)."""
     if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must share dtype bfloat16 or float32")
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -84,6 +85,9 @@ def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale
     a.scale = float(D ** -0.5 if scale is None else scale)
     a.softmax_type = _capi.ATTN_SOFTMAX_OFF_BY_ONE if off_by_one else _capi.ATTN_SOFTMAX_DEFAULT
     a.kv_splits = int(kv_splits)
+    if meta is not None:
+        a.meta = meta.data_ptr()
+        keep.append(meta)
     return a, keep
 
 
@@ -108,11 +112,12 @@ def _check(status: int, where: str):
 
 def attn_fwd(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
              bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0,
-             cu_seqlens_k=None, out=None, lse=None):
+             cu_seqlens_k=None, meta=None, out=None, lse=None):
     """Forward: returns (O [B,Sq,Hq,D] in q's dtype, LSE [B,Hq,Sq] float32)."""
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
                          scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
-                         off_by_one=off_by_one, kv_splits=kv_splits, cu_seqlens_k=cu_seqlens_k)
+                         off_by_one=off_by_one, kv_splits=kv_splits, cu_seqlens_k=cu_seqlens_k,
+                         meta=meta)
     L = lib()
     need = L.attn_fwd_workspace_size(ctypes.byref(a))
     if need == 0:
@@ -146,12 +151,13 @@ def attn_fwd_noalloc(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None,
 
 def attn_bwd(q, k, v, O, LSE, dO, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
              bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0,
-             cu_seqlens_k=None):
+             cu_seqlens_k=None, meta=None):
     """Backward: returns (dQ, dK, dV, dbias or None, dsink or None).  (kv_splits, a forward
     setting, is accepted and ignored so that one set of keyword arguments serves both.)"""
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
                          scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
-                         off_by_one=off_by_one, kv_splits=kv_splits, cu_seqlens_k=cu_seqlens_k)
+                         off_by_one=off_by_one, kv_splits=kv_splits, cu_seqlens_k=cu_seqlens_k,
+                         meta=meta)
     L = lib()
     need = L.attn_bwd_workspace_size(ctypes.byref(a))
     if need == 0:
@@ -172,6 +178,24 @@ def attn_bwd(q, k, v, O, LSE, dO, *, causal=False, window=0, softcap=0.0, sink=N
                       ws.numel(), _stream(q.device)), "attn_bwd")
     del keep
     return dQ, dK, dV, dbias, dsink
+
+
+def attn_meta(q, k, v, *, out=None, **kw) -> Optional[torch.Tensor]:
+    """Mask metadata for these arguments (segments / cu_seqlens), built once on the current
+    stream to be passed as ``meta=`` to attn_fwd and attn_bwd with the same arguments; None
+    when the arguments need none.  ``out``: a uint8 buffer to rebuild it into (reused when it
+    is large enough)."""
+    kw.pop("meta", None)
+    kw.pop("kv_splits", None)
+    a, keep = build_args(q, k, v, **kw)
+    L = lib()
+    need = L.attn_meta_size(ctypes.byref(a))
+    if need == 0:
+        return None
+    buf = out if out is not None and out.numel() >= need else torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(L.attn_meta_build(ctypes.byref(a), buf.data_ptr(), buf.numel(), _stream(q.device)), "attn_meta_build")
+    del keep
+    return buf
 
 
 def attn_check_device_status(device=None) -> int:

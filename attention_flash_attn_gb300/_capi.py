@@ -30,7 +30,7 @@ EXPORTS = (
     "attn_fwd_workspace_size", "attn_fwd", "attn_bwd_workspace_size", "attn_bwd",
     "attn_check_device_status", "attn_status_string", "attn_path_name", "attn_launch_counter",
     "attn_profile_next_main_kernel", "attn_fwd_noalloc", "attn_noalloc_check_device_status",
-    "attn_selftest_wait_expiry",
+    "attn_selftest_wait_expiry", "attn_meta_size", "attn_meta_build",
 )
 
 
@@ -54,6 +54,7 @@ class AttnArgs(ctypes.Structure):
         ("softcap", ctypes.c_float), ("sink", ctypes.c_void_p), ("scale", ctypes.c_float),
         ("softmax_type", ctypes.c_int), ("kv_splits", ctypes.c_int),
         ("cu_seqlens_k", ctypes.c_void_p),
+        ("meta", ctypes.c_void_p),
     ]
 
 
@@ -75,6 +76,10 @@ def lib():
         L.attn_fwd_workspace_size.restype = sz
         L.attn_bwd_workspace_size.argtypes = [A]
         L.attn_bwd_workspace_size.restype = sz
+        L.attn_meta_size.argtypes = [A]
+        L.attn_meta_size.restype = sz
+        L.attn_meta_build.argtypes = [A, vp, sz, vp]
+        L.attn_meta_build.restype = ctypes.c_int
         L.attn_fwd.argtypes = [A, vp, vp, vp, sz, vp]
         L.attn_fwd.restype = ctypes.c_int
         L.attn_fwd_noalloc.argtypes = [A, vp, vp, vp]

@@ -20,9 +20,18 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Mask metadata carve-up (segment / cu_seqlens calls), relative to the start of its region:
+// a caller's buffer from attn_meta_build, or a region of the workspace.  [0, 256) holds a
+// status area of its own (used by attn_meta_build).  Offsets are 0 when a region is absent.
+struct MetaLayout {
+  size_t mono = 0, qrange = 0, krange = 0, seg = 0, segk = 0, qoff = 0, koff = 0;
+  size_t qtile = 0, ktile = 0, qwork = 0, kwork = 0, qorder = 0, korder = 0;
+  size_t total = 0;  // 0: the call needs no metadata
+};
+
 // Workspace carve-up.  Offsets are 0 when a region is absent.
 struct Layout {
-  size_t status = 0, mono = 0, qrange = 0, krange = 0, seg = 0, segk = 0, qoff = 0, koff = 0;
+  size_t meta = 0;  // the metadata region, when the call needs one and args->meta is NULL
   size_t dvec = 0, lse2 = 0, dsplit = 0, dsink_part = 0, dqacc = 0, dbias_acc = 0;
   size_t o_part = 0, lse_part = 0;
   size_t total = 0;
@@ -41,21 +50,47 @@ size_t dbias_elems(const attn_args *a) {
   return bb * hb * (size_t)a->Sq * (size_t)a->Sk;
 }
 
+bool needs_meta(const attn_args *a) { return (a->seg_q || a->cu_seqlens) && a->B > 0; }
+
+// Whether the work lists are built: at most work_order_max_tiles() tiles per axis.
+bool work_lists(const attn_args *a) {
+  const long long nq = (long long)a->B * ((a->Sq + 127) / 128), nk = (long long)a->B * ((a->Sk + 127) / 128);
+  return nq <= work_order_max_tiles() && nk <= work_order_max_tiles();
+}
+
+MetaLayout meta_layout(const attn_args *a) {
+  MetaLayout M;
+  if (!needs_meta(a)) return M;
+  size_t off = kAlign;  // [0, 256): status area of a standalone metadata buffer
+  const size_t nq = (a->Sq + 63) / 64, nk = (a->Sk + 63) / 64;
+  const size_t nq128 = (a->Sq + 127) / 128, nk128 = (a->Sk + 127) / 128;
+  M.mono = off; off += align_up((size_t)a->B);
+  M.qrange = off; off += align_up((size_t)a->B * nq * sizeof(int2));
+  M.krange = off; off += align_up((size_t)a->B * nk * sizeof(int2));
+  if (a->cu_seqlens) { M.seg = off; off += align_up((size_t)a->Sq * sizeof(int)); }
+  if (a->cu_seqlens_k) {
+    M.segk = off; off += align_up((size_t)a->Sk * sizeof(int));
+    M.qoff = off; off += align_up((size_t)a->Sq * sizeof(int));
+    M.koff = off; off += align_up((size_t)a->Sk * sizeof(int));
+  }
+  M.qtile = off; off += align_up((size_t)a->B * nq128 * sizeof(int4));
+  M.ktile = off; off += align_up((size_t)a->B * nk128 * sizeof(int4));
+  M.qwork = off; off += align_up((size_t)a->B * nq128 * sizeof(long long));
+  M.kwork = off; off += align_up((size_t)a->B * nk128 * sizeof(long long));
+  if (work_lists(a)) {
+    M.qorder = off; off += align_up((size_t)a->B * nq128 * sizeof(int2));
+    M.korder = off; off += align_up((size_t)a->B * nk128 * sizeof(int2));
+  }
+  M.total = off;
+  return M;
+}
+
 Layout layout(const attn_args *a, bool bwd) {
   Layout L;
   size_t off = kAlign;  // [0, 256): status word
-  const bool seg = a->seg_q || a->cu_seqlens;
-  if (seg) {
-    const size_t nq = (a->Sq + 63) / 64, nk = (a->Sk + 63) / 64;
-    L.mono = off; off += align_up((size_t)a->B);
-    L.qrange = off; off += align_up((size_t)a->B * nq * sizeof(int2));
-    L.krange = off; off += align_up((size_t)a->B * nk * sizeof(int2));
-    if (a->cu_seqlens) { L.seg = off; off += align_up((size_t)a->Sq * sizeof(int)); }
-    if (a->cu_seqlens_k) {
-      L.segk = off; off += align_up((size_t)a->Sk * sizeof(int));
-      L.qoff = off; off += align_up((size_t)a->Sq * sizeof(int));
-      L.koff = off; off += align_up((size_t)a->Sk * sizeof(int));
-    }
+  if (needs_meta(a) && !a->meta) {
+    L.meta = off;
+    off += meta_layout(a).total;
   }
   if (!bwd && split_kv(a)) {
     const size_t rows = (size_t)a->kv_splits * a->B * a->Hq * a->Sq;
@@ -110,7 +145,31 @@ int validate(const attn_args *a) {
   } else if (a->cu_seqlens_k) {
     return ATTN_ERR_INVALID;
   }
+  if (((uintptr_t)a->meta % kAlign) != 0) return ATTN_ERR_INVALID;
   return ATTN_OK;
+}
+
+// Points the parameter block's metadata fields into a metadata region at `m`.
+void set_meta(const attn_args *a, char *m, Params &p) {
+  const MetaLayout M = meta_layout(a);
+  p.seg_mono = reinterpret_cast<unsigned char *>(m + M.mono);
+  p.qrange = reinterpret_cast<int2 *>(m + M.qrange);
+  p.krange = reinterpret_cast<int2 *>(m + M.krange);
+  p.qtile = reinterpret_cast<int4 *>(m + M.qtile);
+  p.ktile = reinterpret_cast<int4 *>(m + M.ktile);
+  p.qorder = M.qorder ? reinterpret_cast<int2 *>(m + M.qorder) : nullptr;
+  p.korder = M.korder ? reinterpret_cast<int2 *>(m + M.korder) : nullptr;
+  if (a->cu_seqlens) {
+    p.seg_q = p.seg_k = reinterpret_cast<int *>(m + M.seg);
+    if (a->cu_seqlens_k) {
+      p.seg_k = reinterpret_cast<int *>(m + M.segk);
+      p.qoff = reinterpret_cast<int *>(m + M.qoff);
+      p.koff = reinterpret_cast<int *>(m + M.koff);
+    }
+  } else {
+    p.seg_q = a->seg_q;
+    p.seg_k = a->seg_k;
+  }
 }
 
 Params make_params(const attn_args *a, char *ws, const Layout &L) {
@@ -138,22 +197,7 @@ Params make_params(const attn_args *a, char *ws, const Layout &L) {
   p.sink = a->sink;
   p.off_by_one = a->softmax_type == ATTN_SOFTMAX_OFF_BY_ONE ? 1 : 0;
   p.status = reinterpret_cast<unsigned *>(ws);
-  if (a->seg_q || a->cu_seqlens) {
-    p.seg_mono = reinterpret_cast<unsigned char *>(ws + L.mono);
-    p.qrange = reinterpret_cast<int2 *>(ws + L.qrange);
-    p.krange = reinterpret_cast<int2 *>(ws + L.krange);
-    if (a->cu_seqlens) {
-      p.seg_q = p.seg_k = reinterpret_cast<int *>(ws + L.seg);
-      if (a->cu_seqlens_k) {
-        p.seg_k = reinterpret_cast<int *>(ws + L.segk);
-        p.qoff = reinterpret_cast<int *>(ws + L.qoff);
-        p.koff = reinterpret_cast<int *>(ws + L.koff);
-      }
-    } else {
-      p.seg_q = a->seg_q;
-      p.seg_k = a->seg_k;
-    }
-  }
+  if (needs_meta(a)) set_meta(a, a->meta ? static_cast<char *>(const_cast<void *>(a->meta)) : ws + L.meta, p);
   return p;
 }
 
@@ -175,12 +219,26 @@ struct MainKernelEvents {
   }
 };
 
-int run_meta(const attn_args *a, Params &p, cudaStream_t st) {
-  if (!(a->seg_q || a->cu_seqlens) || a->B == 0) return ATTN_OK;
-  return cuda_status(launch_mask_meta(p, a->cu_seqlens, a->cu_seqlens_k, a->nseq, const_cast<int *>(p.seg_q),
-                                      const_cast<int *>(p.seg_k), const_cast<int *>(p.qoff),
-                                      const_cast<int *>(p.koff), const_cast<int2 *>(p.qrange),
-                                      const_cast<int2 *>(p.krange), const_cast<unsigned char *>(p.seg_mono), st));
+// Builds the metadata that p points at (K1), unless the caller passed metadata built before.
+int run_meta(const attn_args *a, const Params &p, cudaStream_t st, bool standalone = false) {
+  if (!needs_meta(a) || (a->meta && !standalone)) return ATTN_OK;
+  const MetaLayout M = meta_layout(a);
+  char *m = reinterpret_cast<char *>(const_cast<unsigned char *>(p.seg_mono)) - M.mono;
+  MetaOut o;
+  o.seg_q = a->cu_seqlens ? const_cast<int *>(p.seg_q) : nullptr;
+  o.seg_k = a->cu_seqlens_k ? const_cast<int *>(p.seg_k) : nullptr;
+  o.qoff = const_cast<int *>(p.qoff);
+  o.koff = const_cast<int *>(p.koff);
+  o.qrange = const_cast<int2 *>(p.qrange);
+  o.krange = const_cast<int2 *>(p.krange);
+  o.mono = const_cast<unsigned char *>(p.seg_mono);
+  o.qtile = const_cast<int4 *>(p.qtile);
+  o.ktile = const_cast<int4 *>(p.ktile);
+  o.qwork = reinterpret_cast<long long *>(m + M.qwork);
+  o.kwork = reinterpret_cast<long long *>(m + M.kwork);
+  o.qorder = const_cast<int2 *>(p.qorder);
+  o.korder = const_cast<int2 *>(p.korder);
+  return cuda_status(launch_mask_meta(p, a->cu_seqlens, a->cu_seqlens_k, a->nseq, o, st));
 }
 
 }  // namespace
@@ -206,6 +264,29 @@ extern "C" {
 size_t attn_fwd_workspace_size(const attn_args *a) {
   if (validate(a) != ATTN_OK) return 0;
   return layout(a, false).total;
+}
+
+size_t attn_meta_size(const attn_args *a) {
+  if (validate(a) != ATTN_OK) return 0;
+  return meta_layout(a).total;
+}
+
+int attn_meta_build(const attn_args *a, void *meta, size_t meta_bytes, attn_stream_t stream) {
+  const int s = validate(a);
+  if (s != ATTN_OK) return s;
+  const MetaLayout M = meta_layout(a);
+  if (M.total == 0) return ATTN_OK;  // nothing to build
+  if (!meta || meta_bytes < M.total || ((uintptr_t)meta % kAlign) != 0) return ATTN_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Params p;
+  memset(&p, 0, sizeof(p));
+  p.B = a->B; p.Sq = a->Sq; p.Sk = a->Sk;
+  p.causal = a->causal ? 1 : 0;
+  p.window = a->window > 0 ? a->window : 0;
+  p.status = static_cast<unsigned *>(meta);  // this buffer's own status area
+  set_meta(a, static_cast<char *>(meta), p);
+  if (cudaMemsetAsync(meta, 0, kAlign, st) != cudaSuccess) return ATTN_ERR_CUDA;
+  return run_meta(a, p, st, true);
 }
 
 size_t attn_bwd_workspace_size(const attn_args *a) {

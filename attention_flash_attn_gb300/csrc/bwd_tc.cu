@@ -354,10 +354,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (misc_i[12]) return;
   }
 
-  // One-dimensional grid, key tile slowest: the early key tiles, which see the most queries
-  // under causal masks, start before any later tile, so the last wave holds the light ones.
-  const int gb = (int)(blockIdx.x % (unsigned)(p.Hkv * p.B));
-  const int kt = (int)(blockIdx.x / (unsigned)(p.Hkv * p.B)), g = gb % p.Hkv, b = gb / p.Hkv;
+  // One-dimensional grid, heaviest tiles first so that the last wave holds the light ones.
+  // With segments the order is the mask metadata's longest-first work list of (batch, key
+  // tile) pairs, every kv head of a pair adjacent; otherwise the key tile varies slowest,
+  // earliest (seen by the most queries under causal masks) first.
+  const int nkt = (p.Sk + kBK - 1) / kBK;
+  int kt, g, b;
+  if (p.korder) {
+    const int2 o = p.korder[blockIdx.x / (unsigned)p.Hkv];
+    b = o.x;
+    kt = o.y;
+    g = (int)(blockIdx.x % (unsigned)p.Hkv);
+  } else {
+    const int gb = (int)(blockIdx.x % (unsigned)(p.Hkv * p.B));
+    kt = (int)(blockIdx.x / (unsigned)(p.Hkv * p.B));
+    g = gb % p.Hkv;
+    b = gb / p.Hkv;
+  }
   const int k0 = kt * kBK, k1 = min(k0 + kBK, p.Sk) - 1;
   const int off = p.Sk - p.Sq;
 
@@ -367,11 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.causal) qlo = max(qlo, k0 - off);
     if (p.window > 0) qhi = min(qhi, k1 - off + p.window);
   }
-  if (p.krange) {
-    const int nt = (p.Sk + 63) / 64;
-    const int2 a = p.krange[(size_t)b * nt + k0 / 64], c = p.krange[(size_t)b * nt + k1 / 64];
-    qlo = max(qlo, min(a.x, c.x));
-    qhi = min(qhi, max(a.y, c.y));
+  if (p.ktile) {  // the tile's class bounds from the mask metadata
+    const int4 c = p.ktile[(size_t)b * nkt + kt];
+    qlo = max(qlo, c.x);
+    qhi = min(qhi, c.y);
   }
   const int s0 = qlo / BQ;
   const int nq = (qlo < qhi) ? (qhi + BQ - 1) / BQ - s0 : 0;  // query steps per head
@@ -525,17 +537,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       lo = p.Sq;
       hi = 0;
     }
-    if (half == 0) {
-      int mlo = __reduce_max_sync(0xffffffffu, lo);
-      int mhi = __reduce_min_sync(0xffffffffu, hi);
-      if (lane == 0) {
-        red[wq] = mlo;
-        red[4 + wq] = mhi;
+    // Queries that see every key of the tile, [cta_lo, cta_hi): query steps inside need no
+    // mask.  The mask metadata carries them (the tile class); otherwise the keys' intervals are
+    // intersected here.
+    int cta_lo, cta_hi;
+    if (p.ktile) {
+      const int4 c = p.ktile[(size_t)b * nkt + kt];
+      cta_lo = c.z;
+      cta_hi = c.w;
+    } else {
+      if (half == 0) {
+        int mlo = __reduce_max_sync(0xffffffffu, lo);
+        int mhi = __reduce_min_sync(0xffffffffu, hi);
+        if (lane == 0) {
+          red[wq] = mlo;
+          red[4 + wq] = mhi;
+        }
       }
+      named_bar<1, kSoftmaxThreads>();
+      cta_lo = max(max(red[0], red[1]), max(red[2], red[3]));
+      cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
     }
-    named_bar<1, kSoftmaxThreads>();
-    const int cta_lo = max(max(red[0], red[1]), max(red[2], red[3]));
-    const int cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
 
     const BwdScore ks(p.scale, p.inv_cap, p.cap);
@@ -1261,7 +1283,9 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const long long nblk = (long long)((p.Sk + kBK - 1) / kBK) * p.Hkv * p.B;
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<(unsigned)nblk, kThreads, C::SMEM, st>>>(tq, tk, tv, tdo, tdq, p);
+  Params q = p;
+  if (!follow_work_list(nblk)) q.korder = nullptr;
+  kern<<<(unsigned)nblk, kThreads, C::SMEM, st>>>(tq, tk, tv, tdo, tdq, q);
   return counted(cudaGetLastError());
 }
 

@@ -34,6 +34,16 @@ struct Params {
   const int2 *qrange;             // [B, ceil(Sq/64)]: key range [x, y) of each 64-row query tile
   const int2 *krange;             // [B, ceil(Sk/64)]: query range [x, y) of each 64-key tile
   const unsigned char *seg_mono;  // [B]: 1 if seg_q and seg_k rows are non-decreasing
+  // Tile classes (segment / cu_seqlens calls; null otherwise): per (b, 128-row query tile)
+  // {klo, khi, flo, fhi} -- the keys some row of the tile sees lie in [klo, khi), the keys every
+  // row sees in [flo, fhi) (empty when flo >= fhi; always empty with unsorted ids).  A key tile
+  // inside [flo, fhi) is FULL (no mask needed), one outside [klo, khi) EMPTY, any other PARTIAL.
+  // Per (b, 128-key tile) the same over the queries that see its keys.
+  const int4 *qtile, *ktile;
+  // Longest-first work lists: every (b, 128-row query tile) / (b, 128-key tile) once, as
+  // {b, tile}, in descending order of visible pairs (ties: lower index first); null when the
+  // call has no segments or more tiles than the sorter takes (the grid's own order then).
+  const int2 *qorder, *korder;
   // Varlen with separate key boundaries (B == 1): per token, the causal / window offset of its
   // sequence, end_k(s) - end_q(s) (bottom-right alignment within every sequence); null: the
   // whole matrix's Sk - Sq.

@@ -231,15 +231,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (misc_i[12]) return;
   }
 
-  // One-dimensional grid, query tile slowest: every (batch, head) takes its latest (heaviest
-  // under causal) tile before any takes an earlier one, so the last wave holds the light tiles.
-  // With a split-KV forward the split index varies fastest.
+  // One-dimensional grid, heaviest tiles first so that the last wave holds the light ones.
+  // With segments the order is the mask metadata's longest-first work list of (batch, query
+  // tile) pairs, every head of a pair adjacent; otherwise the query tile varies slowest,
+  // latest (heaviest under causal masks, equal under a window alone) first.  With a split-KV
+  // forward the split index varies fastest.
   const int nqt = (p.Sq + kBM - 1) / kBM;
   const int ns = p.kv_splits > 1 ? p.kv_splits : 1;
-  const int bhs = (int)(blockIdx.x % (unsigned)(p.Hq * p.B * ns));
-  const int qt = nqt - 1 - (int)(blockIdx.x / (unsigned)(p.Hq * p.B * ns));
-  const int split = bhs % ns, bh = bhs / ns;
-  const int h = bh % p.Hq, b = bh / p.Hq, g = h / p.G;
+  int qt, b, h, split;
+  if (p.qorder) {
+    const int2 o = p.qorder[blockIdx.x / (unsigned)(p.Hq * ns)];
+    const int hs = (int)(blockIdx.x % (unsigned)(p.Hq * ns));
+    b = o.x;
+    qt = o.y;
+    h = hs / ns;
+    split = hs % ns;
+  } else {
+    const int bhs = (int)(blockIdx.x % (unsigned)(p.Hq * p.B * ns));
+    qt = nqt - 1 - (int)(blockIdx.x / (unsigned)(p.Hq * p.B * ns));
+    split = bhs % ns;
+    const int bh = bhs / ns;
+    h = bh % p.Hq;
+    b = bh / p.Hq;
+  }
+  const int g = h / p.G;
   const int i0 = qt * kBM, i1 = min(i0 + kBM, p.Sq) - 1;
   const int off = p.Sk - p.Sq;
 
@@ -249,11 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.window > 0) klo = max(klo, i0 + off - p.window + 1);
     if (p.causal) khi = min(khi, i1 + off + 1);
   }
-  if (p.qrange) {
-    const int nt = (p.Sq + 63) / 64;
-    const int2 a = p.qrange[(size_t)b * nt + i0 / 64], c = p.qrange[(size_t)b * nt + i1 / 64];
-    klo = max(klo, min(a.x, c.x));
-    khi = min(khi, max(a.y, c.y));
+  if (p.qtile) {  // the tile's class bounds from the mask metadata
+    const int4 c = p.qtile[(size_t)b * nqt + qt];
+    klo = max(klo, c.x);
+    khi = min(khi, c.y);
   }
   const int tv0 = klo / BN;
   const int nv = (klo < khi) ? (khi + BN - 1) / BN - tv0 : 0;
@@ -471,17 +485,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       lo = 0;
       hi = p.Sk;
     }
-    if (half == 0) {
-      int mlo = __reduce_max_sync(0xffffffffu, lo);
-      int mhi = __reduce_min_sync(0xffffffffu, hi);
-      if (lane == 0) {
-        red[wq] = mlo;
-        red[4 + wq] = mhi;
+    // Keys every row of the tile sees, [cta_lo, cta_hi): key tiles inside need no mask.  The
+    // mask metadata carries them (the tile class); otherwise the rows' intervals are
+    // intersected here.
+    int cta_lo, cta_hi;
+    if (p.qtile) {
+      const int4 c = p.qtile[(size_t)b * nqt + qt];
+      cta_lo = c.z;
+      cta_hi = c.w;
+    } else {
+      if (half == 0) {
+        int mlo = __reduce_max_sync(0xffffffffu, lo);
+        int mhi = __reduce_min_sync(0xffffffffu, hi);
+        if (lane == 0) {
+          red[wq] = mlo;
+          red[4 + wq] = mhi;
+        }
       }
+      asm volatile("barrier.sync 1, 256;" ::: "memory");
+      cta_lo = max(max(red[0], red[1]), max(red[2], red[3]));
+      cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
     }
-    asm volatile("barrier.sync 1, 256;" ::: "memory");
-    const int cta_lo = max(max(red[0], red[1]), max(red[2], red[3]));
-    const int cta_hi = min(min(red[4], red[5]), min(red[6], red[7]));
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
 
     const FwdScore ks(p.scale, p.inv_cap, p.cap);
@@ -690,7 +714,9 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const long long nblk = (long long)((p.Sq + kBM - 1) / kBM) * p.Hq * p.B * (p.kv_splits > 1 ? p.kv_splits : 1);
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<(unsigned)nblk, kThreads, C::SMEM, st>>>(tq, tk, tv, p);
+  Params q = p;
+  if (!follow_work_list(nblk)) q.qorder = nullptr;
+  kern<<<(unsigned)nblk, kThreads, C::SMEM, st>>>(tq, tk, tv, q);
   return counted(cudaGetLastError());
 }
 

@@ -147,7 +147,35 @@ typedef struct {
      * quoted on tokamax PR #1121: packing lowered to per-segment q / kv seqlens and offsets).
      * Requires cu_seqlens; Sq == Sk is then not required.  NULL: the keys share cu_seqlens.  */
     const int32_t *cu_seqlens_k;
+    /* Optional mask metadata built by attn_meta_build for these same arguments (same shapes,
+     * masks and segment / cu_seqlens arrays -- the library cannot check this), 256-byte
+     * aligned.  With segments or cu_seqlens, attn_fwd and attn_bwd then read it instead of
+     * building it in their workspaces (whose size query shrinks accordingly): build it once per
+     * step and pass it to both.  NULL: each call builds its own.  Ignored without segments.  */
+    const void *meta;
 } attn_args;
+
+/*
+ * Mask metadata (segment ids or cu_seqlens; MaxText commit message quoted on tokamax PR #1121:
+ * packing with segment ids lowered to per-segment boundaries, run starts per row, boundaries
+ * not aligned to tiles).  For each batch row: the effective segment ids (from cu_seqlens), the
+ * per-token bottom-right offsets (cu_seqlens_k), whether the ids are sorted, the key range of
+ * every 64-row query tile and the query range of every 64-key tile; for every 128-row query
+ * tile and 128-key tile its class bounds (the keys some row sees, the keys every row sees:
+ * FULL / PARTIAL / EMPTY key tiles) and its visible pairs; and, with at most 4096 tiles per
+ * axis, the longest-first work lists (tiles in descending order of visible pairs) that the
+ * tensor-core grids follow.
+ *
+ * attn_meta_size: bytes of the metadata buffer (256-byte multiple), or 0 when the arguments
+ * need none (no segments / cu_seqlens, B == 0) or are invalid.
+ * attn_meta_build: builds it into `meta` (256-byte aligned, at least attn_meta_size bytes),
+ * asynchronously on `stream`; pass the buffer as args->meta to attn_fwd and attn_bwd.  The
+ * buffer's first 256 bytes are its own status area, cleared by each build: a malformed
+ * cu_seqlens / cu_seqlens_k is recorded there (read with attn_check_device_status(meta,
+ * stream)).  Returns an attn_status; ATTN_OK without launching when nothing is needed.
+ */
+size_t attn_meta_size(const attn_args *a);
+int attn_meta_build(const attn_args *a, void *meta, size_t meta_bytes, attn_stream_t stream);
 
 /* Bytes of workspace attn_fwd needs for these arguments (256-byte multiple, >= 256). */
 size_t attn_fwd_workspace_size(const attn_args *a);

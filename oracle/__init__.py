@@ -19,4 +19,6 @@ from .oracle import (  # noqa: F401
     capped,
     cap_factor,
     visible,
+    row_visible,
+    col_visible,
 )

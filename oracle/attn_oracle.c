@@ -338,6 +338,37 @@ long long oracle_count_visible(const oracle_problem *p, int b) {
     return n;
 }
 
+/* Visible keys of query row i of batch b (the mask definition, key by key): how many, and the
+ * first and last of them (-1 when none).  Used to check the GPU's per-tile mask metadata. */
+void oracle_row_visible(const oracle_problem *p, int b, int i, long long *count, int *first, int *last) {
+    long long n = 0;
+    int f = -1, l = -1;
+    for (int j = 0; j < p->Sk; ++j) {
+        if (!oracle_visible(p, b, i, j)) continue;
+        if (f < 0) f = j;
+        l = j;
+        ++n;
+    }
+    *count = n;
+    *first = f;
+    *last = l;
+}
+
+/* The same for key j: the queries that see it. */
+void oracle_col_visible(const oracle_problem *p, int b, int j, long long *count, int *first, int *last) {
+    long long n = 0;
+    int f = -1, l = -1;
+    for (int i = 0; i < p->Sq; ++i) {
+        if (!oracle_visible(p, b, i, j)) continue;
+        if (f < 0) f = i;
+        l = i;
+        ++n;
+    }
+    *count = n;
+    *first = f;
+    *last = l;
+}
+
 /* Capped logit and its derivative factor, exposed for the pins. */
 double oracle_capped(const oracle_problem *p, double u) { return capped(p, u); }
 double oracle_cap_factor(const oracle_problem *p, double u) { return cap_factor(p, u); }

@@ -56,6 +56,9 @@ def _load():
         lib.oracle_count_visible.argtypes = [P, ctypes.c_int]
         lib.oracle_count_visible.restype = ctypes.c_longlong
         lib.oracle_visible.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        ll, ip = ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(ctypes.c_int)
+        lib.oracle_row_visible.argtypes = [P, ctypes.c_int, ctypes.c_int, ll, ip, ip]
+        lib.oracle_col_visible.argtypes = [P, ctypes.c_int, ctypes.c_int, ll, ip, ip]
         lib.oracle_capped.argtypes = [P, ctypes.c_double]
         lib.oracle_capped.restype = ctypes.c_double
         lib.oracle_cap_factor.argtypes = [P, ctypes.c_double]
@@ -212,3 +215,28 @@ def cap_factor(p: Problem, u: float) -> float:
     lib = _load()
     c = p._c()
     return lib.oracle_cap_factor(ctypes.byref(c), float(u))
+
+
+def _extents(p: Problem, fn, n):
+    lib = _load()
+    c = p._c()
+    count = np.zeros((p.B, n), np.int64)
+    first = np.zeros((p.B, n), np.int64)
+    last = np.zeros((p.B, n), np.int64)
+    cn, cf, cl = ctypes.c_longlong(), ctypes.c_int(), ctypes.c_int()
+    f = getattr(lib, fn)
+    for b in range(p.B):
+        for x in range(n):
+            f(ctypes.byref(c), b, x, ctypes.byref(cn), ctypes.byref(cf), ctypes.byref(cl))
+            count[b, x], first[b, x], last[b, x] = cn.value, cf.value, cl.value
+    return count, first, last
+
+
+def row_visible(p: Problem):
+    """Per query row: (number of visible keys, first, last) as [B, Sq] arrays (-1: none)."""
+    return _extents(p, "oracle_row_visible", p.Sq)
+
+
+def col_visible(p: Problem):
+    """Per key: (number of queries that see it, first, last) as [B, Sk] arrays (-1: none)."""
+    return _extents(p, "oracle_col_visible", p.Sk)

@@ -467,6 +467,33 @@ def test_bottom_right_alignment_equals_square_problem(causal, window):
                                rtol=0, atol=1e-15)
 
 
+def test_row_and_column_extents_brute_force():
+    """Per-row and per-key visible counts and extents: equal to enumerating oracle.visible pair
+    by pair on tiny shapes (causal + window + sorted and unsorted segments, Sq != Sk), and the
+    counts sum to count_visible (pinned by the closed forms above)."""
+    for Sq, Sk, causal, window, seg_kind in [(9, 9, True, 4, "runs"), (7, 11, True, 3, None),
+                                             (11, 6, False, 2, None), (10, 10, True, 0, "interleaved")]:
+        z = np.zeros
+        kw = dict(scale=1.0, causal=causal, window=window)
+        if seg_kind == "runs":
+            kw["seg_q"] = kw["seg_k"] = np.array([[0, 0, 0, 1, 1, 2, 2, 2, 2]], np.int32)
+        elif seg_kind == "interleaved":
+            kw["seg_q"] = kw["seg_k"] = (np.arange(Sq, dtype=np.int32) % 3)[None]
+        p = Problem(z((1, Sq, 1, 1)), z((1, Sk, 1, 1)), z((1, Sk, 1, 1)), **kw)
+        vis = np.array([[oracle.visible(p, 0, i, j) for j in range(Sk)] for i in range(Sq)])
+        rc, rf, rl = oracle.row_visible(p)
+        cc, cf, cl = oracle.col_visible(p)
+        for i in range(Sq):
+            js = np.flatnonzero(vis[i])
+            assert rc[0, i] == len(js)
+            assert (rf[0, i], rl[0, i]) == ((js[0], js[-1]) if len(js) else (-1, -1))
+        for j in range(Sk):
+            is_ = np.flatnonzero(vis[:, j])
+            assert cc[0, j] == len(is_)
+            assert (cf[0, j], cl[0, j]) == ((is_[0], is_[-1]) if len(is_) else (-1, -1))
+        assert rc.sum() == cc.sum() == oracle.count_visible(p)
+
+
 def test_bias_gradient_follows_bias_broadcast_shape():
     """dbias has the bias's own shape: broadcast over batch it is the sum of the per-batch
     gradients; broadcast over heads, the sum over heads."""
