@@ -41,8 +41,8 @@ bool use_tc(const attn_args *a) { return a->dtype == ATTN_DTYPE_BF16 && a->Sk > 
 bool use_tc_bwd(const attn_args *a) { return use_tc(a) && tc_bwd_supported(a->D); }
 
 constexpr int kMaxKvSplits = 64;
-// The split-KV forward applies to the tensor-core path only.
-bool split_kv(const attn_args *a) { return a->kv_splits > 1 && use_tc(a); }
+// The split-KV forward applies to the tensor-core path only, head dims up to 256.
+bool split_kv(const attn_args *a) { return a->kv_splits > 1 && use_tc(a) && a->D <= 256; }
 
 size_t dbias_elems(const attn_args *a) {
   if (!a->bias) return 0;

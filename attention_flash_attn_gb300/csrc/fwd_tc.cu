@@ -37,11 +37,19 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // tolerate P <= 2^8 before rescaling O
 
+// Wide form (NV == 0; head dim 512): S = Q K^T needs all of D, but O would take every TMEM
+// column, so each CTA produces one half of O (DV = D / 2 columns: the head-dim chunking above
+// 256 of the MaxText commit message quoted on tokamax PR #1121) and S is computed by both
+// halves' CTAs.  Q stays resident (128 KiB); K and V tiles stream through one ring of NK
+// 32 KiB slots, each slot two 64-column chunks of a 128-key tile (K: 4 slots per tile, V: the
+// CTA's half, 2 slots), loaded and consumed in the MMA warp's order.
 template <int D, int BN, int NK, int NV>
 struct FwdCfg {
+  static constexpr bool WIDE = NV == 0;
+  static constexpr int DV = WIDE ? D / 2 : D;           // O columns this CTA produces
   static constexpr int KCH = D / 64;
   static constexpr int Q_BYTES = kBM * D * 2;
-  static constexpr int KV_BYTES = BN * D * 2;
+  static constexpr int KV_BYTES = WIDE ? 2 * BN * 128 : BN * D * 2;  // wide: one ring slot
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = Q_BYTES;                 // NK-deep K ring (released after S)
   static constexpr int OFF_V = OFF_K + NK * KV_BYTES;   // NV-deep V ring (released after PV)
@@ -60,7 +68,8 @@ struct FwdCfg {
   static constexpr int TM_O = 2 * BN;
   static constexpr int TM_COLS = 512;
   static constexpr int HC = BN / 2;  // columns per softmax thread and tile
-  static_assert(2 * BN + D <= TM_COLS, "TMEM budget");
+  static_assert(2 * BN + DV <= TM_COLS, "TMEM budget");
+  static_assert(!WIDE || (BN == 128 && D % 128 == 0 && DV % 128 == 0), "wide form: 128-key tiles, 128-column slots");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(KV_BYTES % 1024 == 0 && Q_BYTES % 1024 == 0, "swizzle atoms must stay 1 KiB aligned");
   static_assert(HC % 32 == 0, "half rows are whole 32-column TMEM loads");
@@ -238,17 +247,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // forward the split index varies fastest.
   const int nqt = (p.Sq + kBM - 1) / kBM;
   const int ns = p.kv_splits > 1 ? p.kv_splits : 1;
+  // Wide form: the two CTAs of a (query tile, head) pair -- one per half of O -- are adjacent.
+  constexpr int NVH = C::WIDE ? 2 : 1;
+  const int vh = (int)(blockIdx.x % (unsigned)NVH);
+  const unsigned bx = blockIdx.x / (unsigned)NVH;
   int qt, b, h, split;
   if (p.qorder) {
-    const int2 o = p.qorder[blockIdx.x / (unsigned)(p.Hq * ns)];
-    const int hs = (int)(blockIdx.x % (unsigned)(p.Hq * ns));
+    const int2 o = p.qorder[bx / (unsigned)(p.Hq * ns)];
+    const int hs = (int)(bx % (unsigned)(p.Hq * ns));
     b = o.x;
     qt = o.y;
     h = hs / ns;
     split = hs % ns;
   } else {
-    const int bhs = (int)(blockIdx.x % (unsigned)(p.Hq * p.B * ns));
-    qt = nqt - 1 - (int)(blockIdx.x / (unsigned)(p.Hq * p.B * ns));
+    const int bhs = (int)(bx % (unsigned)(p.Hq * p.B * ns));
+    qt = nqt - 1 - (int)(bx / (unsigned)(p.Hq * p.B * ns));
     split = bhs % ns;
     const int bh = bhs / ns;
     h = bh % p.Hq;
@@ -318,7 +331,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0 && (tmem & 0xFFFFu) + C::TM_COLS > 512) set_status(p.status, kStatusBadTmemAlloc);
 
-  if (warp == 0) {
+  if (warp == 0 && C::WIDE) {
+    // ------------------------------------------------------------ TMA producer (wide form)
+    // Lane 0 loads Q, then every K and V slot in the order the MMA warp reads them: K_j for
+    // S_j, then V_{j-1} (this CTA's half of O) for PV_{j-1}.
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c)
+        tma_load_4d(sbase + C::OFF_Q + c * (kBM * 128), &tmQ, q_full, c * 64, i0, h, b);
+      int u = 0;  // ring uses so far
+      auto slot_load = [&](const CUtensorMap *tm, int d0, int row) -> bool {
+        const int s = u % NK;
+        if (u >= NK && !mbar_wait(k_empty(s), ((u / NK) - 1) & 1, p.status)) return false;
+        mbar_arrive_expect_tx(k_full(s), C::KV_BYTES);
+        tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES, tm, k_full(s), d0, row, g, b);
+        tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES + BN * 128, tm, k_full(s), d0 + 64, row, g, b);
+        ++u;
+        return true;
+      };
+      bool okp = true;
+      for (int j = 0; okp && j <= n; ++j) {
+        if (j < n)
+          for (int c2 = 0; okp && c2 < D / 128; ++c2) okp = slot_load(&tmK, c2 * 128, (t0 + j) * BN);
+        if (j >= 1)
+          for (int c2 = 0; okp && c2 < C::DV / 128; ++c2) okp = slot_load(&tmV, vh * C::DV + c2 * 128, (t0 + j - 1) * BN);
+      }
+    }
+  } else if (warp == 0) {
+    if constexpr (!C::WIDE) {
     // ------------------------------------------------------------ TMA producers
     // Lane 0 loads Q and the K ring, lane 1 the V ring: K slots free up as soon as their S
     // MMA is done, V slots only after PV, so the two rings advance independently.
@@ -375,7 +419,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    }
+  } else if (warp == 1 && C::WIDE) {
+    // ------------------------------------------------------------ MMA issuer (wide form)
+    // S_j from the four K slots of tile j (8 k-steps of 16 each, over 128 columns of D), then
+    // PV_{j-1}: one N = 128 MMA group per V slot into its 128 columns of O.
+    if (n > 0) {
+      constexpr uint32_t idS = idesc_bf16(kBM, BN, false, false);
+      constexpr uint32_t idO = idesc_bf16(kBM, 128, false, true);
+      const uint64_t dq0 = sw128_desc(sbase + C::OFF_Q, 16, 1024);
+      int u = 0;
+      bool ok = mbar_wait_warp(q_full, 0, p.status);
+      for (int j = 0; ok && j <= n; ++j) {
+        if (j < n) {
+          const uint32_t dS = tmem + (uint32_t)((j & 1) * BN);
+#pragma unroll 1
+          for (int c2 = 0; c2 < D / 128; ++c2, ++u) {
+            const int s = u % NK;
+            if (!mbar_wait_warp(k_full(s), (u / NK) & 1, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t qd = desc_at(dq0, (2 * c2) * (kBM * 128));
+            const uint64_t kd = sw128_desc(sbase + C::OFF_K + s * C::KV_BYTES, 16, 1024);
+#pragma unroll
+            for (int k8 = 0; k8 < 8; ++k8)
+              mma_ss_w(dS, desc_at(qd, (k8 >> 2) * (kBM * 128) + (k8 & 3) * 32),
+                       desc_at(kd, (k8 >> 2) * (BN * 128) + (k8 & 3) * 32), idS, (c2 | k8) != 0);
+            mma_commit_w(k_empty(s));
+          }
+          if (!ok) break;
+          mma_commit_w(s_full(j & 1));
+        }
+        if (j >= 1) {
+          const int jj = j - 1;
+          if (!mbar_wait_warp(p_full(jj & 1), (jj >> 1) & 1, p.status)) break;
+          const uint32_t pa = tmem + (uint32_t)((jj & 1) * BN);
+#pragma unroll 1
+          for (int c2 = 0; c2 < C::DV / 128; ++c2, ++u) {
+            const int s = u % NK;
+            if (!mbar_wait_warp(k_full(s), (u / NK) & 1, p.status)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t dv = sw128_desc(sbase + C::OFF_K + s * C::KV_BYTES, BN * 128, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts_w(tmem + C::TM_O + c2 * 128, pa + p_col<HC>(kk), desc_at(dv, kk * (16 * 128)), idO,
+                       (jj > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_w(k_empty(s));
+          }
+          if (!ok) break;
+          mma_commit_w(o_done);
+        }
+      }
+      if (FIXM) mma_commit_w(o_fin);
+    }
   } else if (warp == 1) {
+    if constexpr (!C::WIDE) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop with warp-uniform values; one elected lane issues each
     // MMA and commit.  Descriptors are built once and advanced by constant offsets.
@@ -454,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (FIXM) mma_commit_w(o_fin);  // the softmax warps skip the per-step o_done phases
+    }
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
@@ -608,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!FIXM && j >= 1 && __any_sync(0xffffffffu, resc)) {
         tc_fence_after();
 #pragma unroll 1
-        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
+        for (int c = half * (C::DV / 64); c < (half + 1) * (C::DV / 64); ++c) {
           uint32_t orr[32];
           tmem_ld32(lane_addr + C::TM_O + c * 32, orr);
           tmem_wait_ld();
@@ -661,9 +759,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (row_ok && half == 0) p.lse_part[prow] = lse;
     } else {
-      __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) + (((size_t)b * p.Sq + i) * p.Hq + h) * D;
+      __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) + (((size_t)b * p.Sq + i) * p.Hq + h) * D + vh * C::DV;
 #pragma unroll 1
-      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
+      for (int c = half * (C::DV / 64); c < (half + 1) * (C::DV / 64); ++c) {
         uint32_t orr[32];
         if (n > 0) {
           tmem_ld32(lane_addr + C::TM_O + c * 32, orr);
@@ -683,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int v = 0; v < 4; ++v) dst[v] = make_uint4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
         }
       }
-      if (row_ok && half == 0) p.LSE[((size_t)b * p.Hq + h) * p.Sq + i] = lse;
+      if (row_ok && half == 0 && vh == 0) p.LSE[((size_t)b * p.Hq + h) * p.Sq + i] = lse;
     }
   }
 
@@ -704,6 +802,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
       !make_tmap_bshd(&tk, p.k, D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, BN) ||
       !make_tmap_bshd(&tv, p.v, D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, C::HALF ? 64 : BN))
     return cudaErrorInvalidValue;
+  if (C::WIDE && p.kv_splits > 1) return cudaErrorInvalidValue;  // the split-KV forward is not built for it
   auto kern = p.bias ? (p.cap <= 0.f                 ? fwd_tc_kernel<D, BN, NK, NV, false, false, true>
                         : p.cap <= kFixedMaxCap ? fwd_tc_kernel<D, BN, NK, NV, true, true, true>
                                                 : fwd_tc_kernel<D, BN, NK, NV, true, false, true>)
@@ -712,7 +811,8 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
                                                 : fwd_tc_kernel<D, BN, NK, NV, true, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const long long nblk = (long long)((p.Sq + kBM - 1) / kBM) * p.Hq * p.B * (p.kv_splits > 1 ? p.kv_splits : 1);
+  const long long nblk =
+      (long long)((p.Sq + kBM - 1) / kBM) * p.Hq * p.B * (p.kv_splits > 1 ? p.kv_splits : 1) * (C::WIDE ? 2 : 1);
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidValue;
   Params q = p;
   if (!follow_work_list(nblk)) q.qorder = nullptr;
@@ -722,7 +822,7 @@ cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
 
 }  // namespace
 
-bool tc_supported(int D) { return D == 64 || D == 128 || D == 256; }
+bool tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 
 // Tiles: 128 keys per step throughout (N = 128 score MMAs run at the full tensor rate; N = 64
 // ones at two thirds of it).  Head dim 256 fills the 512 TMEM columns with two score buffers and
@@ -733,6 +833,7 @@ cudaError_t tc_forward(const Params &p, cudaStream_t st) {
     case 64: return launch_fwd<64, 128, 4, 4>(p, st);
     case 128: return launch_fwd<128, 128, 3, 2>(p, st);
     case 256: return launch_fwd<256, 128, 1, 1>(p, st);
+    case 512: return launch_fwd<512, 128, 2, 0>(p, st);  // wide form: two 32 KiB ring slots
     default: return cudaErrorInvalidValue;
   }
 }

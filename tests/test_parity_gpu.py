@@ -486,6 +486,38 @@ def test_bias_with_sink_dsink_gap():
     assert dsink_stored <= TOL["bf16"] and dsink_pure <= 1.5e-2
 
 
+# Head dim 512 on the tensor cores (the forward's wide form: each CTA one half of O, S over the
+# whole head dim, Q resident and K / V streamed through one ring): GQA, sink, window, cap
+# tracked and fixed, ragged Sq != Sk, bias and packed segments, off-by-one.
+WIDE = [
+    (Workload("wide_d512_gqa_sink_window", "bf16", B=2, Sq=300, Sk=300, Hq=4, Hkv=2, D=512, causal=True,
+              window=120, softcap=30.0, sink=True, q_std=2.0), {}),
+    (Workload("wide_d512_ragged_noncausal_cap60", "bf16", B=1, Sq=200, Sk=333, Hq=2, Hkv=1, D=512, causal=False,
+              softcap=60.0, q_std=2.0), {}),
+    (Workload("wide_d512_bias_segments_cap0", "bf16", B=2, Sq=400, Sk=400, Hq=2, Hkv=2, D=512, causal=True,
+              segments=True, run_lo=40, run_hi=200, bias=True, bias_dims="h"), {}),
+    (Workload("wide_d512_off_by_one", "bf16", B=1, Sq=260, Sk=260, Hq=2, Hkv=1, D=512, causal=True, softcap=20.0,
+              q_std=2.0), {"off_by_one": True}),
+]
+
+
+@pytest.mark.parametrize("w,extra", WIDE, ids=lambda x: x.name if hasattr(x, "name") else "")
+def test_head_dim_512_on_tensor_cores(w, extra):
+    import attention_flash_attn_gb300 as fa
+    inp = make_inputs(w)
+    t = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    name = fa.attn_path_name(t["q"], t["k"], t["v"], causal=w.causal, softcap=w.softcap, bias=t["bias"])
+    assert name.startswith("tc"), name
+    ref_inp = inp
+    if extra.get("off_by_one"):
+        ref_inp = dict(inp, sink=torch.zeros(w.Hq, dtype=torch.float32))
+    ref = full_oracle(w, ref_inp)
+    gpu = run_gpu(w, inp, **extra)
+    if extra.get("off_by_one"):
+        ref["dsink"] = None
+    check(w, gpu, ref)
+
+
 def test_bf16_without_bias_takes_the_tensor_core_path():
     import attention_flash_attn_gb300 as fa
     for w in SMALL[1:]:
