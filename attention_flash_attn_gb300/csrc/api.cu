@@ -32,13 +32,19 @@ struct MetaLayout {
 // Workspace carve-up.  Offsets are 0 when a region is absent.
 struct Layout {
   size_t meta = 0;  // the metadata region, when the call needs one and args->meta is NULL
-  size_t dvec = 0, lse2 = 0, dsplit = 0, dsink_part = 0, dqacc = 0, dbias_acc = 0;
+  size_t dvec = 0, lse2 = 0, dsplit = 0, dsink_part = 0, dqacc = 0, dbias_acc = 0, wide = 0;
   size_t o_part = 0, lse_part = 0;
   size_t total = 0;
 };
 
 bool use_tc(const attn_args *a) { return a->dtype == ATTN_DTYPE_BF16 && a->Sk > 0 && tc_supported(a->D); }
 bool use_tc_bwd(const attn_args *a) { return use_tc(a) && tc_bwd_supported(a->D); }
+// Head dim 512: the scores-plus-GEMMs backward, while its two scratch planes stay within 16 GiB
+// (longer rows fall back to the FFMA kernels).
+constexpr size_t kWideScratchMax = size_t(16) << 30;
+bool use_wide_bwd(const attn_args *a) {
+  return use_tc(a) && a->D == 512 && wide_bwd_scratch_bytes(a->B, a->Hq, a->Sq, a->Sk) <= kWideScratchMax;
+}
 
 constexpr int kMaxKvSplits = 64;
 // The split-KV forward applies to the tensor-core path only, head dims up to 256.
@@ -100,7 +106,7 @@ Layout layout(const attn_args *a, bool bwd) {
   if (bwd) {
     const size_t sq_pad = (size_t)(a->Sq + 127) / 128 * 128;
     L.dvec = off; off += align_up((size_t)a->B * a->Hq * sq_pad * sizeof(float));
-    if (use_tc_bwd(a)) { L.lse2 = off; off += align_up((size_t)a->B * a->Hq * sq_pad * sizeof(float)); }
+    if (use_tc_bwd(a) || use_wide_bwd(a)) { L.lse2 = off; off += align_up((size_t)a->B * a->Hq * sq_pad * sizeof(float)); }
     if (use_tc_bwd(a) && tc_bwd_fused(a->D)) { L.dsplit = off; off += align_up((size_t)a->B * a->Hq * sq_pad * 16); }
     if (a->sink) {
       L.dsink_part = off;
@@ -108,6 +114,7 @@ Layout layout(const attn_args *a, bool bwd) {
     }
     if (use_tc_bwd(a)) { L.dqacc = off; off += align_up((size_t)a->B * a->Sq * a->Hq * a->D * sizeof(float)); }
     if (a->bias) { L.dbias_acc = off; off += align_up(dbias_elems(a) * sizeof(float)); }
+    if (use_wide_bwd(a)) { L.wide = off; off += align_up(wide_bwd_scratch_bytes(a->B, a->Hq, a->Sq, a->Sk)); }
   }
   L.total = off;
   return L;
@@ -296,7 +303,7 @@ size_t attn_bwd_workspace_size(const attn_args *a) {
 
 const char *attn_path_name(const attn_args *a) {
   if (validate(a) != ATTN_OK) return "";
-  return use_tc(a) ? (use_tc_bwd(a) ? "tc" : "tc-fwd/simt-bwd") : "simt";
+  return use_tc(a) ? (use_tc_bwd(a) || use_wide_bwd(a) ? "tc" : "tc-fwd/simt-bwd") : "simt";
 }
 
 int attn_fwd(const attn_args *a, void *O, float *LSE, void *ws, size_t ws_bytes, attn_stream_t stream) {
@@ -354,9 +361,9 @@ int attn_bwd(const attn_args *a, const void *O, const float *LSE, const void *dO
   p.sq_pad = (a->Sq + 127) / 128 * 128;
   p.dsink_part = a->sink ? reinterpret_cast<float *>(w + L.dsink_part) : nullptr;
   p.n_part = bwd_pre_partials(a->B, a->Sq);
-  const bool tc = use_tc_bwd(a);
+  const bool tc = use_tc_bwd(a), wide = !tc && use_wide_bwd(a);
   p.dQacc = tc ? reinterpret_cast<float *>(w + L.dqacc) : nullptr;
-  p.lse2p = tc ? reinterpret_cast<float *>(w + L.lse2) : nullptr;
+  p.lse2p = tc || wide ? reinterpret_cast<float *>(w + L.lse2) : nullptr;
   p.dsplit = tc && tc_bwd_fused(a->D) ? reinterpret_cast<uint4 *>(w + L.dsplit) : nullptr;
   p.dbias_acc = a->bias ? reinterpret_cast<float *>(w + L.dbias_acc) : nullptr;
   if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
@@ -365,7 +372,7 @@ int attn_bwd(const attn_args *a, const void *O, const float *LSE, const void *dO
   if ((s = cuda_status(launch_bwd_pre(p, a->dtype, tc, st))) != ATTN_OK) return s;
   {
     MainKernelEvents ev(st);
-    cudaError_t e = tc ? tc_backward(p, st) : simt_backward(p, a->dtype, st);
+    cudaError_t e = tc ? tc_backward(p, st) : wide ? wide_backward(p, w + L.wide, st) : simt_backward(p, a->dtype, st);
     ev.done();
     if ((s = cuda_status(e)) != ATTN_OK) return s;
   }

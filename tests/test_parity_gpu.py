@@ -487,8 +487,9 @@ def test_bias_with_sink_dsink_gap():
 
 
 # Head dim 512 on the tensor cores (the forward's wide form: each CTA one half of O, S over the
-# whole head dim, Q resident and K / V streamed through one ring): GQA, sink, window, cap
-# tracked and fixed, ragged Sq != Sk, bias and packed segments, off-by-one.
+# whole head dim, Q resident and K / V streamed through one ring; the backward's scores kernel
+# and dV / dK / dQ GEMMs): GQA, sink, window, cap tracked and fixed, ragged Sq != Sk, bias and
+# packed segments, off-by-one.
 WIDE = [
     (Workload("wide_d512_gqa_sink_window", "bf16", B=2, Sq=300, Sk=300, Hq=4, Hkv=2, D=512, causal=True,
               window=120, softcap=30.0, sink=True, q_std=2.0), {}),
@@ -507,7 +508,7 @@ def test_head_dim_512_on_tensor_cores(w, extra):
     inp = make_inputs(w)
     t = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
     name = fa.attn_path_name(t["q"], t["k"], t["v"], causal=w.causal, softcap=w.softcap, bias=t["bias"])
-    assert name.startswith("tc"), name
+    assert name == "tc", name  # forward and backward on tcgen05
     ref_inp = inp
     if extra.get("off_by_one"):
         ref_inp = dict(inp, sink=torch.zeros(w.Hq, dtype=torch.float32))
