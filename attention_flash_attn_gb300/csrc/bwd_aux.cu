@@ -89,9 +89,10 @@ __device__ __forceinline__ uint4 neg_d_parts(float d) {
 // grid (ceil(Sq/64), B), block 256: warp w handles heads w, w+8, ...; rows in order, so the
 // per-(block, head) partial sums are deterministic.
 //
-// NC > 0 (a row is NC 16-byte chunks and NC divides 32): a warp covers 32 / NC rows per load,
-// one lane per chunk, and keeps kPreUnroll such loads in flight per lane before reducing each
-// row over its NC lanes.  NC == 0: any other row length, one row per warp at a time.
+// NC > 0 (a row is NC 16-byte chunks, NC dividing 32 or a multiple of it): a warp covers
+// 32 / NC rows per load, one lane per chunk (NC > 32: one row, NC / 32 chunks per lane), and
+// keeps kPreUnroll such loads in flight per lane before reducing each row over its lanes.
+// NC == 0: any other row length, one row per warp at a time.
 constexpr int kPreUnroll = 4;
 template <typename T, int NC>
 __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int zero_dqacc) {
@@ -105,26 +106,35 @@ __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int z
     float part = 0.f;
     const float sink = p.sink ? p.sink[h] : 0.f;
     if constexpr (NC > 0) {
-      constexpr int RPL = 32 / NC;  // rows per warp-wide load
-      const int sub = lane / NC, c = lane % NC;
+      // LPR lanes per row (NC > 32: the whole warp, CPL chunks per lane)
+      constexpr int LPR = NC > 32 ? 32 : NC, CPL = NC > 32 ? NC / 32 : 1;
+      constexpr int RPL = 32 / LPR;  // rows per warp-wide load
+      const int sub = lane / LPR, c = lane % LPR;
       for (int ib = i0; ib < i1; ib += RPL * kPreUnroll) {
-        uint4 xa[kPreUnroll], xb[kPreUnroll];
+        uint4 xa[kPreUnroll][CPL], xb[kPreUnroll][CPL];
 #pragma unroll
         for (int u = 0; u < kPreUnroll; ++u) {
           const int i = ib + u * RPL + sub;
-          if (i < i1) {
-            const size_t row = (((size_t)b * p.Sq + i) * p.Hq + h) * p.D + (size_t)c * per_chunk;
-            xa[u] = __ldg(reinterpret_cast<const uint4 *>(dO + row));
-            xb[u] = __ldg(reinterpret_cast<const uint4 *>(O + row));
-          } else {
-            xa[u] = xb[u] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int cp = 0; cp < CPL; ++cp) {
+            if (i < i1) {
+              const size_t row = (((size_t)b * p.Sq + i) * p.Hq + h) * p.D + (size_t)(c + cp * LPR) * per_chunk;
+              xa[u][cp] = __ldg(reinterpret_cast<const uint4 *>(dO + row));
+              xb[u][cp] = __ldg(reinterpret_cast<const uint4 *>(O + row));
+            } else {
+              xa[u][cp] = xb[u][cp] = make_uint4(0u, 0u, 0u, 0u);
+            }
           }
         }
         float s[kPreUnroll];
 #pragma unroll
-        for (int u = 0; u < kPreUnroll; ++u) s[u] = chunk_dot_raw<T>(xa[u], xb[u]);
+        for (int u = 0; u < kPreUnroll; ++u) {
+          s[u] = 0.f;
 #pragma unroll
-        for (int o = NC / 2; o > 0; o >>= 1) {
+          for (int cp = 0; cp < CPL; ++cp) s[u] += chunk_dot_raw<T>(xa[u][cp], xb[u][cp]);
+        }
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) {
 #pragma unroll
           for (int u = 0; u < kPreUnroll; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], o);
         }
@@ -142,10 +152,13 @@ __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int z
             if (p.sink) part = fmaf(expf(sink - lse), s[u], part);
           }
           if (zero_dqacc) {
-            float4 *z = reinterpret_cast<float4 *>(p.dQacc + (((size_t)b * p.Sq + i) * p.Hq + h) * p.D +
-                                                   (size_t)c * per_chunk);
 #pragma unroll
-            for (int v = 0; v < per_chunk / 4; ++v) z[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int cp = 0; cp < CPL; ++cp) {
+              float4 *z = reinterpret_cast<float4 *>(p.dQacc + (((size_t)b * p.Sq + i) * p.Hq + h) * p.D +
+                                                     (size_t)(c + cp * LPR) * per_chunk);
+#pragma unroll
+              for (int v = 0; v < per_chunk / 4; ++v) z[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
           }
         }
       }
@@ -239,6 +252,7 @@ cudaError_t launch_pre_t(const Params &p, bool zero_dqacc, cudaStream_t st) {
     case 8: bwd_pre_kernel<T, 8><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
     case 16: bwd_pre_kernel<T, 16><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
     case 32: bwd_pre_kernel<T, 32><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+    case 64: bwd_pre_kernel<T, 64><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
     default: bwd_pre_kernel<T, 0><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
   }
   return counted(cudaGetLastError());

@@ -7,15 +7,15 @@
 //
 //   scores kernel: one CTA per 128-row query tile of one (batch, query head).  Q stays in
 //     shared memory while S_j = Q K_j^T is formed for every visible 128-key tile j (K streamed
-//     through a ring of 32 KiB slots, each two 64-column chunks of the tile); the softmax warps
+//     through a ring of 16 KiB slots, each a 64-column chunk of the tile); the softmax warps
 //     write P = exp(t - LSE) and P f (f = 1 - tanh^2(u / cap), 1 without the cap) as bf16 into
 //     scratch [B, Hq, Sq_pad, Sk_pad].  Then dO replaces Q and dP_j = dO V_j^T is formed for the
 //     same tiles; dU = P f (dP - D) -- the gradient with respect to the pre-cap logits (tokamax
 //     PR #1121, PR body: the factor is applied before dK and dbias) -- overwrites P f, and is
 //     added into the dbias accumulator when there is a bias.
 //   GEMM kernel: dV = sum over the group's query heads of P^T dO, dK = scale sum dU^T Q,
-//     dQ = scale dU K -- one CTA per 128-row tile of the result, all 512 columns accumulated in
-//     TMEM, operands by TMA, the contraction running over the visible range only.
+//     dQ = scale dU K -- one CTA per 128-row tile and 256-column half of the result, accumulated
+//     in TMEM, operands by TMA, the contraction running over the visible range only.
 //
 // Work: 4 D flops per visible pair in the scores kernel (S, dP) and 6 D in the GEMMs (causal
 // masks skip the zero blocks; windows and segments are multiplied through as zeros), against
@@ -35,8 +35,8 @@ using namespace bwd_score;
 constexpr int kWD = 512;    // head dim
 constexpr int kBM = 128;    // query rows per scores CTA, result rows per GEMM CTA
 constexpr int kBN = 128;    // keys per tile
-constexpr int kNR = 2;      // ring slots of the scores kernel
-constexpr int kSlot = 2 * kBN * 128;   // 32 KiB: two 64-column chunks of a 128-row tile
+constexpr int kNR = 4;      // ring slots of the scores kernel
+constexpr int kSlot = kBN * 128;       // 16 KiB: one 64-column chunk of a 128-row tile
 constexpr int kQBytes = kBM * kWD * 2; // 128 KiB
 
 // ---------------------------------------------------------------------------- scores kernel
@@ -170,20 +170,19 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
         if (u >= kNR && !mbar_wait(r_empty(s), ((u / kNR) - 1) & 1, p.status)) return false;
         mbar_arrive_expect_tx(r_full(s), kSlot);
         tma_load_4d(sbase + C::OFF_R + s * kSlot, tm, r_full(s), d0, row, g, b);
-        tma_load_4d(sbase + C::OFF_R + s * kSlot + kBN * 128, tm, r_full(s), d0 + 64, row, g, b);
         ++u;
         return true;
       };
       bool okp = true;
       for (int j = 0; okp && j < n; ++j)
-        for (int c2 = 0; okp && c2 < kWD / 128; ++c2) okp = slot_load(&tmK, c2 * 128, (t0 + j) * kBN);
+        for (int c = 0; okp && c < kWD / 64; ++c) okp = slot_load(&tmK, c * 64, (t0 + j) * kBN);
       if (okp && mbar_wait(q_free, 0, p.status)) {
         mbar_arrive_expect_tx(do_full, kQBytes);
 #pragma unroll 1
         for (int c = 0; c < kWD / 64; ++c)
           tma_load_4d(sbase + C::OFF_Q + c * (kBM * 128), &tmdO, do_full, c * 64, i0, h, b);
         for (int j = 0; okp && j < n; ++j)
-          for (int c2 = 0; okp && c2 < kWD / 128; ++c2) okp = slot_load(&tmV, c2 * 128, (t0 + j) * kBN);
+          for (int c = 0; okp && c < kWD / 64; ++c) okp = slot_load(&tmV, c * 64, (t0 + j) * kBN);
       }
     }
   } else if (warp == 1) {
@@ -202,16 +201,14 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
         tc_fence_after();
         const uint32_t dS = tmem + (uint32_t)(x * kBN);
 #pragma unroll 1
-        for (int c2 = 0; c2 < kWD / 128; ++c2, ++u) {
+        for (int c = 0; c < kWD / 64; ++c, ++u) {
           const int s = u % kNR;
           if (!mbar_wait_warp(r_full(s), (u / kNR) & 1, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t qd = desc_at(dq0, (2 * c2) * (kBM * 128));
+          const uint64_t qd = desc_at(dq0, c * (kBM * 128));
           const uint64_t kd = sw128_desc(sbase + C::OFF_R + s * kSlot, 16, 1024);
 #pragma unroll
-          for (int k8 = 0; k8 < 8; ++k8)
-            mma_ss_w(dS, desc_at(qd, (k8 >> 2) * (kBM * 128) + (k8 & 3) * 32),
-                     desc_at(kd, (k8 >> 2) * (kBN * 128) + (k8 & 3) * 32), idS, (c2 | k8) != 0);
+          for (int k4 = 0; k4 < 4; ++k4) mma_ss_w(dS, desc_at(qd, k4 * 32), desc_at(kd, k4 * 32), idS, (c | k4) != 0);
           mma_commit_w(r_empty(s));
         }
         if (!ok) break;
@@ -376,8 +373,8 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
 
 // ---------------------------------------------------------------------------- GEMM kernel
 //
-// C[m, 0:512] = alpha sum_z sum_k A_z[m, k] B_z[k, 0:512] for one 128-row tile m0 .. m0 + 127,
-// in three forms:
+// C[m, n] = alpha sum_z sum_k A_z[m, k] B_z[k, n] for one 128-row tile m0 .. m0 + 127 and one
+// 256-column half of the head dim (two CTAs per row tile), in three forms:
 //   DV: m = key, k = query, z = the query heads of the kv group: A = P^T, B = dO;  alpha = 1
 //   DK: the same with A = dU^T, B = Q;                                            alpha = scale
 //   DQ: m = query, k = key, z = the query head itself: A = dU, B = K;             alpha = scale
@@ -387,9 +384,10 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
 enum { kGemmDV = 0, kGemmDK = 1, kGemmDQ = 2 };
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
 constexpr int kKStep = 64;
-constexpr int kABytes = kBM * kKStep * 2;   // 16 KiB
-constexpr int kBBytes = kKStep * kWD * 2;   // 64 KiB
-constexpr int kGStages = 2;
+constexpr int kNHalf = kWD / 2;               // result columns per CTA
+constexpr int kABytes = kBM * kKStep * 2;     // 16 KiB
+constexpr int kBBytes = kKStep * kNHalf * 2;  // 32 KiB
+constexpr int kGStages = 4;
 struct GemmCfg {
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = kGStages * kABytes;
@@ -416,8 +414,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     if (misc_i[12]) return;
   }
-  // Grid: (result tile, head or kv group, batch).
-  const int mt = blockIdx.x, hz = blockIdx.y, b = blockIdx.z;
+  // Grid: (result tile and column half, head or kv group, batch).
+  const int mt = blockIdx.x >> 1, nh = blockIdx.x & 1, hz = blockIdx.y, b = blockIdx.z;
   const int M = MODE == kGemmDQ ? p.Sq : p.Sk;
   const int m0 = mt * kBM, m1 = min(m0 + kBM, M) - 1;
   const int nz = MODE == kGemmDQ ? 1 : p.G;
@@ -453,14 +451,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), kNHalf);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (threadIdx.x == 0 && (tmem & 0xFFFFu) != 0) set_status(p.status, kStatusBadTmemAlloc);
+  if (threadIdx.x == 0 && (tmem & 0xFFFFu) + kNHalf > 512) set_status(p.status, kStatusBadTmemAlloc);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -478,16 +476,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // A = dU [queries m, keys k]: one box of 64 keys x 128 queries (K-major)
           tma_load_4d(a_dst, &tmA, f_full(s), k0, m0, hz, b);
 #pragma unroll
-          for (int c = 0; c < kWD / 64; ++c)  // B = K_g [keys k, d]
-            tma_load_4d(b_dst + c * (kKStep * 128), &tmB, f_full(s), c * 64, k0, hz / p.G, b);
+          for (int c = 0; c < kNHalf / 64; ++c)  // B = K_g [keys k, this half of d]
+            tma_load_4d(b_dst + c * (kKStep * 128), &tmB, f_full(s), nh * kNHalf + c * 64, k0, hz / p.G, b);
         } else {
           const int h = hz * p.G + z;
           // A = P^T or dU^T: two boxes of 64 keys (m) x 64 queries (k), keys contiguous (M-major)
           tma_load_4d(a_dst, &tmA, f_full(s), m0, k0, h, b);
           tma_load_4d(a_dst + kKStep * 128, &tmA, f_full(s), m0 + 64, k0, h, b);
 #pragma unroll
-          for (int c = 0; c < kWD / 64; ++c)  // B = dO_h or Q_h [queries k, d]
-            tma_load_4d(b_dst + c * (kKStep * 128), &tmB, f_full(s), c * 64, k0, h, b);
+          for (int c = 0; c < kNHalf / 64; ++c)  // B = dO_h or Q_h [queries k, this half of d]
+            tma_load_4d(b_dst + c * (kKStep * 128), &tmB, f_full(s), nh * kNHalf + c * 64, k0, h, b);
         }
       }
     }
@@ -503,12 +501,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                : sw128_desc(sbase + C::OFF_A + s * kABytes, 16, 1024);
       const uint64_t db = sw128_desc(sbase + C::OFF_B + s * kBBytes, kKStep * 128, 1024);
 #pragma unroll
-      for (int nh = 0; nh < 2; ++nh) {
-#pragma unroll
-        for (int k4 = 0; k4 < kKStep / 16; ++k4)
-          mma_ss_w(tmem + nh * 256, desc_at(da, A_MN ? k4 * 2048 : k4 * 32),
-                   desc_at(db, nh * 4 * (kKStep * 128) + k4 * 2048), idC, (it > 0 || k4 > 0) ? 1u : 0u);
-      }
+      for (int k4 = 0; k4 < kKStep / 16; ++k4)
+        mma_ss_w(tmem, desc_at(da, A_MN ? k4 * 2048 : k4 * 32), desc_at(db, k4 * 2048), idC,
+                 (it > 0 || k4 > 0) ? 1u : 0u);
       mma_commit_w(f_empty(s));
     }
     mma_commit_w(acc_full);  // every MMA of this CTA has completed (or none was issued)
@@ -523,9 +518,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     __nv_bfloat16 *dst = out + (MODE == kGemmDQ ? (((size_t)b * p.Sq + min(m, M - 1)) * p.Hq + hz) * kWD
-                                                : (((size_t)b * p.Sk + min(m, M - 1)) * p.Hkv + hz) * kWD);
+                                                : (((size_t)b * p.Sk + min(m, M - 1)) * p.Hkv + hz) * kWD) +
+                         nh * kNHalf;
 #pragma unroll 1
-    for (int c = 0; c < kWD / 32; ++c) {
+    for (int c = 0; c < kNHalf / 32; ++c) {
       uint32_t v[32];
       if (have && ok) {
         tmem_ld32(lane_addr + c * 32, v);
@@ -552,7 +548,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kNHalf);
   }
 }
 
@@ -563,7 +559,7 @@ cudaError_t launch_gemm(const Params &p, const CUtensorMap &ta, const CUtensorMa
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg::SMEM);
   if (e != cudaSuccess) return e;
   const int M = MODE == kGemmDQ ? p.Sq : p.Sk;
-  const dim3 grid((M + kBM - 1) / kBM, MODE == kGemmDQ ? p.Hq : p.Hkv, p.B);
+  const dim3 grid(2 * ((M + kBM - 1) / kBM), MODE == kGemmDQ ? p.Hq : p.Hkv, p.B);
   kern<<<grid, kGemmThreads, GemmCfg::SMEM, st>>>(ta, tb, p, out, alpha);
   return counted(cudaGetLastError());
 }
