@@ -49,7 +49,7 @@ def _stamp() -> str:
 
 # Sources that the backward main kernel's code depends on: a DRAM-traffic figure recorded by
 # ncu for that kernel stays valid while these files (and the flags) are unchanged.
-BWD_MAIN_SOURCES = ("bwd_tc.cu", "tc_common.cuh", "tc_host.cu", "common.cuh", "internal.h")
+BWD_MAIN_SOURCES = ("bwd_tc.cu", "bwd_score.cuh", "tc_common.cuh", "tc_host.cu", "common.cuh", "internal.h")
 
 
 def _code_only(text: str) -> str:

@@ -133,8 +133,8 @@ typedef struct {
      * exactly once per row (TransformerEngine PR #3551, "What changed": the sink enters each
      * row once when tiles' statistics are merged).  The workspace grows by
      * n * B * Hq * Sq * (D + 1) * 4 bytes.  Results equal the unsplit forward up to rounding.
-     * The FFMA path (fp32 inputs, or a bias) computes unsplit.  Other values:
-     * ATTN_ERR_INVALID.  The backward ignores this field.                                   */
+     * Head dim 512 and the FFMA path (fp32 inputs, other head dims) compute unsplit.  Other
+     * values: ATTN_ERR_INVALID.  The backward ignores this field.                           */
     int kv_splits;
     /* Optional key boundaries for cu_seqlens ("thd" varlen with Sq != Sk per sequence):
      * cu_seqlens_k [nseq+1] int32 with the same rules on the key axis (cu_seqlens_k[nseq] <=
