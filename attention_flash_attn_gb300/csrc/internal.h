@@ -48,6 +48,8 @@ int work_order_max_tiles();
 // in L2, and measured 5-13 % faster (packed rows, forward and backward; chunked prefill
 // backward).
 bool follow_work_list(long long nblk);
+// Streaming multiprocessors of the current device (cached per device; 1 if the query fails).
+int device_sm_count();
 
 // fp32 FFMA kernels (any dtype; used for fp32 inputs and calls with a bias).
 cudaError_t simt_forward(const Params &p, int dtype, cudaStream_t st);

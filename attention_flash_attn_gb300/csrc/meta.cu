@@ -314,16 +314,18 @@ cudaError_t launch_mask_meta(const Params &p, const int *cu_seqlens, const int *
 
 int work_order_max_tiles() { return kSortMax; }
 
-bool follow_work_list(long long nblk) {
+int device_sm_count() {
   static int sms[128] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return false;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 1;
   if (sms[dev] == 0) {
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return false;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
     sms[dev] = n;
   }
-  return nblk <= 4LL * sms[dev];
+  return sms[dev];
 }
+
+bool follow_work_list(long long nblk) { return nblk <= 4LL * device_sm_count(); }
 
 }  // namespace attn

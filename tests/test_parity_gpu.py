@@ -27,6 +27,11 @@ SMALL = [
     W["sink_gqa64_cap30"].replace(name="sink_small_cap30", B=2, Sq=520, Sk=520, Hq=8, Hkv=2),
     W["long_causal_32k_cap50"].replace(name="long_small_causal", Sq=900, Sk=900, Hq=2, Hkv=1),
     W["long_noncausal_16k_cap50"].replace(name="long_small_noncausal", Sq=650, Sk=650, Hq=2, Hkv=1),
+    # grids of at least two CTAs per SM, where the head-dim 64 / 128 forwards run two CTAs per SM
+    # on 64-key tiles (the cases above have fewer CTAs and run one per SM on 128-key tiles)
+    W["sink_gqa64_cap30"].replace(name="pair_grid_d64_sink_cap30", B=2, Sq=300, Sk=300, Hq=64, Hkv=8),
+    W["packed_varlen_cap30"].replace(name="pair_grid_d128_packed", B=4, Sq=300, Sk=300, Hq=32, Hkv=8, run_lo=30,
+                                     run_hi=150),
 ]
 
 
