@@ -86,8 +86,8 @@ __device__ __forceinline__ uint4 neg_d_parts(float d) {
                     (uint32_t)__bfloat16_as_ushort(lo), 0u, 0u);
 }
 
-// grid (ceil(Sq/64), B), block 256: warp w handles heads w, w+8, ...; rows in order, so the
-// per-(block, head) partial sums are deterministic.
+// grid (ceil(Sq/64), B, ceil(Hq/8)), block 256: warp w of z-block z handles head 8 z + w; rows
+// in order, so the per-(block, head) partial sums are deterministic.
 //
 // NC > 0 (a row is NC 16-byte chunks, NC dividing 32 or a multiple of it): a warp covers
 // 32 / NC rows per load, one lane per chunk (NC > 32: one row, NC / 32 chunks per lane), and
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int z
   constexpr int per_chunk = 16 / sizeof(T);
   const T *O = static_cast<const T *>(p.O);
   const T *dO = static_cast<const T *>(p.dO);
-  for (int h = warp; h < p.Hq; h += kPreWarps) {
+  for (int h = blockIdx.z * kPreWarps + warp; h < p.Hq && h < (int)(blockIdx.z + 1) * kPreWarps; h += kPreWarps) {
     float part = 0.f;
     const float sink = p.sink ? p.sink[h] : 0.f;
     if constexpr (NC > 0) {
@@ -245,7 +245,8 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(Params p, int convert_dq,
 
 template <typename T>
 cudaError_t launch_pre_t(const Params &p, bool zero_dqacc, cudaStream_t st) {
-  dim3 grid((p.Sq + kPreRows - 1) / kPreRows, p.B);
+  // z: groups of kPreWarps heads (one per warp), so that heads spread over the SMs too
+  dim3 grid((p.Sq + kPreRows - 1) / kPreRows, p.B, (p.Hq + kPreWarps - 1) / kPreWarps);
   const int nc = p.D * (int)sizeof(T) / 16;
   switch (nc) {
     case 4: bwd_pre_kernel<T, 4><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
