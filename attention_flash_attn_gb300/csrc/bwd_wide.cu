@@ -5,8 +5,9 @@
 // memory.  The backward is therefore done in two steps, both on tcgen05 (the chunked head-dim
 // accumulation above 256 named in the MaxText commit message quoted on tokamax PR #1121):
 //
-//   scores kernel: one CTA per 128-row query tile of one (batch, query head).  Q stays in
-//     shared memory while S_j = Q K_j^T is formed for every visible 128-key tile j (K streamed
+//   scores kernel: one CTA per 128-row query tile of one (batch, query head) and share of at
+//     most four of its visible 128-key tiles.  Q stays in shared memory while S_j = Q K_j^T is
+//     formed for each of those tiles j (K streamed
 //     through a ring of 16 KiB slots, each a 64-column chunk of the tile); the softmax warps
 //     write P = exp(t - LSE) and P f (f = 1 - tanh^2(u / cap), 1 without the cap) as bf16 into
 //     scratch [B, Hq, Sq_pad, Sk_pad].  Then dO replaces Q and dP_j = dO V_j^T is formed for the
@@ -51,6 +52,7 @@ struct ScoresCfg {
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 constexpr int kScoresThreads = 320;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 element-wise
+constexpr int kScoresChunk = 4;      // key tiles per scores CTA at most
 
 __device__ __forceinline__ int lower_bound_g(const int *a, int n, int x) {
   int lo = 0, hi = n;
@@ -99,10 +101,15 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
     if (misc_i[12]) return;
   }
 
-  // Grid: query tile slowest (latest, heaviest under causal masks, first), then batch, head.
+  // Grid: query tile slowest (latest, heaviest under causal masks, first), then batch, head, and
+  // the share of the visible key tiles (at most kScoresChunk each; P and dU of a pair depend on
+  // that pair alone, so the key range splits freely).
   const int nqt = (p.Sq + kBM - 1) / kBM;
-  const int bh = (int)(blockIdx.x % (unsigned)(p.Hq * p.B));
-  const int qt = nqt - 1 - (int)(blockIdx.x / (unsigned)(p.Hq * p.B));
+  const int nks = (p.Sk + kBN * kScoresChunk - 1) / (kBN * kScoresChunk);
+  const int ks = (int)(blockIdx.x % (unsigned)nks);
+  const unsigned bx = blockIdx.x / (unsigned)nks;
+  const int bh = (int)(bx % (unsigned)(p.Hq * p.B));
+  const int qt = nqt - 1 - (int)(bx / (unsigned)(p.Hq * p.B));
   const int h = bh % p.Hq, b = bh / p.Hq, g = h / p.G;
   const int i0 = qt * kBM, i1 = min(i0 + kBM, p.Sq) - 1;
   const int off = p.Sk - p.Sq;
@@ -118,8 +125,11 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
     klo = max(klo, c.x);
     khi = min(khi, c.y);
   }
-  const int t0 = klo / kBN;
-  const int n = (klo < khi) ? (khi + kBN - 1) / kBN - t0 : 0;
+  const int tv0 = klo / kBN;
+  const int nv = (klo < khi) ? (khi + kBN - 1) / kBN - tv0 : 0;
+  const int t0 = tv0 + ks * kScoresChunk;                     // this CTA's share of the tiles
+  const int n = max(0, min(nv - ks * kScoresChunk, kScoresChunk));
+  if (n == 0) return;  // nothing to write: the scratch was zeroed
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t q_full = bar0, do_full = bar0 + 8u, q_free = bar0 + 16u;
@@ -604,7 +614,8 @@ cudaError_t wide_backward(const Params &p, void *scratch, cudaStream_t st) {
                      : (p.cap > 0.f ? wide_scores_kernel<true, false> : wide_scores_kernel<false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ScoresCfg::SMEM);
   if (e != cudaSuccess) return e;
-  const long long nblk = (long long)((p.Sq + kBM - 1) / kBM) * p.Hq * p.B;
+  const long long nks = (p.Sk + kBN * kScoresChunk - 1) / (kBN * kScoresChunk);
+  const long long nblk = (long long)((p.Sq + kBM - 1) / kBM) * p.Hq * p.B * nks;
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<(unsigned)nblk, kScoresThreads, ScoresCfg::SMEM, st>>>(tq, tdo, tk, tv, p, w);
   if ((e = counted(cudaGetLastError())) != cudaSuccess) return e;
