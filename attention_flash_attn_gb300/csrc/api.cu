@@ -245,6 +245,11 @@ int run_meta(const attn_args *a, const Params &p, cudaStream_t st, bool standalo
   o.kwork = reinterpret_cast<long long *>(m + M.kwork);
   o.qorder = const_cast<int2 *>(p.qorder);
   o.korder = const_cast<int2 *>(p.korder);
+  // The lists are only read by grids that follow them (at most four waves): when neither the
+  // forward's nor the backward's grid would, the sort is left out.
+  const long long fwd_blk = (long long)((a->Sq + 127) / 128) * a->Hq * a->B;
+  const long long bwd_blk = (long long)((a->Sk + 127) / 128) * a->Hkv * a->B;
+  if (!follow_work_list(fwd_blk) && !follow_work_list(bwd_blk)) o.qorder = o.korder = nullptr;
   return cuda_status(launch_mask_meta(p, a->cu_seqlens, a->cu_seqlens_k, a->nseq, o, st));
 }
 

@@ -61,6 +61,18 @@ __global__ void __launch_bounds__(1024) meta_rows_kernel(Params p, const int *cu
                                                          int *seg_out, int *segk_out, int *qoff_out,
                                                          int *koff_out, unsigned char *mono) {
   const int b = blockIdx.x;
+  // The boundaries in shared memory when they fit: every token below searches them.
+  constexpr int kCuSmem = 4096;
+  __shared__ int cu_s[kCuSmem], cuk_s[kCuSmem];
+  if (cu && nseq + 1 <= kCuSmem) {
+    for (int x = threadIdx.x; x <= nseq; x += blockDim.x) {
+      cu_s[x] = cu[x];
+      if (cu_k) cuk_s[x] = cu_k[x];
+    }
+    __syncthreads();
+    cu = cu_s;
+    if (cu_k) cu_k = cuk_s;
+  }
   const int *sq, *sk;
   if (cu && cu_k) {
     // B == 1, separate query and key boundaries: ids per axis, and per token the bottom-right
@@ -131,59 +143,20 @@ __global__ void __launch_bounds__(256) meta_tiles_kernel(Params p, const int *cu
 
   const bool per_seq = cu && cu_k;
   const int off = p.Sk - p.Sq;
-  // Causal / window bounds of a 64-row tile: the union of its rows' intervals.  With one offset
-  // for the whole matrix the first / last row decide them; with per-sequence offsets every row
-  // of the tile is visited.
   const int n64 = (n_rows + 63) / 64;
-  const int u64 = blockIdx.x * blockDim.x + threadIdx.x;
-  if (u64 < n64) {
-    const int t = u64;
-    const int r0 = t * 64, r1 = min(r0 + 64, n_rows) - 1;
-    int lo = 0, hi = n_other;
-    if (sorted) {
-      lo = lower_bound_i(other, n_other, own[r0]);
-      hi = upper_bound_i(other, n_other, own[r1]);
-    }
-    if (qside) {
-      int cl = r0 + off - p.window + 1, ch = r1 + off + 1;  // window floor, causal ceiling
-      if (per_seq) {
-        cl = INT_MAX;
-        ch = INT_MIN;
-        for (int i = r0; i <= r1; ++i) {
-          cl = min(cl, i + qoff_out[i] - p.window + 1);
-          ch = max(ch, i + qoff_out[i] + 1);
-        }
-      }
-      if (p.causal) hi = min(hi, ch);
-      if (p.window > 0) lo = max(lo, cl);
-    } else {
-      int cl = r0 - off, ch = r1 - off + p.window;  // causal floor, window ceiling
-      if (per_seq) {
-        cl = INT_MAX;
-        ch = INT_MIN;
-        for (int j = r0; j <= r1; ++j) {
-          cl = min(cl, j - koff_out[j]);
-          ch = max(ch, j - koff_out[j] + p.window);
-        }
-      }
-      if (p.causal) lo = max(lo, cl);
-      if (p.window > 0) hi = min(hi, ch);
-    }
-    lo = max(lo, 0);
-    hi = min(hi, n_other);
-    (qside ? qrange : krange)[(size_t)b * n64 + t] = lo < hi ? make_int2(lo, hi) : make_int2(n_other, 0);
-  }
 
   // Tile classes and work of the 128-row query tiles (forward CTAs) and 128-key tiles
   // (backward CTAs), one warp per tile: every row's visible interval (causal / window bounds
   // at its offset, its segment's run when the ids are sorted), their union and intersection,
   // and the sum of their lengths -- the tile's visible pairs per head (an upper bound with
-  // unsorted ids, where the kernels test pairs one by one and no tile is FULL).
+  // unsorted ids, where the kernels test pairs one by one and no tile is FULL).  The unions of
+  // the two 64-row halves are the 64-granular ranges the FFMA kernels use.
   const int lane = threadIdx.x & 31;
   const int n128 = (n_rows + 127) / 128;
   const int tt = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (tt < n128) {
     int lo_min = INT_MAX, hi_max = INT_MIN, lo_max = INT_MIN, hi_min = INT_MAX;
+    int h_lo[2] = {INT_MAX, INT_MAX}, h_hi[2] = {INT_MIN, INT_MIN};  // per 64-row half
     long long work = 0;
     for (int r = tt * 128 + lane; r < min(tt * 128 + 128, n_rows); r += 32) {
       int lo, hi;
@@ -208,7 +181,19 @@ __global__ void __launch_bounds__(256) meta_tiles_kernel(Params p, const int *cu
         lo_min = min(lo_min, lo);
         hi_max = max(hi_max, hi);
         work += hi - lo;
+        const int hf = (r >> 6) & 1;
+        h_lo[hf] = min(h_lo[hf], lo);
+        h_hi[hf] = max(h_hi[hf], hi);
       }
+    }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      h_lo[hf] = __reduce_min_sync(0xffffffffu, h_lo[hf]);
+      h_hi[hf] = __reduce_max_sync(0xffffffffu, h_hi[hf]);
+      const int t64 = 2 * tt + hf;
+      if (lane == 0 && t64 < n64)
+        (qside ? qrange : krange)[(size_t)b * n64 + t64] =
+            h_lo[hf] < h_hi[hf] ? make_int2(h_lo[hf], h_hi[hf]) : make_int2(n_other, 0);
     }
     lo_min = __reduce_min_sync(0xffffffffu, lo_min);
     hi_max = __reduce_max_sync(0xffffffffu, hi_max);
