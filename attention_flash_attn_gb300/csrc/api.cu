@@ -39,11 +39,11 @@ struct Layout {
 
 bool use_tc(const attn_args *a) { return a->dtype == ATTN_DTYPE_BF16 && a->Sk > 0 && tc_supported(a->D); }
 bool use_tc_bwd(const attn_args *a) { return use_tc(a) && tc_bwd_supported(a->D); }
-// Head dim 512: the scores-plus-GEMMs backward, while its two scratch planes stay within 16 GiB
-// (longer rows fall back to the FFMA kernels).
+// Head dims 320 .. 512 (the wide form): the scores-plus-GEMMs backward, while its two scratch
+// planes stay within 16 GiB (longer rows fall back to the FFMA kernels).
 constexpr size_t kWideScratchMax = size_t(16) << 30;
 bool use_wide_bwd(const attn_args *a) {
-  return use_tc(a) && a->D == 512 && wide_bwd_scratch_bytes(a->B, a->Hq, a->Sq, a->Sk) <= kWideScratchMax;
+  return use_tc(a) && a->D > 256 && wide_bwd_scratch_bytes(a->B, a->Hq, a->Sq, a->Sk) <= kWideScratchMax;
 }
 
 constexpr int kMaxKvSplits = 64;

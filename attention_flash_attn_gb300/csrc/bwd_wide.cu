@@ -1,8 +1,8 @@
-// bwd_wide.cu -- tensor-core backward for bf16 with head dim 512.
+// bwd_wide.cu -- tensor-core backward for bf16 with head dims 320, 384, 448 and 512.
 //
-// At head dim 512 a CTA cannot hold the tensor-core backward's per-key-tile state: dK and dV
+// Above head dim 256 a CTA cannot hold the tensor-core backward's per-key-tile state: dK and dV
 // of a 128-key tile alone need 1024 fp32 TMEM columns, and K and V tiles 256 KiB of shared
-// memory.  The backward is therefore done in two steps, both on tcgen05 (the chunked head-dim
+// memory (at 512).  The backward is therefore done in two steps, both on tcgen05 (the chunked head-dim
 // accumulation above 256 named in the MaxText commit message quoted on tokamax PR #1121):
 //
 //   scores kernel: one CTA per 128-row query tile of one (batch, query head) and share of at
@@ -15,8 +15,12 @@
 //     PR #1121, PR body: the factor is applied before dK and dbias) -- overwrites P f, and is
 //     added into the dbias accumulator when there is a bias.
 //   GEMM kernel: dV = sum over the group's query heads of P^T dO, dK = scale sum dU^T Q,
-//     dQ = scale dU K -- one CTA per 128-row tile and 256-column half of the result, accumulated
+//     dQ = scale dU K -- one CTA per 128-row tile and part of the result's columns (of the
+//     D / 64 column chunks, the first CTA takes ceil(D / 128), the second the rest), accumulated
 //     in TMEM, operands by TMA, the contraction running over the visible range only.
+//
+// The head dim is read at run time in whole 64-column chunks; shared memory and TMEM are sized
+// for 512.
 //
 // Work: 4 D flops per visible pair in the scores kernel (S, dP) and 6 D in the GEMMs (causal
 // masks skip the zero blocks; windows and segments are multiplied through as zeros), against
@@ -33,12 +37,12 @@ namespace {
 using namespace tc;
 using namespace bwd_score;
 
-constexpr int kWD = 512;    // head dim
+constexpr int kWD = 512;    // largest head dim (shared memory and TMEM are sized for it)
 constexpr int kBM = 128;    // query rows per scores CTA, result rows per GEMM CTA
 constexpr int kBN = 128;    // keys per tile
 constexpr int kNR = 4;      // ring slots of the scores kernel
 constexpr int kSlot = kBN * 128;       // 16 KiB: one 64-column chunk of a 128-row tile
-constexpr int kQBytes = kBM * kWD * 2; // 128 KiB
+constexpr int kQBytes = kBM * kWD * 2; // 128 KiB at most
 
 // ---------------------------------------------------------------------------- scores kernel
 
@@ -113,6 +117,7 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
   const int h = bh % p.Hq, b = bh / p.Hq, g = h / p.G;
   const int i0 = qt * kBM, i1 = min(i0 + kBM, p.Sq) - 1;
   const int off = p.Sk - p.Sq;
+  const int nch = p.D / 64;  // 64-column chunks of the head dim
 
   // Keys this query tile can see (uniform across the CTA).
   int klo = 0, khi = p.Sk;
@@ -170,9 +175,9 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
     if (lane == 0 && n > 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      mbar_arrive_expect_tx(q_full, kQBytes);
+      mbar_arrive_expect_tx(q_full, nch * (kBM * 128));
 #pragma unroll 1
-      for (int c = 0; c < kWD / 64; ++c)
+      for (int c = 0; c < nch; ++c)
         tma_load_4d(sbase + C::OFF_Q + c * (kBM * 128), &tmQ, q_full, c * 64, i0, h, b);
       int u = 0;
       auto slot_load = [&](const CUtensorMap *tm, int d0, int row) -> bool {
@@ -185,14 +190,14 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
       };
       bool okp = true;
       for (int j = 0; okp && j < n; ++j)
-        for (int c = 0; okp && c < kWD / 64; ++c) okp = slot_load(&tmK, c * 64, (t0 + j) * kBN);
+        for (int c = 0; okp && c < nch; ++c) okp = slot_load(&tmK, c * 64, (t0 + j) * kBN);
       if (okp && mbar_wait(q_free, 0, p.status)) {
-        mbar_arrive_expect_tx(do_full, kQBytes);
+        mbar_arrive_expect_tx(do_full, nch * (kBM * 128));
 #pragma unroll 1
-        for (int c = 0; c < kWD / 64; ++c)
+        for (int c = 0; c < nch; ++c)
           tma_load_4d(sbase + C::OFF_Q + c * (kBM * 128), &tmdO, do_full, c * 64, i0, h, b);
         for (int j = 0; okp && j < n; ++j)
-          for (int c = 0; okp && c < kWD / 64; ++c) okp = slot_load(&tmV, c * 64, (t0 + j) * kBN);
+          for (int c = 0; okp && c < nch; ++c) okp = slot_load(&tmV, c * 64, (t0 + j) * kBN);
       }
     }
   } else if (warp == 1) {
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
         tc_fence_after();
         const uint32_t dS = tmem + (uint32_t)(x * kBN);
 #pragma unroll 1
-        for (int c = 0; c < kWD / 64; ++c, ++u) {
+        for (int c = 0; c < nch; ++c, ++u) {
           const int s = u % kNR;
           if (!mbar_wait_warp(r_full(s), (u / kNR) & 1, p.status)) { ok = false; break; }
           tc_fence_after();
@@ -384,7 +389,8 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
 // ---------------------------------------------------------------------------- GEMM kernel
 //
 // C[m, n] = alpha sum_z sum_k A_z[m, k] B_z[k, n] for one 128-row tile m0 .. m0 + 127 and one
-// 256-column half of the head dim (two CTAs per row tile), in three forms:
+// part of the head dim's columns (two CTAs per row tile; at most 256 columns each), in three
+// forms:
 //   DV: m = key, k = query, z = the query heads of the kv group: A = P^T, B = dO;  alpha = 1
 //   DK: the same with A = dU^T, B = Q;                                            alpha = scale
 //   DQ: m = query, k = key, z = the query head itself: A = dU, B = K;             alpha = scale
@@ -394,7 +400,7 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
 enum { kGemmDV = 0, kGemmDK = 1, kGemmDQ = 2 };
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
 constexpr int kKStep = 64;
-constexpr int kNHalf = kWD / 2;               // result columns per CTA
+constexpr int kNHalf = kWD / 2;               // result columns per CTA, at most
 constexpr int kABytes = kBM * kKStep * 2;     // 16 KiB
 constexpr int kBBytes = kKStep * kNHalf * 2;  // 32 KiB
 constexpr int kGStages = 4;
@@ -426,6 +432,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   // Grid: (result tile and column half, head or kv group, batch).
   const int mt = blockIdx.x >> 1, nh = blockIdx.x & 1, hz = blockIdx.y, b = blockIdx.z;
+  // This CTA's 64-column chunks of the result: nb of them from chunk cb.
+  const int nch = p.D / 64;
+  const int cb = nh == 0 ? 0 : (nch + 1) / 2, nb = nh == 0 ? (nch + 1) / 2 : nch / 2;
   const int M = MODE == kGemmDQ ? p.Sq : p.Sk;
   const int m0 = mt * kBM, m1 = min(m0 + kBM, M) - 1;
   const int nz = MODE == kGemmDQ ? 1 : p.G;
@@ -479,29 +488,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int z = it / nsteps, ks = s0 + it % nsteps;
         const int s = it % kGStages;
         if (it >= kGStages && !mbar_wait(f_empty(s), ((it / kGStages) - 1) & 1, p.status)) break;
-        mbar_arrive_expect_tx(f_full(s), kABytes + kBBytes);
+        mbar_arrive_expect_tx(f_full(s), kABytes + nb * (kKStep * 128));
         const uint32_t a_dst = sbase + C::OFF_A + s * kABytes, b_dst = sbase + C::OFF_B + s * kBBytes;
         const int k0 = ks * kKStep;
         if constexpr (MODE == kGemmDQ) {
           // A = dU [queries m, keys k]: one box of 64 keys x 128 queries (K-major)
           tma_load_4d(a_dst, &tmA, f_full(s), k0, m0, hz, b);
-#pragma unroll
-          for (int c = 0; c < kNHalf / 64; ++c)  // B = K_g [keys k, this half of d]
-            tma_load_4d(b_dst + c * (kKStep * 128), &tmB, f_full(s), nh * kNHalf + c * 64, k0, hz / p.G, b);
+#pragma unroll 1
+          for (int c = 0; c < nb; ++c)  // B = K_g [keys k, this CTA's columns of d]
+            tma_load_4d(b_dst + c * (kKStep * 128), &tmB, f_full(s), (cb + c) * 64, k0, hz / p.G, b);
         } else {
           const int h = hz * p.G + z;
           // A = P^T or dU^T: two boxes of 64 keys (m) x 64 queries (k), keys contiguous (M-major)
           tma_load_4d(a_dst, &tmA, f_full(s), m0, k0, h, b);
           tma_load_4d(a_dst + kKStep * 128, &tmA, f_full(s), m0 + 64, k0, h, b);
-#pragma unroll
-          for (int c = 0; c < kNHalf / 64; ++c)  // B = dO_h or Q_h [queries k, this half of d]
-            tma_load_4d(b_dst + c * (kKStep * 128), &tmB, f_full(s), nh * kNHalf + c * 64, k0, h, b);
+#pragma unroll 1
+          for (int c = 0; c < nb; ++c)  // B = dO_h or Q_h [queries k, this CTA's columns of d]
+            tma_load_4d(b_dst + c * (kKStep * 128), &tmB, f_full(s), (cb + c) * 64, k0, h, b);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idC = idesc_bf16(kBM, 256, A_MN, true);
+    const uint32_t idC = idesc_bf16(kBM, nb * 64, A_MN, true);
     bool ok = true;
     for (int it = 0; ok && it < total; ++it) {
       const int s = it % kGStages;
@@ -527,11 +536,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (have) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, p.status));
     tc_fence_after();
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-    __nv_bfloat16 *dst = out + (MODE == kGemmDQ ? (((size_t)b * p.Sq + min(m, M - 1)) * p.Hq + hz) * kWD
-                                                : (((size_t)b * p.Sk + min(m, M - 1)) * p.Hkv + hz) * kWD) +
-                         nh * kNHalf;
+    __nv_bfloat16 *dst = out + (MODE == kGemmDQ ? (((size_t)b * p.Sq + min(m, M - 1)) * p.Hq + hz) * p.D
+                                                : (((size_t)b * p.Sk + min(m, M - 1)) * p.Hkv + hz) * p.D) +
+                         cb * 64;
 #pragma unroll 1
-    for (int c = 0; c < kNHalf / 32; ++c) {
+    for (int c = 0; c < 2 * nb; ++c) {
       uint32_t v[32];
       if (have && ok) {
         tmem_ld32(lane_addr + c * 32, v);
@@ -582,7 +591,8 @@ size_t wide_bwd_scratch_bytes(int B, int Hq, int Sq, int Sk) {
 }
 
 cudaError_t wide_backward(const Params &p, void *scratch, cudaStream_t st) {
-  if (p.D != kWD || p.B > 65535 || p.Hq > 65535) return cudaErrorInvalidValue;
+  if (p.D % 64 != 0 || p.D <= 256 || p.D > kWD || p.B > 65535 || p.Hq > 65535) return cudaErrorInvalidValue;
+  const int D = p.D;
   WideScratch w;
   w.sq_pad = (p.Sq + 127) / 128 * 128;
   w.sk_pad = (p.Sk + 127) / 128 * 128;
@@ -594,21 +604,21 @@ cudaError_t wide_backward(const Params &p, void *scratch, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   CUtensorMap tq, tdo, tk, tv, tp, tu_mn, tu_k, tdo_b, tq_b, tk_b;
   const long long ss = w.sk_pad, sh = (long long)w.sq_pad * w.sk_pad, sb = sh * p.Hq;
-  if (!make_tmap_bshd(&tq, p.q, kWD, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, kBM) ||
-      !make_tmap_bshd(&tdo, p.dO, kWD, p.Sq, p.Hq, p.B, (long long)p.Hq * kWD, kWD, (long long)p.Sq * p.Hq * kWD,
+  if (!make_tmap_bshd(&tq, p.q, D, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, kBM) ||
+      !make_tmap_bshd(&tdo, p.dO, D, p.Sq, p.Hq, p.B, (long long)p.Hq * D, D, (long long)p.Sq * p.Hq * D,
                       kBM) ||
-      !make_tmap_bshd(&tk, p.k, kWD, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, kBN) ||
-      !make_tmap_bshd(&tv, p.v, kWD, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, kBN) ||
+      !make_tmap_bshd(&tk, p.k, D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, kBN) ||
+      !make_tmap_bshd(&tv, p.v, D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, kBN) ||
       // scratch planes as (key, query, head, batch): 64 x 64 boxes (M-major A of dV / dK) and
       // 64 keys x 128 queries (K-major A of dQ)
       !make_tmap_bshd(&tp, w.P, w.sk_pad, w.sq_pad, p.Hq, p.B, ss, sh, sb, kKStep) ||
       !make_tmap_bshd(&tu_mn, w.U, w.sk_pad, w.sq_pad, p.Hq, p.B, ss, sh, sb, kKStep) ||
       !make_tmap_bshd(&tu_k, w.U, w.sk_pad, w.sq_pad, p.Hq, p.B, ss, sh, sb, kBM) ||
       // B operands: 64-row boxes of dO, Q, K
-      !make_tmap_bshd(&tdo_b, p.dO, kWD, p.Sq, p.Hq, p.B, (long long)p.Hq * kWD, kWD, (long long)p.Sq * p.Hq * kWD,
+      !make_tmap_bshd(&tdo_b, p.dO, D, p.Sq, p.Hq, p.B, (long long)p.Hq * D, D, (long long)p.Sq * p.Hq * D,
                       kKStep) ||
-      !make_tmap_bshd(&tq_b, p.q, kWD, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, kKStep) ||
-      !make_tmap_bshd(&tk_b, p.k, kWD, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, kKStep))
+      !make_tmap_bshd(&tq_b, p.q, D, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, kKStep) ||
+      !make_tmap_bshd(&tk_b, p.k, D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, kKStep))
     return cudaErrorInvalidValue;
   auto kern = p.bias ? (p.cap > 0.f ? wide_scores_kernel<true, true> : wide_scores_kernel<false, true>)
                      : (p.cap > 0.f ? wide_scores_kernel<true, false> : wide_scores_kernel<false, false>);

@@ -1,4 +1,4 @@
-// fwd_tc.cu -- tcgen05 tensor-core forward for bf16, D in {64, 128, 256}.
+// fwd_tc.cu -- tcgen05 tensor-core forward for bf16, D in {64, 128, 256} and the wide form (320 .. 512).
 //
 // One CTA computes one 128-row query tile of one (batch, query head):
 //   warp 0      TMA producers: the Q tile once, then K tiles (lane 0) and V tiles (lane 1)
@@ -37,16 +37,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // tolerate P <= 2^8 before rescaling O
 
-// Wide form (NV == 0; head dim 512): S = Q K^T needs all of D, but O would take every TMEM
-// column, so each CTA produces one half of O (DV = D / 2 columns: the head-dim chunking above
-// 256 of the MaxText commit message quoted on tokamax PR #1121) and S is computed by both
-// halves' CTAs.  Q stays resident (128 KiB); K and V tiles stream through one ring of NK
-// 32 KiB slots, each slot two 64-column chunks of a 128-key tile (K: 4 slots per tile, V: the
-// CTA's half, 2 slots), loaded and consumed in the MMA warp's order.
+// Wide form (NV == 0; head dims 320, 384, 448 and 512, instantiated once with D = 512 as the
+// capacity and the head dim read at run time): S = Q K^T needs all of D, but O would take every
+// TMEM column, so each CTA produces one part of O -- the head-dim chunking above 256 of the
+// MaxText commit message quoted on tokamax PR #1121: of the D / 64 column chunks, the first
+// CTA of a pair takes the first ceil(D / 128), the second the rest -- and S is computed by both
+// CTAs.  Q stays resident (up to 128 KiB); K and V tiles stream through one ring of NK 32 KiB
+// slots, each slot two 64-column chunks of a 128-key tile (the last slot of an odd chunk count
+// holds one), loaded and consumed in the MMA warp's order.
 template <int D, int BN, int NK, int NV>
 struct FwdCfg {
   static constexpr bool WIDE = NV == 0;
-  static constexpr int DV = WIDE ? D / 2 : D;           // O columns this CTA produces
+  static constexpr int DV = WIDE ? D / 2 : D;           // O columns this CTA produces (wide: at most)
   static constexpr int KCH = D / 64;
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int KV_BYTES = WIDE ? 2 * BN * 128 : BN * D * 2;  // wide: one ring slot
@@ -273,6 +275,10 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D, BN, NK, NV>::MINB)
   const int g = h / p.G;
   const int i0 = qt * kBM, i1 = min(i0 + kBM, p.Sq) - 1;
   const int off = p.Sk - p.Sq;
+  // 64-column chunks of D that S runs over, and this CTA's chunks of O: vcn of them from vc0.
+  const int nch = C::WIDE ? p.D / 64 : C::KCH;
+  const int vc0 = (C::WIDE && vh == 1) ? (nch + 1) / 2 : 0;
+  const int vcn = C::WIDE ? (vh == 0 ? (nch + 1) / 2 : nch / 2) : C::DV / 64;
 
   // Keys this query tile can see (uniform across the CTA).
   int klo = 0, khi = p.Sk;
@@ -342,26 +348,27 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D, BN, NK, NV>::MINB)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-#pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
+      mbar_arrive_expect_tx(q_full, nch * (kBM * 128));
+#pragma unroll 1
+      for (int c = 0; c < nch; ++c)
         tma_load_4d(sbase + C::OFF_Q + c * (kBM * 128), &tmQ, q_full, c * 64, i0, h, b);
       int u = 0;  // ring uses so far
-      auto slot_load = [&](const CUtensorMap *tm, int d0, int row) -> bool {
+      // One slot: chunk c of `tm` (columns 64 c ..), and chunk c + 1 when `two`.
+      auto slot_load = [&](const CUtensorMap *tm, int c, int row, bool two) -> bool {
         const int s = u % NK;
         if (u >= NK && !mbar_wait(k_empty(s), ((u / NK) - 1) & 1, p.status)) return false;
-        mbar_arrive_expect_tx(k_full(s), C::KV_BYTES);
-        tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES, tm, k_full(s), d0, row, g, b);
-        tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES + BN * 128, tm, k_full(s), d0 + 64, row, g, b);
+        mbar_arrive_expect_tx(k_full(s), two ? C::KV_BYTES : C::KV_BYTES / 2);
+        tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES, tm, k_full(s), c * 64, row, g, b);
+        if (two) tma_load_4d(sbase + C::OFF_K + s * C::KV_BYTES + BN * 128, tm, k_full(s), c * 64 + 64, row, g, b);
         ++u;
         return true;
       };
       bool okp = true;
       for (int j = 0; okp && j <= n; ++j) {
         if (j < n)
-          for (int c2 = 0; okp && c2 < D / 128; ++c2) okp = slot_load(&tmK, c2 * 128, (t0 + j) * BN);
+          for (int c = 0; okp && c < nch; c += 2) okp = slot_load(&tmK, c, (t0 + j) * BN, c + 1 < nch);
         if (j >= 1)
-          for (int c2 = 0; okp && c2 < C::DV / 128; ++c2) okp = slot_load(&tmV, vh * C::DV + c2 * 128, (t0 + j - 1) * BN);
+          for (int c = 0; okp && c < vcn; c += 2) okp = slot_load(&tmV, vc0 + c, (t0 + j - 1) * BN, c + 1 < vcn);
       }
     }
   } else if (warp == 0) {
@@ -425,11 +432,13 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D, BN, NK, NV>::MINB)
     }
   } else if (warp == 1 && C::WIDE) {
     // ------------------------------------------------------------ MMA issuer (wide form)
-    // S_j from the four K slots of tile j (8 k-steps of 16 each, over 128 columns of D), then
-    // PV_{j-1}: one N = 128 MMA group per V slot into its 128 columns of O.
+    // S_j from the K slots of tile j (8 k-steps of 16 each over a slot's 128 columns of D, 4
+    // over a one-chunk slot), then PV_{j-1}: one N = 128 (one-chunk slot: N = 64) MMA group per
+    // V slot into its columns of O.
     if (n > 0) {
       constexpr uint32_t idS = idesc_bf16(kBM, BN, false, false);
       constexpr uint32_t idO = idesc_bf16(kBM, 128, false, true);
+      constexpr uint32_t idO64 = idesc_bf16(kBM, 64, false, true);
       const uint64_t dq0 = sw128_desc(sbase + C::OFF_Q, 16, 1024);
       int u = 0;
       bool ok = mbar_wait_warp(q_full, 0, p.status);
@@ -437,16 +446,18 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D, BN, NK, NV>::MINB)
         if (j < n) {
           const uint32_t dS = tmem + (uint32_t)((j & 1) * BN);
 #pragma unroll 1
-          for (int c2 = 0; c2 < D / 128; ++c2, ++u) {
+          for (int c2 = 0; 2 * c2 < nch; ++c2, ++u) {
             const int s = u % NK;
             if (!mbar_wait_warp(k_full(s), (u / NK) & 1, p.status)) { ok = false; break; }
             tc_fence_after();
             const uint64_t qd = desc_at(dq0, (2 * c2) * (kBM * 128));
             const uint64_t kd = sw128_desc(sbase + C::OFF_K + s * C::KV_BYTES, 16, 1024);
+            const int nk8 = 2 * c2 + 1 < nch ? 8 : 4;
 #pragma unroll
             for (int k8 = 0; k8 < 8; ++k8)
-              mma_ss_w(dS, desc_at(qd, (k8 >> 2) * (kBM * 128) + (k8 & 3) * 32),
-                       desc_at(kd, (k8 >> 2) * (BN * 128) + (k8 & 3) * 32), idS, (c2 | k8) != 0);
+              if (k8 < nk8)
+                mma_ss_w(dS, desc_at(qd, (k8 >> 2) * (kBM * 128) + (k8 & 3) * 32),
+                         desc_at(kd, (k8 >> 2) * (BN * 128) + (k8 & 3) * 32), idS, (c2 | k8) != 0);
             mma_commit_w(k_empty(s));
           }
           if (!ok) break;
@@ -457,14 +468,15 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D, BN, NK, NV>::MINB)
           if (!mbar_wait_warp(p_full(jj & 1), (jj >> 1) & 1, p.status)) break;
           const uint32_t pa = tmem + (uint32_t)((jj & 1) * BN);
 #pragma unroll 1
-          for (int c2 = 0; c2 < C::DV / 128; ++c2, ++u) {
+          for (int c2 = 0; 2 * c2 < vcn; ++c2, ++u) {
             const int s = u % NK;
             if (!mbar_wait_warp(k_full(s), (u / NK) & 1, p.status)) { ok = false; break; }
             tc_fence_after();
             const uint64_t dv = sw128_desc(sbase + C::OFF_K + s * C::KV_BYTES, BN * 128, 1024);
+            const uint32_t id = 2 * c2 + 1 < vcn ? idO : idO64;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ts_w(tmem + C::TM_O + c2 * 128, pa + p_col<HC>(kk), desc_at(dv, kk * (16 * 128)), idO,
+              mma_ts_w(tmem + C::TM_O + c2 * 128, pa + p_col<HC>(kk), desc_at(dv, kk * (16 * 128)), id,
                        (jj > 0 || kk > 0) ? 1u : 0u);
             mma_commit_w(k_empty(s));
           }
@@ -709,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D, BN, NK, NV>::MINB)
       if (!FIXM && j >= 1 && __any_sync(0xffffffffu, resc)) {
         tc_fence_after();
 #pragma unroll 1
-        for (int c = half * (C::DV / 64); c < (half + 1) * (C::DV / 64); ++c) {
+        for (int c = half * vcn; c < (half + 1) * vcn; ++c) {
           uint32_t orr[32];
           tmem_ld32(lane_addr + C::TM_O + c * 32, orr);
           tmem_wait_ld();
@@ -762,9 +774,10 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D, BN, NK, NV>::MINB)
       }
       if (row_ok && half == 0) p.lse_part[prow] = lse;
     } else {
-      __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.O) + (((size_t)b * p.Sq + i) * p.Hq + h) * D + vh * C::DV;
+      __nv_bfloat16 *orow =
+          static_cast<__nv_bfloat16 *>(p.O) + (((size_t)b * p.Sq + i) * p.Hq + h) * (C::WIDE ? p.D : D) + vc0 * 64;
 #pragma unroll 1
-      for (int c = half * (C::DV / 64); c < (half + 1) * (C::DV / 64); ++c) {
+      for (int c = half * vcn; c < (half + 1) * vcn; ++c) {
         uint32_t orr[32];
         if (n > 0) {
           tmem_ld32(lane_addr + C::TM_O + c * 32, orr);
@@ -801,9 +814,12 @@ template <int D, int BN, int NK, int NV>
 cudaError_t launch_fwd(const Params &p, cudaStream_t st) {
   using C = FwdCfg<D, BN, NK, NV>;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bshd(&tq, p.q, D, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, kBM) ||
-      !make_tmap_bshd(&tk, p.k, D, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, BN) ||
-      !make_tmap_bshd(&tv, p.v, D, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, C::HALF ? 64 : BN))
+  // The wide form reads the head dim at run time: whole 64-column chunks, above 256, at most D.
+  if (C::WIDE && (p.D % 64 != 0 || p.D <= 256 || p.D > D)) return cudaErrorInvalidValue;
+  const int Dm = C::WIDE ? p.D : D;
+  if (!make_tmap_bshd(&tq, p.q, Dm, p.Sq, p.Hq, p.B, p.q_ss, p.q_sh, p.q_sb, kBM) ||
+      !make_tmap_bshd(&tk, p.k, Dm, p.Sk, p.Hkv, p.B, p.k_ss, p.k_sh, p.k_sb, BN) ||
+      !make_tmap_bshd(&tv, p.v, Dm, p.Sk, p.Hkv, p.B, p.v_ss, p.v_sh, p.v_sb, C::HALF ? 64 : BN))
     return cudaErrorInvalidValue;
   if (C::WIDE && p.kv_splits > 1) return cudaErrorInvalidValue;  // the split-KV forward is not built for it
   auto kern = p.bias ? (p.cap <= 0.f                 ? fwd_tc_kernel<D, BN, NK, NV, false, false, true>
@@ -833,7 +849,7 @@ bool pair_grid(const Params &p) {
 
 }  // namespace
 
-bool tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
+bool tc_supported(int D) { return D == 64 || D == 128 || D == 256 || (D > 256 && D <= 512 && D % 64 == 0); }
 
 // Tiles.  Head dims 64 and 128, grids of at least two CTAs per SM: 64 keys per step, two-deep K
 // and V rings, so that two score buffers and O take 256 TMEM columns and two CTAs share each
@@ -842,8 +858,8 @@ bool tc_supported(int D) { return D == 64 || D == 128 || D == 256 || D == 512; }
 // Smaller grids: 128 keys per step, one CTA per SM.  Head dim 256: 128 keys per step
 // (N = 128 score MMAs run at the full tensor rate, N = 64 ones at two thirds of it); two score
 // buffers and O fill the 512 TMEM columns, and its 64 KiB K and V tiles leave room for one of
-// each next to Q (measured 20 % faster than 64-key tiles with two-deep rings).  Head dim 512:
-// the wide form.
+// each next to Q (measured 20 % faster than 64-key tiles with two-deep rings).  Head dims 320,
+// 384, 448 and 512: the wide form.
 cudaError_t tc_forward(const Params &p, cudaStream_t st) {
   switch (p.D) {
     case 64:
@@ -851,6 +867,9 @@ cudaError_t tc_forward(const Params &p, cudaStream_t st) {
     case 128:
       return pair_grid(p) ? launch_fwd<128, 64, 2, 2>(p, st) : launch_fwd<128, 128, 3, 2>(p, st);
     case 256: return launch_fwd<256, 128, 1, 1>(p, st);
+    case 320:
+    case 384:
+    case 448:
     case 512: return launch_fwd<512, 128, 2, 0>(p, st);  // wide form: two 32 KiB ring slots
     default: return cudaErrorInvalidValue;
   }

@@ -90,11 +90,17 @@ typedef struct {
     int dtype;                 /* enum attn_dtype                                          */
     int B, Sq, Sk, Hq, Hkv, D; /* B, Sq, Sk >= 0 (B == 0 or Sq == 0: nothing to compute);
                                   Hq, Hkv >= 1 with Hq % Hkv == 0; D % 8 == 0, D <= 512.
-                                  Tensor-core kernels: bf16 with D in {64, 128, 256} and
-                                  Sk > 0, with or without a bias, sink, segments or splits.
-                                  The fp32 FFMA kernels take every other call: fp32 inputs,
-                                  and other head dims (up to 512: MaxText's chunked head-dim
-                                  accumulation above 256, tokamax PR #1121)                */
+                                  Tensor-core kernels: bf16 with Sk > 0 and D in {64, 128,
+                                  256}, or D in {320, 384, 448, 512} (the wide form for
+                                  MaxText's chunked head-dim accumulation above 256, tokamax
+                                  PR #1121: two CTAs per query tile, each producing part of
+                                  O; its backward is a scores kernel and three GEMMs through
+                                  two bf16 scratch planes of B*Hq*Sq_pad*Sk_pad elements
+                                  (Sq, Sk rounded up to 128) in the workspace, taken while
+                                  they stay within 16 GiB), with or without a bias, sink,
+                                  segments or splits.  The fp32 FFMA kernels take every
+                                  other call: fp32 inputs, other head dims, and wide-form
+                                  backwards whose planes would exceed 16 GiB.              */
     const void *q;             /* [B,Sq,Hq,D] with the strides below (elements)           */
     int64_t q_stride_b, q_stride_s, q_stride_h;
     const void *k;             /* [B,Sk,Hkv,D]                                             */
@@ -133,7 +139,7 @@ typedef struct {
      * exactly once per row (TransformerEngine PR #3551, "What changed": the sink enters each
      * row once when tiles' statistics are merged).  The workspace grows by
      * n * B * Hq * Sq * (D + 1) * 4 bytes.  Results equal the unsplit forward up to rounding.
-     * Head dim 512 and the FFMA path (fp32 inputs, other head dims) compute unsplit.  Other
+     * Head dims above 256 and the FFMA path (fp32 inputs, other head dims) compute unsplit.  Other
      * values: ATTN_ERR_INVALID.  The backward ignores this field.                           */
     int kv_splits;
     /* Optional key boundaries for cu_seqlens ("thd" varlen with Sq != Sk per sequence):

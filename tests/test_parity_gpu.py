@@ -491,10 +491,11 @@ def test_bias_with_sink_dsink_gap():
     assert dsink_stored <= TOL["bf16"] and dsink_pure <= 1.5e-2
 
 
-# Head dim 512 on the tensor cores (the forward's wide form: each CTA one half of O, S over the
-# whole head dim, Q resident and K / V streamed through one ring; the backward's scores kernel
-# and dV / dK / dQ GEMMs): GQA, sink, window, cap tracked and fixed, ragged Sq != Sk, bias and
-# packed segments, off-by-one.
+# Head dims 320 .. 512 on the tensor cores (the forward's wide form: each CTA one part of O, S
+# over the whole head dim, Q resident and K / V streamed through one ring; the backward's scores
+# kernel and dV / dK / dQ GEMMs): GQA, sink, window, cap tracked and fixed, ragged Sq != Sk, bias
+# and packed segments, off-by-one; odd chunk counts (320, 448: a one-chunk ring slot, the CTAs'
+# parts of O unequal) and 384 (three chunks per CTA).
 WIDE = [
     (Workload("wide_d512_gqa_sink_window", "bf16", B=2, Sq=300, Sk=300, Hq=4, Hkv=2, D=512, causal=True,
               window=120, softcap=30.0, sink=True, q_std=2.0), {}),
@@ -504,11 +505,17 @@ WIDE = [
               segments=True, run_lo=40, run_hi=200, bias=True, bias_dims="h"), {}),
     (Workload("wide_d512_off_by_one", "bf16", B=1, Sq=260, Sk=260, Hq=2, Hkv=1, D=512, causal=True, softcap=20.0,
               q_std=2.0), {"off_by_one": True}),
+    (Workload("wide_d320_gqa_sink_window", "bf16", B=1, Sq=300, Sk=300, Hq=4, Hkv=2, D=320, causal=True,
+              window=130, softcap=30.0, sink=True, q_std=2.0), {}),
+    (Workload("wide_d384_ragged_noncausal_cap60", "bf16", B=1, Sq=150, Sk=290, Hq=2, Hkv=1, D=384, causal=False,
+              softcap=60.0, q_std=2.0), {}),
+    (Workload("wide_d448_bias_cap0", "bf16", B=2, Sq=260, Sk=260, Hq=2, Hkv=2, D=448, causal=True,
+              bias=True, bias_dims="b", sink=True), {}),
 ]
 
 
 @pytest.mark.parametrize("w,extra", WIDE, ids=lambda x: x.name if hasattr(x, "name") else "")
-def test_head_dim_512_on_tensor_cores(w, extra):
+def test_wide_head_dims_on_tensor_cores(w, extra):
     import attention_flash_attn_gb300 as fa
     inp = make_inputs(w)
     t = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
