@@ -102,3 +102,102 @@ def test_noalloc_device_errors_can_be_read_back():
     ref_O, ref_LSE = fa.attn_fwd(t["q"], t["k"], t["v"], causal=True, softcap=20.0, scale=w.scale,
                                  cu_seqlens=good)
     assert frob_rel(to64(O), to64(ref_O)) <= TOL[w.dtype]
+
+
+# Child program: the forward in contexts of the caller's own (driver API), the way a plugin
+# hosted by another runtime calls it.  It makes a context, runs attn_fwd_noalloc there on packed
+# segments (the array then holds the segment metadata), destroys the context, makes a second
+# one and runs the same call: the array lives at a new address in the new context, and both
+# calls must give the same O and LSE, which must also match a float64 softmax of the same
+# bf16-rounded inputs.  Torch's CUDA state is never touched in the child.
+_CONTEXT_CHILD = r'''
+import ctypes, sys
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+from attention_flash_attn_gb300 import _capi
+
+cu = ctypes.CDLL("libcuda.so.1")
+def ck(r, what):
+    if r != 0:
+        raise SystemExit(f"{what}: CUresult {r}")
+ck(cu.cuInit(0), "cuInit")
+dev = ctypes.c_int()
+ck(cu.cuDeviceGet(ctypes.byref(dev), 0), "cuDeviceGet")
+
+B, S, H, D = 1, 300, 2, 64
+rng = np.random.default_rng(7)
+def bf16(x):
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    return r, (r.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+q16, q = bf16(rng.normal(0, 2, (B, S, H, D)))
+k16, k = bf16(rng.normal(0, 2, (B, S, H, D)))
+v16, v = bf16(rng.normal(0, 1, (B, S, H, D)))
+seg = np.repeat(np.arange(4, dtype=np.int32), [70, 101, 29, 100]).reshape(B, S)
+scale, cap = 0.125, 20.0
+
+def run():
+    ctx = ctypes.c_void_p()
+    ck(cu.cuCtxCreate_v2(ctypes.byref(ctx), 0, dev), "cuCtxCreate")
+    bufs = []
+    def up(a):
+        p = ctypes.c_uint64()
+        ck(cu.cuMemAlloc_v2(ctypes.byref(p), ctypes.c_size_t(a.nbytes)), "cuMemAlloc")
+        ck(cu.cuMemcpyHtoD_v2(p, a.ctypes.data_as(ctypes.c_void_p), ctypes.c_size_t(a.nbytes)), "HtoD")
+        bufs.append(p)
+        return p.value
+    O = np.zeros((B, S, H, D), np.uint16)
+    L = np.zeros((B, H, S), np.float32)
+    a = _capi.AttnArgs()
+    a.dtype, a.B, a.Sq, a.Sk, a.Hq, a.Hkv, a.D = _capi.ATTN_DTYPE_BF16, B, S, S, H, H, D
+    st = (S * H * D, H * D, D)
+    a.q, a.k, a.v = up(q16), up(k16), up(v16)
+    a.q_stride_b, a.q_stride_s, a.q_stride_h = st
+    a.k_stride_b, a.k_stride_s, a.k_stride_h = st
+    a.v_stride_b, a.v_stride_s, a.v_stride_h = st
+    a.seg_q = a.seg_k = up(seg)
+    a.causal, a.softcap, a.scale = 1, cap, scale
+    dO, dL = up(O), up(L)
+    lib = _capi.lib()
+    s = lib.attn_fwd_noalloc(ctypes.byref(a), dO, dL, None)
+    if s != 0:
+        raise SystemExit(f"attn_fwd_noalloc: {s}")
+    ck(cu.cuCtxSynchronize(), "sync")
+    s = lib.attn_noalloc_check_device_status(None)
+    if s != 0:
+        raise SystemExit(f"status: {s}")
+    ck(cu.cuMemcpyDtoH_v2(O.ctypes.data_as(ctypes.c_void_p), ctypes.c_uint64(dO), ctypes.c_size_t(O.nbytes)), "DtoH")
+    ck(cu.cuMemcpyDtoH_v2(L.ctypes.data_as(ctypes.c_void_p), ctypes.c_uint64(dL), ctypes.c_size_t(L.nbytes)), "DtoH")
+    for p in bufs:
+        ck(cu.cuMemFree_v2(p), "cuMemFree")
+    ck(cu.cuCtxDestroy_v2(ctx), "cuCtxDestroy")
+    return (O.astype(np.uint32) << 16).view(np.float32), L
+
+O1, L1 = run()
+O2, L2 = run()
+assert np.array_equal(O1, O2) and np.array_equal(L1, L2), "the two contexts disagree"
+# float64 softmax of the same inputs: scale, cap, causal mask within equal segment ids
+i, j = np.arange(S)[:, None], np.arange(S)[None, :]
+vis = (j <= i) & (seg[0][:, None] == seg[0][None, :])
+err = 0.0
+for h in range(H):
+    u = scale * q[0, :, h] @ k[0, :, h].T
+    t = np.where(vis, cap * np.tanh(u / cap), -np.inf)
+    m = t.max(1, keepdims=True)
+    p = np.exp(t - m)
+    o = (p @ v[0, :, h]) / p.sum(1, keepdims=True)
+    err = max(err, np.linalg.norm(O1[0, :, h] - o) / np.linalg.norm(o))
+    lse = (m[:, 0] + np.log(p.sum(1))).astype(np.float64)
+    err = max(err, np.abs(L1[0, h] - lse).max() / np.abs(lse).max())
+assert err < 1e-2, err
+print("ok", err)
+'''
+
+
+def test_noalloc_in_contexts_of_the_caller_s_own():
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _CONTEXT_CHILD, root], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.startswith("ok"), (r.stdout[-2000:], r.stderr[-4000:])
