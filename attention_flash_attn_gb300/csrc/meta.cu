@@ -1,17 +1,19 @@
 // meta.cu -- mask metadata for packed segments (segment ids or cu_seqlens).
 //
-// One block per batch row.  It (1) turns cu_seqlens into segment ids when given (with
-// separate key boundaries, ids per axis and each token's per-sequence bottom-right offset),
-// (2) checks whether the row's query and key ids are non-decreasing, (3) for every 64-row
+// A row pass (1) turns cu_seqlens into segment ids when given (with separate key boundaries,
+// ids per axis and each token's per-sequence bottom-right offset), spread over as many blocks
+// as the tokens need, and (2) decides whether each batch row's query and key ids are
+// non-decreasing (boundaries that pass their checks give non-decreasing ids by construction;
+// given ids are checked, one block per row).  A tile pass then (3) for every 64-row
 // query tile writes the key range [lo, hi) its rows can see, and for every 64-key tile the
 // query range that can see it, intersected with the causal and window bounds, and (4) for
 // every 128-row query tile and 128-key tile (the CTAs of the tensor-core kernels) writes its
 // tile class and its visible pairs.  A second kernel sorts the tiles into longest-first work
 // lists, which the tensor-core grids follow (MaxText commit message quoted on tokamax PR #1121:
 // packed rows with segments of very different lengths, run starts per row).
-// With non-decreasing ids a segment is one contiguous run, found by binary search; with
-// arbitrary ids the ranges fall back to the causal/window bounds alone and the kernels
-// test id equality pair by pair.  An empty range is stored as {n, 0} so that the union of
+// With non-decreasing ids a segment is one contiguous run: read straight from the boundaries
+// with cu_seqlens, found by binary search in given ids; with arbitrary ids the ranges fall back
+// to the causal/window bounds alone and the kernels test id equality pair by pair.  An empty range is stored as {n, 0} so that the union of
 // two tile ranges (min of lo, max of hi) ignores it.
 #include <algorithm>
 #include <climits>
@@ -57,50 +59,57 @@ __device__ __forceinline__ bool bad_bounds(const int *cu, int nseq, int n) {
   return bad;
 }
 
+// Row pass.  With cu_seqlens (B == 1): a grid over the tokens, the boundaries in shared memory,
+// block 0 checking them (a failed check is recorded in the status word and leaves the ids
+// marked unsorted, so that the kernels compare ids pair by pair and every access stays inside
+// its array).  With given ids: one block per batch row checks their order.
+constexpr int kRowsTokensPerBlock = 4096;
 __global__ void __launch_bounds__(1024) meta_rows_kernel(Params p, const int *cu, const int *cu_k, int nseq,
                                                          int *seg_out, int *segk_out, int *qoff_out,
                                                          int *koff_out, unsigned char *mono) {
-  const int b = blockIdx.x;
-  // The boundaries in shared memory when they fit: every token below searches them.
-  constexpr int kCuSmem = 4096;
-  __shared__ int cu_s[kCuSmem], cuk_s[kCuSmem];
-  if (cu && nseq + 1 <= kCuSmem) {
-    for (int x = threadIdx.x; x <= nseq; x += blockDim.x) {
-      cu_s[x] = cu[x];
-      if (cu_k) cuk_s[x] = cu_k[x];
+  const int b = blockIdx.y;
+  if (cu) {
+    // The boundaries in shared memory when they fit: every token below searches them.
+    constexpr int kCuSmem = 4096;
+    __shared__ int cu_s[kCuSmem], cuk_s[kCuSmem];
+    if (nseq + 1 <= kCuSmem) {
+      for (int x = threadIdx.x; x <= nseq; x += blockDim.x) {
+        cu_s[x] = cu[x];
+        if (cu_k) cuk_s[x] = cu_k[x];
+      }
+      __syncthreads();
+      cu = cu_s;
+      if (cu_k) cu_k = cuk_s;
     }
-    __syncthreads();
-    cu = cu_s;
-    if (cu_k) cu_k = cuk_s;
+    if (blockIdx.x == 0) {
+      const int bad = __syncthreads_or(bad_bounds(cu, nseq, p.Sq) || (cu_k && bad_bounds(cu_k, nseq, p.Sk)));
+      if (threadIdx.x == 0) {
+        if (bad) set_status(p.status, kStatusBadCuSeqlens);
+        mono[0] = (unsigned char)!bad;
+      }
+    }
+    const int t0 = blockIdx.x * kRowsTokensPerBlock;
+    if (cu_k) {
+      // Separate query and key boundaries: ids per axis, and per token the bottom-right
+      // offset end_k(s) - end_q(s) of its sequence.
+      for (int t = t0 + threadIdx.x; t < min(t0 + kRowsTokensPerBlock, p.Sq); t += blockDim.x) {
+        const int sq = seq_of(cu, nseq, t);
+        seg_out[t] = sq;
+        qoff_out[t] = seq_end(cu_k, nseq, p.Sk, sq) - seq_end(cu, nseq, p.Sq, sq);
+      }
+      for (int t = t0 + threadIdx.x; t < min(t0 + kRowsTokensPerBlock, p.Sk); t += blockDim.x) {
+        const int sk = seq_of(cu_k, nseq, t);
+        segk_out[t] = sk;
+        koff_out[t] = seq_end(cu_k, nseq, p.Sk, sk) - seq_end(cu, nseq, p.Sq, sk);
+      }
+    } else {
+      // Sq == Sk: one id array serves queries and keys.
+      for (int t = t0 + threadIdx.x; t < min(t0 + kRowsTokensPerBlock, p.Sq); t += blockDim.x)
+        seg_out[t] = seq_of(cu, nseq, t);
+    }
+    return;
   }
-  const int *sq, *sk;
-  if (cu && cu_k) {
-    // B == 1, separate query and key boundaries: ids per axis, and per token the bottom-right
-    // offset end_k(s) - end_q(s) of its sequence.
-    if (bad_bounds(cu, nseq, p.Sq) || bad_bounds(cu_k, nseq, p.Sk)) set_status(p.status, kStatusBadCuSeqlens);
-    for (int t = threadIdx.x; t < p.Sq; t += blockDim.x) {
-      const int s = seq_of(cu, nseq, t);
-      seg_out[t] = s;
-      qoff_out[t] = seq_end(cu_k, nseq, p.Sk, s) - seq_end(cu, nseq, p.Sq, s);
-    }
-    for (int t = threadIdx.x; t < p.Sk; t += blockDim.x) {
-      const int s = seq_of(cu_k, nseq, t);
-      segk_out[t] = s;
-      koff_out[t] = seq_end(cu_k, nseq, p.Sk, s) - seq_end(cu, nseq, p.Sq, s);
-    }
-    __syncthreads();
-    sq = seg_out;
-    sk = segk_out;
-  } else if (cu) {
-    // B == 1 and Sq == Sk: one id array serves queries and keys.
-    if (bad_bounds(cu, nseq, p.Sq)) set_status(p.status, kStatusBadCuSeqlens);
-    for (int t = threadIdx.x; t < p.Sq; t += blockDim.x) seg_out[t] = seq_of(cu, nseq, t);
-    __syncthreads();
-    sq = sk = seg_out;
-  } else {
-    sq = p.seg_q + (size_t)b * p.Sq;
-    sk = p.seg_k + (size_t)b * p.Sk;
-  }
+  const int *sq = p.seg_q + (size_t)b * p.Sq, *sk = p.seg_k + (size_t)b * p.Sk;
   int ok = 1;
   for (int i = threadIdx.x; i + 1 < p.Sq; i += blockDim.x) ok &= sq[i] <= sq[i + 1];
   for (int j = threadIdx.x; j + 1 < p.Sk; j += blockDim.x) ok &= sk[j] <= sk[j + 1];
@@ -109,12 +118,13 @@ __global__ void __launch_bounds__(1024) meta_rows_kernel(Params p, const int *cu
 }
 
 // Per tile, after the row pass.  Grid: x over the tiles of one axis, y the batch row, z the
-// axis (0: query tiles, 1: key tiles); 256 threads.  Each thread computes one 64-granular range,
-// each warp one 128-granular tile class.  With sorted ids every row's segment run on the other
-// axis is found by binary search, in a shared-memory copy of the other axis's ids when they fit
+// axis (0: query tiles, 1: key tiles); 256 threads, each warp one 128-row tile.  With sorted ids
+// every row's segment run on the other axis is read from the boundaries (cu_seqlens: sequence
+// s spans [cu[s], cu[s + 1]) there, tokens at or past cu[nseq] forming sequence nseq) or found
+// by binary search in given ids, in a shared-memory copy of the other axis's ids when they fit
 // (a search in global memory pays a dependent load per step).
 constexpr int kMetaSmemIds = 49152;  // ids copied to shared memory (192 KiB) at most
-__global__ void __launch_bounds__(256) meta_tiles_kernel(Params p, const int *cu, const int *cu_k,
+__global__ void __launch_bounds__(256) meta_tiles_kernel(Params p, const int *cu, const int *cu_k, int nseq,
                                                          const int *seg_out, const int *segk_out,
                                                          const int *qoff_out, const int *koff_out,
                                                          const unsigned char *mono, int2 *qrange, int2 *krange,
@@ -135,7 +145,9 @@ __global__ void __launch_bounds__(256) meta_tiles_kernel(Params p, const int *cu
   const int n_rows = qside ? p.Sq : p.Sk, n_other = qside ? p.Sk : p.Sq;
   const int *own = qside ? sq : sk;       // this axis's ids
   const int *other = qside ? sk : sq;     // the axis searched
-  if (sorted && n_other <= kMetaSmemIds) {
+  // boundaries of the other axis (cu_seqlens)
+  const int *cu_other = cu ? (qside ? (cu_k ? cu_k : cu) : cu) : nullptr;
+  if (sorted && !cu && n_other <= kMetaSmemIds) {
     for (int x = threadIdx.x; x < n_other; x += blockDim.x) ids_s[x] = other[x];
     __syncthreads();
     other = ids_s;
@@ -170,8 +182,14 @@ __global__ void __launch_bounds__(256) meta_tiles_kernel(Params p, const int *cu
         hi = p.window > 0 ? kp + p.window : p.Sq;
       }
       if (sorted) {
-        lo = max(lo, lower_bound_i(other, n_other, own[r]));
-        hi = min(hi, upper_bound_i(other, n_other, own[r]));
+        const int id = own[r];
+        if (cu_other) {  // checked boundaries: id in [0, nseq], cu_other non-decreasing, within n_other
+          lo = max(lo, __ldg(cu_other + id));
+          hi = min(hi, id < nseq ? __ldg(cu_other + id + 1) : n_other);
+        } else {
+          lo = max(lo, lower_bound_i(other, n_other, id));
+          hi = min(hi, upper_bound_i(other, n_other, id));
+        }
       }
       lo = max(lo, 0);
       hi = min(hi, n_other);
@@ -272,7 +290,10 @@ __global__ void __launch_bounds__(1024) work_order_kernel(const long long *qwork
 
 cudaError_t launch_mask_meta(const Params &p, const int *cu_seqlens, const int *cu_seqlens_k, int nseq,
                              const MetaOut &o, cudaStream_t st) {
-  meta_rows_kernel<<<p.B, 1024, 0, st>>>(p, cu_seqlens, cu_seqlens_k, nseq, o.seg_q, o.seg_k, o.qoff, o.koff, o.mono);
+  const int row_blocks = cu_seqlens ? (std::max(p.Sq, p.Sk) + kRowsTokensPerBlock - 1) / kRowsTokensPerBlock : 1;
+  if (p.B > 65535) return cudaErrorInvalidValue;
+  meta_rows_kernel<<<dim3((unsigned)std::max(row_blocks, 1), (unsigned)p.B), 1024, 0, st>>>(
+      p, cu_seqlens, cu_seqlens_k, nseq, o.seg_q, o.seg_k, o.qoff, o.koff, o.mono);
   cudaError_t e = counted(cudaGetLastError());
   if (e != cudaSuccess) return e;
   {
@@ -281,13 +302,13 @@ cudaError_t launch_mask_meta(const Params &p, const int *cu_seqlens, const int *
     const long long blocks = ((long long)(std::max(p.Sq, p.Sk) + 127) / 128 + 7) / 8;
     if (blocks > 0x7fffffffLL || p.B > 65535) return cudaErrorInvalidValue;
     const int n_ids = std::max(p.Sq, p.Sk);
-    const size_t smem = n_ids <= kMetaSmemIds ? (size_t)n_ids * sizeof(int) : 0;
+    const size_t smem = (!cu_seqlens && n_ids <= kMetaSmemIds) ? (size_t)n_ids * sizeof(int) : 0;
     if (smem > 48 * 1024) {
       e = cudaFuncSetAttribute(meta_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
     }
     meta_tiles_kernel<<<dim3((unsigned)blocks, (unsigned)p.B, 2), 256, smem, st>>>(
-        p, cu_seqlens, cu_seqlens_k, o.seg_q, o.seg_k, o.qoff, o.koff, o.mono, o.qrange, o.krange, o.qtile, o.ktile,
+        p, cu_seqlens, cu_seqlens_k, nseq, o.seg_q, o.seg_k, o.qoff, o.koff, o.mono, o.qrange, o.krange, o.qtile, o.ktile,
         o.qwork, o.kwork);
     e = counted(cudaGetLastError());
   }

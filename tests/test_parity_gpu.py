@@ -374,6 +374,32 @@ def test_cu_seqlens_equals_segment_ids():
     check(w, b, full_oracle(w, {**inp, "seg": seg}))
 
 
+def test_cu_seqlens_many_sequences_equals_segment_ids():
+    """More boundaries than the row pass keeps in shared memory (nseq + 1 > 4096) and more
+    tokens than one block of it takes: the same results as the equivalent segment ids, and the
+    oracle's.  Most sequences hold one token, whose probability is exactly 1: by definition its
+    dq and dk are zero, and the kernels' dP - D with D = rowsum(dO * O) from the stored bf16 O
+    leaves a rounding residue there instead, so dq and dk are held to the oracle run on that
+    same stored O (the stored-O reading of the backward's D)."""
+    w = Workload("cu_many", "bf16", B=1, Sq=4500, Sk=4500, Hq=2, Hkv=1, D=64, causal=True, softcap=30.0)
+    inp = make_inputs(w)
+    lens = np.array([1] * 4100 + [100] * 4)
+    np.random.default_rng(5).shuffle(lens)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    seg = torch.repeat_interleave(torch.arange(len(lens), dtype=torch.int32), torch.tensor(lens)).view(1, -1)
+    a = run_gpu(w, {**inp, "seg": None}, cu_seqlens=cu.cuda())
+    b = run_gpu(w, {**inp, "seg": seg})
+    for k in ("O", "LSE", "dq", "dk", "dv"):
+        assert torch.equal(a[k], b[k]), k
+    ref = full_oracle(w, {**inp, "seg": seg})
+    errs = compare_full(w, b, ref)
+    assert all(errs[k] <= TOL["bf16"] for k in ("O", "LSE", "dv")), errs
+    p = problem_from_inputs(w, {**inp, "seg": seg})
+    stored = oracle.backward(p, to64(inp["dO"]), to64(b["O"]), ref["LSE"], want=("dq", "dk"))
+    for k in ("dq", "dk"):
+        assert frob_rel(to64(b[k]), stored[k]) <= TOL["bf16"], (k, errs[k])
+
+
 def test_cross_segment_perturbation_bit_identical():
     """Changing every input of one packed segment leaves the other segments' outputs and
     gradients bit-identical (no attention across boundaries, incl. a tile-unaligned one)."""
