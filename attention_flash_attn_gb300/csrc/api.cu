@@ -110,7 +110,7 @@ Layout layout(const attn_args *a, bool bwd) {
     if (use_tc_bwd(a) && tc_bwd_fused(a->D)) { L.dsplit = off; off += align_up((size_t)a->B * a->Hq * sq_pad * 16); }
     if (a->sink) {
       L.dsink_part = off;
-      off += align_up((size_t)a->Hq * bwd_pre_partials(a->B, a->Sq) * sizeof(float));
+      off += align_up((size_t)a->Hq * bwd_pre_partials_max(a->B, a->Sq) * sizeof(float));
     }
     if (use_tc_bwd(a)) { L.dqacc = off; off += align_up((size_t)a->B * a->Sq * a->Hq * a->D * sizeof(float)); }
     if (a->bias) { L.dbias_acc = off; off += align_up(dbias_elems(a) * sizeof(float)); }
@@ -365,7 +365,7 @@ int attn_bwd(const attn_args *a, const void *O, const float *LSE, const void *dO
   p.Dvec = reinterpret_cast<float *>(w + L.dvec);
   p.sq_pad = (a->Sq + 127) / 128 * 128;
   p.dsink_part = a->sink ? reinterpret_cast<float *>(w + L.dsink_part) : nullptr;
-  p.n_part = bwd_pre_partials(a->B, a->Sq);
+  p.n_part = bwd_pre_partials(a->B, a->Sq, a->Hq);
   const bool tc = use_tc_bwd(a), wide = !tc && use_wide_bwd(a);
   p.dQacc = tc ? reinterpret_cast<float *>(w + L.dqacc) : nullptr;
   p.lse2p = tc || wide ? reinterpret_cast<float *>(w + L.lse2) : nullptr;

@@ -10,13 +10,17 @@
 // bwd_post: the fp32 dQ accumulator converted to the output dtype, the deterministic
 //           final dsink reduction (fixed order), and the fp32 dbias accumulator written
 //           out in the bias dtype.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace attn {
 namespace {
 
-constexpr int kPreRows = 64;   // query positions per preprocess block
+// Query positions per preprocess block: 64, halved down to 16 while the grid would not fill two
+// blocks per SM (chunked-prefill and decode-like shapes: few rows, few heads).
+constexpr int kPreRowsMax = 64, kPreRowsMin = 16;
 constexpr int kPreWarps = 8;
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -86,19 +90,21 @@ __device__ __forceinline__ uint4 neg_d_parts(float d) {
                     (uint32_t)__bfloat16_as_ushort(lo), 0u, 0u);
 }
 
-// grid (ceil(Sq/64), B, ceil(Hq/8)), block 256: warp w of z-block z handles head 8 z + w; rows
-// in order, so the per-(block, head) partial sums are deterministic.
+// grid (ceil(Sq/ROWS), B, ceil(Hq/8)), block 256: warp w of z-block z handles head 8 z + w;
+// rows in order, so the per-(block, head) partial sums are deterministic.  ROWS is a template
+// parameter: the same kernel with a run-time row count measured 1.3 % slower on the D=64 sink
+// workload's step.
 //
 // NC > 0 (a row is NC 16-byte chunks, NC dividing 32 or a multiple of it): a warp covers
 // 32 / NC rows per load, one lane per chunk (NC > 32: one row, NC / 32 chunks per lane), and
 // keeps kPreUnroll such loads in flight per lane before reducing each row over its lanes.
 // NC == 0: any other row length, one row per warp at a time.
 constexpr int kPreUnroll = 4;
-template <typename T, int NC>
+template <typename T, int NC, int ROWS>
 __global__ void __launch_bounds__(kPreWarps * 32) bwd_pre_kernel(Params p, int zero_dqacc) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int b = blockIdx.y;
-  const int i0 = blockIdx.x * kPreRows, i1 = min(i0 + kPreRows, p.Sq);
+  const int i0 = blockIdx.x * ROWS, i1 = min(i0 + ROWS, p.Sq);
   constexpr int per_chunk = 16 / sizeof(T);
   const T *O = static_cast<const T *>(p.O);
   const T *dO = static_cast<const T *>(p.dO);
@@ -246,22 +252,39 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(Params p, int convert_dq,
 template <typename T>
 cudaError_t launch_pre_t(const Params &p, bool zero_dqacc, cudaStream_t st) {
   // z: groups of kPreWarps heads (one per warp), so that heads spread over the SMs too
-  dim3 grid((p.Sq + kPreRows - 1) / kPreRows, p.B, (p.Hq + kPreWarps - 1) / kPreWarps);
+  const int rows = bwd_pre_rows(p.B, p.Sq, p.Hq);
+  dim3 grid((p.Sq + rows - 1) / rows, p.B, (p.Hq + kPreWarps - 1) / kPreWarps);
   const int nc = p.D * (int)sizeof(T) / 16;
-  switch (nc) {
-    case 4: bwd_pre_kernel<T, 4><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
-    case 8: bwd_pre_kernel<T, 8><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
-    case 16: bwd_pre_kernel<T, 16><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
-    case 32: bwd_pre_kernel<T, 32><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
-    case 64: bwd_pre_kernel<T, 64><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
-    default: bwd_pre_kernel<T, 0><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
-  }
+  auto go = [&](auto rc) {
+    constexpr int R = decltype(rc)::value;
+    switch (nc) {
+      case 4: bwd_pre_kernel<T, 4, R><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+      case 8: bwd_pre_kernel<T, 8, R><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+      case 16: bwd_pre_kernel<T, 16, R><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+      case 32: bwd_pre_kernel<T, 32, R><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+      case 64: bwd_pre_kernel<T, 64, R><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+      default: bwd_pre_kernel<T, 0, R><<<grid, kPreWarps * 32, 0, st>>>(p, zero_dqacc); break;
+    }
+  };
+  if (rows == 64) go(std::integral_constant<int, 64>());
+  else if (rows == 32) go(std::integral_constant<int, 32>());
+  else go(std::integral_constant<int, 16>());
   return counted(cudaGetLastError());
 }
 
 }  // namespace
 
-int bwd_pre_partials(int B, int Sq) { return B * ((Sq + kPreRows - 1) / kPreRows); }
+int bwd_pre_rows(int B, int Sq, int Hq) {
+  const long long z = (Hq + kPreWarps - 1) / kPreWarps, target = 2LL * device_sm_count();
+  int rows = kPreRowsMax;
+  while (rows > kPreRowsMin && (long long)((Sq + rows - 1) / rows) * B * z < target) rows /= 2;
+  return rows;
+}
+int bwd_pre_partials(int B, int Sq, int Hq) {
+  const int rows = bwd_pre_rows(B, Sq, Hq);
+  return B * ((Sq + rows - 1) / rows);
+}
+int bwd_pre_partials_max(int B, int Sq) { return B * ((Sq + kPreRowsMin - 1) / kPreRowsMin); }
 
 cudaError_t launch_bwd_pre(const Params &p, int dtype, bool zero_dqacc, cudaStream_t st) {
   return dtype == kF32 ? launch_pre_t<float>(p, zero_dqacc, st) : launch_pre_t<__nv_bfloat16>(p, zero_dqacc, st);

@@ -58,7 +58,9 @@ cudaError_t simt_backward(const Params &p, int dtype, cudaStream_t st);
 // Backward preprocess: D = rowsum(dO * O), per-block dsink partials, zero the fp32 dQ
 // accumulator when one is used.
 cudaError_t launch_bwd_pre(const Params &p, int dtype, bool zero_dqacc, cudaStream_t st);
-int bwd_pre_partials(int B, int Sq);  // partial sums per head the preprocess writes
+int bwd_pre_rows(int B, int Sq, int Hq);      // query positions per preprocess block
+int bwd_pre_partials(int B, int Sq, int Hq);  // partial sums per head the preprocess writes
+int bwd_pre_partials_max(int B, int Sq);      // ... at most, whatever the block size (workspace)
 
 // Backward epilogue: dQ accumulator -> dQ (when used), dsink reduction, dbias conversion.
 cudaError_t launch_bwd_post(const Params &p, int dtype, bool convert_dq, size_t dbias_elems,
