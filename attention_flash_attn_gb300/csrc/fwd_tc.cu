@@ -124,13 +124,14 @@ __device__ __forceinline__ void pair_bar(int wq) {
 // cap log2(e) (1 - 2 r), with r from f2_sigmoid2_neg (FMA-pipe reciprocal).  A huge e (its
 // exponent is clamped at 126) gives r ~ 0 (tanh = 1), an underflowing one r = 1.
 // With a bias the logit is u = scale s + bias; the bias enters as its own term (bin: its
-// factor, 2 log2(e) / cap with the cap, log2(e) without).
+// factor, 2 log2(e) / cap with the cap, log2(e) without).  `off` (the fixed exponent offset,
+// else 0) is subtracted from the capped logit in the same FMA.
 struct FwdScore {
   uint64_t cin, mcap2, cap2, sc2, bin;
-  __device__ FwdScore(float scale, float inv_cap, float cap) {
+  __device__ FwdScore(float scale, float inv_cap, float cap, float off) {
     cin = f2_splat(2.f * kLog2e * scale * inv_cap);
     mcap2 = f2_splat(-2.f * cap * kLog2e);
-    cap2 = f2_splat(cap * kLog2e);
+    cap2 = f2_splat(cap * kLog2e - off);
     sc2 = f2_splat(scale * kLog2e);
     bin = f2_splat(cap > 0.f ? 2.f * kLog2e * inv_cap : kLog2e);
   }
@@ -169,10 +170,12 @@ __device__ __forceinline__ void load_bias_row(uint32_t (&bq)[N2], const __nv_bfl
   }
 }
 
-// Raw scores -> capped, masked base-2 logits in place; returns their maximum.  MIX: every
-// other pair takes the cap's reciprocal from the special-function unit (rcp.approx) instead of
-// the FMA pipe -- 7 issue slots per pair instead of 11, for two more special-function ops --
-// for kernels whose softmax warps are issue-bound with that unit part idle.
+// Raw scores -> capped, masked base-2 logits (less the score's offset) in place; returns their
+// maximum.  MIX: every other pair takes the cap's reciprocal from the special-function unit
+// (rcp.approx) instead of the FMA pipe -- 5 issue slots per pair instead of 11, for two more
+// special-function ops -- for kernels whose softmax warps are issue-bound with that unit part
+// idle.  That form needs no clamp: an exponential that overflows to +inf gives 1 / inf = 0,
+// the cap's own limit (the FMA-pipe reciprocal's bit-level seed needs a finite input).
 template <bool CAP, bool MASKED, bool MIX, bool BIAS, int N>
 __device__ __forceinline__ float logits2(uint32_t (&x)[N], const FwdScore &k, int jbase, int lo, int hi,
                                          bool pairwise, const int *segk, int sid, const uint32_t *bq) {
@@ -187,7 +190,7 @@ __device__ __forceinline__ float logits2(uint32_t (&x)[N], const FwdScore &k, in
       if (MIX && (e & 2)) {
         float xa, xb, da, db;
         f2_unpack(x2, xa, xb);
-        f2_unpack(f2_add(f2_pack(ex2_approx(fminf(xa, 126.f)), ex2_approx(fminf(xb, 126.f))), f2_splat(1.f)), da, db);
+        f2_unpack(f2_add(f2_pack(ex2_approx(xa), ex2_approx(xb)), f2_splat(1.f)), da, db);
         r2 = f2_pack(rcp_approx(da), rcp_approx(db));
       } else {
         r2 = f2_sigmoid2_neg(x2);
@@ -621,7 +624,6 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D, BN, NK, NV>::MINB)
     }
     const bool any_pairwise = p.seg_q != nullptr && !p.seg_mono[b];
 
-    const FwdScore ks(p.scale, p.inv_cap, p.cap);
     // This row's bias (logically [B, Hq, Sq, Sk]; broadcast dimensions have stride 0).  A row
     // past Sq reads row Sq - 1 (never stored), so that every lane takes the same path.
     const __nv_bfloat16 *brow =
@@ -636,6 +638,8 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D, BN, NK, NV>::MINB)
       l = (sink_col && half == 0) ? ex2_approx(m_ref - m_fix) : 0.f;
       m_ref = m_fix;
     }
+    // With the fixed offset the logits come out of logits2 already less it.
+    const FwdScore ks(p.scale, p.inv_cap, p.cap, FIXM ? m_ref : 0.f);
     bool ok = true;
 
     for (int j = 0; j < n; ++j) {
@@ -699,7 +703,8 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D, BN, NK, NV>::MINB)
 #pragma unroll
       for (int e = 0; e < HC / 2; ++e) {
         float ya, yb;
-        f2_unpack(f2_sub(f2_pack(__uint_as_float(xr[2 * e]), __uint_as_float(xr[2 * e + 1])), mr2), ya, yb);
+        const uint64_t x2 = f2_pack(__uint_as_float(xr[2 * e]), __uint_as_float(xr[2 * e + 1]));
+        f2_unpack(FIXM ? x2 : f2_sub(x2, mr2), ya, yb);
         const float p0 = ex2_approx(ya), p1 = ex2_approx(yb);
         const uint64_t p2 = f2_pack(p0, p1);
         rs2 = f2_add(rs2, p2);
