@@ -16,7 +16,8 @@ from . import _capi
 from ._capi import AttnArgs, AttnError, lib  # noqa: F401
 
 __all__ = ["attn_fwd", "attn_fwd_noalloc", "attn_bwd", "attn_meta", "attn_check_device_status", "attn_path_name",
-           "attn_launch_counter", "attn_profile_next_main_kernel", "AttnError", "build_args"]
+           "attn_launch_counter", "attn_profile_next_main_kernel", "attn_profile_next_aux_kernels", "AttnError",
+           "build_args"]
 
 _DTYPES = {torch.bfloat16: _capi.ATTN_DTYPE_BF16, torch.float32: _capi.ATTN_DTYPE_F32}
 _ws_cache: dict = {}
@@ -221,3 +222,10 @@ def attn_profile_next_main_kernel(ev_start: "torch.cuda.Event", ev_end: "torch.c
     main kernel, on the call's stream."""
     lib().attn_profile_next_main_kernel(ctypes.c_void_p(ev_start.cuda_event),
                                         ctypes.c_void_p(ev_end.cuda_event))
+
+
+def attn_profile_next_aux_kernels(pre_start, pre_end, post_start, post_end):
+    """Have the next attn_bwd of this thread record the four events around its preprocess and
+    postprocess kernels, on the call's stream."""
+    lib().attn_profile_next_aux_kernels(*(ctypes.c_void_p(e.cuda_event) for e in (pre_start, pre_end, post_start,
+                                                                                    post_end)))

@@ -29,7 +29,7 @@ ATTN_ERR_DEVICE = 5
 EXPORTS = (
     "attn_fwd_workspace_size", "attn_fwd", "attn_bwd_workspace_size", "attn_bwd",
     "attn_check_device_status", "attn_status_string", "attn_path_name", "attn_launch_counter",
-    "attn_profile_next_main_kernel", "attn_fwd_noalloc", "attn_noalloc_check_device_status",
+    "attn_profile_next_main_kernel", "attn_profile_next_aux_kernels", "attn_fwd_noalloc", "attn_noalloc_check_device_status",
     "attn_selftest_wait_expiry", "attn_meta_size", "attn_meta_build",
 )
 
@@ -98,6 +98,8 @@ def lib():
         L.attn_path_name.restype = ctypes.c_char_p
         L.attn_profile_next_main_kernel.argtypes = [vp, vp]
         L.attn_profile_next_main_kernel.restype = None
+        L.attn_profile_next_aux_kernels.argtypes = [vp, vp, vp, vp]
+        L.attn_profile_next_aux_kernels.restype = None
         L.attn_launch_counter.argtypes = []
         L.attn_launch_counter.restype = ctypes.c_uint64
         _lib = L

@@ -210,8 +210,10 @@ Params make_params(const attn_args *a, char *ws, const Layout &L) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
-// Pending profiling events of this host thread (attn_profile_next_main_kernel).
+// Pending profiling events of this host thread (attn_profile_next_main_kernel,
+// attn_profile_next_aux_kernels).
 thread_local cudaEvent_t t_ev_start = nullptr, t_ev_end = nullptr;
+thread_local cudaEvent_t t_aux[4] = {nullptr, nullptr, nullptr, nullptr};
 
 struct MainKernelEvents {
   cudaEvent_t start, end;
@@ -374,14 +376,24 @@ int attn_bwd(const attn_args *a, const void *O, const float *LSE, const void *dO
   if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
   if (a->bias && cudaMemsetAsync(p.dbias_acc, 0, dbias_elems(a) * sizeof(float), st) != cudaSuccess)
     return ATTN_ERR_CUDA;
+  cudaEvent_t aux[4];
+  for (int x = 0; x < 4; ++x) {
+    aux[x] = t_aux[x];
+    t_aux[x] = nullptr;
+  }
+  if (aux[0]) cudaEventRecord(aux[0], st);
   if ((s = cuda_status(launch_bwd_pre(p, a->dtype, tc, st))) != ATTN_OK) return s;
+  if (aux[1]) cudaEventRecord(aux[1], st);
   {
     MainKernelEvents ev(st);
     cudaError_t e = tc ? tc_backward(p, st) : wide ? wide_backward(p, w + L.wide, st) : simt_backward(p, a->dtype, st);
     ev.done();
     if ((s = cuda_status(e)) != ATTN_OK) return s;
   }
-  return cuda_status(launch_bwd_post(p, a->dtype, tc, dbias_elems(a), st));
+  if (aux[2]) cudaEventRecord(aux[2], st);
+  s = cuda_status(launch_bwd_post(p, a->dtype, tc, dbias_elems(a), st));
+  if (aux[3]) cudaEventRecord(aux[3], st);
+  return s;
 }
 
 int attn_check_device_status(void *ws, attn_stream_t stream) {
@@ -398,6 +410,13 @@ int attn_check_device_status(void *ws, attn_stream_t stream) {
 void attn_profile_next_main_kernel(void *ev_start, void *ev_end) {
   t_ev_start = static_cast<cudaEvent_t>(ev_start);
   t_ev_end = static_cast<cudaEvent_t>(ev_end);
+}
+
+void attn_profile_next_aux_kernels(void *pre_start, void *pre_end, void *post_start, void *post_end) {
+  t_aux[0] = static_cast<cudaEvent_t>(pre_start);
+  t_aux[1] = static_cast<cudaEvent_t>(pre_end);
+  t_aux[2] = static_cast<cudaEvent_t>(post_start);
+  t_aux[3] = static_cast<cudaEvent_t>(post_end);
 }
 
 uint64_t attn_launch_counter(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -172,6 +172,35 @@ def whole_job_tflops(flops_per_step: float, steps: int, world: int, ms: float) -
     return flops_per_step * steps * world / (ms * 1e-3) / 1e12
 
 
+def memory_phase_bytes(w: Workload, path: str, meta_bytes: int, n_bias: int) -> dict:
+    """Algorithmic HBM bytes of the memory-bound kernels, per launch.
+    K1 (mask metadata): the segment ids read (cu_seqlens: a few bytes) and the metadata buffer
+    written (its whole size: an upper bound, since the work lists are only sorted when a grid
+    follows them).  K3 (backward preprocess): O and dO read, LSE read, D written, and on the
+    tensor-core path LSE*log2(e) written, -D's bf16 parts written (head dims 64 / 128) and the
+    fp32 dQ accumulator zeroed.  K5 (postprocess): the accumulator read and dQ written
+    (head dims up to 256 on the tensor cores), the fp32 dbias accumulator read and dbias
+    written (with a bias)."""
+    es = 2 if w.dtype == "bf16" else 4
+    elems = w.B * w.Sq * w.Hq * w.D
+    rows = w.B * w.Hq * w.Sq
+    prow = w.B * w.Hq * ((w.Sq + 127) // 128 * 128)
+    tc = path == "tc" and w.dtype == "bf16"
+    acc = tc and w.D <= 256
+    k1 = (4 * w.B * (w.Sq + w.Sk) if w.segments else 0) + meta_bytes
+    k3 = 2 * elems * es + 4 * rows + 4 * prow + (4 * prow if tc else 0) + (16 * prow if acc and w.D <= 128 else 0) \
+        + (4 * elems if acc else 0)
+    k5 = (4 + es) * elems * acc + (4 + es) * n_bias
+    return {"K1": k1, "K3": k3, "K5": k5}
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return json.load(open(p))["hbm_gbs"], "measured"
+    return 6800.0, "fallback"
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -223,8 +252,8 @@ def run_ours(args, rank, world, local_rank):
         """nsteps timed steps (L2 flushed, untimed, before each).  Per step: the whole step, the
         forward and backward phases (every kernel of attn_fwd, of attn_bwd), and the two main
         kernels alone (events recorded by the library around them, on the same stream)."""
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(nsteps)]
-        for e in [x for seven in ev for x in seven]:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(13)] for _ in range(nsteps)]
+        for e in [x for row in ev for x in row]:
             e.record(stream)  # torch creates the CUDA event lazily, on first record
         if clocks is not None:
             clocks.start()
@@ -237,11 +266,14 @@ def run_ours(args, rank, world, local_rank):
             e = ev[s]
             flush.zero_()
             e[0].record(stream)
+            e[7].record(stream)
             kws = with_meta(kw_run)  # K1 once per step, counted in the forward phase
+            e[8].record(stream)
             fa.attn_profile_next_main_kernel(e[3], e[4])
             O, LSE = fa.attn_fwd(t["q"], t["k"], t["v"], **kws)
             e[1].record(stream)
             fa.attn_profile_next_main_kernel(e[5], e[6])
+            fa.attn_profile_next_aux_kernels(e[9], e[10], e[11], e[12])
             fa.attn_bwd(t["q"], t["k"], t["v"], O, LSE, t["dO"], **kws)
             e[2].record(stream)
         torch.cuda.synchronize(dev)
@@ -254,7 +286,7 @@ def run_ours(args, rank, world, local_rank):
             clk = clocks.stop()
         el = lambda i, j: [x[i].elapsed_time(x[j]) for x in ev]  # noqa: E731
         return {"step": el(0, 2), "fwd": el(0, 1), "bwd": el(1, 2), "fwd_main": el(3, 4), "bwd_main": el(5, 6),
-                "launches": n, "clocks": clk}
+                "K1": el(7, 8), "K3": el(9, 10), "K5": el(11, 12), "launches": n, "clocks": clk}
 
     # Timed region: K steps of the workload.
     run = timed(kw, args.steps, ClockSampler(local_rank))
@@ -354,6 +386,22 @@ def run_ours(args, rank, world, local_rank):
     for name, f, key in (("fwd", f_fwd, "fwd"), ("bwd", f_bwd, "bwd"), ("fwdbwd", f_step, "step")):
         x = tf(f, run[key])
         phases[name] = {"tflops": round(x, 3), "frac": round(x / burst, 4), "ms": round(statistics.mean(run[key]), 4)}
+    # Memory-bound kernels (K1 mask metadata, K3 / K5 backward pre- and postprocess): their
+    # algorithmic bytes over their event-timed durations, against the measured copy bandwidth.
+    hbm, hbm_kind = hbm_peak()
+    n_bias = 0 if inp["bias"] is None else inp["bias"].numel()
+    mbytes = memory_phase_bytes(w, path, 0 if meta_buf is None else meta_buf.numel(), n_bias)
+    memory_phases = {"peak_gbs": hbm, "peak_kind": f"{hbm_kind} copy bandwidth",
+                     "note": "algorithmic bytes per launch / CUDA-event duration (events on the call's stream around "
+                             "the kernel); K1 only with segments or cu_seqlens"}
+    for name in ("K1", "K3", "K5"):
+        if name == "K1" and meta_buf is None:
+            memory_phases[name] = None
+            continue
+        us = statistics.mean(run[name]) * 1e3
+        gbs = mbytes[name] / (us * 1e-6) / 1e9 if us > 0 else 0.0
+        memory_phases[name] = {"us": round(us, 2), "bytes": mbytes[name], "gbs": round(gbs, 1),
+                               "frac": round(gbs / hbm, 4)}
     softcap_cost = None
     if twin is not None:
         cap_ms, unc_ms = statistics.mean(run["step"]), statistics.mean(twin["step"])
@@ -389,6 +437,7 @@ def run_ours(args, rank, world, local_rank):
                                     "fwdbwd = the step; frac of the measured bf16 burst peak; "
                                     "fwd_tflops / bwd_tflops above: the main kernels alone"),
         "softcap_cost": softcap_cost,
+        "memory_phases": memory_phases,
         "roofline": {"bound": "tensor", "kernel": "backward main kernel",
                      "achieved": round(bwd_tf, 3), "peak": burst, "unit": "TFLOP/s",
                      "frac": round(bwd_tf / burst, 4), "peak_kind": f"{kind} bf16 burst",

@@ -286,6 +286,16 @@ const char *attn_path_name(const attn_args *a);
  */
 void attn_profile_next_main_kernel(void *ev_start, void *ev_end);
 
+/*
+ * Profiling hook for the memory-bound kernels of the next attn_bwd call made by this host
+ * thread: it records `pre_start` / `pre_end` (cudaEvent_t) on its stream immediately before
+ * and after the preprocess kernel (D = rowsum(dO * O), LSE * log2(e), the sink gradient's
+ * partial sums, the fp32 dQ accumulator zeroed) and `post_start` / `post_end` around the
+ * postprocess kernel (dQ converted, dsink and dbias written out), then forgets all four.
+ * NULLs cancel a pending request.  Adds no work to the call.
+ */
+void attn_profile_next_aux_kernels(void *pre_start, void *pre_end, void *post_start, void *post_end);
+
 /* Number of kernels this library has launched in this process (all devices), for
  * accounting in benchmarks; monotonic, thread-safe. */
 uint64_t attn_launch_counter(void);

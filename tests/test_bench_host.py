@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import oracle
-from bench import flops, host_cpu, visible_pairs
+from bench import flops, host_cpu, memory_phase_bytes, visible_pairs
 from workloads import WORKLOADS, Workload, make_inputs
 
 
@@ -53,6 +53,29 @@ def test_headline_flop_counts():
     assert flops(w, None, "fwdbwd") == per * w.B * w.Hq * 14 * 256
     w5 = WORKLOADS["long_causal_32k_cap50"]
     assert visible_pairs(w5, None) == 32768 * 32769 // 2 * 32
+
+
+def test_memory_phase_bytes():
+    """K3 / K5 bytes of the headline workload, written out term by term: O and dO read (bf16),
+    LSE read, D and LSE*log2(e) written (fp32, rows padded to 128), the fp32 dQ accumulator
+    zeroed (K3); the accumulator read and dQ written (K5).  Head dim 128 adds -D's 16-byte
+    bf16 parts per row; the FFMA path (fp32) has no accumulator; a bias adds its fp32
+    accumulator read and its own dtype written."""
+    w = WORKLOADS["gemma2_local_w4096_cap50"]
+    elems, rows = 2 * 8192 * 16 * 256, 2 * 16 * 8192
+    b = memory_phase_bytes(w, "tc", 0, 0)
+    assert b["K3"] == 2 * elems * 2 + rows * 4 + rows * 4 + rows * 4 + elems * 4
+    assert b["K5"] == elems * 4 + elems * 2
+    assert b["K1"] == 0
+    w3 = WORKLOADS["packed_varlen_cap30"]
+    e3, r3 = 4 * 8192 * 8 * 128, 4 * 8 * 8192
+    b3 = memory_phase_bytes(w3, "tc", 4096, 0)
+    assert b3["K3"] == 2 * e3 * 2 + 3 * r3 * 4 + 16 * r3 + 4 * e3
+    assert b3["K1"] == 4 * 4 * (8192 + 8192) + 4096
+    f = Workload("f", "f32", B=1, Sq=100, Sk=100, Hq=2, Hkv=2, D=64, causal=True)
+    bf = memory_phase_bytes(f, "simt", 0, 7)
+    assert bf["K3"] == 2 * 100 * 2 * 64 * 4 + 200 * 4 + 256 * 4  # D's rows padded to 128 per head
+    assert bf["K5"] == 7 * 8
 
 
 def test_clock_samples_are_taken_inside_the_timed_region(tmp_path):
