@@ -234,6 +234,7 @@ int run_meta(const attn_args *a, const Params &p, cudaStream_t st, bool standalo
   const MetaLayout M = meta_layout(a);
   char *m = reinterpret_cast<char *>(const_cast<unsigned char *>(p.seg_mono)) - M.mono;
   MetaOut o;
+  o.clear_status = standalone ? 1 : 0;
   o.seg_q = a->cu_seqlens ? const_cast<int *>(p.seg_q) : nullptr;
   o.seg_k = a->cu_seqlens_k ? const_cast<int *>(p.seg_k) : nullptr;
   o.qoff = const_cast<int *>(p.qoff);
@@ -299,8 +300,7 @@ int attn_meta_build(const attn_args *a, void *meta, size_t meta_bytes, attn_stre
   p.window = a->window > 0 ? a->window : 0;
   p.status = static_cast<unsigned *>(meta);  // this buffer's own status area
   set_meta(a, static_cast<char *>(meta), p);
-  if (cudaMemsetAsync(meta, 0, kAlign, st) != cudaSuccess) return ATTN_ERR_CUDA;
-  return run_meta(a, p, st, true);
+  return run_meta(a, p, st, true);  // the metadata kernel clears the status area first
 }
 
 size_t attn_bwd_workspace_size(const attn_args *a) {

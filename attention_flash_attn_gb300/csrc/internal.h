@@ -37,6 +37,7 @@ struct MetaOut {
   int4 *qtile, *ktile;
   long long *qwork, *kwork;
   int2 *qorder, *korder;
+  int clear_status;  // a standalone build: clear the buffer's own status area first
 };
 cudaError_t launch_mask_meta(const Params &p, const int *cu_seqlens, const int *cu_seqlens_k, int nseq,
                              const MetaOut &o, cudaStream_t st);
