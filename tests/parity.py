@@ -27,7 +27,7 @@ def problem_from_inputs(w: Workload, inp: dict, heads=None, batches=None) -> ora
     """Oracle problem on the exact (upcast) inputs; optionally restricted to whole kv groups
     ``heads`` (kv head indices) and batches."""
     q, k, v = to64(inp["q"]), to64(inp["k"]), to64(inp["v"])
-    bias = to64(inp["bias"])
+    bias = inp["bias"]  # sliced before it is upcast: at full size it is a few GB in bf16
     sink = None if inp["sink"] is None else inp["sink"].double().numpy()
     seg = None if inp["seg"] is None else inp["seg"].numpy()
     if batches is not None:
@@ -41,9 +41,9 @@ def problem_from_inputs(w: Workload, inp: dict, heads=None, batches=None) -> ora
         q, k, v = q[:, :, qh], k[:, :, heads], v[:, :, heads]
         sink = None if sink is None else sink[qh]
         if bias is not None and bias.shape[1] > 1:
-            bias = bias[:, qh]
+            bias = bias[:, torch.as_tensor(qh)]
     return oracle.Problem(q, k, v, scale=w.scale, causal=w.causal, window=w.window,
-                          softcap=w.softcap, bias=bias, sink=sink, seg_q=seg, seg_k=seg)
+                          softcap=w.softcap, bias=to64(bias), sink=sink, seg_q=seg, seg_k=seg)
 
 
 def run_gpu(w: Workload, inp: dict, dev="cuda", **extra):

@@ -25,7 +25,8 @@ def sample_positions(S, seg_row=None):
 @pytest.mark.parametrize("name", ["gemma2_local_w4096_cap50", "gemma2_local_w4096_cap0",
                                   "packed_varlen_cap30", "sink_gqa64_cap0", "sink_gqa64_cap30",
                                   "long_noncausal_16k_cap50", "long_causal_32k_cap50",
-                                  "decode_sq128_sk32k_cap30_sink", "hd512_cap30"])
+                                  "decode_sq128_sk32k_cap30_sink", "hd512_cap30",
+                                  "gemma2_local_w4096_cap50_bias"])
 def test_fullsize_sampled(name):
     w = WORKLOADS[name]
     inp = make_inputs(w)
