@@ -78,7 +78,7 @@ bool tc_bwd_fused(int D);      // the backward's one-pass form (it reads -D spli
 cudaError_t tc_forward(const Params &p, cudaStream_t st);
 cudaError_t tc_backward(const Params &p, cudaStream_t st);
 
-// Head dim 512 backward on the tensor cores: a scores kernel writing P and dU into scratch
+// Head dims 320-512 backward on the tensor cores: a scores kernel writing P and dU into scratch
 // [B, Hq, Sq_pad, Sk_pad] (two bf16 planes, wide_bwd_scratch_bytes) and three GEMMs for dV,
 // dK, dQ.  Needs LSE * log2(e) and D from the preprocess; writes dQ directly.
 size_t wide_bwd_scratch_bytes(int B, int Hq, int Sq, int Sk);

@@ -375,8 +375,8 @@ def test_cu_seqlens_equals_segment_ids():
 
 
 def test_cu_seqlens_many_sequences_equals_segment_ids():
-    """More boundaries than the row pass keeps in shared memory (nseq + 1 > 4096) and more
-    tokens than one block of it takes: the same results as the equivalent segment ids, and the
+    """More boundaries than the metadata kernel keeps in shared memory (nseq + 1 > 4096) and
+    more tokens than one of its blocks covers: the same results as the equivalent segment ids, and the
     oracle's.  Most sequences hold one token, whose probability is exactly 1: by definition its
     dq and dk are zero, and the kernels' dP - D with D = rowsum(dO * O) from the stored bf16 O
     leaves a rounding residue there instead, so dq and dk are held to the oracle run on that
