@@ -24,7 +24,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // a caller's buffer from attn_meta_build, or a region of the workspace.  [0, 256) holds a
 // status area of its own (used by attn_meta_build).  Offsets are 0 when a region is absent.
 struct MetaLayout {
-  size_t mono = 0, qrange = 0, krange = 0, seg = 0, segk = 0, qoff = 0, koff = 0;
+  size_t mono = 0, qrange = 0, krange = 0, qrun = 0, krun = 0, seg = 0, segk = 0, qoff = 0, koff = 0;
   size_t qtile = 0, ktile = 0, qwork = 0, kwork = 0, qorder = 0, korder = 0;
   size_t total = 0;  // 0: the call needs no metadata
 };
@@ -73,6 +73,8 @@ MetaLayout meta_layout(const attn_args *a) {
   M.mono = off; off += align_up((size_t)a->B);
   M.qrange = off; off += align_up((size_t)a->B * nq * sizeof(int2));
   M.krange = off; off += align_up((size_t)a->B * nk * sizeof(int2));
+  M.qrun = off; off += align_up((size_t)a->B * a->Sq * sizeof(int2));
+  M.krun = off; off += align_up((size_t)a->B * a->Sk * sizeof(int2));
   if (a->cu_seqlens) { M.seg = off; off += align_up((size_t)a->Sq * sizeof(int)); }
   if (a->cu_seqlens_k) {
     M.segk = off; off += align_up((size_t)a->Sk * sizeof(int));
@@ -162,6 +164,8 @@ void set_meta(const attn_args *a, char *m, Params &p) {
   p.seg_mono = reinterpret_cast<unsigned char *>(m + M.mono);
   p.qrange = reinterpret_cast<int2 *>(m + M.qrange);
   p.krange = reinterpret_cast<int2 *>(m + M.krange);
+  p.qrun = reinterpret_cast<int2 *>(m + M.qrun);
+  p.krun = reinterpret_cast<int2 *>(m + M.krun);
   p.qtile = reinterpret_cast<int4 *>(m + M.qtile);
   p.ktile = reinterpret_cast<int4 *>(m + M.ktile);
   p.qorder = M.qorder ? reinterpret_cast<int2 *>(m + M.qorder) : nullptr;
@@ -241,6 +245,8 @@ int run_meta(const attn_args *a, const Params &p, cudaStream_t st, bool standalo
   o.koff = const_cast<int *>(p.koff);
   o.qrange = const_cast<int2 *>(p.qrange);
   o.krange = const_cast<int2 *>(p.krange);
+  o.qrun = const_cast<int2 *>(p.qrun);
+  o.krun = const_cast<int2 *>(p.krun);
   o.mono = const_cast<unsigned char *>(p.seg_mono);
   o.qtile = const_cast<int4 *>(p.qtile);
   o.ktile = const_cast<int4 *>(p.ktile);

@@ -445,13 +445,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int sid = 0;
     const int *segq = nullptr;
     if (p.seg_q && key_ok) {
-      sid = __ldg(p.seg_k + (size_t)b * p.Sk + k);
-      segq = p.seg_q + (size_t)b * p.Sq;
-      if (p.seg_mono[b]) {
-        lo = max(lo, lower_bound_i(segq, p.Sq, sid));
-        hi = min(hi, upper_bound_i(segq, p.Sq, sid));
+      if (p.seg_mono[b] && p.krun) {  // the metadata's interval for this key: one load, no search
+        const int2 x = __ldg(p.krun + (size_t)b * p.Sk + k);
+        lo = max(lo, x.x);
+        hi = min(hi, x.y);
       } else {
-        seg_pairwise = true;
+        sid = __ldg(p.seg_k + (size_t)b * p.Sk + k);
+        segq = p.seg_q + (size_t)b * p.Sq;
+        if (p.seg_mono[b]) {
+          lo = max(lo, lower_bound_i(segq, p.Sq, sid));
+          hi = min(hi, upper_bound_i(segq, p.Sq, sid));
+        } else {
+          seg_pairwise = true;
+        }
       }
     }
     if (!key_ok) {

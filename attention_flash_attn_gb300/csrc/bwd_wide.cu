@@ -249,13 +249,19 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
     int sid = 0;
     const int *segk = nullptr;
     if (p.seg_q && row_ok) {
-      sid = __ldg(p.seg_q + (size_t)b * p.Sq + i);
-      segk = p.seg_k + (size_t)b * p.Sk;
-      if (p.seg_mono[b]) {
-        lo = max(lo, lower_bound_g(segk, p.Sk, sid));
-        hi = min(hi, upper_bound_g(segk, p.Sk, sid));
+      if (p.seg_mono[b] && p.qrun) {  // the metadata's interval for this row: one load, no search
+        const int2 x = __ldg(p.qrun + (size_t)b * p.Sq + i);
+        lo = max(lo, x.x);
+        hi = min(hi, x.y);
       } else {
-        seg_pairwise = true;
+        sid = __ldg(p.seg_q + (size_t)b * p.Sq + i);
+        segk = p.seg_k + (size_t)b * p.Sk;
+        if (p.seg_mono[b]) {
+          lo = max(lo, lower_bound_g(segk, p.Sk, sid));
+          hi = min(hi, upper_bound_g(segk, p.Sk, sid));
+        } else {
+          seg_pairwise = true;
+        }
       }
     }
     if (!row_ok) {

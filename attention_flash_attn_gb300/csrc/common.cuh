@@ -33,6 +33,8 @@ struct Params {
   const int *seg_q, *seg_k;       // effective segment ids or null
   const int2 *qrange;             // [B, ceil(Sq/64)]: key range [x, y) of each 64-row query tile
   const int2 *krange;             // [B, ceil(Sk/64)]: query range [x, y) of each 64-key tile
+  const int2 *qrun, *krun;        // [B, Sq] / [B, Sk]: each query's key interval [x, y) and each
+                                  // key's query interval (mask metadata; null without it)
   const unsigned char *seg_mono;  // [B]: 1 if seg_q and seg_k rows are non-decreasing
   // Tile classes (segment / cu_seqlens calls; null otherwise): per (b, 128-row query tile)
   // {klo, khi, flo, fhi} -- the keys some row of the tile sees lie in [klo, khi), the keys every

@@ -33,6 +33,7 @@ inline cudaError_t counted(cudaError_t e, int n = 1) {
 struct MetaOut {
   int *seg_q, *seg_k, *qoff, *koff;
   int2 *qrange, *krange;
+  int2 *qrun, *krun;  // per-token visible intervals on the other axis
   unsigned char *mono;
   int4 *qtile, *ktile;
   long long *qwork, *kwork;

@@ -67,7 +67,9 @@ __device__ __forceinline__ bool bad_bounds(const int *cu, int nseq, int n) {
 //      whether both axes' ids of the batch row are non-decreasing.  Block (0, b, 0) stores it.
 //  (2) With cu_seqlens, each warp writes the sequence ids of its tile's rows (with
 //      cu_seqlens_k also their per-sequence bottom-right offsets end_k(s) - end_q(s)).
-//  (3) Each warp: its tile's class and work, and the 64-row ranges of its two halves: every
+//  (3) Each warp: every row's visible interval on the other axis, stored per token (the
+//      kernels read it instead of searching), its tile's class and work, and the 64-row ranges
+//      of its two halves: every
 //      row's visible interval (causal / window bounds at its offset; with sorted ids, its
 //      segment's run on the other axis -- read from the boundaries (sequence s spans
 //      [cu[s], cu[s + 1]), tokens at or past cu[nseq] forming sequence nseq), or found by binary
@@ -173,6 +175,7 @@ __global__ void __launch_bounds__(256) meta_kernel(Params p, const int *cu, cons
       }
       lo = max(lo, 0);
       hi = min(hi, n_other);
+      (qside ? o.qrun : o.krun)[(size_t)b * n_rows + r] = make_int2(lo, hi);
       lo_max = max(lo_max, lo);
       hi_min = min(hi_min, hi);
       if (lo < hi) {

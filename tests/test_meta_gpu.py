@@ -1,5 +1,5 @@
-"""The mask metadata kernel (K1) on the GPU: tile classes, per-tile work and the longest-first
-work lists, checked against the oracle's visibility (the mask definition, pair by pair), and
+"""The mask metadata kernel (K1) on the GPU: per-token visible intervals, tile classes, per-tile
+work and the longest-first work lists, checked against the oracle's visibility (the mask definition, pair by pair), and
 the metadata built once and shared by attn_fwd and attn_bwd (MaxText commit message quoted on
 tokamax PR #1121: packed rows, run starts per row, boundaries not aligned to tiles)."""
 import numpy as np
@@ -23,7 +23,8 @@ def meta_regions(B, Sq, Sk, cu=False, cuk=False):
     nq, nk = -(-Sq // 64), -(-Sk // 64)
     nq128, nk128 = -(-Sq // 128), -(-Sk // 128)
     r, off = {}, 256
-    for name, size in [("mono", B), ("qrange", B * nq * 8), ("krange", B * nk * 8)]:
+    for name, size in [("mono", B), ("qrange", B * nq * 8), ("krange", B * nk * 8), ("qrun", B * Sq * 8),
+                       ("krun", B * Sk * 8)]:
         r[name], off = off, off + _up(size)
     if cu:
         r["seg"], off = off, off + _up(Sq * 4)
@@ -40,6 +41,19 @@ def meta_regions(B, Sq, Sk, cu=False, cuk=False):
 def _read(buf, off, n, dtype, width=1):
     a = buf[off:off + n * width * np.dtype(dtype).itemsize].view(dtype)
     return a.reshape(n, width) if width > 1 else a
+
+
+def _check_runs(runs, count, first, last, sorted_ids):
+    """Per-token intervals [B*n_rows, 2] against the oracle's per-row counts / first / last: with
+    sorted ids exactly the visible run; with unsorted ids an interval holding every visible
+    pair (the kernels then test ids pair by pair)."""
+    runs = runs.reshape(count.shape + (2,))
+    seen = count > 0
+    lo, hi = runs[..., 0], runs[..., 1]
+    assert np.all(lo[seen] <= first[seen]) and np.all(hi[seen] >= last[seen] + 1)
+    if sorted_ids:
+        assert np.array_equal(lo[seen], first[seen]) and np.array_equal(hi[seen], last[seen] + 1)
+        assert np.all(lo[~seen] >= hi[~seen])
 
 
 def _check_axis(tiles, work, order, count, first, last, n_other, sorted_ids, B, n_rows, key_axis):
@@ -117,6 +131,8 @@ def test_tile_classes_work_and_order_against_the_oracle(w, kind):
                 _read(buf, r["qorder"], nq, np.int32, 2), *oracle.row_visible(p), w.Sk, sorted_ids, w.B, w.Sq, False)
     _check_axis(_read(buf, r["ktile"], nk, np.int32, 4), _read(buf, r["kwork"], nk, np.int64),
                 _read(buf, r["korder"], nk, np.int32, 2), *oracle.col_visible(p), w.Sq, sorted_ids, w.B, w.Sk, True)
+    _check_runs(_read(buf, r["qrun"], w.B * w.Sq, np.int32, 2), *oracle.row_visible(p), sorted_ids)
+    _check_runs(_read(buf, r["krun"], w.B * w.Sk, np.int32, 2), *oracle.col_visible(p), sorted_ids)
 
 
 def _same_results(a, b):
