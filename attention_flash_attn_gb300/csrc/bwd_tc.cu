@@ -121,23 +121,6 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
   for (int e = 0; e < N; ++e) asm volatile("" : "+r"(r[e]));
 }
 
-__device__ __forceinline__ int lower_bound_i(const int *a, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    int mid = (lo + hi) >> 1;
-    if (__ldg(a + mid) < x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
-__device__ __forceinline__ int upper_bound_i(const int *a, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    int mid = (lo + hi) >> 1;
-    if (__ldg(a + mid) <= x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
-
 __device__ __forceinline__ uint4 pack8(const uint32_t *o, int v) {
   return make_uint4(pack_bf16(__uint_as_float(o[8 * v]), __uint_as_float(o[8 * v + 1])),
                     pack_bf16(__uint_as_float(o[8 * v + 2]), __uint_as_float(o[8 * v + 3])),
@@ -445,19 +428,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     int sid = 0;
     const int *segq = nullptr;
     if (p.seg_q && key_ok) {
-      if (p.seg_mono[b] && p.krun) {  // the metadata's interval for this key: one load, no search
+      if (p.seg_mono[b]) {  // sorted ids: the metadata's interval for this key (its segment's run)
         const int2 x = __ldg(p.krun + (size_t)b * p.Sk + k);
         lo = max(lo, x.x);
         hi = min(hi, x.y);
       } else {
         sid = __ldg(p.seg_k + (size_t)b * p.Sk + k);
         segq = p.seg_q + (size_t)b * p.Sq;
-        if (p.seg_mono[b]) {
-          lo = max(lo, lower_bound_i(segq, p.Sq, sid));
-          hi = min(hi, upper_bound_i(segq, p.Sq, sid));
-        } else {
-          seg_pairwise = true;
-        }
+        seg_pairwise = true;
       }
     }
     if (!key_ok) {

@@ -59,23 +59,6 @@ struct ScoresCfg {
 constexpr int kScoresThreads = 320;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 element-wise
 constexpr int kScoresChunk = 4;      // key tiles per scores CTA at most
 
-__device__ __forceinline__ int lower_bound_g(const int *a, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    int mid = (lo + hi) >> 1;
-    if (__ldg(a + mid) < x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
-__device__ __forceinline__ int upper_bound_g(const int *a, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    int mid = (lo + hi) >> 1;
-    if (__ldg(a + mid) <= x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
-
 template <int N>
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
 #pragma unroll
@@ -249,19 +232,14 @@ __global__ void __launch_bounds__(kScoresThreads, 1)
     int sid = 0;
     const int *segk = nullptr;
     if (p.seg_q && row_ok) {
-      if (p.seg_mono[b] && p.qrun) {  // the metadata's interval for this row: one load, no search
+      if (p.seg_mono[b]) {  // sorted ids: the metadata's interval for this row (its segment's run)
         const int2 x = __ldg(p.qrun + (size_t)b * p.Sq + i);
         lo = max(lo, x.x);
         hi = min(hi, x.y);
       } else {
         sid = __ldg(p.seg_q + (size_t)b * p.Sq + i);
         segk = p.seg_k + (size_t)b * p.Sk;
-        if (p.seg_mono[b]) {
-          lo = max(lo, lower_bound_g(segk, p.Sk, sid));
-          hi = min(hi, upper_bound_g(segk, p.Sk, sid));
-        } else {
-          seg_pairwise = true;
-        }
+        seg_pairwise = true;
       }
     }
     if (!row_ok) {

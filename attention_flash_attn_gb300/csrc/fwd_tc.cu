@@ -86,23 +86,6 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
   for (int e = 0; e < N; ++e) asm volatile("" : "+r"(r[e]));
 }
 
-__device__ __forceinline__ int lower_bound_i(const int *a, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    int mid = (lo + hi) >> 1;
-    if (__ldg(a + mid) < x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
-__device__ __forceinline__ int upper_bound_i(const int *a, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    int mid = (lo + hi) >> 1;
-    if (__ldg(a + mid) <= x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
-
 // TMEM column (relative to its score buffer) of the bf16 P pairs that the PV MMA's 16-key
 // slice kk reads: the softmax half owning keys 16 kk .. 16 kk + 15 (HC keys per half) wrote
 // its P over the first HC / 2 columns of its own HC score columns.
@@ -588,19 +571,14 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D, BN, NK, NV>::MINB)
     int sid = 0;
     const int *segk = nullptr;
     if (p.seg_q && row_ok) {
-      if (p.seg_mono[b] && p.qrun) {  // the metadata's interval for this row: one load, no search
+      if (p.seg_mono[b]) {  // sorted ids: the metadata's interval for this row (its segment's run)
         const int2 x = __ldg(p.qrun + (size_t)b * p.Sq + i);
         lo = max(lo, x.x);
         hi = min(hi, x.y);
       } else {
         sid = __ldg(p.seg_q + (size_t)b * p.Sq + i);
         segk = p.seg_k + (size_t)b * p.Sk;
-        if (p.seg_mono[b]) {
-          lo = max(lo, lower_bound_i(segk, p.Sk, sid));
-          hi = min(hi, upper_bound_i(segk, p.Sk, sid));
-        } else {
-          seg_pairwise = true;
-        }
+        seg_pairwise = true;
       }
     }
     if (!row_ok) {  // never stored; neutral for the tile classification
