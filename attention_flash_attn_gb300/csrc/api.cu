@@ -2,6 +2,7 @@
 // an invalid or unsupported request never launches anything), workspace layout, and the
 // launch sequence of the forward and backward passes on the caller's stream.
 #include <math.h>
+#include <algorithm>
 #include <stdint.h>
 #include <string.h>
 
@@ -379,6 +380,8 @@ int attn_bwd(const attn_args *a, const void *O, const float *LSE, const void *dO
   p.lse2p = tc || wide ? reinterpret_cast<float *>(w + L.lse2) : nullptr;
   p.dsplit = tc && tc_bwd_fused(a->D) ? reinterpret_cast<uint4 *>(w + L.dsplit) : nullptr;
   p.dbias_acc = a->bias ? reinterpret_cast<float *>(w + L.dbias_acc) : nullptr;
+  // Group-major backward grid for long query ranges without segments (see bwd_tc.cu).
+  p.bwd_group_major = (!needs_meta(a) && (a->window > 0 ? std::min(a->window, a->Sq) : a->Sq) >= 16384) ? 1 : 0;
   if ((s = run_meta(a, p, st)) != ATTN_OK) return s;
   if (a->bias && cudaMemsetAsync(p.dbias_acc, 0, dbias_elems(a) * sizeof(float), st) != cudaSuccess)
     return ATTN_ERR_CUDA;

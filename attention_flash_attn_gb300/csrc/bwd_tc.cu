@@ -241,7 +241,8 @@ __device__ __forceinline__ void clear_hidden(uint32_t (&x)[16], uint32_t vis) {
     x[e2] &= (((vis >> (2 * e2)) & 1u) ? 0x0000ffffu : 0u) | (((vis >> (2 * e2 + 1)) & 1u) ? 0xffff0000u : 0u);
 }
 
-template <class C, bool CAP, bool BIAS>
+// GM: the group-major grid order (chosen on the host, below).
+template <class C, bool CAP, bool BIAS, bool GM>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -261,7 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // One-dimensional grid, heaviest tiles first so that the last wave holds the light ones.
   // With segments the order is the mask metadata's longest-first work list of (batch, key
   // tile) pairs, every kv head of a pair adjacent; otherwise the key tile varies slowest,
-  // earliest (seen by the most queries under causal masks) first.
+  // earliest (seen by the most queries under causal masks) first -- or, for query ranges of
+  // 16k rows and more, the (batch, kv head) group varies slowest.  Measured on the same box:
+  // long causal 32k backward 658 -> 718 TFLOP/s and long non-causal 16k 841 -> 873 group-major,
+  // but the windowed 8k workload 824 -> 642 and the sink workload 685 -> 548: there a group's
+  // key tiles in flight together reduce into the same dQ rows at once.
   const int nkt = (p.Sk + kBK - 1) / kBK;
   int kt, g, b;
   if (p.korder) {
@@ -269,6 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     b = o.x;
     kt = o.y;
     g = (int)(blockIdx.x % (unsigned)p.Hkv);
+  } else if (GM) {
+    // Long query ranges: the key tiles of one (batch, kv head) run together, earliest first, so
+    // the CTAs in flight read that group's Q / dO rows from L2 at staggered starts.
+    const int gb = (int)(blockIdx.x / (unsigned)nkt);
+    kt = (int)(blockIdx.x % (unsigned)nkt);
+    g = gb % p.Hkv;
+    b = gb / p.Hkv;
   } else {
     const int gb = (int)(blockIdx.x % (unsigned)(p.Hkv * p.B));
     kt = (int)(blockIdx.x / (unsigned)(p.Hkv * p.B));
@@ -1182,8 +1194,15 @@ cudaError_t launch_bwd(const Params &p, cudaStream_t st) {
       !make_tmap_f32_bshd(&tdq, p.dQacc, C::D, p.Sq, p.Hq, p.B, C::DQT ? 128 : 32, C::DQT ? (C::TWO ? 16 : 32) : 128,
                           !C::DQT))
     return cudaErrorInvalidValue;
-  auto kern = p.bias ? (p.cap > 0.f ? bwd_tc_kernel<C, true, true> : bwd_tc_kernel<C, false, true>)
-                     : (p.cap > 0.f ? bwd_tc_kernel<C, true, false> : bwd_tc_kernel<C, false, false>);
+  // The group-major order is built for the two-pass form (head dim 256), where it was measured.
+  const bool gm = C::TWO && p.bwd_group_major;
+  auto kern = p.bias ? (p.cap > 0.f ? bwd_tc_kernel<C, true, true, false> : bwd_tc_kernel<C, false, true, false>)
+                     : (p.cap > 0.f ? bwd_tc_kernel<C, true, false, false> : bwd_tc_kernel<C, false, false, false>);
+  if constexpr (C::TWO) {
+    if (gm)
+      kern = p.bias ? (p.cap > 0.f ? bwd_tc_kernel<C, true, true, true> : bwd_tc_kernel<C, false, true, true>)
+                    : (p.cap > 0.f ? bwd_tc_kernel<C, true, false, true> : bwd_tc_kernel<C, false, false, true>);
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const long long nblk = (long long)((p.Sk + kBK - 1) / kBK) * p.Hkv * p.B;

@@ -56,6 +56,9 @@ struct Params {
   // Split-KV forward (kv_splits > 1): each split writes its normalised partial output and LSE
   // (without the sink column) here; a merge kernel combines them.
   int kv_splits;
+  // Backward grid order without segments: 1 = (batch, kv head) slowest, key tile fastest (long
+  // query ranges); 0 = key tile slowest.
+  int bwd_group_major;
   float *o_part;                  // [kv_splits, B, Hq, Sq, D]
   float *lse_part;                // [kv_splits, B, Hq, Sq]
   // forward outputs / backward inputs
