@@ -73,6 +73,10 @@ def test_memory_phase_bytes():
     assert b3["K3"] == 2 * e3 * 2 + 3 * r3 * 4 + 16 * r3 + 4 * e3
     assert b3["K1"] == 4 * 4 * (8192 + 8192) + 4096
     f = Workload("f", "f32", B=1, Sq=100, Sk=100, Hq=2, Hkv=2, D=64, causal=True)
+    w5 = WORKLOADS["hd512_cap30"]  # the wide form: no fp32 dQ accumulator, dQ written by its GEMM
+    e5, r5 = 2048 * 8 * 512, 8 * 2048
+    b5 = memory_phase_bytes(w5, "tc", 0, 0)
+    assert b5["K3"] == 2 * e5 * 2 + 3 * r5 * 4 and b5["K5"] == 0
     bf = memory_phase_bytes(f, "simt", 0, 7)
     assert bf["K3"] == 2 * 100 * 2 * 64 * 4 + 200 * 4 + 256 * 4  # D's rows padded to 128 per head
     assert bf["K5"] == 7 * 8
