@@ -27,6 +27,22 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else t.data_ptr()
 
 
+def _on_device(where: str, device: torch.device, tensors):
+    """Every tensor the library will read or write must live on the CUDA device of q: a host
+    pointer handed to a kernel would fault the GPU instead of failing the call."""
+    if device.type != "cuda":
+        raise ValueError(f"{where}: q, k, v must be CUDA tensors")
+    for t in tensors:
+        if t is not None and t.device != device:
+            raise ValueError(f"{where}: every tensor must be on {device} (got one on {t.device})")
+
+
+def _dense(where: str, name: str, t: torch.Tensor, shape, dtype):
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{where}: {name} must be a contiguous {dtype} tensor of shape {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)}")
+
+
 def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
                bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0,
                cu_seqlens_k=None, meta=None):
@@ -44,6 +60,8 @@ def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale
             raise ValueError("the head dimension must be contiguous")
     B, Sq, Hq, D = q.shape
     Sk, Hkv = k.shape[1], k.shape[2]
+    if k.shape[0] != B or k.shape[3] != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must both be [B, Sk, Hkv, D] with q's B and D")
     a = AttnArgs()
     a.dtype = _DTYPES[q.dtype]
     a.B, a.Sq, a.Sk, a.Hq, a.Hkv, a.D = B, Sq, Sk, Hq, Hkv, D
@@ -62,11 +80,19 @@ def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale
         a.bias_stride_h = 0 if bias.shape[1] == 1 else bias.stride(1)
         keep.append(bias)
     if seg_q is not None:
+        if seg_k is None and Sq != Sk:
+            raise ValueError("seg_k [B, Sk] is required when Sq != Sk")
         seg_k = seg_q if seg_k is None else seg_k
+        if tuple(seg_q.shape) != (B, Sq) or tuple(seg_k.shape) != (B, Sk):
+            raise ValueError("seg_q must be [B, Sq] and seg_k [B, Sk]")
         seg_q, seg_k = seg_q.to(torch.int32).contiguous(), seg_k.to(torch.int32).contiguous()
         a.seg_q, a.seg_k = seg_q.data_ptr(), seg_k.data_ptr()
         keep += [seg_q, seg_k]
+    elif seg_k is not None:
+        raise ValueError("seg_k needs seg_q")
     if cu_seqlens is not None:
+        if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+            raise ValueError("cu_seqlens must be a 1-D tensor of nseq + 1 boundaries")
         cu = cu_seqlens.to(torch.int32).contiguous()
         a.cu_seqlens, a.nseq = cu.data_ptr(), cu.numel() - 1
         keep.append(cu)
@@ -80,6 +106,8 @@ def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale
     a.window = int(window)
     a.softcap = float(softcap)
     if sink is not None:
+        if sink.numel() != Hq:
+            raise ValueError("sink must hold one logit per query head [Hq]")
         sink = sink.to(torch.float32).contiguous()
         a.sink = sink.data_ptr()
         keep.append(sink)
@@ -87,6 +115,11 @@ def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale
     a.softmax_type = _capi.ATTN_SOFTMAX_OFF_BY_ONE if off_by_one else _capi.ATTN_SOFTMAX_DEFAULT
     a.kv_splits = int(kv_splits)
     if meta is not None:
+        if meta.dtype != torch.uint8 or not meta.is_contiguous():
+            raise ValueError("meta must be the contiguous uint8 buffer attn_meta returns")
+        need = lib().attn_meta_size(ctypes.byref(a))
+        if meta.numel() < need:
+            raise ValueError(f"meta holds {meta.numel()} bytes; these arguments need {need}")
         a.meta = meta.data_ptr()
         keep.append(meta)
     return a, keep
@@ -111,6 +144,19 @@ def _check(status: int, where: str):
         raise AttnError(status, where)
 
 
+def _fwd_outputs(where, q, keep, out, lse):
+    """O [B, Sq, Hq, D] in q's dtype and LSE [B, Hq, Sq] float32: the caller's (checked) or new."""
+    B, Sq, Hq, D = q.shape
+    _on_device(where, q.device, keep + [out, lse])
+    if out is not None:
+        _dense(where, "out", out, (B, Sq, Hq, D), q.dtype)
+    if lse is not None:
+        _dense(where, "lse", lse, (B, Hq, Sq), torch.float32)
+    O = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device) if out is None else out
+    LSE = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
+    return O, LSE
+
+
 def attn_fwd(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=None,
              bias=None, seg_q=None, seg_k=None, cu_seqlens=None, off_by_one=False, kv_splits=0,
              cu_seqlens_k=None, meta=None, out=None, lse=None):
@@ -119,13 +165,11 @@ def attn_fwd(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale=N
                          scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
                          off_by_one=off_by_one, kv_splits=kv_splits, cu_seqlens_k=cu_seqlens_k,
                          meta=meta)
+    O, LSE = _fwd_outputs("attn_fwd", q, keep, out, lse)
     L = lib()
     need = L.attn_fwd_workspace_size(ctypes.byref(a))
     if need == 0:
         _check(_capi.ATTN_ERR_INVALID, "attn_fwd")
-    B, Sq, Hq, D = q.shape
-    O = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device) if out is None else out
-    LSE = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
     ws = _workspace(q.device, need)
     _check(L.attn_fwd(ctypes.byref(a), O.data_ptr(), LSE.data_ptr(), ws.data_ptr(), ws.numel(),
                       _stream(q.device)), "attn_fwd")
@@ -141,9 +185,7 @@ def attn_fwd_noalloc(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None,
     a, keep = build_args(q, k, v, causal=causal, window=window, softcap=softcap, sink=sink,
                          scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
                          off_by_one=off_by_one, kv_splits=kv_splits, cu_seqlens_k=cu_seqlens_k)
-    B, Sq, Hq, D = q.shape
-    O = torch.empty((B, Sq, Hq, D), dtype=q.dtype, device=q.device) if out is None else out
-    LSE = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
+    O, LSE = _fwd_outputs("attn_fwd_noalloc", q, keep, out, lse)
     _check(lib().attn_fwd_noalloc(ctypes.byref(a), O.data_ptr(), LSE.data_ptr(), _stream(q.device)),
            "attn_fwd_noalloc")
     del keep
@@ -159,12 +201,15 @@ def attn_bwd(q, k, v, O, LSE, dO, *, causal=False, window=0, softcap=0.0, sink=N
                          scale=scale, bias=bias, seg_q=seg_q, seg_k=seg_k, cu_seqlens=cu_seqlens,
                          off_by_one=off_by_one, kv_splits=kv_splits, cu_seqlens_k=cu_seqlens_k,
                          meta=meta)
+    _on_device("attn_bwd", q.device, keep + [O, LSE, dO])
+    B, Sq, Hq, D = q.shape
+    _dense("attn_bwd", "O", O, (B, Sq, Hq, D), q.dtype)
+    _dense("attn_bwd", "dO", dO, (B, Sq, Hq, D), q.dtype)
+    _dense("attn_bwd", "LSE", LSE, (B, Hq, Sq), torch.float32)
     L = lib()
     need = L.attn_bwd_workspace_size(ctypes.byref(a))
     if need == 0:
         _check(_capi.ATTN_ERR_INVALID, "attn_bwd")
-    if not O.is_contiguous() or not dO.is_contiguous() or not LSE.is_contiguous():
-        raise ValueError("O, dO and LSE must be contiguous")
     dQ = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     dK = torch.empty(k.shape, dtype=q.dtype, device=q.device)
     dV = torch.empty(v.shape, dtype=q.dtype, device=q.device)
@@ -189,6 +234,9 @@ def attn_meta(q, k, v, *, out=None, **kw) -> Optional[torch.Tensor]:
     kw.pop("meta", None)
     kw.pop("kv_splits", None)
     a, keep = build_args(q, k, v, **kw)
+    _on_device("attn_meta", q.device, keep + [out])
+    if out is not None and (out.dtype != torch.uint8 or not out.is_contiguous()):
+        raise ValueError("attn_meta: out must be a contiguous uint8 buffer")
     L = lib()
     need = L.attn_meta_size(ctypes.byref(a))
     if need == 0:

@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(256) meta_kernel(Params p, const int *cu, cons
   } else {
     own = (qside ? p.seg_q : p.seg_k) + (size_t)b * n_rows;
     other = (qside ? p.seg_k : p.seg_q) + (size_t)b * n_other;
-    const bool same = own == other;  // one id array for both axes (then Sq == Sk)
+    const bool same = own == other && n_rows == n_other;  // one id array for both axes
     if (n_other <= kMetaSmemIds) {
 #pragma unroll 4
       for (int x = threadIdx.x; x < n_other; x += blockDim.x) sm[x] = other[x];
@@ -280,8 +280,12 @@ cudaError_t launch_mask_meta(const Params &p, const int *cu_seqlens, const int *
   if (cu_seqlens) {
     if (nseq + 1 <= kCuSmem) smem = 2 * kCuSmem * sizeof(int);
   } else {
-    const int n_ids = std::max(p.Sq, p.Sk);
-    if (n_ids <= kMetaSmemIds) smem = (size_t)n_ids * sizeof(int);
+    // The blocks of each axis keep the other axis's ids in shared memory when they fit; the
+    // launch holds the larger of the two that do (with Sq != Sk one axis may fit alone).
+    int n_ids = 0;
+    if (p.Sk <= kMetaSmemIds) n_ids = std::max(n_ids, p.Sk);
+    if (p.Sq <= kMetaSmemIds) n_ids = std::max(n_ids, p.Sq);
+    smem = (size_t)n_ids * sizeof(int);
   }
   cudaError_t e = cudaSuccess;
   if (smem > 48 * 1024) {

@@ -2,12 +2,15 @@
 work and the longest-first work lists, checked against the oracle's visibility (the mask definition, pair by pair), and
 the metadata built once and shared by attn_fwd and attn_bwd (MaxText commit message quoted on
 tokamax PR #1121: packed rows, run starts per row, boundaries not aligned to tiles)."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from parity import TOL, compare_full, frob_rel, full_oracle, run_gpu, to64, varlen_oracle
+from parity import (TOL, compare_full, frob_rel, full_oracle, problem_from_inputs, run_gpu, to64,
+                    varlen_oracle)
 from workloads import Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -186,3 +189,42 @@ def test_metadata_shared_with_separate_key_boundaries():
     bad = torch.tensor([0, 180, 50, 181, 481], dtype=torch.int32, device="cuda")
     meta_bad = fa.attn_meta(t["q"], t["k"], t["v"], causal=True, cu_seqlens=bad, cu_seqlens_k=ck, out=meta)
     assert fa.lib().attn_check_device_status(meta_bad.data_ptr(), st) == 5
+
+
+# Segment ids given per axis (seg_q [B, Sq], seg_k [B, Sk]) with Sq != Sk, one axis longer than
+# the metadata kernel keeps in shared memory (49152 ids) and the other not: only the blocks of
+# the long axis's tiles stage the other (short) axis's ids there.
+PER_AXIS = [
+    # a chunk of 200 queries continuing the last two sequences of a packed 50 000-key row (causal,
+    # bottom-right): 72 queries of sequence 1, 128 of sequence 2
+    (Workload("seg_per_axis_long_keys", "bf16", B=1, Sq=200, Sk=50000, Hq=2, Hkv=1, D=64, causal=True,
+              softcap=30.0, sink=True, q_std=2.0), [1] * 72 + [2] * 128, [0] * 20000 + [1] * 29872 + [2] * 128),
+    # 50 000 queries over 300 keys in two sequences (non-causal)
+    (Workload("seg_per_axis_long_queries", "bf16", B=1, Sq=50000, Sk=300, Hq=2, Hkv=1, D=64, causal=False,
+              softcap=30.0, q_std=2.0), [0] * 49800 + [1] * 200, [0] * 100 + [1] * 200),
+]
+
+
+@pytest.mark.parametrize("w,ids_q,ids_k", PER_AXIS, ids=lambda x: x.name if hasattr(x, "name") else None)
+def test_segment_ids_per_axis_with_one_long_axis(w, ids_q, ids_k):
+    """Per-token intervals against the oracle's visibility, and the forward and backward against
+    the oracle, with distinct query and key ids and Sq != Sk."""
+    import attention_flash_attn_gb300 as fa
+    inp = {**make_inputs(w), "seg": None}
+    seg_q = torch.tensor(ids_q, dtype=torch.int32).view(1, -1)
+    seg_k = torch.tensor(ids_k, dtype=torch.int32).view(1, -1)
+    p = dataclasses.replace(problem_from_inputs(w, inp), seg_q=seg_q.numpy(), seg_k=seg_k.numpy())
+    t = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    meta = fa.attn_meta(t["q"], t["k"], t["v"], causal=w.causal, seg_q=seg_q.cuda(), seg_k=seg_k.cuda())
+    torch.cuda.synchronize()
+    r = meta_regions(w.B, w.Sq, w.Sk)
+    buf = meta.cpu().numpy()
+    assert buf[r["mono"]] == 1
+    _check_runs(_read(buf, r["qrun"], w.B * w.Sq, np.int32, 2), *oracle.row_visible(p), True)
+    _check_runs(_read(buf, r["krun"], w.B * w.Sk, np.int32, 2), *oracle.col_visible(p), True)
+    gpu = run_gpu(w, inp, seg_q=seg_q.cuda(), seg_k=seg_k.cuda())
+    O, LSE = oracle.forward(p)
+    ref = oracle.backward(p, to64(inp["dO"]), O, LSE)
+    ref["O"], ref["LSE"] = O, LSE
+    errs = compare_full(w, gpu, ref)
+    assert all(v <= TOL["bf16"] for v in errs.values()), errs
