@@ -71,7 +71,8 @@ def build_args(q, k, v, *, causal=False, window=0, softcap=0.0, sink=None, scale
     a.v_stride_b, a.v_stride_s, a.v_stride_h = v.stride(0), v.stride(1), v.stride(2)
     keep = [q, k, v]
     if bias is not None:
-        if bias.dtype != q.dtype or bias.dim() != 4 or tuple(bias.shape[2:]) != (Sq, Sk):
+        if (bias.dtype != q.dtype or bias.dim() != 4 or tuple(bias.shape[2:]) != (Sq, Sk)
+                or bias.shape[0] not in (1, B) or bias.shape[1] not in (1, Hq)):
             raise ValueError("bias must be [1|B, 1|Hq, Sq, Sk] in the dtype of q")
         if bias.stride(-1) != 1 or bias.stride(-2) != Sk:
             raise ValueError("bias rows must be dense [Sq, Sk]")

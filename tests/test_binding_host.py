@@ -83,3 +83,13 @@ def test_metadata_buffer_must_hold_what_its_arguments_need():
         fa.build_args(q, k, v, causal=True, seg_q=seg, meta=buf[: need - 1])
     with pytest.raises(ValueError, match="uint8"):
         fa.build_args(q, k, v, causal=True, seg_q=seg, meta=torch.zeros(need, dtype=torch.int32))
+
+
+@pytest.mark.parametrize("shape", [(3, 1, 16, 16), (1, 3, 16, 16), (1, 1, 16, 15), (2, 16, 16)])
+def test_bias_shape_must_broadcast_over_batch_and_heads(shape):
+    q, k, v = qkv(B=2, Hq=2)
+    with pytest.raises(ValueError, match="bias"):
+        fa.build_args(q, k, v, bias=torch.zeros(shape, dtype=torch.bfloat16))
+    for ok in [(1, 1, 16, 16), (2, 1, 16, 16), (1, 2, 16, 16), (2, 2, 16, 16)]:
+        a, keep = fa.build_args(q, k, v, bias=torch.zeros(ok, dtype=torch.bfloat16))
+        assert a.bias and (a.bias_stride_b != 0) == (ok[0] == 2) and (a.bias_stride_h != 0) == (ok[1] == 2)
