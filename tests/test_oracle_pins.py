@@ -421,6 +421,28 @@ def test_visible_pair_counts_closed_forms():
     assert _count(S, causal=True, B=2, Hq=3) == 6 * S * (S + 1) // 2
 
 
+def test_visible_pairs_with_ids_per_axis():
+    """Ids given per axis with Sq != Sk (a chunk of queries at the end of a packed key row):
+    query i stands at key position i + Sk - Sq and sees the keys of its own id up to there.
+    Sq = 4, Sk = 7, query ids [1, 1, 2, 2], key ids [0, 0, 1, 1, 1, 2, 2], counted by hand:
+    causal rows see keys {2, 3}, {2, 3, 4}, {5}, {5, 6} (8 pairs); without causal every id-1
+    row sees 3 keys and every id-2 row 2 (10 pairs).  Reading a query's id from the key array
+    (or the other way round) gives 10 causal pairs instead."""
+    z = np.zeros
+    seg_q = np.array([[1, 1, 2, 2]], np.int32)
+    seg_k = np.array([[0, 0, 1, 1, 1, 2, 2]], np.int32)
+    for causal, want in ((True, 8), (False, 10)):
+        p = Problem(z((1, 4, 1, 1)), z((1, 7, 1, 1)), z((1, 7, 1, 1)), scale=1.0, causal=causal,
+                    seg_q=seg_q, seg_k=seg_k)
+        assert oracle.count_visible(p) == want, causal
+    p = Problem(z((1, 4, 1, 1)), z((1, 7, 1, 1)), z((1, 7, 1, 1)), scale=1.0, causal=True, seg_q=seg_q, seg_k=seg_k)
+    count, first, last = oracle.row_visible(p)
+    assert count.tolist() == [[2, 3, 1, 2]] and first.tolist() == [[2, 2, 5, 5]] and last.tolist() == [[3, 4, 5, 6]]
+    count, first, last = oracle.col_visible(p)
+    assert count.tolist() == [[0, 0, 2, 2, 1, 2, 1]]
+    assert first.tolist() == [[-1, -1, 0, 0, 1, 2, 3]] and last.tolist() == [[-1, -1, 1, 1, 1, 3, 3]]
+
+
 @pytest.mark.parametrize("causal,window", [(True, 0), (True, 3), (False, 3)])
 def test_bottom_right_alignment_equals_square_problem(causal, window):
     """With Sq < Sk, query i of the short problem is query i + Sk - Sq of the square problem on
