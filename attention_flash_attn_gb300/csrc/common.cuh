@@ -43,8 +43,9 @@ struct Params {
   // Per (b, 128-key tile) the same over the queries that see its keys.
   const int4 *qtile, *ktile;
   // Longest-first work lists: every (b, 128-row query tile) / (b, 128-key tile) once, as
-  // {b, tile}, in descending order of visible pairs (ties: lower index first); null when the
-  // call has no segments or more tiles than the sorter takes (the grid's own order then).
+  // {b, tile}, in descending power-of-two class of visible pairs and, within a class, in the
+  // grid's own locality order; null when the call has no segments, more tiles than the sorter
+  // takes, or a grid too large to follow a list (the grid's own order then).
   const int2 *qorder, *korder;
   // Varlen with separate key boundaries (B == 1): per token, the causal / window offset of its
   // sequence, end_k(s) - end_q(s) (bottom-right alignment within every sequence); null: the

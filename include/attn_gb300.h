@@ -114,9 +114,11 @@ typedef struct {
      * multiples of 8 bf16 elements) are read with 16-byte loads, others element by element. */
     const void *bias;
     int64_t bias_stride_b, bias_stride_h;
-    /* Optional packed segments: seg_q [B,Sq] and seg_k [B,Sk] int32 (both or neither).
-     * A pair is visible only if the ids are equal.  Any ids are accepted; runs of
-     * non-decreasing ids additionally let the kernels skip whole tiles.                   */
+    /* Optional packed segments: seg_q [B,Sq] and seg_k [B,Sk] int32 (both or neither; the
+     * same array for both when Sq == Sk).  A pair is visible only if the ids are equal.  Any
+     * ids are accepted; runs of non-decreasing ids additionally let the kernels skip whole
+     * tiles.  With Sq != Sk, causal and window keep the one bottom-right alignment below (ids
+     * carry no per-sequence offsets; cu_seqlens_k gives those).                            */
     const int32_t *seg_q, *seg_k;
     /* Alternative to seg_q/seg_k (not both): cu_seqlens [nseq+1] int32 with
      * cu_seqlens[0] == 0, non-decreasing, cu_seqlens[nseq] <= Sq; requires B == 1 and, unless
