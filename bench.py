@@ -209,6 +209,13 @@ def peaks():
     return 1900.0, 1700.0, "fallback"
 
 
+def call_kwargs(w: Workload, t: dict) -> dict:
+    """Keyword arguments of attn_fwd / attn_bwd (and attn_meta) for a workload's inputs."""
+    return dict(causal=w.causal, window=w.window, softcap=w.softcap, sink=t["sink"], scale=w.scale,
+                bias=t["bias"], seg_q=t["seg"], seg_k=t["seg"], kv_splits=w.kv_splits,
+                cu_seqlens=t["cu_q"], cu_seqlens_k=t["cu_k"])
+
+
 def run_ours(args, rank, world, local_rank):
     import attention_flash_attn_gb300 as fa
     dev = torch.device("cuda", local_rank)
@@ -219,9 +226,7 @@ def run_ours(args, rank, world, local_rank):
     t = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     if args.kv_splits is not None:
         w = w.replace(kv_splits=args.kv_splits)
-    kw = dict(causal=w.causal, window=w.window, softcap=w.softcap, sink=t["sink"], scale=w.scale,
-              bias=t["bias"], seg_q=t["seg"], seg_k=t["seg"], kv_splits=w.kv_splits,
-              cu_seqlens=t["cu_q"], cu_seqlens_k=t["cu_k"])
+    kw = call_kwargs(w, t)
     bounds = None if inp["cu_q"] is None else (inp["cu_q"], inp["cu_k"])
     path = fa.attn_path_name(t["q"], t["k"], t["v"], **kw)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)

@@ -122,3 +122,29 @@ def test_host_cpu_names_the_processor():
     assert name.startswith(platform.machine())
     assert len(name) > len(platform.machine())
 
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_bench_call_arguments_pass_the_binding_checks(name):
+    """Every bench workload's arguments (shapes of q / k / v, ids, boundaries, sink, bias, a
+    metadata buffer of the size the library asks for) pass the binding's checks; the workload
+    is cut to at most 1024 query rows (the checks depend on shapes, not sizes)."""
+    import ctypes
+    import attention_flash_attn_gb300 as fa
+    from bench import call_kwargs
+    w = WORKLOADS[name]
+    sq = min(w.Sq, 1024)
+    w = w.replace(Sq=sq, Sk=w.Sk * sq // w.Sq, run_lo=min(w.run_lo, 32), run_hi=min(w.run_hi, 256),
+                  prefix_hi=min(w.prefix_hi, 256))
+    t = make_inputs(w)
+    kw = call_kwargs(w, t)
+    a, keep = fa.build_args(t["q"], t["k"], t["v"], **kw)
+    need = fa.lib().attn_meta_size(ctypes.byref(a))
+    assert (need > 0) == (w.segments or w.thd_prefix)
+    if need:  # a buffer of that size at a 256-byte boundary, as a device allocation would be
+        import torch
+        raw = torch.zeros(need + 256, dtype=torch.uint8)
+        off = -raw.data_ptr() % 256
+        a, keep = fa.build_args(t["q"], t["k"], t["v"], meta=raw[off:off + need], **kw)
+    assert fa.lib().attn_fwd_workspace_size(ctypes.byref(a)) > 0
+    assert fa.lib().attn_bwd_workspace_size(ctypes.byref(a)) > 0
