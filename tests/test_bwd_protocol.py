@@ -20,8 +20,6 @@ the s_full chain.
 import random
 from collections import defaultdict
 
-import pytest
-
 
 STEP_COUNTS = [1, 2, 3, 4, 5, 6, 8, 13, 33, 66, 80]
 

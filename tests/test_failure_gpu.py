@@ -11,7 +11,7 @@ import time
 import pytest
 import torch
 
-from parity import TOL, check_against_oracle_small
+from parity import check_against_oracle_small
 from workloads import Workload, make_inputs
 
 pytestmark = pytest.mark.gpu

@@ -4,7 +4,6 @@ of dK / dV for one (batch, kv group), plus dsink over every batch for that group
 Same tolerance as the small cases (Frobenius-relative 1e-2 for bf16)."""
 import numpy as np
 import pytest
-import torch
 
 import oracle
 from parity import TOL, frob_rel, problem_from_inputs, run_gpu, to64
